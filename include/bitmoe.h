@@ -1,0 +1,194 @@
+/*
+ * bitmoe.h -- C ABI of the int4 mixture-of-experts layer and int4 LM head
+ * for NVIDIA B300 (sm_103a).
+ *
+ * What is computed.  One sparse MoE layer of a 256-expert, top-k coding model
+ * with 4-bit weights ("Flint 40B : Best Mid Sized LLM", video transcript
+ * 02:35: 256 routed experts per mixture layer, a small router picks a few per
+ * token; 06:11: dedicated kernels for low-bit projections and mixture-of-
+ * experts routing), and the 4-bit output projection (same transcript 03:36
+ * and 05:39; "Recursive_SI's First Model Unveiled!", section "Quantization"):
+ *
+ *   logits l = x Wr^T + b          softmax p = softmax(l)     top-k ids, gates w
+ *   rows grouped by expert (stable)                              [moe_permute]
+ *   a = x Wg^T, u = x Wu^T, h = silu(a) * u, y = h Wd^T          [moe_expert_ffn_int4]
+ *   out = residual + sum_j w_j y_j                               [moe_combine]
+ *   z = h Wlm^T, argmax z                                        [lmhead_int4_gemv]
+ *
+ * Conventions.
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller; nothing is
+ *    freed or retained by the library.  bf16 and fp16 tensors are passed as
+ *    raw 16-bit patterns (uint16_t).  All tensors are dense row-major.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ *    default stream) and returns a bitmoe_status_t synchronously.  A call that
+ *    returns an error launched nothing.
+ *  - Scratch memory comes from a caller-provided workspace whose size is given
+ *    by the matching *_workspace_size() function; pass the workspace of the
+ *    same shape to every call that needs one.  Calls sharing one workspace must
+ *    be ordered on one stream.
+ *  - int4 weights are used in the library's packed tile layout, produced once
+ *    by bitmoe_pack_int4() from the canonical layout below.
+ *  - Device-side checks (forced expert ids out of range, a bounded wait that
+ *    ran out) do not fault: they set a status word inside the workspace, read
+ *    with bitmoe_get_device_status().
+ *
+ * Canonical int4 layout (input of bitmoe_pack_int4).  A bank of n_mats
+ * matrices, each rows x K: q [n_mats, rows, K/2] bytes, element 2b of a row in
+ * the low nibble of byte b and 2b+1 in the high nibble, two's complement in
+ * [-8, 7]; scale [n_mats, rows, K/group] fp16.  W[n,i] = q[n,i] * s[n, i/group]
+ * (symmetric, no zero point).  The expert banks are gate [E, I, d],
+ * up [E, I, d] and down [E, d, I]; the LM head is one matrix [V, d].
+ */
+#ifndef BITMOE_H_
+#define BITMOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum bitmoe_status {
+  BITMOE_OK = 0,
+  BITMOE_ERR_INVALID_ARG = 1,  /* null pointer, bad shape, misaligned pointer, k > E ... */
+  BITMOE_ERR_UNSUPPORTED = 2,  /* shape outside what the kernels handle (see each call) */
+  BITMOE_ERR_WORKSPACE = 3,    /* workspace missing or smaller than *_workspace_size() */
+  BITMOE_ERR_CUDA = 4,         /* a launch failed; bitmoe_last_cuda_error() has the code */
+  BITMOE_ERR_TIMEOUT = 5,      /* device status: a bounded wait ran out */
+  BITMOE_ERR_DEVICE_CHECK = 6  /* device status: an input failed a device-side check */
+} bitmoe_status_t;
+
+/* Shape of one MoE layer.  d: hidden size; E: routed experts; k: experts per
+ * token; I: expert intermediate size; group: int4 scale group (32);
+ * renormalize: 1 = gates are the chosen softmax probabilities rescaled to sum
+ * 1, 0 = the raw probabilities.  Supported: d and I multiples of 128,
+ * group == 32, 1 <= k <= min(E, 32), E <= 1024. */
+typedef struct bitmoe_moe_shape {
+  int64_t d, E, k, I, group;
+  int32_t renormalize;
+} bitmoe_moe_shape_t;
+
+/* Packed expert banks (bitmoe_pack_int4 output, 16-byte aligned) and the
+ * router: w_router [E, d] fp32, b_router [E] fp32 or NULL (no bias). */
+typedef struct bitmoe_moe_weights {
+  const uint8_t* gate;
+  const uint8_t* up;
+  const uint8_t* down;
+  const float* w_router;
+  const float* b_router;
+} bitmoe_moe_weights_t;
+
+/* ------------------------------------------------------------ utilities */
+
+const char* bitmoe_status_string(bitmoe_status_t status);
+/* cudaError_t code of the last failed launch in this thread (0 if none). */
+int bitmoe_last_cuda_error(void);
+const char* bitmoe_version(void);
+
+/* Bytes of a packed bank of n_mats matrices of rows x K (rows % 16 == 0,
+ * K % 128 == 0, group == 32); 0 for an unsupported shape.  Equal to the
+ * canonical size q + scale: n_mats * rows * K * 9 / 16. */
+size_t bitmoe_packed_int4_bytes(int64_t n_mats, int64_t rows, int64_t K, int64_t group);
+
+/* Reorder a canonical int4 bank (device q, scale) into the packed tile layout
+ * the kernels stream: 16-row tiles, each a run of 128-column chunks holding
+ * the nibbles of every (row, 32-column group) in the order one mma fragment
+ * consumes them, followed by the chunk's fp16 scales.  Off the timed path. */
+bitmoe_status_t bitmoe_pack_int4(const uint8_t* q, const uint16_t* scale, int64_t n_mats, int64_t rows,
+                                 int64_t K, int64_t group, uint8_t* packed, void* stream);
+
+/* Read (and clear, when clear != 0) the device status word of a workspace.
+ * Synchronises `stream`.  *status_out receives BITMOE_OK, BITMOE_ERR_TIMEOUT
+ * or BITMOE_ERR_DEVICE_CHECK. */
+bitmoe_status_t bitmoe_get_device_status(void* workspace, int clear, int32_t* status_out, void* stream);
+
+/* ------------------------------------------------------------ MoE layer */
+
+/* Workspace bytes for any MoE call below on T tokens of this shape. */
+size_t moe_workspace_size(const bitmoe_moe_shape_t* shape, int64_t T);
+
+/*
+ * Router: logits l[t,e] = sum_i x[t,i] w_router[e,i] + b_router[e] in fp32;
+ * softmax over the E experts; the k largest logits (descending, equal
+ * logits -> lower expert index) give topk_ids [T, k] int32; topk_w [T, k] fp32
+ * are their softmax probabilities, renormalised to sum 1 if shape->renormalize.
+ * x [T, d] bf16.  logits_out [T, E] fp32 may be NULL.  T = 0 is a no-op.
+ * Source: "Flint 40B : Best Mid Sized LLM", transcript 02:35 (the router picks
+ * a few of 256 experts per token).
+ */
+bitmoe_status_t moe_route(const uint16_t* x, int64_t T, const bitmoe_moe_shape_t* shape, const float* w_router,
+                          const float* b_router, int32_t* topk_ids, float* topk_w, float* logits_out,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Token -> expert grouping.  Row r = t*k + j of topk_ids is placed at
+ * position inv_rows[r]; sorted_rows[p] = r; expert e owns positions
+ * [expert_offsets[e], expert_offsets[e+1]); inside one expert the rows keep
+ * ascending r (a stable counting sort, so the result is unique).
+ * expert_offsets [E+1], sorted_rows [T*k], inv_rows [T*k], all int32.
+ * Rows whose id is outside [0, E) are left out (inv_rows[r] = -1) and flag
+ * BITMOE_ERR_DEVICE_CHECK in the device status word.
+ */
+bitmoe_status_t moe_permute(const int32_t* topk_ids, int64_t T, const bitmoe_moe_shape_t* shape,
+                            int32_t* expert_offsets, int32_t* sorted_rows, int32_t* inv_rows, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/*
+ * Expert FFNs of every grouped row: for position p holding row r = t*k + j of
+ * expert e, a = Wg[e] x[t], u = Wu[e] x[t], h = a / (1 + exp(-a)) * u and
+ * y_rows[p] = Wd[e] h (fp32 [T*k, d], sorted order), with int4 weights
+ * dequantised group by group.  expert_offsets / sorted_rows are moe_permute's.
+ * Source: "Flint 40B : Best Mid Sized LLM", transcript 02:35 and 06:11.
+ */
+bitmoe_status_t moe_expert_ffn_int4(const uint16_t* x, int64_t T, const bitmoe_moe_shape_t* shape,
+                                    const bitmoe_moe_weights_t* weights, const int32_t* expert_offsets,
+                                    const int32_t* sorted_rows, float* y_rows, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+
+/*
+ * Gate-weighted combine into the residual:
+ * out_f32[t,c] = residual[t,c] + sum_{j=0}^{k-1} topk_w[t,j] * y_rows[inv_rows[t*k+j], c]
+ * summed in ascending j in fp32; out [T, d] bf16 = round-to-nearest-even of
+ * out_f32.  out_f32 may be NULL.  out may alias residual.
+ */
+bitmoe_status_t moe_combine(const float* y_rows, const int32_t* inv_rows, const float* topk_w,
+                            const uint16_t* residual, int64_t T, const bitmoe_moe_shape_t* shape, uint16_t* out,
+                            float* out_f32, void* stream);
+
+/*
+ * The whole layer: route (unless forced), group, expert FFNs, combine.
+ * residual may equal x.  forced_ids [T, k] / forced_w [T, k] (both or neither)
+ * replace the router's choice; forced ids are range-checked on the device.
+ * topk_ids_out / topk_w_out / out_f32 may be NULL.  out may alias residual but
+ * not x.  Decode-sized batches (T*k <= 512) run the streaming path; larger
+ * batches run the grouped-GEMM path.
+ */
+bitmoe_status_t moe_forward(const uint16_t* x, const uint16_t* residual, int64_t T, const bitmoe_moe_shape_t* shape,
+                            const bitmoe_moe_weights_t* weights, const int32_t* forced_ids, const float* forced_w,
+                            int32_t* topk_ids_out, float* topk_w_out, uint16_t* out, float* out_f32,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------ LM head */
+
+size_t lmhead_workspace_size(int64_t T, int64_t d, int64_t V);
+
+/*
+ * 4-bit output projection: logits[t,v] = sum_i Wlm[v,i] h[t,i] (fp32) and
+ * argmax[t] = the lowest v reaching the maximum.  h [T, d] bf16; w_packed is
+ * the packed [V, d] bank; logits [T, V] may be NULL.  V % 16 == 0, T <= 64.
+ * Source: "Flint 40B : Best Mid Sized LLM", transcript 03:36 and 05:39.
+ */
+bitmoe_status_t lmhead_int4_gemv(const uint16_t* h, int64_t T, int64_t d, int64_t V, int64_t group,
+                                 const uint8_t* w_packed, float* logits, int32_t* argmax, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/* RMSNorm with unit gain between stacked layers: y = x / sqrt(mean(x^2) + eps),
+ * computed in fp32, rounded to bf16.  x, y [T, d] bf16 (y may alias x). */
+bitmoe_status_t bitmoe_rmsnorm(const uint16_t* x, int64_t T, int64_t d, float eps, uint16_t* y, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BITMOE_H_ */

@@ -1,0 +1,235 @@
+"""Seeded synthetic inputs for the int4 MoE layer and the int4 LM head.
+
+This module only draws numbers. It holds none of the layer's arithmetic (no
+dequantisation, no routing, no matrix products), so the CPU oracle and the CUDA
+path can both take their inputs from here without sharing any of the method.
+
+Two generators are used:
+
+* Uniform tensors (packed int4 weight bytes, fp16 group scales) come from a
+  counter-based hash: the SplitMix64 sequence of Steele, Lea and Flood
+  ("Fast splittable pseudorandom number generators", OOPSLA 2014), whose i-th
+  output from state ``key`` is ``mix64(key + (i + 1) * GAMMA)``.  Element ``i``
+  of a tensor depends only on (seed, tag, layer, i), so any slice (one expert,
+  one layer) can be drawn on its own, and ``synth_dev.cu`` draws the same bits
+  on the device for the multi-GB weight banks.
+* Normal tensors (activations, router weights and biases) are drawn on the
+  host with numpy's PCG64 seeded by ``SeedSequence([seed, tag, layer, step])``.
+
+Value recipes (the workload of a 256-expert, top-8, int4 coding-model MoE
+layer as described on the Flint model pages):
+
+* int4 weights: every nibble uniform over the 16 two's-complement values
+  -8..7 (one byte holds element 2b in its low nibble, 2b+1 in its high one);
+* fp16 scales: ``RNE_fp16(0.005 + 0.015 * u)``, u uniform in [0, 1) with 53 bits;
+* activations: N(0, 1) rounded to bf16 (nearest-even);
+* router weights: N(0, 1/d) in fp32; router bias: N(0, 1) in fp32, or the
+  Zipf(s) bias ``b[pi(r)] = ln(r^-s / H)`` over a seeded permutation pi.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import numpy as np
+
+GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+_MASK64 = (1 << 64) - 1
+
+# Tensor tags: one independent stream per tensor kind.
+TAG = {
+    "gate_q": 1, "gate_s": 2, "up_q": 3, "up_s": 4, "down_q": 5, "down_s": 6,
+    "router_w": 7, "router_b": 8, "x": 9, "lm_q": 10, "lm_s": 11, "zipf": 12,
+}
+
+
+def _mix64_int(z: int) -> int:
+    z &= _MASK64
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & _MASK64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & _MASK64
+    return z ^ (z >> 31)
+
+
+def stream_key(seed: int, tag: int, layer: int = 0) -> int:
+    """Key of the (seed, tag, layer) stream: three chained SplitMix64 steps."""
+    g = 0x9E3779B97F4A7C15
+    k0 = _mix64_int(seed + g)
+    k1 = _mix64_int(k0 + (tag + 1) * g)
+    return _mix64_int(k1 + (layer + 1) * g)
+
+
+def mix64(z: np.ndarray) -> np.ndarray:
+    """SplitMix64 finaliser on a uint64 array (wrapping arithmetic)."""
+    z = z ^ (z >> np.uint64(30))
+    z = z * _M1
+    z = z ^ (z >> np.uint64(27))
+    z = z * _M2
+    return z ^ (z >> np.uint64(31))
+
+
+def hash_words(key: int, start: int, count: int) -> np.ndarray:
+    """Outputs start .. start+count-1 of the SplitMix64 sequence from ``key``."""
+    idx = np.arange(start, start + count, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = np.uint64(key) + (idx + np.uint64(1)) * GAMMA
+        return mix64(z)
+
+
+def int4_bytes(key: int, start: int, count: int) -> np.ndarray:
+    """Bytes start .. start+count-1 of a packed uniform-int4 tensor.
+
+    Byte b is byte (b mod 8) (little-endian) of hash word b // 8.
+    """
+    if count == 0:
+        return np.zeros(0, np.uint8)
+    w0 = start // 8
+    w1 = (start + count + 7) // 8
+    words = hash_words(key, w0, w1 - w0)
+    raw = words.view(np.uint8) if words.dtype.byteorder in ("=", "<") else words.byteswap().view(np.uint8)
+    off = start - w0 * 8
+    return raw[off:off + count].copy()
+
+
+def f16_scales(key: int, start: int, count: int) -> np.ndarray:
+    """fp16 scales (as uint16 bits): RNE_fp16(0.005 + 0.015 * u), u = (h >> 11) * 2^-53."""
+    if count == 0:
+        return np.zeros(0, np.uint16)
+    h = hash_words(key, start, count)
+    u = (h >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+    v = 0.005 + 0.015 * u
+    return v.astype(np.float16).view(np.uint16)
+
+
+def f64_to_bf16_bits(v: np.ndarray) -> np.ndarray:
+    """Round float64 values to bf16 (nearest-even), returned as uint16 bits.
+
+    Used only to store drawn normals in the activation format; finite inputs
+    of moderate magnitude only (no overflow / subnormal handling needed here).
+    """
+    v = np.asarray(v, dtype=np.float64)
+    m, e = np.frexp(v)                      # v = m * 2^e, 0.5 <= |m| < 1
+    r = np.ldexp(np.rint(m * 256.0), e - 8)  # 8 significant bits, ties to even
+    return (r.astype(np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def _rng(seed: int, tag: int, layer: int = 0, step: int = 0) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, tag, layer, step])))
+
+
+# ---------------------------------------------------------------- activations
+
+
+def activations(seed: int, T: int, d: int, step: int = 0, layer: int = 0) -> np.ndarray:
+    """x [T, d] ~ N(0, 1) stored as bf16 bits (uint16)."""
+    return f64_to_bf16_bits(_rng(seed, TAG["x"], layer, step).standard_normal((T, d)))
+
+
+def router_weight(seed: int, E: int, d: int, layer: int = 0) -> np.ndarray:
+    """W_r [E, d] ~ N(0, 1/d) in fp32."""
+    g = _rng(seed, TAG["router_w"], layer).standard_normal((E, d))
+    return (g * (1.0 / math.sqrt(d))).astype(np.float32)
+
+
+def router_bias(seed: int, E: int, kind: str = "normal", layer: int = 0, zipf_s: float = 1.1) -> np.ndarray:
+    """Per-expert router bias [E] fp32: 'zero', 'normal' (N(0,1)) or 'zipf'."""
+    if kind == "zero":
+        return np.zeros(E, np.float32)
+    if kind == "normal":
+        return _rng(seed, TAG["router_b"], layer).standard_normal(E).astype(np.float32)
+    if kind == "zipf":
+        r = np.arange(1, E + 1, dtype=np.float64)
+        w = r ** (-zipf_s)
+        p = w / w.sum()
+        perm = _rng(seed, TAG["zipf"], layer).permutation(E)
+        b = np.empty(E, np.float64)
+        b[perm] = np.log(p)
+        return b.astype(np.float32)
+    raise ValueError(kind)
+
+
+# ---------------------------------------------------------------- int4 weights
+
+
+def int4_matrix(seed: int, qtag: str, stag: str, layer: int, n_mats: int, rows: int, K: int,
+                group: int = 32, mat0: int = 0, mat1: int | None = None):
+    """Packed int4 bank [n_mats, rows, K] (canonical layout) and its fp16 scales.
+
+    Returns (q [m, rows, K/2] uint8, s [m, rows, K/group] uint16) for matrices
+    mat0 .. mat1-1 only; element indices are those of the full bank, so a slice
+    holds exactly the bytes the full bank holds there.
+    """
+    if mat1 is None:
+        mat1 = n_mats
+    m = mat1 - mat0
+    qb = rows * K // 2
+    sb = rows * K // group
+    kq = stream_key(seed, TAG[qtag], layer)
+    ks = stream_key(seed, TAG[stag], layer)
+    q = int4_bytes(kq, mat0 * qb, m * qb).reshape(m, rows, K // 2)
+    s = f16_scales(ks, mat0 * sb, m * sb).reshape(m, rows, K // group)
+    return q, s
+
+
+def moe_layer(seed: int, d: int, E: int, I: int, group: int = 32, layer: int = 0,
+              bias: str = "normal", experts: tuple[int, int] | None = None) -> dict:
+    """All tensors of one MoE layer (or of experts [e0, e1) only)."""
+    e0, e1 = experts if experts is not None else (0, E)
+    gq, gs = int4_matrix(seed, "gate_q", "gate_s", layer, E, I, d, group, e0, e1)
+    uq, us = int4_matrix(seed, "up_q", "up_s", layer, E, I, d, group, e0, e1)
+    dq, ds = int4_matrix(seed, "down_q", "down_s", layer, E, d, I, group, e0, e1)
+    return {
+        "gate_q": gq, "gate_s": gs, "up_q": uq, "up_s": us, "down_q": dq, "down_s": ds,
+        "w_router": router_weight(seed, E, d, layer),
+        "b_router": router_bias(seed, E, bias, layer),
+    }
+
+
+def lm_head(seed: int, V: int, d: int, group: int = 32, rows: tuple[int, int] | None = None):
+    """LM-head bank q [V, d/2], s [V, d/32] (or rows [r0, r1) of it)."""
+    r0, r1 = rows if rows is not None else (0, V)
+    kq = stream_key(seed, TAG["lm_q"], 0)
+    ks = stream_key(seed, TAG["lm_s"], 0)
+    q = int4_bytes(kq, r0 * (d // 2), (r1 - r0) * (d // 2)).reshape(r1 - r0, d // 2)
+    s = f16_scales(ks, r0 * (d // group), (r1 - r0) * (d // group)).reshape(r1 - r0, d // group)
+    return q, s
+
+
+# ---------------------------------------------------------------- device twin
+
+_DEV = None
+
+
+def _dev_lib():
+    global _DEV
+    if _DEV is None:
+        path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsynth.so")
+        if not os.path.exists(path):
+            raise RuntimeError(f"device generator not built: {path} (run __graft_entry__.build())")
+        lib = ctypes.CDLL(path)
+        for name in ("synth_fill_int4_bytes", "synth_fill_f16_scales"):
+            fn = getattr(lib, name)
+            fn.restype = ctypes.c_int
+            fn.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_void_p]
+        _DEV = lib
+    return _DEV
+
+
+def device_fill_int4(dst_ptr: int, count: int, key: int, start: int = 0, stream: int = 0) -> None:
+    """Write bytes start .. start+count-1 of stream ``key`` to device memory."""
+    rc = _dev_lib().synth_fill_int4_bytes(dst_ptr, count, key, start, stream)
+    if rc != 0:
+        raise RuntimeError(f"synth_fill_int4_bytes failed: cuda error {rc}")
+
+
+def device_fill_scales(dst_ptr: int, count: int, key: int, start: int = 0, stream: int = 0) -> None:
+    """Write fp16 scales start .. start+count-1 of stream ``key`` to device memory."""
+    rc = _dev_lib().synth_fill_f16_scales(dst_ptr, count, key, start, stream)
+    if rc != 0:
+        raise RuntimeError(f"synth_fill_f16_scales failed: cuda error {rc}")
