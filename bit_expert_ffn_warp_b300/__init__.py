@@ -1,0 +1,299 @@
+"""Python binding of the bitmoe C ABI (include/bitmoe.h): argument marshalling only.
+
+Every function here takes torch CUDA tensors, checks dtypes and shapes, and
+calls the entry point of the same name in ``libbitmoe.so`` on the current
+torch stream.  All arithmetic runs in the library's CUDA kernels; there is no
+fallback.  If the library is missing the import fails.
+
+Tensor formats: activations bf16 ``[T, d]``; router weight fp32 ``[E, d]``,
+bias fp32 ``[E]``; int4 banks are packed with :func:`bitmoe_pack_int4` from the
+canonical ``q uint8 [n, rows, K/2]`` + ``scale fp16 [n, rows, K/32]``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbitmoe.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"bitmoe CUDA library not built: {LIB_PATH} (run __graft_entry__.build())")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+OK = 0
+STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE", 4: "CUDA", 5: "TIMEOUT",
+                6: "DEVICE_CHECK"}
+ERR_TIMEOUT = 5
+ERR_DEVICE_CHECK = 6
+GROUP = 32
+
+
+class BitmoeError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        msg = _lib.bitmoe_status_string(code).decode()
+        extra = f" (cuda error {_lib.bitmoe_last_cuda_error()})" if code == 4 else ""
+        super().__init__(f"{fn}: {STATUS_NAMES.get(code, code)}: {msg}{extra}")
+        self.code = code
+
+
+class MoeShape(ctypes.Structure):
+    _fields_ = [("d", ctypes.c_int64), ("E", ctypes.c_int64), ("k", ctypes.c_int64), ("I", ctypes.c_int64),
+                ("group", ctypes.c_int64), ("renormalize", ctypes.c_int32)]
+
+
+class MoeWeights(ctypes.Structure):
+    _fields_ = [("gate", ctypes.c_void_p), ("up", ctypes.c_void_p), ("down", ctypes.c_void_p),
+                ("w_router", ctypes.c_void_p), ("b_router", ctypes.c_void_p)]
+
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+_SIGS = {
+    "bitmoe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "bitmoe_last_cuda_error": (ctypes.c_int, []),
+    "bitmoe_version": (ctypes.c_char_p, []),
+    "bitmoe_packed_int4_bytes": (_SZ, [_I64, _I64, _I64, _I64]),
+    "bitmoe_pack_int4": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I64, _P, _P]),
+    "bitmoe_get_device_status": (ctypes.c_int, [_P, ctypes.c_int, ctypes.POINTER(ctypes.c_int32), _P]),
+    "moe_workspace_size": (_SZ, [ctypes.POINTER(MoeShape), _I64]),
+    "moe_route": (ctypes.c_int, [_P, _I64, ctypes.POINTER(MoeShape), _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_permute": (ctypes.c_int, [_P, _I64, ctypes.POINTER(MoeShape), _P, _P, _P, _P, _SZ, _P]),
+    "moe_expert_ffn_int4": (ctypes.c_int, [_P, _I64, ctypes.POINTER(MoeShape), ctypes.POINTER(MoeWeights), _P, _P,
+                                           _P, _P, _SZ, _P]),
+    "moe_combine": (ctypes.c_int, [_P, _P, _P, _P, _I64, ctypes.POINTER(MoeShape), _P, _P, _P]),
+    "moe_forward": (ctypes.c_int, [_P, _P, _I64, ctypes.POINTER(MoeShape), ctypes.POINTER(MoeWeights), _P, _P, _P,
+                                   _P, _P, _P, _P, _SZ, _P]),
+    "lmhead_workspace_size": (_SZ, [_I64, _I64, _I64]),
+    "lmhead_int4_gemv": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _SZ, _P]),
+    "bitmoe_rmsnorm": (ctypes.c_int, [_P, _I64, _I64, ctypes.c_float, _P, _P]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+EXPORTED = tuple(_SIGS)
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != OK:
+        raise BitmoeError(fn, rc)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _need(t, dtype, shape, name):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: expected {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def version() -> str:
+    return _lib.bitmoe_version().decode()
+
+
+# ---------------------------------------------------------------- weights
+
+
+def bitmoe_packed_int4_bytes(n_mats: int, rows: int, K: int, group: int = GROUP) -> int:
+    return int(_lib.bitmoe_packed_int4_bytes(n_mats, rows, K, group))
+
+
+def bitmoe_pack_int4(q: torch.Tensor, scale: torch.Tensor, group: int = GROUP) -> torch.Tensor:
+    """Canonical bank q uint8 [n, rows, K/2] + scale fp16 [n, rows, K/group] -> packed uint8 tiles."""
+    if q.dim() == 2:
+        q, scale = q.unsqueeze(0), scale.unsqueeze(0)
+    n, rows, kh = q.shape
+    K = kh * 2
+    _need(q, torch.uint8, (n, rows, kh), "q")
+    _need(scale, torch.float16, (n, rows, K // group), "scale")
+    nbytes = bitmoe_packed_int4_bytes(n, rows, K, group)
+    if nbytes == 0:
+        raise BitmoeError("bitmoe_pack_int4", 2)
+    out = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    _check("bitmoe_pack_int4", _lib.bitmoe_pack_int4(_ptr(q), _ptr(scale), n, rows, K, group, _ptr(out), _stream()))
+    return out
+
+
+@dataclass
+class MoeLayer:
+    """Device-resident weights of one MoE layer (packed banks + fp32 router)."""
+    d: int
+    E: int
+    k: int
+    I: int
+    gate: torch.Tensor
+    up: torch.Tensor
+    down: torch.Tensor
+    w_router: torch.Tensor
+    b_router: torch.Tensor | None
+    renormalize: bool = True
+
+    @property
+    def shape(self) -> MoeShape:
+        return MoeShape(self.d, self.E, self.k, self.I, GROUP, int(self.renormalize))
+
+    @property
+    def weights(self) -> MoeWeights:
+        return MoeWeights(self.gate.data_ptr(), self.up.data_ptr(), self.down.data_ptr(),
+                          self.w_router.data_ptr(), None if self.b_router is None else self.b_router.data_ptr())
+
+    @classmethod
+    def from_canonical(cls, tensors: dict, k: int, device="cuda", renormalize: bool = True) -> "MoeLayer":
+        """Build from host/device canonical tensors (gate_q/gate_s/.../w_router/b_router)."""
+        def dev(name, dtype):
+            t = tensors[name]
+            if not isinstance(t, torch.Tensor):
+                t = torch.from_numpy(t)
+            if dtype == torch.float16 and t.dtype != torch.float16:
+                t = t.view(torch.float16) if t.dtype in (torch.int16, torch.uint16) else t.to(torch.float16)
+            return t.to(device=device).contiguous()
+        gq, gs = dev("gate_q", torch.uint8), dev("gate_s", torch.float16)
+        E, I, dh = gq.shape
+        d = dh * 2
+        b = tensors.get("b_router")
+        return cls(
+            d=d, E=E, k=k, I=I,
+            gate=bitmoe_pack_int4(gq, gs),
+            up=bitmoe_pack_int4(dev("up_q", torch.uint8), dev("up_s", torch.float16)),
+            down=bitmoe_pack_int4(dev("down_q", torch.uint8), dev("down_s", torch.float16)),
+            w_router=dev("w_router", torch.float32),
+            b_router=None if b is None else dev("b_router", torch.float32),
+            renormalize=renormalize)
+
+
+def moe_workspace_size(layer_or_shape, T: int) -> int:
+    sh = layer_or_shape.shape if isinstance(layer_or_shape, MoeLayer) else layer_or_shape
+    return int(_lib.moe_workspace_size(ctypes.byref(sh), T))
+
+
+def moe_workspace(layer: MoeLayer, T: int) -> torch.Tensor:
+    """A zero-filled workspace for calls on up to T tokens (its status word starts clear)."""
+    n = moe_workspace_size(layer, T)
+    if n == 0:
+        raise BitmoeError("moe_workspace_size", 2)
+    return torch.zeros(n, dtype=torch.uint8, device=layer.gate.device)
+
+
+def bitmoe_get_device_status(workspace: torch.Tensor, clear: bool = False) -> int:
+    out = ctypes.c_int32(0)
+    _check("bitmoe_get_device_status",
+           _lib.bitmoe_get_device_status(_ptr(workspace), int(clear), ctypes.byref(out), _stream()))
+    return out.value
+
+
+# ---------------------------------------------------------------- MoE layer entry points
+
+
+def moe_route(x, layer: MoeLayer, workspace, want_logits: bool = False):
+    T = x.shape[0]
+    _need(x, torch.bfloat16, (T, layer.d), "x")
+    ids = torch.empty((T, layer.k), dtype=torch.int32, device=x.device)
+    w = torch.empty((T, layer.k), dtype=torch.float32, device=x.device)
+    logits = torch.empty((T, layer.E), dtype=torch.float32, device=x.device) if want_logits else None
+    sh = layer.shape
+    _check("moe_route", _lib.moe_route(_ptr(x), T, ctypes.byref(sh), _ptr(layer.w_router), _ptr(layer.b_router),
+                                       _ptr(ids), _ptr(w), _ptr(logits), _ptr(workspace), workspace.numel(),
+                                       _stream()))
+    return (ids, w, logits) if want_logits else (ids, w)
+
+
+def moe_permute(ids, layer: MoeLayer, workspace):
+    T = ids.shape[0]
+    _need(ids, torch.int32, (T, layer.k), "ids")
+    dev = ids.device
+    offsets = torch.empty(layer.E + 1, dtype=torch.int32, device=dev)
+    rows = torch.empty(T * layer.k, dtype=torch.int32, device=dev)
+    inv = torch.empty(T * layer.k, dtype=torch.int32, device=dev)
+    sh = layer.shape
+    _check("moe_permute", _lib.moe_permute(_ptr(ids), T, ctypes.byref(sh), _ptr(offsets), _ptr(rows), _ptr(inv),
+                                           _ptr(workspace), workspace.numel(), _stream()))
+    return offsets, rows, inv
+
+
+def moe_expert_ffn_int4(x, layer: MoeLayer, offsets, sorted_rows, workspace):
+    T = x.shape[0]
+    _need(x, torch.bfloat16, (T, layer.d), "x")
+    _need(offsets, torch.int32, (layer.E + 1,), "offsets")
+    _need(sorted_rows, torch.int32, (T * layer.k,), "sorted_rows")
+    y = torch.empty((T * layer.k, layer.d), dtype=torch.float32, device=x.device)
+    sh, wt = layer.shape, layer.weights
+    _check("moe_expert_ffn_int4", _lib.moe_expert_ffn_int4(_ptr(x), T, ctypes.byref(sh), ctypes.byref(wt),
+                                                           _ptr(offsets), _ptr(sorted_rows), _ptr(y),
+                                                           _ptr(workspace), workspace.numel(), _stream()))
+    return y
+
+
+def moe_combine(y_rows, inv_rows, topk_w, residual, layer: MoeLayer, out=None, want_f32: bool = True):
+    T = residual.shape[0]
+    _need(residual, torch.bfloat16, (T, layer.d), "residual")
+    out = torch.empty_like(residual) if out is None else out
+    out_f32 = torch.empty((T, layer.d), dtype=torch.float32, device=residual.device) if want_f32 else None
+    sh = layer.shape
+    _check("moe_combine", _lib.moe_combine(_ptr(y_rows), _ptr(inv_rows), _ptr(topk_w), _ptr(residual), T,
+                                           ctypes.byref(sh), _ptr(out), _ptr(out_f32), _stream()))
+    return out, out_f32
+
+
+def moe_forward(x, layer: MoeLayer, workspace, residual=None, forced_ids=None, forced_w=None, out=None,
+                out_f32=None, ids_out=None, w_out=None):
+    """One MoE layer: returns (out bf16 [T,d], out_f32 or None, ids or None, w or None)."""
+    T = x.shape[0]
+    _need(x, torch.bfloat16, (T, layer.d), "x")
+    residual = x if residual is None else residual
+    _need(residual, torch.bfloat16, (T, layer.d), "residual")
+    if forced_ids is not None:
+        _need(forced_ids, torch.int32, (T, layer.k), "forced_ids")
+        _need(forced_w, torch.float32, (T, layer.k), "forced_w")
+    out = torch.empty_like(x) if out is None else out
+    sh, wt = layer.shape, layer.weights
+    _check("moe_forward", _lib.moe_forward(_ptr(x), _ptr(residual), T, ctypes.byref(sh), ctypes.byref(wt),
+                                           _ptr(forced_ids), _ptr(forced_w), _ptr(ids_out), _ptr(w_out), _ptr(out),
+                                           _ptr(out_f32), _ptr(workspace), workspace.numel(), _stream()))
+    return out, out_f32, ids_out, w_out
+
+
+# ---------------------------------------------------------------- LM head and norm
+
+
+def lmhead_workspace(T: int, d: int, V: int, device="cuda") -> torch.Tensor:
+    return torch.zeros(int(_lib.lmhead_workspace_size(T, d, V)), dtype=torch.uint8, device=device)
+
+
+def lmhead_int4_gemv(h, w_packed, V: int, workspace, want_logits: bool = True, logits=None, argmax=None):
+    T, d = h.shape
+    _need(h, torch.bfloat16, (T, d), "h")
+    logits = (torch.empty((T, V), dtype=torch.float32, device=h.device) if want_logits else None) \
+        if logits is None else logits
+    argmax = torch.empty(T, dtype=torch.int32, device=h.device) if argmax is None else argmax
+    _check("lmhead_int4_gemv", _lib.lmhead_int4_gemv(_ptr(h), T, d, V, GROUP, _ptr(w_packed), _ptr(logits),
+                                                     _ptr(argmax), _ptr(workspace), workspace.numel(), _stream()))
+    return logits, argmax
+
+
+def bitmoe_rmsnorm(x, eps: float = 1e-6, out=None):
+    T, d = x.shape
+    _need(x, torch.bfloat16, (T, d), "x")
+    out = torch.empty_like(x) if out is None else out
+    _check("bitmoe_rmsnorm", _lib.bitmoe_rmsnorm(_ptr(x), T, d, eps, _ptr(out), _stream()))
+    return out

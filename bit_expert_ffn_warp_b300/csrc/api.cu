@@ -1,0 +1,298 @@
+// C ABI of the int4 MoE layer and LM head: argument checks, workspace layout
+// and the launch sequence of each entry point.  See include/bitmoe.h.
+#include <string.h>
+
+#include "kernels.h"
+
+using namespace bitmoe;
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+bitmoe_status_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return BITMOE_OK;
+  g_last_cuda_error = (int)e;
+  return BITMOE_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int64_t kMaxRows = int64_t(1) << 22;  // T*k limit (int32 positions with headroom)
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Workspace carve-up shared by every MoE entry point.
+struct MoeWs {
+  DevStatus* st;
+  int32_t* ids;
+  float* w;
+  float* logits;
+  int32_t* offsets;
+  int32_t* sorted_rows;
+  int32_t* inv;
+  int32_t* blk_prefix;
+  void* perm_scratch;
+  __half* h_hi;
+  __half* h_lo;
+  float* y_rows;
+  size_t total;
+};
+
+MoeWs moe_layout(const bitmoe_moe_shape_t* sh, int64_t T, void* base) {
+  const int64_t R = T * sh->k;
+  char* p = static_cast<char*>(base);
+  size_t off = 0;
+  MoeWs w;
+  auto take = [&](size_t bytes) {
+    char* q = p ? p + off : nullptr;
+    off += align256(bytes);
+    return q;
+  };
+  w.st = reinterpret_cast<DevStatus*>(take(256));
+  w.ids = reinterpret_cast<int32_t*>(take((size_t)R * 4));
+  w.w = reinterpret_cast<float*>(take((size_t)R * 4));
+  w.logits = reinterpret_cast<float*>(take((size_t)T * sh->E * 4));
+  w.offsets = reinterpret_cast<int32_t*>(take((size_t)(sh->E + 1) * 4));
+  w.sorted_rows = reinterpret_cast<int32_t*>(take((size_t)R * 4));
+  w.inv = reinterpret_cast<int32_t*>(take((size_t)R * 4));
+  w.blk_prefix = reinterpret_cast<int32_t*>(take((size_t)(sh->E + 1) * 4));
+  w.perm_scratch = take(permute_scratch_bytes(R, (int)sh->E));
+  w.h_hi = reinterpret_cast<__half*>(take((size_t)R * sh->I * 2));
+  w.h_lo = reinterpret_cast<__half*>(take((size_t)R * sh->I * 2));
+  w.y_rows = reinterpret_cast<float*>(take((size_t)R * sh->d * 4));
+  w.total = off;
+  return w;
+}
+
+bitmoe_status_t check_shape(const bitmoe_moe_shape_t* sh, int64_t T) {
+  if (sh == nullptr || T < 0) return BITMOE_ERR_INVALID_ARG;
+  if (sh->d <= 0 || sh->E <= 0 || sh->k <= 0 || sh->I <= 0) return BITMOE_ERR_INVALID_ARG;
+  if (sh->k > sh->E || sh->k > kMaxK) return BITMOE_ERR_INVALID_ARG;
+  if (sh->group != kGroup) return BITMOE_ERR_UNSUPPORTED;
+  if (sh->d % kChunkK || sh->I % kChunkK) return BITMOE_ERR_UNSUPPORTED;
+  if (sh->E > kMaxE || sh->d > 16384 || sh->I > 16384) return BITMOE_ERR_UNSUPPORTED;
+  if (T * sh->k > kMaxRows) return BITMOE_ERR_UNSUPPORTED;
+  return BITMOE_OK;
+}
+
+bitmoe_status_t check_ws(const bitmoe_moe_shape_t* sh, int64_t T, void* ws, size_t ws_bytes) {
+  if (ws == nullptr || !aligned16(ws)) return BITMOE_ERR_WORKSPACE;
+  if (ws_bytes < moe_layout(sh, T, nullptr).total) return BITMOE_ERR_WORKSPACE;
+  return BITMOE_OK;
+}
+
+bitmoe_status_t check_weights(const bitmoe_moe_weights_t* wt, bool need_router) {
+  if (wt == nullptr) return BITMOE_ERR_INVALID_ARG;
+  if (!wt->gate || !wt->up || !wt->down) return BITMOE_ERR_INVALID_ARG;
+  if (!aligned16(wt->gate) || !aligned16(wt->up) || !aligned16(wt->down)) return BITMOE_ERR_INVALID_ARG;
+  if (need_router && (!wt->w_router || !aligned16(wt->w_router))) return BITMOE_ERR_INVALID_ARG;
+  return BITMOE_OK;
+}
+
+FfnArgs ffn_args(const uint16_t* x, int64_t T, const bitmoe_moe_shape_t* sh, const bitmoe_moe_weights_t* wt,
+                 const int32_t* offsets, const int32_t* sorted_rows, const int32_t* blk_prefix, const MoeWs& w,
+                 float* y_rows) {
+  FfnArgs a;
+  a.x = x;
+  a.T = (int)T;
+  a.d = (int)sh->d;
+  a.I = (int)sh->I;
+  a.E = (int)sh->E;
+  a.k = (int)sh->k;
+  a.gate = wt->gate;
+  a.up = wt->up;
+  a.down = wt->down;
+  a.offsets = offsets;
+  a.sorted_rows = sorted_rows;
+  a.blk_prefix = blk_prefix;
+  a.h_hi = w.h_hi;
+  a.h_lo = w.h_lo;
+  a.y_rows = y_rows;
+  a.st = w.st;
+  return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* bitmoe_status_string(bitmoe_status_t status) {
+  switch (status) {
+    case BITMOE_OK: return "ok";
+    case BITMOE_ERR_INVALID_ARG: return "invalid argument";
+    case BITMOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case BITMOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case BITMOE_ERR_CUDA: return "CUDA launch error";
+    case BITMOE_ERR_TIMEOUT: return "device wait timed out";
+    case BITMOE_ERR_DEVICE_CHECK: return "device-side input check failed";
+  }
+  return "unknown status";
+}
+
+int bitmoe_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* bitmoe_version(void) { return "bitmoe 0.1 (sm_103a)"; }
+
+size_t bitmoe_packed_int4_bytes(int64_t n_mats, int64_t rows, int64_t K, int64_t group) {
+  if (n_mats <= 0 || rows <= 0 || K <= 0 || group != kGroup || rows % kTileRows || K % kChunkK) return 0;
+  return (size_t)n_mats * (size_t)(rows / kTileRows) * (size_t)tile_bytes(K);
+}
+
+bitmoe_status_t bitmoe_pack_int4(const uint8_t* q, const uint16_t* scale, int64_t n_mats, int64_t rows, int64_t K,
+                                 int64_t group, uint8_t* packed, void* stream) {
+  if (!q || !scale || !packed) return BITMOE_ERR_INVALID_ARG;
+  if (bitmoe_packed_int4_bytes(n_mats, rows, K, group) == 0) return BITMOE_ERR_UNSUPPORTED;
+  if (!aligned16(packed) || (reinterpret_cast<uintptr_t>(q) & 3u) || (reinterpret_cast<uintptr_t>(scale) & 1u))
+    return BITMOE_ERR_INVALID_ARG;
+  return cuda_status(launch_pack_int4(q, scale, n_mats, rows, K, packed, (cudaStream_t)stream));
+}
+
+bitmoe_status_t bitmoe_get_device_status(void* workspace, int clear, int32_t* status_out, void* stream) {
+  if (!workspace || !status_out) return BITMOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  DevStatus hs;
+  cudaError_t e = cudaMemcpyAsync(&hs, workspace, sizeof(hs), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && clear) {
+    e = cudaMemsetAsync(workspace, 0, sizeof(DevStatus), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  }
+  if (e != cudaSuccess) return cuda_status(e);
+  *status_out = hs.code;
+  return BITMOE_OK;
+}
+
+size_t moe_workspace_size(const bitmoe_moe_shape_t* shape, int64_t T) {
+  if (check_shape(shape, T) != BITMOE_OK) return 0;
+  return moe_layout(shape, T, nullptr).total;
+}
+
+bitmoe_status_t moe_route(const uint16_t* x, int64_t T, const bitmoe_moe_shape_t* shape, const float* w_router,
+                          const float* b_router, int32_t* topk_ids, float* topk_w, float* logits_out,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  bitmoe_status_t st = check_shape(shape, T);
+  if (st != BITMOE_OK) return st;
+  if (T == 0) return BITMOE_OK;
+  if (!x || !w_router || !topk_ids || !topk_w) return BITMOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router)) return BITMOE_ERR_INVALID_ARG;
+  if ((st = check_ws(shape, T, workspace, workspace_bytes)) != BITMOE_OK) return st;
+  const MoeWs w = moe_layout(shape, T, workspace);
+  cudaStream_t s = (cudaStream_t)stream;
+  float* logits = logits_out ? logits_out : w.logits;
+  cudaError_t e = launch_router_logits(x, (int)T, (int)shape->d, (int)shape->E, w_router, b_router, logits, s);
+  if (e == cudaSuccess)
+    e = launch_topk_gates(logits, (int)T, (int)shape->E, (int)shape->k, shape->renormalize, topk_ids, topk_w, s);
+  return cuda_status(e);
+}
+
+bitmoe_status_t moe_permute(const int32_t* topk_ids, int64_t T, const bitmoe_moe_shape_t* shape,
+                            int32_t* expert_offsets, int32_t* sorted_rows, int32_t* inv_rows, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  bitmoe_status_t st = check_shape(shape, T);
+  if (st != BITMOE_OK) return st;
+  if (!expert_offsets || (T > 0 && (!topk_ids || !sorted_rows || !inv_rows))) return BITMOE_ERR_INVALID_ARG;
+  if ((st = check_ws(shape, T, workspace, workspace_bytes)) != BITMOE_OK) return st;
+  const MoeWs w = moe_layout(shape, T, workspace);
+  return cuda_status(launch_permute(topk_ids, (int)(T * shape->k), (int)shape->E, expert_offsets, sorted_rows,
+                                    inv_rows, w.blk_prefix, w.perm_scratch, w.st, (cudaStream_t)stream));
+}
+
+bitmoe_status_t moe_expert_ffn_int4(const uint16_t* x, int64_t T, const bitmoe_moe_shape_t* shape,
+                                    const bitmoe_moe_weights_t* weights, const int32_t* expert_offsets,
+                                    const int32_t* sorted_rows, float* y_rows, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  bitmoe_status_t st = check_shape(shape, T);
+  if (st != BITMOE_OK) return st;
+  if (T == 0) return BITMOE_OK;
+  if ((st = check_weights(weights, false)) != BITMOE_OK) return st;
+  if (!x || !expert_offsets || !sorted_rows || !y_rows || !aligned16(x) || !aligned16(y_rows))
+    return BITMOE_ERR_INVALID_ARG;
+  if ((st = check_ws(shape, T, workspace, workspace_bytes)) != BITMOE_OK) return st;
+  const MoeWs w = moe_layout(shape, T, workspace);
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = launch_blk_prefix(expert_offsets, (int)shape->E, w.blk_prefix, s);
+  const FfnArgs a = ffn_args(x, T, shape, weights, expert_offsets, sorted_rows, w.blk_prefix, w, y_rows);
+  if (e == cudaSuccess) e = launch_ffn_up(a, s);
+  if (e == cudaSuccess) e = launch_ffn_down(a, s);
+  return cuda_status(e);
+}
+
+bitmoe_status_t moe_combine(const float* y_rows, const int32_t* inv_rows, const float* topk_w,
+                            const uint16_t* residual, int64_t T, const bitmoe_moe_shape_t* shape, uint16_t* out,
+                            float* out_f32, void* stream) {
+  bitmoe_status_t st = check_shape(shape, T);
+  if (st != BITMOE_OK) return st;
+  if (T == 0) return BITMOE_OK;
+  if (!y_rows || !inv_rows || !topk_w || !residual || !out) return BITMOE_ERR_INVALID_ARG;
+  if (!aligned16(y_rows) || !aligned16(residual) || !aligned16(out) || (out_f32 && !aligned16(out_f32)))
+    return BITMOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(y_rows, inv_rows, topk_w, residual, (int)T, (int)shape->d, (int)shape->k, out,
+                                    out_f32, (cudaStream_t)stream));
+}
+
+bitmoe_status_t moe_forward(const uint16_t* x, const uint16_t* residual, int64_t T, const bitmoe_moe_shape_t* shape,
+                            const bitmoe_moe_weights_t* weights, const int32_t* forced_ids, const float* forced_w,
+                            int32_t* topk_ids_out, float* topk_w_out, uint16_t* out, float* out_f32,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  bitmoe_status_t st = check_shape(shape, T);
+  if (st != BITMOE_OK) return st;
+  if (T == 0) return BITMOE_OK;
+  if ((forced_ids == nullptr) != (forced_w == nullptr)) return BITMOE_ERR_INVALID_ARG;
+  if ((st = check_weights(weights, forced_ids == nullptr)) != BITMOE_OK) return st;
+  if (!x || !residual || !out || !aligned16(x) || !aligned16(residual) || !aligned16(out) ||
+      (out_f32 && !aligned16(out_f32)))
+    return BITMOE_ERR_INVALID_ARG;
+  if ((st = check_ws(shape, T, workspace, workspace_bytes)) != BITMOE_OK) return st;
+  const MoeWs w = moe_layout(shape, T, workspace);
+  cudaStream_t s = (cudaStream_t)stream;
+  const int Ti = (int)T, d = (int)shape->d, E = (int)shape->E, k = (int)shape->k;
+  cudaError_t e;
+  if (forced_ids) {
+    e = launch_forced_select(forced_ids, forced_w, Ti, E, k, w.ids, w.w, w.st, s);
+  } else {
+    e = launch_router_logits(x, Ti, d, E, weights->w_router, weights->b_router, w.logits, s);
+    if (e == cudaSuccess) e = launch_topk_gates(w.logits, Ti, E, k, shape->renormalize, w.ids, w.w, s);
+  }
+  if (e == cudaSuccess)
+    e = launch_permute(w.ids, Ti * k, E, w.offsets, w.sorted_rows, w.inv, w.blk_prefix, w.perm_scratch, w.st, s);
+  const FfnArgs a = ffn_args(x, T, shape, weights, w.offsets, w.sorted_rows, w.blk_prefix, w, w.y_rows);
+  if (e == cudaSuccess) e = launch_ffn_up(a, s);
+  if (e == cudaSuccess) e = launch_ffn_down(a, s);
+  if (e == cudaSuccess) e = launch_combine(w.y_rows, w.inv, w.w, residual, Ti, d, k, out, out_f32, s);
+  if (e == cudaSuccess && topk_ids_out)
+    e = cudaMemcpyAsync(topk_ids_out, w.ids, (size_t)T * k * 4, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && topk_w_out)
+    e = cudaMemcpyAsync(topk_w_out, w.w, (size_t)T * k * 4, cudaMemcpyDeviceToDevice, s);
+  return cuda_status(e);
+}
+
+size_t lmhead_workspace_size(int64_t T, int64_t d, int64_t V) {
+  if (T < 0 || d <= 0 || V <= 0) return 0;
+  return 256 + align256(lmhead_scratch_bytes((int)T));
+}
+
+bitmoe_status_t lmhead_int4_gemv(const uint16_t* h, int64_t T, int64_t d, int64_t V, int64_t group,
+                                 const uint8_t* w_packed, float* logits, int32_t* argmax, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  if (T < 0 || d <= 0 || V <= 0) return BITMOE_ERR_INVALID_ARG;
+  if (group != kGroup || d % kChunkK || V % kTileRows || T > 64 || d > 16384 || V > (int64_t(1) << 30))
+    return BITMOE_ERR_UNSUPPORTED;
+  if (T == 0) return BITMOE_OK;
+  if (!h || !w_packed || !argmax || !aligned16(h) || !aligned16(w_packed)) return BITMOE_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < lmhead_workspace_size(T, d, V))
+    return BITMOE_ERR_WORKSPACE;
+  DevStatus* st = static_cast<DevStatus*>(workspace);
+  void* keys = static_cast<char*>(workspace) + 256;
+  return cuda_status(launch_lmhead(h, (int)T, (int)d, (int)V, w_packed, logits, argmax, keys, st,
+                                   (cudaStream_t)stream));
+}
+
+bitmoe_status_t bitmoe_rmsnorm(const uint16_t* x, int64_t T, int64_t d, float eps, uint16_t* y, void* stream) {
+  if (T < 0 || d <= 0 || d % 8 || !(eps >= 0.f)) return BITMOE_ERR_INVALID_ARG;
+  if (T == 0) return BITMOE_OK;
+  if (!x || !y || !aligned16(x) || !aligned16(y)) return BITMOE_ERR_INVALID_ARG;
+  return cuda_status(launch_rmsnorm(x, (int)T, (int)d, eps, y, (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,193 @@
+// Device helpers shared by the bitmoe kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "../../include/bitmoe.h"
+
+namespace bitmoe {
+
+// ---------------------------------------------------------------- constants
+
+constexpr int kGroup = 32;          // int4 scale group along the reduction dim
+constexpr int kTileRows = 16;       // rows per packed tile (one mma M)
+constexpr int kChunkK = 128;        // columns per packed chunk (four groups)
+constexpr int kChunkQBytes = 1024;  // 16 rows x 128 cols x 4 bits
+constexpr int kChunkSBytes = 128;   // 16 rows x 4 groups x fp16
+constexpr int kChunkBytes = kChunkQBytes + kChunkSBytes;
+constexpr int kTokBlock = 16;       // tokens per unit of the streaming FFN kernels
+constexpr int kSmemRowPad = 64;     // bytes of padding per staged activation row (bank spread)
+constexpr int kPermChunk = 1024;    // rows per permutation chunk
+constexpr int kMaxE = 1024;
+constexpr int kMaxK = 32;
+
+// Device status word values (see bitmoe_get_device_status).
+constexpr int kStatusTimeout = BITMOE_ERR_TIMEOUT;
+constexpr int kStatusCheck = BITMOE_ERR_DEVICE_CHECK;
+
+// A bounded wait gives up after this long and records kStatusTimeout.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+__host__ __device__ constexpr int64_t tile_bytes(int64_t K) { return (K / kChunkK) * kChunkBytes; }
+
+// ---------------------------------------------------------------- status word
+
+struct DevStatus {
+  int code;        // first error code recorded (0 = none)
+  int where;       // site id of the first error
+  int detail;      // extra (e.g. offending index)
+  int pad;
+};
+
+__device__ __forceinline__ void record_status(DevStatus* st, int code, int where, int detail) {
+  if (st == nullptr) return;
+  if (atomicCAS(&st->code, 0, code) == 0) {
+    st->where = where;
+    st->detail = detail;
+  }
+}
+
+// ---------------------------------------------------------------- PTX: timers, smem, mbarrier, bulk copy
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of an mbarrier; false (and a recorded timeout) if it
+// does not complete within kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, DevStatus* st, int where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      record_status(st, kStatusTimeout, where, 0);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Bulk copy global -> shared (TMA, non-tensor), completion counted on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// L2 prefetch of a global range (bulk, no completion tracking).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// ---------------------------------------------------------------- mma.sync m16n8k16
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
+                                         const float (&c)[4]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%11,%12,%13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
+        "f"(c[3]));
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
+                                        const float (&c)[4]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%11,%12,%13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
+        "f"(c[3]));
+}
+
+// ---------------------------------------------------------------- int4 -> 16-bit pairs
+//
+// A packed word holds the 8 nibbles one thread feeds to two k16 mma steps:
+// pair p (p = 0..3) sits at bits [4p, 4p+4) (first element) and
+// [16+4p, 20+4p) (second element).  Masking with 0x000F000F after a shift by
+// 4p puts the two nibbles in the low bits of each 16-bit half; XOR with 8
+// turns the two's-complement nibble n into q + 8, and OR-ing an exponent
+// pattern makes each half the float B + q + 8 with B = 128 (bf16) or 1024
+// (fp16), whose spacing is 1.  Subtracting B + 8 leaves q exactly.
+
+__device__ __forceinline__ uint32_t nib_pair_bf16(uint32_t w, int p) {
+  uint32_t t = ((w >> (4 * p)) & 0x000F000Fu) ^ 0x43084308u;  // 136 + q in each half
+  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&t);
+  const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
+  v = __hsub2(v, off);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t nib_pair_f16(uint32_t w, int p) {
+  uint32_t t = ((w >> (4 * p)) & 0x000F000Fu) ^ 0x64086408u;  // 1032 + q in each half
+  __half2 v = *reinterpret_cast<__half2*>(&t);
+  const __half2 off = __floats2half2_rn(1032.0f, 1032.0f);
+  v = __hsub2(v, off);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ---------------------------------------------------------------- misc
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
+  __nv_bfloat16 h = __float2bfloat16_rn(f);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+
+__device__ __forceinline__ float silu_mul(float a, float u) { return a / (1.0f + expf(-a)) * u; }
+
+// Order-preserving map of a float onto uint32 (for packed argmax keys).
+__device__ __forceinline__ uint32_t float_order_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+template <typename T>
+__host__ __device__ constexpr T ceil_div(T a, T b) {
+  return (a + b - 1) / b;
+}
+
+}  // namespace bitmoe

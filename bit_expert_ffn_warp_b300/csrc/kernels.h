@@ -1,0 +1,59 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace bitmoe {
+
+// ---------------------------------------------------------------- routing (route.cu)
+cudaError_t launch_router_logits(const uint16_t* x, int T, int d, int E, const float* w_router,
+                                 const float* b_router, float* logits, cudaStream_t s);
+cudaError_t launch_topk_gates(const float* logits, int T, int E, int k, int renorm, int32_t* ids, float* w,
+                              cudaStream_t s);
+cudaError_t launch_forced_select(const int32_t* forced_ids, const float* forced_w, int T, int E, int k,
+                                 int32_t* ids, float* w, DevStatus* st, cudaStream_t s);
+
+// ---------------------------------------------------------------- permutation (permute.cu)
+// Scratch needed by launch_permute (bytes), for R = T*k rows.
+size_t permute_scratch_bytes(int64_t R, int E);
+// Stable counting sort of R ids into E buckets; also writes blk_prefix[E+1]:
+// exclusive prefix of ceil(count_e / kTokBlock).
+cudaError_t launch_permute(const int32_t* ids, int R, int E, int32_t* offsets, int32_t* sorted_rows, int32_t* inv,
+                           int32_t* blk_prefix, void* scratch, DevStatus* st, cudaStream_t s);
+// blk_prefix from offsets only (standalone expert-FFN entry point).
+cudaError_t launch_blk_prefix(const int32_t* offsets, int E, int32_t* blk_prefix, cudaStream_t s);
+
+// ---------------------------------------------------------------- expert FFN (ffn.cu)
+struct FfnArgs {
+  const uint16_t* x;  // [T, d] bf16
+  int T, d, I, E, k;
+  const uint8_t* gate;  // packed banks
+  const uint8_t* up;
+  const uint8_t* down;
+  const int32_t* offsets;      // [E+1]
+  const int32_t* sorted_rows;  // [R]
+  const int32_t* blk_prefix;   // [E+1]
+  __half* h_hi;                // [R, I]
+  __half* h_lo;                // [R, I]
+  float* y_rows;               // [R, d]
+  DevStatus* st;
+};
+cudaError_t launch_ffn_up(const FfnArgs& a, cudaStream_t s);
+cudaError_t launch_ffn_down(const FfnArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------- combine / norm / pack (misc.cu)
+cudaError_t launch_combine(const float* y_rows, const int32_t* inv, const float* w, const uint16_t* resid, int T,
+                           int d, int k, uint16_t* out, float* out_f32, cudaStream_t s);
+cudaError_t launch_rmsnorm(const uint16_t* x, int T, int d, float eps, uint16_t* y, cudaStream_t s);
+cudaError_t launch_pack_int4(const uint8_t* q, const uint16_t* scale, int64_t n_mats, int64_t rows, int64_t K,
+                             uint8_t* packed, cudaStream_t s);
+
+// ---------------------------------------------------------------- LM head (lmhead.cu)
+size_t lmhead_scratch_bytes(int T);
+cudaError_t launch_lmhead(const uint16_t* h, int T, int d, int V, const uint8_t* w_packed, float* logits,
+                          int32_t* argmax, void* scratch, DevStatus* st, cudaStream_t s);
+
+}  // namespace bitmoe

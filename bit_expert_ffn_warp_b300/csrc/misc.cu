@@ -1,0 +1,153 @@
+// Combine into the residual, RMSNorm between stacked layers, weight packing.
+#include "kernels.h"
+
+namespace bitmoe {
+namespace {
+
+// out[t,c] = resid[t,c] + sum_j w[t,j] * y[inv[t*k+j], c]  (j ascending, fp32),
+// bf16 = round-to-nearest-even of that fp32 value.  8 columns per thread.
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ inv,
+                                                      const float* __restrict__ w, const uint16_t* resid, int d, int k,
+                                                      uint16_t* out, float* __restrict__ out_f32) {
+  const int t = blockIdx.x;
+  for (int c8 = threadIdx.x * 8; c8 < d; c8 += blockDim.x * 8) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < k; ++j) {
+      const int pos = inv[(size_t)t * k + j];
+      if (pos < 0) continue;
+      const float wj = w[(size_t)t * k + j];
+      const float4 y0 = *reinterpret_cast<const float4*>(y + (size_t)pos * d + c8);
+      const float4 y1 = *reinterpret_cast<const float4*>(y + (size_t)pos * d + c8 + 4);
+      acc[0] = fmaf(wj, y0.x, acc[0]);
+      acc[1] = fmaf(wj, y0.y, acc[1]);
+      acc[2] = fmaf(wj, y0.z, acc[2]);
+      acc[3] = fmaf(wj, y0.w, acc[3]);
+      acc[4] = fmaf(wj, y1.x, acc[4]);
+      acc[5] = fmaf(wj, y1.y, acc[5]);
+      acc[6] = fmaf(wj, y1.z, acc[6]);
+      acc[7] = fmaf(wj, y1.w, acc[7]);
+    }
+    const uint4 r = *reinterpret_cast<const uint4*>(resid + (size_t)t * d + c8);
+    const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+    float o[8];
+    uint32_t ob[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o[2 * i] = __uint_as_float(rw[i] << 16) + acc[2 * i];
+      o[2 * i + 1] = __uint_as_float(rw[i] & 0xffff0000u) + acc[2 * i + 1];
+      ob[i] = (uint32_t)float_to_bf16_bits(o[2 * i]) | ((uint32_t)float_to_bf16_bits(o[2 * i + 1]) << 16);
+    }
+    if (out_f32) {
+      *reinterpret_cast<float4*>(out_f32 + (size_t)t * d + c8) = make_float4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<float4*>(out_f32 + (size_t)t * d + c8 + 4) = make_float4(o[4], o[5], o[6], o[7]);
+    }
+    *reinterpret_cast<uint4*>(out + (size_t)t * d + c8) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+  }
+}
+
+// y = x / sqrt(mean(x^2) + eps) with unit gain; fp32 sums in a fixed tree order.
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t* x, int d, float eps, uint16_t* y) {
+  __shared__ float part[8];
+  const int t = blockIdx.x;
+  const uint16_t* xr = x + (size_t)t * d;
+  float ss = 0.f;
+  for (int c8 = threadIdx.x * 8; c8 < d; c8 += blockDim.x * 8) {
+    const uint4 r = *reinterpret_cast<const uint4*>(xr + c8);
+    const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float a = __uint_as_float(rw[i] << 16), b = __uint_as_float(rw[i] & 0xffff0000u);
+      ss = fmaf(a, a, ss);
+      ss = fmaf(b, b, ss);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) tot += part[i];
+  const float inv = 1.0f / sqrtf(tot / (float)d + eps);
+  for (int c8 = threadIdx.x * 8; c8 < d; c8 += blockDim.x * 8) {
+    const uint4 r = *reinterpret_cast<const uint4*>(xr + c8);
+    const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+    uint32_t ob[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float a = __uint_as_float(rw[i] << 16) * inv, b = __uint_as_float(rw[i] & 0xffff0000u) * inv;
+      ob[i] = (uint32_t)float_to_bf16_bits(a) | ((uint32_t)float_to_bf16_bits(b) << 16);
+    }
+    // each thread rewrites only the elements it read, so y may alias x
+    *reinterpret_cast<uint4*>(y + (size_t)t * d + c8) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+  }
+}
+
+// Canonical int4 bank -> packed tiles.  Packed word (row r, group G, quarter c)
+// holds the 8 values at columns 32G + 8c + m, m = 0..7: value m = 2p at bits
+// [4p, 4p+4), value m = 2p+1 at bits [16+4p, 20+4p).  Inside a 128-column
+// chunk the words are ordered [row][quarter][group-in-chunk], then the chunk's
+// fp16 scales as [row][group-in-chunk].
+__global__ void pack_int4_kernel(const uint8_t* __restrict__ q, const uint16_t* __restrict__ scale, int64_t n_mats,
+                                 int64_t rows, int64_t K, uint8_t* __restrict__ packed) {
+  const int64_t nch = K / kChunkK;
+  const int64_t tiles = n_mats * (rows / kTileRows);
+  const int64_t items = tiles * nch * kTileRows;  // one (tile, chunk, row) per thread
+  for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < items;
+       it += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(it % kTileRows);
+    const int64_t ch = (it / kTileRows) % nch;
+    const int64_t tile = it / (kTileRows * nch);
+    const int64_t grow = tile * kTileRows + r;  // row index over the whole bank (n_mats * rows)
+    const uint8_t* qrow = q + grow * (K / 2);
+    const uint16_t* srow = scale + grow * (K / kGroup);
+    uint8_t* chunk = packed + tile * tile_bytes(K) + ch * kChunkBytes;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t words[4];
+#pragma unroll
+      for (int gg = 0; gg < 4; ++gg) {
+        const int64_t k0 = (ch * 4 + gg) * kGroup + c * 8;
+        const uint32_t src = *reinterpret_cast<const uint32_t*>(qrow + k0 / 2);
+        uint32_t wv = 0;
+#pragma unroll
+        for (int pr = 0; pr < 4; ++pr) {
+          const uint32_t byte = (src >> (8 * pr)) & 0xffu;
+          wv |= (byte & 0xfu) << (4 * pr);
+          wv |= (byte >> 4) << (16 + 4 * pr);
+        }
+        words[gg] = wv;
+      }
+      *reinterpret_cast<uint4*>(chunk + (r * 4 + c) * 16) = make_uint4(words[0], words[1], words[2], words[3]);
+    }
+    uint16_t* sdst = reinterpret_cast<uint16_t*>(chunk + kChunkQBytes + r * 8);
+#pragma unroll
+    for (int gg = 0; gg < 4; ++gg) sdst[gg] = srow[ch * 4 + gg];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const float* y_rows, const int32_t* inv, const float* w, const uint16_t* resid, int T,
+                           int d, int k, uint16_t* out, float* out_f32, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  combine_kernel<<<T, 256, 0, s>>>(y_rows, inv, w, resid, d, k, out, out_f32);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(const uint16_t* x, int T, int d, float eps, uint16_t* y, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  rmsnorm_kernel<<<T, 256, 0, s>>>(x, d, eps, y);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_int4(const uint8_t* q, const uint16_t* scale, int64_t n_mats, int64_t rows, int64_t K,
+                             uint8_t* packed, cudaStream_t s) {
+  const int64_t items = n_mats * (rows / kTileRows) * (K / kChunkK) * kTileRows;
+  if (items == 0) return cudaSuccess;
+  const int grid = (int)(ceil_div<int64_t>(items, 256) < 148 * 64 ? ceil_div<int64_t>(items, 256) : 148 * 64);
+  pack_int4_kernel<<<grid, 256, 0, s>>>(q, scale, n_mats, rows, K, packed);
+  return cudaGetLastError();
+}
+
+}  // namespace bitmoe

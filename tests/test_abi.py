@@ -1,0 +1,87 @@
+"""The C-ABI library loads, exports every symbol include/bitmoe.h declares, and
+rejects bad arguments on the host before any launch (no GPU needed)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bitmoe.h")
+LIB = os.path.join(ROOT, "bit_expert_ffn_warp_b300", "libbitmoe.so")
+
+
+@pytest.fixture(scope="module")
+def built():
+    from bit_expert_ffn_warp_b300 import build
+    build.build()
+    assert os.path.exists(LIB)
+    return LIB
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[a-z_][\w\s\*]*?\b([a-z_]\w*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+def test_header_declares_the_six_path_calls():
+    names = declared_functions()
+    for n in ("moe_route", "moe_permute", "moe_expert_ffn_int4", "moe_combine", "moe_forward", "lmhead_int4_gemv"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(built):
+    out = subprocess.run(["nm", "-D", "--defined-only", built], capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    lib = ctypes.CDLL(built)
+    for n in declared_functions():
+        assert hasattr(lib, n)
+
+
+def test_binding_wraps_every_declared_symbol(built):
+    import bit_expert_ffn_warp_b300 as bm
+    assert sorted(bm.EXPORTED) == declared_functions()
+
+
+def test_host_side_validation_without_gpu(built):
+    import bit_expert_ffn_warp_b300 as bm
+    lib = bm._lib
+    sh = bm.MoeShape(2048, 256, 8, 512, 32, 1)
+    ws = lib.moe_workspace_size(ctypes.byref(sh), 1)
+    assert ws > 0
+    # the workspace grows with T and covers the per-row buffers
+    assert lib.moe_workspace_size(ctypes.byref(sh), 64) > ws
+    assert lib.moe_workspace_size(ctypes.byref(sh), 4096) >= 4096 * 8 * 2048 * 4
+    bad = [bm.MoeShape(2048, 256, 0, 512, 32, 1), bm.MoeShape(2048, 4, 8, 512, 32, 1),
+           bm.MoeShape(2048, 256, 33, 512, 32, 1)]
+    for b in bad:
+        assert lib.moe_workspace_size(ctypes.byref(b), 1) == 0
+    assert lib.moe_workspace_size(ctypes.byref(bm.MoeShape(2000, 256, 8, 512, 32, 1)), 1) == 0
+    assert lib.moe_workspace_size(ctypes.byref(bm.MoeShape(2048, 256, 8, 512, 64, 1)), 1) == 0
+    # null pointers -> INVALID_ARG, nothing launched
+    rc = lib.moe_route(None, 1, ctypes.byref(sh), None, None, None, None, None, None, 0, None)
+    assert rc == 1
+    wt = bm.MoeWeights(None, None, None, None, None)
+    rc = lib.moe_forward(None, None, 1, ctypes.byref(sh), ctypes.byref(wt), None, None, None, None, None, None,
+                         None, 0, None)
+    assert rc == 1
+    # forced ids without forced gates -> INVALID_ARG
+    rc = lib.moe_forward(None, None, 1, ctypes.byref(sh), ctypes.byref(wt), ctypes.c_void_p(16), None, None, None,
+                         None, None, None, 0, None)
+    assert rc == 1
+    # unsupported shapes
+    assert lib.bitmoe_packed_int4_bytes(1, 15, 2048, 32) == 0
+    assert lib.bitmoe_packed_int4_bytes(1, 16, 2000, 32) == 0
+    assert lib.bitmoe_packed_int4_bytes(256, 512, 2048, 32) == 256 * 512 * 2048 * 9 // 16
+    assert lib.lmhead_int4_gemv(None, 65, 2048, 131072, 32, None, None, None, None, 0, None) == 2
+    assert lib.lmhead_int4_gemv(None, 1, 2048, 131072, 16, None, None, None, None, 0, None) == 2
+    # T = 0 is a no-op that succeeds
+    assert lib.moe_forward(None, None, 0, ctypes.byref(sh), ctypes.byref(wt), None, None, None, None, None, None,
+                           None, 0, None) == 0
+    for code in range(7):
+        assert lib.bitmoe_status_string(code)

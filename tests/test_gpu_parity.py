@@ -1,0 +1,323 @@
+"""GPU parity of every kernel of the path against the fp64 oracle, called
+through the C ABI (via the ctypes binding), on seeded synthetic inputs.
+
+Bars: expert ids and the permutation bit-exact (oracle choice fed to both
+sides where its k-th/(k+1)-th logit gap is below 1e-5); layer outputs within
+max-abs 2e-2 and rel-L2 1e-3 on the fp32 copy, whose bf16 rounding must equal
+the bf16 output bit for bit; the LM-head argmax exact unless its top-2 gap is
+below 1e-5.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import (FLINT, MAX_ABS, NEAR_TIE, REL_L2, TINY, bf16_bits_to_f64, bf16_ulp, bits_from_torch_bf16,
+                     device_layer, layer_tensors, max_abs, rel_l2, torch_bf16_from_bits)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import bit_expert_ffn_warp_b300 as bm  # noqa: E402
+
+
+# ------------------------------------------------------------------ fixtures
+
+_CACHE = {}
+
+
+def flint_layer(bias="normal", seed=11):
+    key = ("flint", bias, seed)
+    if key not in _CACHE:
+        t = layer_tensors(seed, FLINT["d"], FLINT["E"], FLINT["I"], bias=bias)
+        _CACHE[key] = (t, device_layer(t, FLINT["k"]))
+    return _CACHE[key]
+
+
+def tiny_layer(seed=0, bias="zero", renorm=True):
+    t = layer_tensors(seed, TINY["d"], TINY["E"], TINY["I"], bias=bias)
+    return t, device_layer(t, TINY["k"], renormalize=renorm)
+
+
+def check_layer_output(out, out_f32, ref, tag=""):
+    o32 = out_f32.cpu().numpy().astype(np.float64)
+    ma, rl = max_abs(o32, ref), rel_l2(o32, ref)
+    assert ma <= MAX_ABS and rl <= REL_L2, f"{tag}: max-abs {ma:.3g} rel-L2 {rl:.3g}"
+    # bf16 output is the nearest-even rounding of the fp32 copy, bit for bit
+    rounded = bits_from_torch_bf16(out_f32.to(torch.bfloat16))
+    assert np.array_equal(bits_from_torch_bf16(out), rounded), tag
+    # and, away from cancellation, it is the oracle's own bf16 rounding: both
+    # sides round the same value unless it lies within the fp32 error of a
+    # rounding boundary, which happens for a small fraction of elements
+    ob = bits_from_torch_bf16(out)
+    agree = float(np.mean(ob == oracle.f64_to_bf16(ref.reshape(-1)).reshape(ref.shape))) if ref.size < 300000 else \
+        float(np.mean(ob.reshape(-1)[::7] == oracle.f64_to_bf16(ref.reshape(-1)[::7])))
+    assert agree >= 0.98, f"{tag}: bf16 rounding agreement {agree:.4f}"
+    obv = bf16_bits_to_f64(ob)
+    assert np.all(np.abs(obv - ref) <= bf16_ulp(ref) + 2 * ma), tag
+    return ma, rl
+
+
+def run_layer_step(x_bits, tensors, lay, k, renorm=True):
+    """Oracle first; feed its choice to the GPU if any token is a near tie."""
+    ref = oracle.moe_forward(x_bits, tensors, k, renorm=renorm)
+    x = torch_bf16_from_bits(x_bits)
+    ws = bm.moe_workspace(lay, x.shape[0])
+    T = x.shape[0]
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    out_f32 = torch.empty((T, lay.d), dtype=torch.float32, device="cuda")
+    forced = bool(np.any(ref["gap"] < NEAR_TIE))
+    if forced:
+        fi = torch.from_numpy(ref["ids"]).cuda()
+        fw = torch.from_numpy(ref["w"].astype(np.float32)).cuda()
+        out, _, _, _ = bm.moe_forward(x, lay, ws, forced_ids=fi, forced_w=fw, out_f32=out_f32, ids_out=ids, w_out=w)
+    else:
+        out, _, _, _ = bm.moe_forward(x, lay, ws, out_f32=out_f32, ids_out=ids, w_out=w)
+    torch.cuda.synchronize()
+    assert bm.bitmoe_get_device_status(ws) == 0
+    assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+    assert np.allclose(w.cpu().numpy(), ref["w"], rtol=1e-5, atol=1e-6)
+    return out, out_f32, ref, forced
+
+
+# ------------------------------------------------------------------ packing
+
+
+def test_pack_layout_matches_the_documented_order():
+    rng = np.random.default_rng(0)
+    n, rows, K = 2, 32, 256
+    q = rng.integers(0, 256, (n, rows, K // 2), dtype=np.uint8)
+    s = rng.uniform(0.005, 0.02, (n, rows, K // 32)).astype(np.float16)
+    packed = bm.bitmoe_pack_int4(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda()).cpu().numpy()
+    assert packed.size == n * rows * K * 9 // 16
+    # decode the packed bytes on the host following the layout in include/bitmoe.h / misc.cu
+    nib = np.stack([q & 0xF, q >> 4], -1).reshape(n, rows, K)
+    tile_bytes = (K // 128) * 1152
+    for m in range(n):
+        for r in range(rows):
+            tile = packed[(m * rows + r) // 16 * tile_bytes:][:tile_bytes]
+            rr = r % 16
+            for ch in range(K // 128):
+                chunk = tile[ch * 1152:(ch + 1) * 1152]
+                for c in range(4):
+                    words = chunk[(rr * 4 + c) * 16:(rr * 4 + c) * 16 + 16].view(np.uint32)
+                    for gg in range(4):
+                        wv = int(words[gg])
+                        k0 = (ch * 4 + gg) * 32 + c * 8
+                        got = [(wv >> (4 * (mm // 2) + (16 if mm % 2 else 0))) & 0xF for mm in range(8)]
+                        assert got == list(nib[m, r, k0:k0 + 8])
+                sc = chunk[1024 + rr * 8:1024 + rr * 8 + 8].view(np.float16)
+                assert np.array_equal(sc, s[m, r, ch * 4:ch * 4 + 4])
+
+
+def test_device_generator_matches_numpy():
+    key = synth.stream_key(3, synth.TAG["down_q"], 5)
+    n = 1 << 20
+    buf = torch.empty(n, dtype=torch.uint8, device="cuda")
+    synth.device_fill_int4(buf.data_ptr(), n, key, start=12345)
+    torch.cuda.synchronize()
+    assert np.array_equal(buf.cpu().numpy(), synth.int4_bytes(key, 12345, n))
+    ks = synth.stream_key(3, synth.TAG["down_s"], 5)
+    sb = torch.empty(n, dtype=torch.float16, device="cuda")
+    synth.device_fill_scales(sb.data_ptr(), n, ks, start=777)
+    torch.cuda.synchronize()
+    assert np.array_equal(sb.cpu().numpy().view(np.uint16), synth.f16_scales(ks, 777, n))
+
+
+# ------------------------------------------------------------------ routing
+
+
+@pytest.mark.parametrize("T,bias", [(1, "normal"), (8, "zipf"), (64, "zipf"), (300, "normal"), (4096, "zipf")])
+def test_route_parity(T, bias):
+    tensors, lay = flint_layer(bias)
+    x_bits = synth.activations(100 + T, T, FLINT["d"])
+    ids_ref, w_ref, l_ref, gap = oracle.route(x_bits, tensors["w_router"], tensors["b_router"], FLINT["k"])
+    ws = bm.moe_workspace(lay, T)
+    ids, w, logits = bm.moe_route(torch_bf16_from_bits(x_bits), lay, ws, want_logits=True)
+    torch.cuda.synchronize()
+    l = logits.cpu().numpy().astype(np.float64)
+    assert max_abs(l, l_ref) < 2e-5
+    ok = gap >= NEAR_TIE
+    assert np.array_equal(ids.cpu().numpy()[ok], ids_ref[ok])
+    assert np.allclose(w.cpu().numpy()[ok], w_ref[ok], rtol=2e-5, atol=1e-6)
+
+
+def test_route_tiny_unrenormalised_gates():
+    tensors, lay = tiny_layer(renorm=False)
+    x_bits = synth.activations(1, 4, TINY["d"])
+    ids_ref, w_ref, _, gap = oracle.route(x_bits, tensors["w_router"], tensors["b_router"], TINY["k"], renorm=False)
+    ids, w = bm.moe_route(torch_bf16_from_bits(x_bits), lay, bm.moe_workspace(lay, 4))
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+    assert np.allclose(w.cpu().numpy(), w_ref, rtol=1e-5, atol=1e-7)
+
+
+# ------------------------------------------------------------------ permutation
+
+
+@pytest.mark.parametrize("R_tokens,E,k,dist", [(1, 256, 8, "u"), (4, 16, 2, "u"), (64, 256, 8, "z"),
+                                                (512, 256, 8, "u"), (513, 64, 8, "z"), (4096, 256, 8, "z"),
+                                                (16384, 256, 8, "u"), (3, 1024, 32, "u")])
+def test_permute_parity(R_tokens, E, k, dist):
+    rng = np.random.default_rng(R_tokens + E)
+    T = R_tokens
+    if dist == "u":
+        ids = np.array([rng.permutation(E)[:k] for _ in range(T)], np.int32)
+    else:
+        p = np.arange(1, E + 1, dtype=np.float64) ** -1.1
+        p /= p.sum()
+        ids = np.array([rng.choice(E, k, replace=False, p=p) for _ in range(T)], np.int32)
+    off_ref, rows_ref, inv_ref = oracle.permute(ids, E)
+    lay = bm.MoeLayer(d=256, E=E, k=k, I=128, gate=None, up=None, down=None, w_router=None, b_router=None)
+    ws = torch.zeros(bm.moe_workspace_size(lay, T), dtype=torch.uint8, device="cuda")
+    off, rows, inv = bm.moe_permute(torch.from_numpy(ids).cuda(), lay, ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(off.cpu().numpy(), off_ref)
+    assert np.array_equal(rows.cpu().numpy(), rows_ref)
+    assert np.array_equal(inv.cpu().numpy(), inv_ref)
+    assert bm.bitmoe_get_device_status(ws) == 0
+
+
+def test_permute_flags_out_of_range_ids():
+    E, k = 16, 2
+    ids = np.array([[3, 5], [16, 2], [7, -1]], np.int32)
+    lay = bm.MoeLayer(d=256, E=E, k=k, I=128, gate=None, up=None, down=None, w_router=None, b_router=None)
+    ws = torch.zeros(bm.moe_workspace_size(lay, 3), dtype=torch.uint8, device="cuda")
+    off, rows, inv = bm.moe_permute(torch.from_numpy(ids).cuda(), lay, ws)
+    inv = inv.cpu().numpy()
+    assert inv[2] == -1 and inv[5] == -1
+    assert off.cpu().numpy()[-1] == 4
+    assert bm.bitmoe_get_device_status(ws, clear=True) == bm.ERR_DEVICE_CHECK
+    assert bm.bitmoe_get_device_status(ws) == 0
+
+
+# ------------------------------------------------------------------ experts and combine
+
+
+@pytest.mark.parametrize("which,T", [("tiny", 4), ("flint", 1), ("flint", 37)])
+def test_expert_ffn_and_combine_parity(which, T):
+    if which == "tiny":
+        tensors, lay = tiny_layer()
+    else:
+        tensors, lay = flint_layer("zipf")
+    k = lay.k
+    x_bits = synth.activations(7 + T, T, lay.d)
+    ids_ref, w_ref, _, _ = oracle.route(x_bits, tensors["w_router"], tensors["b_router"], k)
+    y_ref, h_ref = oracle.expert_ffn(x_bits, tensors, ids_ref, want_h=True)
+    off_ref, rows_ref, inv_ref = oracle.permute(ids_ref, lay.E)
+    ws = bm.moe_workspace(lay, T)
+    x = torch_bf16_from_bits(x_bits)
+    y = bm.moe_expert_ffn_int4(x, lay, torch.from_numpy(off_ref).cuda(), torch.from_numpy(rows_ref).cuda(), ws)
+    torch.cuda.synchronize()
+    y_sorted_ref = y_ref[rows_ref]
+    yg = y.cpu().numpy().astype(np.float64)
+    assert rel_l2(yg, y_sorted_ref) < 1e-5 and max_abs(yg, y_sorted_ref) < 1e-3
+    out, out_f32 = bm.moe_combine(y, torch.from_numpy(inv_ref).cuda(), torch.from_numpy(w_ref.astype(np.float32)).cuda(),
+                                  x, lay)
+    ref = oracle.combine(y_ref, w_ref, x_bits)
+    check_layer_output(out, out_f32, ref, f"{which} T={T}")
+
+
+# ------------------------------------------------------------------ whole layer
+
+
+def test_layer_tiny_smoke_workload():
+    tensors, lay = tiny_layer()
+    x_bits = synth.activations(0, 4, TINY["d"])
+    out, out_f32, ref, _ = run_layer_step(x_bits, tensors, lay, TINY["k"])
+    check_layer_output(out, out_f32, ref["out"], "tiny")
+
+
+@pytest.mark.parametrize("step", range(6))
+def test_layer_decode_batch1(step):
+    tensors, lay = flint_layer("normal")
+    x_bits = synth.activations(0, 1, FLINT["d"], step=step)
+    out, out_f32, ref, _ = run_layer_step(x_bits, tensors, lay, FLINT["k"])
+    check_layer_output(out, out_f32, ref["out"], f"decode step {step}")
+
+
+@pytest.mark.parametrize("T", [8, 32, 64])
+def test_layer_decode_small_batch_zipf(T):
+    tensors, lay = flint_layer("zipf")
+    x_bits = synth.activations(1, T, FLINT["d"], step=T)
+    out, out_f32, ref, _ = run_layer_step(x_bits, tensors, lay, FLINT["k"])
+    check_layer_output(out, out_f32, ref["out"], f"zipf T={T}")
+
+
+@pytest.mark.parametrize("T", [200, 4096])
+def test_layer_prefill_zipf(T):
+    tensors, lay = flint_layer("zipf")
+    x_bits = synth.activations(2, T, FLINT["d"], step=T)
+    out, out_f32, ref, _ = run_layer_step(x_bits, tensors, lay, FLINT["k"])
+    check_layer_output(out, out_f32, ref["out"], f"prefill T={T}")
+
+
+def test_layer_forced_invalid_ids_flag_and_skip():
+    tensors, lay = tiny_layer()
+    x = torch_bf16_from_bits(synth.activations(3, 2, TINY["d"]))
+    ws = bm.moe_workspace(lay, 2)
+    fi = torch.tensor([[0, 99], [1, 1]], dtype=torch.int32, device="cuda")
+    fw = torch.full((2, 2), 0.5, dtype=torch.float32, device="cuda")
+    bm.moe_forward(x, lay, ws, forced_ids=fi, forced_w=fw)
+    assert bm.bitmoe_get_device_status(ws, clear=True) == bm.ERR_DEVICE_CHECK
+
+
+def test_zero_tokens_is_a_no_op():
+    _, lay = tiny_layer()
+    ws = bm.moe_workspace(lay, 1)
+    x = torch.empty((0, lay.d), dtype=torch.bfloat16, device="cuda")
+    out, _, _, _ = bm.moe_forward(x, lay, ws)
+    assert out.shape == (0, lay.d)
+
+
+def test_undersized_workspace_is_rejected():
+    _, lay = tiny_layer()
+    ws = bm.moe_workspace(lay, 1)
+    x = torch_bf16_from_bits(synth.activations(0, 4, TINY["d"]))
+    with pytest.raises(bm.BitmoeError) as e:
+        bm.moe_forward(x, lay, ws)
+    assert e.value.code == 3
+
+
+# ------------------------------------------------------------------ LM head and norm
+
+
+@pytest.mark.parametrize("T,V,d", [(1, 131072, 2048), (16, 131072, 2048), (3, 48, 256), (17, 4096, 256),
+                                   (64, 1024, 2048)])
+def test_lmhead_parity(T, V, d):
+    q, s = synth.lm_head(5, V, d)
+    h_bits = synth.activations(6, T, d)
+    logits_ref, am_ref, gap = oracle.lmhead(h_bits, q, s)
+    wp = bm.bitmoe_pack_int4(torch.from_numpy(q).cuda(), torch.from_numpy(s.view(np.float16)).cuda())
+    ws = bm.lmhead_workspace(T, d, V)
+    logits, am = bm.lmhead_int4_gemv(torch_bf16_from_bits(h_bits), wp, V, ws)
+    torch.cuda.synchronize()
+    lg = logits.cpu().numpy().astype(np.float64)
+    assert max_abs(lg, logits_ref) < 1e-3 and rel_l2(lg, logits_ref) < 1e-6
+    ok = gap >= NEAR_TIE
+    assert np.array_equal(am.cpu().numpy()[ok], am_ref[ok])
+
+
+def test_lmhead_argmax_ties_lowest_row():
+    d, V = 256, 64
+    q = np.zeros((V, d // 2), np.uint8)
+    q[10] = 0x11  # every weight +1
+    q[40] = 0x11
+    s = np.full((V, d // 32), 1.0, np.float16)
+    h_bits = synth.f64_to_bf16_bits(np.full((2, d), 0.25))
+    wp = bm.bitmoe_pack_int4(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda())
+    _, am = bm.lmhead_int4_gemv(torch_bf16_from_bits(h_bits), wp, V, bm.lmhead_workspace(2, d, V),
+                                want_logits=False)
+    assert am.cpu().tolist() == [10, 10]
+
+
+@pytest.mark.parametrize("T,d", [(1, 2048), (16, 2048), (5, 256)])
+def test_rmsnorm_parity(T, d):
+    x_bits = synth.activations(9, T, d)
+    ref = oracle.rmsnorm(x_bits)
+    y = bm.bitmoe_rmsnorm(torch_bf16_from_bits(x_bits))
+    yb = bf16_bits_to_f64(bits_from_torch_bf16(y))
+    assert np.all(np.abs(yb - ref) <= bf16_ulp(ref) * 0.5 + 1e-7)
