@@ -247,7 +247,8 @@ def bench_decode(args, world, rank):
     with torch.cuda.graph(graph):
         run_chunk()
     torch.cuda.synchronize()
-    launches_per_step = count_graph_kernels(graph) // G if hasattr(graph, "raw_cuda_graph") else 6
+    n_kernels = count_graph_kernels(graph)
+    launches_per_step = n_kernels / G if n_kernels else (1 if T <= 4 else 6)
 
     n_chunks_w = max(1, math.ceil(args.warmup / G))
     n_chunks = max(1, math.ceil(args.steps / G))
@@ -300,7 +301,7 @@ def bench_decode(args, world, rank):
                      "frac": round(achieved / hbm, 4), "traffic": None,
                      "kernel": "whole layer step", "bytes_per_step": int(step_bytes),
                      "unique_experts_per_step": uniq, "peak_source": which},
-        "gpu_launches": launches_per_step * steps,
+        "gpu_launches": int(round(launches_per_step * steps)),
         "e2e": e2e,
         "clocks": clk.summary(),
     }
@@ -308,13 +309,14 @@ def bench_decode(args, world, rank):
 
 
 def count_graph_kernels(graph):
+    """Kernel nodes in a captured torch CUDA graph (0 if it cannot be read)."""
     try:
         from cuda.bindings import runtime as cudart
-        g = graph.raw_cuda_graph()
-        err, nodes, n = cudart.cudaGraphGetNodes(g, 0)
+        g = cudart.cudaGraph_t(init_value=int(graph.raw_cuda_graph()))
+        err, _, n = cudart.cudaGraphGetNodes(g, 0)
         err, nodes, n = cudart.cudaGraphGetNodes(g, n)
         cnt = 0
-        for nd in nodes:
+        for nd in nodes[:n]:
             err, t = cudart.cudaGraphNodeGetType(nd)
             if t == cudart.cudaGraphNodeType.cudaGraphNodeTypeKernel:
                 cnt += 1

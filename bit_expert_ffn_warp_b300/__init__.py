@@ -58,6 +58,7 @@ _SIGS = {
     "bitmoe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "bitmoe_last_cuda_error": (ctypes.c_int, []),
     "bitmoe_version": (ctypes.c_char_p, []),
+    "bitmoe_set_trace_buffer": (ctypes.c_int, [_P, _SZ]),
     "bitmoe_packed_int4_bytes": (_SZ, [_I64, _I64, _I64, _I64]),
     "bitmoe_pack_int4": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I64, _P, _P]),
     "bitmoe_get_device_status": (ctypes.c_int, [_P, ctypes.c_int, ctypes.POINTER(ctypes.c_int32), _P]),
@@ -110,6 +111,14 @@ def _need(t, dtype, shape, name):
 
 def version() -> str:
     return _lib.bitmoe_version().decode()
+
+
+def bitmoe_set_trace_buffer(buf) -> None:
+    """Turn the fused-decode phase trace on (a uint64 CUDA tensor) or off (None)."""
+    if buf is None:
+        _check("bitmoe_set_trace_buffer", _lib.bitmoe_set_trace_buffer(None, 0))
+    else:
+        _check("bitmoe_set_trace_buffer", _lib.bitmoe_set_trace_buffer(_ptr(buf), buf.numel() * buf.element_size()))
 
 
 # ---------------------------------------------------------------- weights

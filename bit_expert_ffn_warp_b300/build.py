@@ -4,7 +4,8 @@
 * synth/libsynth.so                     -- the device twin of the input generator
 
 Objects go to ``_build/``; a library is rebuilt when any of its sources or
-headers is newer than it.  ``python -m bit_expert_ffn_warp_b300.build [-v]``.
+headers is newer than it.  ``python bit_expert_ffn_warp_b300/build.py [-f] [-v] [--ptxas]``
+(run it by path: importing the package itself needs the built library).
 """
 from __future__ import annotations
 

@@ -132,6 +132,14 @@ const char* bitmoe_status_string(bitmoe_status_t status) {
 
 int bitmoe_last_cuda_error(void) { return g_last_cuda_error; }
 
+bitmoe_status_t bitmoe_set_trace_buffer(void* device_buf, size_t bytes) {
+  if ((device_buf == nullptr) != (bytes == 0)) return BITMOE_ERR_INVALID_ARG;
+  if (device_buf && (reinterpret_cast<uintptr_t>(device_buf) & 7u)) return BITMOE_ERR_INVALID_ARG;
+  g_trace_buf = device_buf;
+  g_trace_bytes = bytes;
+  return BITMOE_OK;
+}
+
 const char* bitmoe_version(void) { return "bitmoe 0.1 (sm_103a)"; }
 
 size_t bitmoe_packed_int4_bytes(int64_t n_mats, int64_t rows, int64_t K, int64_t group) {
@@ -155,7 +163,7 @@ bitmoe_status_t bitmoe_get_device_status(void* workspace, int clear, int32_t* st
   cudaError_t e = cudaMemcpyAsync(&hs, workspace, sizeof(hs), cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e == cudaSuccess && clear) {
-    e = cudaMemsetAsync(workspace, 0, sizeof(DevStatus), s);
+    e = cudaMemsetAsync(workspace, 0, 256, s);  // status word and grid-barrier words
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   }
   if (e != cudaSuccess) return cuda_status(e);
@@ -248,6 +256,37 @@ bitmoe_status_t moe_forward(const uint16_t* x, const uint16_t* residual, int64_t
   cudaStream_t s = (cudaStream_t)stream;
   const int Ti = (int)T, d = (int)shape->d, E = (int)shape->E, k = (int)shape->k;
   cudaError_t e;
+  if (decode_fused_eligible(Ti, d, E, k, (int)shape->I)) {
+    DecodeLaunch L;
+    L.x = x;
+    L.resid = residual;
+    L.T = Ti;
+    L.d = d;
+    L.E = E;
+    L.k = k;
+    L.I = (int)shape->I;
+    L.renorm = shape->renormalize;
+    L.gate = weights->gate;
+    L.up = weights->up;
+    L.down = weights->down;
+    L.w_router = weights->w_router;
+    L.b_router = weights->b_router;
+    L.forced_ids = forced_ids;
+    L.forced_w = forced_w;
+    L.out = out;
+    L.out_f32 = out_f32;
+    L.ids_out = topk_ids_out;
+    L.w_out = topk_w_out;
+    L.logits = w.logits;
+    L.h_hi = w.h_hi;
+    L.h_lo = w.h_lo;
+    L.gbar = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(w.st) + 64);
+    L.st = w.st;
+    L.pdl = 1;
+    e = launch_decode_fused(L, s);
+    if (e != cudaErrorNotSupported) return cuda_status(e);
+    (void)cudaGetLastError();
+  }
   if (forced_ids) {
     e = launch_forced_select(forced_ids, forced_w, Ti, E, k, w.ids, w.w, w.st, s);
   } else {

@@ -185,6 +185,21 @@ __device__ __forceinline__ uint32_t float_order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Sets a kernel's dynamic shared-memory limit once per device (the call is
+// host-side state only, so later launches -- including ones being captured
+// into a CUDA graph -- issue nothing but the launch itself).
+template <typename F>
+inline cudaError_t ensure_smem_attr(F* kernel, size_t bytes, int* max_set) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (max_set[dev] >= (int)bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) max_set[dev] = (int)bytes;
+  return e;
+}
+
 template <typename T>
 __host__ __device__ constexpr T ceil_div(T a, T b) {
   return (a + b - 1) / b;

@@ -1,0 +1,771 @@
+// Fused decode step of the int4 MoE layer: one persistent launch per token
+// batch (T <= 4) runs router -> top-k -> grouping -> gate/up + SwiGLU ->
+// down + combine.
+//
+// The pages' decode speed comes from a kernel that does the whole decode pass
+// in one launch ("Flint 40B : Best Mid Sized LLM", transcript 06:43; "Recursive
+// abre o Flint ...", section "O papel da quantizacao e dos kernels no
+// lancamento").  That kernel was written for Apple GPUs; this one is built for
+// B300.  One CTA per SM: a producer warp streams the CTA's share of the chosen
+// experts' weights through a ring of TMA bulk copies (the ring holds a CTA's
+// whole share at batch 1, so every byte of the step is requested at once), 16
+// consumer warps run mma.sync, and two grid-wide barriers (bounded spins on a
+// monotonic counter) separate the phases.  Programmatic dependent launch lets
+// the next step's router rows be fetched before this step has drained.
+//
+// Single-warp serial code is slow on this part (a few cycles per dependent
+// instruction), so every phase spreads over the 16 warps:
+//   P0  router logits of this CTA's experts, K split over warps (W_r rows are
+//       fetched before the grid-dependency wait).            -- grid barrier A
+//   P1  every CTA reads all logits and selects top-k per token in parallel:
+//       the k-th largest of the 16 warp maxima bounds the k-th logit from
+//       below, so only the few logits above it are ranked.  Gates, the stable
+//       grouping and the work split follow (identical in every CTA).
+//   P2  gate/up units (expert, 16-row tile), one 128-column chunk per warp;
+//       h = silu(a) * u stored as an fp16 hi + lo pair.      -- grid barrier B
+//       (the producer streams the CTA's W_down tiles meanwhile)
+//   P3  16 output columns per CTA: four warps per expert tile (a K quarter
+//       each), then out = resid + sum_j w_j y_j in ascending j.
+#include "kernels.h"
+
+namespace bitmoe {
+namespace {
+
+constexpr int kDecWarps = 16;
+constexpr int kConsumers = kDecWarps * 32;
+constexpr int kDecThreads = kConsumers + 32;
+constexpr int kMaxStages = 16;
+constexpr int kDecMaxE = kConsumers;  // one logit per consumer thread
+constexpr int kDecMaxK = kDecWarps;   // the warp-maxima bound needs k <= number of warps
+constexpr int kDecMaxT = 4;
+constexpr int kTracePoints = 16;
+
+struct DecodeArgs {
+  const uint16_t* x;
+  const uint16_t* resid;
+  int T, d, E, k, I, renorm;
+  const uint8_t* gate;
+  const uint8_t* up;
+  const uint8_t* down;
+  const float* w_router;
+  const float* b_router;
+  const int32_t* forced_ids;
+  const float* forced_w;
+  uint16_t* out;
+  float* out_f32;
+  int32_t* ids_out;
+  float* w_out;
+  float* logits;  // [T, E] (global scratch)
+  __half* h_hi;   // [R, I]
+  __half* h_lo;
+  unsigned* gbar;
+  DevStatus* st;
+  int nstages;
+  int offA, offB, offR, offRing;  // shared-memory carve-up (bytes)
+  unsigned long long* trace;       // optional [grid][kTracePoints] globaltimer stamps
+};
+
+// Phase timestamps for the optional trace buffer (thread 0 of each CTA).
+__device__ __forceinline__ void stamp(const DecodeArgs& p, int point) {
+  if (p.trace != nullptr && threadIdx.x == 0) p.trace[blockIdx.x * kTracePoints + point] = globaltimer_ns();
+}
+
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers)); }
+
+__device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Grid-wide barrier over the consumer warps of every CTA (called by all
+// consumer threads).  gb[0] is a monotonic arrival counter: every launch calls
+// each barrier once from every CTA, so a launch starts with gb[0] a multiple
+// of gridDim.x and an arrival that returns `old` waits for the next multiple.
+// (A launch that timed out can leave it misaligned; clearing the device
+// status word resets it.)  The release-add publishes the CTA's writes (made
+// CTA-visible by the preceding bar.sync); the acquire fence after the poll
+// makes the other CTAs' writes visible.  Returns false on timeout.
+__device__ bool grid_barrier(unsigned* gb, int* fail, DevStatus* st, int where) {
+  consumer_sync();
+  if (threadIdx.x == 0) {
+    unsigned old;
+    asm volatile("atom.add.release.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(gb) : "memory");
+    const unsigned target = (old / gridDim.x + 1u) * gridDim.x;
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(gb) : "memory");
+    if ((int)(v - target) < 0) {
+      const uint64_t t0 = globaltimer_ns();
+      do {
+        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(gb) : "memory");
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          record_status(st, kStatusTimeout, where, blockIdx.x);
+          *(volatile int*)fail = 1;
+          break;
+        }
+      } while ((int)(v - target) < 0);
+    }
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+  }
+  consumer_sync();
+  return *(volatile int*)fail == 0;
+}
+
+// Float value of an order-preserving arg-max key (inverse of float_order_key).
+__device__ __forceinline__ float key_value(unsigned long long key) {
+  const uint32_t u = (uint32_t)(key >> 32);
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
+}
+
+__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) { return a > b ? a : b; }
+
+__device__ __forceinline__ float scale_at(uint2 s, int gg) {
+  const uint32_t w = (gg < 2) ? s.x : s.y;
+  const uint16_t b = (gg & 1) ? (uint16_t)(w >> 16) : (uint16_t)(w & 0xffffu);
+  return __half2float(__ushort_as_half(b));
+}
+
+__device__ __forceinline__ uint32_t word_at(const uint4& q, int gg) {
+  return gg == 0 ? q.x : gg == 1 ? q.y : gg == 2 ? q.z : q.w;
+}
+
+struct Routing {  // shared-memory routing tables (identical in every CTA)
+  int* ids;      // [R]   expert of row r (-1 = dropped)
+  float* w;      // [R]
+  int* pos;      // [R]   sorted position of row r (-1 = dropped)
+  int* sorted;   // [R]   row at sorted position p
+  int* first;    // [R]   1 + first position of the row's expert if r is its first row, else 0
+  int* act_e;    // [R]   active experts, ascending
+  int* act_off;  // [R+1] first sorted position of active expert a
+  unsigned long long* wmax;  // [kDecWarps]
+  unsigned long long* cand;  // [kConsumers]
+  unsigned long long* sel;   // [kDecMaxT][kDecMaxK]
+  float* zall;   // [kDecMaxT]
+  float* part;   // [kDecWarps] partial sums
+  int* misc;     // [0] U, [1] fail flag, [2] candidate count, [3] tau slot
+};
+
+__global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* xbar = empty + kMaxStages;
+  uint64_t* wrbar = xbar + 1;
+  uint64_t* hbar = wrbar + 1;
+  unsigned char* regA = smem + p.offA;
+  unsigned char* regB = smem + p.offB;
+  unsigned char* ring = smem + p.offRing;
+  const int T = p.T, d = p.d, E = p.E, k = p.k, I = p.I, R = T * k;
+  const int G = gridDim.x, cta = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tbd = (int)tile_bytes(d), tbi = (int)tile_bytes(I);
+  const int dps = tbd / tbi;  // down tiles per ring stage
+  const int RT = I / kTileRows, CT = d / kTileRows;
+  const int xstride = 2 * d + kSmemRowPad;
+  const int NS = p.nstages;
+
+  Routing rt;
+  {
+    unsigned long long* q8 = reinterpret_cast<unsigned long long*>(smem + p.offR);
+    rt.wmax = q8; q8 += kDecWarps;
+    rt.cand = q8; q8 += kConsumers;
+    rt.sel = q8; q8 += kDecMaxT * kDecMaxK;
+    int* q = reinterpret_cast<int*>(q8);
+    rt.zall = reinterpret_cast<float*>(q); q += kDecMaxT;
+    rt.part = reinterpret_cast<float*>(q); q += kDecWarps;
+    rt.ids = q; q += R;
+    rt.w = reinterpret_cast<float*>(q); q += R;
+    rt.pos = q; q += R;
+    rt.sorted = q; q += R;
+    rt.first = q; q += R;
+    rt.act_e = q; q += R;
+    rt.act_off = q; q += R + 1;
+    rt.misc = q;
+  }
+  int* fail = rt.misc + 1;
+
+  // experts whose router rows this CTA computes
+  const int e_lo = (int)((long)cta * E / G), e_hi = (int)((long)(cta + 1) * E / G);
+  const int nexp = e_hi - e_lo;
+  float* wr_s = reinterpret_cast<float*>(regB);
+  const bool routed = (p.forced_ids == nullptr);
+
+  if (tid == 0) {
+    for (int s = 0; s < kMaxStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kDecWarps);
+    }
+    mbar_init(xbar, 1);
+    mbar_init(wrbar, 1);
+    mbar_init(hbar, 1);
+    rt.misc[0] = 0;
+    rt.misc[1] = 0;
+    rt.misc[2] = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  stamp(p, 0);
+  if (tid == 0) grid_dep_launch();  // the next launch may be scheduled as SMs free up
+
+  // ---------------- P0: router rows (independent of the previous step) then x
+  if (warp == kDecWarps && lane == 0) {
+    if (routed && nexp > 0) {
+      mbar_arrive_expect_tx(wrbar, (uint32_t)nexp * d * 4u);
+      bulk_g2s(wr_s, p.w_router + (size_t)e_lo * d, (uint32_t)nexp * d * 4u, wrbar);
+    }
+  }
+  grid_dep_wait();  // the previous launch on this stream is complete and visible
+  stamp(p, 1);
+  if (warp == kDecWarps && lane == 0) {
+    mbar_arrive_expect_tx(xbar, (uint32_t)T * 2u * d);
+    for (int t = 0; t < T; ++t) bulk_g2s(regA + t * xstride, p.x + (size_t)t * d, 2u * d, xbar);
+  }
+
+  if (warp < kDecWarps) {
+    bool ok = mbar_wait(xbar, 0, p.st, 30);
+    if (routed) {
+      if (nexp > 0) ok = mbar_wait(wrbar, 0, p.st, 31) && ok;
+      if (!ok) *(volatile int*)fail = 1;
+      // (token, expert, K part) items; parts sized so that the warps are busy
+      const int pairs = T * nexp;
+      int parts = pairs > 0 ? kDecWarps / pairs : 1;
+      if (parts < 1) parts = 1;
+      while (parts > 1 && (d / parts) % 256) --parts;
+      const int span = d / parts;
+      float* psum = reinterpret_cast<float*>(regB + (size_t)nexp * d * 4);  // [pairs][parts]
+      for (int it = warp; it < pairs * parts; it += kDecWarps) {
+        const int pr = it / parts, part = it % parts;
+        const int t = pr / nexp, el = pr % nexp;
+        const uint16_t* xr = reinterpret_cast<const uint16_t*>(regA + t * xstride);
+        const float* wrow = wr_s + (size_t)el * d;
+        float acc = 0.f;
+        for (int i = part * span + lane * 8; i < (part + 1) * span; i += 256) {
+          const uint4 xv = *reinterpret_cast<const uint4*>(xr + i);
+          const float4 w0 = *reinterpret_cast<const float4*>(wrow + i);
+          const float4 w1 = *reinterpret_cast<const float4*>(wrow + i + 4);
+          acc = fmaf(__uint_as_float(xv.x << 16), w0.x, acc);
+          acc = fmaf(__uint_as_float(xv.x & 0xffff0000u), w0.y, acc);
+          acc = fmaf(__uint_as_float(xv.y << 16), w0.z, acc);
+          acc = fmaf(__uint_as_float(xv.y & 0xffff0000u), w0.w, acc);
+          acc = fmaf(__uint_as_float(xv.z << 16), w1.x, acc);
+          acc = fmaf(__uint_as_float(xv.z & 0xffff0000u), w1.y, acc);
+          acc = fmaf(__uint_as_float(xv.w << 16), w1.z, acc);
+          acc = fmaf(__uint_as_float(xv.w & 0xffff0000u), w1.w, acc);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) psum[it] = acc;
+      }
+      consumer_sync();
+      for (int pr = tid; pr < pairs; pr += kConsumers) {
+        float acc = 0.f;
+        for (int part = 0; part < parts; ++part) acc += psum[pr * parts + part];
+        const int t = pr / nexp, el = pr % nexp;
+        p.logits[(size_t)t * E + e_lo + el] = acc + (p.b_router ? p.b_router[e_lo + el] : 0.f);
+      }
+      stamp(p, 2);
+      grid_barrier(p.gbar, fail, p.st, 32);  // A: every logit written
+      stamp(p, 3);
+    } else if (!ok) {
+      *(volatile int*)fail = 1;
+    }
+
+    // ---------------- P1: routing tables, replicated in every CTA
+    if (*(volatile int*)fail == 0) {
+      if (routed) {
+        // Per token: keys = order-preserving logit bits, then the inverted
+        // expert index (equal logits put the lower expert first).  The k-th
+        // largest of the 16 warp maxima is a lower bound tau for the k-th key
+        // (k distinct elements reach it), so only keys >= tau can be chosen and
+        // ranking those few candidates against each other gives the top-k.
+        for (int t = 0; t < T; ++t) {
+          const unsigned long long key =
+              (tid < E) ? (((unsigned long long)float_order_key(__ldcg(p.logits + (size_t)t * E + tid)) << 32) |
+                           (0xffffffffu - (uint32_t)tid))
+                        : 0ull;
+          unsigned long long m = key;
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) m = umax64(m, __shfl_xor_sync(0xffffffffu, m, off));
+          if (lane == 0) rt.wmax[warp] = m;
+          consumer_sync();
+          if (tid < kDecWarps) {
+            const unsigned long long mw = rt.wmax[tid];
+            int rank = 0;
+#pragma unroll
+            for (int w = 0; w < kDecWarps; ++w) {
+              const unsigned long long o = rt.wmax[w];
+              rank += (o > mw) || (o == mw && w < tid);
+            }
+            if (rank == k - 1) rt.misc[3] = tid;
+          }
+          consumer_sync();
+          const unsigned long long tau = rt.wmax[rt.misc[3]];
+          const bool is_cand = key != 0ull && key >= tau;
+          if (is_cand) rt.cand[atomicAdd(&rt.misc[2], 1)] = key;
+          if (!p.renorm) {
+            unsigned long long top = 0ull;
+#pragma unroll
+            for (int w = 0; w < kDecWarps; ++w) top = umax64(top, rt.wmax[w]);
+            float ez = (key != 0ull) ? expf(key_value(key) - key_value(top)) : 0.f;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ez += __shfl_xor_sync(0xffffffffu, ez, off);
+            if (lane == 0) rt.part[warp] = ez;
+          }
+          consumer_sync();
+          if (is_cand) {
+            const int nc = rt.misc[2];
+            int rank = 0;
+            for (int j = 0; j < nc; ++j) rank += rt.cand[j] > key;
+            if (rank < k) rt.sel[t * kDecMaxK + rank] = key;
+          }
+          if (tid == 0 && !p.renorm) {
+            float z = 0.f;
+            for (int w = 0; w < kDecWarps; ++w) z += rt.part[w];
+            rt.zall[t] = z;
+          }
+          consumer_sync();
+          if (tid == 0) rt.misc[2] = 0;
+        }
+        // gates: exp(l_j - l_max) over the chosen k (renormalised) or over all E
+        if (tid < R) {
+          const int t = tid / k, j = tid % k;
+          const unsigned long long* sk = rt.sel + t * kDecMaxK;
+          const float vmax = key_value(sk[0]);
+          float z = 0.f;
+          if (p.renorm) {
+            for (int jj = 0; jj < k; ++jj) z += expf(key_value(sk[jj]) - vmax);
+          } else {
+            z = rt.zall[t];
+          }
+          const int e = (int)(0xffffffffu - (uint32_t)(sk[j] & 0xffffffffull));
+          rt.ids[tid] = (sk[j] != 0ull && e < E) ? e : -1;
+          rt.w[tid] = expf(key_value(sk[j]) - vmax) / z;
+        }
+      } else {
+        for (int r = tid; r < R; r += kConsumers) {
+          int e = p.forced_ids[r];
+          if (e < 0 || e >= E) {
+            if (cta == 0) record_status(p.st, kStatusCheck, 33, r);
+            e = -1;
+          } else if (cta == 0) {
+            const int t = r / k;
+            for (int jj = t * k; jj < r; ++jj)
+              if (p.forced_ids[jj] == e) record_status(p.st, kStatusCheck, 34, r);
+          }
+          rt.ids[r] = e;
+          rt.w[r] = p.forced_w[r];
+        }
+      }
+      consumer_sync();
+      // stable grouping by ranks: row r goes to (rows of smaller experts) +
+      // (earlier rows of its own expert); the first row of each expert also
+      // places the expert in the ascending list of active experts
+      for (int r = tid; r < R; r += kConsumers) {
+        const int e = rt.ids[r];
+        int less = 0, before = 0;
+        if (e >= 0) {
+          for (int rr = 0; rr < R; ++rr) {
+            const int f = rt.ids[rr];
+            less += (f >= 0 && f < e);
+            before += (rr < r && f == e);
+          }
+          rt.pos[r] = less + before;
+          rt.sorted[less + before] = r;
+        } else {
+          rt.pos[r] = -1;
+        }
+        rt.first[r] = (e >= 0 && before == 0) ? less + 1 : 0;
+      }
+      consumer_sync();
+      stamp(p, 10);
+      for (int r = tid; r < R; r += kConsumers) {
+        if (rt.first[r] > 0) {
+          const int e = rt.ids[r];
+          int a = 0;
+          for (int rr = 0; rr < R; ++rr) a += (rt.first[rr] > 0 && rt.ids[rr] < e);
+          rt.act_e[a] = e;
+          rt.act_off[a] = rt.first[r] - 1;
+        }
+      }
+      if (tid == 0) {
+        int U = 0, Rv = 0;
+        for (int r = 0; r < R; ++r) {
+          U += rt.first[r] > 0;
+          Rv += rt.ids[r] >= 0;
+        }
+        rt.misc[0] = U;
+        rt.act_off[U] = Rv;
+      }
+      consumer_sync();
+      stamp(p, 11);
+      if (cta == 0) {
+        for (int r = tid; r < R; r += kConsumers) {
+          if (p.ids_out) p.ids_out[r] = rt.ids[r];
+          if (p.w_out) p.w_out[r] = rt.w[r];
+        }
+      }
+    }
+  }
+  __syncthreads();  // routing tables visible to the producer warp
+  stamp(p, 4);
+  if (*(volatile int*)fail) return;
+
+  const int U = rt.misc[0];
+  const int n_up = U * RT;
+  const int u_lo = (int)((long)cta * n_up / G), u_hi = (int)((long)(cta + 1) * n_up / G);
+
+  // ---------------- producer: this CTA's tiles, in consumption order
+  if (warp == kDecWarps) {
+    if (lane == 0) {
+      int i = 0;
+      for (int u = u_lo; u < u_hi; ++u) {
+        const int a = u / RT, r16 = u - a * RT;
+        const size_t toff = ((size_t)rt.act_e[a] * RT + r16) * tbd;
+        for (int m = 0; m < 2; ++m, ++i) {
+          const int s = i % NS;
+          if (i >= NS && !mbar_wait(&empty[s], ((i / NS) - 1) & 1, p.st, 35)) return;
+          mbar_arrive_expect_tx(&full[s], (uint32_t)tbd);
+          bulk_g2s(ring + (size_t)s * tbd, (m == 0 ? p.gate : p.up) + toff, (uint32_t)tbd, &full[s]);
+        }
+      }
+      for (int ct = cta; ct < CT; ct += G) {
+        for (int a0 = 0; a0 < U; a0 += dps, ++i) {
+          const int s = i % NS;
+          if (i >= NS && !mbar_wait(&empty[s], ((i / NS) - 1) & 1, p.st, 36)) return;
+          const int n = min(dps, U - a0);
+          mbar_arrive_expect_tx(&full[s], (uint32_t)n * tbi);
+          for (int j = 0; j < n; ++j)
+            bulk_g2s(ring + (size_t)s * tbd + (size_t)j * tbi,
+                     p.down + ((size_t)rt.act_e[a0 + j] * CT + ct) * tbi, (uint32_t)tbi, &full[s]);
+        }
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumers
+  const int g = lane >> 2, c = lane & 3;
+  float* red = reinterpret_cast<float*>(regB);            // [2][16 warps][32][8]
+  float* ypart = red + 2 * kDecWarps * 32 * 8;            // [4][R][16]
+  int i = 0;
+  bool ok = true;
+
+  // P2: gate/up units, one 128-column chunk per warp
+  for (int u = u_lo; u < u_hi; ++u) {
+    const int a = u / RT, r16 = u - a * RT;
+    const int na = rt.act_off[a + 1] - rt.act_off[a];
+    const int sg = i % NS, su = (i + 1) % NS;
+    if (ok) ok = mbar_wait(&full[sg], (i / NS) & 1, p.st, 37) && mbar_wait(&full[su], ((i + 1) / NS) & 1, p.st, 38);
+    if (u == u_lo) stamp(p, 12);
+    if (u == u_lo + 1) stamp(p, 9);
+    const unsigned char* tg = ring + (size_t)sg * tbd;
+    const unsigned char* tu = ring + (size_t)su * tbd;
+    // token row of this lane's B fragment (n = g)
+    const unsigned char* xrow = nullptr;
+    if (g < na) xrow = regA + (rt.sorted[rt.act_off[a] + g] / k) * xstride;
+    float ag4[4] = {0.f, 0.f, 0.f, 0.f}, au4[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int ch = warp; ch < d / kChunkK; ch += kDecWarps) {
+      const unsigned char* cg = tg + ch * kChunkBytes;
+      const unsigned char* cu = tu + ch * kChunkBytes;
+      const uint4 qg0 = *reinterpret_cast<const uint4*>(cg + (g * 4 + c) * 16);
+      const uint4 qg1 = *reinterpret_cast<const uint4*>(cg + ((g + 8) * 4 + c) * 16);
+      const uint4 qu0 = *reinterpret_cast<const uint4*>(cu + (g * 4 + c) * 16);
+      const uint4 qu1 = *reinterpret_cast<const uint4*>(cu + ((g + 8) * 4 + c) * 16);
+      const uint2 sg0 = *reinterpret_cast<const uint2*>(cg + kChunkQBytes + g * 8);
+      const uint2 sg1 = *reinterpret_cast<const uint2*>(cg + kChunkQBytes + (g + 8) * 8);
+      const uint2 su0 = *reinterpret_cast<const uint2*>(cu + kChunkQBytes + g * 8);
+      const uint2 su1 = *reinterpret_cast<const uint2*>(cu + kChunkQBytes + (g + 8) * 8);
+#pragma unroll
+      for (int gg = 0; gg < 4; ++gg) {
+        const int col = (ch * 4 + gg) * kGroup + c * 8;
+        uint4 xb = make_uint4(0, 0, 0, 0);
+        if (xrow) xb = *reinterpret_cast<const uint4*>(xrow + col * 2);
+        uint32_t A[2][4], B[2][4];
+        const uint32_t wg0 = word_at(qg0, gg), wg1 = word_at(qg1, gg);
+        const uint32_t wu0 = word_at(qu0, gg), wu1 = word_at(qu1, gg);
+#pragma unroll
+        for (int st = 0; st < 2; ++st) {
+          A[st][0] = nib_pair_bf16(wg0, 2 * st);
+          A[st][1] = nib_pair_bf16(wg1, 2 * st);
+          A[st][2] = nib_pair_bf16(wg0, 2 * st + 1);
+          A[st][3] = nib_pair_bf16(wg1, 2 * st + 1);
+          B[st][0] = nib_pair_bf16(wu0, 2 * st);
+          B[st][1] = nib_pair_bf16(wu1, 2 * st);
+          B[st][2] = nib_pair_bf16(wu0, 2 * st + 1);
+          B[st][3] = nib_pair_bf16(wu1, 2 * st + 1);
+        }
+        const float z[4] = {0.f, 0.f, 0.f, 0.f};
+        float dg[4], du[4];
+        mma_bf16(dg, A[0], xb.x, xb.y, z);
+        mma_bf16(dg, A[1], xb.z, xb.w, dg);
+        mma_bf16(du, B[0], xb.x, xb.y, z);
+        mma_bf16(du, B[1], xb.z, xb.w, du);
+        const float s_g0 = scale_at(sg0, gg), s_g1 = scale_at(sg1, gg);
+        const float s_u0 = scale_at(su0, gg), s_u1 = scale_at(su1, gg);
+        ag4[0] = fmaf(s_g0, dg[0], ag4[0]);
+        ag4[1] = fmaf(s_g0, dg[1], ag4[1]);
+        ag4[2] = fmaf(s_g1, dg[2], ag4[2]);
+        ag4[3] = fmaf(s_g1, dg[3], ag4[3]);
+        au4[0] = fmaf(s_u0, du[0], au4[0]);
+        au4[1] = fmaf(s_u0, du[1], au4[1]);
+        au4[2] = fmaf(s_u1, du[2], au4[2]);
+        au4[3] = fmaf(s_u1, du[3], au4[3]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive1(&empty[sg]);
+      mbar_arrive1(&empty[su]);
+    }
+    i += 2;
+    float* my = red + ((size_t)(u & 1) * kDecWarps * 32 + warp * 32 + lane) * 8;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      my[j] = ag4[j];
+      my[4 + j] = au4[j];
+    }
+    if (!ok) *(volatile int*)fail = 1;
+    if (u == u_lo) stamp(p, 8);
+    consumer_sync();
+    // one thread per (row, token) output of the 16 x 8 tile
+    if (tid < kTileRows * 8) {
+      const int row = tid >> 3, tok = tid & 7;
+      if (tok < na) {
+        const int ln = (row & 7) * 4 + (tok >> 1);
+        const int ix = ((row >= 8) ? 2 : 0) + (tok & 1);
+        const float* rb = red + (size_t)(u & 1) * kDecWarps * 32 * 8;
+        float av = 0.f, uv = 0.f;
+#pragma unroll
+        for (int w = 0; w < kDecWarps; ++w) {
+          av += rb[(w * 32 + ln) * 8 + ix];
+          uv += rb[(w * 32 + ln) * 8 + 4 + ix];
+        }
+        const float h = silu_mul(av, uv);
+        const __half hi = __float2half_rn(h);
+        const __half lo = __float2half_rn(h - __half2float(hi));
+        const size_t o = (size_t)(rt.act_off[a] + tok) * I + r16 * kTileRows + row;
+        p.h_hi[o] = hi;
+        p.h_lo[o] = lo;
+      }
+    }
+    if (u == u_lo) stamp(p, 15);
+  }
+  stamp(p, 5);
+  if (!grid_barrier(p.gbar, fail, p.st, 39)) return;  // B: every h written
+  stamp(p, 6);
+
+  // P3: down projection of this CTA's 16-column tiles, then the combine
+  const int Rv = rt.act_off[U];  // rows that reached an expert
+  const int hstride = 2 * I;     // bytes per staged h row
+  unsigned char* hhi = regA;
+  unsigned char* hlo = regA + (size_t)Rv * hstride;
+  bool h_loaded = false;
+  for (int ct = cta; ct < CT; ct += G) {
+    if (!h_loaded) {
+      if (tid == 0) {
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(hbar, (uint32_t)Rv * 2u * hstride);
+        bulk_g2s(hhi, p.h_hi, (uint32_t)Rv * hstride, hbar);
+        bulk_g2s(hlo, p.h_lo, (uint32_t)Rv * hstride, hbar);
+      }
+      if (ok) ok = mbar_wait(hbar, 0, p.st, 40);
+      h_loaded = true;
+      stamp(p, 13);
+    }
+    for (int a0 = 0; a0 < U; a0 += dps) {
+      const int s = i % NS;
+      if (ok) ok = mbar_wait(&full[s], (i / NS) & 1, p.st, 41);
+      const int quarter = warp & 3;  // four warps per tile, one per quarter of the reduction
+      for (int j = warp >> 2; j < dps; j += kDecWarps / 4) {
+        const int a = a0 + j;
+        if (a >= U) break;
+        const unsigned char* tw = ring + (size_t)s * tbd + (size_t)j * tbi;
+        const int na = rt.act_off[a + 1] - rt.act_off[a];
+        const int p0 = rt.act_off[a];
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const bool has = g < na;
+        for (int ch = quarter; ch < I / kChunkK; ch += 4) {
+          const unsigned char* cw = tw + ch * kChunkBytes;
+          const uint4 q0 = *reinterpret_cast<const uint4*>(cw + (g * 4 + c) * 16);
+          const uint4 q1 = *reinterpret_cast<const uint4*>(cw + ((g + 8) * 4 + c) * 16);
+          const uint2 s0 = *reinterpret_cast<const uint2*>(cw + kChunkQBytes + g * 8);
+          const uint2 s1 = *reinterpret_cast<const uint2*>(cw + kChunkQBytes + (g + 8) * 8);
+#pragma unroll
+          for (int gg = 0; gg < 4; ++gg) {
+            const int col = (ch * 4 + gg) * kGroup + c * 8;
+            uint4 bh = make_uint4(0, 0, 0, 0), bl = make_uint4(0, 0, 0, 0);
+            if (has) {
+              bh = *reinterpret_cast<const uint4*>(hhi + (size_t)(p0 + g) * hstride + col * 2);
+              bl = *reinterpret_cast<const uint4*>(hlo + (size_t)(p0 + g) * hstride + col * 2);
+            }
+            uint32_t A[2][4];
+            const uint32_t w0 = word_at(q0, gg), w1 = word_at(q1, gg);
+#pragma unroll
+            for (int st = 0; st < 2; ++st) {
+              A[st][0] = nib_pair_f16(w0, 2 * st);
+              A[st][1] = nib_pair_f16(w1, 2 * st);
+              A[st][2] = nib_pair_f16(w0, 2 * st + 1);
+              A[st][3] = nib_pair_f16(w1, 2 * st + 1);
+            }
+            const float z[4] = {0.f, 0.f, 0.f, 0.f};
+            float dd[4];
+            mma_f16(dd, A[0], bh.x, bh.y, z);
+            mma_f16(dd, A[0], bl.x, bl.y, dd);
+            mma_f16(dd, A[1], bh.z, bh.w, dd);
+            mma_f16(dd, A[1], bl.z, bl.w, dd);
+            const float sc0 = scale_at(s0, gg), sc1 = scale_at(s1, gg);
+            acc[0] = fmaf(sc0, dd[0], acc[0]);
+            acc[1] = fmaf(sc0, dd[1], acc[1]);
+            acc[2] = fmaf(sc1, dd[2], acc[2]);
+            acc[3] = fmaf(sc1, dd[3], acc[3]);
+          }
+        }
+        // D rows g, g+8 (output columns) x tokens 2c, 2c+1 -> this quarter's partial
+        float* yp = ypart + (size_t)quarter * R * kTileRows;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int tok = 2 * c + (q & 1);
+          const int row = (q < 2) ? g : g + 8;
+          if (tok < na) yp[(size_t)(p0 + tok) * kTileRows + row] = acc[q];
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(&empty[s]);
+      ++i;
+    }
+    if (!ok) *(volatile int*)fail = 1;
+    consumer_sync();
+    stamp(p, 14);
+    // combine: out[t, ct*16 + col] = resid + sum_j w_j * y_j (ascending j)
+    if (tid < T * kTileRows) {
+      const int t = tid >> 4, col = tid & 15;
+      float acc = 0.f;
+      for (int j = 0; j < k; ++j) {
+        const int ps = rt.pos[t * k + j];
+        if (ps >= 0) {
+          float y = 0.f;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) y += ypart[((size_t)q * R + ps) * kTileRows + col];
+          acc = fmaf(rt.w[t * k + j], y, acc);
+        }
+      }
+      const size_t o = (size_t)t * d + (size_t)ct * kTileRows + col;
+      const float v = bf16_bits_to_float(p.resid[o]) + acc;
+      if (*(volatile int*)fail == 0) {
+        if (p.out_f32) p.out_f32[o] = v;
+        p.out[o] = float_to_bf16_bits(v);
+      }
+    }
+    consumer_sync();
+  }
+  stamp(p, 7);
+}
+
+struct DecodePlan {
+  int offA, offB, offR, offRing, nstages;
+  size_t smem;
+  bool ok;
+};
+
+DecodePlan plan(int T, int d, int E, int k, int I, int G) {
+  DecodePlan pl{};
+  pl.ok = false;
+  const int R = T * k;
+  if (T < 1 || T > kDecMaxT || k > kDecMaxK || E > kDecMaxE || I > d || d > 8192) return pl;
+  if (tile_bytes(d) % tile_bytes(I)) return pl;
+  const size_t xall = (size_t)T * (2 * d + kSmemRowPad);
+  const size_t hall = (size_t)R * 2 * (2 * I);
+  const size_t regA = ((xall > hall ? xall : hall) + 127) / 128 * 128;
+  const int nexp = (E + G - 1) / G;
+  const size_t p0 = (size_t)nexp * d * 4 + (size_t)T * nexp * kDecWarps * 4;
+  const size_t p2 = (size_t)2 * kDecWarps * 32 * 8 * 4 + (size_t)4 * R * kTileRows * 4;
+  const size_t regB = ((p0 > p2 ? p0 : p2) + 127) / 128 * 128;
+  const size_t regR = ((size_t)(kDecWarps + kConsumers + kDecMaxT * kDecMaxK) * 8 +
+                       (size_t)(kDecMaxT + kDecWarps + 7 * R + 1 + 4) * 4 + 127) / 128 * 128;
+  pl.offA = 1024;
+  pl.offB = pl.offA + (int)regA;
+  pl.offR = pl.offB + (int)regB;
+  pl.offRing = pl.offR + (int)regR;
+  const size_t budget = 227 * 1024;
+  if ((size_t)pl.offRing + 2 * tile_bytes(d) > budget) return pl;
+  int ns = (int)((budget - pl.offRing) / tile_bytes(d));
+  if (ns > kMaxStages) ns = kMaxStages;
+  pl.nstages = ns;
+  pl.smem = (size_t)pl.offRing + (size_t)ns * tile_bytes(d);
+  pl.ok = true;
+  return pl;
+}
+
+int sm_count() {
+  static int cnt[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 148;
+  if (cnt[dev] == 0) cudaDeviceGetAttribute(&cnt[dev], cudaDevAttrMultiProcessorCount, dev);
+  return cnt[dev] > 0 ? cnt[dev] : 148;
+}
+
+}  // namespace
+
+void* g_trace_buf = nullptr;
+size_t g_trace_bytes = 0;
+
+bool decode_fused_eligible(int T, int d, int E, int k, int I) { return plan(T, d, E, k, I, sm_count()).ok; }
+
+cudaError_t launch_decode_fused(const DecodeLaunch& L, cudaStream_t s) {
+  const int G = sm_count();
+  const DecodePlan pl = plan(L.T, L.d, L.E, L.k, L.I, G);
+  if (!pl.ok) return cudaErrorNotSupported;
+  static int attr_set[64] = {};
+  cudaError_t err = ensure_smem_attr(decode_layer_kernel, pl.smem, attr_set);
+  if (err != cudaSuccess) return err;
+
+  DecodeArgs a;
+  a.x = L.x;
+  a.resid = L.resid;
+  a.T = L.T;
+  a.d = L.d;
+  a.E = L.E;
+  a.k = L.k;
+  a.I = L.I;
+  a.renorm = L.renorm;
+  a.gate = L.gate;
+  a.up = L.up;
+  a.down = L.down;
+  a.w_router = L.w_router;
+  a.b_router = L.b_router;
+  a.forced_ids = L.forced_ids;
+  a.forced_w = L.forced_w;
+  a.out = L.out;
+  a.out_f32 = L.out_f32;
+  a.ids_out = L.ids_out;
+  a.w_out = L.w_out;
+  a.logits = L.logits;
+  a.h_hi = L.h_hi;
+  a.h_lo = L.h_lo;
+  a.gbar = L.gbar;
+  a.st = L.st;
+  a.nstages = pl.nstages;
+  a.offA = pl.offA;
+  a.offB = pl.offB;
+  a.offR = pl.offR;
+  a.offRing = pl.offRing;
+  a.trace = static_cast<unsigned long long*>(g_trace_buf);
+  if (a.trace && g_trace_bytes < (size_t)G * kTracePoints * sizeof(unsigned long long)) a.trace = nullptr;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(G);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = L.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_layer_kernel, a);
+}
+
+}  // namespace bitmoe

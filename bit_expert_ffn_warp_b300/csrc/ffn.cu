@@ -317,7 +317,8 @@ cudaError_t launch_ffn_up(const FfnArgs& a, cudaStream_t s) {
   const int R = a.T * a.k;
   if (R == 0) return cudaSuccess;
   const size_t sm = up_smem(a.d);
-  cudaError_t err = cudaFuncSetAttribute(ffn_up_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  static int attr_set[64] = {};
+  cudaError_t err = ensure_smem_attr(ffn_up_kernel, sm, attr_set);
   if (err != cudaSuccess) return err;
   const long units = (long)(a.I / kTileRows) * max_blocks(R, a.E);
   const int grid = (int)(units < 2L * num_sms() ? units : 2L * num_sms());
@@ -329,7 +330,8 @@ cudaError_t launch_ffn_down(const FfnArgs& a, cudaStream_t s) {
   const int R = a.T * a.k;
   if (R == 0) return cudaSuccess;
   const size_t sm = down_smem(a.I);
-  cudaError_t err = cudaFuncSetAttribute(ffn_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  static int attr_set[64] = {};
+  cudaError_t err = ensure_smem_attr(ffn_down_kernel, sm, attr_set);
   if (err != cudaSuccess) return err;
   const long units = (long)(a.d / kTileRows) * max_blocks(R, a.E);
   const int grid = (int)(units < 4L * num_sms() ? units : 4L * num_sms());

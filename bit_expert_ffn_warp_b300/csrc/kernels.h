@@ -44,6 +44,35 @@ struct FfnArgs {
 cudaError_t launch_ffn_up(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_ffn_down(const FfnArgs& a, cudaStream_t s);
 
+// ---------------------------------------------------------------- fused decode step (decode.cu)
+struct DecodeLaunch {
+  const uint16_t* x;
+  const uint16_t* resid;
+  int T, d, E, k, I, renorm;
+  const uint8_t* gate;
+  const uint8_t* up;
+  const uint8_t* down;
+  const float* w_router;
+  const float* b_router;
+  const int32_t* forced_ids;  // null = route
+  const float* forced_w;
+  uint16_t* out;
+  float* out_f32;   // may be null
+  int32_t* ids_out;  // may be null
+  float* w_out;      // may be null
+  float* logits;     // scratch [T, E]
+  __half* h_hi;      // scratch [T*k, I]
+  __half* h_lo;
+  unsigned* gbar;    // grid-barrier words (arrivals, epoch), arrivals 0 at launch
+  DevStatus* st;
+  int pdl;           // launch with programmatic dependent launch
+};
+bool decode_fused_eligible(int T, int d, int E, int k, int I);
+// Optional phase-timestamp buffer for the fused decode kernel (null = off).
+extern void* g_trace_buf;
+extern size_t g_trace_bytes;
+cudaError_t launch_decode_fused(const DecodeLaunch& L, cudaStream_t s);
+
 // ---------------------------------------------------------------- combine / norm / pack (misc.cu)
 cudaError_t launch_combine(const float* y_rows, const int32_t* inv, const float* w, const uint16_t* resid, int T,
                            int d, int k, uint16_t* out, float* out_f32, cudaStream_t s);

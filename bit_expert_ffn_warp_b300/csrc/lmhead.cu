@@ -222,13 +222,16 @@ cudaError_t launch_lmhead(const uint16_t* h, int T, int d, int V, const uint8_t*
   cudaError_t err = cudaMemsetAsync(keys, 0, (size_t)T * sizeof(unsigned long long), s);
   if (err != cudaSuccess) return err;
   const size_t sm = lm_smem(d);
-  err = cudaFuncSetAttribute(lmhead_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  static int attr1[64] = {}, attr2[64] = {};
+  err = ensure_smem_attr(lmhead_kernel<1>, sm, attr1);
   if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(lmhead_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  err = ensure_smem_attr(lmhead_kernel<2>, sm, attr2);
   if (err != cudaSuccess) return err;
-  int dev = 0, sms = 148;
+  static int sm_count[64] = {};
+  int dev = 0;
   cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sm_count[dev] == 0) cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+  const int sms = sm_count[dev] > 0 ? sm_count[dev] : 148;
   const int VT = V / kTileRows;
   const int grid = VT < sms ? VT : sms;
   for (int t0 = 0; t0 < T; t0 += kLmTok) {

@@ -204,8 +204,8 @@ cudaError_t launch_permute(const int32_t* ids, int R, int E, int32_t* offsets, i
                            int32_t* blk_prefix, void* scratch, DevStatus* st, cudaStream_t s) {
   if (R <= kSingleMaxRows) {
     const size_t sm = single_smem(E);
-    cudaError_t err = cudaFuncSetAttribute(permute_single_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)sm);
+    static int attr_set[64] = {};
+    cudaError_t err = ensure_smem_attr(permute_single_kernel, sm, attr_set);
     if (err != cudaSuccess) return err;
     permute_single_kernel<<<1, kPermThreads, sm, s>>>(ids, R, E, offsets, sorted_rows, inv, blk_prefix, st);
     return cudaGetLastError();
@@ -215,7 +215,8 @@ cudaError_t launch_permute(const int32_t* ids, int R, int E, int32_t* offsets, i
   permute_hist_kernel<<<nchunks, kPermThreads, (size_t)E * 4, s>>>(ids, R, E, chunk_hist);
   permute_scan_kernel<<<1, kPermThreads, 0, s>>>(chunk_hist, nchunks, E, offsets, blk_prefix);
   const size_t sm = place_smem(E);
-  cudaError_t err = cudaFuncSetAttribute(permute_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  static int attr_set[64] = {};
+  cudaError_t err = ensure_smem_attr(permute_place_kernel, sm, attr_set);
   if (err != cudaSuccess) return err;
   permute_place_kernel<<<nchunks, kPermThreads, sm, s>>>(ids, R, E, chunk_hist, sorted_rows, inv, st);
   return cudaGetLastError();

@@ -86,6 +86,18 @@ const char* bitmoe_status_string(bitmoe_status_t status);
 int bitmoe_last_cuda_error(void);
 const char* bitmoe_version(void);
 
+/* Tracing (off by default): while a device buffer is set, every fused decode
+ * launch writes 16 globaltimer stamps (ns) per CTA into it, as
+ * uint64 [gridDim][16]: 0 start, 1 after the grid-dependency wait, 2 logits
+ * done, 3 after barrier A, 4 routing done, 5 gate/up done, 6 after barrier B,
+ * 7 end; 8 first gate/up unit computed, 9 second unit's tiles landed,
+ * 10 grouping ranks done, 11 routing tables done, 12 first gate/up tiles
+ * landed, 13 h staged, 14 down projection done, 15 first unit's h stored
+ * (0 = not reached).
+ * The buffer must hold gridDim (= SM count) * 128 bytes, else tracing is skipped.
+ * Pass NULL, 0 to turn it off.  Process-wide; not for concurrent callers. */
+bitmoe_status_t bitmoe_set_trace_buffer(void* device_buf, size_t bytes);
+
 /* Bytes of a packed bank of n_mats matrices of rows x K (rows % 16 == 0,
  * K % 128 == 0, group == 32); 0 for an unsupported shape.  Equal to the
  * canonical size q + scale: n_mats * rows * K * 9 / 16. */

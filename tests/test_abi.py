@@ -14,8 +14,8 @@ LIB = os.path.join(ROOT, "bit_expert_ffn_warp_b300", "libbitmoe.so")
 
 @pytest.fixture(scope="module")
 def built():
-    from bit_expert_ffn_warp_b300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__._load_build_module().build()
     assert os.path.exists(LIB)
     return LIB
 

@@ -321,3 +321,57 @@ def test_rmsnorm_parity(T, d):
     y = bm.bitmoe_rmsnorm(torch_bf16_from_bits(x_bits))
     yb = bf16_bits_to_f64(bits_from_torch_bf16(y))
     assert np.all(np.abs(yb - ref) <= bf16_ulp(ref) * 0.5 + 1e-7)
+
+
+# ------------------------------------------------------------------ fused decode launches
+
+
+def test_decode_repeated_launches_share_one_workspace():
+    tensors, lay = flint_layer("normal")
+    ws = bm.moe_workspace(lay, 4)
+    for step in range(12):
+        T = 1 + step % 4
+        x_bits = synth.activations(50, T, FLINT["d"], step=step)
+        ref = oracle.moe_forward(x_bits, tensors, FLINT["k"])
+        if np.any(ref["gap"] < NEAR_TIE):
+            continue
+        x = torch_bf16_from_bits(x_bits)
+        out_f32 = torch.empty((T, FLINT["d"]), dtype=torch.float32, device="cuda")
+        ids = torch.empty((T, FLINT["k"]), dtype=torch.int32, device="cuda")
+        out, _, _, _ = bm.moe_forward(x, lay, ws, out_f32=out_f32, ids_out=ids)
+        torch.cuda.synchronize()
+        assert np.array_equal(ids.cpu().numpy(), ref["ids"]), step
+        check_layer_output(out, out_f32, ref["out"], f"repeat step {step}")
+    assert bm.bitmoe_get_device_status(ws) == 0
+
+
+def test_decode_in_a_cuda_graph():
+    tensors, lay = flint_layer("normal")
+    G = 6
+    xs_bits = [synth.activations(60, 1, FLINT["d"], step=s) for s in range(G)]
+    xs = [torch_bf16_from_bits(b) for b in xs_bits]
+    outs = [torch.empty((1, FLINT["d"]), dtype=torch.float32, device="cuda") for _ in range(G)]
+    ob = [torch.empty((1, FLINT["d"]), dtype=torch.bfloat16, device="cuda") for _ in range(G)]
+    ws = bm.moe_workspace(lay, 1)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for g in range(G):
+            bm.moe_forward(xs[g], lay, ws, out=ob[g], out_f32=outs[g])
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for g in range(G):
+            bm.moe_forward(xs[g], lay, ws, out=ob[g], out_f32=outs[g])
+    for o in outs:
+        o.zero_()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    for g in range(G):
+        ref = oracle.moe_forward(xs_bits[g], tensors, FLINT["k"])
+        if np.any(ref["gap"] < NEAR_TIE):
+            continue
+        check_layer_output(ob[g], outs[g], ref["out"], f"graph step {g}")
+    assert bm.bitmoe_get_device_status(ws) == 0
