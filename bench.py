@@ -351,6 +351,82 @@ def bench_decode_e2e(args, graph, x_slots, out_slots, xs_host, G, T, world):
             "how": f"per {G}-step chunk: pinned host x -> device, graph replay of moe_forward, out -> pinned host"}
 
 
+# ---------------------------------------------------------------- prefill workload
+
+
+def bench_prefill(args, world, rank):
+    """T-token prefill chunk through one MoE layer (Zipf routing skew)."""
+    import torch
+
+    import bit_expert_ffn_warp_b300 as bm
+    import synth
+
+    T = args.T or 4096
+    G = min(args.copies, 4)
+    layers = make_device_layers(G, seed=1 + rank, bias="zipf")
+    xs = [torch.from_numpy(synth.activations(rank, T, D, step=s).view(np.int16)).view(torch.bfloat16).cuda()
+          for s in range(G)]
+    ws = bm.moe_workspace(layers[0], T)
+    out = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    steps = max(1, args.steps)
+    warm = max(3, args.warmup)
+    for s in range(warm):
+        bm.moe_forward(xs[s % G], layers[s % G], ws, out=out)
+    torch.cuda.synchronize()
+    barrier(world)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for s in range(steps):
+            bm.moe_forward(xs[s % G], layers[s % G], ws, out=out)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world) / steps
+
+    # the grouped GEMMs alone (expert FFN call on routed, grouped rows), same inputs
+    ffn_ms, rows_used, active = [], [], []
+    for s in range(G):
+        ids, w = bm.moe_route(xs[s], layers[s], ws)
+        off, rows, inv = bm.moe_permute(ids, layers[s], ws)
+        for _ in range(2):
+            bm.moe_expert_ffn_int4(xs[s], layers[s], off, rows, ws)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        reps = 5
+        for _ in range(reps):
+            bm.moe_expert_ffn_int4(xs[s], layers[s], off, rows, ws)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ffn_ms.append(e0.elapsed_time(e1) / reps)
+        cnt = np.diff(off.cpu().numpy())
+        rows_used.append(int(cnt.sum()))
+        active.append(int((cnt > 0).sum()))
+    flops = 6.0 * T * K_TOP * D * I_FF
+    gemm_ms = float(np.median(ffn_ms))
+    _, bf16_peak, bf16_sus, which = peaks()
+    achieved = flops / (gemm_ms * 1e-3) / 1e12
+    tokens = steps * T * world
+    return {
+        "metric": "MoE-layer prefill tokens/s on 1 B300; grouped-GEMM TFLOP/s vs dense 16-bit tensor peak",
+        "value": round(tokens / (ms * steps / 1e3), 1), "unit": "tokens/s", "n_gpus": world, "steps": steps,
+        "warmup": warm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int4->f16 x f16 -> f32", "data": "synthetic (seeded; weights drawn on device)",
+        "config": {"workload": f"moe_layer_prefill_T{T}", "T": T, "d": D, "E": E, "top_k": K_TOP, "I": I_FF,
+                   "router_bias": "zipf(1.1)", "layer_copies": G,
+                   "l2": f"inputs larger than L2: {G} layer copies of {E * EXPERT_BYTES / 1e6:.0f} MB cycled",
+                   "active_experts_mean": float(np.mean(active)), "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16_peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / bf16_peak, 4), "traffic": None,
+                     "kernel": "expert FFN grouped GEMMs (x->fp16, gate/up+SwiGLU, down)",
+                     "flops_per_launch": flops, "ms_per_launch": gemm_ms, "peak_source": which + " burst bf16 (fp16 same rate)"},
+        "gpu_launches": None,
+        "clocks": clk.summary(),
+    }
+
+
 # ---------------------------------------------------------------- main
 
 
@@ -383,6 +459,8 @@ def main():
     world, rank, local = dist_setup(args)
     if args.workload in ("decode", "batch"):
         res = bench_decode(args, world, rank)
+    elif args.workload == "prefill":
+        res = bench_prefill(args, world, rank)
     else:
         raise SystemExit(f"workload {args.workload} not wired yet")
     if rank == 0:

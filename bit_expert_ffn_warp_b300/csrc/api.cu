@@ -36,6 +36,8 @@ struct MoeWs {
   __half* h_hi;
   __half* h_lo;
   float* y_rows;
+  __half* x16;        // fp16 copy of the activations (grouped-GEMM path)
+  int32_t* nb_prefix;  // [E+1] 128-row blocks per expert (grouped-GEMM path)
   size_t total;
 };
 
@@ -61,6 +63,8 @@ MoeWs moe_layout(const bitmoe_moe_shape_t* sh, int64_t T, void* base) {
   w.h_hi = reinterpret_cast<__half*>(take((size_t)R * sh->I * 2));
   w.h_lo = reinterpret_cast<__half*>(take((size_t)R * sh->I * 2));
   w.y_rows = reinterpret_cast<float*>(take((size_t)R * sh->d * 4));
+  w.x16 = reinterpret_cast<__half*>(take((size_t)T * sh->d * 2));
+  w.nb_prefix = reinterpret_cast<int32_t*>(take((size_t)(sh->E + 1) * 4));
   w.total = off;
   return w;
 }
@@ -111,6 +115,19 @@ FfnArgs ffn_args(const uint16_t* x, int64_t T, const bitmoe_moe_shape_t* sh, con
   a.y_rows = y_rows;
   a.st = w.st;
   return a;
+}
+
+// Expert FFNs of the grouped rows: the tcgen05 grouped GEMMs when the batch
+// routes more than 512 rows (a dense contraction per expert), else the
+// streaming mma.sync kernels.
+// y16 (optional): write fp16 y rows there instead of fp32 a.y_rows (grouped-GEMM path only).
+bool uses_grouped_gemm(const FfnArgs& a) { return (int64_t)a.T * a.k > 512 && prefill_eligible(a.d, a.I); }
+
+cudaError_t run_expert_ffn(const FfnArgs& a, const MoeWs& w, __half* y16, cudaStream_t s) {
+  if (uses_grouped_gemm(a)) return launch_prefill_ffn(a, w.nb_prefix, w.x16, y16, s);
+  cudaError_t e = launch_ffn_up(a, s);
+  if (e == cudaSuccess) e = launch_ffn_down(a, s);
+  return e;
 }
 
 }  // namespace
@@ -221,8 +238,7 @@ bitmoe_status_t moe_expert_ffn_int4(const uint16_t* x, int64_t T, const bitmoe_m
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = launch_blk_prefix(expert_offsets, (int)shape->E, w.blk_prefix, s);
   const FfnArgs a = ffn_args(x, T, shape, weights, expert_offsets, sorted_rows, w.blk_prefix, w, y_rows);
-  if (e == cudaSuccess) e = launch_ffn_up(a, s);
-  if (e == cudaSuccess) e = launch_ffn_down(a, s);
+  if (e == cudaSuccess) e = run_expert_ffn(a, w, nullptr, s);
   return cuda_status(e);
 }
 
@@ -296,9 +312,13 @@ bitmoe_status_t moe_forward(const uint16_t* x, const uint16_t* residual, int64_t
   if (e == cudaSuccess)
     e = launch_permute(w.ids, Ti * k, E, w.offsets, w.sorted_rows, w.inv, w.blk_prefix, w.perm_scratch, w.st, s);
   const FfnArgs a = ffn_args(x, T, shape, weights, w.offsets, w.sorted_rows, w.blk_prefix, w, w.y_rows);
-  if (e == cudaSuccess) e = launch_ffn_up(a, s);
-  if (e == cudaSuccess) e = launch_ffn_down(a, s);
-  if (e == cudaSuccess) e = launch_combine(w.y_rows, w.inv, w.w, residual, Ti, d, k, out, out_f32, s);
+  // the grouped-GEMM path keeps y in fp16 (half the bytes through HBM twice)
+  __half* y16 = uses_grouped_gemm(a) ? reinterpret_cast<__half*>(w.y_rows) : nullptr;
+  if (e == cudaSuccess) e = run_expert_ffn(a, w, y16, s);
+  if (e == cudaSuccess) {
+    if (y16) e = launch_combine_f16(y16, w.inv, w.w, residual, Ti, d, k, out, out_f32, s);
+    else e = launch_combine(w.y_rows, w.inv, w.w, residual, Ti, d, k, out, out_f32, s);
+  }
   if (e == cudaSuccess && topk_ids_out)
     e = cudaMemcpyAsync(topk_ids_out, w.ids, (size_t)T * k * 4, cudaMemcpyDeviceToDevice, s);
   if (e == cudaSuccess && topk_w_out)

@@ -44,6 +44,15 @@ struct FfnArgs {
 cudaError_t launch_ffn_up(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_ffn_down(const FfnArgs& a, cudaStream_t s);
 
+// ---------------------------------------------------------------- prefill grouped GEMMs (prefill.cu)
+// tcgen05 path for many routed rows: writes fp16 h into a.h_hi and y rows
+// into y16 (fp16) when given, else a.y_rows (fp32); nb_prefix [E+1] and
+// x16 [T, d] fp16 are scratch.
+bool prefill_eligible(int d, int I);
+cudaError_t launch_prefill_ffn(const FfnArgs& a, int32_t* nb_prefix, __half* x16, __half* y16, cudaStream_t s);
+cudaError_t launch_combine_f16(const __half* y_rows, const int32_t* inv, const float* w, const uint16_t* resid, int T,
+                               int d, int k, uint16_t* out, float* out_f32, cudaStream_t s);
+
 // ---------------------------------------------------------------- fused decode step (decode.cu)
 struct DecodeLaunch {
   const uint16_t* x;

@@ -45,6 +45,44 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   }
 }
 
+// The same combine reading fp16 y rows (grouped-GEMM path).
+__global__ void __launch_bounds__(256) combine_f16_kernel(const __half* __restrict__ y, const int32_t* __restrict__ inv,
+                                                          const float* __restrict__ w, const uint16_t* resid, int d,
+                                                          int k, uint16_t* out, float* __restrict__ out_f32) {
+  const int t = blockIdx.x;
+  for (int c8 = threadIdx.x * 8; c8 < d; c8 += blockDim.x * 8) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < k; ++j) {
+      const int pos = inv[(size_t)t * k + j];
+      if (pos < 0) continue;
+      const float wj = w[(size_t)t * k + j];
+      const uint4 yv = *reinterpret_cast<const uint4*>(y + (size_t)pos * d + c8);
+      const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&yw[i]));
+        acc[2 * i] = fmaf(wj, f.x, acc[2 * i]);
+        acc[2 * i + 1] = fmaf(wj, f.y, acc[2 * i + 1]);
+      }
+    }
+    const uint4 r = *reinterpret_cast<const uint4*>(resid + (size_t)t * d + c8);
+    const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+    float o[8];
+    uint32_t ob[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o[2 * i] = __uint_as_float(rw[i] << 16) + acc[2 * i];
+      o[2 * i + 1] = __uint_as_float(rw[i] & 0xffff0000u) + acc[2 * i + 1];
+      ob[i] = (uint32_t)float_to_bf16_bits(o[2 * i]) | ((uint32_t)float_to_bf16_bits(o[2 * i + 1]) << 16);
+    }
+    if (out_f32) {
+      *reinterpret_cast<float4*>(out_f32 + (size_t)t * d + c8) = make_float4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<float4*>(out_f32 + (size_t)t * d + c8 + 4) = make_float4(o[4], o[5], o[6], o[7]);
+    }
+    *reinterpret_cast<uint4*>(out + (size_t)t * d + c8) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+  }
+}
+
 // y = x / sqrt(mean(x^2) + eps) with unit gain; fp32 sums in a fixed tree order.
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t* x, int d, float eps, uint16_t* y) {
   __shared__ float part[8];
@@ -132,6 +170,13 @@ cudaError_t launch_combine(const float* y_rows, const int32_t* inv, const float*
                            int d, int k, uint16_t* out, float* out_f32, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   combine_kernel<<<T, 256, 0, s>>>(y_rows, inv, w, resid, d, k, out, out_f32);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_f16(const __half* y_rows, const int32_t* inv, const float* w, const uint16_t* resid, int T,
+                               int d, int k, uint16_t* out, float* out_f32, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  combine_f16_kernel<<<T, 256, 0, s>>>(y_rows, inv, w, resid, d, k, out, out_f32);
   return cudaGetLastError();
 }
 

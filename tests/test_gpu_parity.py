@@ -42,7 +42,7 @@ def tiny_layer(seed=0, bias="zero", renorm=True):
     return t, device_layer(t, TINY["k"], renormalize=renorm)
 
 
-def check_layer_output(out, out_f32, ref, tag=""):
+def check_layer_output(out, out_f32, ref, tag="", exact_path=True):
     o32 = out_f32.cpu().numpy().astype(np.float64)
     ma, rl = max_abs(o32, ref), rel_l2(o32, ref)
     assert ma <= MAX_ABS and rl <= REL_L2, f"{tag}: max-abs {ma:.3g} rel-L2 {rl:.3g}"
@@ -55,7 +55,11 @@ def check_layer_output(out, out_f32, ref, tag=""):
     ob = bits_from_torch_bf16(out)
     agree = float(np.mean(ob == oracle.f64_to_bf16(ref.reshape(-1)).reshape(ref.shape))) if ref.size < 300000 else \
         float(np.mean(ob.reshape(-1)[::7] == oracle.f64_to_bf16(ref.reshape(-1)[::7])))
-    assert agree >= 0.98, f"{tag}: bf16 rounding agreement {agree:.4f}"
+    # the streaming path (exact dequantisation, fp32 sums) rounds like the
+    # oracle almost everywhere; the grouped-GEMM path (fp16 operands) only
+    # has to meet the tolerance above
+    if exact_path:
+        assert agree >= 0.98, f"{tag}: bf16 rounding agreement {agree:.4f}"
     obv = bf16_bits_to_f64(ob)
     assert np.all(np.abs(obv - ref) <= bf16_ulp(ref) + 2 * ma), tag
     return ma, rl
@@ -252,7 +256,7 @@ def test_layer_prefill_zipf(T):
     tensors, lay = flint_layer("zipf")
     x_bits = synth.activations(2, T, FLINT["d"], step=T)
     out, out_f32, ref, _ = run_layer_step(x_bits, tensors, lay, FLINT["k"])
-    check_layer_output(out, out_f32, ref["out"], f"prefill T={T}")
+    check_layer_output(out, out_f32, ref["out"], f"prefill T={T}", exact_path=T * FLINT["k"] <= 512)
 
 
 def test_layer_forced_invalid_ids_flag_and_skip():
