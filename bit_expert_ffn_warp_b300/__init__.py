@@ -72,6 +72,8 @@ _SIGS = {
                                    _P, _P, _P, _P, _SZ, _P]),
     "lmhead_workspace_size": (_SZ, [_I64, _I64, _I64]),
     "lmhead_int4_gemv": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _SZ, _P]),
+    "lmhead_static_scratch_bytes": (_SZ, []),
+    "lmhead_int4_gemv_static": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P, _P, _P]),
     "bitmoe_rmsnorm": (ctypes.c_int, [_P, _I64, _I64, ctypes.c_float, _P, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -297,6 +299,19 @@ def lmhead_int4_gemv(h, w_packed, V: int, workspace, want_logits: bool = True, l
     argmax = torch.empty(T, dtype=torch.int32, device=h.device) if argmax is None else argmax
     _check("lmhead_int4_gemv", _lib.lmhead_int4_gemv(_ptr(h), T, d, V, GROUP, _ptr(w_packed), _ptr(logits),
                                                      _ptr(argmax), _ptr(workspace), workspace.numel(), _stream()))
+    return logits, argmax
+
+
+def lmhead_int4_gemv_static(h, w_packed, V: int, argmax, logits=None):
+    """LM head that allocates nothing: the caller passes every output buffer
+    (``logits`` may be None) and the scratch is the library's fixed array."""
+    T, d = h.shape
+    _need(h, torch.bfloat16, (T, d), "h")
+    _need(argmax, torch.int32, (T,), "argmax")
+    if logits is not None:
+        _need(logits, torch.float32, (T, V), "logits")
+    _check("lmhead_int4_gemv_static", _lib.lmhead_int4_gemv_static(_ptr(h), T, d, V, GROUP, _ptr(w_packed),
+                                                                   _ptr(logits), _ptr(argmax), _stream()))
     return logits, argmax
 
 

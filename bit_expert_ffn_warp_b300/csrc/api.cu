@@ -132,6 +132,10 @@ cudaError_t run_expert_ffn(const FfnArgs& a, const MoeWs& w, __half* y16, cudaSt
 
 }  // namespace
 
+namespace bitmoe {
+bitmoe_status_t api_cuda_status(cudaError_t e) { return cuda_status(e); }
+}  // namespace bitmoe
+
 extern "C" {
 
 const char* bitmoe_status_string(bitmoe_status_t status) {

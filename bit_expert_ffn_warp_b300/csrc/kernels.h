@@ -94,4 +94,8 @@ size_t lmhead_scratch_bytes(int T);
 cudaError_t launch_lmhead(const uint16_t* h, int T, int d, int V, const uint8_t* w_packed, float* logits,
                           int32_t* argmax, void* scratch, DevStatus* st, cudaStream_t s);
 
+// ---------------------------------------------------------------- C-ABI helpers (api.cu)
+// Records e as the thread's last CUDA error (read by bitmoe_last_cuda_error) and maps it to a status.
+bitmoe_status_t api_cuda_status(cudaError_t e);
+
 }  // namespace bitmoe

@@ -195,6 +195,33 @@ bitmoe_status_t lmhead_int4_gemv(const uint16_t* h, int64_t T, int64_t d, int64_
                                  const uint8_t* w_packed, float* logits, int32_t* argmax, void* workspace,
                                  size_t workspace_bytes, void* stream);
 
+/*
+ * lmhead_int4_gemv_static: the LM head above without a workspace argument.
+ * For callers that cannot allocate device memory: code embedded in another
+ * runtime that owns all device memory through its own pool and hands this
+ * library only the pointers of its inputs and outputs, or a per-token loop
+ * that must not call cudaMalloc, which can synchronise the whole device.
+ * The paper has no counterpart to this entry point.
+ *
+ * Arguments, layout and results are those of lmhead_int4_gemv.  The scratch
+ * (a status word and one arg-max key per token) lives in a fixed 1 KiB device
+ * array inside the library, which every GPU that loads the library holds until
+ * the process exits; lmhead_static_scratch_bytes() returns its size.  T <= 64
+ * (768 bytes of it); a larger T returns BITMOE_ERR_WORKSPACE before any launch.
+ * The call allocates nothing.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (the current device); make that first call before any stream
+ * capture.  Each call clears the status word and the keys it uses itself.
+ * All calls share the one array: two calls whose work overlaps on the GPU
+ * (different streams, or different host threads, without ordering between
+ * them) race and may return wrong arg-max values.  If a bounded device-side
+ * wait runs out, every argmax[t] is set to -1.
+ */
+size_t lmhead_static_scratch_bytes(void);
+bitmoe_status_t lmhead_int4_gemv_static(const uint16_t* h, int64_t T, int64_t d, int64_t V, int64_t group,
+                                        const uint8_t* w_packed, float* logits, int32_t* argmax, void* stream);
+
 /* RMSNorm with unit gain between stacked layers: y = x / sqrt(mean(x^2) + eps),
  * computed in fp32, rounded to bf16.  x, y [T, d] bf16 (y may alias x). */
 bitmoe_status_t bitmoe_rmsnorm(const uint16_t* x, int64_t T, int64_t d, float eps, uint16_t* y, void* stream);
