@@ -56,3 +56,48 @@ def bf16_ulp(v):
     v = np.abs(np.asarray(v, np.float64))
     e = np.floor(np.log2(np.maximum(v, 2.0 ** -126)))
     return 2.0 ** (e - 7)
+
+
+def device_drawn_layer(seed, layer, d, E, I, k, bias="normal"):
+    """One MoE layer whose int4 banks are drawn on the device by the generator twin
+    (same bits as ``synth.moe_layer(seed, ..., layer=layer)``) and packed there."""
+    import torch
+
+    import bit_expert_ffn_warp_b300 as bm
+    banks = {}
+    for name, (rows, K) in {"gate": (I, d), "up": (I, d), "down": (d, I)}.items():
+        q = torch.empty(E * rows * K // 2, dtype=torch.uint8, device="cuda")
+        s = torch.empty(E * rows * K // 32, dtype=torch.float16, device="cuda")
+        synth.device_fill_int4(q.data_ptr(), q.numel(), synth.stream_key(seed, synth.TAG[name + "_q"], layer))
+        synth.device_fill_scales(s.data_ptr(), s.numel(), synth.stream_key(seed, synth.TAG[name + "_s"], layer))
+        banks[name] = bm.bitmoe_pack_int4(q.view(E, rows, K // 2), s.view(E, rows, K // 32))
+    wr = torch.from_numpy(synth.router_weight(seed, E, d, layer)).cuda()
+    br = torch.from_numpy(synth.router_bias(seed, E, bias, layer)).cuda()
+    return bm.MoeLayer(d=d, E=E, k=k, I=I, gate=banks["gate"], up=banks["up"], down=banks["down"],
+                       w_router=wr, b_router=br)
+
+
+def device_drawn_lm_head(seed, V, d):
+    """The int4 LM head drawn on the device (same bits as ``synth.lm_head``), packed."""
+    import torch
+
+    import bit_expert_ffn_warp_b300 as bm
+    q = torch.empty(V * d // 2, dtype=torch.uint8, device="cuda")
+    s = torch.empty(V * d // 32, dtype=torch.float16, device="cuda")
+    synth.device_fill_int4(q.data_ptr(), q.numel(), synth.stream_key(seed, synth.TAG["lm_q"], 0))
+    synth.device_fill_scales(s.data_ptr(), s.numel(), synth.stream_key(seed, synth.TAG["lm_s"], 0))
+    return bm.bitmoe_pack_int4(q.view(V, d // 2), s.view(V, d // 32))
+
+
+def expert_bank(seed, layer, d, I, experts, E=256):
+    """Canonical gate/up/down tensors of the listed experts of one layer, in that order."""
+    parts = {}
+    for name, (rows, K) in {"gate": (I, d), "up": (I, d), "down": (d, I)}.items():
+        qs, ss = [], []
+        for e in experts:
+            q, s = synth.int4_matrix(seed, name + "_q", name + "_s", layer, E, rows, K, 32, e, e + 1)
+            qs.append(q)
+            ss.append(s)
+        parts[name + "_q"] = np.concatenate(qs)
+        parts[name + "_s"] = np.concatenate(ss)
+    return parts

@@ -1,0 +1,79 @@
+"""The multi-GPU host path of the benchmark, on CPU with two gloo ranks.
+
+Every rank runs an independent replica of the workload (no data exchange); the
+job's rate is the units all ranks processed over the slowest rank's time, and
+only rank 0 prints.  These tests run the rank arithmetic and the launch under
+torchrun with the gloo backend on 127.0.0.1.
+"""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+torch = pytest.importorskip("torch")
+import torch.distributed as dist  # noqa: E402
+import torch.multiprocessing as mp  # noqa: E402
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    sys.path.insert(0, ROOT)
+    import bench
+    units = 100.0 * (rank + 1)   # rank r processed 100 (r+1) tokens
+    ms = 10.0 * (rank + 1)       # in 10 (r+1) ms
+    res = {
+        "max": bench.max_over_ranks(ms, world),
+        "sum": bench.sum_over_ranks(units, world),
+        "rate": bench.job_throughput(units, ms, world),
+    }
+    bench.barrier(world)
+    out[rank] = res
+    dist.destroy_process_group()
+
+
+def test_rank_reductions_over_two_gloo_ranks():
+    world, port = 2, free_port()
+    with mp.Manager() as mgr:
+        out = mgr.dict()
+        mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
+        res = dict(out)
+    for r in range(world):
+        assert res[r]["max"] == 20.0
+        assert res[r]["sum"] == 300.0
+        # 300 tokens over the slowest rank's 20 ms
+        assert abs(res[r]["rate"] - 15000.0) < 1e-9
+
+
+def test_single_rank_reductions_are_identity():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(3.5, 1) == 3.5
+    assert bench.sum_over_ranks(7.0, 1) == 7.0
+    assert bench.job_throughput(50.0, 10.0, 1) == 5000.0
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    port = free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl", "reference",
+           "--gpus", "2", "--steps", "1", "--warmup", "1", "--cpu-seconds", "0.25"]
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
+    assert rec["cpu_baseline"]["kind"] == "oracle"
