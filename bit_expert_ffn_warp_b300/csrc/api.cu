@@ -36,8 +36,8 @@ struct MoeWs {
   __half* h_hi;
   __half* h_lo;
   float* y_rows;
-  __half* x16;        // fp16 copy of the activations (grouped-GEMM path)
-  int32_t* nb_prefix;  // [E+1] 128-row blocks per expert (grouped-GEMM path)
+  __half* xs;         // [R, d] routed rows in grouped order, fp16 (grouped-GEMM path)
+  int32_t* nb_prefix;  // [E+1] 256-row blocks per expert, then the block list (grouped-GEMM path)
   size_t total;
 };
 
@@ -63,8 +63,9 @@ MoeWs moe_layout(const bitmoe_moe_shape_t* sh, int64_t T, void* base) {
   w.h_hi = reinterpret_cast<__half*>(take((size_t)R * sh->I * 2));
   w.h_lo = reinterpret_cast<__half*>(take((size_t)R * sh->I * 2));
   w.y_rows = reinterpret_cast<float*>(take((size_t)R * sh->d * 4));
-  w.x16 = reinterpret_cast<__half*>(take((size_t)T * sh->d * 2));
-  w.nb_prefix = reinterpret_cast<int32_t*>(take((size_t)(sh->E + 1) * 4));
+  w.xs = reinterpret_cast<__half*>(take((size_t)R * sh->d * 2));
+  // prefix of 256-row expert blocks [E+1], then the blocks widest first [R/256 + E]
+  w.nb_prefix = reinterpret_cast<int32_t*>(take((size_t)(sh->E + 1) * 4 + (size_t)(R / 256 + sh->E + 1) * 4));
   w.total = off;
   return w;
 }
@@ -124,7 +125,7 @@ FfnArgs ffn_args(const uint16_t* x, int64_t T, const bitmoe_moe_shape_t* sh, con
 bool uses_grouped_gemm(const FfnArgs& a) { return (int64_t)a.T * a.k > 512 && prefill_eligible(a.d, a.I); }
 
 cudaError_t run_expert_ffn(const FfnArgs& a, const MoeWs& w, __half* y16, cudaStream_t s) {
-  if (uses_grouped_gemm(a)) return launch_prefill_ffn(a, w.nb_prefix, w.x16, y16, s);
+  if (uses_grouped_gemm(a)) return launch_prefill_ffn(a, w.nb_prefix, w.xs, y16, s);
   cudaError_t e = launch_ffn_up(a, s);
   if (e == cudaSuccess) e = launch_ffn_down(a, s);
   return e;

@@ -1,62 +1,69 @@
 // Prefill expert FFN: grouped GEMMs on the 5th-generation tensor cores.
 //
-// "Flint 40B : Best Mid Sized LLM", transcript 06:11 (kernels for prompt
+// "Flint 40B : Best Mid Sized LLM", transcript 06:43 (kernels for prompt
 // processing and low-bit projections) -- here with B300's tcgen05.mma and
 // tensor memory.  With thousands of routed rows per layer each expert's
 // projection is a real dense contraction:
-//   GEMM1  [n_e x d] x [d x 2I]   gate and up, SwiGLU in the epilogue -> h (fp16)
-//   GEMM2  [n_e x I] x [I x d]    down -> y rows (fp16 inside the layer, fp32 standalone)
+//   GEMM1  h = silu(Wg x) * (Wu x)   per routed row, fp16 h
+//   GEMM2  y = Wd h                  per routed row (fp16 inside the layer, fp32 standalone)
 //
-// Tile: M = 128 routed rows (tokens of one expert), N = 256 weight rows, K in
-// blocks of 64.  For GEMM1 the 256 weight rows are 128 gate rows stacked on
-// the same 128 up rows, so one MMA per k-step produces both halves and a
-// thread of the epilogue holds gate and up of the same features.  Operands
-// live in 128-byte-swizzled K-major shared memory:
-//   A  fp16 token rows, copied with cp.async (activations converted once to
-//      fp16; GEMM1 gathers the rows through the grouping, GEMM2 reads the h
-//      rows of the expert, which are contiguous);
-//   B  int4 weights dequantised by producer warps to fp16 RNE(q * s) -- the
-//      dequantised weight rounded once -- one weight row per thread, with
-//      the packed words of the next four k-blocks in flight in registers.
+// Orientation: D[m, n] = sum_k W[m, k] * X[n, k] -- the MMA's M side is 128
+// weight rows, its N side the routed rows of one expert, up to 256 and cut to
+// the expert's row count rounded up to 16, so a lightly used expert costs
+// little tensor time and a busy one dequantises each weight tile once per 256
+// rows.  For GEMM1 the 128 weight rows are 64 gate rows over the same 64 up
+// rows.  K advances in stages of 64.  Operands live in 128-byte-swizzled
+// K-major shared memory:
+//   A  int4 weights, streamed as packed 1152-byte chunks by TMA bulk copies
+//      into a ring, then dequantised by eight warps to fp16 RNE(q * s) --
+//      the dequantised weight rounded once;
+//   B  fp16 routed rows, contiguous in grouped order (GEMM1: the activations
+//      gathered and converted once to fp16 by a small kernel; GEMM2: the h rows
+//      GEMM1 wrote), loaded by 2-D TMA boxes of 16 rows x 64 K.
 // One thread issues tcgen05.mma (kind::f16, fp32 accumulate) into tensor
-// memory; the two 256-column accumulators alternate so that the epilogue of
-// one tile runs under the MMAs of the next.  Shared memory carries each
-// operand byte once in and once out (a single-thread MMA stream reaches the
-// full tensor rate on this part; what limits a producer-fed GEMM is how much
-// it asks of shared memory).  Roles per CTA (17 warps):
-//   0-7 B producers (weights), 8 MMA issuer + TMEM owner, 9-12 A producers
-//   (tokens), 13-16 epilogue.
+// memory; two 256-column accumulators alternate so that the epilogue of one
+// tile runs under the MMAs of the next.  The epilogue moves each 16-column
+// slice of the accumulator through shared memory so that every warp turns
+// whole routed rows into coalesced stores (GEMM1 pairs gate and up there).
+// Roles per CTA (19 warps): 0 MMA issuer + TMEM owner, 1 weight-chunk TMA,
+// 2-9 dequantisation, 10 routed-row TMA, 11-18 epilogue (two per TMEM lane quarter).
 // Every wait is bounded (status word + clean exit, TMEM freed).
+#include <cuda.h>
+
 #include "kernels.h"
 
 namespace bitmoe {
 namespace {
 
-constexpr int kPM = 128;        // routed rows per tile (MMA M)
-constexpr int kPN = 256;        // weight rows per tile (MMA N)
-constexpr int kPK = 64;         // K per stage (one 128-byte swizzle row of fp16)
-constexpr int kPStages = 4;
-constexpr int kPWarps = 17;
-constexpr int kPThreads = kPWarps * 32;
-constexpr int kABytes = kPM * kPK * 2;  // 16 KB token tile
-constexpr int kBBytes = kPN * kPK * 2;  // 32 KB weight tile
+constexpr int kPM = 128;                  // weight rows per tile (MMA M)
+constexpr int kPNMax = 256;               // routed rows per tile (MMA N, multiple of 16)
+constexpr int kPK = 64;                   // K per operand stage (one 128-byte swizzle row of fp16)
+constexpr int kPStages = 4;               // operand stages
+constexpr int kRawStages = 2;             // packed-weight stages
+constexpr int kRawBytes = 8 * kChunkBytes;            // 128 rows x 128 K packed (9216 B)
+constexpr int kABytes = kPM * kPK * 2;                // 16 KB weight tile
+constexpr int kBBytes = kPNMax * kPK * 2;             // 32 KB routed-row tile
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kPrefetch = 4;            // k-blocks of packed weight words in flight per producer thread
-constexpr int kWarpMMA = 8, kWarpA0 = 9, kWarpEpi0 = 13;
+constexpr int kXchgBytes = 2 * 16 * kPM * 4;          // two 16-column slices of the accumulator, fp32
+constexpr int kPWarps = 19;
+constexpr int kPThreads = kPWarps * 32;
+constexpr int kWarpMMA = 0, kWarpRaw = 1, kWarpDq0 = 2, kWarpB = 10, kWarpEpi0 = 11;
+constexpr int kDqWarps = 8, kEpiWarps = 8;
+constexpr int kBoxRows = 64;              // routed rows per TMA box (a tile loads whole boxes)
+constexpr int kRowsPerBlock = kPNMax;     // routed rows per expert block (tile N bound)
 
 struct PrefillArgs {
+  CUtensorMap tmap_b;  // routed rows [R, Kdim] fp16, box 64 x 16, 128-byte swizzle
   int mode;            // 1 = gate/up + SwiGLU, 2 = down
   int T, d, I, E, k;   // shapes
   int Kdim;            // reduction length (d for mode 1, I for mode 2)
-  int MT;              // weight tiles per expert (I/128 for mode 1, d/256 for mode 2)
+  int FB;              // weight tiles per expert (I/64 for mode 1, d/128 for mode 2)
   const uint8_t* wa;   // packed bank (gate for mode 1, down for mode 2)
   const uint8_t* wb;   // packed bank (up for mode 1)
   int wrows;           // rows per expert in the packed banks (I or d)
-  const __half* x16;   // [T, d] fp16 copy of the activations (mode 1)
-  const __half* hin;   // [R, I] fp16 (mode 2)
   const int32_t* offsets;      // [E+1]
-  const int32_t* sorted_rows;  // [R]
-  const int32_t* nb_prefix;    // [E+1] prefix of ceil(n_e / 128)
+  const int32_t* nb_prefix;    // [E+1] prefix of ceil(n_e / 256)
+  const int32_t* pair_list;    // [nb_prefix[E]] expert blocks, widest first
   __half* hout;        // [R, I] fp16 (mode 1 output)
   float* yout;         // [R, d] fp32 (mode 2 output, when y16 is null)
   __half* y16;         // [R, d] fp16 (mode 2 output)
@@ -65,10 +72,12 @@ struct PrefillArgs {
 };
 
 // Optional per-role cycle counters (clock64) written per CTA when a trace
-// buffer is set: 0 MMA waiting on tokens, 1 MMA waiting on weights, 2 MMA
-// waiting for a free accumulator, 3 MMA total, 5 weight producers waiting for
-// a free stage, 6 weight producers total, 7 token producers waiting for a free
-// stage, 8 epilogue waiting for an accumulator, 9 epilogue total, 11 tiles.
+// buffer is set: 0 MMA waiting on weights, 1 MMA waiting on routed rows,
+// 2 MMA waiting for a free accumulator, 3 MMA total, 4 TMA waiting for a free
+// chunk slot, 5 dequantisation waiting for chunks, 6 dequantisation waiting
+// for a free stage, 7 dequantisation total, 8 row copies waiting for a free
+// stage, 9 epilogue waiting for an accumulator, 10 epilogue total, 11 tiles,
+// 12 MMA issue (fence, four MMAs, commit), 13 sum of the tiles' N.
 __device__ __forceinline__ void ptrace(const PrefillArgs& p, int slot, unsigned long long v) {
   if (p.trace) p.trace[blockIdx.x * 16 + slot] = v;
 }
@@ -117,6 +126,13 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 
+// 8 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar) {
@@ -139,18 +155,46 @@ __device__ __forceinline__ int expert_of(const int32_t* __restrict__ pre, int E,
 }
 
 struct TileInfo {
-  int e, m, p0, nval;
+  int e;      // expert
+  int f;      // weight tile inside the expert (0..FB-1)
+  int p0;     // first grouped row of the tile
+  int nval;   // routed rows in the tile (<= 256)
+  int n;      // MMA N: nval rounded up to 16
 };
 
-__device__ __forceinline__ TileInfo tile_info(const PrefillArgs& p, int tile) {
+// The j-th tile a CTA takes: tiles are ordered widest block first and dealt out in a
+// snake (c, then G-1-c, ...) so that every CTA gets a similar sum of widths.
+__device__ __forceinline__ int snake_tile(int j) {
+  const int G = gridDim.x, c = blockIdx.x;
+  return j * G + ((j & 1) ? G - 1 - c : c);
+}
+
+__device__ __forceinline__ TileInfo tile_info(const PrefillArgs& p, int sidx) {
   TileInfo ti;
-  const int b = tile / p.MT;
-  ti.m = tile - b * p.MT;
+  const int pi = sidx / p.FB;
+  ti.f = sidx - pi * p.FB;
+  const int b = p.pair_list[pi];
   ti.e = expert_of(p.nb_prefix, p.E, b);
-  ti.p0 = p.offsets[ti.e] + (b - p.nb_prefix[ti.e]) * kPM;
+  ti.p0 = p.offsets[ti.e] + (b - p.nb_prefix[ti.e]) * kRowsPerBlock;
   const int rem = p.offsets[ti.e + 1] - ti.p0;
-  ti.nval = rem < kPM ? rem : kPM;
+  ti.nval = rem < kRowsPerBlock ? rem : kRowsPerBlock;
+  ti.n = (ti.nval + 15) & ~15;
   return ti;
+}
+
+// Packed 16-row tile index (inside the expert) of sub-tile i (0..7) of weight tile f.
+__device__ __forceinline__ const uint8_t* subtile_base(const PrefillArgs& p, const TileInfo& ti, int i) {
+  const int rtiles = p.wrows / kTileRows;
+  const uint8_t* bank;
+  int rt;
+  if (p.mode == 1) {  // sub-tiles 0-3: gate rows 64f.., 4-7: the same up rows
+    bank = (i < 4) ? p.wa : p.wb;
+    rt = ti.f * 4 + (i & 3);
+  } else {
+    bank = p.wa;
+    rt = ti.f * 8 + i;
+  }
+  return bank + ((size_t)ti.e * rtiles + rt) * (size_t)tile_bytes(p.Kdim);
 }
 
 // Dequantise the 8 int4 values of one packed word times scale s into 16 bytes of fp16.
@@ -165,48 +209,51 @@ __device__ __forceinline__ uint4 dequant_word_f16(uint32_t w, __half2 s2) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-struct WRaw {
-  uint2 w[4];   // [quarter]: the two group words of this k-block
-  uint32_t sc;  // the two fp16 group scales
-};
-
-// Packed words of row rr (inside its 16-row tile at `tile`) for k-block kb.
-__device__ __forceinline__ void load_wraw(WRaw& a, const uint8_t* tile, int kb, int rr) {
-  const uint8_t* c0 = tile + (size_t)(kb >> 1) * kChunkBytes;
-  const int gg0 = (kb & 1) * 2;
-  a.sc = __ldg(reinterpret_cast<const unsigned int*>(c0 + kChunkQBytes + rr * 8 + gg0 * 2));
-#pragma unroll
-  for (int c = 0; c < 4; ++c) a.w[c] = __ldg(reinterpret_cast<const uint2*>(c0 + (rr * 4 + c) * 16 + gg0 * 4));
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-__global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(PrefillArgs p) {
-  extern __shared__ unsigned char smem_raw[];
-  // 1024-byte aligned base for the swizzled operand tiles
-  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+__global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid_constant__ PrefillArgs p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // the swizzled operand tiles need a 1024-byte aligned base; the dynamic shared memory
+  // window starts there (checked: a misaligned base stops the kernel with a status)
+  if ((smem_u32(smem_raw) & 1023u) != 0) {
+    if (threadIdx.x == 0) record_status(p.st, kStatusCheck, 70, (int)(smem_u32(smem_raw) & 1023u));
+    return;
+  }
+  unsigned char* smem = smem_raw;
   unsigned char* stages = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPStages * kStageBytes);
-  uint64_t* a_full = bars;                 // [kPStages], one arrival per token-producer thread
-  uint64_t* b_full = a_full + kPStages;    // [kPStages], one arrival per weight-producer warp
-  uint64_t* s_empty = b_full + kPStages;   // [kPStages], MMA commit
-  uint64_t* acc_full = s_empty + kPStages; // [2], MMA commit
-  uint64_t* acc_empty = acc_full + 2;      // [2], one arrival per epilogue warp
+  unsigned char* raw = stages + (size_t)kPStages * kStageBytes;
+  float* xchg = reinterpret_cast<float*>(raw + (size_t)kRawStages * kRawBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<unsigned char*>(xchg) + kXchgBytes);
+  uint64_t* raw_full = bars;                  // [kRawStages] TMA transaction count
+  uint64_t* raw_empty = raw_full + kRawStages; // [kRawStages] one arrival per dequantisation warp
+  uint64_t* a_full = raw_empty + kRawStages;   // [kPStages] one arrival per dequantisation warp
+  uint64_t* b_full = a_full + kPStages;        // [kPStages] TMA transaction count
+  uint64_t* s_empty = b_full + kPStages;       // [kPStages] MMA commit
+  uint64_t* acc_full = s_empty + kPStages;     // [2] MMA commit
+  uint64_t* acc_empty = acc_full + 2;          // [2] one arrival per epilogue warp
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
-  int* fail = reinterpret_cast<int*>(tmem_slot + 1);
+  volatile int* epi_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);  // an epilogue wait ran out
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  constexpr uint32_t kTmemCols = 2 * kPN;  // two 256-column accumulators
+  constexpr uint32_t kTmemCols = 2 * kPNMax;  // two 256-column accumulators
 
   if (tid == 0) {
+    for (int s = 0; s < kRawStages; ++s) {
+      mbar_init(&raw_full[s], 1);
+      mbar_init(&raw_empty[s], kDqWarps);
+    }
     for (int s = 0; s < kPStages; ++s) {
-      mbar_init(&a_full[s], 128);
-      mbar_init(&b_full[s], 8);
+      mbar_init(&a_full[s], kDqWarps);
+      mbar_init(&b_full[s], 1);
       mbar_init(&s_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);
+      mbar_init(&acc_empty[b], kEpiWarps);
     }
-    *fail = 0;
+    *epi_abort = 0;
     fence_mbar_init();
   }
   if (warp == kWarpMMA) {
@@ -220,147 +267,175 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(PrefillArgs 
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int nblocks = p.nb_prefix[p.E];
-  const int n_tiles = nblocks * p.MT;
-  const int nkb = p.Kdim / kPK;
-  const int wrow_tiles = p.wrows / kTileRows;  // packed 16-row tiles per expert
-  const int tb = (int)tile_bytes(p.Kdim);       // bytes per packed 16-row tile
+  const int n_tiles = p.nb_prefix[p.E] * p.FB;
+  const int nchunks = p.Kdim / kChunkK;  // 128-K packed chunks per weight row
+  const int nkb = 2 * nchunks;           // 64-K operand stages per tile
 
-  if (warp < 8) {
-    // ---------------- weight producers: one weight row per thread -> fp16 RNE(q*s) into the B tile
-    const int brow = warp * 32 + lane;  // 0..255 inside the tile
-    int it = 0;
-    long long t_wait = 0;
-    const long long t_start = clock64();
-    bool ok = true;
-    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-      const TileInfo ti = tile_info(p, tile);
-      const uint8_t* bank;
-      int wrow;
-      if (p.mode == 1) {  // rows 0..127 gate, 128..255 up, same 128 features
-        bank = (brow < 128) ? p.wa : p.wb;
-        wrow = ti.m * 128 + (brow & 127);
-      } else {
-        bank = p.wa;
-        wrow = ti.m * kPN + brow;
-      }
-      const uint8_t* tile16 = bank + ((size_t)ti.e * wrow_tiles + (wrow >> 4)) * tb;
-      const int rr = wrow & 15;
-      WRaw raw[kPrefetch];
+  if (warp == kWarpRaw) {
+    // ---------------- packed weight chunks: 8 sub-tiles x 1152 B per 128 K, TMA bulk copies
+    if (lane == 0) {
+      int rit = 0;
+      long long t_wait = 0;
+      bool ok = true;
+      for (int j = 0, tile = snake_tile(0); tile < n_tiles && ok; tile = snake_tile(++j)) {
+        const TileInfo ti = tile_info(p, tile);
+        const uint8_t* sb[8];
 #pragma unroll
-      for (int j = 0; j < kPrefetch; ++j)
-        if (j < nkb) load_wraw(raw[j], tile16, j, rr);
-      for (int kb0 = 0; kb0 < nkb && ok; kb0 += kPrefetch) {
-#pragma unroll
-        for (int j = 0; j < kPrefetch; ++j) {
-          const int kb = kb0 + j;
-          if (kb >= nkb) break;
-          const int s = it % kPStages;
+        for (int i = 0; i < 8; ++i) sb[i] = subtile_base(p, ti, i);
+        for (int c = 0; c < nchunks; ++c, ++rit) {
+          const int s = rit % kRawStages;
           const long long w0 = clock64();
-          if (it >= kPStages && !mbar_wait(&s_empty[s], ((it / kPStages) - 1) & 1, p.st, 50)) {
-            *(volatile int*)fail = 1;
+          if (rit >= kRawStages && !mbar_wait(&raw_empty[s], ((rit / kRawStages) - 1) & 1, p.st, 60)) {
             ok = false;
             break;
           }
           t_wait += clock64() - w0;
-          unsigned char* dst = stages + (size_t)s * kStageBytes + kABytes;
-          const __half2 s0 = __half2half2(__ushort_as_half((uint16_t)(raw[j].sc & 0xffffu)));
-          const __half2 s1 = __half2half2(__ushort_as_half((uint16_t)(raw[j].sc >> 16)));
+          mbar_arrive_expect_tx(&raw_full[s], kRawBytes);
+          unsigned char* dst = raw + (size_t)s * kRawBytes;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            // first group of the k-block -> k in [8c, 8c+8), second group -> [32+8c, ...)
-            *reinterpret_cast<uint4*>(dst + swz_off(brow, c)) = dequant_word_f16(raw[j].w[c].x, s0);
-            *reinterpret_cast<uint4*>(dst + swz_off(brow, 4 + c)) = dequant_word_f16(raw[j].w[c].y, s1);
-          }
-          if (kb + kPrefetch < nkb) load_wraw(raw[j], tile16, kb + kPrefetch, rr);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cta(&b_full[s]);
-          ++it;
+          for (int i = 0; i < 8; ++i) bulk_g2s(dst + i * kChunkBytes, sb[i] + (size_t)c * kChunkBytes, kChunkBytes, &raw_full[s]);
         }
       }
+      // copies still in flight land before this thread leaves (every issued chunk is
+      // awaited by the dequantisation warps on the normal path)
+      for (int n = (rit > kRawStages ? rit - kRawStages : 0); n < rit; ++n)
+        mbar_wait(&raw_full[n % kRawStages], (n / kRawStages) & 1, p.st, 61);
+      ptrace(p, 4, t_wait);
     }
-    if (warp == 0 && lane == 0) {
-      ptrace(p, 5, t_wait);
-      ptrace(p, 6, clock64() - t_start);
-    }
-  } else if (warp >= kWarpA0 && warp < kWarpA0 + 4) {
-    // ---------------- token producers: one routed row per thread, cp.async into the A tile;
-    // a stage is published (proxy fence + arrival) once its copies have landed,
-    // keeping up to kInFlight stages of copies outstanding
-    constexpr int kInFlight = 2;
-    const int n = (warp - kWarpA0) * 32 + lane;
-    int it = 0, published = 0;
-    long long t_wait = 0;
+  } else if (warp >= kWarpDq0 && warp < kWarpDq0 + kDqWarps) {
+    // ---------------- dequantisation: warp w owns sub-tile w (16 weight rows); per 128-K chunk
+    // a lane reads one 16-byte quarter (four group words) of two rows and writes the
+    // fp16 values of both 64-K stages
+    const int w = warp - kWarpDq0;
+    const int cq = lane & 3;  // quarter of the chunk: k = 32 g + 8 cq + m
+    int rit = 0, it = 0;
+    long long t_raw = 0, t_stage = 0;
+    const long long t_start = clock64();
     bool ok = true;
-    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-      const TileInfo ti = tile_info(p, tile);
-      const bool valid = n < ti.nval;
-      const int pos = ti.p0 + (valid ? n : 0);
-      const __half* src = (p.mode == 1) ? p.x16 + (size_t)(p.sorted_rows[pos] / p.k) * p.d
-                                        : p.hin + (size_t)pos * p.I;
-      const uint32_t nbytes = valid ? 16u : 0u;  // 0 = zero fill
-      for (int kb = 0; kb < nkb; ++kb, ++it) {
-        const int s = it % kPStages;
+    for (int j = 0, tile = snake_tile(0); tile < n_tiles && ok; tile = snake_tile(++j)) {
+      for (int c = 0; c < nchunks && ok; ++c, ++rit) {
+        const int rs = rit % kRawStages;
         const long long w0 = clock64();
-        if (it >= kPStages && !mbar_wait(&s_empty[s], ((it / kPStages) - 1) & 1, p.st, 51)) {
-          *(volatile int*)fail = 1;
+        if (!mbar_wait(&raw_full[rs], (rit / kRawStages) & 1, p.st, 62)) {
           ok = false;
           break;
         }
-        t_wait += clock64() - w0;
-        const uint32_t dst = smem_u32(stages + (size_t)s * kStageBytes);
+        t_raw += clock64() - w0;
+        const unsigned char* src = raw + (size_t)rs * kRawBytes + w * kChunkBytes;
+        uint4 q[2];
+        uint2 sc[2];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst + swz_off(n, j)),
-                       "l"(src + kb * kPK + j * 8), "r"(nbytes)
-                       : "memory");
-        asm volatile("cp.async.commit_group;" ::: "memory");
-        if (it + 1 - published > kInFlight) {
-          asm volatile("cp.async.wait_group %0;" ::"n"(kInFlight) : "memory");
+        for (int u = 0; u < 2; ++u) {
+          const int rr = 8 * u + (lane >> 2);
+          q[u] = *reinterpret_cast<const uint4*>(src + (rr * 4 + cq) * 16);
+          sc[u] = *reinterpret_cast<const uint2*>(src + kChunkQBytes + rr * 8);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h, ++it) {  // the two 64-K stages of this chunk
+          const int s = it % kPStages;
+          const long long w1 = clock64();
+          if (it >= kPStages && !mbar_wait(&s_empty[s], ((it / kPStages) - 1) & 1, p.st, 63)) {
+            ok = false;
+            break;
+          }
+          t_stage += clock64() - w1;
+          unsigned char* dst = stages + (size_t)s * kStageBytes;
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int row = 16 * w + 8 * u + (lane >> 2);
+            const uint32_t wg0 = h ? q[u].z : q[u].x;  // group 2h
+            const uint32_t wg1 = h ? q[u].w : q[u].y;  // group 2h+1
+            const uint32_t s01 = h ? sc[u].y : sc[u].x;
+            const __half2 s0 = __half2half2(__ushort_as_half((uint16_t)(s01 & 0xffffu)));
+            const __half2 s1 = __half2half2(__ushort_as_half((uint16_t)(s01 >> 16)));
+            const uint4 d0 = dequant_word_f16(wg0, s0), d1 = dequant_word_f16(wg1, s1);
+            // a 128-bit store goes out in phases of 8 lanes = rows r, r+1 of the same 4-chunk
+            // swizzle group; odd rows store their second chunk first so that each phase
+            // covers all 8 chunk positions (no bank conflict)
+            const bool odd = (lane >> 2) & 1;
+            *reinterpret_cast<uint4*>(dst + swz_off(row, odd ? 4 + cq : cq)) = odd ? d1 : d0;
+            *reinterpret_cast<uint4*>(dst + swz_off(row, odd ? cq : 4 + cq)) = odd ? d0 : d1;
+          }
           fence_proxy_async_smem();
-          mbar_arrive_cta(&a_full[published % kPStages]);
-          ++published;
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive_cta(&a_full[s]);
+            // the chunk slot is free only once every lane has used what it loaded from
+            // it: the stores above consumed those registers, and the warp has synced
+            if (h == 0) mbar_arrive_cta(&raw_empty[rs]);
+          }
         }
       }
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    fence_proxy_async_smem();
-    while (published < it) {
-      mbar_arrive_cta(&a_full[published % kPStages]);
-      ++published;
+    if (w == 0 && lane == 0) {
+      ptrace(p, 5, t_raw);
+      ptrace(p, 6, t_stage);
+      ptrace(p, 7, clock64() - t_start);
     }
-    if (warp == kWarpA0 && lane == 0) ptrace(p, 7, t_wait);
+  } else if (warp == kWarpB) {
+    // ---------------- routed rows: N/16 TMA boxes of 16 rows x 64 K per stage
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_b)) : "memory");
+      int it = 0;
+      long long t_wait = 0;
+      bool ok = true;
+      for (int j = 0, tile = snake_tile(0); tile < n_tiles && ok; tile = snake_tile(++j)) {
+        const TileInfo ti = tile_info(p, tile);
+        const int nbox = (ti.n + kBoxRows - 1) / kBoxRows;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % kPStages;
+          const long long w0 = clock64();
+          if (it >= kPStages && !mbar_wait(&s_empty[s], ((it / kPStages) - 1) & 1, p.st, 64)) {
+            ok = false;
+            break;
+          }
+          t_wait += clock64() - w0;
+          mbar_arrive_expect_tx(&b_full[s], (uint32_t)(nbox * kBoxRows * kPK * 2));
+          const uint32_t dst = smem_u32(stages + (size_t)s * kStageBytes + kABytes);
+          for (int i = 0; i < nbox; ++i)
+            asm volatile(
+                "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+                    dst + (uint32_t)(i * kBoxRows * kPK * 2)),
+                "l"(reinterpret_cast<uint64_t>(&p.tmap_b)), "r"(kb * kPK), "r"(ti.p0 + i * kBoxRows),
+                "r"(smem_u32(&b_full[s]))
+                : "memory");
+        }
+      }
+      // boxes still in flight land before this thread leaves
+      for (int n = (it > kPStages ? it - kPStages : 0); n < it; ++n)
+        mbar_wait(&b_full[n % kPStages], (n / kPStages) & 1, p.st, 69);
+      ptrace(p, 8, t_wait);
+    }
   } else if (warp == kWarpMMA) {
     // ---------------- MMA issuer (one thread)
     if (lane == 0) {
-      const uint32_t idesc = umma_idesc_f16(kPM, kPN);
       int it = 0, lt = 0;
-      long long t_a = 0, t_b = 0, t_acc = 0;
+      long long t_a = 0, t_b = 0, t_acc = 0, t_issue = 0, sum_n = 0;
       const long long t_start = clock64();
-      for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++lt) {
+      bool ok = true;
+      for (int j = 0, tile = snake_tile(0); tile < n_tiles && ok; tile = snake_tile(++j), ++lt) {
         const int buf = lt & 1;
         const long long w0 = clock64();
-        if (lt >= 2 && !mbar_wait(&acc_empty[buf], ((lt >> 1) - 1) & 1, p.st, 52)) {
-          *(volatile int*)fail = 1;
-          break;
-        }
+        if (lt >= 2 && !mbar_wait(&acc_empty[buf], ((lt >> 1) - 1) & 1, p.st, 65)) break;
         t_acc += clock64() - w0;
         tc_fence_after();
-        const uint32_t d0 = tmem_base + (uint32_t)(buf * kPN);
-        bool ok = true;
+        const TileInfo ti = tile_info(p, tile);
+        const uint32_t idesc = umma_idesc_f16(kPM, ti.n);
+        sum_n += ti.n;
+        const uint32_t d0 = tmem_base + (uint32_t)(buf * kPNMax);
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % kPStages;
           const long long w1 = clock64();
-          const bool got_a = mbar_wait(&a_full[s], (it / kPStages) & 1, p.st, 53);
+          const bool got_a = mbar_wait(&a_full[s], (it / kPStages) & 1, p.st, 66);
           const long long w2 = clock64();
-          const bool got_b = got_a && mbar_wait(&b_full[s], (it / kPStages) & 1, p.st, 54);
+          const bool got_b = got_a && mbar_wait(&b_full[s], (it / kPStages) & 1, p.st, 67);
           t_a += w2 - w1;
           t_b += clock64() - w2;
           if (!got_b) {
             ok = false;
             break;
           }
+          const long long w3 = clock64();
           tc_fence_after();
           const uint32_t asm_ = smem_u32(stages + (size_t)s * kStageBytes);
           const uint32_t bsm = asm_ + (uint32_t)kABytes;
@@ -369,11 +444,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(PrefillArgs 
             umma_f16(d0, umma_smem_desc(asm_ + ks * 32), umma_smem_desc(bsm + ks * 32), idesc,
                      (kb > 0 || ks > 0) ? 1u : 0u);
           umma_commit(&s_empty[s]);  // frees the stage once these MMAs have read it
+          t_issue += clock64() - w3;
         }
-        if (!ok) {
-          *(volatile int*)fail = 1;
-          break;
-        }
+        if (!ok) break;
         umma_commit(&acc_full[buf]);
       }
       ptrace(p, 0, t_a);
@@ -381,68 +454,77 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(PrefillArgs 
       ptrace(p, 2, t_acc);
       ptrace(p, 3, clock64() - t_start);
       ptrace(p, 11, lt);
+      ptrace(p, 12, t_issue);
+      ptrace(p, 13, sum_n);
     }
   } else if (warp >= kWarpEpi0) {
-    // ---------------- epilogue: TMEM -> registers -> outputs; one routed row per thread
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int n = q * 32 + lane;
-    int lt = 0;
-    long long t_wait = 0;
+    // ---------------- epilogue: per 16-column slice, warp (q, hf) reads columns 8 hf..8 hf+7 of
+    // TMEM lane quarter q into xchg[col][row] (fp32, two slice buffers), the next slice's TMEM
+    // load in flight meanwhile; after one barrier, warp e = 2 q + hf finishes columns 2e, 2e+1
+    // for all 128 rows (GEMM1: SwiGLU of gate rows 0..63 and up rows 64..127 -> h; GEMM2: y)
+    const int q = warp & 3;                    // TMEM lane quarter this warp may access
+    const int hf = (warp - kWarpEpi0) >> 2;    // which 8 columns of a slice it reads
+    const int e2 = 2 * q + hf;                 // which 2 columns of a slice it finishes
+    int lt = 0, slice = 0;
+    long long t_wait = 0, t_bar = 0;
     const long long t_start = clock64();
-    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++lt) {
+    for (int j = 0, tile = snake_tile(0); tile < n_tiles; tile = snake_tile(++j), ++lt) {
       const int buf = lt & 1;
       const long long w0 = clock64();
-      if (!mbar_wait(&acc_full[buf], (lt >> 1) & 1, p.st, 55)) {
-        *(volatile int*)fail = 1;
-        break;
-      }
+      // every epilogue warp runs the same tiles and the same named barriers per tile; once
+      // a wait has run out (flag set) the remaining tiles skip their waits and stores but
+      // keep the barriers, so the eight warps stay in step to the end
+      const bool aborted = *epi_abort != 0;
+      const bool got = !aborted && __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (lt >> 1) & 1, p.st, 68));
+      if (!got && lane == 0) *epi_abort = 1;
       t_wait += clock64() - w0;
       tc_fence_after();
       const TileInfo ti = tile_info(p, tile);
-      const bool valid = n < ti.nval;
-      const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kPN);
-      if (p.mode == 1) {
-        __half* hrow = p.hout + (size_t)(ti.p0 + (valid ? n : 0)) * p.I + ti.m * 128;
-        for (int c0 = 0; c0 < 128; c0 += 16) {
-          uint32_t g[16], u[16];
-          tmem_ld16(tq + (uint32_t)c0, g);
-          tmem_ld16(tq + (uint32_t)(128 + c0), u);
-          tmem_ld_wait();
-          uint32_t hv[8];
+      const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kPNMax + 8 * hf);
+      uint32_t cur[8] = {}, nxt[8] = {};
+      if (got) {
+        tmem_ld8(tq, cur);
+        tmem_ld_wait();
+      }
+      for (int c0 = 0; c0 < ti.n; c0 += 16, ++slice) {
+        const bool more = got && c0 + 16 < ti.n;
+        if (more) tmem_ld8(tq + (uint32_t)(c0 + 16), nxt);
+        float* xb = xchg + (slice & 1) * (16 * kPM);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float h0 = silu_mul(__uint_as_float(g[2 * j]), __uint_as_float(u[2 * j]));
-            const float h1 = silu_mul(__uint_as_float(g[2 * j + 1]), __uint_as_float(u[2 * j + 1]));
-            __half2 h2 = __floats2half2_rn(h0, h1);
-            hv[j] = *reinterpret_cast<uint32_t*>(&h2);
-          }
-          if (valid) {
-            *reinterpret_cast<uint4*>(hrow + c0) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-            *reinterpret_cast<uint4*>(hrow + c0 + 8) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+        for (int c = 0; c < 8; ++c) xb[(8 * hf + c) * kPM + q * 32 + lane] = __uint_as_float(cur[c]);
+        const long long w2 = clock64();
+        named_bar_sync(1, kEpiWarps * 32);
+        t_bar += clock64() - w2;
+        const bool store = got && !*epi_abort;
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const int c = 2 * e2 + jj;
+          const int n = c0 + c;
+          if (n >= ti.nval || !store) continue;
+          const float* col = xb + c * kPM;
+          const size_t pos = (size_t)(ti.p0 + n);
+          if (p.mode == 1) {
+            // features 2 lane, 2 lane + 1 of the 64: gate rows 0..63, up rows 64..127
+            const float2 g = *reinterpret_cast<const float2*>(col + 2 * lane);
+            const float2 u = *reinterpret_cast<const float2*>(col + 64 + 2 * lane);
+            __half2 h2 = __floats2half2_rn(silu_mul(g.x, u.x), silu_mul(g.y, u.y));
+            *reinterpret_cast<__half2*>(p.hout + pos * p.I + ti.f * 64 + 2 * lane) = h2;
+          } else {
+            const float4 y = *reinterpret_cast<const float4*>(col + 4 * lane);
+            const size_t off = pos * p.d + (size_t)ti.f * kPM + 4 * lane;
+            if (p.y16) {
+              __half2 a = __floats2half2_rn(y.x, y.y), b = __floats2half2_rn(y.z, y.w);
+              *reinterpret_cast<uint2*>(p.y16 + off) =
+                  make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+            } else {
+              *reinterpret_cast<float4*>(p.yout + off) = y;
+            }
           }
         }
-      } else {
-        const size_t rowoff = (size_t)(ti.p0 + (valid ? n : 0)) * p.d + (size_t)ti.m * kPN;
-        for (int c0 = 0; c0 < kPN; c0 += 16) {
-          uint32_t g[16];
-          tmem_ld16(tq + (uint32_t)c0, g);
+        if (more) {
           tmem_ld_wait();
-          if (!valid) continue;
-          if (p.y16) {
-            uint32_t hv[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              __half2 h2 = __floats2half2_rn(__uint_as_float(g[2 * j]), __uint_as_float(g[2 * j + 1]));
-              hv[j] = *reinterpret_cast<uint32_t*>(&h2);
-            }
-            *reinterpret_cast<uint4*>(p.y16 + rowoff + c0) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-            *reinterpret_cast<uint4*>(p.y16 + rowoff + c0 + 8) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              *reinterpret_cast<uint4*>(p.yout + rowoff + c0 + 4 * j) =
-                  make_uint4(g[4 * j], g[4 * j + 1], g[4 * j + 2], g[4 * j + 3]);
-          }
+          for (int c = 0; c < 8; ++c) cur[c] = nxt[c];
         }
       }
       tc_fence_before();
@@ -450,8 +532,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(PrefillArgs 
       if (lane == 0) mbar_arrive_cta(&acc_empty[buf]);
     }
     if (warp == kWarpEpi0 && lane == 0) {
-      ptrace(p, 8, t_wait);
-      ptrace(p, 9, clock64() - t_start);
+      ptrace(p, 9, t_wait);
+      ptrace(p, 10, clock64() - t_start);
+      ptrace(p, 15, t_bar);
     }
   }
 
@@ -463,33 +546,97 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(PrefillArgs 
   }
 }
 
-__global__ void nb_prefix_kernel(const int32_t* __restrict__ offsets, int E, int32_t* __restrict__ pre) {
-  // one thread: E <= 1024 small serial scan (prefill only)
-  if (threadIdx.x == 0 && blockIdx.x == 0) {
+// pre[e] = sum over e' < e of ceil(n_e' / 256) (pre[E] = the number of 256-row expert
+// blocks), and list = those blocks ordered by width, widest first.  One CTA of 1024
+// threads, one expert per thread (E <= 1024).
+__global__ void __launch_bounds__(1024) block_list_kernel(const int32_t* __restrict__ offsets, int E,
+                                                          int32_t* __restrict__ pre, int32_t* __restrict__ list) {
+  __shared__ int scan[1024];
+  __shared__ int cnt[17], fill[17];
+  const int e = threadIdx.x;
+  const int n = e < E ? offsets[e + 1] - offsets[e] : 0;
+  const int nb = (n + kRowsPerBlock - 1) / kRowsPerBlock;
+  scan[e] = nb;
+  if (e < 17) cnt[e] = fill[e] = 0;
+  __syncthreads();
+  for (int o = 1; o < 1024; o <<= 1) {  // inclusive scan
+    const int v = e >= o ? scan[e - o] : 0;
+    __syncthreads();
+    scan[e] += v;
+    __syncthreads();
+  }
+  const int first = scan[e] - nb;
+  if (e < E) pre[e] = first;
+  if (e == 1023) pre[E] = scan[1023];
+  // bucket 0 = 256 rows wide, bucket 15 = 16 rows wide
+  for (int j = 0; j < nb; ++j) {
+    const int w = min(kRowsPerBlock, n - j * kRowsPerBlock);
+    atomicAdd(&cnt[16 - (w + 15) / 16], 1);
+  }
+  __syncthreads();
+  if (e == 0) {
     int run = 0;
-    for (int e = 0; e < E; ++e) {
-      pre[e] = run;
-      run += (offsets[e + 1] - offsets[e] + kPM - 1) / kPM;
+    for (int b = 0; b < 16; ++b) {
+      const int c = cnt[b];
+      cnt[b] = run;
+      run += c;
     }
-    pre[E] = run;
+  }
+  __syncthreads();
+  for (int j = 0; j < nb; ++j) {
+    const int w = min(kRowsPerBlock, n - j * kRowsPerBlock);
+    const int b = 16 - (w + 15) / 16;
+    list[cnt[b] + atomicAdd(&fill[b], 1)] = first + j;
   }
 }
 
-__global__ void bf16_to_f16_kernel(const uint16_t* __restrict__ x, size_t n8, __half* __restrict__ y) {
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
-    const uint4 v = reinterpret_cast<const uint4*>(x)[i];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[4];
+// xs[pos] = fp16(x[sorted_rows[pos] / k]): the routed rows in grouped order, one warp per row.
+__global__ void gather_f16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_rows, int R,
+                                  int k, int d, __half* __restrict__ xs) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int pos = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; pos < R; pos += warps) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(sorted_rows[pos] / k) * d);
+    uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)pos * d);
+    for (int i = lane; i < d / 8; i += 32) {
+      const uint4 v = src[i];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      __half2 h2 = __floats2half2_rn(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xffff0000u));
-      o[q] = *reinterpret_cast<uint32_t*>(&h2);
+      for (int q = 0; q < 4; ++q) {
+        __half2 h2 = __floats2half2_rn(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xffff0000u));
+        o[q] = *reinterpret_cast<uint32_t*>(&h2);
+      }
+      dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    reinterpret_cast<uint4*>(y)[i] = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
-constexpr size_t kPSmem = 1024 + (size_t)kPStages * kStageBytes + 256;
+// Tensor map of a row-major [rows, K] fp16 matrix for 64 x 16 boxes with 128-byte swizzle.
+cudaError_t encode_rows_map(CUtensorMap* map, const void* base, int rows, int K) {
+  using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static EncodeFn encode = nullptr;
+  if (encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) return cudaErrorNotSupported;
+    encode = reinterpret_cast<EncodeFn>(fn);
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kPK, (cuuint32_t)kBoxRows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+constexpr size_t kPSmem = (size_t)kPStages * kStageBytes + (size_t)kRawStages * kRawBytes + kXchgBytes + 256;
+static_assert(kPSmem <= 227 * 1024, "shared memory budget");
 
 int sm_count_prefill() {
   static int cnt[64] = {};
@@ -502,26 +649,30 @@ int sm_count_prefill() {
 
 }  // namespace
 
-bool prefill_eligible(int d, int I) { return d % 256 == 0 && I % 256 == 0; }
+bool prefill_eligible(int d, int I) { return d % 128 == 0 && I % 128 == 0 && d >= 128 && I >= 128; }
 
-cudaError_t launch_prefill_ffn(const FfnArgs& a, int32_t* nb_prefix, __half* x16, __half* y16, cudaStream_t s) {
+cudaError_t launch_prefill_ffn(const FfnArgs& a, int32_t* nb_prefix, __half* xs, __half* y16, cudaStream_t s) {
   const int R = a.T * a.k;
   if (R == 0) return cudaSuccess;
   if (!prefill_eligible(a.d, a.I)) return cudaErrorNotSupported;
-  nb_prefix_kernel<<<1, 32, 0, s>>>(a.offsets, a.E, nb_prefix);
-  const size_t n8 = (size_t)a.T * a.d / 8;
-  bf16_to_f16_kernel<<<(int)(n8 / 256 + 1 < 148 * 16 ? n8 / 256 + 1 : 148 * 16), 256, 0, s>>>(a.x, n8, x16);
-  cudaError_t err = cudaGetLastError();
+  PrefillArgs p1 = {};
+  cudaError_t err = encode_rows_map(&p1.tmap_b, xs, R, a.d);
   if (err != cudaSuccess) return err;
+  PrefillArgs p2 = {};
+  if ((err = encode_rows_map(&p2.tmap_b, a.h_hi, R, a.I)) != cudaSuccess) return err;
+  int32_t* pair_list = nb_prefix + a.E + 1;  // [R/256 + E] entries after the prefix
+  block_list_kernel<<<1, 1024, 0, s>>>(a.offsets, a.E, nb_prefix, pair_list);
+  const int gw = (R + 7) / 8;  // blocks of 8 warps
+  gather_f16_kernel<<<gw < 148 * 8 ? gw : 148 * 8, 256, 0, s>>>(a.x, a.sorted_rows, R, a.k, a.d, xs);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
   static int attr1[64] = {};
   if ((err = ensure_smem_attr(prefill_gemm_kernel, kPSmem, attr1)) != cudaSuccess) return err;
   const int G = sm_count_prefill();
-  // upper bound on the 128-row blocks, for the grid size
-  const long blocks = (long)R / kPM + (R < a.E ? R : a.E) + 1;
+  // upper bound on the 256-row expert blocks, for the grid size
+  const long blocks = (long)R / kRowsPerBlock + (R < a.E ? R : a.E) + 1;
   const size_t need = (size_t)2 * G * 16 * sizeof(unsigned long long);
   unsigned long long* tr = (g_trace_buf && g_trace_bytes >= need) ? static_cast<unsigned long long*>(g_trace_buf) : nullptr;
 
-  PrefillArgs p1 = {};
   p1.mode = 1;
   p1.T = a.T;
   p1.d = a.d;
@@ -529,35 +680,40 @@ cudaError_t launch_prefill_ffn(const FfnArgs& a, int32_t* nb_prefix, __half* x16
   p1.E = a.E;
   p1.k = a.k;
   p1.Kdim = a.d;
-  p1.MT = a.I / 128;
+  p1.FB = a.I / 64;
   p1.wa = a.gate;
   p1.wb = a.up;
   p1.wrows = a.I;
-  p1.x16 = x16;
   p1.offsets = a.offsets;
-  p1.sorted_rows = a.sorted_rows;
   p1.nb_prefix = nb_prefix;
+  p1.pair_list = pair_list;
   p1.hout = a.h_hi;  // fp16 h, [R, I]
   p1.st = a.st;
   p1.trace = tr;
-  const long g1 = blocks * p1.MT;
+  const long g1 = blocks * p1.FB;
   prefill_gemm_kernel<<<(int)(g1 < G ? g1 : G), kPThreads, kPSmem, s>>>(p1);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
-  PrefillArgs p2 = p1;
   p2.mode = 2;
+  p2.T = a.T;
+  p2.d = a.d;
+  p2.I = a.I;
+  p2.E = a.E;
+  p2.k = a.k;
   p2.Kdim = a.I;
-  p2.MT = a.d / kPN;
+  p2.FB = a.d / kPM;
   p2.wa = a.down;
   p2.wb = nullptr;
   p2.wrows = a.d;
-  p2.x16 = nullptr;
-  p2.hin = a.h_hi;
+  p2.offsets = a.offsets;
+  p2.nb_prefix = nb_prefix;
+  p2.pair_list = pair_list;
   p2.hout = nullptr;
   p2.yout = a.y_rows;
   p2.y16 = y16;
+  p2.st = a.st;
   p2.trace = tr ? tr + (size_t)G * 16 : nullptr;
-  const long g2 = blocks * p2.MT;
+  const long g2 = blocks * p2.FB;
   prefill_gemm_kernel<<<(int)(g2 < G ? g2 : G), kPThreads, kPSmem, s>>>(p2);
   return cudaGetLastError();
 }
