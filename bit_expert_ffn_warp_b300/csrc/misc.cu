@@ -9,9 +9,10 @@ namespace {
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ inv,
                                                       const float* __restrict__ w, const uint16_t* resid, int d, int k,
                                                       uint16_t* out, float* __restrict__ out_f32) {
-  const int t = blockIdx.x;
-  for (int c8 = threadIdx.x * 8; c8 < d; c8 += blockDim.x * 8) {
+  const int t = blockIdx.y;
+  for (int c8 = (blockIdx.x * blockDim.x + threadIdx.x) * 8; c8 < d; c8 += gridDim.x * blockDim.x * 8) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
     for (int j = 0; j < k; ++j) {
       const int pos = inv[(size_t)t * k + j];
       if (pos < 0) continue;
@@ -49,9 +50,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 __global__ void __launch_bounds__(256) combine_f16_kernel(const __half* __restrict__ y, const int32_t* __restrict__ inv,
                                                           const float* __restrict__ w, const uint16_t* resid, int d,
                                                           int k, uint16_t* out, float* __restrict__ out_f32) {
-  const int t = blockIdx.x;
-  for (int c8 = threadIdx.x * 8; c8 < d; c8 += blockDim.x * 8) {
+  const int t = blockIdx.y;
+  for (int c8 = (blockIdx.x * blockDim.x + threadIdx.x) * 8; c8 < d; c8 += gridDim.x * blockDim.x * 8) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
     for (int j = 0; j < k; ++j) {
       const int pos = inv[(size_t)t * k + j];
       if (pos < 0) continue;
@@ -169,14 +171,26 @@ __global__ void pack_int4_kernel(const uint8_t* __restrict__ q, const uint16_t* 
 cudaError_t launch_combine(const float* y_rows, const int32_t* inv, const float* w, const uint16_t* resid, int T,
                            int d, int k, uint16_t* out, float* out_f32, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  combine_kernel<<<T, 256, 0, s>>>(y_rows, inv, w, resid, d, k, out, out_f32);
+  // 64 threads x 8 columns per CTA, one token per grid row (at most 65535 rows per launch)
+  for (int t0 = 0; t0 < T; t0 += 65535) {
+    const int n = T - t0 < 65535 ? T - t0 : 65535;
+    const size_t o = (size_t)t0 * d;
+    combine_kernel<<<dim3(ceil_div(d, 512), n), 64, 0, s>>>(y_rows, inv + (size_t)t0 * k, w + (size_t)t0 * k,
+                                                             resid + o, d, k, out + o, out_f32 ? out_f32 + o : nullptr);
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_combine_f16(const __half* y_rows, const int32_t* inv, const float* w, const uint16_t* resid, int T,
                                int d, int k, uint16_t* out, float* out_f32, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  combine_f16_kernel<<<T, 256, 0, s>>>(y_rows, inv, w, resid, d, k, out, out_f32);
+  for (int t0 = 0; t0 < T; t0 += 65535) {
+    const int n = T - t0 < 65535 ? T - t0 : 65535;
+    const size_t o = (size_t)t0 * d;
+    combine_f16_kernel<<<dim3(ceil_div(d, 512), n), 64, 0, s>>>(y_rows, inv + (size_t)t0 * k, w + (size_t)t0 * k,
+                                                                 resid + o, d, k, out + o,
+                                                                 out_f32 ? out_f32 + o : nullptr);
+  }
   return cudaGetLastError();
 }
 

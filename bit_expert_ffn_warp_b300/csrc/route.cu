@@ -1,4 +1,4 @@
-// Router: logits = x Wr^T + b (fp32), then per-token top-k and gate weights.
+// Router: logits = x Wr^T + b (fp32 accuracy), then per-token top-k and gate weights.
 //
 // "Flint 40B : Best Mid Sized LLM", transcript 02:35: a small router picks a
 // few of the 256 routed experts for every token.  Softmax over all experts,
@@ -11,106 +11,74 @@
 namespace bitmoe {
 namespace {
 
-// ---------------------------------------------------------------- decode-size router GEMV
+// ---------------------------------------------------------------- router on the tensor cores
 //
-// One CTA per pair of experts, so the 2 MB router matrix is read by every SM
-// at once; each warp owns (token, expert) dot products and reduces them with
-// shuffles.  Lanes read 8 consecutive elements (16 B of x, 32 B of Wr).
-constexpr int kRouteEB = 2;
+// logits = x Wr^T with mma.sync m16n8k16 (bf16 in, fp32 accumulate).  x is bf16
+// already; every fp32 weight is split exactly into three bf16 parts
+// w = hi + mid + lo (each part the truncation of what remains, which fp32
+// holds exactly), so every product x * part is exact in fp32 and the logit
+// carries only fp32 summation error, as a fp32 FMA chain would.  A warp owns
+// 16 tokens x 8 experts over one eighth of K; the eight partial sums are added
+// in a fixed order.
+constexpr int kRmTok = 16, kRmExp = 8, kRmWarps = 8;
 
-__global__ void __launch_bounds__(256) router_gemv_kernel(const uint16_t* __restrict__ x, int T, int d, int E,
-                                                          const float* __restrict__ Wr,
-                                                          const float* __restrict__ b, float* __restrict__ logits) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e0 = blockIdx.x * kRouteEB;
-  const int pairs = T * kRouteEB;
-  for (int pr = warp; pr < pairs; pr += 8) {
-    const int t = pr / kRouteEB;
-    const int e = e0 + pr % kRouteEB;
-    if (e >= E) continue;
-    const uint16_t* xr = x + (size_t)t * d;
-    const float* wr = Wr + (size_t)e * d;
-    float acc = 0.f;
-#pragma unroll 4
-    for (int i = lane * 8; i < d; i += 256) {
-      const uint4 xv = *reinterpret_cast<const uint4*>(xr + i);
-      const float4 w0 = *reinterpret_cast<const float4*>(wr + i);
-      const float4 w1 = *reinterpret_cast<const float4*>(wr + i + 4);
-      acc = fmaf(__uint_as_float(xv.x << 16), w0.x, acc);
-      acc = fmaf(__uint_as_float(xv.x & 0xffff0000u), w0.y, acc);
-      acc = fmaf(__uint_as_float(xv.y << 16), w0.z, acc);
-      acc = fmaf(__uint_as_float(xv.y & 0xffff0000u), w0.w, acc);
-      acc = fmaf(__uint_as_float(xv.z << 16), w1.x, acc);
-      acc = fmaf(__uint_as_float(xv.z & 0xffff0000u), w1.y, acc);
-      acc = fmaf(__uint_as_float(xv.w << 16), w1.z, acc);
-      acc = fmaf(__uint_as_float(xv.w & 0xffff0000u), w1.w, acc);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) logits[(size_t)t * E + e] = acc + (b ? b[e] : 0.f);
-  }
+__device__ __forceinline__ void split3_bf16(float v, uint32_t& hi, uint32_t& mid, uint32_t& lo) {
+  const uint32_t b0 = __float_as_uint(v);
+  const float r1 = v - __uint_as_float(b0 & 0xffff0000u);
+  const uint32_t b1 = __float_as_uint(r1);
+  const float r2 = r1 - __uint_as_float(b1 & 0xffff0000u);
+  hi = b0 >> 16;
+  mid = b1 >> 16;
+  lo = __float_as_uint(r2) >> 16;
 }
 
-// ---------------------------------------------------------------- prefill-size router GEMM
-//
-// 64 tokens x 64 experts per CTA, 32-column slabs of x (bf16 -> fp32) and Wr
-// in shared memory, 4x4 outputs per thread, fp32 FMA in ascending column order.
-constexpr int kRtM = 64, kRtN = 64, kRtK = 32;
-
-__global__ void __launch_bounds__(256) router_gemm_kernel(const uint16_t* __restrict__ x, int T, int d, int E,
-                                                          const float* __restrict__ Wr,
-                                                          const float* __restrict__ b, float* __restrict__ logits) {
-  __shared__ float xs[kRtK][kRtM + 4];
-  __shared__ float ws[kRtK][kRtN + 4];
-  const int tid = threadIdx.x;
-  const int tx = tid & 15, ty = tid >> 4;
-  const int t0 = blockIdx.x * kRtM, e0 = blockIdx.y * kRtN;
-  float acc[4][4] = {};
-  // load mapping: row = tid / 4 (0..63), 8 columns at (tid % 4) * 8
-  const int lr = tid >> 2, lc = (tid & 3) * 8;
-  for (int k0 = 0; k0 < d; k0 += kRtK) {
-    {
-      const int t = t0 + lr;
-      uint4 xv = make_uint4(0, 0, 0, 0);
-      if (t < T) xv = *reinterpret_cast<const uint4*>(x + (size_t)t * d + k0 + lc);
-      const uint32_t wv[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        xs[lc + 2 * i][lr] = __uint_as_float(wv[i] << 16);
-        xs[lc + 2 * i + 1][lr] = __uint_as_float(wv[i] & 0xffff0000u);
-      }
-      const int e = e0 + lr;
-      float4 a = make_float4(0, 0, 0, 0), c = make_float4(0, 0, 0, 0);
-      if (e < E) {
-        a = *reinterpret_cast<const float4*>(Wr + (size_t)e * d + k0 + lc);
-        c = *reinterpret_cast<const float4*>(Wr + (size_t)e * d + k0 + lc + 4);
-      }
-      ws[lc + 0][lr] = a.x; ws[lc + 1][lr] = a.y; ws[lc + 2][lr] = a.z; ws[lc + 3][lr] = a.w;
-      ws[lc + 4][lr] = c.x; ws[lc + 5][lr] = c.y; ws[lc + 6][lr] = c.z; ws[lc + 7][lr] = c.w;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < kRtK; ++kk) {
-      float av[4], bv[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) av[i] = xs[kk][ty * 4 + i];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) bv[j] = ws[kk][tx * 4 + j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
-    }
-    __syncthreads();
+__global__ void __launch_bounds__(kRmWarps * 32) router_mma_kernel(const uint16_t* __restrict__ x, int T, int d, int E,
+                                                                   const float* __restrict__ Wr,
+                                                                   const float* __restrict__ b,
+                                                                   float* __restrict__ logits) {
+  __shared__ float part[kRmWarps][kRmTok][kRmExp];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int t0 = blockIdx.x * kRmTok, e0 = blockIdx.y * kRmExp;
+  const int slice = d / kRmWarps;
+  const int ta = t0 + g, tb = t0 + g + 8, ew = e0 + g;
+  const bool va = ta < T, vb = tb < T;
+  const uint32_t* xa = reinterpret_cast<const uint32_t*>(x + (size_t)(va ? ta : 0) * d);
+  const uint32_t* xb = reinterpret_cast<const uint32_t*>(x + (size_t)(vb ? tb : 0) * d);
+  const float* wr = Wr + (size_t)(ew < E ? ew : 0) * d;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+  for (int kk = warp * slice; kk < (warp + 1) * slice; kk += 16) {
+    uint32_t A[4];
+    A[0] = va ? xa[(kk + 2 * c) >> 1] : 0u;
+    A[1] = vb ? xb[(kk + 2 * c) >> 1] : 0u;
+    A[2] = va ? xa[(kk + 8 + 2 * c) >> 1] : 0u;
+    A[3] = vb ? xb[(kk + 8 + 2 * c) >> 1] : 0u;
+    const float2 w0 = *reinterpret_cast<const float2*>(wr + kk + 2 * c);
+    const float2 w1 = *reinterpret_cast<const float2*>(wr + kk + 8 + 2 * c);
+    uint32_t h0, m0, l0, h1, m1, l1, h2, m2, l2, h3, m3, l3;
+    split3_bf16(w0.x, h0, m0, l0);
+    split3_bf16(w0.y, h1, m1, l1);
+    split3_bf16(w1.x, h2, m2, l2);
+    split3_bf16(w1.y, h3, m3, l3);
+    mma_bf16(acc, A, h0 | (h1 << 16), h2 | (h3 << 16), acc);
+    mma_bf16(acc, A, m0 | (m1 << 16), m2 | (m3 << 16), acc);
+    mma_bf16(acc, A, l0 | (l1 << 16), l2 | (l3 << 16), acc);
   }
+  // D: acc[0..1] token g, experts 2c, 2c+1; acc[2..3] token g+8
+  part[warp][g][2 * c] = acc[0];
+  part[warp][g][2 * c + 1] = acc[1];
+  part[warp][g + 8][2 * c] = acc[2];
+  part[warp][g + 8][2 * c + 1] = acc[3];
+  __syncthreads();
+  if (threadIdx.x < kRmTok * kRmExp) {
+    const int tok = threadIdx.x / kRmExp, ex = threadIdx.x % kRmExp;
+    const int t = t0 + tok, e = e0 + ex;
+    if (t < T && e < E) {
+      float v = 0.f;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = t0 + ty * 4 + i;
-    if (t >= T) continue;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = e0 + tx * 4 + j;
-      if (e < E) logits[(size_t)t * E + e] = acc[i][j] + (b ? b[e] : 0.f);
+      for (int w = 0; w < kRmWarps; ++w) v += part[w][tok][ex];
+      logits[(size_t)t * E + e] = v + (b ? b[e] : 0.f);
     }
   }
 }
@@ -120,6 +88,7 @@ __global__ void __launch_bounds__(256) router_gemm_kernel(const uint16_t* __rest
 // One warp per token.  Lane l holds logits e = l, l+32, ...; k rounds of a
 // warp arg-max over (value desc, index asc) pick the experts in order.  Gates:
 // exp(l_j - l_max) normalised over the chosen k (renorm) or over all E.
+template <int NPER>  // logits per lane: E <= 32 * NPER
 __global__ void __launch_bounds__(256) topk_gates_kernel(const float* __restrict__ logits, int T, int E, int k,
                                                          int renorm, int32_t* __restrict__ ids,
                                                          float* __restrict__ w) {
@@ -127,10 +96,10 @@ __global__ void __launch_bounds__(256) topk_gates_kernel(const float* __restrict
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
   const float* l = logits + (size_t)t * E;
-  float v[kMaxE / 32];
+  float v[NPER];
   const int nper = (E + 31) / 32;
 #pragma unroll
-  for (int i = 0; i < kMaxE / 32; ++i) {
+  for (int i = 0; i < NPER; ++i) {
     const int e = i * 32 + lane;
     v[i] = (i < nper && e < E) ? l[e] : -INFINITY;
   }
@@ -142,7 +111,7 @@ __global__ void __launch_bounds__(256) topk_gates_kernel(const float* __restrict
     float bv = -INFINITY;
     int bi = 0x7fffffff;
 #pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i) {
+    for (int i = 0; i < NPER; ++i) {
       const int e = i * 32 + lane;
       if (i < nper && e < E && !((taken >> i) & 1u)) {
         if (v[i] > bv || (v[i] == bv && e < bi)) {
@@ -173,7 +142,7 @@ __global__ void __launch_bounds__(256) topk_gates_kernel(const float* __restrict
     z = my_e;
   } else {
 #pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i) {
+    for (int i = 0; i < NPER; ++i) {
       const int e = i * 32 + lane;
       if (i < nper && e < E) z += expf(v[i] - vmax);
     }
@@ -213,19 +182,19 @@ __global__ void forced_select_kernel(const int32_t* __restrict__ fid, const floa
 cudaError_t launch_router_logits(const uint16_t* x, int T, int d, int E, const float* w_router,
                                  const float* b_router, float* logits, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  if (T <= 64) {
-    router_gemv_kernel<<<ceil_div(E, kRouteEB), 256, 0, s>>>(x, T, d, E, w_router, b_router, logits);
-  } else {
-    dim3 grid(ceil_div(T, kRtM), ceil_div(E, kRtN));
-    router_gemm_kernel<<<grid, 256, 0, s>>>(x, T, d, E, w_router, b_router, logits);
-  }
+  if (d % (kRmWarps * 16)) return cudaErrorNotSupported;
+  const dim3 grid(ceil_div(T, kRmTok), ceil_div(E, kRmExp));
+  router_mma_kernel<<<grid, kRmWarps * 32, 0, s>>>(x, T, d, E, w_router, b_router, logits);
   return cudaGetLastError();
 }
 
 cudaError_t launch_topk_gates(const float* logits, int T, int E, int k, int renorm, int32_t* ids, float* w,
                               cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  topk_gates_kernel<<<ceil_div(T, 8), 256, 0, s>>>(logits, T, E, k, renorm, ids, w);
+  if (E <= 256)
+    topk_gates_kernel<8><<<ceil_div(T, 8), 256, 0, s>>>(logits, T, E, k, renorm, ids, w);
+  else
+    topk_gates_kernel<kMaxE / 32><<<ceil_div(T, 8), 256, 0, s>>>(logits, T, E, k, renorm, ids, w);
   return cudaGetLastError();
 }
 
