@@ -37,7 +37,7 @@ struct MoeWs {
   __half* h_lo;
   float* y_rows;
   __half* xs;         // [R, d] routed rows in grouped order, fp16 (grouped-GEMM path)
-  int32_t* nb_prefix;  // [E+1] 256-row blocks per expert, then the block list (grouped-GEMM path)
+  int32_t* nb_prefix;  // [E+1] 128-row blocks per expert, then the block list (grouped-GEMM path)
   size_t total;
 };
 
@@ -64,8 +64,8 @@ MoeWs moe_layout(const bitmoe_moe_shape_t* sh, int64_t T, void* base) {
   w.h_lo = reinterpret_cast<__half*>(take((size_t)R * sh->I * 2));
   w.y_rows = reinterpret_cast<float*>(take((size_t)R * sh->d * 4));
   w.xs = reinterpret_cast<__half*>(take((size_t)R * sh->d * 2));
-  // prefix of 256-row expert blocks [E+1], then the blocks widest first [R/256 + E]
-  w.nb_prefix = reinterpret_cast<int32_t*>(take((size_t)(sh->E + 1) * 4 + (size_t)(R / 256 + sh->E + 1) * 4));
+  // prefix of 128-row expert blocks [E+1], then the blocks widest first [R/128 + E]
+  w.nb_prefix = reinterpret_cast<int32_t*>(take((size_t)(sh->E + 1) * 4 + (size_t)(R / 128 + sh->E + 1) * 4));
   w.total = off;
   return w;
 }

@@ -46,7 +46,7 @@ cudaError_t launch_ffn_down(const FfnArgs& a, cudaStream_t s);
 
 // ---------------------------------------------------------------- prefill grouped GEMMs (prefill.cu)
 // tcgen05 path for many routed rows: writes fp16 h into a.h_hi and y rows
-// into y16 (fp16) when given, else a.y_rows (fp32); nb_prefix [E+1 + T*k/256
+// into y16 (fp16) when given, else a.y_rows (fp32); nb_prefix [E+1 + T*k/128
 // + E + 1] and xs [T*k, d] fp16 (the routed rows in grouped order) are scratch.
 bool prefill_eligible(int d, int I);
 cudaError_t launch_prefill_ffn(const FfnArgs& a, int32_t* nb_prefix, __half* xs, __half* y16, cudaStream_t s);

@@ -7,24 +7,25 @@
 //   GEMM1  h = silu(Wg x) * (Wu x)   per routed row, fp16 h
 //   GEMM2  y = Wd h                  per routed row (fp16 inside the layer, fp32 standalone)
 //
-// Orientation: D[m, n] = sum_k W[m, k] * X[n, k] -- the MMA's M side is 128
-// weight rows, its N side the routed rows of one expert, up to 256 and cut to
-// the expert's row count rounded up to 16, so a lightly used expert costs
-// little tensor time and a busy one dequantises each weight tile once per 256
-// rows.  For GEMM1 the 128 weight rows are 64 gate rows over the same 64 up
-// rows.  K advances in stages of 64.  Operands live in 128-byte-swizzled
-// K-major shared memory:
-//   A  int4 weights, streamed as packed 1152-byte chunks by TMA bulk copies
-//      into a ring, then dequantised by eight warps to fp16 RNE(q * s) --
-//      the dequantised weight rounded once;
-//   B  fp16 routed rows, contiguous in grouped order (GEMM1: the activations
+// Orientation: D[m, n] = sum_k X[m, k] * W[n, k] -- the MMA's M side is 128
+// routed rows of one expert (a 128-row block of its grouped rows), its N side
+// 256 weight rows.  For GEMM1 the 256 weight rows are 128 gate rows over the
+// same 128 up rows, so a thread of the epilogue holds gate and up of the same
+// features for its routed row and writes h directly; for GEMM2 they are 256
+// rows of W_down, so a thread writes 256 consecutive y values of its row.
+// K advances in stages of 64.  Operands live in 128-byte-swizzled K-major
+// shared memory:
+//   A  fp16 routed rows, contiguous in grouped order (GEMM1: the activations
 //      gathered and converted once to fp16 by a small kernel; GEMM2: the h rows
-//      GEMM1 wrote), loaded by 2-D TMA boxes of 16 rows x 64 K.
+//      GEMM1 wrote), loaded by 2-D TMA boxes of 64 rows x 64 K;
+//   B  int4 weights, streamed as packed 1152-byte chunks by TMA bulk copies
+//      into a ring, then dequantised by eight warps to fp16 RNE(q * s) --
+//      the dequantised weight rounded once.
 // One thread issues tcgen05.mma (kind::f16, fp32 accumulate) into tensor
 // memory; two 256-column accumulators alternate so that the epilogue of one
-// tile runs under the MMAs of the next.  The epilogue moves each 16-column
-// slice of the accumulator through shared memory so that every warp turns
-// whole routed rows into coalesced stores (GEMM1 pairs gate and up there).
+// tile runs under the MMAs of the next.  A block of an expert with fewer than
+// 128 routed rows still costs a full 128-row MMA; the tensor pipe has room for
+// that, and it keeps every tile the same cost and the epilogue a plain copy.
 // Roles per CTA (19 warps): 0 MMA issuer + TMEM owner, 1 weight-chunk TMA,
 // 2-9 dequantisation, 10 routed-row TMA, 11-18 epilogue (two per TMEM lane quarter).
 // Every wait is bounded (status word + clean exit, TMEM freed).
@@ -35,34 +36,34 @@
 namespace bitmoe {
 namespace {
 
-constexpr int kPM = 128;                  // weight rows per tile (MMA M)
-constexpr int kPNMax = 256;               // routed rows per tile (MMA N, multiple of 16)
+constexpr int kPM = 128;                  // routed rows per tile (MMA M)
+constexpr int kPN = 256;                  // weight rows per tile (MMA N)
 constexpr int kPK = 64;                   // K per operand stage (one 128-byte swizzle row of fp16)
-constexpr int kPStages = 4;               // operand stages
-constexpr int kRawStages = 2;             // packed-weight stages
-constexpr int kRawBytes = 8 * kChunkBytes;            // 128 rows x 128 K packed (9216 B)
-constexpr int kABytes = kPM * kPK * 2;                // 16 KB weight tile
-constexpr int kBBytes = kPNMax * kPK * 2;             // 32 KB routed-row tile
+constexpr int kPStages = 3;               // operand stages
+constexpr int kRawStages = 4;             // packed-weight stages
+constexpr int kSubTiles = kPN / kTileRows;            // 16 packed 16-row tiles per weight tile
+constexpr int kRawBytes = kSubTiles * kChunkBytes;    // 256 rows x 128 K packed (18432 B)
+constexpr int kABytes = kPM * kPK * 2;                // 16 KB routed-row tile
+constexpr int kBBytes = kPN * kPK * 2;                // 32 KB weight tile
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kXchgBytes = 2 * 16 * kPM * 4;          // two 16-column slices of the accumulator, fp32
 constexpr int kPWarps = 19;
 constexpr int kPThreads = kPWarps * 32;
-constexpr int kWarpMMA = 0, kWarpRaw = 1, kWarpDq0 = 2, kWarpB = 10, kWarpEpi0 = 11;
+constexpr int kWarpMMA = 0, kWarpRaw = 1, kWarpDq0 = 2, kWarpA = 10, kWarpEpi0 = 11;
 constexpr int kDqWarps = 8, kEpiWarps = 8;
-constexpr int kBoxRows = 64;              // routed rows per TMA box (a tile loads whole boxes)
-constexpr int kRowsPerBlock = kPNMax;     // routed rows per expert block (tile N bound)
+constexpr int kBoxRows = 64;              // routed rows per TMA box
+constexpr int kRowsPerBlock = kPM;        // routed rows per expert block
 
 struct PrefillArgs {
-  CUtensorMap tmap_b;  // routed rows [R, Kdim] fp16, box 64 x 16, 128-byte swizzle
+  CUtensorMap tmap_a;  // routed rows [R, Kdim] fp16, box 64 x 64, 128-byte swizzle
   int mode;            // 1 = gate/up + SwiGLU, 2 = down
   int T, d, I, E, k;   // shapes
   int Kdim;            // reduction length (d for mode 1, I for mode 2)
-  int FB;              // weight tiles per expert (I/64 for mode 1, d/128 for mode 2)
+  int FB;              // weight tiles per expert (I/128 for mode 1, d/256 for mode 2)
   const uint8_t* wa;   // packed bank (gate for mode 1, down for mode 2)
   const uint8_t* wb;   // packed bank (up for mode 1)
   int wrows;           // rows per expert in the packed banks (I or d)
   const int32_t* offsets;      // [E+1]
-  const int32_t* nb_prefix;    // [E+1] prefix of ceil(n_e / 256)
+  const int32_t* nb_prefix;    // [E+1] prefix of ceil(n_e / 128)
   const int32_t* pair_list;    // [nb_prefix[E]] expert blocks, widest first
   __half* hout;        // [R, I] fp16 (mode 1 output)
   float* yout;         // [R, d] fp32 (mode 2 output, when y16 is null)
@@ -72,7 +73,7 @@ struct PrefillArgs {
 };
 
 // Optional per-role cycle counters (clock64) written per CTA when a trace
-// buffer is set: 0 MMA waiting on weights, 1 MMA waiting on routed rows,
+// buffer is set: 0 MMA waiting on routed rows, 1 MMA waiting on weights,
 // 2 MMA waiting for a free accumulator, 3 MMA total, 4 TMA waiting for a free
 // chunk slot, 5 dequantisation waiting for chunks, 6 dequantisation waiting
 // for a free stage, 7 dequantisation total, 8 row copies waiting for a free
@@ -158,12 +159,11 @@ struct TileInfo {
   int e;      // expert
   int f;      // weight tile inside the expert (0..FB-1)
   int p0;     // first grouped row of the tile
-  int nval;   // routed rows in the tile (<= 256)
-  int n;      // MMA N: nval rounded up to 16
+  int nval;   // routed rows in the tile (<= 128)
 };
 
 // The j-th tile a CTA takes: tiles are ordered widest block first and dealt out in a
-// snake (c, then G-1-c, ...) so that every CTA gets a similar sum of widths.
+// snake (c, then G-1-c, ...).
 __device__ __forceinline__ int snake_tile(int j) {
   const int G = gridDim.x, c = blockIdx.x;
   return j * G + ((j & 1) ? G - 1 - c : c);
@@ -178,21 +178,20 @@ __device__ __forceinline__ TileInfo tile_info(const PrefillArgs& p, int sidx) {
   ti.p0 = p.offsets[ti.e] + (b - p.nb_prefix[ti.e]) * kRowsPerBlock;
   const int rem = p.offsets[ti.e + 1] - ti.p0;
   ti.nval = rem < kRowsPerBlock ? rem : kRowsPerBlock;
-  ti.n = (ti.nval + 15) & ~15;
   return ti;
 }
 
-// Packed 16-row tile index (inside the expert) of sub-tile i (0..7) of weight tile f.
+// Packed 16-row tile (inside the expert's bank) of sub-tile i (0..15) of weight tile f.
 __device__ __forceinline__ const uint8_t* subtile_base(const PrefillArgs& p, const TileInfo& ti, int i) {
   const int rtiles = p.wrows / kTileRows;
   const uint8_t* bank;
   int rt;
-  if (p.mode == 1) {  // sub-tiles 0-3: gate rows 64f.., 4-7: the same up rows
-    bank = (i < 4) ? p.wa : p.wb;
-    rt = ti.f * 4 + (i & 3);
+  if (p.mode == 1) {  // sub-tiles 0-7: gate rows 128f.., 8-15: the same up rows
+    bank = (i < 8) ? p.wa : p.wb;
+    rt = ti.f * 8 + (i & 7);
   } else {
     bank = p.wa;
-    rt = ti.f * 8 + i;
+    rt = ti.f * 16 + i;
   }
   return bank + ((size_t)ti.e * rtiles + rt) * (size_t)tile_bytes(p.Kdim);
 }
@@ -221,23 +220,20 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
     if (threadIdx.x == 0) record_status(p.st, kStatusCheck, 70, (int)(smem_u32(smem_raw) & 1023u));
     return;
   }
-  unsigned char* smem = smem_raw;
-  unsigned char* stages = smem;
+  unsigned char* stages = smem_raw;  // [stage]: A routed rows (16 KB), B weights (32 KB)
   unsigned char* raw = stages + (size_t)kPStages * kStageBytes;
-  float* xchg = reinterpret_cast<float*>(raw + (size_t)kRawStages * kRawBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<unsigned char*>(xchg) + kXchgBytes);
-  uint64_t* raw_full = bars;                  // [kRawStages] TMA transaction count
+  uint64_t* bars = reinterpret_cast<uint64_t*>(raw + (size_t)kRawStages * kRawBytes);
+  uint64_t* raw_full = bars;                   // [kRawStages] TMA transaction count
   uint64_t* raw_empty = raw_full + kRawStages; // [kRawStages] one arrival per dequantisation warp
-  uint64_t* a_full = raw_empty + kRawStages;   // [kPStages] one arrival per dequantisation warp
-  uint64_t* b_full = a_full + kPStages;        // [kPStages] TMA transaction count
-  uint64_t* s_empty = b_full + kPStages;       // [kPStages] MMA commit
+  uint64_t* t_full = raw_empty + kRawStages;   // [kPStages] routed rows: TMA transaction count
+  uint64_t* w_full = t_full + kPStages;        // [kPStages] weights: one arrival per dequantisation warp
+  uint64_t* s_empty = w_full + kPStages;       // [kPStages] MMA commit
   uint64_t* acc_full = s_empty + kPStages;     // [2] MMA commit
   uint64_t* acc_empty = acc_full + 2;          // [2] one arrival per epilogue warp
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
-  volatile int* epi_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);  // an epilogue wait ran out
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  constexpr uint32_t kTmemCols = 2 * kPNMax;  // two 256-column accumulators
+  constexpr uint32_t kTmemCols = 2 * kPN;  // two 256-column accumulators
 
   if (tid == 0) {
     for (int s = 0; s < kRawStages; ++s) {
@@ -245,15 +241,14 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
       mbar_init(&raw_empty[s], kDqWarps);
     }
     for (int s = 0; s < kPStages; ++s) {
-      mbar_init(&a_full[s], kDqWarps);
-      mbar_init(&b_full[s], 1);
+      mbar_init(&t_full[s], 1);
+      mbar_init(&w_full[s], kDqWarps);
       mbar_init(&s_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], kEpiWarps);
     }
-    *epi_abort = 0;
     fence_mbar_init();
   }
   if (warp == kWarpMMA) {
@@ -272,16 +267,16 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
   const int nkb = 2 * nchunks;           // 64-K operand stages per tile
 
   if (warp == kWarpRaw) {
-    // ---------------- packed weight chunks: 8 sub-tiles x 1152 B per 128 K, TMA bulk copies
+    // ---------------- packed weight chunks: 16 sub-tiles x 1152 B per 128 K, TMA bulk copies
     if (lane == 0) {
       int rit = 0;
       long long t_wait = 0;
       bool ok = true;
       for (int j = 0, tile = snake_tile(0); tile < n_tiles && ok; tile = snake_tile(++j)) {
         const TileInfo ti = tile_info(p, tile);
-        const uint8_t* sb[8];
+        const uint8_t* sb[kSubTiles];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) sb[i] = subtile_base(p, ti, i);
+        for (int i = 0; i < kSubTiles; ++i) sb[i] = subtile_base(p, ti, i);
         for (int c = 0; c < nchunks; ++c, ++rit) {
           const int s = rit % kRawStages;
           const long long w0 = clock64();
@@ -293,19 +288,19 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
           mbar_arrive_expect_tx(&raw_full[s], kRawBytes);
           unsigned char* dst = raw + (size_t)s * kRawBytes;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) bulk_g2s(dst + i * kChunkBytes, sb[i] + (size_t)c * kChunkBytes, kChunkBytes, &raw_full[s]);
+          for (int i = 0; i < kSubTiles; ++i)
+            bulk_g2s(dst + i * kChunkBytes, sb[i] + (size_t)c * kChunkBytes, kChunkBytes, &raw_full[s]);
         }
       }
-      // copies still in flight land before this thread leaves (every issued chunk is
-      // awaited by the dequantisation warps on the normal path)
+      // copies still in flight land before this thread leaves
       for (int n = (rit > kRawStages ? rit - kRawStages : 0); n < rit; ++n)
         mbar_wait(&raw_full[n % kRawStages], (n / kRawStages) & 1, p.st, 61);
       ptrace(p, 4, t_wait);
     }
   } else if (warp >= kWarpDq0 && warp < kWarpDq0 + kDqWarps) {
-    // ---------------- dequantisation: warp w owns sub-tile w (16 weight rows); per 128-K chunk
-    // a lane reads one 16-byte quarter (four group words) of two rows and writes the
-    // fp16 values of both 64-K stages
+    // ---------------- dequantisation: warp w owns sub-tiles w and w + 8 (16 weight rows each);
+    // per 128-K chunk a lane reads one 16-byte quarter (four group words) of two rows per
+    // sub-tile and writes the fp16 values of both 64-K stages
     const int w = warp - kWarpDq0;
     const int cq = lane & 3;  // quarter of the chunk: k = 32 g + 8 cq + m
     int rit = 0, it = 0;
@@ -321,14 +316,17 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
           break;
         }
         t_raw += clock64() - w0;
-        const unsigned char* src = raw + (size_t)rs * kRawBytes + w * kChunkBytes;
-        uint4 q[2];
-        uint2 sc[2];
+        uint4 q[2][2];
+        uint2 sc[2][2];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int rr = 8 * u + (lane >> 2);
-          q[u] = *reinterpret_cast<const uint4*>(src + (rr * 4 + cq) * 16);
-          sc[u] = *reinterpret_cast<const uint2*>(src + kChunkQBytes + rr * 8);
+        for (int st = 0; st < 2; ++st) {
+          const unsigned char* src = raw + (size_t)rs * kRawBytes + (w + 8 * st) * kChunkBytes;
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int rr = 8 * u + (lane >> 2);
+            q[st][u] = *reinterpret_cast<const uint4*>(src + (rr * 4 + cq) * 16);
+            sc[st][u] = *reinterpret_cast<const uint2*>(src + kChunkQBytes + rr * 8);
+          }
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h, ++it) {  // the two 64-K stages of this chunk
@@ -339,27 +337,30 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
             break;
           }
           t_stage += clock64() - w1;
-          unsigned char* dst = stages + (size_t)s * kStageBytes;
+          unsigned char* dst = stages + (size_t)s * kStageBytes + kABytes;
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int row = 16 * w + 8 * u + (lane >> 2);
-            const uint32_t wg0 = h ? q[u].z : q[u].x;  // group 2h
-            const uint32_t wg1 = h ? q[u].w : q[u].y;  // group 2h+1
-            const uint32_t s01 = h ? sc[u].y : sc[u].x;
-            const __half2 s0 = __half2half2(__ushort_as_half((uint16_t)(s01 & 0xffffu)));
-            const __half2 s1 = __half2half2(__ushort_as_half((uint16_t)(s01 >> 16)));
-            const uint4 d0 = dequant_word_f16(wg0, s0), d1 = dequant_word_f16(wg1, s1);
-            // a 128-bit store goes out in phases of 8 lanes = rows r, r+1 of the same 4-chunk
-            // swizzle group; odd rows store their second chunk first so that each phase
-            // covers all 8 chunk positions (no bank conflict)
-            const bool odd = (lane >> 2) & 1;
-            *reinterpret_cast<uint4*>(dst + swz_off(row, odd ? 4 + cq : cq)) = odd ? d1 : d0;
-            *reinterpret_cast<uint4*>(dst + swz_off(row, odd ? cq : 4 + cq)) = odd ? d0 : d1;
+          for (int st = 0; st < 2; ++st) {
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int row = 16 * (w + 8 * st) + 8 * u + (lane >> 2);
+              const uint32_t wg0 = h ? q[st][u].z : q[st][u].x;  // group 2h
+              const uint32_t wg1 = h ? q[st][u].w : q[st][u].y;  // group 2h+1
+              const uint32_t s01 = h ? sc[st][u].y : sc[st][u].x;
+              const __half2 s0 = __half2half2(__ushort_as_half((uint16_t)(s01 & 0xffffu)));
+              const __half2 s1 = __half2half2(__ushort_as_half((uint16_t)(s01 >> 16)));
+              const uint4 d0 = dequant_word_f16(wg0, s0), d1 = dequant_word_f16(wg1, s1);
+              // a 128-bit store goes out in phases of 8 lanes = rows r, r+1 of the same
+              // 4-chunk swizzle group; odd rows store their second chunk first so that each
+              // phase covers all 8 chunk positions (no bank conflict)
+              const bool odd = (lane >> 2) & 1;
+              *reinterpret_cast<uint4*>(dst + swz_off(row, odd ? 4 + cq : cq)) = odd ? d1 : d0;
+              *reinterpret_cast<uint4*>(dst + swz_off(row, odd ? cq : 4 + cq)) = odd ? d0 : d1;
+            }
           }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive_cta(&a_full[s]);
+            mbar_arrive_cta(&w_full[s]);
             // the chunk slot is free only once every lane has used what it loaded from
             // it: the stores above consumed those registers, and the warp has synced
             if (h == 0) mbar_arrive_cta(&raw_empty[rs]);
@@ -372,16 +373,15 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
       ptrace(p, 6, t_stage);
       ptrace(p, 7, clock64() - t_start);
     }
-  } else if (warp == kWarpB) {
-    // ---------------- routed rows: N/16 TMA boxes of 16 rows x 64 K per stage
+  } else if (warp == kWarpA) {
+    // ---------------- routed rows: two TMA boxes of 64 rows x 64 K per stage
     if (lane == 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_b)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_a)) : "memory");
       int it = 0;
       long long t_wait = 0;
       bool ok = true;
       for (int j = 0, tile = snake_tile(0); tile < n_tiles && ok; tile = snake_tile(++j)) {
         const TileInfo ti = tile_info(p, tile);
-        const int nbox = (ti.n + kBoxRows - 1) / kBoxRows;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % kPStages;
           const long long w0 = clock64();
@@ -390,27 +390,29 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
             break;
           }
           t_wait += clock64() - w0;
-          mbar_arrive_expect_tx(&b_full[s], (uint32_t)(nbox * kBoxRows * kPK * 2));
-          const uint32_t dst = smem_u32(stages + (size_t)s * kStageBytes + kABytes);
-          for (int i = 0; i < nbox; ++i)
+          mbar_arrive_expect_tx(&t_full[s], (uint32_t)kABytes);
+          const uint32_t dst = smem_u32(stages + (size_t)s * kStageBytes);
+#pragma unroll
+          for (int i = 0; i < kPM / kBoxRows; ++i)
             asm volatile(
                 "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
                     dst + (uint32_t)(i * kBoxRows * kPK * 2)),
-                "l"(reinterpret_cast<uint64_t>(&p.tmap_b)), "r"(kb * kPK), "r"(ti.p0 + i * kBoxRows),
-                "r"(smem_u32(&b_full[s]))
+                "l"(reinterpret_cast<uint64_t>(&p.tmap_a)), "r"(kb * kPK), "r"(ti.p0 + i * kBoxRows),
+                "r"(smem_u32(&t_full[s]))
                 : "memory");
         }
       }
       // boxes still in flight land before this thread leaves
       for (int n = (it > kPStages ? it - kPStages : 0); n < it; ++n)
-        mbar_wait(&b_full[n % kPStages], (n / kPStages) & 1, p.st, 69);
+        mbar_wait(&t_full[n % kPStages], (n / kPStages) & 1, p.st, 69);
       ptrace(p, 8, t_wait);
     }
   } else if (warp == kWarpMMA) {
     // ---------------- MMA issuer (one thread)
     if (lane == 0) {
+      const uint32_t idesc = umma_idesc_f16(kPM, kPN);
       int it = 0, lt = 0;
-      long long t_a = 0, t_b = 0, t_acc = 0, t_issue = 0, sum_n = 0;
+      long long t_a = 0, t_b = 0, t_acc = 0, t_issue = 0;
       const long long t_start = clock64();
       bool ok = true;
       for (int j = 0, tile = snake_tile(0); tile < n_tiles && ok; tile = snake_tile(++j), ++lt) {
@@ -419,23 +421,20 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
         if (lt >= 2 && !mbar_wait(&acc_empty[buf], ((lt >> 1) - 1) & 1, p.st, 65)) break;
         t_acc += clock64() - w0;
         tc_fence_after();
-        const TileInfo ti = tile_info(p, tile);
-        const uint32_t idesc = umma_idesc_f16(kPM, ti.n);
-        sum_n += ti.n;
-        const uint32_t d0 = tmem_base + (uint32_t)(buf * kPNMax);
+        const uint32_t d0 = tmem_base + (uint32_t)(buf * kPN);
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % kPStages;
           const long long w1 = clock64();
-          const bool got_a = mbar_wait(&a_full[s], (it / kPStages) & 1, p.st, 66);
+          const bool got_a = mbar_wait(&t_full[s], (it / kPStages) & 1, p.st, 66);
           const long long w2 = clock64();
-          const bool got_b = got_a && mbar_wait(&b_full[s], (it / kPStages) & 1, p.st, 67);
+          const bool got_b = got_a && mbar_wait(&w_full[s], (it / kPStages) & 1, p.st, 67);
+          const long long w3 = clock64();
           t_a += w2 - w1;
-          t_b += clock64() - w2;
+          t_b += w3 - w2;
           if (!got_b) {
             ok = false;
             break;
           }
-          const long long w3 = clock64();
           tc_fence_after();
           const uint32_t asm_ = smem_u32(stages + (size_t)s * kStageBytes);
           const uint32_t bsm = asm_ + (uint32_t)kABytes;
@@ -455,76 +454,77 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
       ptrace(p, 3, clock64() - t_start);
       ptrace(p, 11, lt);
       ptrace(p, 12, t_issue);
-      ptrace(p, 13, sum_n);
     }
   } else if (warp >= kWarpEpi0) {
-    // ---------------- epilogue: per 16-column slice, warp (q, hf) reads columns 8 hf..8 hf+7 of
-    // TMEM lane quarter q into xchg[col][row] (fp32, two slice buffers), the next slice's TMEM
-    // load in flight meanwhile; after one barrier, warp e = 2 q + hf finishes columns 2e, 2e+1
-    // for all 128 rows (GEMM1: SwiGLU of gate rows 0..63 and up rows 64..127 -> h; GEMM2: y)
-    const int q = warp & 3;                    // TMEM lane quarter this warp may access
-    const int hf = (warp - kWarpEpi0) >> 2;    // which 8 columns of a slice it reads
-    const int e2 = 2 * q + hf;                 // which 2 columns of a slice it finishes
-    int lt = 0, slice = 0;
-    long long t_wait = 0, t_bar = 0;
+    // ---------------- epilogue: thread = one routed row (TMEM lane), warp (q, hf) takes half
+    // of the 256 columns; GEMM1: h = silu(gate col c) * (up col 128 + c) for its 64 features,
+    // GEMM2: its 128 y values; the next 16 columns' TMEM load is in flight meanwhile
+    const int q = warp & 3;                  // TMEM lane quarter this warp may access
+    const int hf = (warp - kWarpEpi0) >> 2;  // which half of the columns
+    const int n = q * 32 + lane;             // routed row inside the tile
+    int lt = 0;
+    long long t_wait = 0;
     const long long t_start = clock64();
+    bool dead = false;  // a wait ran out: no more waits or stores
     for (int j = 0, tile = snake_tile(0); tile < n_tiles; tile = snake_tile(++j), ++lt) {
       const int buf = lt & 1;
       const long long w0 = clock64();
-      // every epilogue warp runs the same tiles and the same named barriers per tile; once
-      // a wait has run out (flag set) the remaining tiles skip their waits and stores but
-      // keep the barriers, so the eight warps stay in step to the end
-      const bool aborted = *epi_abort != 0;
-      const bool got = !aborted && __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (lt >> 1) & 1, p.st, 68));
-      if (!got && lane == 0) *epi_abort = 1;
+      const bool got = !dead && __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (lt >> 1) & 1, p.st, 68));
+      dead = !got;
       t_wait += clock64() - w0;
+      if (dead) break;
       tc_fence_after();
       const TileInfo ti = tile_info(p, tile);
-      const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kPNMax + 8 * hf);
-      uint32_t cur[8] = {}, nxt[8] = {};
-      if (got) {
-        tmem_ld8(tq, cur);
+      const bool valid = n < ti.nval;
+      const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kPN);
+      if (p.mode == 1) {
+        __half* hrow = p.hout + (size_t)(ti.p0 + (valid ? n : 0)) * p.I + ti.f * 128;
+        for (int c0 = hf * 64; c0 < hf * 64 + 64; c0 += 16) {
+          uint32_t g[16], u[16];
+          tmem_ld16(tq + (uint32_t)c0, g);
+          tmem_ld16(tq + (uint32_t)(128 + c0), u);
+          tmem_ld_wait();
+          if (!valid) continue;
+          uint32_t hv[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            __half2 h2 = __floats2half2_rn(silu_mul(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
+                                           silu_mul(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1])));
+            hv[i] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          *reinterpret_cast<uint4*>(hrow + c0) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+          *reinterpret_cast<uint4*>(hrow + c0 + 8) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+        }
+      } else {
+        const size_t rowoff = (size_t)(ti.p0 + (valid ? n : 0)) * p.d + (size_t)ti.f * kPN;
+        uint32_t cur[16], nxt[16];
+        tmem_ld16(tq + (uint32_t)(hf * 128), cur);
         tmem_ld_wait();
-      }
-      for (int c0 = 0; c0 < ti.n; c0 += 16, ++slice) {
-        const bool more = got && c0 + 16 < ti.n;
-        if (more) tmem_ld8(tq + (uint32_t)(c0 + 16), nxt);
-        float* xb = xchg + (slice & 1) * (16 * kPM);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) xb[(8 * hf + c) * kPM + q * 32 + lane] = __uint_as_float(cur[c]);
-        const long long w2 = clock64();
-        named_bar_sync(1, kEpiWarps * 32);
-        t_bar += clock64() - w2;
-        const bool store = got && !*epi_abort;
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          const int c = 2 * e2 + jj;
-          const int n = c0 + c;
-          if (n >= ti.nval || !store) continue;
-          const float* col = xb + c * kPM;
-          const size_t pos = (size_t)(ti.p0 + n);
-          if (p.mode == 1) {
-            // features 2 lane, 2 lane + 1 of the 64: gate rows 0..63, up rows 64..127
-            const float2 g = *reinterpret_cast<const float2*>(col + 2 * lane);
-            const float2 u = *reinterpret_cast<const float2*>(col + 64 + 2 * lane);
-            __half2 h2 = __floats2half2_rn(silu_mul(g.x, u.x), silu_mul(g.y, u.y));
-            *reinterpret_cast<__half2*>(p.hout + pos * p.I + ti.f * 64 + 2 * lane) = h2;
-          } else {
-            const float4 y = *reinterpret_cast<const float4*>(col + 4 * lane);
-            const size_t off = pos * p.d + (size_t)ti.f * kPM + 4 * lane;
+        for (int c0 = hf * 128; c0 < hf * 128 + 128; c0 += 16) {
+          const bool more = c0 + 16 < hf * 128 + 128;
+          if (more) tmem_ld16(tq + (uint32_t)(c0 + 16), nxt);
+          if (valid) {
             if (p.y16) {
-              __half2 a = __floats2half2_rn(y.x, y.y), b = __floats2half2_rn(y.z, y.w);
-              *reinterpret_cast<uint2*>(p.y16 + off) =
-                  make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+              uint32_t hv[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                __half2 h2 = __floats2half2_rn(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1]));
+                hv[i] = *reinterpret_cast<uint32_t*>(&h2);
+              }
+              *reinterpret_cast<uint4*>(p.y16 + rowoff + c0) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+              *reinterpret_cast<uint4*>(p.y16 + rowoff + c0 + 8) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
             } else {
-              *reinterpret_cast<float4*>(p.yout + off) = y;
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                *reinterpret_cast<uint4*>(p.yout + rowoff + c0 + 4 * i) =
+                    make_uint4(cur[4 * i], cur[4 * i + 1], cur[4 * i + 2], cur[4 * i + 3]);
             }
           }
-        }
-        if (more) {
-          tmem_ld_wait();
+          if (more) {
+            tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 8; ++c) cur[c] = nxt[c];
+            for (int i = 0; i < 16; ++i) cur[i] = nxt[i];
+          }
         }
       }
       tc_fence_before();
@@ -534,7 +534,6 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
     if (warp == kWarpEpi0 && lane == 0) {
       ptrace(p, 9, t_wait);
       ptrace(p, 10, clock64() - t_start);
-      ptrace(p, 15, t_bar);
     }
   }
 
@@ -546,7 +545,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
   }
 }
 
-// pre[e] = sum over e' < e of ceil(n_e' / 256) (pre[E] = the number of 256-row expert
+// pre[e] = sum over e' < e of ceil(n_e' / 128) (pre[E] = the number of 128-row expert
 // blocks), and list = those blocks ordered by width, widest first.  One CTA of 1024
 // threads, one expert per thread (E <= 1024).
 __global__ void __launch_bounds__(1024) block_list_kernel(const int32_t* __restrict__ offsets, int E,
@@ -568,7 +567,7 @@ __global__ void __launch_bounds__(1024) block_list_kernel(const int32_t* __restr
   const int first = scan[e] - nb;
   if (e < E) pre[e] = first;
   if (e == 1023) pre[E] = scan[1023];
-  // bucket 0 = 256 rows wide, bucket 15 = 16 rows wide
+  // bucket 0 = 256 rows wide, bucket 15 = 16 rows wide (blocks are at most kRowsPerBlock wide)
   for (int j = 0; j < nb; ++j) {
     const int w = min(kRowsPerBlock, n - j * kRowsPerBlock);
     atomicAdd(&cnt[16 - (w + 15) / 16], 1);
@@ -635,7 +634,7 @@ cudaError_t encode_rows_map(CUtensorMap* map, const void* base, int rows, int K)
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-constexpr size_t kPSmem = (size_t)kPStages * kStageBytes + (size_t)kRawStages * kRawBytes + kXchgBytes + 256;
+constexpr size_t kPSmem = (size_t)kPStages * kStageBytes + (size_t)kRawStages * kRawBytes + 256;
 static_assert(kPSmem <= 227 * 1024, "shared memory budget");
 
 int sm_count_prefill() {
@@ -649,18 +648,18 @@ int sm_count_prefill() {
 
 }  // namespace
 
-bool prefill_eligible(int d, int I) { return d % 128 == 0 && I % 128 == 0 && d >= 128 && I >= 128; }
+bool prefill_eligible(int d, int I) { return d % 256 == 0 && I % 128 == 0 && d >= 256 && I >= 128; }
 
 cudaError_t launch_prefill_ffn(const FfnArgs& a, int32_t* nb_prefix, __half* xs, __half* y16, cudaStream_t s) {
   const int R = a.T * a.k;
   if (R == 0) return cudaSuccess;
   if (!prefill_eligible(a.d, a.I)) return cudaErrorNotSupported;
   PrefillArgs p1 = {};
-  cudaError_t err = encode_rows_map(&p1.tmap_b, xs, R, a.d);
+  cudaError_t err = encode_rows_map(&p1.tmap_a, xs, R, a.d);
   if (err != cudaSuccess) return err;
   PrefillArgs p2 = {};
-  if ((err = encode_rows_map(&p2.tmap_b, a.h_hi, R, a.I)) != cudaSuccess) return err;
-  int32_t* pair_list = nb_prefix + a.E + 1;  // [R/256 + E] entries after the prefix
+  if ((err = encode_rows_map(&p2.tmap_a, a.h_hi, R, a.I)) != cudaSuccess) return err;
+  int32_t* pair_list = nb_prefix + a.E + 1;  // [R/128 + E] entries after the prefix
   block_list_kernel<<<1, 1024, 0, s>>>(a.offsets, a.E, nb_prefix, pair_list);
   const int gw = (R + 7) / 8;  // blocks of 8 warps
   gather_f16_kernel<<<gw < 148 * 8 ? gw : 148 * 8, 256, 0, s>>>(a.x, a.sorted_rows, R, a.k, a.d, xs);
@@ -668,7 +667,7 @@ cudaError_t launch_prefill_ffn(const FfnArgs& a, int32_t* nb_prefix, __half* xs,
   static int attr1[64] = {};
   if ((err = ensure_smem_attr(prefill_gemm_kernel, kPSmem, attr1)) != cudaSuccess) return err;
   const int G = sm_count_prefill();
-  // upper bound on the 256-row expert blocks, for the grid size
+  // upper bound on the 128-row expert blocks, for the grid size
   const long blocks = (long)R / kRowsPerBlock + (R < a.E ? R : a.E) + 1;
   const size_t need = (size_t)2 * G * 16 * sizeof(unsigned long long);
   unsigned long long* tr = (g_trace_buf && g_trace_bytes >= need) ? static_cast<unsigned long long*>(g_trace_buf) : nullptr;
@@ -680,7 +679,7 @@ cudaError_t launch_prefill_ffn(const FfnArgs& a, int32_t* nb_prefix, __half* xs,
   p1.E = a.E;
   p1.k = a.k;
   p1.Kdim = a.d;
-  p1.FB = a.I / 64;
+  p1.FB = a.I / 128;
   p1.wa = a.gate;
   p1.wb = a.up;
   p1.wrows = a.I;
@@ -701,7 +700,7 @@ cudaError_t launch_prefill_ffn(const FfnArgs& a, int32_t* nb_prefix, __half* xs,
   p2.E = a.E;
   p2.k = a.k;
   p2.Kdim = a.I;
-  p2.FB = a.d / kPM;
+  p2.FB = a.d / kPN;
   p2.wa = a.down;
   p2.wb = nullptr;
   p2.wrows = a.d;
