@@ -460,6 +460,27 @@ def bench_prefill(args, world, rank):
     _, bf16_peak, bf16_sus, which = peaks()
     achieved = flops / (gemm_ms * 1e-3) / 1e12
     launches_per_step = count_kernels(lambda: bm.moe_forward(xs[0], layers[0], ws, out=out))
+
+    # end to end through the public call: pinned host tokens in, the layer output back, every step
+    x_pin = [torch.from_numpy(synth.activations(rank, T, D, step=s).view(np.int16)).view(torch.bfloat16).pin_memory()
+             for s in range(G)]
+    out_pin = torch.empty((T, D), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+    e_steps = max(1, min(steps, 20))
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s_ in range(e_steps):
+        x_dev.copy_(x_pin[s_ % G], non_blocking=True)
+        bm.moe_forward(x_dev, layers[s_ % G], ws, out=out)
+        out_pin.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e = {"value": round(job_throughput(e_steps * T, e0.elapsed_time(e1), world), 1), "unit": "tokens/s",
+           "h2d_bytes_per_step": T * D * 2, "d2h_bytes_per_step": T * D * 2,
+           "how": "per step: pinned host tokens -> device, moe_forward, layer output -> pinned host"}
     return {
         "metric": "MoE-layer prefill tokens/s on 1 B300; grouped-GEMM TFLOP/s vs dense 16-bit tensor peak",
         "value": round(job_throughput(steps * T, ms_local, world), 1), "unit": "tokens/s", "n_gpus": world,
@@ -476,6 +497,7 @@ def bench_prefill(args, world, rank):
                      "kernel": "expert FFN grouped GEMMs (x->fp16, gate/up+SwiGLU, down)",
                      "flops_per_launch": flops, "ms_per_launch": gemm_ms, "peak_source": which + " burst bf16 (fp16 same rate)"},
         "gpu_launches": launches_per_step * steps if launches_per_step else None,
+        "e2e": e2e,
         "clocks": clk.summary(),
     }
 
