@@ -1,5 +1,5 @@
 // Fused decode step of the int4 MoE layer: one persistent launch per token
-// batch (T <= 4) runs router -> top-k -> grouping -> gate/up + SwiGLU ->
+// batch (T <= 8) runs router -> top-k -> grouping -> gate/up + SwiGLU ->
 // down + combine.
 //
 // The pages' decode speed comes from a kernel that does the whole decode pass
@@ -37,7 +37,7 @@ constexpr int kDecThreads = kConsumers + 32;
 constexpr int kMaxStages = 16;
 constexpr int kDecMaxE = kConsumers;  // one logit per consumer thread
 constexpr int kDecMaxK = kDecWarps;   // the warp-maxima bound needs k <= number of warps
-constexpr int kDecMaxT = 4;
+constexpr int kDecMaxT = 8;
 constexpr int kTracePoints = 16;
 
 struct DecodeArgs {
