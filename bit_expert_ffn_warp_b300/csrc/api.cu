@@ -122,7 +122,7 @@ FfnArgs ffn_args(const uint16_t* x, int64_t T, const bitmoe_moe_shape_t* sh, con
 // routes more than 512 rows (a dense contraction per expert), else the
 // streaming mma.sync kernels.
 // y16 (optional): write fp16 y rows there instead of fp32 a.y_rows (grouped-GEMM path only).
-bool uses_grouped_gemm(const FfnArgs& a) { return (int64_t)a.T * a.k > 512 && prefill_eligible(a.d, a.I); }
+bool uses_grouped_gemm(const FfnArgs& a) { return (int64_t)a.T * a.k >= 512 && prefill_eligible(a.d, a.I); }
 
 cudaError_t run_expert_ffn(const FfnArgs& a, const MoeWs& w, __half* y16, cudaStream_t s) {
   if (uses_grouped_gemm(a)) return launch_prefill_ffn(a, w.nb_prefix, w.xs, y16, s);

@@ -173,8 +173,9 @@ bitmoe_status_t moe_combine(const float* y_rows, const int32_t* inv_rows, const 
  * residual may equal x.  forced_ids [T, k] / forced_w [T, k] (both or neither)
  * replace the router's choice; forced ids are range-checked on the device.
  * topk_ids_out / topk_w_out / out_f32 may be NULL.  out may alias residual but
- * not x.  Decode-sized batches (T*k <= 512) run the streaming path; larger
- * batches run the grouped-GEMM path.
+ * not x.  Batches of T <= 8 tokens run one fused decode kernel, other batches
+ * with T*k < 512 routed rows the streaming kernels (both exact int4 x bf16 with
+ * fp32 sums); T*k >= 512 runs the tcgen05 grouped GEMM (fp16 operands).
  */
 bitmoe_status_t moe_forward(const uint16_t* x, const uint16_t* residual, int64_t T, const bitmoe_moe_shape_t* shape,
                             const bitmoe_moe_weights_t* weights, const int32_t* forced_ids, const float* forced_w,
