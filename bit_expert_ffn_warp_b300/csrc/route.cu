@@ -61,9 +61,13 @@ __global__ void __launch_bounds__(kRmWarps * 32) router_mma_kernel(const uint16_
     split3_bf16(w0.y, h1, m1, l1);
     split3_bf16(w1.x, h2, m2, l2);
     split3_bf16(w1.y, h3, m3, l3);
-    mma_bf16(acc, A, h0 | (h1 << 16), h2 | (h3 << 16), acc);
-    mma_bf16(acc, A, m0 | (m1 << 16), m2 | (m3 << 16), acc);
-    mma_bf16(acc, A, l0 | (l1 << 16), l2 | (l3 << 16), acc);
+    // one 16-wide step summed from zero on the tensor core, then added in fp32
+    float st[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_bf16(st, A, h0 | (h1 << 16), h2 | (h3 << 16), st);
+    mma_bf16(st, A, m0 | (m1 << 16), m2 | (m3 << 16), st);
+    mma_bf16(st, A, l0 | (l1 << 16), l2 | (l3 << 16), st);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] += st[i];
   }
   // D: acc[0..1] token g, experts 2c, 2c+1; acc[2..3] token g+8
   part[warp][g][2 * c] = acc[0];
@@ -79,6 +83,90 @@ __global__ void __launch_bounds__(kRmWarps * 32) router_mma_kernel(const uint16_
 #pragma unroll
       for (int w = 0; w < kRmWarps; ++w) v += part[w][tok][ex];
       logits[(size_t)t * E + e] = v + (b ? b[e] : 0.f);
+    }
+  }
+}
+
+// The same product for many tokens: 64 tokens x 64 experts per CTA, K in chunks
+// of 64 staged once in shared memory (x as bf16, Wr split into its three bf16
+// parts), eight warps of 16 tokens x 32 experts.  Rows are padded to 72 elements
+// so the fragment loads of a warp hit distinct banks.  Each 16-wide K step is
+// summed on the tensor core from zero and added to the running fp32 sum, which
+// keeps the logits as close to the exact value as a fp32 FMA chain.
+constexpr int kRtT = 64, kRtE = 64, kRtK = 64, kRtPad = 72;
+
+__global__ void __launch_bounds__(256) router_mma_tiled_kernel(const uint16_t* __restrict__ x, int T, int d, int E,
+                                                               const float* __restrict__ Wr,
+                                                               const float* __restrict__ b,
+                                                               float* __restrict__ logits) {
+  __shared__ __align__(16) uint16_t xs[kRtT][kRtPad];
+  __shared__ __align__(16) uint16_t wp[3][kRtE][kRtPad];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int wm = warp & 3, wn = warp >> 2;  // 16-token row block, 32-expert column block
+  const int t0 = blockIdx.x * kRtT, e0 = blockIdx.y * kRtE;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < d; k0 += kRtK) {
+    // x tile: 64 rows x 128 B, two 16-byte pieces per thread
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int piece = tid + i * 256, r = piece >> 3, c8 = (piece & 7) * 8;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (t0 + r < T) v = *reinterpret_cast<const uint4*>(x + (size_t)(t0 + r) * d + k0 + c8);
+      *reinterpret_cast<uint4*>(&xs[r][c8]) = v;
+    }
+    // Wr tile: 64 rows x 256 B, four 16-byte pieces per thread, split into hi / mid / lo
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int piece = tid + i * 256, r = piece >> 4, c4 = (piece & 15) * 4;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e0 + r < E) v = *reinterpret_cast<const float4*>(Wr + (size_t)(e0 + r) * d + k0 + c4);
+      uint32_t h[4], m[4], l[4];
+      split3_bf16(v.x, h[0], m[0], l[0]);
+      split3_bf16(v.y, h[1], m[1], l[1]);
+      split3_bf16(v.z, h[2], m[2], l[2]);
+      split3_bf16(v.w, h[3], m[3], l[3]);
+      *reinterpret_cast<uint2*>(&wp[0][r][c4]) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+      *reinterpret_cast<uint2*>(&wp[1][r][c4]) = make_uint2(m[0] | (m[1] << 16), m[2] | (m[3] << 16));
+      *reinterpret_cast<uint2*>(&wp[2][r][c4]) = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < kRtK; kk += 16) {
+      uint32_t A[4];
+      const int ra = wm * 16 + g;
+      A[0] = *reinterpret_cast<const uint32_t*>(&xs[ra][kk + 2 * c]);
+      A[1] = *reinterpret_cast<const uint32_t*>(&xs[ra + 8][kk + 2 * c]);
+      A[2] = *reinterpret_cast<const uint32_t*>(&xs[ra][kk + 8 + 2 * c]);
+      A[3] = *reinterpret_cast<const uint32_t*>(&xs[ra + 8][kk + 8 + 2 * c]);
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const int rb = wn * 32 + nt * 8 + g;
+        // the three parts of one 16-wide step go into a fresh fragment, which is then
+        // added in fp32: the tensor core's own accumulation never runs over long chains
+        float st[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int part = 0; part < 3; ++part) {
+          const uint32_t b0 = *reinterpret_cast<const uint32_t*>(&wp[part][rb][kk + 2 * c]);
+          const uint32_t b1 = *reinterpret_cast<const uint32_t*>(&wp[part][rb][kk + 8 + 2 * c]);
+          mma_bf16(st, A, b0, b1, st);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[nt][i] += st[i];
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt) {
+    const int e = e0 + wn * 32 + nt * 8 + 2 * c;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int t = t0 + wm * 16 + g + 8 * h;
+      if (t >= T) continue;
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+        if (e + q < E) logits[(size_t)t * E + e + q] = acc[nt][2 * h + q] + (b ? b[e + q] : 0.f);
     }
   }
 }
@@ -182,9 +270,14 @@ __global__ void forced_select_kernel(const int32_t* __restrict__ fid, const floa
 cudaError_t launch_router_logits(const uint16_t* x, int T, int d, int E, const float* w_router,
                                  const float* b_router, float* logits, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  if (d % (kRmWarps * 16)) return cudaErrorNotSupported;
-  const dim3 grid(ceil_div(T, kRmTok), ceil_div(E, kRmExp));
-  router_mma_kernel<<<grid, kRmWarps * 32, 0, s>>>(x, T, d, E, w_router, b_router, logits);
+  if (d % (kRmWarps * 16) || d % kRtK) return cudaErrorNotSupported;
+  if (T <= 64) {
+    const dim3 grid(ceil_div(T, kRmTok), ceil_div(E, kRmExp));
+    router_mma_kernel<<<grid, kRmWarps * 32, 0, s>>>(x, T, d, E, w_router, b_router, logits);
+  } else {
+    const dim3 grid(ceil_div(T, kRtT), ceil_div(E, kRtE));
+    router_mma_tiled_kernel<<<grid, 256, 0, s>>>(x, T, d, E, w_router, b_router, logits);
+  }
   return cudaGetLastError();
 }
 
