@@ -550,9 +550,8 @@ def bench_stack(args, world, rank):
 
     def step():
         resid.copy_(x_slot)
-        for l in range(N_LAYERS):
-            bm.bitmoe_rmsnorm(resid, out=xh)
-            bm.moe_forward(xh, layers[l], ws, residual=resid, out=resid, ids_out=ids[l])
+        for l in range(N_LAYERS):  # RMSNorm inside the layer step, residual updated in place
+            bm.moe_forward_prenorm(resid, layers[l], ws, out=resid, ids_out=ids[l])
         bm.bitmoe_rmsnorm(resid, out=xh)
         bm.lmhead_int4_gemv(xh, lm, V, lm_ws, want_logits=False, argmax=am)
 
@@ -623,7 +622,7 @@ def bench_stack(args, world, rank):
                    "parallelism": f"replicas x{world}", "timing": "CUDA graph of one step, events on stream"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "traffic": None,
-                     "kernel": "whole stack step (49 x decode layer + RMSNorm, LM head)",
+                     "kernel": "whole stack step (49 x pre-norm decode layer, RMSNorm, LM head)",
                      "bytes_per_step": int(step_bytes), "unique_experts_per_layer_mean": float(np.mean(uniq)),
                      "peak_source": which},
         "gpu_launches": launches_per_step * steps if launches_per_step else None,

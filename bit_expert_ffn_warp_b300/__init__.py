@@ -70,6 +70,8 @@ _SIGS = {
     "moe_combine": (ctypes.c_int, [_P, _P, _P, _P, _I64, ctypes.POINTER(MoeShape), _P, _P, _P]),
     "moe_forward": (ctypes.c_int, [_P, _P, _I64, ctypes.POINTER(MoeShape), ctypes.POINTER(MoeWeights), _P, _P, _P,
                                    _P, _P, _P, _P, _SZ, _P]),
+    "moe_forward_prenorm": (ctypes.c_int, [_P, _I64, _P, _P, ctypes.c_float, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                                           _P]),
     "lmhead_workspace_size": (_SZ, [_I64, _I64, _I64]),
     "lmhead_int4_gemv": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _SZ, _P]),
     "lmhead_static_scratch_bytes": (_SZ, []),
@@ -282,6 +284,21 @@ def moe_forward(x, layer: MoeLayer, workspace, residual=None, forced_ids=None, f
                                            _ptr(forced_ids), _ptr(forced_w), _ptr(ids_out), _ptr(w_out), _ptr(out),
                                            _ptr(out_f32), _ptr(workspace), workspace.numel(), _stream()))
     return out, out_f32, ids_out, w_out
+
+
+def moe_forward_prenorm(residual, layer: MoeLayer, workspace, eps: float = 1e-6, out=None, out_f32=None,
+                        xh_out=None, ids_out=None, w_out=None, forced_ids=None, forced_w=None):
+    """out = residual + MoE(RMSNorm(residual)); out may be residual itself (in place)."""
+    T = residual.shape[0]
+    _need(residual, torch.bfloat16, (T, layer.d), "residual")
+    out = torch.empty_like(residual) if out is None else out
+    wts = layer.weights
+    sh = layer.shape
+    _check("moe_forward_prenorm",
+           _lib.moe_forward_prenorm(_ptr(residual), T, ctypes.byref(sh), ctypes.byref(wts), float(eps),
+                                    _ptr(forced_ids), _ptr(forced_w), _ptr(ids_out), _ptr(w_out), _ptr(xh_out),
+                                    _ptr(out), _ptr(out_f32), _ptr(workspace), workspace.numel(), _stream()))
+    return out
 
 
 # ---------------------------------------------------------------- LM head and norm

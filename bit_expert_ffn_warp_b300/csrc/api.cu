@@ -38,6 +38,7 @@ struct MoeWs {
   float* y_rows;
   __half* xs;         // [R, d] routed rows in grouped order, fp16 (grouped-GEMM path)
   int32_t* nb_prefix;  // [E+1] 128-row blocks per expert, then the block list (grouped-GEMM path)
+  uint16_t* xh;        // [T, d] bf16 RMSNorm of the residual (pre-norm step, unfused path)
   size_t total;
 };
 
@@ -66,6 +67,7 @@ MoeWs moe_layout(const bitmoe_moe_shape_t* sh, int64_t T, void* base) {
   w.xs = reinterpret_cast<__half*>(take((size_t)R * sh->d * 2));
   // prefix of 128-row expert blocks [E+1], then the blocks widest first [R/128 + E]
   w.nb_prefix = reinterpret_cast<int32_t*>(take((size_t)(sh->E + 1) * 4 + (size_t)(R / 128 + sh->E + 1) * 4));
+  w.xh = reinterpret_cast<uint16_t*>(take((size_t)T * sh->d * 2));
   w.total = off;
   return w;
 }
@@ -136,6 +138,93 @@ cudaError_t run_expert_ffn(const FfnArgs& a, const MoeWs& w, __half* y16, cudaSt
 namespace bitmoe {
 bitmoe_status_t api_cuda_status(cudaError_t e) { return cuda_status(e); }
 }  // namespace bitmoe
+
+namespace {
+
+// One layer step.  prenorm: x is the residual and the layer runs on RMSNorm(x) (unit gain,
+// eps), optionally copied to xh_out.
+bitmoe_status_t forward_impl(const uint16_t* x, const uint16_t* residual, int64_t T, const bitmoe_moe_shape_t* shape,
+                             const bitmoe_moe_weights_t* weights, const int32_t* forced_ids, const float* forced_w,
+                             int32_t* topk_ids_out, float* topk_w_out, uint16_t* out, float* out_f32,
+                             void* workspace, size_t workspace_bytes, void* stream, int prenorm, float eps,
+                             uint16_t* xh_out) {
+  bitmoe_status_t st = check_shape(shape, T);
+  if (st != BITMOE_OK) return st;
+  if (T == 0) return BITMOE_OK;
+  if ((forced_ids == nullptr) != (forced_w == nullptr)) return BITMOE_ERR_INVALID_ARG;
+  if ((st = check_weights(weights, forced_ids == nullptr)) != BITMOE_OK) return st;
+  if (!x || !residual || !out || !aligned16(x) || !aligned16(residual) || !aligned16(out) ||
+      (out_f32 && !aligned16(out_f32)) || (xh_out && !aligned16(xh_out)) || !(eps >= 0.f))
+    return BITMOE_ERR_INVALID_ARG;
+  if ((st = check_ws(shape, T, workspace, workspace_bytes)) != BITMOE_OK) return st;
+  const MoeWs w = moe_layout(shape, T, workspace);
+  cudaStream_t s = (cudaStream_t)stream;
+  const int Ti = (int)T, d = (int)shape->d, E = (int)shape->E, k = (int)shape->k;
+  cudaError_t e;
+  if (decode_fused_eligible(Ti, d, E, k, (int)shape->I)) {
+    DecodeLaunch L;
+    L.x = x;
+    L.resid = residual;
+    L.T = Ti;
+    L.d = d;
+    L.E = E;
+    L.k = k;
+    L.I = (int)shape->I;
+    L.renorm = shape->renormalize;
+    L.gate = weights->gate;
+    L.up = weights->up;
+    L.down = weights->down;
+    L.w_router = weights->w_router;
+    L.b_router = weights->b_router;
+    L.forced_ids = forced_ids;
+    L.forced_w = forced_w;
+    L.out = out;
+    L.out_f32 = out_f32;
+    L.ids_out = topk_ids_out;
+    L.w_out = topk_w_out;
+    L.logits = w.logits;
+    L.h_hi = w.h_hi;
+    L.h_lo = w.h_lo;
+    L.gbar = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(w.st) + 64);
+    L.st = w.st;
+    L.pdl = 1;
+    L.prenorm = prenorm;
+    L.eps = eps;
+    L.xh_out = xh_out;
+    e = launch_decode_fused(L, s);
+    if (e != cudaErrorNotSupported) return cuda_status(e);
+    (void)cudaGetLastError();
+  }
+  if (prenorm) {  // the unfused path normalises first, into xh_out or the workspace
+    uint16_t* xh = xh_out ? xh_out : w.xh;
+    e = launch_rmsnorm(x, Ti, d, eps, xh, s);
+    if (e != cudaSuccess) return cuda_status(e);
+    x = xh;
+  }
+  if (forced_ids) {
+    e = launch_forced_select(forced_ids, forced_w, Ti, E, k, w.ids, w.w, w.st, s);
+  } else {
+    e = launch_router_logits(x, Ti, d, E, weights->w_router, weights->b_router, w.logits, s);
+    if (e == cudaSuccess) e = launch_topk_gates(w.logits, Ti, E, k, shape->renormalize, w.ids, w.w, s);
+  }
+  if (e == cudaSuccess)
+    e = launch_permute(w.ids, Ti * k, E, w.offsets, w.sorted_rows, w.inv, w.blk_prefix, w.perm_scratch, w.st, s);
+  const FfnArgs a = ffn_args(x, T, shape, weights, w.offsets, w.sorted_rows, w.blk_prefix, w, w.y_rows);
+  // the grouped-GEMM path keeps y in fp16 (half the bytes through HBM twice)
+  __half* y16 = uses_grouped_gemm(a) ? reinterpret_cast<__half*>(w.y_rows) : nullptr;
+  if (e == cudaSuccess) e = run_expert_ffn(a, w, y16, s);
+  if (e == cudaSuccess) {
+    if (y16) e = launch_combine_f16(y16, w.inv, w.w, residual, Ti, d, k, out, out_f32, s);
+    else e = launch_combine(w.y_rows, w.inv, w.w, residual, Ti, d, k, out, out_f32, s);
+  }
+  if (e == cudaSuccess && topk_ids_out)
+    e = cudaMemcpyAsync(topk_ids_out, w.ids, (size_t)T * k * 4, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && topk_w_out)
+    e = cudaMemcpyAsync(topk_w_out, w.w, (size_t)T * k * 4, cudaMemcpyDeviceToDevice, s);
+  return cuda_status(e);
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -264,71 +353,17 @@ bitmoe_status_t moe_forward(const uint16_t* x, const uint16_t* residual, int64_t
                             const bitmoe_moe_weights_t* weights, const int32_t* forced_ids, const float* forced_w,
                             int32_t* topk_ids_out, float* topk_w_out, uint16_t* out, float* out_f32,
                             void* workspace, size_t workspace_bytes, void* stream) {
-  bitmoe_status_t st = check_shape(shape, T);
-  if (st != BITMOE_OK) return st;
-  if (T == 0) return BITMOE_OK;
-  if ((forced_ids == nullptr) != (forced_w == nullptr)) return BITMOE_ERR_INVALID_ARG;
-  if ((st = check_weights(weights, forced_ids == nullptr)) != BITMOE_OK) return st;
-  if (!x || !residual || !out || !aligned16(x) || !aligned16(residual) || !aligned16(out) ||
-      (out_f32 && !aligned16(out_f32)))
-    return BITMOE_ERR_INVALID_ARG;
-  if ((st = check_ws(shape, T, workspace, workspace_bytes)) != BITMOE_OK) return st;
-  const MoeWs w = moe_layout(shape, T, workspace);
-  cudaStream_t s = (cudaStream_t)stream;
-  const int Ti = (int)T, d = (int)shape->d, E = (int)shape->E, k = (int)shape->k;
-  cudaError_t e;
-  if (decode_fused_eligible(Ti, d, E, k, (int)shape->I)) {
-    DecodeLaunch L;
-    L.x = x;
-    L.resid = residual;
-    L.T = Ti;
-    L.d = d;
-    L.E = E;
-    L.k = k;
-    L.I = (int)shape->I;
-    L.renorm = shape->renormalize;
-    L.gate = weights->gate;
-    L.up = weights->up;
-    L.down = weights->down;
-    L.w_router = weights->w_router;
-    L.b_router = weights->b_router;
-    L.forced_ids = forced_ids;
-    L.forced_w = forced_w;
-    L.out = out;
-    L.out_f32 = out_f32;
-    L.ids_out = topk_ids_out;
-    L.w_out = topk_w_out;
-    L.logits = w.logits;
-    L.h_hi = w.h_hi;
-    L.h_lo = w.h_lo;
-    L.gbar = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(w.st) + 64);
-    L.st = w.st;
-    L.pdl = 1;
-    e = launch_decode_fused(L, s);
-    if (e != cudaErrorNotSupported) return cuda_status(e);
-    (void)cudaGetLastError();
-  }
-  if (forced_ids) {
-    e = launch_forced_select(forced_ids, forced_w, Ti, E, k, w.ids, w.w, w.st, s);
-  } else {
-    e = launch_router_logits(x, Ti, d, E, weights->w_router, weights->b_router, w.logits, s);
-    if (e == cudaSuccess) e = launch_topk_gates(w.logits, Ti, E, k, shape->renormalize, w.ids, w.w, s);
-  }
-  if (e == cudaSuccess)
-    e = launch_permute(w.ids, Ti * k, E, w.offsets, w.sorted_rows, w.inv, w.blk_prefix, w.perm_scratch, w.st, s);
-  const FfnArgs a = ffn_args(x, T, shape, weights, w.offsets, w.sorted_rows, w.blk_prefix, w, w.y_rows);
-  // the grouped-GEMM path keeps y in fp16 (half the bytes through HBM twice)
-  __half* y16 = uses_grouped_gemm(a) ? reinterpret_cast<__half*>(w.y_rows) : nullptr;
-  if (e == cudaSuccess) e = run_expert_ffn(a, w, y16, s);
-  if (e == cudaSuccess) {
-    if (y16) e = launch_combine_f16(y16, w.inv, w.w, residual, Ti, d, k, out, out_f32, s);
-    else e = launch_combine(w.y_rows, w.inv, w.w, residual, Ti, d, k, out, out_f32, s);
-  }
-  if (e == cudaSuccess && topk_ids_out)
-    e = cudaMemcpyAsync(topk_ids_out, w.ids, (size_t)T * k * 4, cudaMemcpyDeviceToDevice, s);
-  if (e == cudaSuccess && topk_w_out)
-    e = cudaMemcpyAsync(topk_w_out, w.w, (size_t)T * k * 4, cudaMemcpyDeviceToDevice, s);
-  return cuda_status(e);
+  return forward_impl(x, residual, T, shape, weights, forced_ids, forced_w, topk_ids_out, topk_w_out, out, out_f32,
+                      workspace, workspace_bytes, stream, 0, 0.f, nullptr);
+}
+
+bitmoe_status_t moe_forward_prenorm(const uint16_t* residual, int64_t T, const bitmoe_moe_shape_t* shape,
+                                    const bitmoe_moe_weights_t* weights, float eps, const int32_t* forced_ids,
+                                    const float* forced_w, int32_t* topk_ids_out, float* topk_w_out, uint16_t* xh_out,
+                                    uint16_t* out, float* out_f32, void* workspace, size_t workspace_bytes,
+                                    void* stream) {
+  return forward_impl(residual, residual, T, shape, weights, forced_ids, forced_w, topk_ids_out, topk_w_out, out,
+                      out_f32, workspace, workspace_bytes, stream, 1, eps, xh_out);
 }
 
 size_t lmhead_workspace_size(int64_t T, int64_t d, int64_t V) {

@@ -63,6 +63,9 @@ struct DecodeArgs {
   int nstages;
   int offA, offB, offR, offRing;  // shared-memory carve-up (bytes)
   unsigned long long* trace;       // optional [grid][kTracePoints] globaltimer stamps
+  int prenorm;                     // x holds the residual: route and run the experts on RMSNorm(x)
+  float eps;
+  uint16_t* xh_out;                // optional [T, d] copy of RMSNorm(x) (CTA 0 writes it)
 };
 
 // Phase timestamps for the optional trace buffer (thread 0 of each CTA).
@@ -224,6 +227,54 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
 
   if (warp < kDecWarps) {
     bool ok = mbar_wait(xbar, 0, p.st, 30);
+    if (p.prenorm) {  // taken by every consumer thread alike (the block has barriers)
+      // the staged rows are the residual: replace them in place by RMSNorm(x) with unit
+      // gain, reduced exactly as the standalone RMSNorm kernel does (256 threads per token,
+      // fp32 FMA chains, then eight warp partials in order), so both give the same bits;
+      // two tokens at a time
+      const int half = tid >> 8, lt = tid & 255;
+      for (int t0 = 0; t0 < T; t0 += 2) {
+        const int t = t0 + half;
+        uint16_t* xr = reinterpret_cast<uint16_t*>(regA + t * xstride);
+        float ss = 0.f;
+        if (t < T) {
+          for (int c8 = lt * 8; c8 < d; c8 += 256 * 8) {
+            const uint4 r = *reinterpret_cast<const uint4*>(xr + c8);
+            const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float a = __uint_as_float(rw[i] << 16), b = __uint_as_float(rw[i] & 0xffff0000u);
+              ss = fmaf(a, a, ss);
+              ss = fmaf(b, b, ss);
+            }
+          }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        if (lane == 0) rt.part[warp] = ss;
+        consumer_sync();
+        float tot = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) tot += rt.part[half * 8 + i];
+        const float inv = 1.0f / sqrtf(tot / (float)d + p.eps);
+        if (t < T) {
+          for (int c8 = lt * 8; c8 < d; c8 += 256 * 8) {
+            const uint4 r = *reinterpret_cast<const uint4*>(xr + c8);
+            const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+            uint32_t ob[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float a = __uint_as_float(rw[i] << 16) * inv, b = __uint_as_float(rw[i] & 0xffff0000u) * inv;
+              ob[i] = (uint32_t)float_to_bf16_bits(a) | ((uint32_t)float_to_bf16_bits(b) << 16);
+            }
+            const uint4 o = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+            *reinterpret_cast<uint4*>(xr + c8) = o;
+            if (p.xh_out && cta == 0) *reinterpret_cast<uint4*>(p.xh_out + (size_t)t * d + c8) = o;
+          }
+        }
+        consumer_sync();  // the partials are read; the normalised rows are in place
+      }
+    }
     if (routed) {
       if (nexp > 0) ok = mbar_wait(wrbar, 0, p.st, 31) && ok;
       if (!ok) *(volatile int*)fail = 1;
@@ -752,6 +803,9 @@ cudaError_t launch_decode_fused(const DecodeLaunch& L, cudaStream_t s) {
   a.offB = pl.offB;
   a.offR = pl.offR;
   a.offRing = pl.offRing;
+  a.prenorm = L.prenorm;
+  a.eps = L.eps;
+  a.xh_out = L.xh_out;
   a.trace = static_cast<unsigned long long*>(g_trace_buf);
   if (a.trace && g_trace_bytes < (size_t)G * kTracePoints * sizeof(unsigned long long)) a.trace = nullptr;
 

@@ -75,6 +75,9 @@ struct DecodeLaunch {
   unsigned* gbar;    // grid-barrier words (arrivals, epoch), arrivals 0 at launch
   DevStatus* st;
   int pdl;           // launch with programmatic dependent launch
+  int prenorm;       // x is the residual: the layer runs on RMSNorm(x) (unit gain, eps)
+  float eps;
+  uint16_t* xh_out;  // optional [T, d] copy of RMSNorm(x)
 };
 bool decode_fused_eligible(int T, int d, int E, int k, int I);
 // Optional phase-timestamp buffer for the fused decode kernel (null = off).

@@ -182,6 +182,23 @@ bitmoe_status_t moe_forward(const uint16_t* x, const uint16_t* residual, int64_t
                             int32_t* topk_ids_out, float* topk_w_out, uint16_t* out, float* out_f32,
                             void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * One pre-norm layer step of a decode stack: xh = RMSNorm(residual) with unit
+ * gain (y = x / sqrt(mean(x^2) + eps), fp32, rounded to bf16), then
+ * out = residual + MoE(xh), as moe_forward(xh, residual, ...) computes it.
+ * For T <= 8 the normalisation runs inside the fused decode kernel (no extra
+ * launch); other T normalise first into xh_out (or the workspace).  xh_out
+ * [T, d] bf16 may be NULL; out may alias residual.  Forced ids/gates as in
+ * moe_forward.  Source: "Flint 40B : Best Mid Sized LLM", transcript 03:36
+ * (per-layer normalisation in the decoder stack); the stack shape follows the
+ * pages' 49-layer decoder with attention left out.
+ */
+bitmoe_status_t moe_forward_prenorm(const uint16_t* residual, int64_t T, const bitmoe_moe_shape_t* shape,
+                                    const bitmoe_moe_weights_t* weights, float eps, const int32_t* forced_ids,
+                                    const float* forced_w, int32_t* topk_ids_out, float* topk_w_out, uint16_t* xh_out,
+                                    uint16_t* out, float* out_f32, void* workspace, size_t workspace_bytes,
+                                    void* stream);
+
 /* ------------------------------------------------------------ LM head */
 
 size_t lmhead_workspace_size(int64_t T, int64_t d, int64_t V);

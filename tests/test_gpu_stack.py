@@ -1,5 +1,5 @@
-"""GPU parity of the 49-layer decode stack (RMSNorm, MoE layer, residual in bf16;
-attention replaced by identity) followed by the int4 LM head and its arg-max.
+"""GPU parity of the 49-layer decode stack (pre-norm MoE layer steps, residual in
+bf16; attention replaced by identity) followed by the int4 LM head and its arg-max.
 
 Every checked layer is teacher-forced: the oracle starts from the GPU's own bf16
 residual at that layer's input, so the check measures that layer alone and not
@@ -49,11 +49,10 @@ def run_stack(x_bits):
     rec = []
     for l in range(N_LAYERS):
         resid_in = resid.clone()
-        bm.bitmoe_rmsnorm(resid, out=xh)
-        xh_l = xh.clone()
+        xh_l = torch.empty_like(resid)
         o32 = torch.empty((T, D), dtype=torch.float32, device="cuda")
         ids = torch.empty((T, K), dtype=torch.int32, device="cuda")
-        bm.moe_forward(xh, layers[l], ws, residual=resid, out=resid, out_f32=o32, ids_out=ids)
+        bm.moe_forward_prenorm(resid, layers[l], ws, out=resid, out_f32=o32, xh_out=xh_l, ids_out=ids)
         rec.append((resid_in, xh_l, o32, ids))
     bm.bitmoe_rmsnorm(resid, out=xh)
     _, am = bm.lmhead_int4_gemv(xh, lm, V, bm.lmhead_workspace(T, D, V), want_logits=False)
@@ -102,3 +101,22 @@ def test_stack_teacher_forced_and_lm_head(T, checked):
     assert np.array_equal(am.cpu().numpy()[sure], ref_am[sure])
     print(f"stack T={T}: {len(checked)} layers checked, near-tie layers {near}, "
           f"arg-max exempt tokens {int((~sure).sum())}")
+
+
+@pytest.mark.parametrize("T", [1, 5, 16])
+def test_prenorm_step_equals_rmsnorm_then_layer(T):
+    """moe_forward_prenorm gives the bits of bitmoe_rmsnorm followed by moe_forward."""
+    layers, _ = stack()
+    lay = layers[3]
+    x = torch_bf16_from_bits(synth.activations(SEED + 7, T, D, step=T))
+    ws = bm.moe_workspace(lay, T)
+    xh_a = torch.empty_like(x)
+    o_a = torch.empty((T, D), dtype=torch.float32, device="cuda")
+    out_a = bm.moe_forward_prenorm(x, lay, ws, out_f32=o_a, xh_out=xh_a)
+    xh_b = bm.bitmoe_rmsnorm(x)
+    o_b = torch.empty((T, D), dtype=torch.float32, device="cuda")
+    out_b, _, _, _ = bm.moe_forward(xh_b, lay, ws, residual=x, out_f32=o_b)
+    torch.cuda.synchronize()
+    assert bm.bitmoe_get_device_status(ws) == 0
+    assert torch.equal(xh_a, xh_b)
+    assert torch.equal(out_a, out_b) and torch.equal(o_a, o_b)
