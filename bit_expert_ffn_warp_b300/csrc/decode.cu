@@ -38,7 +38,7 @@ constexpr int kMaxStages = 16;
 constexpr int kDecMaxE = kConsumers;  // one logit per consumer thread
 constexpr int kDecMaxK = kDecWarps;   // the warp-maxima bound needs k <= number of warps
 constexpr int kDecMaxT = 8;
-constexpr int kTracePoints = 16;
+constexpr int kTracePoints = 32;
 
 struct DecodeArgs {
   const uint16_t* x;
@@ -62,16 +62,23 @@ struct DecodeArgs {
   DevStatus* st;
   int nstages;
   int offA, offB, offR, offRing;  // shared-memory carve-up (bytes)
-  unsigned long long* trace;       // optional [grid][kTracePoints] globaltimer stamps
+  unsigned long long* trace;       // optional [grid][kTracePoints] SM-clock stamps
   int prenorm;                     // x holds the residual: route and run the experts on RMSNorm(x)
   float eps;
   uint16_t* xh_out;                // optional [T, d] copy of RMSNorm(x) (CTA 0 writes it)
 };
 
-// Phase timestamps for the optional trace buffer (thread 0 of each CTA).
-__device__ __forceinline__ void stamp(const DecodeArgs& p, int point) {
-  if (p.trace != nullptr && threadIdx.x == 0) p.trace[blockIdx.x * kTracePoints + point] = globaltimer_ns();
+// Phase timestamps for the optional trace buffer (thread 0 of each CTA): the
+// SM's cycle counter, which resolves single phases of a few hundred cycles;
+// point 0 also records the global timer in the last slot, to line the CTAs up.
+__device__ __forceinline__ void stamp(const unsigned long long* trace, int point) {
+  if (trace != nullptr && threadIdx.x == 0) {
+    unsigned long long* row = const_cast<unsigned long long*>(trace) + blockIdx.x * kTracePoints;
+    row[point] = clock64();
+    if (point == 0) row[kTracePoints - 1] = globaltimer_ns();
+  }
 }
+__device__ __forceinline__ void stamp(const DecodeArgs& p, int point) { stamp(p.trace, point); }
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers)); }
 
@@ -90,11 +97,13 @@ __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol
 // status word resets it.)  The release-add publishes the CTA's writes (made
 // CTA-visible by the preceding bar.sync); the acquire fence after the poll
 // makes the other CTAs' writes visible.  Returns false on timeout.
-__device__ bool grid_barrier(unsigned* gb, int* fail, DevStatus* st, int where) {
+__device__ bool grid_barrier(unsigned* gb, int* fail, DevStatus* st, int where, const unsigned long long* trace,
+                             int arrived_point) {
   consumer_sync();
   if (threadIdx.x == 0) {
     unsigned old;
     asm volatile("atom.add.release.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(gb) : "memory");
+    stamp(trace, arrived_point);
     const unsigned target = (old / gridDim.x + 1u) * gridDim.x;
     unsigned v;
     asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(gb) : "memory");
@@ -132,6 +141,7 @@ __device__ __forceinline__ float scale_at(uint2 s, int gg) {
 __device__ __forceinline__ uint32_t word_at(const uint4& q, int gg) {
   return gg == 0 ? q.x : gg == 1 ? q.y : gg == 2 ? q.z : q.w;
 }
+
 
 struct Routing {  // shared-memory routing tables (identical in every CTA)
   int* ids;      // [R]   expert of row r (-1 = dropped)
@@ -218,8 +228,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
       bulk_g2s(wr_s, p.w_router + (size_t)e_lo * d, (uint32_t)nexp * d * 4u, wrbar);
     }
   }
+  // router bias of the logit this warp's lane 0 writes first (pair = warp), read now
+  const int pairs = T * nexp;
+  float bias0 = 0.f;
+  if (routed && lane == 0 && warp < kDecWarps && warp < pairs && p.b_router != nullptr)
+    bias0 = p.b_router[e_lo + warp % nexp];
   grid_dep_wait();  // the previous launch on this stream is complete and visible
   stamp(p, 1);
+  // residual of this CTA's first output tile, read now so that its latency is
+  // off the combine at the end (one value per combine thread)
+  uint16_t resid0 = 0;
+  if (tid < T * kTileRows && cta < CT) resid0 = p.resid[(size_t)(tid >> 4) * d + (size_t)cta * kTileRows + (tid & 15)];
   if (warp == kDecWarps && lane == 0) {
     mbar_arrive_expect_tx(xbar, (uint32_t)T * 2u * d);
     for (int t = 0; t < T; ++t) bulk_g2s(regA + t * xstride, p.x + (size_t)t * d, 2u * d, xbar);
@@ -227,6 +246,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
 
   if (warp < kDecWarps) {
     bool ok = mbar_wait(xbar, 0, p.st, 30);
+    stamp(p, 16);
     if (p.prenorm) {  // taken by every consumer thread alike (the block has barriers)
       // the staged rows are the residual: replace them in place by RMSNorm(x) with unit
       // gain, reduced exactly as the standalone RMSNorm kernel does (256 threads per token,
@@ -277,46 +297,47 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
     }
     if (routed) {
       if (nexp > 0) ok = mbar_wait(wrbar, 0, p.st, 31) && ok;
+      stamp(p, 17);
       if (!ok) *(volatile int*)fail = 1;
-      // (token, expert, K part) items; parts sized so that the warps are busy
-      const int pairs = T * nexp;
-      int parts = pairs > 0 ? kDecWarps / pairs : 1;
-      if (parts < 1) parts = 1;
-      while (parts > 1 && (d / parts) % 256) --parts;
-      const int span = d / parts;
-      float* psum = reinterpret_cast<float*>(regB + (size_t)nexp * d * 4);  // [pairs][parts]
-      for (int it = warp; it < pairs * parts; it += kDecWarps) {
-        const int pr = it / parts, part = it % parts;
+      // one warp per (token, expert) pair over the whole K (two accumulators),
+      // lane 0 adds the bias and stores the logit: no cross-warp reduction
+      for (int pr = warp; pr < pairs; pr += kDecWarps) {
         const int t = pr / nexp, el = pr % nexp;
         const uint16_t* xr = reinterpret_cast<const uint16_t*>(regA + t * xstride);
         const float* wrow = wr_s + (size_t)el * d;
-        float acc = 0.f;
-        for (int i = part * span + lane * 8; i < (part + 1) * span; i += 256) {
-          const uint4 xv = *reinterpret_cast<const uint4*>(xr + i);
-          const float4 w0 = *reinterpret_cast<const float4*>(wrow + i);
-          const float4 w1 = *reinterpret_cast<const float4*>(wrow + i + 4);
-          acc = fmaf(__uint_as_float(xv.x << 16), w0.x, acc);
-          acc = fmaf(__uint_as_float(xv.x & 0xffff0000u), w0.y, acc);
-          acc = fmaf(__uint_as_float(xv.y << 16), w0.z, acc);
-          acc = fmaf(__uint_as_float(xv.y & 0xffff0000u), w0.w, acc);
-          acc = fmaf(__uint_as_float(xv.z << 16), w1.x, acc);
-          acc = fmaf(__uint_as_float(xv.z & 0xffff0000u), w1.y, acc);
-          acc = fmaf(__uint_as_float(xv.w << 16), w1.z, acc);
-          acc = fmaf(__uint_as_float(xv.w & 0xffff0000u), w1.w, acc);
+        float acc0 = 0.f, acc1 = 0.f;
+        for (int i = lane * 8; i < d; i += 512) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int ii = i + h * 256;
+            if (ii < d) {
+              const uint4 xv = *reinterpret_cast<const uint4*>(xr + ii);
+              const float4 w0 = *reinterpret_cast<const float4*>(wrow + ii);
+              const float4 w1 = *reinterpret_cast<const float4*>(wrow + ii + 4);
+              float a = h ? acc1 : acc0;
+              a = fmaf(__uint_as_float(xv.x << 16), w0.x, a);
+              a = fmaf(__uint_as_float(xv.x & 0xffff0000u), w0.y, a);
+              a = fmaf(__uint_as_float(xv.y << 16), w0.z, a);
+              a = fmaf(__uint_as_float(xv.y & 0xffff0000u), w0.w, a);
+              a = fmaf(__uint_as_float(xv.z << 16), w1.x, a);
+              a = fmaf(__uint_as_float(xv.z & 0xffff0000u), w1.y, a);
+              a = fmaf(__uint_as_float(xv.w << 16), w1.z, a);
+              a = fmaf(__uint_as_float(xv.w & 0xffff0000u), w1.w, a);
+              if (h) acc1 = a; else acc0 = a;
+            }
+          }
         }
+        float acc = acc0 + acc1;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) psum[it] = acc;
+        if (lane == 0) {
+          const float b = (pr == warp) ? bias0 : (p.b_router ? p.b_router[e_lo + el] : 0.f);
+          p.logits[(size_t)t * E + e_lo + el] = acc + b;
+        }
       }
-      consumer_sync();
-      for (int pr = tid; pr < pairs; pr += kConsumers) {
-        float acc = 0.f;
-        for (int part = 0; part < parts; ++part) acc += psum[pr * parts + part];
-        const int t = pr / nexp, el = pr % nexp;
-        p.logits[(size_t)t * E + e_lo + el] = acc + (p.b_router ? p.b_router[e_lo + el] : 0.f);
-      }
+      stamp(p, 18);
       stamp(p, 2);
-      grid_barrier(p.gbar, fail, p.st, 32);  // A: every logit written
+      grid_barrier(p.gbar, fail, p.st, 32, p.trace, 22);  // A: every logit written
       stamp(p, 3);
     } else if (!ok) {
       *(volatile int*)fail = 1;
@@ -549,8 +570,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
         const float z[4] = {0.f, 0.f, 0.f, 0.f};
         float dg[4], du[4];
         mma_bf16(dg, A[0], xb.x, xb.y, z);
-        mma_bf16(dg, A[1], xb.z, xb.w, dg);
         mma_bf16(du, B[0], xb.x, xb.y, z);
+        mma_bf16(dg, A[1], xb.z, xb.w, dg);
         mma_bf16(du, B[1], xb.z, xb.w, du);
         const float s_g0 = scale_at(sg0, gg), s_g1 = scale_at(sg1, gg);
         const float s_u0 = scale_at(su0, gg), s_u1 = scale_at(su1, gg);
@@ -603,7 +624,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
     if (u == u_lo) stamp(p, 15);
   }
   stamp(p, 5);
-  if (!grid_barrier(p.gbar, fail, p.st, 39)) return;  // B: every h written
+  if (!grid_barrier(p.gbar, fail, p.st, 39, p.trace, 23)) return;  // B: every h written
   stamp(p, 6);
 
   // P3: down projection of this CTA's 16-column tiles, then the combine
@@ -625,12 +646,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
       h_loaded = true;
       stamp(p, 13);
     }
-    for (int a0 = 0; a0 < U; a0 += dps) {
-      const int s = i % NS;
-      if (ok) ok = mbar_wait(&full[s], (i / NS) & 1, p.st, 41);
-      const int quarter = warp & 3;  // four warps per tile, one per quarter of the reduction
+    // W_down stages of this output tile in ring order; four warps per expert
+    // tile, a quarter of the reduction each.  A warp releases a stage as soon
+    // as its own tiles of it are done, so warps run ahead into later stages.
+    const int nst = (U + dps - 1) / dps;
+    const int quarter = warp & 3;
+    for (int st = 0; st < nst; ++st) {
+      const int s = (i + st) % NS;
+      if (ok) ok = mbar_wait(&full[s], ((i + st) / NS) & 1, p.st, 41);
+      if (st == 0 && ct == cta) stamp(p, 19);
       for (int j = warp >> 2; j < dps; j += kDecWarps / 4) {
-        const int a = a0 + j;
+        const int a = st * dps + j;
         if (a >= U) break;
         const unsigned char* tw = ring + (size_t)s * tbd + (size_t)j * tbi;
         const int na = rt.act_off[a + 1] - rt.act_off[a];
@@ -654,23 +680,24 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
             uint32_t A[2][4];
             const uint32_t w0 = word_at(q0, gg), w1 = word_at(q1, gg);
 #pragma unroll
-            for (int st = 0; st < 2; ++st) {
-              A[st][0] = nib_pair_f16(w0, 2 * st);
-              A[st][1] = nib_pair_f16(w1, 2 * st);
-              A[st][2] = nib_pair_f16(w0, 2 * st + 1);
-              A[st][3] = nib_pair_f16(w1, 2 * st + 1);
+            for (int sp = 0; sp < 2; ++sp) {
+              A[sp][0] = nib_pair_f16(w0, 2 * sp);
+              A[sp][1] = nib_pair_f16(w1, 2 * sp);
+              A[sp][2] = nib_pair_f16(w0, 2 * sp + 1);
+              A[sp][3] = nib_pair_f16(w1, 2 * sp + 1);
             }
+            // h = hi + lo: two independent chains of two MMAs, summed afterwards
             const float z[4] = {0.f, 0.f, 0.f, 0.f};
-            float dd[4];
-            mma_f16(dd, A[0], bh.x, bh.y, z);
-            mma_f16(dd, A[0], bl.x, bl.y, dd);
-            mma_f16(dd, A[1], bh.z, bh.w, dd);
-            mma_f16(dd, A[1], bl.z, bl.w, dd);
+            float dh[4], dl[4];
+            mma_f16(dh, A[0], bh.x, bh.y, z);
+            mma_f16(dl, A[0], bl.x, bl.y, z);
+            mma_f16(dh, A[1], bh.z, bh.w, dh);
+            mma_f16(dl, A[1], bl.z, bl.w, dl);
             const float sc0 = scale_at(s0, gg), sc1 = scale_at(s1, gg);
-            acc[0] = fmaf(sc0, dd[0], acc[0]);
-            acc[1] = fmaf(sc0, dd[1], acc[1]);
-            acc[2] = fmaf(sc1, dd[2], acc[2]);
-            acc[3] = fmaf(sc1, dd[3], acc[3]);
+            acc[0] = fmaf(sc0, dh[0] + dl[0], acc[0]);
+            acc[1] = fmaf(sc0, dh[1] + dl[1], acc[1]);
+            acc[2] = fmaf(sc1, dh[2] + dl[2], acc[2]);
+            acc[3] = fmaf(sc1, dh[3] + dl[3], acc[3]);
           }
         }
         // D rows g, g+8 (output columns) x tokens 2c, 2c+1 -> this quarter's partial
@@ -684,8 +711,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
       }
       __syncwarp();
       if (lane == 0) mbar_arrive1(&empty[s]);
-      ++i;
+      if (st == 0 && ct == cta) stamp(p, 20);
     }
+    i += nst;
     if (!ok) *(volatile int*)fail = 1;
     consumer_sync();
     stamp(p, 14);
@@ -703,7 +731,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
         }
       }
       const size_t o = (size_t)t * d + (size_t)ct * kTileRows + col;
-      const float v = bf16_bits_to_float(p.resid[o]) + acc;
+      const float v = bf16_bits_to_float(ct == cta ? resid0 : p.resid[o]) + acc;
       if (*(volatile int*)fail == 0) {
         if (p.out_f32) p.out_f32[o] = v;
         p.out[o] = float_to_bf16_bits(v);

@@ -87,14 +87,17 @@ int bitmoe_last_cuda_error(void);
 const char* bitmoe_version(void);
 
 /* Tracing (off by default): while a device buffer is set, every fused decode
- * launch writes 16 globaltimer stamps (ns) per CTA into it, as
- * uint64 [gridDim][16]: 0 start, 1 after the grid-dependency wait, 2 logits
- * done, 3 after barrier A, 4 routing done, 5 gate/up done, 6 after barrier B,
- * 7 end; 8 first gate/up unit computed, 9 second unit's tiles landed,
- * 10 grouping ranks done, 11 routing tables done, 12 first gate/up tiles
- * landed, 13 h staged, 14 down projection done, 15 first unit's h stored
- * (0 = not reached).
- * The buffer must hold gridDim (= SM count) * 128 bytes, else tracing is skipped.
+ * launch writes 32 stamps per CTA into it, as uint64 [gridDim][32]: slots
+ * 0..30 hold the SM's cycle counter (clock64) at 0 start, 1 after the
+ * grid-dependency wait, 2 logits done, 3 after barrier A, 4 routing done,
+ * 5 gate/up done, 6 after barrier B, 7 end; 8 first gate/up unit computed,
+ * 9 second unit's tiles landed, 10 grouping ranks done, 11 routing tables
+ * done, 12 first gate/up tiles landed, 13 h staged, 14 down projection done,
+ * 15 first unit's h stored, 16 x landed, 17 router rows landed, 18 router dot
+ * products done, 19 first W_down stage landed, 20 first W_down stage done,
+ * 22 / 23 barrier A / B arrival counted; slot 31 holds the global timer (ns)
+ * at point 0 (0 = not reached).
+ * The buffer must hold gridDim (= SM count) * 256 bytes, else tracing is skipped.
  * Pass NULL, 0 to turn it off.  Process-wide; not for concurrent callers. */
 bitmoe_status_t bitmoe_set_trace_buffer(void* device_buf, size_t bytes);
 
@@ -117,7 +120,11 @@ bitmoe_status_t bitmoe_get_device_status(void* workspace, int clear, int32_t* st
 
 /* ------------------------------------------------------------ MoE layer */
 
-/* Workspace bytes for any MoE call below on T tokens of this shape. */
+/* Workspace bytes for any MoE call below on T tokens of this shape.  A
+ * workspace must be zero-filled before its first use (it holds the device
+ * status word and the fused decode kernel's grid-barrier counter, which
+ * carry state from one call to the next); after that, pass it unchanged to
+ * every call of this shape, on one stream. */
 size_t moe_workspace_size(const bitmoe_moe_shape_t* shape, int64_t T);
 
 /*
