@@ -168,6 +168,27 @@ __device__ __forceinline__ uint32_t nib_pair_f16(uint32_t w, int p) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// All four fp16 pairs of a word, p = 0..3, with one shift instead of three:
+// an odd pair (nibbles at bits 4..7 of each half) is read in place as
+// 1024 + 16 (q + 8), which fits fp16's 10-bit mantissa, and one fused
+// multiply-add by 1/16 minus 72 leaves q (every step exact).  bf16 has only 7
+// mantissa bits, so it keeps the shifted form of nib_pair_bf16.
+__device__ __forceinline__ void nib_pairs4_f16(uint32_t w, uint32_t (&o)[4]) {
+  const __half2 off = __floats2half2_rn(1032.0f, 1032.0f);
+  const __half2 sixteenth = __floats2half2_rn(0.0625f, 0.0625f);
+  const __half2 off_hi = __floats2half2_rn(-72.0f, -72.0f);
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    const uint32_t v = b ? (w >> 8) : w;
+    uint32_t te = (v & 0x000F000Fu) ^ 0x64086408u;  // 1032 + q
+    uint32_t to = (v & 0x00F000F0u) ^ 0x64806480u;  // 1024 + 16 (q + 8)
+    __half2 he = __hsub2(*reinterpret_cast<__half2*>(&te), off);
+    __half2 ho = __hfma2(*reinterpret_cast<__half2*>(&to), sixteenth, off_hi);
+    o[2 * b] = *reinterpret_cast<uint32_t*>(&he);
+    o[2 * b + 1] = *reinterpret_cast<uint32_t*>(&ho);
+  }
+}
+
 // ---------------------------------------------------------------- misc
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }

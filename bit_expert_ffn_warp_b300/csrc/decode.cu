@@ -677,14 +677,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
               bh = *reinterpret_cast<const uint4*>(hhi + (size_t)(p0 + g) * hstride + col * 2);
               bl = *reinterpret_cast<const uint4*>(hlo + (size_t)(p0 + g) * hstride + col * 2);
             }
-            uint32_t A[2][4];
-            const uint32_t w0 = word_at(q0, gg), w1 = word_at(q1, gg);
+            uint32_t A[2][4], p0[4], p1[4];
+            nib_pairs4_f16(word_at(q0, gg), p0);
+            nib_pairs4_f16(word_at(q1, gg), p1);
 #pragma unroll
             for (int sp = 0; sp < 2; ++sp) {
-              A[sp][0] = nib_pair_f16(w0, 2 * sp);
-              A[sp][1] = nib_pair_f16(w1, 2 * sp);
-              A[sp][2] = nib_pair_f16(w0, 2 * sp + 1);
-              A[sp][3] = nib_pair_f16(w1, 2 * sp + 1);
+              A[sp][0] = p0[2 * sp];
+              A[sp][1] = p1[2 * sp];
+              A[sp][2] = p0[2 * sp + 1];
+              A[sp][3] = p1[2 * sp + 1];
             }
             // h = hi + lo: two independent chains of two MMAs, summed afterwards
             const float z[4] = {0.f, 0.f, 0.f, 0.f};

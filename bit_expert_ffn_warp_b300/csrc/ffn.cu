@@ -40,12 +40,15 @@ __device__ __forceinline__ void frag_bf16(uint32_t w0, uint32_t w1, uint32_t (&a
 }
 
 __device__ __forceinline__ void frag_f16(uint32_t w0, uint32_t w1, uint32_t (&a)[2][4]) {
+  uint32_t p0[4], p1[4];
+  nib_pairs4_f16(w0, p0);
+  nib_pairs4_f16(w1, p1);
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
-    a[s][0] = nib_pair_f16(w0, 2 * s);
-    a[s][1] = nib_pair_f16(w1, 2 * s);
-    a[s][2] = nib_pair_f16(w0, 2 * s + 1);
-    a[s][3] = nib_pair_f16(w1, 2 * s + 1);
+    a[s][0] = p0[2 * s];
+    a[s][1] = p1[2 * s];
+    a[s][2] = p0[2 * s + 1];
+    a[s][3] = p1[2 * s + 1];
   }
 }
 

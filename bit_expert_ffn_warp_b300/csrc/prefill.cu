@@ -198,11 +198,11 @@ __device__ __forceinline__ const uint8_t* subtile_base(const PrefillArgs& p, con
 
 // Dequantise the 8 int4 values of one packed word times scale s into 16 bytes of fp16.
 __device__ __forceinline__ uint4 dequant_word_f16(uint32_t w, __half2 s2) {
-  uint32_t o[4];
+  uint32_t q[4], o[4];
+  nib_pairs4_f16(w, q);
 #pragma unroll
   for (int pr = 0; pr < 4; ++pr) {
-    const uint32_t q = nib_pair_f16(w, pr);
-    __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&q), s2);
+    __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&q[pr]), s2);
     o[pr] = *reinterpret_cast<uint32_t*>(&v);
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
