@@ -56,8 +56,8 @@ def _lib():
             "oracle_permute": (ctypes.c_int, [P, I64, I64, I64, P, P, P]),
             "oracle_expert_ffn": (ctypes.c_int, [P, I64, I64, I64, I64, I64, I64, P, P, P, P, P, P, P, P, P]),
             "oracle_combine": (ctypes.c_int, [P, P, P, I64, I64, I64, P]),
-            "oracle_moe_forward": (ctypes.c_int, [P, P, I64, I64, I64, I64, I64, I64, ctypes.c_int, P, P,
-                                                  P, P, P, P, P, P, P, P, P, P, P, P]),
+            "oracle_moe_forward": (ctypes.c_int, [P, P, I64, I64, I64, I64, I64, I64, I64, ctypes.c_int, P,
+                                                  P, P, P, P, P, P, P, P, P, P, P, P, P]),
             "oracle_rmsnorm": (ctypes.c_int, [P, I64, I64, ctypes.c_double, P]),
             "oracle_lmhead": (ctypes.c_int, [P, I64, I64, I64, I64, P, P, P, P, P]),
             "oracle_num_threads": (ctypes.c_int, []),
@@ -216,13 +216,18 @@ def combine(y, w, resid):
     return out
 
 
-def moe_forward(x, layer, k, resid=None, group=32, renorm=True, forced_ids=None, forced_w=None):
-    """One MoE layer. Returns dict(out fp64 [T,d], ids, w, gap)."""
+def moe_forward(x, layer, k, resid=None, group=32, renorm=True, forced_ids=None, forced_w=None, n_shared=0):
+    """One MoE layer. Returns dict(out fp64 [T,d], ids, w, gap).
+
+    n_shared = 1: the banks hold E + 1 experts, the last being the shared
+    expert that every token uses with weight 1 after its k routed ones; ids
+    and w (and forced_ids / forced_w) then have k + 1 columns.
+    """
     x = _c(x, np.uint16)
     resid = x if resid is None else _c(resid, np.uint16)
     T, d = x.shape
     gq = layer["gate_q"]
-    E, I = gq.shape[0], gq.shape[1]
+    E, I = gq.shape[0] - n_shared, gq.shape[1]
     args = [_c(layer[n], np.uint8 if n.endswith("_q") else np.uint16)
             for n in ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")]
     Wr = _c(layer.get("w_router"), np.float32)
@@ -231,11 +236,11 @@ def moe_forward(x, layer, k, resid=None, group=32, renorm=True, forced_ids=None,
         raise ValueError("moe_forward: router weights are needed unless the selection is forced")
     fi = _c(forced_ids, np.int32)
     fw = _c(forced_w, np.float64)
-    ids = np.empty((T, k), np.int32)
-    w = np.empty((T, k), np.float64)
+    ids = np.empty((T, k + n_shared), np.int32)
+    w = np.empty((T, k + n_shared), np.float64)
     gap = np.empty(T, np.float64)
     out = np.empty((T, d), np.float64)
-    _check(_lib().oracle_moe_forward(_p(x), _p(resid), T, d, E, k, I, group, int(renorm), _p(Wr), _p(b),
+    _check(_lib().oracle_moe_forward(_p(x), _p(resid), T, d, E, k, n_shared, I, group, int(renorm), _p(Wr), _p(b),
                                      *[_p(a) for a in args], _p(fi), _p(fw), _p(ids), _p(w), _p(gap), _p(out)),
            "moe_forward")
     return {"out": out, "ids": ids, "w": w, "gap": gap}

@@ -312,21 +312,30 @@ int oracle_combine(const double* y, const double* w, const uint16_t* resid, int6
 
 /*
  * Whole layer: route (or take forced ids / gates), expert FFNs, combine.
- * forced_ids / forced_w may be NULL (then both must be NULL).  ids_out, w_out,
- * gap_out may be NULL.  out [T, d] fp64.
+ * With n_shared = 1 the banks hold E + 1 experts and the last one is the
+ * shared expert, which every token uses with gate weight 1 besides its k
+ * routed experts (the router, Wr [E, d] and b [E], scores only the routed
+ * ones): each token then has k + 1 rows, the shared one last
+ * ("Flint 40B : Best Mid Sized LLM", transcript 02:35).
+ * forced_ids / forced_w ([T, k + n_shared]) may be NULL (then both must be
+ * NULL).  ids_out, w_out ([T, k + n_shared]), gap_out may be NULL.  out [T, d].
  */
 int oracle_moe_forward(const uint16_t* x, const uint16_t* resid, int64_t T, int64_t d, int64_t E, int64_t k,
-                       int64_t I, int64_t group, int renorm, const float* Wr, const float* b, const uint8_t* gq,
-                       const uint16_t* gs, const uint8_t* uq, const uint16_t* us, const uint8_t* dq,
-                       const uint16_t* ds, const int32_t* forced_ids, const double* forced_w, int32_t* ids_out,
-                       double* w_out, double* gap_out, double* out) {
+                       int64_t n_shared, int64_t I, int64_t group, int renorm, const float* Wr, const float* b,
+                       const uint8_t* gq, const uint16_t* gs, const uint8_t* uq, const uint16_t* us,
+                       const uint8_t* dq, const uint16_t* ds, const int32_t* forced_ids, const double* forced_w,
+                       int32_t* ids_out, double* w_out, double* gap_out, double* out) {
   if ((forced_ids == NULL) != (forced_w == NULL)) return ORACLE_EINVAL;
-  int64_t R = T * k;
+  if (n_shared < 0 || n_shared > 1 || k <= 0) return ORACLE_EINVAL;
+  const int64_t kt = k + n_shared;  // rows per token
+  int64_t R = T * kt;
   int32_t* ids = (int32_t*)malloc(sizeof(int32_t) * (size_t)(R + 1));
   double* w = (double*)malloc(sizeof(double) * (size_t)(R + 1));
   double* y = (double*)malloc(sizeof(double) * (size_t)(R * d + 1));
+  int32_t* rids = (int32_t*)malloc(sizeof(int32_t) * (size_t)(T * k + 1));
+  double* rw = (double*)malloc(sizeof(double) * (size_t)(T * k + 1));
   int rc = ORACLE_EINVAL;
-  if (ids && w && y) {
+  if (ids && w && y && rids && rw) {
     if (forced_ids) {
       memcpy(ids, forced_ids, sizeof(int32_t) * (size_t)R);
       memcpy(w, forced_w, sizeof(double) * (size_t)R);
@@ -334,16 +343,28 @@ int oracle_moe_forward(const uint16_t* x, const uint16_t* resid, int64_t T, int6
       if (gap_out)
         for (int64_t t = 0; t < T; ++t) gap_out[t] = NAN;
     } else {
-      rc = oracle_route(x, T, d, E, k, Wr, b, renorm, ids, w, NULL, gap_out);
+      rc = oracle_route(x, T, d, E, k, Wr, b, renorm, rids, rw, NULL, gap_out);
+      for (int64_t t = 0; !rc && t < T; ++t) {
+        for (int64_t j = 0; j < k; ++j) {
+          ids[t * kt + j] = rids[t * k + j];
+          w[t * kt + j] = rw[t * k + j];
+        }
+        if (n_shared) {  // the shared expert: bank entry E, weight 1
+          ids[t * kt + k] = (int32_t)E;
+          w[t * kt + k] = 1.0;
+        }
+      }
     }
-    if (!rc) rc = oracle_expert_ffn(x, T, d, I, E, k, group, gq, gs, uq, us, dq, ds, ids, y, NULL);
-    if (!rc) rc = oracle_combine(y, w, resid, T, d, k, out);
+    if (!rc) rc = oracle_expert_ffn(x, T, d, I, E + n_shared, kt, group, gq, gs, uq, us, dq, ds, ids, y, NULL);
+    if (!rc) rc = oracle_combine(y, w, resid, T, d, kt, out);
     if (!rc && ids_out) memcpy(ids_out, ids, sizeof(int32_t) * (size_t)R);
     if (!rc && w_out) memcpy(w_out, w, sizeof(double) * (size_t)R);
   }
   free(ids);
   free(w);
   free(y);
+  free(rids);
+  free(rw);
   return rc;
 }
 

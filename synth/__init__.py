@@ -191,6 +191,17 @@ def moe_layer(seed: int, d: int, E: int, I: int, group: int = 32, layer: int = 0
     }
 
 
+def moe_layer_shared(seed: int, d: int, E: int, I: int, group: int = 32, layer: int = 0,
+                     bias: str = "normal") -> dict:
+    """A layer with E routed experts plus one shared expert: the banks hold E + 1
+    experts (the last is the shared one; the first E equal those of
+    moe_layer(seed, d, E, I)), the router scores the E routed experts only."""
+    t = moe_layer(seed, d, E + 1, I, group, layer, bias)
+    t["w_router"] = router_weight(seed, E, d, layer)
+    t["b_router"] = router_bias(seed, E, bias, layer)
+    return t
+
+
 def lm_head(seed: int, V: int, d: int, group: int = 32, rows: tuple[int, int] | None = None):
     """LM-head bank q [V, d/2], s [V, d/32] (or rows [r0, r1) of it)."""
     r0, r1 = rows if rows is not None else (0, V)

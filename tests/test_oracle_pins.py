@@ -284,6 +284,36 @@ def test_one_hot_gate_selects_one_expert_and_down_scale_is_linear():
     assert not np.allclose(y3, y)
 
 
+def test_shared_expert_adds_its_dense_swiglu_ffn_with_weight_one():
+    """Top-k routed experts plus one always-on shared expert ("Flint 40B : Best Mid
+    Sized LLM", transcript 02:35): the routing of the E routed experts is that of
+    the layer without the shared expert, and the output differs from that
+    layer's by the shared expert's dense SwiGLU FFN (numpy on independently
+    dequantised weights), added with weight 1."""
+    d, E, I, T, k = 128, 6, 64, 5, 2
+    lay = synth.moe_layer_shared(9, d, E, I, bias="normal")
+    assert lay["gate_q"].shape[0] == E + 1 and lay["w_router"].shape[0] == E
+    x = synth.activations(9, T, d)
+    res = oracle.moe_forward(x, lay, k, n_shared=1)
+    routed = {n: (v[:E] if n.endswith(("_q", "_s")) else v) for n, v in lay.items()}
+    base = oracle.moe_forward(x, routed, k)
+    assert res["ids"].shape == (T, k + 1)
+    assert np.array_equal(res["ids"][:, :k], base["ids"]) and np.all(res["ids"][:, k] == E)
+    assert np.array_equal(res["w"][:, :k], base["w"]) and np.all(res["w"][:, k] == 1.0)
+    Wg, Wu, Wd = (np_dequant(lay[n + "_q"][E], lay[n + "_s"][E]) for n in ("gate", "up", "down"))
+    xv = bf16_to_np(x)
+    dense = (silu(xv @ Wg.T) * (xv @ Wu.T)) @ Wd.T
+    assert np.allclose(res["out"] - base["out"], dense, rtol=1e-11, atol=1e-12)
+    # feeding the same selection reproduces the routed result exactly
+    fed = oracle.moe_forward(x, lay, k, n_shared=1, forced_ids=res["ids"], forced_w=res["w"])
+    assert np.array_equal(fed["out"], res["out"])
+    # the shared expert's weight is 1 whatever the routed gates: halving every routed gate
+    # halves the routed part only
+    half = oracle.moe_forward(x, lay, k, n_shared=1, forced_ids=res["ids"],
+                              forced_w=np.concatenate([res["w"][:, :k] / 2, res["w"][:, k:]], axis=1))
+    assert np.allclose(half["out"] - dense, bf16_to_np(x) + (base["out"] - bf16_to_np(x)) / 2, rtol=1e-11, atol=1e-12)
+
+
 def test_expert_ffn_matches_numpy_per_row():
     d, E, I, T, k = 128, 6, 64, 4, 3
     lay = synth.moe_layer(8, d, E, I, bias="normal")
