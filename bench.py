@@ -37,6 +37,7 @@ D, E, K_TOP, I_FF, V = 2048, 256, 8, 512, 131072
 EXPERT_BYTES = 3 * I_FF * D * 9 // 16          # int4 + fp16 group scales of one expert (gate, up, down)
 ROUTER_BYTES = E * D * 4 + E * 4               # fp32 router weight + bias
 LM_BYTES = V * D * 9 // 16
+K_SHARED = 6                                   # routed experts per token beside the shared expert
 
 
 def parse():
@@ -45,7 +46,8 @@ def parse():
     p.add_argument("--steps", type=int, default=10000)
     p.add_argument("--warmup", type=int, default=256)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--workload", default="decode", choices=["decode", "batch", "prefill", "stack"])
+    p.add_argument("--workload", default="decode", choices=["decode", "batch", "prefill", "stack", "shared"],
+                   help="shared: batch-1 decode with the pages' routing, top-6 of 256 plus one shared expert")
     p.add_argument("--T", type=int, default=None, help="tokens per step (batch / prefill / stack)")
     p.add_argument("--copies", type=int, default=64, help="independent layer copies cycled per step")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -202,15 +204,17 @@ def job_throughput(units, ms, world):
 # ---------------------------------------------------------------- device weights
 
 
-def make_device_layers(n_layers, seed, bias, device="cuda"):
-    """n independently seeded layers, drawn on the device and packed."""
+def make_device_layers(n_layers, seed, bias, device="cuda", k=K_TOP, n_shared=0):
+    """n independently seeded layers, drawn on the device and packed (with
+    n_shared = 1 the banks hold E + 1 experts, the last one shared)."""
     import torch
 
     import bit_expert_ffn_warp_b300 as bm
     import synth
     layers = []
-    qbuf = torch.empty(E * I_FF * D // 2, dtype=torch.uint8, device=device)
-    sbuf = torch.empty(E * I_FF * D // 32, dtype=torch.float16, device=device)
+    Et = E + n_shared
+    qbuf = torch.empty(Et * I_FF * D // 2, dtype=torch.uint8, device=device)
+    sbuf = torch.empty(Et * I_FF * D // 32, dtype=torch.float16, device=device)
     for l in range(n_layers):
         banks = {}
         for name, (rows, K) in {"gate": (I_FF, D), "up": (I_FF, D), "down": (D, I_FF)}.items():
@@ -218,11 +222,11 @@ def make_device_layers(n_layers, seed, bias, device="cuda"):
             ks = synth.stream_key(seed, synth.TAG[name + "_s"], l)
             synth.device_fill_int4(qbuf.data_ptr(), qbuf.numel(), kq)
             synth.device_fill_scales(sbuf.data_ptr(), sbuf.numel(), ks)
-            banks[name] = bm.bitmoe_pack_int4(qbuf.view(E, rows, K // 2), sbuf.view(E, rows, K // 32))
+            banks[name] = bm.bitmoe_pack_int4(qbuf.view(Et, rows, K // 2), sbuf.view(Et, rows, K // 32))
         wr = torch.from_numpy(synth.router_weight(seed, E, D, l)).to(device)
         br = torch.from_numpy(synth.router_bias(seed, E, bias, l)).to(device)
-        layers.append(bm.MoeLayer(d=D, E=E, k=K_TOP, I=I_FF, gate=banks["gate"], up=banks["up"],
-                                  down=banks["down"], w_router=wr, b_router=br))
+        layers.append(bm.MoeLayer(d=D, E=E, k=k, I=I_FF, gate=banks["gate"], up=banks["up"],
+                                  down=banks["down"], w_router=wr, b_router=br, n_shared=n_shared))
     torch.cuda.synchronize()
     return layers
 
@@ -234,21 +238,24 @@ def cpu_oracle_sample(workload, T, seconds, seed=0):
     """Time the fp64 oracle on a bounded sample of the workload; returns dict."""
     import oracle
     import synth
-    bias = "normal" if workload == "decode" else "zipf"
-    tensors = synth.moe_layer(seed, D, E, I_FF, bias=bias, layer=0)
+    one = workload in ("decode", "shared")
+    bias = "normal" if one else "zipf"
+    shared = workload == "shared"
+    k = K_SHARED if shared else K_TOP
+    tensors = (synth.moe_layer_shared if shared else synth.moe_layer)(seed, D, E, I_FF, bias=bias, layer=0)
     cores = oracle.num_threads()
     done, t0, step = 0, time.perf_counter(), 0
     # decode: one token per call (batch 1, as the workload), until the time budget is spent
-    per_call = 1 if workload == "decode" else max(1, min(T or 1, 64))
+    per_call = 1 if one else max(1, min(T or 1, 64))
     while time.perf_counter() - t0 < seconds:
         x = synth.activations(seed, per_call, D, step=step)
-        oracle.moe_forward(x, tensors, K_TOP)
+        oracle.moe_forward(x, tensors, k, n_shared=int(shared))
         done += per_call
         step += 1
     el = time.perf_counter() - t0
     return {"value": done / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"{done} tokens in {step} calls of T={per_call} on layer copy 0 ({el:.1f} s, fp64, "
-                      f"OpenMP over the {per_call * K_TOP} routed rows of each call)"}
+                      f"OpenMP over the {per_call * (k + int(shared))} rows of each call)"}
 
 
 # ---------------------------------------------------------------- our decode workload
@@ -260,10 +267,12 @@ def bench_decode(args, world, rank):
     import bit_expert_ffn_warp_b300 as bm
     import synth
 
-    T = 1 if args.workload == "decode" else (args.T or 8)
-    bias = "normal" if args.workload == "decode" else "zipf"
+    shared = args.workload == "shared"
+    T = 1 if args.workload in ("decode", "shared") else (args.T or 8)
+    bias = "normal" if args.workload in ("decode", "shared") else "zipf"
     G = args.copies
-    layers = make_device_layers(G, seed=1 + rank, bias=bias)
+    k = K_SHARED if shared else K_TOP
+    layers = make_device_layers(G, seed=1 + rank, bias=bias, k=k, n_shared=int(shared))
     ws = bm.moe_workspace(layers[0], T)
     stream = torch.cuda.current_stream()
 
@@ -274,7 +283,7 @@ def bench_decode(args, world, rank):
     xs = torch.from_numpy(xs_host.view(np.int16)).view(torch.bfloat16).cuda()
     x_slots = torch.empty((G, T, D), dtype=torch.bfloat16, device="cuda")
     out_slots = torch.empty((G, T, D), dtype=torch.bfloat16, device="cuda")
-    ids_slots = torch.empty((G, T, K_TOP), dtype=torch.int32, device="cuda")
+    ids_slots = torch.empty((G, T, layers[0].kt), dtype=torch.int32, device="cuda")
 
     def run_chunk():
         for g in range(G):
@@ -331,15 +340,16 @@ def bench_decode(args, world, rank):
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": steps,
         "warmup": n_chunks_w * G, "ms_per_step": per_step_us / 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int4xbf16->fp32", "data": "synthetic (seeded; weights drawn on device)",
-        "config": {"workload": f"moe_layer_decode_T{T}" if T > 1 else "moe_layer_decode_batch1", "T": T, "d": D,
-                   "E": E, "top_k": K_TOP, "I": I_FF, "group": 32,
+        "config": {"workload": ("moe_layer_shared_decode_batch1" if shared else
+                                f"moe_layer_decode_T{T}" if T > 1 else "moe_layer_decode_batch1"), "T": T, "d": D,
+                   "E": E, "top_k": k, "n_shared": int(shared), "I": I_FF, "group": 32,
                    "router_bias": bias, "layer_copies": G,
                    "l2": f"inputs larger than L2: {G} independently seeded layer copies "
-                         f"({G * (E * EXPERT_BYTES + ROUTER_BYTES) / 1e9:.1f} GB) cycled per step",
+                         f"({G * ((E + int(shared)) * EXPERT_BYTES + ROUTER_BYTES) / 1e9:.1f} GB) cycled per step",
                    "parallelism": f"replicas x{world}", "timing": "CUDA graph of 64 steps, events on stream"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4),
-                     "traffic": profiled_traffic("decode_layer_kernel") if T <= 4 else None,
+                     "traffic": profiled_traffic("decode_layer_kernel") if T == 1 and not shared else None,
                      "kernel": "decode_layer_kernel (the whole layer step, one launch)" if T <= 4
                      else "whole layer step", "bytes_per_step": int(step_bytes),
                      "unique_experts_per_step": uniq, "peak_source": which},
@@ -672,6 +682,8 @@ def main():
             return
         if args.workload == "decode":
             T, name, metric = 1, "moe_layer_decode_batch1", METRIC
+        elif args.workload == "shared":
+            T, name, metric = 1, "moe_layer_shared_decode_batch1", METRIC
         elif args.workload == "batch":
             T = args.T or 8
             name, metric = f"moe_layer_decode_T{T}", METRIC
@@ -694,7 +706,9 @@ def main():
         res = {"metric": metric, "impl": "reference", "value": round(cb["value"], 3), "unit": "tokens/s",
                "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-               "config": {"workload": name, "T": T, "d": D, "E": E, "top_k": K_TOP, "I": I_FF},
+               "config": {"workload": name, "T": T, "d": D, "E": E,
+                          "top_k": K_SHARED if args.workload == "shared" else K_TOP,
+                          "n_shared": int(args.workload == "shared"), "I": I_FF},
                "ms_per_step": 1e3 / cb["value"] * T,
                "cpu_baseline": cb,
                "e2e": {"value": round(cb["value"], 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -705,7 +719,7 @@ def main():
 
     import torch
     world, rank, local = dist_setup(args)
-    if args.workload in ("decode", "batch"):
+    if args.workload in ("decode", "batch", "shared"):
         res = bench_decode(args, world, rank)
     elif args.workload == "prefill":
         res = bench_prefill(args, world, rank)

@@ -43,7 +43,7 @@ class BitmoeError(RuntimeError):
 
 class MoeShape(ctypes.Structure):
     _fields_ = [("d", ctypes.c_int64), ("E", ctypes.c_int64), ("k", ctypes.c_int64), ("I", ctypes.c_int64),
-                ("group", ctypes.c_int64), ("renormalize", ctypes.c_int32)]
+                ("group", ctypes.c_int64), ("renormalize", ctypes.c_int32), ("n_shared", ctypes.c_int32)]
 
 
 class MoeWeights(ctypes.Structure):
@@ -150,7 +150,12 @@ def bitmoe_pack_int4(q: torch.Tensor, scale: torch.Tensor, group: int = GROUP) -
 
 @dataclass
 class MoeLayer:
-    """Device-resident weights of one MoE layer (packed banks + fp32 router)."""
+    """Device-resident weights of one MoE layer (packed banks + fp32 router).
+
+    E routed experts, k of them per token; with n_shared = 1 the banks hold one
+    more expert (entry E), the shared expert every token uses with weight 1, and
+    the per-token arrays have kt = k + 1 entries, the shared one last.
+    """
     d: int
     E: int
     k: int
@@ -161,10 +166,21 @@ class MoeLayer:
     w_router: torch.Tensor
     b_router: torch.Tensor | None
     renormalize: bool = True
+    n_shared: int = 0
+
+    @property
+    def kt(self) -> int:
+        """Rows per token: the routed experts, then the shared one."""
+        return self.k + self.n_shared
+
+    @property
+    def Et(self) -> int:
+        """Bank entries: the routed experts, then the shared one."""
+        return self.E + self.n_shared
 
     @property
     def shape(self) -> MoeShape:
-        return MoeShape(self.d, self.E, self.k, self.I, GROUP, int(self.renormalize))
+        return MoeShape(self.d, self.E, self.k, self.I, GROUP, int(self.renormalize), int(self.n_shared))
 
     @property
     def weights(self) -> MoeWeights:
@@ -182,11 +198,14 @@ class MoeLayer:
                 t = t.view(torch.float16) if t.dtype in (torch.int16, torch.uint16) else t.to(torch.float16)
             return t.to(device=device).contiguous()
         gq, gs = dev("gate_q", torch.uint8), dev("gate_s", torch.float16)
-        E, I, dh = gq.shape
+        Et, I, dh = gq.shape
         d = dh * 2
+        E = tensors["w_router"].shape[0] if tensors.get("w_router") is not None else Et
+        if Et - E not in (0, 1):
+            raise ValueError("the banks hold the routed experts plus at most one shared expert")
         b = tensors.get("b_router")
         return cls(
-            d=d, E=E, k=k, I=I,
+            d=d, E=E, k=k, I=I, n_shared=Et - E,
             gate=bitmoe_pack_int4(gq, gs),
             up=bitmoe_pack_int4(dev("up_q", torch.uint8), dev("up_s", torch.float16)),
             down=bitmoe_pack_int4(dev("down_q", torch.uint8), dev("down_s", torch.float16)),
@@ -221,8 +240,8 @@ def bitmoe_get_device_status(workspace: torch.Tensor, clear: bool = False) -> in
 def moe_route(x, layer: MoeLayer, workspace, want_logits: bool = False):
     T = x.shape[0]
     _need(x, torch.bfloat16, (T, layer.d), "x")
-    ids = torch.empty((T, layer.k), dtype=torch.int32, device=x.device)
-    w = torch.empty((T, layer.k), dtype=torch.float32, device=x.device)
+    ids = torch.empty((T, layer.kt), dtype=torch.int32, device=x.device)
+    w = torch.empty((T, layer.kt), dtype=torch.float32, device=x.device)
     logits = torch.empty((T, layer.E), dtype=torch.float32, device=x.device) if want_logits else None
     sh = layer.shape
     _check("moe_route", _lib.moe_route(_ptr(x), T, ctypes.byref(sh), _ptr(layer.w_router), _ptr(layer.b_router),
@@ -233,11 +252,11 @@ def moe_route(x, layer: MoeLayer, workspace, want_logits: bool = False):
 
 def moe_permute(ids, layer: MoeLayer, workspace):
     T = ids.shape[0]
-    _need(ids, torch.int32, (T, layer.k), "ids")
+    _need(ids, torch.int32, (T, layer.kt), "ids")
     dev = ids.device
-    offsets = torch.empty(layer.E + 1, dtype=torch.int32, device=dev)
-    rows = torch.empty(T * layer.k, dtype=torch.int32, device=dev)
-    inv = torch.empty(T * layer.k, dtype=torch.int32, device=dev)
+    offsets = torch.empty(layer.Et + 1, dtype=torch.int32, device=dev)
+    rows = torch.empty(T * layer.kt, dtype=torch.int32, device=dev)
+    inv = torch.empty(T * layer.kt, dtype=torch.int32, device=dev)
     sh = layer.shape
     _check("moe_permute", _lib.moe_permute(_ptr(ids), T, ctypes.byref(sh), _ptr(offsets), _ptr(rows), _ptr(inv),
                                            _ptr(workspace), workspace.numel(), _stream()))
@@ -247,9 +266,9 @@ def moe_permute(ids, layer: MoeLayer, workspace):
 def moe_expert_ffn_int4(x, layer: MoeLayer, offsets, sorted_rows, workspace):
     T = x.shape[0]
     _need(x, torch.bfloat16, (T, layer.d), "x")
-    _need(offsets, torch.int32, (layer.E + 1,), "offsets")
-    _need(sorted_rows, torch.int32, (T * layer.k,), "sorted_rows")
-    y = torch.empty((T * layer.k, layer.d), dtype=torch.float32, device=x.device)
+    _need(offsets, torch.int32, (layer.Et + 1,), "offsets")
+    _need(sorted_rows, torch.int32, (T * layer.kt,), "sorted_rows")
+    y = torch.empty((T * layer.kt, layer.d), dtype=torch.float32, device=x.device)
     sh, wt = layer.shape, layer.weights
     _check("moe_expert_ffn_int4", _lib.moe_expert_ffn_int4(_ptr(x), T, ctypes.byref(sh), ctypes.byref(wt),
                                                            _ptr(offsets), _ptr(sorted_rows), _ptr(y),
@@ -276,8 +295,8 @@ def moe_forward(x, layer: MoeLayer, workspace, residual=None, forced_ids=None, f
     residual = x if residual is None else residual
     _need(residual, torch.bfloat16, (T, layer.d), "residual")
     if forced_ids is not None:
-        _need(forced_ids, torch.int32, (T, layer.k), "forced_ids")
-        _need(forced_w, torch.float32, (T, layer.k), "forced_w")
+        _need(forced_ids, torch.int32, (T, layer.kt), "forced_ids")
+        _need(forced_w, torch.float32, (T, layer.kt), "forced_w")
     out = torch.empty_like(x) if out is None else out
     sh, wt = layer.shape, layer.weights
     _check("moe_forward", _lib.moe_forward(_ptr(x), _ptr(residual), T, ctypes.byref(sh), ctypes.byref(wt),

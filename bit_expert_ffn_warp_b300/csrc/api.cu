@@ -22,6 +22,10 @@ constexpr int64_t kMaxRows = int64_t(1) << 22;  // T*k limit (int32 positions wi
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
+// Bank entries (routed + shared) and rows per token (routed + shared).
+int64_t bank_experts(const bitmoe_moe_shape_t* sh) { return sh->E + sh->n_shared; }
+int64_t rows_per_token(const bitmoe_moe_shape_t* sh) { return sh->k + sh->n_shared; }
+
 // Workspace carve-up shared by every MoE entry point.
 struct MoeWs {
   DevStatus* st;
@@ -43,7 +47,7 @@ struct MoeWs {
 };
 
 MoeWs moe_layout(const bitmoe_moe_shape_t* sh, int64_t T, void* base) {
-  const int64_t R = T * sh->k;
+  const int64_t R = T * rows_per_token(sh), Et = bank_experts(sh);
   char* p = static_cast<char*>(base);
   size_t off = 0;
   MoeWs w;
@@ -56,17 +60,17 @@ MoeWs moe_layout(const bitmoe_moe_shape_t* sh, int64_t T, void* base) {
   w.ids = reinterpret_cast<int32_t*>(take((size_t)R * 4));
   w.w = reinterpret_cast<float*>(take((size_t)R * 4));
   w.logits = reinterpret_cast<float*>(take((size_t)T * sh->E * 4));
-  w.offsets = reinterpret_cast<int32_t*>(take((size_t)(sh->E + 1) * 4));
+  w.offsets = reinterpret_cast<int32_t*>(take((size_t)(Et + 1) * 4));
   w.sorted_rows = reinterpret_cast<int32_t*>(take((size_t)R * 4));
   w.inv = reinterpret_cast<int32_t*>(take((size_t)R * 4));
-  w.blk_prefix = reinterpret_cast<int32_t*>(take((size_t)(sh->E + 1) * 4));
-  w.perm_scratch = take(permute_scratch_bytes(R, (int)sh->E));
+  w.blk_prefix = reinterpret_cast<int32_t*>(take((size_t)(Et + 1) * 4));
+  w.perm_scratch = take(permute_scratch_bytes(R, (int)Et));
   w.h_hi = reinterpret_cast<__half*>(take((size_t)R * sh->I * 2));
   w.h_lo = reinterpret_cast<__half*>(take((size_t)R * sh->I * 2));
   w.y_rows = reinterpret_cast<float*>(take((size_t)R * sh->d * 4));
   w.xs = reinterpret_cast<__half*>(take((size_t)R * sh->d * 2));
   // prefix of 128-row expert blocks [E+1], then the blocks widest first [R/128 + E]
-  w.nb_prefix = reinterpret_cast<int32_t*>(take((size_t)(sh->E + 1) * 4 + (size_t)(R / 128 + sh->E + 1) * 4));
+  w.nb_prefix = reinterpret_cast<int32_t*>(take((size_t)(Et + 1) * 4 + (size_t)(R / 128 + Et + 1) * 4));
   w.xh = reinterpret_cast<uint16_t*>(take((size_t)T * sh->d * 2));
   w.total = off;
   return w;
@@ -75,11 +79,12 @@ MoeWs moe_layout(const bitmoe_moe_shape_t* sh, int64_t T, void* base) {
 bitmoe_status_t check_shape(const bitmoe_moe_shape_t* sh, int64_t T) {
   if (sh == nullptr || T < 0) return BITMOE_ERR_INVALID_ARG;
   if (sh->d <= 0 || sh->E <= 0 || sh->k <= 0 || sh->I <= 0) return BITMOE_ERR_INVALID_ARG;
-  if (sh->k > sh->E || sh->k > kMaxK) return BITMOE_ERR_INVALID_ARG;
+  if (sh->n_shared < 0 || sh->n_shared > 1) return BITMOE_ERR_INVALID_ARG;
+  if (sh->k > sh->E || rows_per_token(sh) > kMaxK) return BITMOE_ERR_INVALID_ARG;
   if (sh->group != kGroup) return BITMOE_ERR_UNSUPPORTED;
   if (sh->d % kChunkK || sh->I % kChunkK) return BITMOE_ERR_UNSUPPORTED;
-  if (sh->E > kMaxE || sh->d > 16384 || sh->I > 16384) return BITMOE_ERR_UNSUPPORTED;
-  if (T * sh->k > kMaxRows) return BITMOE_ERR_UNSUPPORTED;
+  if (bank_experts(sh) > kMaxE || sh->d > 16384 || sh->I > 16384) return BITMOE_ERR_UNSUPPORTED;
+  if (T * rows_per_token(sh) > kMaxRows) return BITMOE_ERR_UNSUPPORTED;
   return BITMOE_OK;
 }
 
@@ -105,8 +110,8 @@ FfnArgs ffn_args(const uint16_t* x, int64_t T, const bitmoe_moe_shape_t* sh, con
   a.T = (int)T;
   a.d = (int)sh->d;
   a.I = (int)sh->I;
-  a.E = (int)sh->E;
-  a.k = (int)sh->k;
+  a.E = (int)bank_experts(sh);
+  a.k = (int)rows_per_token(sh);
   a.gate = wt->gate;
   a.up = wt->up;
   a.down = wt->down;
@@ -160,8 +165,9 @@ bitmoe_status_t forward_impl(const uint16_t* x, const uint16_t* residual, int64_
   const MoeWs w = moe_layout(shape, T, workspace);
   cudaStream_t s = (cudaStream_t)stream;
   const int Ti = (int)T, d = (int)shape->d, E = (int)shape->E, k = (int)shape->k;
+  const int ns = (int)shape->n_shared, Et = E + ns, kt = k + ns;
   cudaError_t e;
-  if (decode_fused_eligible(Ti, d, E, k, (int)shape->I)) {
+  if (decode_fused_eligible(Ti, d, E, k, (int)shape->I, ns)) {
     DecodeLaunch L;
     L.x = x;
     L.resid = residual;
@@ -171,6 +177,7 @@ bitmoe_status_t forward_impl(const uint16_t* x, const uint16_t* residual, int64_
     L.k = k;
     L.I = (int)shape->I;
     L.renorm = shape->renormalize;
+    L.n_shared = ns;
     L.gate = weights->gate;
     L.up = weights->up;
     L.down = weights->down;
@@ -202,25 +209,28 @@ bitmoe_status_t forward_impl(const uint16_t* x, const uint16_t* residual, int64_
     x = xh;
   }
   if (forced_ids) {
-    e = launch_forced_select(forced_ids, forced_w, Ti, E, k, w.ids, w.w, w.st, s);
+    e = launch_forced_select(forced_ids, forced_w, Ti, Et, kt, w.ids, w.w, w.st, s);
   } else {
     e = launch_router_logits(x, Ti, d, E, weights->w_router, weights->b_router, w.logits, s);
-    if (e == cudaSuccess) e = launch_topk_gates(w.logits, Ti, E, k, shape->renormalize, w.ids, w.w, s);
+    if (e == cudaSuccess) e = launch_topk_gates(w.logits, Ti, E, k, shape->renormalize, ns, w.ids, w.w, s);
   }
   if (e == cudaSuccess)
-    e = launch_permute(w.ids, Ti * k, E, w.offsets, w.sorted_rows, w.inv, w.blk_prefix, w.perm_scratch, w.st, s);
+    e = launch_permute(w.ids, Ti * kt, Et, w.offsets, w.sorted_rows, w.inv, w.blk_prefix, w.perm_scratch, w.st, s);
   const FfnArgs a = ffn_args(x, T, shape, weights, w.offsets, w.sorted_rows, w.blk_prefix, w, w.y_rows);
-  // the grouped-GEMM path keeps y in fp16 (half the bytes through HBM twice)
-  __half* y16 = uses_grouped_gemm(a) ? reinterpret_cast<__half*>(w.y_rows) : nullptr;
+  // the grouped-GEMM path keeps y in fp16 (half the bytes through HBM twice), except
+  // with a shared expert: its rows enter the combine with weight 1, not a gate of
+  // about 1/k, and fp16's rounding of y (half an ulp is 1/64 at |y| in [32, 64))
+  // would then reach the output undamped
+  __half* y16 = (uses_grouped_gemm(a) && ns == 0) ? reinterpret_cast<__half*>(w.y_rows) : nullptr;
   if (e == cudaSuccess) e = run_expert_ffn(a, w, y16, s);
   if (e == cudaSuccess) {
-    if (y16) e = launch_combine_f16(y16, w.inv, w.w, residual, Ti, d, k, out, out_f32, s);
-    else e = launch_combine(w.y_rows, w.inv, w.w, residual, Ti, d, k, out, out_f32, s);
+    if (y16) e = launch_combine_f16(y16, w.inv, w.w, residual, Ti, d, kt, out, out_f32, s);
+    else e = launch_combine(w.y_rows, w.inv, w.w, residual, Ti, d, kt, out, out_f32, s);
   }
   if (e == cudaSuccess && topk_ids_out)
-    e = cudaMemcpyAsync(topk_ids_out, w.ids, (size_t)T * k * 4, cudaMemcpyDeviceToDevice, s);
+    e = cudaMemcpyAsync(topk_ids_out, w.ids, (size_t)T * kt * 4, cudaMemcpyDeviceToDevice, s);
   if (e == cudaSuccess && topk_w_out)
-    e = cudaMemcpyAsync(topk_w_out, w.w, (size_t)T * k * 4, cudaMemcpyDeviceToDevice, s);
+    e = cudaMemcpyAsync(topk_w_out, w.w, (size_t)T * kt * 4, cudaMemcpyDeviceToDevice, s);
   return cuda_status(e);
 }
 
@@ -301,7 +311,8 @@ bitmoe_status_t moe_route(const uint16_t* x, int64_t T, const bitmoe_moe_shape_t
   float* logits = logits_out ? logits_out : w.logits;
   cudaError_t e = launch_router_logits(x, (int)T, (int)shape->d, (int)shape->E, w_router, b_router, logits, s);
   if (e == cudaSuccess)
-    e = launch_topk_gates(logits, (int)T, (int)shape->E, (int)shape->k, shape->renormalize, topk_ids, topk_w, s);
+    e = launch_topk_gates(logits, (int)T, (int)shape->E, (int)shape->k, shape->renormalize, (int)shape->n_shared,
+                          topk_ids, topk_w, s);
   return cuda_status(e);
 }
 
@@ -313,8 +324,9 @@ bitmoe_status_t moe_permute(const int32_t* topk_ids, int64_t T, const bitmoe_moe
   if (!expert_offsets || (T > 0 && (!topk_ids || !sorted_rows || !inv_rows))) return BITMOE_ERR_INVALID_ARG;
   if ((st = check_ws(shape, T, workspace, workspace_bytes)) != BITMOE_OK) return st;
   const MoeWs w = moe_layout(shape, T, workspace);
-  return cuda_status(launch_permute(topk_ids, (int)(T * shape->k), (int)shape->E, expert_offsets, sorted_rows,
-                                    inv_rows, w.blk_prefix, w.perm_scratch, w.st, (cudaStream_t)stream));
+  return cuda_status(launch_permute(topk_ids, (int)(T * rows_per_token(shape)), (int)bank_experts(shape),
+                                    expert_offsets, sorted_rows, inv_rows, w.blk_prefix, w.perm_scratch, w.st,
+                                    (cudaStream_t)stream));
 }
 
 bitmoe_status_t moe_expert_ffn_int4(const uint16_t* x, int64_t T, const bitmoe_moe_shape_t* shape,
@@ -330,7 +342,7 @@ bitmoe_status_t moe_expert_ffn_int4(const uint16_t* x, int64_t T, const bitmoe_m
   if ((st = check_ws(shape, T, workspace, workspace_bytes)) != BITMOE_OK) return st;
   const MoeWs w = moe_layout(shape, T, workspace);
   cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = launch_blk_prefix(expert_offsets, (int)shape->E, w.blk_prefix, s);
+  cudaError_t e = launch_blk_prefix(expert_offsets, (int)bank_experts(shape), w.blk_prefix, s);
   const FfnArgs a = ffn_args(x, T, shape, weights, expert_offsets, sorted_rows, w.blk_prefix, w, y_rows);
   if (e == cudaSuccess) e = run_expert_ffn(a, w, nullptr, s);
   return cuda_status(e);
@@ -345,8 +357,8 @@ bitmoe_status_t moe_combine(const float* y_rows, const int32_t* inv_rows, const 
   if (!y_rows || !inv_rows || !topk_w || !residual || !out) return BITMOE_ERR_INVALID_ARG;
   if (!aligned16(y_rows) || !aligned16(residual) || !aligned16(out) || (out_f32 && !aligned16(out_f32)))
     return BITMOE_ERR_INVALID_ARG;
-  return cuda_status(launch_combine(y_rows, inv_rows, topk_w, residual, (int)T, (int)shape->d, (int)shape->k, out,
-                                    out_f32, (cudaStream_t)stream));
+  return cuda_status(launch_combine(y_rows, inv_rows, topk_w, residual, (int)T, (int)shape->d,
+                                    (int)rows_per_token(shape), out, out_f32, (cudaStream_t)stream));
 }
 
 bitmoe_status_t moe_forward(const uint16_t* x, const uint16_t* residual, int64_t T, const bitmoe_moe_shape_t* shape,

@@ -43,7 +43,8 @@ constexpr int kTracePoints = 32;
 struct DecodeArgs {
   const uint16_t* x;
   const uint16_t* resid;
-  int T, d, E, k, I, renorm;
+  int T, d, E, k, I, renorm;  // E, k: routed experts, routed experts per token
+  int n_shared;               // 1: bank entry E is a shared expert, every token's last row, weight 1
   const uint8_t* gate;
   const uint8_t* up;
   const uint8_t* down;
@@ -169,7 +170,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
   unsigned char* regA = smem + p.offA;
   unsigned char* regB = smem + p.offB;
   unsigned char* ring = smem + p.offRing;
-  const int T = p.T, d = p.d, E = p.E, k = p.k, I = p.I, R = T * k;
+  // kr routed experts per token; k rows per token (the shared expert's row last)
+  const int T = p.T, d = p.d, E = p.E, kr = p.k, k = kr + p.n_shared, I = p.I, R = T * k;
   const int G = gridDim.x, cta = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int tbd = (int)tile_bytes(d), tbi = (int)tile_bytes(I);
@@ -369,7 +371,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
               const unsigned long long o = rt.wmax[w];
               rank += (o > mw) || (o == mw && w < tid);
             }
-            if (rank == k - 1) rt.misc[3] = tid;
+            if (rank == kr - 1) rt.misc[3] = tid;
           }
           consumer_sync();
           const unsigned long long tau = rt.wmax[rt.misc[3]];
@@ -389,7 +391,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
             const int nc = rt.misc[2];
             int rank = 0;
             for (int j = 0; j < nc; ++j) rank += rt.cand[j] > key;
-            if (rank < k) rt.sel[t * kDecMaxK + rank] = key;
+            if (rank < kr) rt.sel[t * kDecMaxK + rank] = key;
           }
           if (tid == 0 && !p.renorm) {
             float z = 0.f;
@@ -399,25 +401,31 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
           consumer_sync();
           if (tid == 0) rt.misc[2] = 0;
         }
-        // gates: exp(l_j - l_max) over the chosen k (renormalised) or over all E
+        // gates: exp(l_j - l_max) over the chosen kr (renormalised) or over all E;
+        // the shared expert's row (j = kr) is bank entry E with weight 1
         if (tid < R) {
           const int t = tid / k, j = tid % k;
-          const unsigned long long* sk = rt.sel + t * kDecMaxK;
-          const float vmax = key_value(sk[0]);
-          float z = 0.f;
-          if (p.renorm) {
-            for (int jj = 0; jj < k; ++jj) z += expf(key_value(sk[jj]) - vmax);
+          if (j >= kr) {
+            rt.ids[tid] = E;
+            rt.w[tid] = 1.0f;
           } else {
-            z = rt.zall[t];
+            const unsigned long long* sk = rt.sel + t * kDecMaxK;
+            const float vmax = key_value(sk[0]);
+            float z = 0.f;
+            if (p.renorm) {
+              for (int jj = 0; jj < kr; ++jj) z += expf(key_value(sk[jj]) - vmax);
+            } else {
+              z = rt.zall[t];
+            }
+            const int e = (int)(0xffffffffu - (uint32_t)(sk[j] & 0xffffffffull));
+            rt.ids[tid] = (sk[j] != 0ull && e < E) ? e : -1;
+            rt.w[tid] = expf(key_value(sk[j]) - vmax) / z;
           }
-          const int e = (int)(0xffffffffu - (uint32_t)(sk[j] & 0xffffffffull));
-          rt.ids[tid] = (sk[j] != 0ull && e < E) ? e : -1;
-          rt.w[tid] = expf(key_value(sk[j]) - vmax) / z;
         }
       } else {
         for (int r = tid; r < R; r += kConsumers) {
           int e = p.forced_ids[r];
-          if (e < 0 || e >= E) {
+          if (e < 0 || e >= E + p.n_shared) {
             if (cta == 0) record_status(p.st, kStatusCheck, 33, r);
             e = -1;
           } else if (cta == 0) {
@@ -749,10 +757,11 @@ struct DecodePlan {
   bool ok;
 };
 
-DecodePlan plan(int T, int d, int E, int k, int I, int G) {
+// k: routed experts per token; n_shared: 0 or 1 (one more row per token)
+DecodePlan plan(int T, int d, int E, int k, int I, int n_shared, int G) {
   DecodePlan pl{};
   pl.ok = false;
-  const int R = T * k;
+  const int R = T * (k + n_shared);
   if (T < 1 || T > kDecMaxT || k > kDecMaxK || E > kDecMaxE || I > d || d > 8192) return pl;
   if (tile_bytes(d) % tile_bytes(I)) return pl;
   const size_t xall = (size_t)T * (2 * d + kSmemRowPad);
@@ -792,11 +801,13 @@ int sm_count() {
 void* g_trace_buf = nullptr;
 size_t g_trace_bytes = 0;
 
-bool decode_fused_eligible(int T, int d, int E, int k, int I) { return plan(T, d, E, k, I, sm_count()).ok; }
+bool decode_fused_eligible(int T, int d, int E, int k, int I, int n_shared) {
+  return plan(T, d, E, k, I, n_shared, sm_count()).ok;
+}
 
 cudaError_t launch_decode_fused(const DecodeLaunch& L, cudaStream_t s) {
   const int G = sm_count();
-  const DecodePlan pl = plan(L.T, L.d, L.E, L.k, L.I, G);
+  const DecodePlan pl = plan(L.T, L.d, L.E, L.k, L.I, L.n_shared, G);
   if (!pl.ok) return cudaErrorNotSupported;
   static int attr_set[64] = {};
   cudaError_t err = ensure_smem_attr(decode_layer_kernel, pl.smem, attr_set);
@@ -809,6 +820,7 @@ cudaError_t launch_decode_fused(const DecodeLaunch& L, cudaStream_t s) {
   a.d = L.d;
   a.E = L.E;
   a.k = L.k;
+  a.n_shared = L.n_shared;
   a.I = L.I;
   a.renorm = L.renorm;
   a.gate = L.gate;

@@ -11,8 +11,10 @@ namespace bitmoe {
 // ---------------------------------------------------------------- routing (route.cu)
 cudaError_t launch_router_logits(const uint16_t* x, int T, int d, int E, const float* w_router,
                                  const float* b_router, float* logits, cudaStream_t s);
-cudaError_t launch_topk_gates(const float* logits, int T, int E, int k, int renorm, int32_t* ids, float* w,
-                              cudaStream_t s);
+// ids / w rows of k + n_shared entries: the k routed experts, then (n_shared = 1)
+// the shared expert, bank entry E, with weight 1.
+cudaError_t launch_topk_gates(const float* logits, int T, int E, int k, int renorm, int n_shared, int32_t* ids,
+                              float* w, cudaStream_t s);
 cudaError_t launch_forced_select(const int32_t* forced_ids, const float* forced_w, int T, int E, int k,
                                  int32_t* ids, float* w, DevStatus* st, cudaStream_t s);
 
@@ -57,13 +59,14 @@ cudaError_t launch_combine_f16(const __half* y_rows, const int32_t* inv, const f
 struct DecodeLaunch {
   const uint16_t* x;
   const uint16_t* resid;
-  int T, d, E, k, I, renorm;
+  int T, d, E, k, I, renorm;  // E, k: routed experts and routed experts per token
+  int n_shared;               // 1: bank entry E is a shared expert every token uses with weight 1
   const uint8_t* gate;
   const uint8_t* up;
   const uint8_t* down;
   const float* w_router;
   const float* b_router;
-  const int32_t* forced_ids;  // null = route
+  const int32_t* forced_ids;  // null = route; else [T, k + n_shared]
   const float* forced_w;
   uint16_t* out;
   float* out_f32;   // may be null
@@ -79,7 +82,7 @@ struct DecodeLaunch {
   float eps;
   uint16_t* xh_out;  // optional [T, d] copy of RMSNorm(x)
 };
-bool decode_fused_eligible(int T, int d, int E, int k, int I);
+bool decode_fused_eligible(int T, int d, int E, int k, int I, int n_shared);
 // Optional phase-timestamp buffer for the fused decode kernel (null = off).
 extern void* g_trace_buf;
 extern size_t g_trace_bytes;

@@ -175,10 +175,12 @@ __global__ void __launch_bounds__(256) router_mma_tiled_kernel(const uint16_t* _
 //
 // One warp per token.  Lane l holds logits e = l, l+32, ...; k rounds of a
 // warp arg-max over (value desc, index asc) pick the experts in order.  Gates:
-// exp(l_j - l_max) normalised over the chosen k (renorm) or over all E.
+// exp(l_j - l_max) normalised over the chosen k (renorm) or over all E.  With
+// a shared expert (n_shared = 1) each token's row of ids / w has k + 1
+// entries, the last naming bank entry E with weight 1.
 template <int NPER>  // logits per lane: E <= 32 * NPER
 __global__ void __launch_bounds__(256) topk_gates_kernel(const float* __restrict__ logits, int T, int E, int k,
-                                                         int renorm, int32_t* __restrict__ ids,
+                                                         int renorm, int n_shared, int32_t* __restrict__ ids,
                                                          float* __restrict__ w) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
@@ -237,9 +239,14 @@ __global__ void __launch_bounds__(256) topk_gates_kernel(const float* __restrict
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+  // rows of token t: its k routed experts, then the shared expert (bank entry E, weight 1)
+  const int kt = k + n_shared;
   if (lane < k) {
-    ids[(size_t)t * k + lane] = my_id;
-    w[(size_t)t * k + lane] = my_e / z;
+    ids[(size_t)t * kt + lane] = my_id;
+    w[(size_t)t * kt + lane] = my_e / z;
+  } else if (lane < kt) {
+    ids[(size_t)t * kt + lane] = E;
+    w[(size_t)t * kt + lane] = 1.0f;
   }
 }
 
@@ -281,13 +288,13 @@ cudaError_t launch_router_logits(const uint16_t* x, int T, int d, int E, const f
   return cudaGetLastError();
 }
 
-cudaError_t launch_topk_gates(const float* logits, int T, int E, int k, int renorm, int32_t* ids, float* w,
-                              cudaStream_t s) {
+cudaError_t launch_topk_gates(const float* logits, int T, int E, int k, int renorm, int n_shared, int32_t* ids,
+                              float* w, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   if (E <= 256)
-    topk_gates_kernel<8><<<ceil_div(T, 8), 256, 0, s>>>(logits, T, E, k, renorm, ids, w);
+    topk_gates_kernel<8><<<ceil_div(T, 8), 256, 0, s>>>(logits, T, E, k, renorm, n_shared, ids, w);
   else
-    topk_gates_kernel<kMaxE / 32><<<ceil_div(T, 8), 256, 0, s>>>(logits, T, E, k, renorm, ids, w);
+    topk_gates_kernel<kMaxE / 32><<<ceil_div(T, 8), 256, 0, s>>>(logits, T, E, k, renorm, n_shared, ids, w);
   return cudaGetLastError();
 }
 

@@ -59,14 +59,24 @@ typedef enum bitmoe_status {
   BITMOE_ERR_DEVICE_CHECK = 6  /* device status: an input failed a device-side check */
 } bitmoe_status_t;
 
-/* Shape of one MoE layer.  d: hidden size; E: routed experts; k: experts per
- * token; I: expert intermediate size; group: int4 scale group (32);
- * renormalize: 1 = gates are the chosen softmax probabilities rescaled to sum
- * 1, 0 = the raw probabilities.  Supported: d and I multiples of 128,
- * group == 32, 1 <= k <= min(E, 32), E <= 1024. */
+/* Shape of one MoE layer.  d: hidden size; E: routed experts; k: routed
+ * experts per token; I: expert intermediate size; group: int4 scale group
+ * (32); renormalize: 1 = gates are the chosen softmax probabilities rescaled
+ * to sum 1, 0 = the raw probabilities; n_shared: 0, or 1 for a shared expert
+ * that every token uses with gate weight 1 besides its k routed ones ("Flint
+ * 40B : Best Mid Sized LLM", transcript 02:35: six routed experts of 256 plus
+ * one shared expert that is always on).  The shared expert is entry E of each
+ * expert bank (the banks then hold E + 1 experts; the router still scores the
+ * E routed ones), and every per-token array below -- topk_ids, topk_w, the
+ * forced selection, the rows of the permutation -- has kt = k + n_shared
+ * entries per token, the shared one last (id E, weight 1).  Supported: d and
+ * I multiples of 128, group == 32, 1 <= k <= E, k + n_shared <= 32,
+ * E + n_shared <= 1024.  (n_shared fills what was padding: the struct's size
+ * is that of the version without it, where it read as 0 when zero-filled.) */
 typedef struct bitmoe_moe_shape {
   int64_t d, E, k, I, group;
   int32_t renormalize;
+  int32_t n_shared;
 } bitmoe_moe_shape_t;
 
 /* Packed expert banks (bitmoe_pack_int4 output, 16-byte aligned) and the
@@ -130,9 +140,11 @@ size_t moe_workspace_size(const bitmoe_moe_shape_t* shape, int64_t T);
 /*
  * Router: logits l[t,e] = sum_i x[t,i] w_router[e,i] + b_router[e] in fp32;
  * softmax over the E experts; the k largest logits (descending, equal
- * logits -> lower expert index) give topk_ids [T, k] int32; topk_w [T, k] fp32
- * are their softmax probabilities, renormalised to sum 1 if shape->renormalize.
- * x [T, d] bf16.  logits_out [T, E] fp32 may be NULL.  T = 0 is a no-op.
+ * logits -> lower expert index) give topk_ids [T, kt] int32; topk_w [T, kt]
+ * fp32 are their softmax probabilities, renormalised to sum 1 if
+ * shape->renormalize, followed (n_shared = 1) by the shared expert, id E with
+ * weight 1.  x [T, d] bf16.  logits_out [T, E] fp32 may be NULL.  T = 0 is a
+ * no-op.
  * Source: "Flint 40B : Best Mid Sized LLM", transcript 02:35 (the router picks
  * a few of 256 experts per token).
  */
@@ -141,22 +153,23 @@ bitmoe_status_t moe_route(const uint16_t* x, int64_t T, const bitmoe_moe_shape_t
                           void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * Token -> expert grouping.  Row r = t*k + j of topk_ids is placed at
+ * Token -> expert grouping.  Row r = t*kt + j of topk_ids is placed at
  * position inv_rows[r]; sorted_rows[p] = r; expert e owns positions
  * [expert_offsets[e], expert_offsets[e+1]); inside one expert the rows keep
- * ascending r (a stable counting sort, so the result is unique).
- * expert_offsets [E+1], sorted_rows [T*k], inv_rows [T*k], all int32.
- * Rows whose id is outside [0, E) are left out (inv_rows[r] = -1) and flag
- * BITMOE_ERR_DEVICE_CHECK in the device status word.
+ * ascending r (a stable counting sort, so the result is unique).  With
+ * Et = E + n_shared bank entries: expert_offsets [Et+1], sorted_rows [T*kt],
+ * inv_rows [T*kt], all int32.  Rows whose id is outside [0, Et) are left out
+ * (inv_rows[r] = -1) and flag BITMOE_ERR_DEVICE_CHECK in the device status
+ * word.
  */
 bitmoe_status_t moe_permute(const int32_t* topk_ids, int64_t T, const bitmoe_moe_shape_t* shape,
                             int32_t* expert_offsets, int32_t* sorted_rows, int32_t* inv_rows, void* workspace,
                             size_t workspace_bytes, void* stream);
 
 /*
- * Expert FFNs of every grouped row: for position p holding row r = t*k + j of
+ * Expert FFNs of every grouped row: for position p holding row r = t*kt + j of
  * expert e, a = Wg[e] x[t], u = Wu[e] x[t], h = a / (1 + exp(-a)) * u and
- * y_rows[p] = Wd[e] h (fp32 [T*k, d], sorted order), with int4 weights
+ * y_rows[p] = Wd[e] h (fp32 [T*kt, d], sorted order), with int4 weights
  * dequantised group by group.  expert_offsets / sorted_rows are moe_permute's.
  * Source: "Flint 40B : Best Mid Sized LLM", transcript 02:35 and 06:11.
  */
@@ -167,7 +180,7 @@ bitmoe_status_t moe_expert_ffn_int4(const uint16_t* x, int64_t T, const bitmoe_m
 
 /*
  * Gate-weighted combine into the residual:
- * out_f32[t,c] = residual[t,c] + sum_{j=0}^{k-1} topk_w[t,j] * y_rows[inv_rows[t*k+j], c]
+ * out_f32[t,c] = residual[t,c] + sum_{j=0}^{kt-1} topk_w[t,j] * y_rows[inv_rows[t*kt+j], c]
  * summed in ascending j in fp32; out [T, d] bf16 = round-to-nearest-even of
  * out_f32.  out_f32 may be NULL.  out may alias residual.
  */
@@ -177,8 +190,9 @@ bitmoe_status_t moe_combine(const float* y_rows, const int32_t* inv_rows, const 
 
 /*
  * The whole layer: route (unless forced), group, expert FFNs, combine.
- * residual may equal x.  forced_ids [T, k] / forced_w [T, k] (both or neither)
- * replace the router's choice; forced ids are range-checked on the device.
+ * residual may equal x.  forced_ids [T, kt] / forced_w [T, kt] (both or
+ * neither) replace the router's choice; forced ids are range-checked on the
+ * device.  topk_ids_out / topk_w_out are [T, kt].
  * topk_ids_out / topk_w_out / out_f32 may be NULL.  out may alias residual but
  * not x.  Batches of T <= 8 tokens run one fused decode kernel, other batches
  * with T*k < 512 routed rows the streaming kernels (both exact int4 x bf16 with

@@ -63,6 +63,13 @@ def test_host_side_validation_without_gpu(built):
         assert lib.moe_workspace_size(ctypes.byref(b), 1) == 0
     assert lib.moe_workspace_size(ctypes.byref(bm.MoeShape(2000, 256, 8, 512, 32, 1)), 1) == 0
     assert lib.moe_workspace_size(ctypes.byref(bm.MoeShape(2048, 256, 8, 512, 64, 1)), 1) == 0
+    # the shared expert adds a bank entry and a row per token; it fills padding of the struct
+    assert ctypes.sizeof(bm.MoeShape) == 48
+    shared = lib.moe_workspace_size(ctypes.byref(bm.MoeShape(2048, 256, 6, 512, 32, 1, 1)), 64)
+    assert shared > lib.moe_workspace_size(ctypes.byref(bm.MoeShape(2048, 256, 6, 512, 32, 1, 0)), 64)
+    assert lib.moe_workspace_size(ctypes.byref(bm.MoeShape(2048, 256, 6, 512, 32, 1, 2)), 1) == 0
+    assert lib.moe_workspace_size(ctypes.byref(bm.MoeShape(2048, 256, 32, 512, 32, 1, 1)), 1) == 0
+    assert lib.moe_workspace_size(ctypes.byref(bm.MoeShape(2048, 1024, 8, 512, 32, 1, 1)), 1) == 0
     # null pointers -> INVALID_ARG, nothing launched
     rc = lib.moe_route(None, 1, ctypes.byref(sh), None, None, None, None, None, None, 0, None)
     assert rc == 1
