@@ -221,7 +221,8 @@ def moe_forward(x, layer, k, resid=None, group=32, renorm=True, forced_ids=None,
 
     n_shared = 1: the banks hold E + 1 experts, the last being the shared
     expert that every token uses with weight 1 after its k routed ones; ids
-    and w (and forced_ids / forced_w) then have k + 1 columns.
+    and w (and forced_ids / forced_w) then have k + 1 columns.  k = 0 with
+    n_shared = 1 is a dense SwiGLU layer (no router).
     """
     x = _c(x, np.uint16)
     resid = x if resid is None else _c(resid, np.uint16)
@@ -232,7 +233,7 @@ def moe_forward(x, layer, k, resid=None, group=32, renorm=True, forced_ids=None,
             for n in ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")]
     Wr = _c(layer.get("w_router"), np.float32)
     b = _c(layer.get("b_router"), np.float32)
-    if Wr is None and forced_ids is None:
+    if Wr is None and forced_ids is None and k > 0:
         raise ValueError("moe_forward: router weights are needed unless the selection is forced")
     fi = _c(forced_ids, np.int32)
     fw = _c(forced_w, np.float64)

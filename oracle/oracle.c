@@ -316,7 +316,9 @@ int oracle_combine(const double* y, const double* w, const uint16_t* resid, int6
  * shared expert, which every token uses with gate weight 1 besides its k
  * routed experts (the router, Wr [E, d] and b [E], scores only the routed
  * ones): each token then has k + 1 rows, the shared one last
- * ("Flint 40B : Best Mid Sized LLM", transcript 02:35).
+ * ("Flint 40B : Best Mid Sized LLM", transcript 02:35).  k = 0 with
+ * n_shared = 1 is a dense SwiGLU layer (the same transcript: the stack opens
+ * with two dense layers): no router, every token through bank entry 0.
  * forced_ids / forced_w ([T, k + n_shared]) may be NULL (then both must be
  * NULL).  ids_out, w_out ([T, k + n_shared]), gap_out may be NULL.  out [T, d].
  */
@@ -326,7 +328,7 @@ int oracle_moe_forward(const uint16_t* x, const uint16_t* resid, int64_t T, int6
                        const uint8_t* dq, const uint16_t* ds, const int32_t* forced_ids, const double* forced_w,
                        int32_t* ids_out, double* w_out, double* gap_out, double* out) {
   if ((forced_ids == NULL) != (forced_w == NULL)) return ORACLE_EINVAL;
-  if (n_shared < 0 || n_shared > 1 || k <= 0) return ORACLE_EINVAL;
+  if (n_shared < 0 || n_shared > 1 || k < 0 || (k == 0 && n_shared == 0)) return ORACLE_EINVAL;
   const int64_t kt = k + n_shared;  // rows per token
   int64_t R = T * kt;
   int32_t* ids = (int32_t*)malloc(sizeof(int32_t) * (size_t)(R + 1));
@@ -343,7 +345,13 @@ int oracle_moe_forward(const uint16_t* x, const uint16_t* resid, int64_t T, int6
       if (gap_out)
         for (int64_t t = 0; t < T; ++t) gap_out[t] = NAN;
     } else {
-      rc = oracle_route(x, T, d, E, k, Wr, b, renorm, rids, rw, NULL, gap_out);
+      if (k > 0) {
+        rc = oracle_route(x, T, d, E, k, Wr, b, renorm, rids, rw, NULL, gap_out);
+      } else {  // dense layer: nothing to route
+        rc = ORACLE_OK;
+        if (gap_out)
+          for (int64_t t = 0; t < T; ++t) gap_out[t] = INFINITY;
+      }
       for (int64_t t = 0; !rc && t < T; ++t) {
         for (int64_t j = 0; j < k; ++j) {
           ids[t * kt + j] = rids[t * k + j];

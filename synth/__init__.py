@@ -202,6 +202,15 @@ def moe_layer_shared(seed: int, d: int, E: int, I: int, group: int = 32, layer: 
     return t
 
 
+def dense_layer(seed: int, d: int, I: int, group: int = 32, layer: int = 0) -> dict:
+    """A dense SwiGLU layer as a one-entry bank (no router): the gate/up/down
+    matrices of expert 0 of moe_layer(seed, d, 1, I)."""
+    t = moe_layer(seed, d, 1, I, group, layer, "zero")
+    t["w_router"] = None
+    t["b_router"] = None
+    return t
+
+
 def lm_head(seed: int, V: int, d: int, group: int = 32, rows: tuple[int, int] | None = None):
     """LM-head bank q [V, d/2], s [V, d/32] (or rows [r0, r1) of it)."""
     r0, r1 = rows if rows is not None else (0, V)

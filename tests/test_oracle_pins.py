@@ -314,6 +314,22 @@ def test_shared_expert_adds_its_dense_swiglu_ffn_with_weight_one():
     assert np.allclose(half["out"] - dense, bf16_to_np(x) + (base["out"] - bf16_to_np(x)) / 2, rtol=1e-11, atol=1e-12)
 
 
+def test_dense_layer_is_a_swiglu_ffn_of_every_token():
+    """k = 0 routed experts with the shared expert only: the stack's leading dense
+    layers ("Flint 40B : Best Mid Sized LLM", transcript 02:35) as x + FFN(x),
+    the FFN computed with numpy on independently dequantised weights."""
+    d, I, T = 128, 96, 4
+    lay = synth.dense_layer(12, d, I)
+    x = synth.activations(12, T, d)
+    res = oracle.moe_forward(x, lay, 0, n_shared=1)
+    assert np.all(res["ids"] == 0) and np.all(res["w"] == 1.0) and res["ids"].shape == (T, 1)
+    Wg, Wu, Wd = (np_dequant(lay[n + "_q"][0], lay[n + "_s"][0]) for n in ("gate", "up", "down"))
+    xv = bf16_to_np(x)
+    assert np.allclose(res["out"], xv + (silu(xv @ Wg.T) * (xv @ Wu.T)) @ Wd.T, rtol=1e-12, atol=1e-12)
+    with pytest.raises(ValueError):
+        oracle.moe_forward(x, lay, 0, n_shared=0)
+
+
 def test_expert_ffn_matches_numpy_per_row():
     d, E, I, T, k = 128, 6, 64, 4, 3
     lay = synth.moe_layer(8, d, E, I, bias="normal")
