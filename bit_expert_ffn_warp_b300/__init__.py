@@ -154,7 +154,8 @@ class MoeLayer:
 
     E routed experts, k of them per token; with n_shared = 1 the banks hold one
     more expert (entry E), the shared expert every token uses with weight 1, and
-    the per-token arrays have kt = k + 1 entries, the shared one last.
+    the per-token arrays have kt = k + 1 entries, the shared one last.  k = 0
+    (with n_shared = 1) is a dense SwiGLU layer: no router, w_router None.
     """
     d: int
     E: int
@@ -163,7 +164,7 @@ class MoeLayer:
     gate: torch.Tensor
     up: torch.Tensor
     down: torch.Tensor
-    w_router: torch.Tensor
+    w_router: torch.Tensor | None
     b_router: torch.Tensor | None
     renormalize: bool = True
     n_shared: int = 0
@@ -185,7 +186,8 @@ class MoeLayer:
     @property
     def weights(self) -> MoeWeights:
         return MoeWeights(self.gate.data_ptr(), self.up.data_ptr(), self.down.data_ptr(),
-                          self.w_router.data_ptr(), None if self.b_router is None else self.b_router.data_ptr())
+                          None if self.w_router is None else self.w_router.data_ptr(),
+                          None if self.b_router is None else self.b_router.data_ptr())
 
     @classmethod
     def from_canonical(cls, tensors: dict, k: int, device="cuda", renormalize: bool = True) -> "MoeLayer":
@@ -200,16 +202,20 @@ class MoeLayer:
         gq, gs = dev("gate_q", torch.uint8), dev("gate_s", torch.float16)
         Et, I, dh = gq.shape
         d = dh * 2
-        E = tensors["w_router"].shape[0] if tensors.get("w_router") is not None else Et
+        if k == 0:  # dense layer: the bank's one entry is the shared expert
+            E = Et - 1
+        else:
+            E = tensors["w_router"].shape[0] if tensors.get("w_router") is not None else Et
         if Et - E not in (0, 1):
             raise ValueError("the banks hold the routed experts plus at most one shared expert")
         b = tensors.get("b_router")
+        wr = tensors.get("w_router")
         return cls(
             d=d, E=E, k=k, I=I, n_shared=Et - E,
             gate=bitmoe_pack_int4(gq, gs),
             up=bitmoe_pack_int4(dev("up_q", torch.uint8), dev("up_s", torch.float16)),
             down=bitmoe_pack_int4(dev("down_q", torch.uint8), dev("down_s", torch.float16)),
-            w_router=dev("w_router", torch.float32),
+            w_router=None if wr is None else dev("w_router", torch.float32),
             b_router=None if b is None else dev("b_router", torch.float32),
             renormalize=renormalize)
 

@@ -78,7 +78,10 @@ MoeWs moe_layout(const bitmoe_moe_shape_t* sh, int64_t T, void* base) {
 
 bitmoe_status_t check_shape(const bitmoe_moe_shape_t* sh, int64_t T) {
   if (sh == nullptr || T < 0) return BITMOE_ERR_INVALID_ARG;
-  if (sh->d <= 0 || sh->E <= 0 || sh->k <= 0 || sh->I <= 0) return BITMOE_ERR_INVALID_ARG;
+  if (sh->d <= 0 || sh->E < 0 || sh->k < 0 || sh->I <= 0) return BITMOE_ERR_INVALID_ARG;
+  // k = 0 routed experts is a dense layer: the shared expert alone, no router
+  if (sh->k == 0 && sh->n_shared != 1) return BITMOE_ERR_INVALID_ARG;
+  if (sh->k > 0 && sh->E == 0) return BITMOE_ERR_INVALID_ARG;
   if (sh->n_shared < 0 || sh->n_shared > 1) return BITMOE_ERR_INVALID_ARG;
   if (sh->k > sh->E || rows_per_token(sh) > kMaxK) return BITMOE_ERR_INVALID_ARG;
   if (sh->group != kGroup) return BITMOE_ERR_UNSUPPORTED;
@@ -157,7 +160,7 @@ bitmoe_status_t forward_impl(const uint16_t* x, const uint16_t* residual, int64_
   if (st != BITMOE_OK) return st;
   if (T == 0) return BITMOE_OK;
   if ((forced_ids == nullptr) != (forced_w == nullptr)) return BITMOE_ERR_INVALID_ARG;
-  if ((st = check_weights(weights, forced_ids == nullptr)) != BITMOE_OK) return st;
+  if ((st = check_weights(weights, forced_ids == nullptr && shape->k > 0)) != BITMOE_OK) return st;
   if (!x || !residual || !out || !aligned16(x) || !aligned16(residual) || !aligned16(out) ||
       (out_f32 && !aligned16(out_f32)) || (xh_out && !aligned16(xh_out)) || !(eps >= 0.f))
     return BITMOE_ERR_INVALID_ARG;
@@ -211,7 +214,7 @@ bitmoe_status_t forward_impl(const uint16_t* x, const uint16_t* residual, int64_
   if (forced_ids) {
     e = launch_forced_select(forced_ids, forced_w, Ti, Et, kt, w.ids, w.w, w.st, s);
   } else {
-    e = launch_router_logits(x, Ti, d, E, weights->w_router, weights->b_router, w.logits, s);
+    e = k > 0 ? launch_router_logits(x, Ti, d, E, weights->w_router, weights->b_router, w.logits, s) : cudaSuccess;
     if (e == cudaSuccess) e = launch_topk_gates(w.logits, Ti, E, k, shape->renormalize, ns, w.ids, w.w, s);
   }
   if (e == cudaSuccess)
@@ -303,13 +306,15 @@ bitmoe_status_t moe_route(const uint16_t* x, int64_t T, const bitmoe_moe_shape_t
   bitmoe_status_t st = check_shape(shape, T);
   if (st != BITMOE_OK) return st;
   if (T == 0) return BITMOE_OK;
-  if (!x || !w_router || !topk_ids || !topk_w) return BITMOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(w_router)) return BITMOE_ERR_INVALID_ARG;
+  const bool scored = shape->k > 0;  // k = 0: a dense layer, only the shared expert's column
+  if (!x || (scored && !w_router) || !topk_ids || !topk_w) return BITMOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || (scored && !aligned16(w_router))) return BITMOE_ERR_INVALID_ARG;
   if ((st = check_ws(shape, T, workspace, workspace_bytes)) != BITMOE_OK) return st;
   const MoeWs w = moe_layout(shape, T, workspace);
   cudaStream_t s = (cudaStream_t)stream;
   float* logits = logits_out ? logits_out : w.logits;
-  cudaError_t e = launch_router_logits(x, (int)T, (int)shape->d, (int)shape->E, w_router, b_router, logits, s);
+  cudaError_t e = scored ? launch_router_logits(x, (int)T, (int)shape->d, (int)shape->E, w_router, b_router, logits, s)
+                         : cudaSuccess;
   if (e == cudaSuccess)
     e = launch_topk_gates(logits, (int)T, (int)shape->E, (int)shape->k, shape->renormalize, (int)shape->n_shared,
                           topk_ids, topk_w, s);

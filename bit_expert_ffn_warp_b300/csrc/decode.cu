@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
         consumer_sync();  // the partials are read; the normalised rows are in place
       }
     }
-    if (routed) {
+    if (routed && kr > 0) {  // (kr = 0: a dense layer, nothing to score)
       if (nexp > 0) ok = mbar_wait(wrbar, 0, p.st, 31) && ok;
       stamp(p, 17);
       if (!ok) *(volatile int*)fail = 1;
@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
         // largest of the 16 warp maxima is a lower bound tau for the k-th key
         // (k distinct elements reach it), so only keys >= tau can be chosen and
         // ranking those few candidates against each other gives the top-k.
-        for (int t = 0; t < T; ++t) {
+        for (int t = 0; t < T && kr > 0; ++t) {
           const unsigned long long key =
               (tid < E) ? (((unsigned long long)float_order_key(__ldcg(p.logits + (size_t)t * E + tid)) << 32) |
                            (0xffffffffu - (uint32_t)tid))

@@ -69,9 +69,12 @@ typedef enum bitmoe_status {
  * expert bank (the banks then hold E + 1 experts; the router still scores the
  * E routed ones), and every per-token array below -- topk_ids, topk_w, the
  * forced selection, the rows of the permutation -- has kt = k + n_shared
- * entries per token, the shared one last (id E, weight 1).  Supported: d and
- * I multiples of 128, group == 32, 1 <= k <= E, k + n_shared <= 32,
- * E + n_shared <= 1024.  (n_shared fills what was padding: the struct's size
+ * entries per token, the shared one last (id E, weight 1).  k = 0 with
+ * n_shared = 1 is a dense SwiGLU layer (the stack's two leading layers in the
+ * same transcript): the bank's one entry serves every token with weight 1 and
+ * there is no router (w_router may be NULL; E is normally 0).  Supported: d and
+ * I multiples of 128, group == 32, 1 <= k <= E or k = 0 with n_shared = 1,
+ * k + n_shared <= 32, E + n_shared <= 1024.  (n_shared fills what was padding: the struct's size
  * is that of the version without it, where it read as 0 when zero-filled.) */
 typedef struct bitmoe_moe_shape {
   int64_t d, E, k, I, group;

@@ -70,6 +70,10 @@ def test_host_side_validation_without_gpu(built):
     assert lib.moe_workspace_size(ctypes.byref(bm.MoeShape(2048, 256, 6, 512, 32, 1, 2)), 1) == 0
     assert lib.moe_workspace_size(ctypes.byref(bm.MoeShape(2048, 256, 32, 512, 32, 1, 1)), 1) == 0
     assert lib.moe_workspace_size(ctypes.byref(bm.MoeShape(2048, 1024, 8, 512, 32, 1, 1)), 1) == 0
+    # a dense layer: no routed experts, the shared one alone
+    assert lib.moe_workspace_size(ctypes.byref(bm.MoeShape(2048, 0, 0, 512, 32, 1, 1)), 4) > 0
+    assert lib.moe_workspace_size(ctypes.byref(bm.MoeShape(2048, 0, 0, 512, 32, 1, 0)), 4) == 0
+    assert lib.moe_workspace_size(ctypes.byref(bm.MoeShape(2048, 0, 2, 512, 32, 1, 1)), 4) == 0
     # null pointers -> INVALID_ARG, nothing launched
     rc = lib.moe_route(None, 1, ctypes.byref(sh), None, None, None, None, None, None, 0, None)
     assert rc == 1

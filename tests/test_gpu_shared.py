@@ -102,3 +102,25 @@ def test_shared_expert_separate_calls():
     ref = oracle.moe_forward(x_bits, t, K, n_shared=1, forced_ids=g, forced_w=w.cpu().numpy().astype(np.float64))
     o32 = out_f32.cpu().numpy().astype(np.float64)
     assert max_abs(o32, ref["out"]) <= MAX_ABS and rel_l2(o32, ref["out"]) <= REL_L2
+
+
+@pytest.mark.parametrize("T", [1, 8, 16, 600])
+def test_dense_layer(T):
+    """k = 0 with the shared expert alone: the stack's leading dense layers, on the
+    fused decode kernel (T <= 8), the streaming kernels and the grouped GEMM."""
+    t = synth.dense_layer(31, D, I)
+    lay = bm.MoeLayer.from_canonical(t, 0)
+    assert lay.E == 0 and lay.n_shared == 1 and lay.kt == 1 and lay.w_router is None
+    x_bits = synth.activations(500 + T, T, D)
+    ref = oracle.moe_forward(x_bits, t, 0, n_shared=1)
+    x = torch_bf16_from_bits(x_bits)
+    ws = bm.moe_workspace(lay, T)
+    ids = torch.empty((T, 1), dtype=torch.int32, device="cuda")
+    out_f32 = torch.empty((T, D), dtype=torch.float32, device="cuda")
+    bm.moe_forward(x, lay, ws, out_f32=out_f32, ids_out=ids)
+    torch.cuda.synchronize()
+    assert bm.bitmoe_get_device_status(ws) == 0
+    assert np.all(ids.cpu().numpy() == 0)
+    o32 = out_f32.cpu().numpy().astype(np.float64)
+    ma, rl = max_abs(o32, ref["out"]), rel_l2(o32, ref["out"])
+    assert ma <= MAX_ABS and rl <= REL_L2, f"T={T}: max-abs {ma:.3g} rel-L2 {rl:.3g}"
