@@ -19,7 +19,6 @@
 namespace bitmoe {
 namespace {
 
-constexpr int kFfnThreads = 128;
 constexpr int kNT = kTokBlock / 8;  // n-tiles of 8 tokens per unit
 
 __device__ __forceinline__ float scale_at(uint2 s, int gg) {
@@ -67,238 +66,461 @@ __device__ __forceinline__ int expert_of_block(const int32_t* __restrict__ blk_p
   return lo;
 }
 
-// ---------------------------------------------------------------- gate/up + SwiGLU
+// ---------------------------------------------------------------- pipeline plumbing
+//
+// Both kernels run one CTA per SM over a contiguous range of units.  Warp 8
+// streams the units' weight tiles through a ring of stages (TMA bulk copies on
+// full / empty mbarriers), warp 9 stages the activation rows of each token
+// block once (x_full / x_empty), and consumer warps 0..7 compute, so the weight
+// bytes of the next units are in flight while the current one is multiplied.
+// Every wait is bounded.  A wait that runs out raises a CTA-wide flag that makes
+// later waits give up at once; the consumers OR their failures into the
+// per-unit barrier itself (bar.red.or), so all of them leave at the same unit,
+// and the producers stop issuing and wait (bounded) for what they issued.
 
-__global__ void __launch_bounds__(kFfnThreads) ffn_up_kernel(FfnArgs p) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
-  const int d = p.d, I = p.I;
-  const int tbytes = (int)tile_bytes(d);
-  unsigned char* sg = smem + 128;
-  unsigned char* su = sg + tbytes;
-  unsigned char* sx = su + tbytes;
-  const int xstride = 2 * d + kSmemRowPad;
-  float* red = reinterpret_cast<float*>(sx + kTokBlock * xstride);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
-  if (tid == 0) {
-    mbar_init(bar, 1);
+constexpr int kConsWarps = 8;
+
+// Plain arrival (one count) on a shared-memory mbarrier.
+__device__ __forceinline__ void mbar_arrive_one(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+constexpr int kPipeThreads = (kConsWarps + 2) * 32;
+constexpr int kWProd = kConsWarps, kXProd = kConsWarps + 1;
+constexpr int kMaxRing = 16;
+
+struct Pipe {
+  uint64_t* full;   // [kMaxRing]
+  uint64_t* empty;  // [kMaxRing], one arrival per consumer warp
+  uint64_t* xfull;
+  uint64_t* xempty;  // one arrival per consumer warp
+  int* dead;
+};
+
+// Barrier of the consumer warps that also ORs a per-thread flag across them.
+__device__ __forceinline__ bool cons_sync_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.or.pred q, 1, %2, p; selp.u32 %0, 1, 0, q; }"
+      : "=r"(r)
+      : "r"((uint32_t)v), "n"(kConsWarps * 32)
+      : "memory");
+  return r != 0;
+}
+
+// Bounded wait that gives up at once when the CTA is already aborting.
+__device__ __forceinline__ bool pwait(uint64_t* bar, uint32_t parity, const Pipe& pp, DevStatus* st, int where) {
+  if (*(volatile int*)pp.dead) return false;
+  if (mbar_wait(bar, parity, st, where)) return true;
+  *(volatile int*)pp.dead = 1;
+  return false;
+}
+
+__device__ __forceinline__ Pipe pipe_init(unsigned char* smem, int ns) {
+  Pipe pp;
+  uint64_t* b = reinterpret_cast<uint64_t*>(smem);
+  pp.full = b;
+  pp.empty = b + kMaxRing;
+  pp.xfull = b + 2 * kMaxRing;
+  pp.xempty = b + 2 * kMaxRing + 1;
+  pp.dead = reinterpret_cast<int*>(b + 2 * kMaxRing + 2);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < ns; ++i) {
+      mbar_init(&pp.full[i], 1);
+      mbar_init(&pp.empty[i], kConsWarps);
+    }
+    mbar_init(pp.xfull, 1);
+    mbar_init(pp.xempty, kConsWarps);
+    *pp.dead = 0;
     fence_mbar_init();
   }
   __syncthreads();
+  return pp;
+}
+
+// The producer's last act: wait (bounded) until every copy it issued has landed.
+__device__ __forceinline__ void drain(const Pipe& pp, int issued, int ns, DevStatus* st) {
+  for (int i = issued - 1; i >= 0 && i >= issued - ns; --i) mbar_wait(&pp.full[i % ns], (i / ns) & 1, st, 19);
+}
+
+// Unit range of this CTA.
+__device__ __forceinline__ void unit_range(int n_units, int& lo, int& hi) {
+  lo = (int)((long)blockIdx.x * n_units / gridDim.x);
+  hi = (int)((long)(blockIdx.x + 1) * n_units / gridDim.x);
+}
+
+struct Blk {
+  int e, p0, nval;
+};
+
+__device__ __forceinline__ Blk block_info(const FfnArgs& p, int b) {
+  Blk k;
+  k.e = expert_of_block(p.blk_prefix, p.E, b);
+  k.p0 = p.offsets[k.e] + (b - p.blk_prefix[k.e]) * kTokBlock;
+  k.nval = min(kTokBlock, p.offsets[k.e + 1] - k.p0);
+  return k;
+}
+
+// ---------------------------------------------------------------- gate/up + SwiGLU
+//
+// Unit = (token block b, 16-row tile rt of W_gate and W_up); u = b * RT + rt.
+// A stage holds the gate and the up tile (2 x 18 KB at d = 2048).  Consumer
+// warp w takes the 128-column chunks w, w + 8, ...; partial sums meet in a
+// double-buffered shared array and one thread per (row, token) applies SwiGLU.
+
+__global__ void __launch_bounds__(kPipeThreads, 1) ffn_up_kernel(FfnArgs p, int ns) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int d = p.d, I = p.I;
+  const int tbytes = (int)tile_bytes(d);
+  const int xstride = 2 * d + kSmemRowPad;
+  unsigned char* sx = smem + 1024;                                        // [16][xstride]
+  float* red = reinterpret_cast<float*>(sx + kTokBlock * xstride);        // [2][8 warps][32][8 * kNT]
+  unsigned char* ring = reinterpret_cast<unsigned char*>(red + 2 * kConsWarps * 32 * 8 * kNT);
+  const Pipe pp = pipe_init(smem, ns);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
   const int RT = I / kTileRows;
-  const int n_units = RT * p.blk_prefix[p.E];
-  const int nch = d / kChunkK;
-  uint32_t phase = 0;
-  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-    const int b = u / RT, rt = u - b * RT;
-    const int e = expert_of_block(p.blk_prefix, p.E, b);
-    const int p0 = p.offsets[e] + (b - p.blk_prefix[e]) * kTokBlock;
-    const int nval = min(kTokBlock, p.offsets[e + 1] - p0);
-    if (tid == 0) {
-      mbar_arrive_expect_tx(bar, 2u * tbytes + (uint32_t)nval * 2u * d);
-      const size_t toff = ((size_t)e * RT + rt) * tbytes;
-      bulk_g2s(sg, p.gate + toff, tbytes, bar);
-      bulk_g2s(su, p.up + toff, tbytes, bar);
-      for (int i = 0; i < nval; ++i) {
-        const int t = p.sorted_rows[p0 + i] / p.k;
-        bulk_g2s(sx + i * xstride, p.x + (size_t)t * d, 2 * d, bar);
+  int u_lo, u_hi;
+  unit_range(RT * p.blk_prefix[p.E], u_lo, u_hi);
+  if (u_lo >= u_hi) return;
+
+  if (warp == kWProd) {  // weight tiles
+    if (lane == 0) {
+      int i = 0;
+      for (int u = u_lo; u < u_hi; ++u, ++i) {
+        const int s = i % ns;
+        if (i >= ns && !pwait(&pp.empty[s], ((i / ns) - 1) & 1, pp, p.st, 12)) break;
+        const int b = u / RT, rt = u - b * RT;
+        const int e = expert_of_block(p.blk_prefix, p.E, b);
+        const size_t toff = ((size_t)e * RT + rt) * tbytes;
+        mbar_arrive_expect_tx(&pp.full[s], 2u * tbytes);
+        bulk_g2s(ring + (size_t)s * 2 * tbytes, p.gate + toff, tbytes, &pp.full[s]);
+        bulk_g2s(ring + (size_t)s * 2 * tbytes + tbytes, p.up + toff, tbytes, &pp.full[s]);
+      }
+      drain(pp, i, ns, p.st);
+    }
+    return;
+  }
+  if (warp == kXProd) {  // activation rows, once per token block
+    if (lane == 0) {
+      int j = 0;
+      bool ok = true;
+      for (int u = u_lo; u < u_hi && ok; ++j) {
+        const int b = u / RT;
+        if (j > 0 && !pwait(pp.xempty, (j - 1) & 1, pp, p.st, 13)) break;
+        const Blk k = block_info(p, b);
+        mbar_arrive_expect_tx(pp.xfull, (uint32_t)k.nval * 2u * d);
+        for (int r = 0; r < k.nval; ++r) {
+          const int t = p.sorted_rows[k.p0 + r] / p.k;
+          bulk_g2s(sx + r * xstride, p.x + (size_t)t * d, 2 * d, pp.xfull);
+        }
+        if (!pwait(pp.xfull, j & 1, pp, p.st, 14)) ok = false;  // landed before the next refill
+        u = min(u_hi, (b + 1) * RT);
       }
     }
-    const bool ok = mbar_wait(bar, phase, p.st, 10);
-    if (__syncthreads_or(!ok)) return;  // uniform exit: every thread leaves together
-    phase ^= 1;
+    return;
+  }
+
+  // consumers
+  const int nch = d / kChunkK;
+  int cur_b = -1, j = 0, i = 0;
+  Blk k{};
+  for (int u = u_lo; u < u_hi; ++u, ++i) {
+    const int b = u / RT, rt = u - b * RT;
+    bool ok = true;
+    if (b != cur_b) {
+      if (cur_b >= 0) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive_one(pp.xempty);
+      }
+      ok = pwait(pp.xfull, j & 1, pp, p.st, 15);
+      ++j;
+      cur_b = b;
+      k = block_info(p, b);
+    }
+    const int s = i % ns;
+    ok = ok && pwait(&pp.full[s], (i / ns) & 1, pp, p.st, 16);
+    const unsigned char* sg = ring + (size_t)s * 2 * tbytes;
+    const unsigned char* su = sg + tbytes;
 
     float acc_g[kNT][4], acc_u[kNT][4];
 #pragma unroll
     for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc_g[nt][i] = acc_u[nt][i] = 0.f;
-
-    for (int ch = warp; ch < nch; ch += kFfnThreads / 32) {
-      const unsigned char* cg = sg + ch * kChunkBytes;
-      const unsigned char* cu = su + ch * kChunkBytes;
-      const uint4 qg0 = *reinterpret_cast<const uint4*>(cg + (g * 4 + c) * 16);
-      const uint4 qg1 = *reinterpret_cast<const uint4*>(cg + ((g + 8) * 4 + c) * 16);
-      const uint4 qu0 = *reinterpret_cast<const uint4*>(cu + (g * 4 + c) * 16);
-      const uint4 qu1 = *reinterpret_cast<const uint4*>(cu + ((g + 8) * 4 + c) * 16);
-      const uint2 sg0 = *reinterpret_cast<const uint2*>(cg + kChunkQBytes + g * 8);
-      const uint2 sg1 = *reinterpret_cast<const uint2*>(cg + kChunkQBytes + (g + 8) * 8);
-      const uint2 su0 = *reinterpret_cast<const uint2*>(cu + kChunkQBytes + g * 8);
-      const uint2 su1 = *reinterpret_cast<const uint2*>(cu + kChunkQBytes + (g + 8) * 8);
+      for (int q = 0; q < 4; ++q) acc_g[nt][q] = acc_u[nt][q] = 0.f;
+    const int nt_lim = (k.nval + 7) >> 3;  // n-tiles holding tokens (uniform in the CTA)
+    if (ok) {
+      for (int ch = warp; ch < nch; ch += kConsWarps) {
+        const unsigned char* cg = sg + ch * kChunkBytes;
+        const unsigned char* cu = su + ch * kChunkBytes;
+        const uint4 qg0 = *reinterpret_cast<const uint4*>(cg + (g * 4 + c) * 16);
+        const uint4 qg1 = *reinterpret_cast<const uint4*>(cg + ((g + 8) * 4 + c) * 16);
+        const uint4 qu0 = *reinterpret_cast<const uint4*>(cu + (g * 4 + c) * 16);
+        const uint4 qu1 = *reinterpret_cast<const uint4*>(cu + ((g + 8) * 4 + c) * 16);
+        const uint2 sg0 = *reinterpret_cast<const uint2*>(cg + kChunkQBytes + g * 8);
+        const uint2 sg1 = *reinterpret_cast<const uint2*>(cg + kChunkQBytes + (g + 8) * 8);
+        const uint2 su0 = *reinterpret_cast<const uint2*>(cu + kChunkQBytes + g * 8);
+        const uint2 su1 = *reinterpret_cast<const uint2*>(cu + kChunkQBytes + (g + 8) * 8);
 #pragma unroll
-      for (int gg = 0; gg < 4; ++gg) {
-        const int col = (ch * 4 + gg) * kGroup + c * 8;
-        uint32_t ag[2][4], au[2][4];
-        frag_bf16(word_at(qg0, gg), word_at(qg1, gg), ag);
-        frag_bf16(word_at(qu0, gg), word_at(qu1, gg), au);
-        const float s_g0 = scale_at(sg0, gg), s_g1 = scale_at(sg1, gg);
-        const float s_u0 = scale_at(su0, gg), s_u1 = scale_at(su1, gg);
+        for (int gg = 0; gg < 4; ++gg) {
+          const int col = (ch * 4 + gg) * kGroup + c * 8;
+          uint32_t ag[2][4], au[2][4];
+          frag_bf16(word_at(qg0, gg), word_at(qg1, gg), ag);
+          frag_bf16(word_at(qu0, gg), word_at(qu1, gg), au);
+          const float s_g0 = scale_at(sg0, gg), s_g1 = scale_at(sg1, gg);
+          const float s_u0 = scale_at(su0, gg), s_u1 = scale_at(su1, gg);
+          uint4 xb[kNT];
 #pragma unroll
-        for (int nt = 0; nt < kNT; ++nt) {
-          const int tok = nt * 8 + g;
-          uint4 xb = make_uint4(0, 0, 0, 0);
-          if (tok < nval) xb = *reinterpret_cast<const uint4*>(sx + tok * xstride + col * 2);
+          for (int nt = 0; nt < kNT; ++nt) {
+            const int tok = nt * 8 + g;
+            xb[nt] = make_uint4(0, 0, 0, 0);
+            if (nt < nt_lim && tok < k.nval) xb[nt] = *reinterpret_cast<const uint4*>(sx + tok * xstride + col * 2);
+          }
+          // the first halves of every n-tile, then the dependent second halves
           const float z[4] = {0.f, 0.f, 0.f, 0.f};
-          float dg[4], du[4];
-          mma_bf16(dg, ag[0], xb.x, xb.y, z);
-          mma_bf16(dg, ag[1], xb.z, xb.w, dg);
-          mma_bf16(du, au[0], xb.x, xb.y, z);
-          mma_bf16(du, au[1], xb.z, xb.w, du);
-          acc_g[nt][0] = fmaf(s_g0, dg[0], acc_g[nt][0]);
-          acc_g[nt][1] = fmaf(s_g0, dg[1], acc_g[nt][1]);
-          acc_g[nt][2] = fmaf(s_g1, dg[2], acc_g[nt][2]);
-          acc_g[nt][3] = fmaf(s_g1, dg[3], acc_g[nt][3]);
-          acc_u[nt][0] = fmaf(s_u0, du[0], acc_u[nt][0]);
-          acc_u[nt][1] = fmaf(s_u0, du[1], acc_u[nt][1]);
-          acc_u[nt][2] = fmaf(s_u1, du[2], acc_u[nt][2]);
-          acc_u[nt][3] = fmaf(s_u1, du[3], acc_u[nt][3]);
+          float dg[kNT][4], du[kNT][4];
+#pragma unroll
+          for (int nt = 0; nt < kNT; ++nt) {
+            if (nt < nt_lim) {
+              mma_bf16(dg[nt], ag[0], xb[nt].x, xb[nt].y, z);
+              mma_bf16(du[nt], au[0], xb[nt].x, xb[nt].y, z);
+            }
+          }
+#pragma unroll
+          for (int nt = 0; nt < kNT; ++nt) {
+            if (nt < nt_lim) {
+              mma_bf16(dg[nt], ag[1], xb[nt].z, xb[nt].w, dg[nt]);
+              mma_bf16(du[nt], au[1], xb[nt].z, xb[nt].w, du[nt]);
+            }
+          }
+#pragma unroll
+          for (int nt = 0; nt < kNT; ++nt) {
+            if (nt >= nt_lim) continue;
+            acc_g[nt][0] = fmaf(s_g0, dg[nt][0], acc_g[nt][0]);
+            acc_g[nt][1] = fmaf(s_g0, dg[nt][1], acc_g[nt][1]);
+            acc_g[nt][2] = fmaf(s_g1, dg[nt][2], acc_g[nt][2]);
+            acc_g[nt][3] = fmaf(s_g1, dg[nt][3], acc_g[nt][3]);
+            acc_u[nt][0] = fmaf(s_u0, du[nt][0], acc_u[nt][0]);
+            acc_u[nt][1] = fmaf(s_u0, du[nt][1], acc_u[nt][1]);
+            acc_u[nt][2] = fmaf(s_u1, du[nt][2], acc_u[nt][2]);
+            acc_u[nt][3] = fmaf(s_u1, du[nt][3], acc_u[nt][3]);
+          }
         }
       }
     }
-    float* my = red + (size_t)(warp * 32 + lane) * (8 * kNT);
+    __syncwarp();
+    if (lane == 0) mbar_arrive_one(&pp.empty[s]);  // the stage's bytes are in registers
+    float* rb = red + (size_t)(i & 1) * kConsWarps * 32 * 8 * kNT;  // [warp][value][lane]
+    float* my = rb + (size_t)warp * (8 * kNT) * 32 + lane;
 #pragma unroll
     for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        my[nt * 4 + i] = acc_g[nt][i];
-        my[4 * kNT + nt * 4 + i] = acc_u[nt][i];
+      for (int q = 0; q < 4; ++q) {
+        my[(nt * 4 + q) * 32] = acc_g[nt][q];
+        my[(4 * kNT + nt * 4 + q) * 32] = acc_u[nt][q];
       }
-    __syncthreads();
-    if (warp == 0) {
+    if (cons_sync_or(!ok)) break;  // the same decision in every consumer
+    {  // one thread per (row, token) of the 16 x 16 tile
+      const int row = tid >> 4, tok = tid & 15;
+      if (tok < k.nval) {
+        const int nt = tok >> 3, cc = (tok & 7) >> 1, q = ((row >= 8) ? 2 : 0) + (tok & 1);
+        const int ln = (row & 7) * 4 + cc;
+        float a = 0.f, uu = 0.f;
 #pragma unroll
-      for (int nt = 0; nt < kNT; ++nt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float a = 0.f, uu = 0.f;
-#pragma unroll
-          for (int w = 0; w < kFfnThreads / 32; ++w) {
-            a += red[(size_t)(w * 32 + lane) * (8 * kNT) + nt * 4 + i];
-            uu += red[(size_t)(w * 32 + lane) * (8 * kNT) + 4 * kNT + nt * 4 + i];
-          }
-          const int row = rt * kTileRows + ((i < 2) ? g : g + 8);
-          const int tok = nt * 8 + 2 * c + (i & 1);
-          if (tok < nval) {
-            const float h = silu_mul(a, uu);
-            const __half hi = __float2half_rn(h);
-            const __half lo = __float2half_rn(h - __half2float(hi));
-            p.h_hi[(size_t)(p0 + tok) * I + row] = hi;
-            p.h_lo[(size_t)(p0 + tok) * I + row] = lo;
-          }
+        for (int w = 0; w < kConsWarps; ++w) {
+          a += rb[((size_t)w * (8 * kNT) + nt * 4 + q) * 32 + ln];
+          uu += rb[((size_t)w * (8 * kNT) + 4 * kNT + nt * 4 + q) * 32 + ln];
         }
+        const float h = silu_mul(a, uu);
+        const __half hi = __float2half_rn(h);
+        const __half lo = __float2half_rn(h - __half2float(hi));
+        const size_t o = (size_t)(k.p0 + tok) * I + rt * kTileRows + row;
+        p.h_hi[o] = hi;
+        p.h_lo[o] = lo;
+      }
     }
-    __syncthreads();
   }
 }
 
 // ---------------------------------------------------------------- down projection
+//
+// Unit = (token block b, pair cp of 16-row W_down tiles); u = b * CT2 + cp.  A
+// stage holds the two tiles (2 x 4.6 KB at I = 512); the block's h rows (fp16 hi
+// and lo) are staged once per block.  A block of at most 8 rows has one n-tile:
+// warp w computes tile w >> 2 over chunks (w & 3) + 4m.  A larger block has two:
+// warp w computes tile w >> 2, n-tile w & 1, over the chunk pairs
+// {2 ((w >> 1) & 1), +1} + 4m.
 
-__global__ void __launch_bounds__(kFfnThreads) ffn_down_kernel(FfnArgs p) {
+__device__ __forceinline__ void down_chunk(const unsigned char* cw, const unsigned char* hh, const unsigned char* hl,
+                                           bool has, int ch, int g, int c, float (&acc)[4]) {
+  const uint4 q0 = *reinterpret_cast<const uint4*>(cw + (g * 4 + c) * 16);
+  const uint4 q1 = *reinterpret_cast<const uint4*>(cw + ((g + 8) * 4 + c) * 16);
+  const uint2 s0 = *reinterpret_cast<const uint2*>(cw + kChunkQBytes + g * 8);
+  const uint2 s1 = *reinterpret_cast<const uint2*>(cw + kChunkQBytes + (g + 8) * 8);
+#pragma unroll
+  for (int gp = 0; gp < 4; gp += 2) {  // two groups at a time: four independent chains
+    uint32_t a[2][2][4];
+    uint4 bh[2], bl[2];
+    float sc0[2], sc1[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int gg = gp + h;
+      const int col = (ch * 4 + gg) * kGroup + c * 8;
+      frag_f16(word_at(q0, gg), word_at(q1, gg), a[h]);
+      sc0[h] = scale_at(s0, gg);
+      sc1[h] = scale_at(s1, gg);
+      bh[h] = make_uint4(0, 0, 0, 0);
+      bl[h] = make_uint4(0, 0, 0, 0);
+      if (has) {
+        bh[h] = *reinterpret_cast<const uint4*>(hh + col * 2);
+        bl[h] = *reinterpret_cast<const uint4*>(hl + col * 2);
+      }
+    }
+    const float z[4] = {0.f, 0.f, 0.f, 0.f};
+    float dh[2][4], dl[2][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      mma_f16(dh[h], a[h][0], bh[h].x, bh[h].y, z);
+      mma_f16(dl[h], a[h][0], bl[h].x, bl[h].y, z);
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      mma_f16(dh[h], a[h][1], bh[h].z, bh[h].w, dh[h]);
+      mma_f16(dl[h], a[h][1], bl[h].z, bl[h].w, dl[h]);
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      acc[0] = fmaf(sc0[h], dh[h][0] + dl[h][0], acc[0]);
+      acc[1] = fmaf(sc0[h], dh[h][1] + dl[h][1], acc[1]);
+      acc[2] = fmaf(sc1[h], dh[h][2] + dl[h][2], acc[2]);
+      acc[3] = fmaf(sc1[h], dh[h][3] + dl[h][3], acc[3]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kPipeThreads, 1) ffn_down_kernel(FfnArgs p, int ns) {
   extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
   const int d = p.d, I = p.I;
   const int tbytes = (int)tile_bytes(I);
-  unsigned char* sw = smem + 128;
   const int hstride = 2 * I + kSmemRowPad;
-  unsigned char* shh = sw + tbytes;
+  unsigned char* shh = smem + 1024;
   unsigned char* shl = shh + kTokBlock * hstride;
-  float* red = reinterpret_cast<float*>(shl + kTokBlock * hstride);
+  float* red = reinterpret_cast<float*>(shl + kTokBlock * hstride);  // [2][8 warps][4][32]
+  unsigned char* ring = reinterpret_cast<unsigned char*>(red + 2 * kConsWarps * 32 * 4);
+  const Pipe pp = pipe_init(smem, ns);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
-  if (tid == 0) {
-    mbar_init(bar, 1);
-    fence_mbar_init();
+  const int CT = d / kTileRows, CT2 = CT / 2;
+  int u_lo, u_hi;
+  unit_range(CT2 * p.blk_prefix[p.E], u_lo, u_hi);
+  if (u_lo >= u_hi) return;
+
+  if (warp == kWProd) {
+    if (lane == 0) {
+      int i = 0;
+      for (int u = u_lo; u < u_hi; ++u, ++i) {
+        const int s = i % ns;
+        if (i >= ns && !pwait(&pp.empty[s], ((i / ns) - 1) & 1, pp, p.st, 22)) break;
+        const int b = u / CT2, cp = u - b * CT2;
+        const int e = expert_of_block(p.blk_prefix, p.E, b);
+        mbar_arrive_expect_tx(&pp.full[s], 2u * tbytes);
+        bulk_g2s(ring + (size_t)s * 2 * tbytes, p.down + ((size_t)e * CT + 2 * cp) * tbytes, 2u * tbytes,
+                 &pp.full[s]);
+      }
+      drain(pp, i, ns, p.st);
+    }
+    return;
   }
-  __syncthreads();
-  const int CT = d / kTileRows;
-  const int n_units = CT * p.blk_prefix[p.E];
-  const int nch = I / kChunkK;
-  uint32_t phase = 0;
-  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-    const int b = u / CT, ct = u - b * CT;
-    const int e = expert_of_block(p.blk_prefix, p.E, b);
-    const int p0 = p.offsets[e] + (b - p.blk_prefix[e]) * kTokBlock;
-    const int nval = min(kTokBlock, p.offsets[e + 1] - p0);
-    if (tid == 0) {
-      mbar_arrive_expect_tx(bar, (uint32_t)tbytes + (uint32_t)nval * 4u * I);
-      bulk_g2s(sw, p.down + ((size_t)e * CT + ct) * tbytes, tbytes, bar);
-      for (int i = 0; i < nval; ++i) {
-        bulk_g2s(shh + i * hstride, p.h_hi + (size_t)(p0 + i) * I, 2 * I, bar);
-        bulk_g2s(shl + i * hstride, p.h_lo + (size_t)(p0 + i) * I, 2 * I, bar);
-      }
-    }
-    const bool ok = mbar_wait(bar, phase, p.st, 11);
-    if (__syncthreads_or(!ok)) return;  // uniform exit: every thread leaves together
-    phase ^= 1;
-
-    float acc[kNT][4];
-#pragma unroll
-    for (int nt = 0; nt < kNT; ++nt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
-
-    for (int ch = warp; ch < nch; ch += kFfnThreads / 32) {
-      const unsigned char* cw = sw + ch * kChunkBytes;
-      const uint4 q0 = *reinterpret_cast<const uint4*>(cw + (g * 4 + c) * 16);
-      const uint4 q1 = *reinterpret_cast<const uint4*>(cw + ((g + 8) * 4 + c) * 16);
-      const uint2 s0 = *reinterpret_cast<const uint2*>(cw + kChunkQBytes + g * 8);
-      const uint2 s1 = *reinterpret_cast<const uint2*>(cw + kChunkQBytes + (g + 8) * 8);
-#pragma unroll
-      for (int gg = 0; gg < 4; ++gg) {
-        const int col = (ch * 4 + gg) * kGroup + c * 8;
-        uint32_t a[2][4];
-        frag_f16(word_at(q0, gg), word_at(q1, gg), a);
-        const float sc0 = scale_at(s0, gg), sc1 = scale_at(s1, gg);
-#pragma unroll
-        for (int nt = 0; nt < kNT; ++nt) {
-          const int tok = nt * 8 + g;
-          uint4 bh = make_uint4(0, 0, 0, 0), bl = make_uint4(0, 0, 0, 0);
-          if (tok < nval) {
-            bh = *reinterpret_cast<const uint4*>(shh + tok * hstride + col * 2);
-            bl = *reinterpret_cast<const uint4*>(shl + tok * hstride + col * 2);
-          }
-          const float z[4] = {0.f, 0.f, 0.f, 0.f};
-          float dd[4];
-          mma_f16(dd, a[0], bh.x, bh.y, z);
-          mma_f16(dd, a[0], bl.x, bl.y, dd);
-          mma_f16(dd, a[1], bh.z, bh.w, dd);
-          mma_f16(dd, a[1], bl.z, bl.w, dd);
-          acc[nt][0] = fmaf(sc0, dd[0], acc[nt][0]);
-          acc[nt][1] = fmaf(sc0, dd[1], acc[nt][1]);
-          acc[nt][2] = fmaf(sc1, dd[2], acc[nt][2]);
-          acc[nt][3] = fmaf(sc1, dd[3], acc[nt][3]);
+  if (warp == kXProd) {
+    if (lane == 0) {
+      int j = 0;
+      bool ok = true;
+      for (int u = u_lo; u < u_hi && ok; ++j) {
+        const int b = u / CT2;
+        if (j > 0 && !pwait(pp.xempty, (j - 1) & 1, pp, p.st, 23)) break;
+        const Blk k = block_info(p, b);
+        mbar_arrive_expect_tx(pp.xfull, (uint32_t)k.nval * 4u * I);
+        for (int r = 0; r < k.nval; ++r) {
+          bulk_g2s(shh + r * hstride, p.h_hi + (size_t)(k.p0 + r) * I, 2 * I, pp.xfull);
+          bulk_g2s(shl + r * hstride, p.h_lo + (size_t)(k.p0 + r) * I, 2 * I, pp.xfull);
         }
+        if (!pwait(pp.xfull, j & 1, pp, p.st, 24)) ok = false;
+        u = min(u_hi, (b + 1) * CT2);
       }
     }
-    float* my = red + (size_t)(warp * 32 + lane) * (4 * kNT);
+    return;
+  }
+
+  const int nch = I / kChunkK;
+  const int tile = warp >> 2;
+  int cur_b = -1, j = 0, i = 0;
+  Blk k{};
+  for (int u = u_lo; u < u_hi; ++u, ++i) {
+    const int b = u / CT2, cp = u - b * CT2;
+    bool ok = true;
+    if (b != cur_b) {
+      if (cur_b >= 0) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive_one(pp.xempty);
+      }
+      ok = pwait(pp.xfull, j & 1, pp, p.st, 25);
+      ++j;
+      cur_b = b;
+      k = block_info(p, b);
+    }
+    const bool small = k.nval <= 8;  // one n-tile (uniform in the CTA)
+    const int s = i % ns;
+    ok = ok && pwait(&pp.full[s], (i / ns) & 1, pp, p.st, 26);
+    const unsigned char* sw = ring + (size_t)s * 2 * tbytes + (size_t)tile * tbytes;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (ok) {
+      if (small) {
+        const bool has = g < k.nval;
+        for (int ch = warp & 3; ch < nch; ch += 4)
+          down_chunk(sw + ch * kChunkBytes, shh + g * hstride, shl + g * hstride, has, ch, g, c, acc);
+      } else {
+        const int nt = warp & 1, tok = nt * 8 + g;
+        const bool has = tok < k.nval;
+        for (int ch0 = 2 * ((warp >> 1) & 1); ch0 < nch; ch0 += 4)
+          for (int ch = ch0; ch < ch0 + 2 && ch < nch; ++ch)
+            down_chunk(sw + ch * kChunkBytes, shh + tok * hstride, shl + tok * hstride, has, ch, g, c, acc);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive_one(&pp.empty[s]);
+    float* rb = red + (size_t)(i & 1) * kConsWarps * 32 * 4;  // [warp][value][lane]
 #pragma unroll
-    for (int nt = 0; nt < kNT; ++nt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) my[nt * 4 + i] = acc[nt][i];
-    __syncthreads();
-    if (warp == 0) {
-#pragma unroll
-      for (int nt = 0; nt < kNT; ++nt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
+    for (int q = 0; q < 4; ++q) rb[((size_t)warp * 4 + q) * 32 + lane] = acc[q];
+    if (cons_sync_or(!ok)) break;  // the same decision in every consumer
+    {  // thread -> (tile, column, token low bits); four (small) or two partial sums per output
+      const int tl = tid >> 7, col = (tid >> 3) & 15, t8 = tid & 7;
+      const int cc = t8 >> 1, q = ((col >= 8) ? 2 : 0) + (t8 & 1), ln = (col & 7) * 4 + cc;
+      const size_t ybase = (size_t)(2 * cp + tl) * kTileRows + col;
+      if (small) {
+        if (t8 < k.nval) {
           float v = 0.f;
 #pragma unroll
-          for (int w = 0; w < kFfnThreads / 32; ++w) v += red[(size_t)(w * 32 + lane) * (4 * kNT) + nt * 4 + i];
-          const int col = ct * kTileRows + ((i < 2) ? g : g + 8);
-          const int tok = nt * 8 + 2 * c + (i & 1);
-          if (tok < nval) p.y_rows[(size_t)(p0 + tok) * d + col] = v;
+          for (int w = 0; w < 4; ++w) v += rb[((size_t)(tl * 4 + w) * 4 + q) * 32 + ln];
+          p.y_rows[(size_t)(k.p0 + t8) * d + ybase] = v;
         }
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int tk = nt * 8 + t8;
+          if (tk < k.nval) {
+            const float v = rb[((size_t)(tl * 4 + nt) * 4 + q) * 32 + ln] + rb[((size_t)(tl * 4 + 2 + nt) * 4 + q) * 32 + ln];
+            p.y_rows[(size_t)(k.p0 + tk) * d + ybase] = v;
+          }
+        }
+      }
     }
-    __syncthreads();
   }
 }
 
-size_t up_smem(int d) {
-  return 128 + 2 * (size_t)tile_bytes(d) + (size_t)kTokBlock * (2 * d + kSmemRowPad) +
-         (size_t)kFfnThreads * 8 * kNT * sizeof(float);
+size_t up_fixed_smem(int d) {
+  return 1024 + (size_t)kTokBlock * (2 * d + kSmemRowPad) + (size_t)2 * kConsWarps * 32 * 8 * kNT * sizeof(float);
 }
-size_t down_smem(int I) {
-  return 128 + (size_t)tile_bytes(I) + 2 * (size_t)kTokBlock * (2 * I + kSmemRowPad) +
-         (size_t)kFfnThreads * 4 * kNT * sizeof(float);
+size_t down_fixed_smem(int I) {
+  return 1024 + 2 * (size_t)kTokBlock * (2 * I + kSmemRowPad) + (size_t)2 * kConsWarps * 32 * 4 * sizeof(float);
 }
+constexpr size_t kFfnSmemBudget = 227 * 1024;
 
 int num_sms() {
   static int n = 0;
@@ -319,26 +541,35 @@ int max_blocks(int R, int E) { return min(R, E) + R / kTokBlock + 1; }
 cudaError_t launch_ffn_up(const FfnArgs& a, cudaStream_t s) {
   const int R = a.T * a.k;
   if (R == 0) return cudaSuccess;
-  const size_t sm = up_smem(a.d);
+  const size_t fixed = up_fixed_smem(a.d), stage = 2 * (size_t)tile_bytes(a.d);
+  if (fixed + 2 * stage > kFfnSmemBudget) return cudaErrorNotSupported;
+  int ns = (int)((kFfnSmemBudget - fixed) / stage);
+  if (ns > kMaxRing) ns = kMaxRing;
+  const size_t sm = fixed + (size_t)ns * stage;
   static int attr_set[64] = {};
   cudaError_t err = ensure_smem_attr(ffn_up_kernel, sm, attr_set);
   if (err != cudaSuccess) return err;
   const long units = (long)(a.I / kTileRows) * max_blocks(R, a.E);
-  const int grid = (int)(units < 2L * num_sms() ? units : 2L * num_sms());
-  ffn_up_kernel<<<grid, kFfnThreads, sm, s>>>(a);
+  const int grid = (int)(units < num_sms() ? units : num_sms());
+  ffn_up_kernel<<<grid, kPipeThreads, sm, s>>>(a, ns);
   return cudaGetLastError();
 }
 
 cudaError_t launch_ffn_down(const FfnArgs& a, cudaStream_t s) {
   const int R = a.T * a.k;
   if (R == 0) return cudaSuccess;
-  const size_t sm = down_smem(a.I);
+  if ((a.d / kTileRows) % 2) return cudaErrorNotSupported;
+  const size_t fixed = down_fixed_smem(a.I), stage = 2 * (size_t)tile_bytes(a.I);
+  if (fixed + 2 * stage > kFfnSmemBudget) return cudaErrorNotSupported;
+  int ns = (int)((kFfnSmemBudget - fixed) / stage);
+  if (ns > kMaxRing) ns = kMaxRing;
+  const size_t sm = fixed + (size_t)ns * stage;
   static int attr_set[64] = {};
   cudaError_t err = ensure_smem_attr(ffn_down_kernel, sm, attr_set);
   if (err != cudaSuccess) return err;
-  const long units = (long)(a.d / kTileRows) * max_blocks(R, a.E);
-  const int grid = (int)(units < 4L * num_sms() ? units : 4L * num_sms());
-  ffn_down_kernel<<<grid, kFfnThreads, sm, s>>>(a);
+  const long units = (long)(a.d / kTileRows / 2) * max_blocks(R, a.E);
+  const int grid = (int)(units < num_sms() ? units : num_sms());
+  ffn_down_kernel<<<grid, kPipeThreads, sm, s>>>(a, ns);
   return cudaGetLastError();
 }
 
