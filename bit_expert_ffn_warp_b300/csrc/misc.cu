@@ -11,24 +11,40 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       uint16_t* out, float* __restrict__ out_f32) {
   const int t = blockIdx.y;
   for (int c8 = (blockIdx.x * blockDim.x + threadIdx.x) * 8; c8 < d; c8 += gridDim.x * blockDim.x * 8) {
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-    for (int j = 0; j < k; ++j) {
-      const int pos = inv[(size_t)t * k + j];
-      if (pos < 0) continue;
-      const float wj = w[(size_t)t * k + j];
-      const float4 y0 = *reinterpret_cast<const float4*>(y + (size_t)pos * d + c8);
-      const float4 y1 = *reinterpret_cast<const float4*>(y + (size_t)pos * d + c8 + 4);
-      acc[0] = fmaf(wj, y0.x, acc[0]);
-      acc[1] = fmaf(wj, y0.y, acc[1]);
-      acc[2] = fmaf(wj, y0.z, acc[2]);
-      acc[3] = fmaf(wj, y0.w, acc[3]);
-      acc[4] = fmaf(wj, y1.x, acc[4]);
-      acc[5] = fmaf(wj, y1.y, acc[5]);
-      acc[6] = fmaf(wj, y1.z, acc[6]);
-      acc[7] = fmaf(wj, y1.w, acc[7]);
-    }
+    // the residual, then each batch of 8 rows' positions and gates, then their y
+    // pieces, are requested together; the sum still runs in ascending j
     const uint4 r = *reinterpret_cast<const uint4*>(resid + (size_t)t * d + c8);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      int pos[8];
+      float wj[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int j = j0 + i;
+        pos[i] = j < k ? inv[(size_t)t * k + j] : -1;
+        wj[i] = j < k ? w[(size_t)t * k + j] : 0.f;
+      }
+      float4 y0[8], y1[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (pos[i] >= 0) {
+          y0[i] = *reinterpret_cast<const float4*>(y + (size_t)pos[i] * d + c8);
+          y1[i] = *reinterpret_cast<const float4*>(y + (size_t)pos[i] * d + c8 + 4);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (pos[i] < 0) continue;
+        acc[0] = fmaf(wj[i], y0[i].x, acc[0]);
+        acc[1] = fmaf(wj[i], y0[i].y, acc[1]);
+        acc[2] = fmaf(wj[i], y0[i].z, acc[2]);
+        acc[3] = fmaf(wj[i], y0[i].w, acc[3]);
+        acc[4] = fmaf(wj[i], y1[i].x, acc[4]);
+        acc[5] = fmaf(wj[i], y1[i].y, acc[5]);
+        acc[6] = fmaf(wj[i], y1[i].z, acc[6]);
+        acc[7] = fmaf(wj[i], y1[i].w, acc[7]);
+      }
+    }
     const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
     float o[8];
     uint32_t ob[4];
@@ -52,22 +68,34 @@ __global__ void __launch_bounds__(256) combine_f16_kernel(const __half* __restri
                                                           int k, uint16_t* out, float* __restrict__ out_f32) {
   const int t = blockIdx.y;
   for (int c8 = (blockIdx.x * blockDim.x + threadIdx.x) * 8; c8 < d; c8 += gridDim.x * blockDim.x * 8) {
+    // as combine_kernel: residual, positions and gates, then y pieces requested together
+    const uint4 r = *reinterpret_cast<const uint4*>(resid + (size_t)t * d + c8);
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-    for (int j = 0; j < k; ++j) {
-      const int pos = inv[(size_t)t * k + j];
-      if (pos < 0) continue;
-      const float wj = w[(size_t)t * k + j];
-      const uint4 yv = *reinterpret_cast<const uint4*>(y + (size_t)pos * d + c8);
-      const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      int pos[8];
+      float wj[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&yw[i]));
-        acc[2 * i] = fmaf(wj, f.x, acc[2 * i]);
-        acc[2 * i + 1] = fmaf(wj, f.y, acc[2 * i + 1]);
+      for (int i = 0; i < 8; ++i) {
+        const int j = j0 + i;
+        pos[i] = j < k ? inv[(size_t)t * k + j] : -1;
+        wj[i] = j < k ? w[(size_t)t * k + j] : 0.f;
+      }
+      uint4 yv[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (pos[i] >= 0) yv[i] = *reinterpret_cast<const uint4*>(y + (size_t)pos[i] * d + c8);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (pos[i] < 0) continue;
+        const uint32_t yw[4] = {yv[i].x, yv[i].y, yv[i].z, yv[i].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&yw[q]));
+          acc[2 * q] = fmaf(wj[i], f.x, acc[2 * q]);
+          acc[2 * q + 1] = fmaf(wj[i], f.y, acc[2 * q + 1]);
+        }
       }
     }
-    const uint4 r = *reinterpret_cast<const uint4*>(resid + (size_t)t * d + c8);
     const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
     float o[8];
     uint32_t ob[4];

@@ -46,8 +46,14 @@ __global__ void __launch_bounds__(kRmWarps * 32) router_mma_kernel(const uint16_
   const uint32_t* xa = reinterpret_cast<const uint32_t*>(x + (size_t)(va ? ta : 0) * d);
   const uint32_t* xb = reinterpret_cast<const uint32_t*>(x + (size_t)(vb ? tb : 0) * d);
   const float* wr = Wr + (size_t)(ew < E ? ew : 0) * d;
+  // the CTA's router rows are contiguous: one bulk prefetch pulls them into L2 at
+  // full bandwidth, so the warps' small loads below meet L2 instead of DRAM
+  if (threadIdx.x == 0) {
+    const int ne = min(kRmExp, E - e0);
+    bulk_prefetch_l2(Wr + (size_t)e0 * d, (uint32_t)ne * (uint32_t)d * 4u);
+  }
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
+#pragma unroll 4  // four steps' loads in flight per round trip
   for (int kk = warp * slice; kk < (warp + 1) * slice; kk += 16) {
     uint32_t A[4];
     A[0] = va ? xa[(kk + 2 * c) >> 1] : 0u;
@@ -106,21 +112,37 @@ __global__ void __launch_bounds__(256) router_mma_tiled_kernel(const uint16_t* _
   const int wm = warp & 3, wn = warp >> 2;  // 16-token row block, 32-expert column block
   const int t0 = blockIdx.x * kRtT, e0 = blockIdx.y * kRtE;
   float acc[4][4] = {};
-  for (int k0 = 0; k0 < d; k0 += kRtK) {
-    // x tile: 64 rows x 128 B, two 16-byte pieces per thread
+  // the next K chunk's global pieces are loaded into registers while the current
+  // chunk is multiplied: x as two 16-byte pieces, Wr as four float4 per thread
+  uint4 xr[2];
+  float4 wr[4];
+  auto load_chunk = [&](int k0) {
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const int piece = tid + i * 256, r = piece >> 3, c8 = (piece & 7) * 8;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (t0 + r < T) v = *reinterpret_cast<const uint4*>(x + (size_t)(t0 + r) * d + k0 + c8);
-      *reinterpret_cast<uint4*>(&xs[r][c8]) = v;
+      xr[i] = make_uint4(0, 0, 0, 0);
+      if (t0 + r < T) xr[i] = *reinterpret_cast<const uint4*>(x + (size_t)(t0 + r) * d + k0 + c8);
     }
-    // Wr tile: 64 rows x 256 B, four 16-byte pieces per thread, split into hi / mid / lo
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int piece = tid + i * 256, r = piece >> 4, c4 = (piece & 15) * 4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (e0 + r < E) v = *reinterpret_cast<const float4*>(Wr + (size_t)(e0 + r) * d + k0 + c4);
+      wr[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e0 + r < E) wr[i] = *reinterpret_cast<const float4*>(Wr + (size_t)(e0 + r) * d + k0 + c4);
+    }
+  };
+  load_chunk(0);
+  for (int k0 = 0; k0 < d; k0 += kRtK) {
+    // x tile: 64 rows x 128 B
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int piece = tid + i * 256, r = piece >> 3, c8 = (piece & 7) * 8;
+      *reinterpret_cast<uint4*>(&xs[r][c8]) = xr[i];
+    }
+    // Wr tile: 64 rows x 256 B, split into hi / mid / lo
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int piece = tid + i * 256, r = piece >> 4, c4 = (piece & 15) * 4;
+      const float4 v = wr[i];
       uint32_t h[4], m[4], l[4];
       split3_bf16(v.x, h[0], m[0], l[0]);
       split3_bf16(v.y, h[1], m[1], l[1]);
@@ -131,6 +153,7 @@ __global__ void __launch_bounds__(256) router_mma_tiled_kernel(const uint16_t* _
       *reinterpret_cast<uint2*>(&wp[2][r][c4]) = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
     }
     __syncthreads();
+    if (k0 + kRtK < d) load_chunk(k0 + kRtK);
 #pragma unroll
     for (int kk = 0; kk < kRtK; kk += 16) {
       uint32_t A[4];
