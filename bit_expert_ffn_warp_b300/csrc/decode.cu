@@ -160,6 +160,74 @@ struct Routing {  // shared-memory routing tables (identical in every CTA)
   int* misc;     // [0] U, [1] fail flag, [2] candidate count, [3] tau slot
 };
 
+// Top-k of one token by one warp, for batches of several tokens (one warp per
+// token, all tokens at once): lane l holds logits e = l, l + 32, ...; kr rounds
+// of a warp arg-max over (value descending, index ascending) pick the experts in
+// order; gates exp(l_j - l_max) over the chosen kr (renormalised) or over all E.
+// Writes the token's rows t*k + j of the routing tables (the shared expert's
+// row, if any, last with weight 1).
+template <int NPER>  // logits per lane: E <= 32 * NPER
+__device__ void warp_topk_token(const float* __restrict__ lrow, int E, int kr, int k, int renorm, int t, int* ids,
+                                float* w, int lane) {
+  float v[NPER];
+  const int nper = (E + 31) / 32;
+#pragma unroll
+  for (int i = 0; i < NPER; ++i) {
+    const int e = i * 32 + lane;
+    v[i] = (i < nper && e < E) ? __ldcg(lrow + e) : -INFINITY;
+  }
+  uint32_t taken = 0;
+  float my_sel = -INFINITY, vmax = 0.f;
+  int my_id = 0;
+  for (int j = 0; j < kr; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < NPER; ++i) {
+      const int e = i * 32 + lane;
+      if (i < nper && e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+        bv = v[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (bi < E && (bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (j == 0) vmax = bv;
+    if (j == lane) {
+      my_sel = bv;
+      my_id = bi;
+    }
+  }
+  const float my_e = (lane < kr) ? expf(my_sel - vmax) : 0.f;
+  float z = 0.f;
+  if (renorm) {
+    z = my_e;
+  } else {
+#pragma unroll
+    for (int i = 0; i < NPER; ++i) {
+      const int e = i * 32 + lane;
+      if (i < nper && e < E) z += expf(v[i] - vmax);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+  if (lane < kr) {
+    ids[t * k + lane] = (my_id < E) ? my_id : -1;
+    w[t * k + lane] = my_e / z;
+  } else if (lane < k) {
+    ids[t * k + lane] = E;
+    w[t * k + lane] = 1.0f;
+  }
+}
+
 __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs p) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -347,7 +415,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
 
     // ---------------- P1: routing tables, replicated in every CTA
     if (*(volatile int*)fail == 0) {
-      if (routed) {
+      if (routed && T > 1 && kr > 0) {
+        // several tokens: one warp per token, all tokens at once
+        if (warp < T) {
+          if (E <= 256)
+            warp_topk_token<8>(p.logits + (size_t)warp * E, E, kr, k, p.renorm, warp, rt.ids, rt.w, lane);
+          else
+            warp_topk_token<kDecMaxE / 32>(p.logits + (size_t)warp * E, E, kr, k, p.renorm, warp, rt.ids, rt.w,
+                                            lane);
+        }
+      } else if (routed) {
         // Per token: keys = order-preserving logit bits, then the inverted
         // expert index (equal logits put the lower expert first).  The k-th
         // largest of the 16 warp maxima is a lower bound tau for the k-th key
