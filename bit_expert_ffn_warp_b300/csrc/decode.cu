@@ -39,6 +39,7 @@ constexpr int kDecMaxE = kConsumers;  // one logit per consumer thread
 constexpr int kDecMaxK = kDecWarps;   // the warp-maxima bound needs k <= number of warps
 constexpr int kDecMaxT = 8;
 constexpr int kTracePoints = 32;
+static_assert(kDecMaxT * (kDecMaxK + 1) <= kConsumers, "one routed row per consumer thread in the counts");
 
 struct DecodeArgs {
   const uint16_t* x;
@@ -82,6 +83,16 @@ __device__ __forceinline__ void stamp(const unsigned long long* trace, int point
 __device__ __forceinline__ void stamp(const DecodeArgs& p, int point) { stamp(p.trace, point); }
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers)); }
+
+// Barrier of the consumer warps that returns how many of their threads passed pred.
+__device__ __forceinline__ int consumer_popc(bool pred) {
+  int n;
+  asm volatile("{ .reg .pred p; setp.ne.u32 p, %1, 0; bar.red.popc.u32 %0, 1, %2, p; }"
+               : "=r"(n)
+               : "r"((uint32_t)pred), "n"(kConsumers)
+               : "memory");
+  return n;
+}
 
 __device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -522,6 +533,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
         const int e = rt.ids[r];
         int less = 0, before = 0;
         if (e >= 0) {
+#pragma unroll 8  // eight broadcast loads in flight (R is up to 136 rows)
           for (int rr = 0; rr < R; ++rr) {
             const int f = rt.ids[rr];
             less += (f >= 0 && f < e);
@@ -540,19 +552,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
         if (rt.first[r] > 0) {
           const int e = rt.ids[r];
           int a = 0;
+#pragma unroll 8
           for (int rr = 0; rr < R; ++rr) a += (rt.first[rr] > 0 && rt.ids[rr] < e);
           rt.act_e[a] = e;
           rt.act_off[a] = rt.first[r] - 1;
         }
       }
-      if (tid == 0) {
-        int U = 0, Rv = 0;
-        for (int r = 0; r < R; ++r) {
-          U += rt.first[r] > 0;
-          Rv += rt.ids[r] >= 0;
+      {  // active experts and routed rows, counted by the barrier itself (R <= kConsumers)
+        const int U = consumer_popc(tid < R && rt.first[tid] > 0);
+        const int Rv = consumer_popc(tid < R && rt.ids[tid] >= 0);
+        if (tid == 0) {
+          rt.misc[0] = U;
+          rt.act_off[U] = Rv;
         }
-        rt.misc[0] = U;
-        rt.act_off[U] = Rv;
       }
       consumer_sync();
       stamp(p, 11);
