@@ -124,3 +124,37 @@ def test_dense_layer(T):
     o32 = out_f32.cpu().numpy().astype(np.float64)
     ma, rl = max_abs(o32, ref["out"]), rel_l2(o32, ref["out"])
     assert ma <= MAX_ABS and rl <= REL_L2, f"T={T}: max-abs {ma:.3g} rel-L2 {rl:.3g}"
+
+
+@pytest.mark.parametrize("T", [1, 16])
+def test_shared_expert_prenorm_step_and_graph_replay(T):
+    """A pre-norm stack step on a shared-expert layer (fused at T = 1, unfused at
+    T = 16): the RMSNorm'd input and the output against the oracle fed the same
+    bf16 normalised rows, then the same step replayed from a CUDA graph."""
+    t, lay = shared_layer()
+    x_bits = synth.activations(600 + T, T, D)
+    x = torch_bf16_from_bits(x_bits)
+    ws = bm.moe_workspace(lay, T)
+    xh = torch.empty_like(x)
+    o32 = torch.empty((T, D), dtype=torch.float32, device="cuda")
+    ids = torch.empty((T, K + 1), dtype=torch.int32, device="cuda")
+    out = bm.moe_forward_prenorm(x, lay, ws, out_f32=o32, xh_out=xh, ids_out=ids)
+    torch.cuda.synchronize()
+    assert bm.bitmoe_get_device_status(ws) == 0
+    xh_bits = bits_from_torch_bf16(xh)
+    assert np.array_equal(xh_bits, oracle.f64_to_bf16(oracle.rmsnorm(x_bits)))
+    ref = oracle.moe_forward(xh_bits, t, K, resid=x_bits, n_shared=1)
+    sure = ref["gap"] >= NEAR_TIE
+    assert np.array_equal(ids.cpu().numpy()[sure], ref["ids"][sure])
+    if np.all(sure):
+        got = o32.cpu().numpy().astype(np.float64)
+        assert max_abs(got, ref["out"]) <= MAX_ABS and rel_l2(got, ref["out"]) <= REL_L2
+    # graph capture and replay give the same bits
+    out_g = torch.empty_like(x)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        bm.moe_forward_prenorm(x, lay, ws, out=out_g)
+    g.replay()
+    torch.cuda.synchronize()
+    assert bm.bitmoe_get_device_status(ws) == 0
+    assert torch.equal(out_g, out)
