@@ -77,3 +77,28 @@ def test_reference_arm_under_torchrun_prints_once():
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
     assert rec["cpu_baseline"]["kind"] == "oracle"
+
+
+@pytest.mark.parametrize("workload", ["decode", "shared"])
+def test_reference_arm_json_line_keeps_the_contract(workload):
+    """One rank, the oracle arm: one JSON line with the contract's keys, the workload's
+    name and routing, a bounded oracle sample and a zero-copy e2e record."""
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--workload", workload, "--steps", "1",
+           "--warmup", "1", "--cpu-seconds", "0.25"]
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in rec, key
+    assert rec["impl"] == "reference" and rec["unit"] == "tokens/s" and rec["value"] > 0
+    assert rec["cpu_baseline"]["kind"] == "oracle" and rec["cpu_baseline"]["cores"] >= 1
+    assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["e2e"]["value"] == rec["value"]
+    cfg = rec["config"]
+    if workload == "shared":
+        assert cfg["workload"] == "moe_layer_shared_decode_batch1" and cfg["top_k"] == 6 and cfg["n_shared"] == 1
+    else:
+        assert cfg["workload"] == "moe_layer_decode_batch1" and cfg["top_k"] == 8 and cfg["n_shared"] == 0
