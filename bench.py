@@ -6,15 +6,25 @@ fp32 router with an N(0,1) per-expert bias), a fresh seeded token every step.
 A "step" is one token through the whole layer: router, top-k, grouping, the
 eight expert FFNs and the combine into the residual.
 
-Inputs larger than L2: the step cycles through 64 independently seeded copies
+Inputs larger than L2: the steps cycle through 64 independently seeded copies
 of the layer (29 GB of weights), so no step finds its weights in the 126 MB L2.
-Timing: CUDA graph of 64 steps, replayed; CUDA events on the launching stream
-around the timed replays, barrier + synchronize on both sides, max over ranks.
+
+Timing.  W warm-up steps, then a timed region of exactly K steps (``--steps``),
+captured as CUDA graphs.  Short regions say little on their own, so the region
+is repeated back to back until at least 0.4 s of GPU time has been timed; each
+repetition is bracketed by CUDA events on the launching stream and the median
+repetition is reported (``timing`` in the JSON line gives the count and the
+spread).  Successive repetitions replay graphs that start at different layer
+copies, so a repetition never finds the previous one's weights in L2.  A barrier
+and a device synchronisation bracket the whole timed part; the clock sampler runs
+from before the warm-up to after the last repetition.
 
 Other workloads (``--workload``): ``batch`` (T tokens per step, Zipf(1.1)
 router skew), ``prefill`` (T=4096 chunk, Zipf skew), ``stack`` (49 layers +
-RMSNorm + int4 LM head + argmax).  ``--impl reference`` times the fp64 CPU
-oracle on a bounded sample of the same workload.
+RMSNorm + int4 LM head + argmax), ``shared`` (the pages' routing: top-6 of 256
+plus one shared expert), ``lmhead`` (the int4 LM head alone, V = 131072).
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same
+workload.
 """
 from __future__ import annotations
 
@@ -33,26 +43,40 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer decode tokens/s on 1 B300; achieved HBM GB/s vs ~8 TB/s roofline"
+PREFILL_METRIC = "MoE-layer prefill tokens/s on 1 B300; grouped-GEMM TFLOP/s vs dense 16-bit tensor peak"
+STACK_METRIC = "49-layer MoE stack + int4 LM head decode tokens/s on 1 B300; achieved HBM GB/s"
+LMHEAD_METRIC = "int4 LM-head GEMV + argmax tokens/s on 1 B300; achieved HBM GB/s"
 D, E, K_TOP, I_FF, V = 2048, 256, 8, 512, 131072
 EXPERT_BYTES = 3 * I_FF * D * 9 // 16          # int4 + fp16 group scales of one expert (gate, up, down)
 ROUTER_BYTES = E * D * 4 + E * 4               # fp32 router weight + bias
 LM_BYTES = V * D * 9 // 16
 K_SHARED = 6                                   # routed experts per token beside the shared expert
+MIN_TIMED_S = 0.4                              # GPU time the repeated timed region adds up to, at least
+DEFAULT_STEPS = {"decode": 2000, "shared": 2000, "batch": 500, "prefill": 20, "stack": 50, "lmhead": 500}
+DEFAULT_WARMUP = {"decode": 200, "shared": 200, "batch": 50, "prefill": 5, "stack": 5, "lmhead": 50}
 
 
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=10000)
-    p.add_argument("--warmup", type=int, default=256)
+    p.add_argument("--steps", type=int, default=None, help="steps in one timed region (per-workload default)")
+    p.add_argument("--warmup", type=int, default=None, help="untimed warm-up steps (per-workload default, >= 3)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--workload", default="decode", choices=["decode", "batch", "prefill", "stack", "shared"],
+    p.add_argument("--workload", default="decode",
+                   choices=["decode", "batch", "prefill", "stack", "shared", "lmhead"],
                    help="shared: batch-1 decode with the pages' routing, top-6 of 256 plus one shared expert")
-    p.add_argument("--T", type=int, default=None, help="tokens per step (batch / prefill / stack)")
+    p.add_argument("--T", type=int, default=None, help="tokens per step (batch / prefill / stack / lmhead)")
     p.add_argument("--copies", type=int, default=64, help="independent layer copies cycled per step")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
-    return p.parse_args()
+    a = p.parse_args()
+    if a.steps is None:
+        a.steps = DEFAULT_STEPS[a.workload]
+    if a.warmup is None:
+        a.warmup = DEFAULT_WARMUP[a.workload]
+    a.steps = max(1, a.steps)
+    a.warmup = max(3, a.warmup)
+    return a
 
 
 # ---------------------------------------------------------------- helpers
@@ -77,12 +101,14 @@ def kernel_source_hash(kernel):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel, units=1.0):
-    """DRAM bytes (read + write) per launch from the ncu summary of `kernel`, scaled by
-    `units` (launch size / captured size), or None when absent or stale."""
+def profiled_traffic(kernel, units=1.0, workload=None):
+    """DRAM bytes (read + write) per launch from the ncu summary of `kernel` (for
+    `workload`, when given), scaled by `units` (launch size / captured size), or
+    None when absent or stale."""
     import glob
     want = kernel_source_hash(kernel)
-    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", f"{kernel}*.md"))):
+    pat = f"{kernel}__{workload}.md" if workload else f"{kernel}*.md"
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", pat))):
         vals = {}
         for line in open(path):
             if line.startswith("- ") and " = " in line:
@@ -102,7 +128,8 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
+    """nvidia-smi clock / throttle sampling, started before the warm-up and stopped
+    after the last timed region."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -111,6 +138,7 @@ class ClockSampler:
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.lines = []
 
     def __enter__(self):
         try:
@@ -119,13 +147,11 @@ class ClockSampler:
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
-        time.sleep(0.3)
         return self
 
     def __exit__(self, *a):
         self.lines = []
         if self.proc is not None:
-            time.sleep(0.25)
             self.proc.terminate()
             try:
                 out, _ = self.proc.communicate(timeout=5)
@@ -135,24 +161,28 @@ class ClockSampler:
             self.lines = [l for l in out.splitlines() if l.strip()]
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
+        """Median SM clock over the samples taken under load (power above the idle
+        draw), the maximum clock, and every throttle reason seen."""
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in getattr(self, "lines", []):
+        for l in self.lines:
             f = [x.strip() for x in l.split(",")]
             if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                rows.append((float(f[1]), float(f[2]), float(f[3]), [n for n, v in zip(names, f[5:9])
+                                                                      if v.lower() == "active"]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        pw = [r[2] for r in rows]
+        cut = min(pw) + 0.25 * (max(pw) - min(pw))
+        busy = [r for r in rows if r[2] >= cut] or rows
+        reasons = sorted({n for r in rows for n in r[3]})
+        return {"sm_mhz": statistics.median(r[0] for r in busy), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(busy),
+                "power_w_max": max(pw)}
 
 
 def dist_setup(args):
@@ -201,6 +231,101 @@ def job_throughput(units, ms, world):
     return sum_over_ranks(units, world) / (max_over_ranks(ms, world) / 1e3)
 
 
+def capture(fn):
+    """fn() captured into a CUDA graph (its launches only; nothing runs)."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def region_graphs(step, K, n_graphs):
+    """n_graphs CUDA graphs of exactly K steps each; graph j runs step(j*K + i) for
+    i = 0..K-1, so successive regions continue the step sequence."""
+    def body(j):
+        def f():
+            for i in range(K):
+                step(j * K + i)
+        return f
+    return [capture(body(j)) for j in range(n_graphs)]
+
+
+def run_warmup(step, W):
+    """W untimed steps (eager launches)."""
+    import torch
+    for i in range(W):
+        step(i)
+    torch.cuda.synchronize()
+
+
+def time_regions(graphs, world, min_total_s=MIN_TIMED_S, min_regions=5, max_regions=20000):
+    """Replays the K-step region graphs (cycling through them) back to back, each
+    replay between two CUDA events on the current stream, until at least
+    min_total_s of GPU time is timed.  Barrier + synchronize on both sides.
+    Returns the per-region times (ms)."""
+    import torch
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    barrier(world)
+    times, total, batch, j = [], 0.0, min_regions, 0
+    while True:
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(batch + 1)]
+        evs[0].record(stream)
+        for i in range(batch):
+            graphs[j % len(graphs)].replay()
+            j += 1
+            evs[i + 1].record(stream)
+        torch.cuda.synchronize()
+        ts = [evs[i].elapsed_time(evs[i + 1]) for i in range(batch)]
+        times += ts
+        total += sum(ts)
+        if total >= min_total_s * 1e3 or len(times) >= max_regions:
+            break
+        per = total / len(times)
+        batch = int(min(max_regions - len(times), max(min_regions, math.ceil((min_total_s * 1e3 - total) / per))))
+    barrier(world)
+    return times
+
+
+def timing_record(times, K, what):
+    ts = sorted(times)
+    return {"regions": len(ts), "steps_per_region": K, "stat": "median region",
+            "region_ms": {"min": round(ts[0], 5), "median": round(statistics.median(ts), 5), "max": round(ts[-1], 5)},
+            "timed_s": round(sum(ts) / 1e3, 3), "what": what}
+
+
+def n_region_graphs(K, copies):
+    """Enough K-step graphs that consecutive regions start at different layer copies
+    and a copy comes back only after every other one was used (at most 16 graphs)."""
+    return max(1, min(16, math.ceil(copies / K)))
+
+
+def count_kernels(fn):
+    """Kernel launches one call of fn() makes: fn is captured once into a CUDA graph
+    that is kept un-instantiated and whose kernel nodes are counted (0 if unreadable)."""
+    import torch
+    try:
+        from cuda.bindings import runtime as cudart
+        g = torch.cuda.CUDAGraph(keep_graph=True)
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize()
+        cg = cudart.cudaGraph_t(init_value=int(g.raw_cuda_graph()))
+        err, _, n = cudart.cudaGraphGetNodes(cg, 0)
+        err, nodes, n = cudart.cudaGraphGetNodes(cg, n)
+        cnt = 0
+        for nd in nodes[:n]:
+            err, t = cudart.cudaGraphNodeGetType(nd)
+            if t == cudart.cudaGraphNodeType.cudaGraphNodeTypeKernel:
+                cnt += 1
+        del g
+        return cnt
+    except Exception as exc:  # report, do not guess
+        print(f"bench: kernel count unavailable ({exc!r})", file=sys.stderr)
+        return 0
+
+
 # ---------------------------------------------------------------- device weights
 
 
@@ -231,6 +356,33 @@ def make_device_layers(n_layers, seed, bias, device="cuda", k=K_TOP, n_shared=0)
     return layers
 
 
+def make_device_lm_head(seed, device="cuda"):
+    """The int4 LM head [V, D] drawn on the device and packed."""
+    import torch
+
+    import bit_expert_ffn_warp_b300 as bm
+    import synth
+    q = torch.empty(V * D // 2, dtype=torch.uint8, device=device)
+    sc = torch.empty(V * D // 32, dtype=torch.float16, device=device)
+    synth.device_fill_int4(q.data_ptr(), q.numel(), synth.stream_key(seed, synth.TAG["lm_q"], 0))
+    synth.device_fill_scales(sc.data_ptr(), sc.numel(), synth.stream_key(seed, synth.TAG["lm_s"], 0))
+    packed = bm.bitmoe_pack_int4(q.view(V, D // 2), sc.view(V, D // 32))
+    torch.cuda.synchronize()
+    return packed
+
+
+def token_pool(rank, n, T):
+    """n distinct seeded token batches [n, T, D] as bf16 bit patterns (host)."""
+    import synth
+    return np.stack([synth.activations(rank, T, D, step=s) for s in range(n)])
+
+
+def to_bf16(host_bits, pin=False, device="cuda"):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(host_bits).view(np.int16)).view(torch.bfloat16)
+    return t.pin_memory() if pin else t.to(device)
+
+
 # ---------------------------------------------------------------- CPU oracle leg
 
 
@@ -258,389 +410,22 @@ def cpu_oracle_sample(workload, T, seconds, seed=0):
                       f"OpenMP over the {per_call * (k + int(shared))} rows of each call)"}
 
 
-# ---------------------------------------------------------------- our decode workload
-
-
-def bench_decode(args, world, rank):
-    import torch
-
-    import bit_expert_ffn_warp_b300 as bm
+def cpu_lmhead_sample(T, seconds, seed=0):
+    """Oracle LM head on a row sample of the V = 131072 bank, scaled to all rows."""
+    import oracle
     import synth
-
-    shared = args.workload == "shared"
-    T = 1 if args.workload in ("decode", "shared") else (args.T or 8)
-    bias = "normal" if args.workload in ("decode", "shared") else "zipf"
-    G = args.copies
-    k = K_SHARED if shared else K_TOP
-    layers = make_device_layers(G, seed=1 + rank, bias=bias, k=k, n_shared=int(shared))
-    ws = bm.moe_workspace(layers[0], T)
-    stream = torch.cuda.current_stream()
-
-    # fresh token(s) per step: a pool of distinct steps, cycled in chunks of G
-    n_pool = max(G, min(args.steps + args.warmup, 4096))
-    n_pool = (n_pool // G) * G
-    xs_host = np.stack([synth.activations(rank, T, D, step=s) for s in range(n_pool)])  # [P, T, D] bf16 bits
-    xs = torch.from_numpy(xs_host.view(np.int16)).view(torch.bfloat16).cuda()
-    x_slots = torch.empty((G, T, D), dtype=torch.bfloat16, device="cuda")
-    out_slots = torch.empty((G, T, D), dtype=torch.bfloat16, device="cuda")
-    ids_slots = torch.empty((G, T, layers[0].kt), dtype=torch.int32, device="cuda")
-
-    def run_chunk():
-        for g in range(G):
-            bm.moe_forward(x_slots[g], layers[g], ws, out=out_slots[g], ids_out=ids_slots[g])
-
-    # warm the kernels (first launches set shared-memory attributes) then capture
-    x_slots.copy_(xs[:G])
-    run_chunk()
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        run_chunk()
-    torch.cuda.synchronize()
-    launches_per_step = count_kernels(lambda: bm.moe_forward(x_slots[0], layers[0], ws, out=out_slots[0],
-                                                             ids_out=ids_slots[0]))
-
-    n_chunks_w = max(1, math.ceil(args.warmup / G))
-    n_chunks = max(1, math.ceil(args.steps / G))
-    steps = n_chunks * G
-
-    def timed(nc, start_chunk=0):
-        for c in range(nc):
-            base = ((start_chunk + c) * G) % n_pool
-            x_slots.copy_(xs[base:base + G], non_blocking=True)
-            graph.replay()
-
-    timed(n_chunks_w)
-    torch.cuda.synchronize()
-    barrier(world)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        torch.cuda.synchronize()
-        ev0.record(stream)
-        timed(n_chunks, n_chunks_w)
-        ev1.record(stream)
-        torch.cuda.synchronize()
-    barrier(world)
-    ms_local = ev0.elapsed_time(ev1)
-    ms = max_over_ranks(ms_local, world)
-
-    # bytes actually touched per step: unique experts of each step + router + activations
-    ids_all = ids_slots.cpu().numpy()
-    uniq = float(np.mean([len(np.unique(ids_all[g])) for g in range(G)]))
-    step_bytes = uniq * EXPERT_BYTES + ROUTER_BYTES + 2 * T * D * 2
-
-    # e2e through the public call with host buffers: pinned x in, pinned out back, every chunk
-    e2e = bench_decode_e2e(args, graph, x_slots, out_slots, xs_host, G, T, world)
-
-    value = job_throughput(steps * T, ms_local, world)
-    per_step_us = ms * 1e3 / steps
-    hbm, _, _, which = peaks()
-    achieved = step_bytes / (per_step_us * 1e-6) / 1e9
-    res = {
-        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": steps,
-        "warmup": n_chunks_w * G, "ms_per_step": per_step_us / 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int4xbf16->fp32", "data": "synthetic (seeded; weights drawn on device)",
-        "config": {"workload": ("moe_layer_shared_decode_batch1" if shared else
-                                f"moe_layer_decode_T{T}" if T > 1 else "moe_layer_decode_batch1"), "T": T, "d": D,
-                   "E": E, "top_k": k, "n_shared": int(shared), "I": I_FF, "group": 32,
-                   "router_bias": bias, "layer_copies": G,
-                   "l2": f"inputs larger than L2: {G} independently seeded layer copies "
-                         f"({G * ((E + int(shared)) * EXPERT_BYTES + ROUTER_BYTES) / 1e9:.1f} GB) cycled per step",
-                   "parallelism": f"replicas x{world}", "timing": "CUDA graph of 64 steps, events on stream"},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4),
-                     "traffic": profiled_traffic("decode_layer_kernel") if T == 1 and not shared else None,
-                     "kernel": "decode_layer_kernel (the whole layer step, one launch)" if T <= 4
-                     else "whole layer step", "bytes_per_step": int(step_bytes),
-                     "unique_experts_per_step": uniq, "peak_source": which},
-        "gpu_launches": launches_per_step * steps if launches_per_step else None,
-        "e2e": e2e,
-        "clocks": clk.summary(),
-    }
-    return res
-
-
-def count_kernels(fn):
-    """Kernel launches one call of fn() makes: fn is captured once into a CUDA graph
-    that is kept un-instantiated and whose kernel nodes are counted (0 if unreadable)."""
-    import torch
-    try:
-        from cuda.bindings import runtime as cudart
-        g = torch.cuda.CUDAGraph(keep_graph=True)
-        with torch.cuda.graph(g):
-            fn()
-        torch.cuda.synchronize()
-        cg = cudart.cudaGraph_t(init_value=int(g.raw_cuda_graph()))
-        err, _, n = cudart.cudaGraphGetNodes(cg, 0)
-        err, nodes, n = cudart.cudaGraphGetNodes(cg, n)
-        cnt = 0
-        for nd in nodes[:n]:
-            err, t = cudart.cudaGraphNodeGetType(nd)
-            if t == cudart.cudaGraphNodeType.cudaGraphNodeTypeKernel:
-                cnt += 1
-        del g
-        return cnt
-    except Exception as exc:  # report, do not guess
-        print(f"bench: kernel count unavailable ({exc!r})", file=sys.stderr)
-        return 0
-
-
-def bench_decode_e2e(args, graph, x_slots, out_slots, xs_host, G, T, world):
-    import torch
-    stream = torch.cuda.current_stream()
-    n_chunks = max(1, min(math.ceil(args.steps / G), 64))
-    hx = torch.from_numpy(xs_host[:G].view(np.int16)).view(torch.bfloat16).pin_memory()
-    hout = torch.empty((G, T, D), dtype=torch.bfloat16).pin_memory()
-    for _ in range(2):
-        x_slots.copy_(hx, non_blocking=True)
-        graph.replay()
-        hout.copy_(out_slots, non_blocking=True)
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(n_chunks):
-        x_slots.copy_(hx, non_blocking=True)
-        graph.replay()
-        hout.copy_(out_slots, non_blocking=True)
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    steps = n_chunks * G
-    value = job_throughput(steps * T, ev0.elapsed_time(ev1), world)
-    return {"value": round(value, 1), "unit": "tokens/s",
-            "h2d_bytes_per_step": T * D * 2, "d2h_bytes_per_step": T * D * 2,
-            "how": f"per {G}-step chunk: pinned host x -> device, graph replay of moe_forward, out -> pinned host"}
-
-
-# ---------------------------------------------------------------- prefill workload
-
-
-def bench_prefill(args, world, rank):
-    """T-token prefill chunk through one MoE layer (Zipf routing skew)."""
-    import torch
-
-    import bit_expert_ffn_warp_b300 as bm
-    import synth
-
-    T = args.T or 4096
-    G = min(args.copies, 4)
-    layers = make_device_layers(G, seed=1 + rank, bias="zipf")
-    xs = [torch.from_numpy(synth.activations(rank, T, D, step=s).view(np.int16)).view(torch.bfloat16).cuda()
-          for s in range(G)]
-    ws = bm.moe_workspace(layers[0], T)
-    out = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
-    stream = torch.cuda.current_stream()
-    steps = max(1, args.steps)
-    warm = max(3, args.warmup)
-    for s in range(warm):
-        bm.moe_forward(xs[s % G], layers[s % G], ws, out=out)
-    torch.cuda.synchronize()
-    barrier(world)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        torch.cuda.synchronize()
-        ev0.record(stream)
-        for s in range(steps):
-            bm.moe_forward(xs[s % G], layers[s % G], ws, out=out)
-        ev1.record(stream)
-        torch.cuda.synchronize()
-    barrier(world)
-    ms_local = ev0.elapsed_time(ev1)
-    ms = max_over_ranks(ms_local, world) / steps
-
-    # the grouped GEMMs alone (expert FFN call on routed, grouped rows), same inputs
-    ffn_ms, rows_used, active = [], [], []
-    for s in range(G):
-        ids, w = bm.moe_route(xs[s], layers[s], ws)
-        off, rows, inv = bm.moe_permute(ids, layers[s], ws)
-        for _ in range(2):
-            bm.moe_expert_ffn_int4(xs[s], layers[s], off, rows, ws)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        reps = 5
-        for _ in range(reps):
-            bm.moe_expert_ffn_int4(xs[s], layers[s], off, rows, ws)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ffn_ms.append(e0.elapsed_time(e1) / reps)
-        cnt = np.diff(off.cpu().numpy())
-        rows_used.append(int(cnt.sum()))
-        active.append(int((cnt > 0).sum()))
-    flops = 6.0 * T * K_TOP * D * I_FF
-    gemm_ms = float(np.median(ffn_ms))
-    _, bf16_peak, bf16_sus, which = peaks()
-    achieved = flops / (gemm_ms * 1e-3) / 1e12
-    launches_per_step = count_kernels(lambda: bm.moe_forward(xs[0], layers[0], ws, out=out))
-
-    # end to end through the public call: pinned host tokens in, the layer output back, every step
-    x_pin = [torch.from_numpy(synth.activations(rank, T, D, step=s).view(np.int16)).view(torch.bfloat16).pin_memory()
-             for s in range(G)]
-    out_pin = torch.empty((T, D), dtype=torch.bfloat16).pin_memory()
-    x_dev = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
-    e_steps = max(1, min(steps, 20))
-    torch.cuda.synchronize()
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for s_ in range(e_steps):
-        x_dev.copy_(x_pin[s_ % G], non_blocking=True)
-        bm.moe_forward(x_dev, layers[s_ % G], ws, out=out)
-        out_pin.copy_(out, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    e2e = {"value": round(job_throughput(e_steps * T, e0.elapsed_time(e1), world), 1), "unit": "tokens/s",
-           "h2d_bytes_per_step": T * D * 2, "d2h_bytes_per_step": T * D * 2,
-           "how": "per step: pinned host tokens -> device, moe_forward, layer output -> pinned host"}
-    return {
-        "metric": "MoE-layer prefill tokens/s on 1 B300; grouped-GEMM TFLOP/s vs dense 16-bit tensor peak",
-        "value": round(job_throughput(steps * T, ms_local, world), 1), "unit": "tokens/s", "n_gpus": world,
-        "steps": steps,
-        "warmup": warm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "int4->f16 x f16 -> f32", "data": "synthetic (seeded; weights drawn on device)",
-        "config": {"workload": f"moe_layer_prefill_T{T}", "T": T, "d": D, "E": E, "top_k": K_TOP, "I": I_FF,
-                   "router_bias": "zipf(1.1)", "layer_copies": G,
-                   "l2": f"inputs larger than L2: {G} layer copies of {E * EXPERT_BYTES / 1e6:.0f} MB cycled",
-                   "active_experts_mean": float(np.mean(active)), "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16_peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / bf16_peak, 4),
-                     "traffic": profiled_traffic("prefill_gemm_kernel") if T == 4096 else None,
-                     "kernel": "expert FFN grouped GEMMs (x->fp16, gate/up+SwiGLU, down)",
-                     "flops_per_launch": flops, "ms_per_launch": gemm_ms, "peak_source": which + " burst bf16 (fp16 same rate)"},
-        "gpu_launches": launches_per_step * steps if launches_per_step else None,
-        "e2e": e2e,
-        "clocks": clk.summary(),
-    }
-
-
-# ---------------------------------------------------------------- 49-layer stack + LM head
-
-
-N_LAYERS = 49
-
-
-def make_device_lm_head(seed, device="cuda"):
-    """The int4 LM head [V, D] drawn on the device and packed."""
-    import torch
-
-    import bit_expert_ffn_warp_b300 as bm
-    import synth
-    q = torch.empty(V * D // 2, dtype=torch.uint8, device=device)
-    sc = torch.empty(V * D // 32, dtype=torch.float16, device=device)
-    synth.device_fill_int4(q.data_ptr(), q.numel(), synth.stream_key(seed, synth.TAG["lm_q"], 0))
-    synth.device_fill_scales(sc.data_ptr(), sc.numel(), synth.stream_key(seed, synth.TAG["lm_s"], 0))
-    packed = bm.bitmoe_pack_int4(q.view(V, D // 2), sc.view(V, D // 32))
-    torch.cuda.synchronize()
-    return packed
-
-
-def bench_stack(args, world, rank):
-    """One decode step = T tokens through 49 MoE layers (RMSNorm before each, residual
-    kept in bf16, attention replaced by identity), then RMSNorm, the int4 LM head and
-    the arg-max."""
-    import torch
-
-    import bit_expert_ffn_warp_b300 as bm
-    import synth
-
-    T = args.T or 1
-    layers = make_device_layers(N_LAYERS, seed=1 + rank, bias="normal")
-    lm = make_device_lm_head(seed=1 + rank)
-    ws = bm.moe_workspace(layers[0], T)
-    lm_ws = bm.lmhead_workspace(T, D, V)
-    stream = torch.cuda.current_stream()
-
-    n_pool = max(8, min(args.steps + args.warmup, 1024))
-    xs_host = np.stack([synth.activations(rank, T, D, step=s) for s in range(n_pool)])
-    xs = torch.from_numpy(xs_host.view(np.int16)).view(torch.bfloat16).cuda()
-    x_slot = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
-    resid = torch.empty_like(x_slot)
-    xh = torch.empty_like(x_slot)
-    am = torch.empty(T, dtype=torch.int32, device="cuda")
-    ids = torch.empty((N_LAYERS, T, K_TOP), dtype=torch.int32, device="cuda")
-
-    def step():
-        resid.copy_(x_slot)
-        for l in range(N_LAYERS):  # RMSNorm inside the layer step, residual updated in place
-            bm.moe_forward_prenorm(resid, layers[l], ws, out=resid, ids_out=ids[l])
-        bm.bitmoe_rmsnorm(resid, out=xh)
-        bm.lmhead_int4_gemv(xh, lm, V, lm_ws, want_logits=False, argmax=am)
-
-    x_slot.copy_(xs[0])
-    step()
-    torch.cuda.synchronize()
-    launches_per_step = count_kernels(step)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        step()
-    torch.cuda.synchronize()
-
-    def run(n, first):
-        for i in range(n):
-            x_slot.copy_(xs[(first + i) % n_pool], non_blocking=True)
-            graph.replay()
-
-    warm = max(3, args.warmup)
-    steps = max(1, args.steps)
-    run(warm, 0)
-    torch.cuda.synchronize()
-    barrier(world)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        torch.cuda.synchronize()
-        ev0.record(stream)
-        run(steps, warm)
-        ev1.record(stream)
-        torch.cuda.synchronize()
-    barrier(world)
-    ms_local = ev0.elapsed_time(ev1)
-    ms = max_over_ranks(ms_local, world) / steps
-
-    # bytes touched per step: the unique experts of every layer (last step), routers, LM head
-    ids_np = ids.cpu().numpy()
-    uniq = [len(np.unique(ids_np[l])) for l in range(N_LAYERS)]
-    step_bytes = sum(u * EXPERT_BYTES + ROUTER_BYTES for u in uniq) + LM_BYTES + 2 * T * D * 2 * (N_LAYERS + 1)
-    hbm, _, _, which = peaks()
-    achieved = step_bytes / (ms * 1e-3) / 1e9
-
-    # end to end through the public calls: pinned host tokens in, arg-max back, every step
-    x_pin = torch.from_numpy(xs_host.view(np.int16)).view(torch.bfloat16).pin_memory()
-    am_pin = torch.empty(T, dtype=torch.int32).pin_memory()
-    e_steps = min(steps, 256)
-    torch.cuda.synchronize()
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(e_steps):
-        x_slot.copy_(x_pin[i % n_pool], non_blocking=True)
-        graph.replay()
-        am_pin.copy_(am, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    e_value = job_throughput(e_steps * T, e0.elapsed_time(e1), world)
-
-    return {
-        "metric": "49-layer MoE stack + int4 LM head decode tokens/s on 1 B300; achieved HBM GB/s",
-        "value": round(job_throughput(steps * T, ms_local, world), 1), "unit": "tokens/s", "n_gpus": world,
-        "steps": steps,
-        "warmup": warm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "int4xbf16->fp32", "data": "synthetic (seeded; weights drawn on device)",
-        "config": {"workload": f"moe_stack49_lmhead_T{T}", "T": T, "layers": N_LAYERS, "d": D, "E": E,
-                   "top_k": K_TOP, "I": I_FF, "V": V, "router_bias": "normal",
-                   "l2": f"inputs larger than L2: {N_LAYERS} layers ({N_LAYERS * (E * EXPERT_BYTES + ROUTER_BYTES) / 1e9:.1f}"
-                         f" GB) + LM head {LM_BYTES / 1e6:.0f} MB per step",
-                   "parallelism": f"replicas x{world}", "timing": "CUDA graph of one step, events on stream"},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4), "traffic": None,
-                     "kernel": "whole stack step (49 x pre-norm decode layer, RMSNorm, LM head)",
-                     "bytes_per_step": int(step_bytes), "unique_experts_per_layer_mean": float(np.mean(uniq)),
-                     "peak_source": which},
-        "gpu_launches": launches_per_step * steps if launches_per_step else None,
-        "e2e": {"value": round(e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": T * D * 2,
-                "d2h_bytes_per_step": T * 4,
-                "how": "per step: pinned host tokens -> device, graph replay, arg-max -> pinned host"},
-        "clocks": clk.summary(),
-    }
+    cores = oracle.num_threads()
+    h = synth.activations(seed, T, D)
+    rows, el, n = 4096, 0.0, 0
+    q, s = synth.lm_head(seed, rows, D)
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds or n == 0:
+        oracle.lmhead(h, q, s, want_logits=False)
+        n += 1
+    el = time.perf_counter() - t0
+    per_call = el / n * (V / rows)
+    return {"value": T / per_call, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} passes of T={T} over {rows} of {V} rows ({el:.1f} s), scaled to {V} rows; fp64, OpenMP"}
 
 
 def cpu_stack_sample(T, seconds, seed=0):
@@ -670,67 +455,430 @@ def cpu_stack_sample(T, seconds, seed=0):
                       f"on {rows} of {V} rows scaled to {V} ({t_lm * 1e3:.1f} ms); fp64, OpenMP"}
 
 
+# ---------------------------------------------------------------- decode workloads
+
+
+def bench_decode(args, world, rank):
+    import torch
+
+    import bit_expert_ffn_warp_b300 as bm
+
+    shared = args.workload == "shared"
+    T = 1 if args.workload in ("decode", "shared") else (args.T or 8)
+    bias = "normal" if args.workload in ("decode", "shared") else "zipf"
+    G = args.copies
+    k = K_SHARED if shared else K_TOP
+    K, W = args.steps, args.warmup
+    layers = make_device_layers(G, seed=1 + rank, bias=bias, k=k, n_shared=int(shared))
+    ws = bm.moe_workspace(layers[0], T)
+    kt = layers[0].kt
+
+    ng = n_region_graphs(K, G)
+    n_pool = min(max(K * ng, W, G), 4096)
+    xs_host = token_pool(rank, n_pool, T)                      # [P, T, D] bf16 bits
+    xs = to_bf16(xs_host)
+    out_slots = torch.empty((G, T, D), dtype=torch.bfloat16, device="cuda")
+    ids_slots = torch.zeros((G, T, kt), dtype=torch.int32, device="cuda")
+
+    def step(s):
+        g = s % G
+        bm.moe_forward(xs[s % n_pool], layers[g], ws, out=out_slots[g], ids_out=ids_slots[g])
+
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        run_warmup(step, W)
+        graphs = region_graphs(step, K, ng)
+        times = time_regions(graphs, world)
+    ms_local = statistics.median(times)
+    launches_per_step = count_kernels(lambda: step(0))
+
+    # bytes actually touched per step: unique experts of each step + router + activations
+    ids_all = ids_slots.cpu().numpy()
+    uniq = float(np.mean([len(np.unique(ids_all[g])) for g in range(G)]))
+    step_bytes = uniq * EXPERT_BYTES + ROUTER_BYTES + 2 * T * D * 2
+
+    e2e = bench_decode_e2e(args, layers, ws, xs_host, T, world, K, ng)
+
+    value = job_throughput(K * T, ms_local, world)
+    per_step_us = max_over_ranks(ms_local, world) * 1e3 / K
+    hbm, _, _, which = peaks()
+    achieved = step_bytes / (per_step_us * 1e-6) / 1e9
+    name = ("moe_layer_shared_decode_batch1" if shared else
+            f"moe_layer_decode_T{T}" if T > 1 else "moe_layer_decode_batch1")
+    fused = T <= 8
+    return {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": per_step_us / 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int4xbf16->fp32", "data": "synthetic (seeded; weights drawn on device)",
+        "config": {"workload": name, "T": T, "d": D, "E": E, "top_k": k, "n_shared": int(shared), "I": I_FF,
+                   "group": 32, "router_bias": bias, "layer_copies": G,
+                   "l2": f"inputs larger than L2: {G} independently seeded layer copies "
+                         f"({G * ((E + int(shared)) * EXPERT_BYTES + ROUTER_BYTES) / 1e9:.1f} GB) cycled step by step",
+                   "parallelism": f"replicas x{world}"},
+        "timing": timing_record(times, K, f"CUDA graphs of {K} moe_forward steps, {ng} graph(s) in rotation"),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4),
+                     "traffic": profiled_traffic("decode_layer_kernel", workload=name) if fused else None,
+                     "kernel": "decode_layer_kernel (the whole layer step, one launch)" if fused
+                     else "whole layer step", "bytes_per_step": int(step_bytes),
+                     "unique_experts_per_step": uniq, "peak_source": which + " (copy, burst)"},
+        "gpu_launches": launches_per_step * K if launches_per_step else None,
+        "e2e": e2e,
+        "clocks": clk.summary(),
+    }
+
+
+def bench_decode_e2e(args, layers, ws, xs_host, T, world, K, ng):
+    """The same steps through moe_forward with host buffers: every step copies its
+    token(s) from pinned host memory to the device and its output back."""
+    import torch
+
+    import bit_expert_ffn_warp_b300 as bm
+    G = len(layers)
+    n_pool = xs_host.shape[0]
+    hx = to_bf16(xs_host, pin=True)
+    hout = torch.empty((n_pool, T, D), dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty((G, T, D), dtype=torch.bfloat16, device="cuda")
+    od = torch.empty((G, T, D), dtype=torch.bfloat16, device="cuda")
+
+    def step(s):
+        g = s % G
+        xd[g].copy_(hx[s % n_pool], non_blocking=True)
+        bm.moe_forward(xd[g], layers[g], ws, out=od[g])
+        hout[s % n_pool].copy_(od[g], non_blocking=True)
+
+    run_warmup(step, 3)
+    times = time_regions(region_graphs(step, K, ng), world)
+    return {"value": round(job_throughput(K * T, statistics.median(times), world), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": T * D * 2, "d2h_bytes_per_step": T * D * 2,
+            "how": "every step: pinned host token(s) -> device, moe_forward, layer output -> pinned host "
+                   "(graph-captured copies); median of repeated K-step regions",
+            "regions": len(times)}
+
+
+# ---------------------------------------------------------------- prefill workload
+
+
+def bench_prefill(args, world, rank):
+    """T-token prefill chunk through one MoE layer (Zipf routing skew)."""
+    import torch
+
+    import bit_expert_ffn_warp_b300 as bm
+
+    T = args.T or 4096
+    G = min(args.copies, 4)
+    K, W = args.steps, args.warmup
+    layers = make_device_layers(G, seed=1 + rank, bias="zipf")
+    xs_host = token_pool(rank, G, T)
+    xs = to_bf16(xs_host)
+    ws = bm.moe_workspace(layers[0], T)
+    out = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+
+    def step(s):
+        bm.moe_forward(xs[s % G], layers[s % G], ws, out=out)
+
+    # the grouped GEMMs alone: the expert-FFN call on routed, grouped rows, same inputs
+    groups = []
+    for s in range(G):
+        ids, w = bm.moe_route(xs[s], layers[s], ws)
+        off, rows, inv = bm.moe_permute(ids, layers[s], ws)
+        groups.append((off, rows))
+    torch.cuda.synchronize()
+    y_rows = torch.empty((T * K_TOP, D), dtype=torch.float32, device="cuda")
+
+    def ffn_step(s):
+        off, rows = groups[s % G]
+        bm.moe_expert_ffn_int4(xs[s % G], layers[s % G], off, rows, ws, y_out=y_rows)
+
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        run_warmup(step, W)
+        times = time_regions(region_graphs(step, K, 1), world)
+        run_warmup(ffn_step, 3)
+        ffn_times = time_regions(region_graphs(ffn_step, K, 1), world)
+    ms_local = statistics.median(times)
+    ms = max_over_ranks(ms_local, world) / K
+    gemm_ms = max_over_ranks(statistics.median(ffn_times), world) / K
+    cnt = [np.diff(g[0].cpu().numpy()) for g in groups]
+    flops = 6.0 * T * K_TOP * D * I_FF
+    _, bf16_peak, bf16_sus, which = peaks()
+    achieved = flops / (gemm_ms * 1e-3) / 1e12
+    launches_per_step = count_kernels(lambda: step(0))
+
+    # end to end through the public call: pinned host tokens in, the layer output back, every step
+    x_pin = to_bf16(xs_host, pin=True)
+    out_pin = torch.empty((T, D), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+
+    def e2e_step(s):
+        x_dev.copy_(x_pin[s % G], non_blocking=True)
+        bm.moe_forward(x_dev, layers[s % G], ws, out=out)
+        out_pin.copy_(out, non_blocking=True)
+
+    run_warmup(e2e_step, 3)
+    e_times = time_regions(region_graphs(e2e_step, K, 1), world)
+    e2e = {"value": round(job_throughput(K * T, statistics.median(e_times), world), 1), "unit": "tokens/s",
+           "h2d_bytes_per_step": T * D * 2, "d2h_bytes_per_step": T * D * 2,
+           "how": "every step: pinned host tokens -> device, moe_forward, layer output -> pinned host",
+           "regions": len(e_times)}
+    return {
+        "metric": PREFILL_METRIC,
+        "value": round(job_throughput(K * T, ms_local, world), 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int4->f16 x f16 -> f32", "data": "synthetic (seeded; weights drawn on device)",
+        "config": {"workload": f"moe_layer_prefill_T{T}", "T": T, "d": D, "E": E, "top_k": K_TOP, "I": I_FF,
+                   "router_bias": "zipf(1.1)", "layer_copies": G,
+                   "l2": f"inputs larger than L2: {G} layer copies of {E * EXPERT_BYTES / 1e6:.0f} MB cycled",
+                   "active_experts_mean": float(np.mean([(c > 0).sum() for c in cnt])),
+                   "parallelism": f"replicas x{world}"},
+        "timing": timing_record(times, K, f"CUDA graph of {K} moe_forward steps"),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16_peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / bf16_peak, 4),
+                     "traffic": profiled_traffic("prefill_gemm_kernel", workload=f"moe_layer_prefill_T{T}"),
+                     "kernel": "expert FFN grouped GEMMs (gate/up+SwiGLU, down)",
+                     "flops_per_launch": flops, "ms_per_launch": gemm_ms,
+                     "launch_timing": timing_record(ffn_times, K, f"CUDA graph of {K} moe_expert_ffn_int4 calls"),
+                     "peak_source": which + " burst bf16 (fp16 same rate)"},
+        "gpu_launches": launches_per_step * K if launches_per_step else None,
+        "e2e": e2e,
+        "clocks": clk.summary(),
+    }
+
+
+# ---------------------------------------------------------------- 49-layer stack + LM head
+
+
+N_LAYERS = 49
+
+
+def bench_stack(args, world, rank):
+    """One decode step = T tokens through 49 MoE layers (RMSNorm before each, residual
+    kept in bf16, attention replaced by identity), then RMSNorm, the int4 LM head and
+    the arg-max."""
+    import torch
+
+    import bit_expert_ffn_warp_b300 as bm
+
+    T = args.T or 1
+    K, W = args.steps, args.warmup
+    layers = make_device_layers(N_LAYERS, seed=1 + rank, bias="normal")
+    lm = make_device_lm_head(seed=1 + rank)
+    ws = bm.moe_workspace(layers[0], T)
+    lm_ws = bm.lmhead_workspace(T, D, V)
+
+    n_pool = max(8, min(K + W, 1024))
+    xs_host = token_pool(rank, n_pool, T)
+    xs = to_bf16(xs_host)
+    resid = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+    xh = torch.empty_like(resid)
+    am = torch.empty(T, dtype=torch.int32, device="cuda")
+    ids = torch.empty((N_LAYERS, T, K_TOP), dtype=torch.int32, device="cuda")
+
+    def layers_and_head():
+        for l in range(N_LAYERS):  # RMSNorm inside the layer step, residual updated in place
+            bm.moe_forward_prenorm(resid, layers[l], ws, out=resid, ids_out=ids[l])
+        bm.bitmoe_rmsnorm(resid, out=xh)
+        bm.lmhead_int4_gemv(xh, lm, V, lm_ws, want_logits=False, argmax=am)
+
+    def step(s):
+        resid.copy_(xs[s % n_pool])
+        layers_and_head()
+
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        run_warmup(step, W)
+        times = time_regions(region_graphs(step, K, 1), world)
+    ms_local = statistics.median(times)
+    ms = max_over_ranks(ms_local, world) / K
+    launches_per_step = count_kernels(layers_and_head)
+
+    # bytes touched per step: the unique experts of every layer (last step), routers, LM head
+    ids_np = ids.cpu().numpy()
+    uniq = [len(np.unique(ids_np[l])) for l in range(N_LAYERS)]
+    step_bytes = sum(u * EXPERT_BYTES + ROUTER_BYTES for u in uniq) + LM_BYTES + 2 * T * D * 2 * (N_LAYERS + 1)
+    hbm, _, _, which = peaks()
+    achieved = step_bytes / (ms * 1e-3) / 1e9
+
+    # end to end through the public calls: pinned host tokens in, arg-max back, every step
+    x_pin = to_bf16(xs_host, pin=True)
+    am_pin = torch.empty((n_pool, T), dtype=torch.int32).pin_memory()
+
+    def e2e_step(s):
+        resid.copy_(x_pin[s % n_pool], non_blocking=True)
+        layers_and_head()
+        am_pin[s % n_pool].copy_(am, non_blocking=True)
+
+    run_warmup(e2e_step, 3)
+    e_times = time_regions(region_graphs(e2e_step, K, 1), world)
+    e_value = job_throughput(K * T, statistics.median(e_times), world)
+
+    return {
+        "metric": STACK_METRIC,
+        "value": round(job_throughput(K * T, ms_local, world), 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int4xbf16->fp32", "data": "synthetic (seeded; weights drawn on device)",
+        "config": {"workload": f"moe_stack49_lmhead_T{T}", "T": T, "layers": N_LAYERS, "d": D, "E": E,
+                   "top_k": K_TOP, "I": I_FF, "V": V, "router_bias": "normal",
+                   "l2": f"inputs larger than L2: {N_LAYERS} layers ({N_LAYERS * (E * EXPERT_BYTES + ROUTER_BYTES) / 1e9:.1f}"
+                         f" GB) + LM head {LM_BYTES / 1e6:.0f} MB per step",
+                   "parallelism": f"replicas x{world}"},
+        "timing": timing_record(times, K, f"CUDA graph of {K} stack steps"),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "kernel": "whole stack step (49 x pre-norm decode layer, RMSNorm, LM head)",
+                     "bytes_per_step": int(step_bytes), "unique_experts_per_layer_mean": float(np.mean(uniq)),
+                     "peak_source": which + " (copy, burst)"},
+        "gpu_launches": launches_per_step * K if launches_per_step else None,
+        "e2e": {"value": round(e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": T * D * 2,
+                "d2h_bytes_per_step": T * 4,
+                "how": "every step: pinned host tokens -> device, the stack, arg-max -> pinned host",
+                "regions": len(e_times)},
+        "clocks": clk.summary(),
+    }
+
+
+# ---------------------------------------------------------------- LM head alone
+
+
+def bench_lmhead(args, world, rank):
+    """T tokens through the int4 LM head (V = 131072, 151 MB) and its arg-max."""
+    import torch
+
+    import bit_expert_ffn_warp_b300 as bm
+
+    T = args.T or 1
+    K, W = args.steps, args.warmup
+    n_heads = 4   # 604 MB of LM-head copies cycled: each call streams its 151 MB from HBM
+    heads = [make_device_lm_head(seed=1 + rank + 1000 * c) for c in range(n_heads)]
+    lm_ws = bm.lmhead_workspace(T, D, V)
+    n_pool = 256
+    xs_host = token_pool(rank, n_pool, T)
+    xs = to_bf16(xs_host)
+    am = torch.empty((n_heads, T), dtype=torch.int32, device="cuda")
+
+    def step(s):
+        c = s % n_heads
+        bm.lmhead_int4_gemv(xs[s % n_pool], heads[c], V, lm_ws, want_logits=False, argmax=am[c])
+
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        run_warmup(step, W)
+        times = time_regions(region_graphs(step, K, 1), world)
+    ms_local = statistics.median(times)
+    ms = max_over_ranks(ms_local, world) / K
+    launches_per_step = count_kernels(lambda: step(0))
+    call_bytes = LM_BYTES + T * D * 2 + T * 4
+    hbm, _, _, which = peaks()
+    achieved = call_bytes / (ms * 1e-3) / 1e9
+
+    x_pin = to_bf16(xs_host, pin=True)
+    am_pin = torch.empty((n_pool, T), dtype=torch.int32).pin_memory()
+    xd = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+
+    def e2e_step(s):
+        c = s % n_heads
+        xd.copy_(x_pin[s % n_pool], non_blocking=True)
+        bm.lmhead_int4_gemv(xd, heads[c], V, lm_ws, want_logits=False, argmax=am[c])
+        am_pin[s % n_pool].copy_(am[c], non_blocking=True)
+
+    run_warmup(e2e_step, 3)
+    e_times = time_regions(region_graphs(e2e_step, K, 1), world)
+    name = f"lmhead_V{V}_T{T}"
+    return {
+        "metric": LMHEAD_METRIC,
+        "value": round(job_throughput(K * T, ms_local, world), 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int4xbf16->fp32", "data": "synthetic (seeded; weights drawn on device)",
+        "config": {"workload": name, "T": T, "d": D, "V": V, "group": 32, "lm_head_copies": n_heads,
+                   "l2": f"inputs larger than L2: {n_heads} LM-head copies ({n_heads * LM_BYTES / 1e6:.0f} MB) cycled",
+                   "parallelism": f"replicas x{world}"},
+        "timing": timing_record(times, K, f"CUDA graph of {K} lmhead_int4_gemv calls"),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4),
+                     "traffic": profiled_traffic("lmhead_kernel", workload=name),
+                     "kernel": "lmhead_kernel (+ key clear and arg-max finalise)", "bytes_per_step": call_bytes,
+                     "peak_source": which + " (copy, burst)"},
+        "gpu_launches": launches_per_step * K if launches_per_step else None,
+        "e2e": {"value": round(job_throughput(K * T, statistics.median(e_times), world), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": T * D * 2, "d2h_bytes_per_step": T * 4,
+                "how": "every step: pinned host tokens -> device, lmhead_int4_gemv, arg-max -> pinned host",
+                "regions": len(e_times)},
+        "clocks": clk.summary(),
+    }
+
+
 # ---------------------------------------------------------------- main
+
+
+def reference_arm(args):
+    """The fp64 oracle on the host cores, on this workload, a bounded sample per step."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl = args.workload
+    if wl in ("decode", "shared"):
+        T = 1
+        name = "moe_layer_shared_decode_batch1" if wl == "shared" else "moe_layer_decode_batch1"
+        metric = METRIC
+    elif wl == "batch":
+        T = args.T or 8
+        name, metric = f"moe_layer_decode_T{T}", METRIC
+    elif wl == "prefill":
+        T = args.T or 4096
+        name, metric = f"moe_layer_prefill_T{T}", PREFILL_METRIC
+    elif wl == "lmhead":
+        T = args.T or 1
+        name, metric = f"lmhead_V{V}_T{T}", LMHEAD_METRIC
+    else:
+        T = args.T or 1
+        name, metric = f"moe_stack49_lmhead_T{T}", STACK_METRIC
+    # each timed step is a bounded sample of the workload; the whole run stays within minutes
+    budget = min(max(1.0, 150.0 / max(1, args.steps + args.warmup)) * args.steps, args.cpu_seconds * 4)
+    t0 = time.perf_counter()
+    if wl == "stack":
+        cb = cpu_stack_sample(T, budget)
+    elif wl == "lmhead":
+        cb = cpu_lmhead_sample(T, budget)
+    else:
+        cb = cpu_oracle_sample(wl, T, budget)
+    el = time.perf_counter() - t0
+    cfg = {"workload": name, "T": T, "d": D}
+    if wl == "lmhead":
+        cfg["V"] = V
+    else:
+        cfg.update({"E": E, "top_k": K_SHARED if wl == "shared" else K_TOP, "n_shared": int(wl == "shared"),
+                    "I": I_FF})
+    res = {"metric": metric, "impl": "reference", "value": round(cb["value"], 3), "unit": "tokens/s",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+           "config": cfg, "ms_per_step": 1e3 / cb["value"] * T, "cpu_baseline": cb,
+           "e2e": {"value": round(cb["value"], 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0},
+           "wall_s": round(el, 1)}
+    print(json.dumps(res))
 
 
 def main():
     args = parse()
     if args.impl == "reference":
-        world = int(os.environ.get("WORLD_SIZE", "1"))
-        rank = int(os.environ.get("RANK", "0"))
-        if rank != 0:
-            return
-        if args.workload == "decode":
-            T, name, metric = 1, "moe_layer_decode_batch1", METRIC
-        elif args.workload == "shared":
-            T, name, metric = 1, "moe_layer_shared_decode_batch1", METRIC
-        elif args.workload == "batch":
-            T = args.T or 8
-            name, metric = f"moe_layer_decode_T{T}", METRIC
-        elif args.workload == "prefill":
-            T = args.T or 4096
-            name = f"moe_layer_prefill_T{T}"
-            metric = "MoE-layer prefill tokens/s on 1 B300; grouped-GEMM TFLOP/s vs dense 16-bit tensor peak"
-        else:
-            T = args.T or 1
-            name = f"moe_stack49_lmhead_T{T}"
-            metric = "49-layer MoE stack + int4 LM head decode tokens/s on 1 B300; achieved HBM GB/s"
-        # each timed step is a bounded sample of the workload; the whole run stays within minutes
-        budget = min(max(1.0, 150.0 / max(1, args.steps + args.warmup)) * args.steps, args.cpu_seconds * 4)
-        t0 = time.perf_counter()
-        if args.workload == "stack":
-            cb = cpu_stack_sample(T, budget)
-        else:
-            cb = cpu_oracle_sample(args.workload, T, budget)
-        el = time.perf_counter() - t0
-        res = {"metric": metric, "impl": "reference", "value": round(cb["value"], 3), "unit": "tokens/s",
-               "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
-               "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-               "config": {"workload": name, "T": T, "d": D, "E": E,
-                          "top_k": K_SHARED if args.workload == "shared" else K_TOP,
-                          "n_shared": int(args.workload == "shared"), "I": I_FF},
-               "ms_per_step": 1e3 / cb["value"] * T,
-               "cpu_baseline": cb,
-               "e2e": {"value": round(cb["value"], 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
-                       "d2h_bytes_per_step": 0},
-               "wall_s": round(el, 1)}
-        print(json.dumps(res))
+        reference_arm(args)
         return
 
-    import torch
     world, rank, local = dist_setup(args)
     if args.workload in ("decode", "batch", "shared"):
         res = bench_decode(args, world, rank)
     elif args.workload == "prefill":
         res = bench_prefill(args, world, rank)
+    elif args.workload == "lmhead":
+        res = bench_lmhead(args, world, rank)
     else:
         res = bench_stack(args, world, rank)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
+            T = res["config"]["T"]
             if args.workload == "stack":
-                res["cpu_baseline"] = cpu_stack_sample(res["config"]["T"], args.cpu_seconds)
+                res["cpu_baseline"] = cpu_stack_sample(T, args.cpu_seconds)
+            elif args.workload == "lmhead":
+                res["cpu_baseline"] = cpu_lmhead_sample(T, args.cpu_seconds)
             else:
-                res["cpu_baseline"] = cpu_oracle_sample(args.workload, res["config"]["T"], args.cpu_seconds)
+                res["cpu_baseline"] = cpu_oracle_sample(args.workload, T, args.cpu_seconds)
         print(json.dumps(res))
     if world > 1:
         import torch.distributed as dist

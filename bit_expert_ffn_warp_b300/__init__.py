@@ -269,12 +269,15 @@ def moe_permute(ids, layer: MoeLayer, workspace):
     return offsets, rows, inv
 
 
-def moe_expert_ffn_int4(x, layer: MoeLayer, offsets, sorted_rows, workspace):
+def moe_expert_ffn_int4(x, layer: MoeLayer, offsets, sorted_rows, workspace, y_out=None):
     T = x.shape[0]
     _need(x, torch.bfloat16, (T, layer.d), "x")
     _need(offsets, torch.int32, (layer.Et + 1,), "offsets")
     _need(sorted_rows, torch.int32, (T * layer.kt,), "sorted_rows")
-    y = torch.empty((T * layer.kt, layer.d), dtype=torch.float32, device=x.device)
+    if y_out is None:
+        y = torch.empty((T * layer.kt, layer.d), dtype=torch.float32, device=x.device)
+    else:
+        y = _need(y_out, torch.float32, (T * layer.kt, layer.d), "y_out")
     sh, wt = layer.shape, layer.weights
     _check("moe_expert_ffn_int4", _lib.moe_expert_ffn_int4(_ptr(x), T, ctypes.byref(sh), ctypes.byref(wt),
                                                            _ptr(offsets), _ptr(sorted_rows), _ptr(y),

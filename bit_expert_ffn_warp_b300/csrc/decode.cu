@@ -901,6 +901,20 @@ cudaError_t launch_decode_fused(const DecodeLaunch& L, cudaStream_t s) {
   static int attr_set[64] = {};
   cudaError_t err = ensure_smem_attr(decode_layer_kernel, pl.smem, attr_set);
   if (err != cudaSuccess) return err;
+  // The CTAs wait on each other at the grid barriers, so all G of them must be
+  // resident at once: one per SM.  Checked once per device and shared-memory
+  // size; a device where they do not fit takes the unfused kernels.
+  static size_t occ_ok[64] = {};
+  int dev = 0;
+  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorNotSupported;
+  if (occ_ok[dev] < pl.smem) {
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_layer_kernel, kDecThreads, pl.smem);
+    if (err != cudaSuccess) return err;
+    if ((long)per_sm * sm_count() < G) return cudaErrorNotSupported;
+    occ_ok[dev] = pl.smem;
+  }
 
   DecodeArgs a;
   a.x = L.x;

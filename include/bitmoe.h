@@ -122,7 +122,14 @@ size_t bitmoe_packed_int4_bytes(int64_t n_mats, int64_t rows, int64_t K, int64_t
 /* Reorder a canonical int4 bank (device q, scale) into the packed tile layout
  * the kernels stream: 16-row tiles, each a run of 128-column chunks holding
  * the nibbles of every (row, 32-column group) in the order one mma fragment
- * consumes them, followed by the chunk's fp16 scales.  Off the timed path. */
+ * consumes them, followed by the chunk's fp16 scales.  Off the timed path.
+ * q 4-byte aligned, scale 2-byte aligned; packed: a 16-byte aligned device
+ * buffer of bitmoe_packed_int4_bytes().  The packed bank holds the same bytes as q + scale
+ * (nothing added), so a 4-bit weight with a 16-bit scale per 32 weights costs
+ * 4.5 bits, as the pages' ~23 GB 4-bit release of the 39.8B model implies.
+ * Source: "Flint 40B : Best Mid Sized LLM", transcript 07:15 (four-bit and
+ * integer-four builds, GGUF files around 23 GB); "Recursive_SI's First Model
+ * Unveiled!", section "Quantization" (4-bit weights, the output layer too). */
 bitmoe_status_t bitmoe_pack_int4(const uint8_t* q, const uint16_t* scale, int64_t n_mats, int64_t rows,
                                  int64_t K, int64_t group, uint8_t* packed, void* stream);
 
@@ -156,14 +163,19 @@ bitmoe_status_t moe_route(const uint16_t* x, int64_t T, const bitmoe_moe_shape_t
                           void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * Token -> expert grouping.  Row r = t*kt + j of topk_ids is placed at
+ * Token -> expert grouping (the dispatch step of the mixture-of-experts
+ * kernels).  Row r = t*kt + j of topk_ids is placed at
  * position inv_rows[r]; sorted_rows[p] = r; expert e owns positions
  * [expert_offsets[e], expert_offsets[e+1]); inside one expert the rows keep
  * ascending r (a stable counting sort, so the result is unique).  With
  * Et = E + n_shared bank entries: expert_offsets [Et+1], sorted_rows [T*kt],
  * inv_rows [T*kt], all int32.  Rows whose id is outside [0, Et) are left out
  * (inv_rows[r] = -1) and flag BITMOE_ERR_DEVICE_CHECK in the device status
- * word.
+ * word.  The workspace supplies the counting sort's scratch.
+ * Source: "Flint 40B : Best Mid Sized LLM", transcript 02:35 (each token goes
+ * to six of 256 routed experts) and 06:11 (dedicated kernels for mixture-of-
+ * experts routing); "Recursive_SI's First Model Unveiled!", section "Inference
+ * Kernel" (kernels for MoE operations).
  */
 bitmoe_status_t moe_permute(const int32_t* topk_ids, int64_t T, const bitmoe_moe_shape_t* shape,
                             int32_t* expert_offsets, int32_t* sorted_rows, int32_t* inv_rows, void* workspace,
@@ -185,7 +197,16 @@ bitmoe_status_t moe_expert_ffn_int4(const uint16_t* x, int64_t T, const bitmoe_m
  * Gate-weighted combine into the residual:
  * out_f32[t,c] = residual[t,c] + sum_{j=0}^{kt-1} topk_w[t,j] * y_rows[inv_rows[t*kt+j], c]
  * summed in ascending j in fp32; out [T, d] bf16 = round-to-nearest-even of
- * out_f32.  out_f32 may be NULL.  out may alias residual.
+ * out_f32.  out_f32 may be NULL.  out may alias residual.  y_rows [T*kt, d]
+ * fp32 in grouped order (moe_expert_ffn_int4's output); inv_rows and topk_w
+ * [T*kt]; residual [T, d] bf16; all 16-byte aligned except inv_rows / topk_w.
+ * A row whose inv_rows entry is negative (left out by moe_permute) adds
+ * nothing.  No workspace.
+ * Source: "Flint 40B : Best Mid Sized LLM", transcript 02:35 (a token's output
+ * is the mix of the experts the router chose for it) and 06:11 (mixture-of-
+ * experts kernels); "Recursive_SI's First Model Unveiled!", section "Inference
+ * Kernel" (kernels for MoE operations).  The gate-weighted sum is the plain
+ * reading of a top-k mixture; the pages print no formula.
  */
 bitmoe_status_t moe_combine(const float* y_rows, const int32_t* inv_rows, const float* topk_w,
                             const uint16_t* residual, int64_t T, const bitmoe_moe_shape_t* shape, uint16_t* out,
@@ -200,6 +221,17 @@ bitmoe_status_t moe_combine(const float* y_rows, const int32_t* inv_rows, const 
  * not x.  Batches of T <= 8 tokens run one fused decode kernel, other batches
  * with T*k < 512 routed rows the streaming kernels (both exact int4 x bf16 with
  * fp32 sums); T*k >= 512 runs the tcgen05 grouped GEMM (fp16 operands).
+ * The fused decode kernel is one persistent launch of one CTA per SM whose
+ * CTAs wait on each other; it runs only where the occupancy query says every
+ * CTA of the grid can be resident at once (else the call takes the unfused
+ * kernels), and it should not share the device with concurrent kernels that
+ * occupy SMs for long (its CTAs would then wait, up to the 2 s limit, for SMs
+ * that another kernel holds).
+ * Source: "Flint 40B : Best Mid Sized LLM", transcript 02:35 (the MoE layer:
+ * 256 routed experts, a few per token), 06:11 (kernels for low-bit projections
+ * and mixture-of-experts routing) and 06:43 (the whole decode pass fused into
+ * one launch on Apple GPUs; here one launch per layer step); "Recursive_SI's
+ * First Model Unveiled!", section "Inference Kernel".
  */
 bitmoe_status_t moe_forward(const uint16_t* x, const uint16_t* residual, int64_t T, const bitmoe_moe_shape_t* shape,
                             const bitmoe_moe_weights_t* weights, const int32_t* forced_ids, const float* forced_w,
@@ -213,9 +245,10 @@ bitmoe_status_t moe_forward(const uint16_t* x, const uint16_t* residual, int64_t
  * For T <= 8 the normalisation runs inside the fused decode kernel (no extra
  * launch); other T normalise first into xh_out (or the workspace).  xh_out
  * [T, d] bf16 may be NULL; out may alias residual.  Forced ids/gates as in
- * moe_forward.  Source: "Flint 40B : Best Mid Sized LLM", transcript 03:36
- * (per-layer normalisation in the decoder stack); the stack shape follows the
- * pages' 49-layer decoder with attention left out.
+ * moe_forward.  Source: "Flint 40B : Best Mid Sized LLM", transcript 02:35
+ * (the 49-layer decoder stack of MoE layers) and 03:36 (RMS norm is the
+ * model's normalisation); the pre-norm placement, unit gain and eps are this
+ * library's reading (the pages give none), and attention is left out.
  */
 bitmoe_status_t moe_forward_prenorm(const uint16_t* residual, int64_t T, const bitmoe_moe_shape_t* shape,
                                     const bitmoe_moe_weights_t* weights, float eps, const int32_t* forced_ids,
@@ -259,13 +292,22 @@ bitmoe_status_t lmhead_int4_gemv(const uint16_t* h, int64_t T, int64_t d, int64_
  * (different streams, or different host threads, without ordering between
  * them) race and may return wrong arg-max values.  If a bounded device-side
  * wait runs out, every argmax[t] is set to -1.
+ *
+ * The looked-up address is kept for the life of the process: after
+ * cudaDeviceReset() (or any teardown of the device's primary context) it is
+ * stale, so do not call this entry point on a device that was reset.
  */
 size_t lmhead_static_scratch_bytes(void);
 bitmoe_status_t lmhead_int4_gemv_static(const uint16_t* h, int64_t T, int64_t d, int64_t V, int64_t group,
                                         const uint8_t* w_packed, float* logits, int32_t* argmax, void* stream);
 
 /* RMSNorm with unit gain between stacked layers: y = x / sqrt(mean(x^2) + eps),
- * computed in fp32, rounded to bf16.  x, y [T, d] bf16 (y may alias x). */
+ * computed in fp32, rounded to bf16.  x, y [T, d] bf16, 16-byte aligned
+ * (y may alias x); d % 8 == 0.  No workspace.
+ * Source: "Flint 40B : Best Mid Sized LLM", transcript 03:36 (RMS norm is the
+ * model's normalisation; the page names it for the attention heads).  Its
+ * place before each stacked MoE layer, the unit gain and eps are this
+ * library's reading: the pages give none of them. */
 bitmoe_status_t bitmoe_rmsnorm(const uint16_t* x, int64_t T, int64_t d, float eps, uint16_t* y, void* stream);
 
 #ifdef __cplusplus

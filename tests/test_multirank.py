@@ -79,7 +79,7 @@ def test_reference_arm_under_torchrun_prints_once():
     assert rec["cpu_baseline"]["kind"] == "oracle"
 
 
-@pytest.mark.parametrize("workload", ["decode", "shared"])
+@pytest.mark.parametrize("workload", ["decode", "shared", "lmhead"])
 def test_reference_arm_json_line_keeps_the_contract(workload):
     """One rank, the oracle arm: one JSON line with the contract's keys, the workload's
     name and routing, a bounded oracle sample and a zero-copy e2e record."""
@@ -100,5 +100,32 @@ def test_reference_arm_json_line_keeps_the_contract(workload):
     cfg = rec["config"]
     if workload == "shared":
         assert cfg["workload"] == "moe_layer_shared_decode_batch1" and cfg["top_k"] == 6 and cfg["n_shared"] == 1
+    elif workload == "lmhead":
+        assert cfg["workload"] == "lmhead_V131072_T1" and cfg["V"] == 131072
     else:
         assert cfg["workload"] == "moe_layer_decode_batch1" and cfg["top_k"] == 8 and cfg["n_shared"] == 0
+
+
+def test_clock_summary_counts_only_samples_under_load():
+    """The clocks record: median SM clock over samples drawing well above idle power,
+    and every throttle reason seen in any sample."""
+    sys.path.insert(0, ROOT)
+    import bench
+    cs = bench.ClockSampler(0)
+    idle = "0, 1100, 2032, 200.0, 0x0, Not Active, Not Active, Not Active, Not Active"
+    busy = "0, {}, 2032, 900.0, 0x0, Not Active, Not Active, Not Active, {}"
+    cs.lines = [idle, busy.format(2032, "Not Active"), busy.format(1990, "Active"), busy.format(2032, "Not Active"),
+                idle, "garbage"]
+    s = cs.summary()
+    assert s["sm_mhz"] == 2032 and s["sm_max_mhz"] == 2032 and s["samples"] == 5
+    assert s["samples_under_load"] == 3 and s["reasons"] == ["sw_power_cap"]
+
+
+def test_timing_record_reports_the_median_region():
+    sys.path.insert(0, ROOT)
+    import bench
+    rec = bench.timing_record([3.0, 1.0, 2.0, 2.5, 100.0], 20, "x")
+    assert rec["regions"] == 5 and rec["steps_per_region"] == 20
+    assert rec["region_ms"] == {"min": 1.0, "median": 2.5, "max": 100.0}
+    assert bench.n_region_graphs(20, 64) == 4 and bench.n_region_graphs(2000, 64) == 1
+    assert bench.n_region_graphs(1, 64) == 16
