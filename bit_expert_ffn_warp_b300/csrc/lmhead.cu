@@ -6,27 +6,39 @@
 // (the output layer is a large share of the weights read per token).
 //
 // The bank is 151 MB at V = 131072 and is read once per call, so the kernel is
-// a weight stream: one CTA per SM, a producer warp keeps a ring of 16-row tiles
-// in flight with TMA bulk copies (full / empty mbarriers per stage), eight
-// consumer warps split each tile's 2048 columns, reduce through shared memory
-// and fold every logit into a per-token running arg-max.  The final arg-max is
-// an atomicMax on a 64-bit key (order-preserving logit bits, then the inverted
-// row index so that the lowest row wins ties).
+// a weight stream that has to keep HBM busy: one CTA per SM, a producer warp
+// keeps a ring of 16-row tiles in flight with TMA bulk copies, and each
+// consumer warp owns whole tiles -- it multiplies its tile's 16 rows over the
+// full reduction on its own, so no consumer waits for another.  A warp folds
+// its logits into a per-token running arg-max in registers; at the end the
+// warps' maxima meet in shared memory and one 64-bit atomicMax per token and
+// CTA (order-preserving logit bits, then the inverted row index so that the
+// lowest row wins ties) publishes them.
+//
+// Dequantisation costs more instructions than anything else here, so the
+// weights become fp16 (the magic-number conversion needs one shift per 8
+// nibbles) and the activations are fed to the tensor cores as fp16 too.  To
+// keep every product exact, token t is multiplied by 2^s_t first, s_t chosen
+// so that its largest |h| lands in [2^14, 2^15): a power-of-two scale is
+// exact, the scaled bf16 values fit fp16 without rounding (only elements below
+// 2^-24 of the token's largest would round), and the fp32 logit is scaled back
+// by 2^-s_t, again exactly.
 #include "kernels.h"
 
 namespace bitmoe {
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kLmThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 6;
-constexpr int kLmTok = 16;  // tokens per launch (two n-tiles)
+constexpr int kLmConsumers = 8;                 // consumer warps, each owning whole tiles
+constexpr int kLmThreads = (kLmConsumers + 1) * 32;
+constexpr int kLmTok = 16;                      // tokens per launch (two mma n-tiles)
+constexpr int kLmMaxStages = 16;
+constexpr int kLmSmemBudget = 227 * 1024;
 
 struct LmArgs {
   const uint16_t* h;  // [T, d] bf16, this launch's first token
-  int ntok, d, V, tok0;
+  int ntok, d, V, tok0, nstages;
   const uint8_t* w;
-  float* logits;            // [T_total, V] or null
+  float* logits;             // [T_total, V] or null
   unsigned long long* keys;  // [T_total]
   DevStatus* st;
 };
@@ -45,29 +57,48 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32)); }
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kLmConsumers * 32)); }
+
+// 2^s as a float, exactly, for |s| <= 126.
+__device__ __forceinline__ float pow2i(int s) { return __int_as_float((s + 127) << 23); }
+
+// Shared memory: barriers (256 B), the per-token scale exponents and arg-max
+// partials, the fp16 tokens [8 * NT][d + pad], then the tile ring.
+struct LmSmem {
+  static constexpr int kBars = 0;                                   // full[16], empty[16], xbar
+  static constexpr int kExp = 384;                                  // int [16]
+  static constexpr int kBestV = kExp + 64;                          // float [8 warps][16 tokens]
+  static constexpr int kBestI = kBestV + kLmConsumers * kLmTok * 4; // int   [8 warps][16 tokens]
+  static constexpr int kFail = kBestI + kLmConsumers * kLmTok * 4;  // int
+  static constexpr int kX = 2048;                                   // fp16 tokens
+  __host__ __device__ static int xstride(int d) { return 2 * d + kSmemRowPad; }
+  __host__ __device__ static int ring(int d, int nt) { return kX + ((8 * nt * xstride(d) + 127) / 128) * 128; }
+};
+static_assert((2 * kLmMaxStages + 1) * 8 <= LmSmem::kExp, "lm head barriers");
+static_assert(LmSmem::kFail + 4 <= LmSmem::kX, "lm head smem header");
 
 template <int NT>
 __global__ void __launch_bounds__(kLmThreads, 1) lmhead_kernel(LmArgs p) {
   extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = full + kStages;
-  uint64_t* xbar = empty + kStages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + LmSmem::kBars);
+  uint64_t* empty = full + kLmMaxStages;
+  uint64_t* xbar = empty + kLmMaxStages;
+  int* sexp = reinterpret_cast<int*>(smem + LmSmem::kExp);
+  float* bestv_s = reinterpret_cast<float*>(smem + LmSmem::kBestV);
+  int* besti_s = reinterpret_cast<int*>(smem + LmSmem::kBestI);
+  int* fail_flag = reinterpret_cast<int*>(smem + LmSmem::kFail);
   const int d = p.d;
+  const int xstride = LmSmem::xstride(d);
+  unsigned char* sx = smem + LmSmem::kX;
+  unsigned char* ring = smem + LmSmem::ring(d, NT);
   const int tbytes = (int)tile_bytes(d);
-  const int xstride = 2 * d + kSmemRowPad;
-  unsigned char* stages = smem + 256;
-  unsigned char* sx = stages + (size_t)kStages * tbytes;
-  float* red = reinterpret_cast<float*>(sx + (size_t)kLmTok * xstride);  // [2][8 warps][32][8]
-  float* bestv = red + 2 * kConsumerWarps * 32 * 8;                      // [256]
-  int* besti = reinterpret_cast<int*>(bestv + kConsumerWarps * 32);       // [256]
-  int* fail_flag = besti + kConsumerWarps * 32;
+  const int NS = p.nstages;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
+      mbar_init(&empty[s], 1);  // the one warp that consumed the tile
     }
     mbar_init(xbar, 1);
     fence_mbar_init();
@@ -78,50 +109,113 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_kernel(LmArgs p) {
   const int VT = p.V / kTileRows;
   const int my_tiles = (VT > (int)blockIdx.x) ? (VT - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
 
-  if (warp == kConsumerWarps) {
-    // ---------------- producer
+  if (warp == kLmConsumers) {
+    // ---------------- producer: the tokens, then this CTA's tiles in order
     if (lane == 0) {
       mbar_arrive_expect_tx(xbar, (uint32_t)p.ntok * 2u * d);
       for (int i = 0; i < p.ntok; ++i) bulk_g2s(sx + i * xstride, p.h + (size_t)i * d, 2 * d, xbar);
+      int issued = 0;
       for (int i = 0; i < my_tiles; ++i) {
-        const int s = i % kStages;
-        if (i >= kStages && !mbar_wait(&empty[s], ((i / kStages) - 1) & 1, p.st, 20)) return;
+        const int s = i % NS;
+        if (i >= NS) {
+          // a stage is free once its consumer released it; stop early if a
+          // consumer gave up (it will not release any more stages)
+          bool ok = false;
+          const uint32_t par = ((i / NS) - 1) & 1;
+          const uint64_t t0 = globaltimer_ns();
+          while (!(ok = mbar_try_wait(&empty[s], par))) {
+            if (*(volatile int*)fail_flag) break;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+              record_status(p.st, kStatusTimeout, 20, (int)blockIdx.x);
+              atomicOr(fail_flag, 1);
+              break;
+            }
+          }
+          if (!ok) break;
+        }
         mbar_arrive_expect_tx(&full[s], (uint32_t)tbytes);
         const size_t vt = (size_t)blockIdx.x + (size_t)i * gridDim.x;
-        bulk_g2s(stages + (size_t)s * tbytes, p.w + vt * tbytes, tbytes, &full[s]);
+        bulk_g2s(ring + (size_t)s * tbytes, p.w + vt * tbytes, tbytes, &full[s]);
+        issued = i + 1;
       }
+      // every copy this thread started lands before the CTA can exit
+      for (int n = (issued > NS ? issued - NS : 0); n < issued; ++n)
+        mbar_wait(&full[n % NS], (n / NS) & 1, p.st, 23);
+      mbar_wait(xbar, 0, p.st, 24);
     }
     return;
   }
 
-  // ---------------- consumers
-  const int g = lane >> 2, c = lane & 3;
-  const int nch = d / kChunkK;
-  float best_v = -INFINITY;
-  int best_i = 0x7fffffff;
-  // reducer mapping: consumer thread -> (row, token) of the 16 x 16 tile output
-  const int rrow = tid >> 4, rtok = tid & 15;
-  const int r_nt = rtok >> 3, r_tl = rtok & 7;
-  const int r_lane = (rrow & 7) * 4 + (r_tl >> 1);
-  const int r_idx = r_nt * 4 + ((rrow >= 8) ? 2 : 0) + (r_tl & 1);
-
-  // A wait that runs out sets fail_flag; every consumer reads the flag after
-  // the same barrier, so all of them leave the loop together.
+  // ---------------- consumers: stage the tokens as scaled fp16
   bool ok = mbar_wait(xbar, 0, p.st, 21);
   if (!ok) atomicOr(fail_flag, 1);
-  for (int i = 0; i < my_tiles; ++i) {
-    const int s = i % kStages;
-    if (ok && !mbar_wait(&full[s], (i / kStages) & 1, p.st, 22)) {
-      ok = false;
-      atomicOr(fail_flag, 1);
+  consumer_sync();
+  if (*(volatile int*)fail_flag == 0) {
+    // per token (one warp each, two passes for 16 tokens over 8 warps): largest
+    // |h| -> exponent e; scale 2^(14 - e) puts the largest element in [2^14, 2^15)
+    for (int t = warp; t < p.ntok; t += kLmConsumers) {
+      uint16_t* xr = reinterpret_cast<uint16_t*>(sx + t * xstride);
+      uint32_t m = 0;
+      for (int c = lane * 8; c < d; c += 256) {
+        const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) m = max(m, max(w4[i] & 0x7fffu, (w4[i] >> 16) & 0x7fffu));
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+      // bf16 exponent field of the largest magnitude (0 for an all-zero or
+      // subnormal-only token); both 2^s and 2^-s stay normal floats
+      const int ef = (int)(m >> 7);
+      const int s = (ef == 0) ? 0 : min(126, max(-126, 14 - (ef - 127)));
+      if (lane == 0) sexp[t] = s;
+      const float f = pow2i(s);
+      for (int c = lane * 8; c < d; c += 256) {
+        const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const __half2 h2 = __floats2half2_rn(__uint_as_float(w4[i] << 16) * f,
+                                               __uint_as_float(w4[i] & 0xffff0000u) * f);
+          o[i] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        *reinterpret_cast<uint4*>(xr + c) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
     }
-    const unsigned char* tile = stages + (size_t)s * tbytes;
+  }
+  consumer_sync();
+
+  const int g = lane >> 2, c = lane & 3;
+  const int nch = d / kChunkK;
+  // running arg-max of the lane's token slots: tokens nt*8 + 2c + b, rows g and g+8
+  float best_v[NT][2];
+  int best_i[NT][2];
+  float unscale[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      best_v[nt][b] = -INFINITY;
+      best_i[nt][b] = 0x7fffffff;
+      const int tok = nt * 8 + 2 * c + b;
+      unscale[nt][b] = (tok < p.ntok) ? pow2i(-sexp[tok]) : 0.f;
+    }
+
+  for (int i = warp; i < my_tiles && *(volatile int*)fail_flag == 0; i += kLmConsumers) {
+    const int s = i % NS;
+    if (!mbar_wait(&full[s], (i / NS) & 1, p.st, 22)) {
+      atomicOr(fail_flag, 1);
+      break;
+    }
+    const unsigned char* tile = ring + (size_t)s * tbytes;
     float acc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int j = 0; j < 4; ++j) acc[nt][j] = 0.f;
-    for (int ch = warp; ch < nch; ch += kConsumerWarps) {
+#pragma unroll 2
+    for (int ch = 0; ch < nch; ++ch) {
       const unsigned char* cw = tile + ch * kChunkBytes;
       const uint4 q0 = *reinterpret_cast<const uint4*>(cw + (g * 4 + c) * 16);
       const uint4 q1 = *reinterpret_cast<const uint4*>(cw + ((g + 8) * 4 + c) * 16);
@@ -130,15 +224,11 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_kernel(LmArgs p) {
 #pragma unroll
       for (int gg = 0; gg < 4; ++gg) {
         const int col = (ch * 4 + gg) * kGroup + c * 8;
-        uint32_t a[2][4];
-        const uint32_t w0 = word_at(q0, gg), w1 = word_at(q1, gg);
-#pragma unroll
-        for (int st = 0; st < 2; ++st) {
-          a[st][0] = nib_pair_bf16(w0, 2 * st);
-          a[st][1] = nib_pair_bf16(w1, 2 * st);
-          a[st][2] = nib_pair_bf16(w0, 2 * st + 1);
-          a[st][3] = nib_pair_bf16(w1, 2 * st + 1);
-        }
+        uint32_t p0[4], p1[4];
+        nib_pairs4_f16(word_at(q0, gg), p0);
+        nib_pairs4_f16(word_at(q1, gg), p1);
+        const uint32_t a0[4] = {p0[0], p1[0], p0[1], p1[1]};
+        const uint32_t a1[4] = {p0[2], p1[2], p0[3], p1[3]};
         const float sc0 = scale_at(s0, gg), sc1 = scale_at(s1, gg);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -147,8 +237,8 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_kernel(LmArgs p) {
           if (tok < p.ntok) xb = *reinterpret_cast<const uint4*>(sx + tok * xstride + col * 2);
           const float z[4] = {0.f, 0.f, 0.f, 0.f};
           float dd[4];
-          mma_bf16(dd, a[0], xb.x, xb.y, z);
-          mma_bf16(dd, a[1], xb.z, xb.w, dd);
+          mma_f16(dd, a0, xb.x, xb.y, z);
+          mma_f16(dd, a1, xb.z, xb.w, dd);
           acc[nt][0] = fmaf(sc0, dd[0], acc[nt][0]);
           acc[nt][1] = fmaf(sc0, dd[1], acc[nt][1]);
           acc[nt][2] = fmaf(sc1, dd[2], acc[nt][2]);
@@ -157,38 +247,55 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_kernel(LmArgs p) {
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-    float* my = red + ((size_t)(i & 1) * kConsumerWarps * 32 + warp * 32 + lane) * 8;
+    if (lane == 0) mbar_arrive(&empty[s]);  // every lane has read the stage
+    const int vrow0 = (int)(((size_t)blockIdx.x + (size_t)i * gridDim.x) * kTileRows);
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) my[nt * 4 + j] = (nt < NT) ? acc[nt][j] : 0.f;
-    consumer_sync();
-    if (*(volatile int*)fail_flag) break;
-    if (rtok < p.ntok) {
-      const float* rb = red + (size_t)(i & 1) * kConsumerWarps * 32 * 8;
-      float v = 0.f;
+      for (int j = 0; j < 4; ++j) {
+        const int b = j & 1;
+        const int tok = nt * 8 + 2 * c + b;
+        const int vrow = vrow0 + g + ((j >= 2) ? 8 : 0);
+        if (tok < p.ntok) {
+          const float v = acc[nt][j] * unscale[nt][b];
+          if (p.logits) p.logits[(size_t)(p.tok0 + tok) * p.V + vrow] = v;
+          if (v > best_v[nt][b] || (v == best_v[nt][b] && vrow < best_i[nt][b])) {
+            best_v[nt][b] = v;
+            best_i[nt][b] = vrow;
+          }
+        }
+      }
+  }
+  // the warp's arg-max per token: reduce over the eight row groups g (lanes
+  // with the same c), then over the warps in shared memory
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) v += rb[(w * 32 + r_lane) * 8 + r_idx];
-      const int vrow = (int)(((size_t)blockIdx.x + (size_t)i * gridDim.x) * kTileRows) + rrow;
-      if (p.logits) p.logits[(size_t)(p.tok0 + rtok) * p.V + vrow] = v;
-      if (v > best_v || (v == best_v && vrow < best_i)) {
-        best_v = v;
-        best_i = vrow;
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      float v = best_v[nt][b];
+      int ix = best_i[nt][b];
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, ix, off);
+        if (ov > v || (ov == v && oi < ix)) {
+          v = ov;
+          ix = oi;
+        }
+      }
+      if (g == 0) {
+        bestv_s[warp * kLmTok + nt * 8 + 2 * c + b] = v;
+        besti_s[warp * kLmTok + nt * 8 + 2 * c + b] = ix;
       }
     }
-  }
-  if (*(volatile int*)fail_flag) return;
-  // per-token arg-max over the 16 rows each thread folded, then one atomic per token
-  bestv[tid] = best_v;
-  besti[tid] = best_i;
   consumer_sync();
+  if (*(volatile int*)fail_flag) return;
   if (tid < p.ntok) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-    for (int r = 0; r < kTileRows; ++r) {
-      const float v = bestv[r * 16 + tid];
-      const int ix = besti[r * 16 + tid];
+    for (int w = 0; w < kLmConsumers; ++w) {
+      const float v = bestv_s[w * kLmTok + tid];
+      const int ix = besti_s[w * kLmTok + tid];
       if (v > bv || (v == bv && ix < bi)) {
         bv = v;
         bi = ix;
@@ -206,10 +313,12 @@ __global__ void argmax_finalize_kernel(const unsigned long long* keys, int T, in
   if (t < T) argmax[t] = (int32_t)(0xffffffffu - (uint32_t)(keys[t] & 0xffffffffull));
 }
 
-size_t lm_smem(int d) {
-  return 256 + (size_t)kStages * tile_bytes(d) + (size_t)kLmTok * (2 * d + kSmemRowPad) +
-         (size_t)2 * kConsumerWarps * 32 * 8 * 4 + (size_t)kConsumerWarps * 32 * 8 + 16;
+int lm_stages(int d, int nt) {
+  const int n = (kLmSmemBudget - LmSmem::ring(d, nt)) / (int)tile_bytes(d);
+  return n < kLmMaxStages ? n : kLmMaxStages;
 }
+
+size_t lm_smem(int d, int nt) { return (size_t)LmSmem::ring(d, nt) + (size_t)lm_stages(d, nt) * tile_bytes(d); }
 
 }  // namespace
 
@@ -218,18 +327,19 @@ size_t lmhead_scratch_bytes(int T) { return (size_t)T * sizeof(unsigned long lon
 cudaError_t launch_lmhead(const uint16_t* h, int T, int d, int V, const uint8_t* w_packed, float* logits,
                           int32_t* argmax, void* scratch, DevStatus* st, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
+  if (lm_stages(d, 2) < 2) return cudaErrorNotSupported;  // d too large for two tiles beside the tokens
   unsigned long long* keys = static_cast<unsigned long long*>(scratch);
   cudaError_t err = cudaMemsetAsync(keys, 0, (size_t)T * sizeof(unsigned long long), s);
   if (err != cudaSuccess) return err;
-  const size_t sm = lm_smem(d);
   static int attr1[64] = {}, attr2[64] = {};
-  err = ensure_smem_attr(lmhead_kernel<1>, sm, attr1);
+  err = ensure_smem_attr(lmhead_kernel<1>, lm_smem(d, 1), attr1);
   if (err != cudaSuccess) return err;
-  err = ensure_smem_attr(lmhead_kernel<2>, sm, attr2);
+  err = ensure_smem_attr(lmhead_kernel<2>, lm_smem(d, 2), attr2);
   if (err != cudaSuccess) return err;
   static int sm_count[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (sm_count[dev] == 0) cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
   const int sms = sm_count[dev] > 0 ? sm_count[dev] : 148;
   const int VT = V / kTileRows;
@@ -241,14 +351,16 @@ cudaError_t launch_lmhead(const uint16_t* h, int T, int d, int V, const uint8_t*
     a.d = d;
     a.V = V;
     a.tok0 = t0;
+    const int nt = a.ntok <= 8 ? 1 : 2;
+    a.nstages = lm_stages(d, nt);
     a.w = w_packed;
     a.logits = logits;
     a.keys = keys;
     a.st = st;
-    if (a.ntok <= 8)
-      lmhead_kernel<1><<<grid, kLmThreads, sm, s>>>(a);
+    if (nt == 1)
+      lmhead_kernel<1><<<grid, kLmThreads, lm_smem(d, 1), s>>>(a);
     else
-      lmhead_kernel<2><<<grid, kLmThreads, sm, s>>>(a);
+      lmhead_kernel<2><<<grid, kLmThreads, lm_smem(d, 2), s>>>(a);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }

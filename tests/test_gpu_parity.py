@@ -311,6 +311,30 @@ def test_lmhead_parity(T, V, d):
     assert np.array_equal(am.cpu().numpy()[ok], am_ref[ok])
 
 
+@pytest.mark.parametrize("log2_scale", [40, 17, -20, -60])
+def test_lmhead_parity_extreme_magnitudes(log2_scale):
+    """Tokens far outside fp16's range (or far below it): the kernel feeds the tensor
+    cores fp16 activations scaled by a power of two per token, which must leave the
+    logits those of the unscaled bf16 tokens."""
+    T, V, d = 3, 4096, 2048
+    q, s = synth.lm_head(5, V, d)
+    h = synth.bf16_bits_to_f32(synth.activations(7, T, d)).astype(np.float64) * 2.0 ** log2_scale
+    h[1] *= 2.0 ** -9          # tokens of different magnitude in one call
+    h[2, ::5] *= 2.0 ** -12    # and a wide spread inside one token
+    h_bits = synth.f64_to_bf16_bits(h)
+    logits_ref, am_ref, gap = oracle.lmhead(h_bits, q, s)
+    wp = bm.bitmoe_pack_int4(torch.from_numpy(q).cuda(), torch.from_numpy(s.view(np.float16)).cuda())
+    logits, am = bm.lmhead_int4_gemv(torch_bf16_from_bits(h_bits), wp, V, bm.lmhead_workspace(T, d, V))
+    torch.cuda.synchronize()
+    lg = logits.cpu().numpy().astype(np.float64)
+    for t in range(T):
+        scale = np.max(np.abs(logits_ref[t]))
+        assert np.all(np.isfinite(lg[t]))
+        assert max_abs(lg[t], logits_ref[t]) <= 2e-5 * scale and rel_l2(lg[t], logits_ref[t]) < 1e-6
+    ok = gap >= NEAR_TIE * np.max(np.abs(logits_ref), axis=1)
+    assert np.array_equal(am.cpu().numpy()[ok], am_ref[ok])
+
+
 def test_lmhead_argmax_ties_lowest_row():
     d, V = 256, 64
     q = np.zeros((V, d // 2), np.uint8)

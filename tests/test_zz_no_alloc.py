@@ -12,8 +12,9 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle
 import synth
-from tests.helpers import torch_bf16_from_bits
+from tests.helpers import NEAR_TIE, max_abs, rel_l2, torch_bf16_from_bits
 
 
 @pytest.fixture(scope="module")
@@ -55,3 +56,25 @@ def test_static_lmhead_matches_workspace_lmhead_on_consecutive_calls(bm):
         assert torch.equal(am_only, ref_am), f"call {call}: arg-max without logits differs"
         err = float((logits - ref_logits).abs().max())
         assert err <= 1e-3, f"call {call}: logits max-abs {err}"
+
+
+@pytest.mark.gpu
+def test_static_lmhead_matches_the_oracle_at_full_vocabulary(bm):
+    """The workspace-free LM head against the fp64 oracle directly, at the full
+    V = 131072, two calls in a row (the second must not see the first's scratch)."""
+    import torch
+    d, V = 2048, 131072
+    q, s = synth.lm_head(5, V, d)
+    wp = bm.bitmoe_pack_int4(torch.from_numpy(q).cuda(), torch.from_numpy(s.view(np.float16)).cuda())
+    for T, seed in [(1, 41), (16, 42)]:
+        h_bits = synth.activations(seed, T, d)
+        logits_ref, am_ref, gap = oracle.lmhead(h_bits, q, s)
+        logits = torch.empty((T, V), dtype=torch.float32, device="cuda")
+        am = torch.full((T,), -7, dtype=torch.int32, device="cuda")
+        bm.lmhead_int4_gemv_static(torch_bf16_from_bits(h_bits), wp, V, am, logits)
+        torch.cuda.synchronize()
+        lg = logits.cpu().numpy().astype(np.float64)
+        assert max_abs(lg, logits_ref) < 1e-3 and rel_l2(lg, logits_ref) < 1e-6
+        ok = gap >= NEAR_TIE
+        assert ok.any()
+        assert np.array_equal(am.cpu().numpy()[ok], am_ref[ok])
