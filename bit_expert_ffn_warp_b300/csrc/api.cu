@@ -395,6 +395,7 @@ bitmoe_status_t lmhead_int4_gemv(const uint16_t* h, int64_t T, int64_t d, int64_
   if (group != kGroup || d % kChunkK || V % kTileRows || T > 64 || d > 16384 || V > (int64_t(1) << 30))
     return BITMOE_ERR_UNSUPPORTED;
   if (T == 0) return BITMOE_OK;
+  if (!lmhead_supported((int)d, (int)T)) return BITMOE_ERR_UNSUPPORTED;
   if (!h || !w_packed || !argmax || !aligned16(h) || !aligned16(w_packed)) return BITMOE_ERR_INVALID_ARG;
   if (!workspace || !aligned16(workspace) || workspace_bytes < lmhead_workspace_size(T, d, V))
     return BITMOE_ERR_WORKSPACE;

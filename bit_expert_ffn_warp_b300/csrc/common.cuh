@@ -168,25 +168,43 @@ __device__ __forceinline__ uint32_t nib_pair_f16(uint32_t w, int p) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// (a & b) ^ c in one LOP3 (truth table 0x6A for the operand order a, b, c).
+// The compiler otherwise splits a mask-and-flip into two logic instructions;
+// the constants stay in registers.
+__device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
 // All four fp16 pairs of a word, p = 0..3, with one shift instead of three:
 // an odd pair (nibbles at bits 4..7 of each half) is read in place as
 // 1024 + 16 (q + 8), which fits fp16's 10-bit mantissa, and one fused
 // multiply-add by 1/16 minus 72 leaves q (every step exact).  bf16 has only 7
-// mantissa bits, so it keeps the shifted form of nib_pair_bf16.
+// mantissa bits, so it keeps the shifted form of nib_pair_bf16.  The f16x2
+// constants are bit patterns held in registers (1032 = 0x6408, 1/16 = 0x2C00,
+// -72 = 0xD480), so each step is a single instruction: per 8 weights one
+// shift, four logic ops, two subtracts and two fused multiply-adds.
 __device__ __forceinline__ void nib_pairs4_f16(uint32_t w, uint32_t (&o)[4]) {
-  const __half2 off = __floats2half2_rn(1032.0f, 1032.0f);
-  const __half2 sixteenth = __floats2half2_rn(0.0625f, 0.0625f);
-  const __half2 off_hi = __floats2half2_rn(-72.0f, -72.0f);
+  const uint32_t m_lo = 0x000F000Fu, m_hi = 0x00F000F0u, x_lo = 0x64086408u, x_hi = 0x64806480u;
+  const uint32_t off = 0x64086408u, sixteenth = 0x2C002C00u, off_hi = 0xD480D480u;
 #pragma unroll
   for (int b = 0; b < 2; ++b) {
     const uint32_t v = b ? (w >> 8) : w;
-    uint32_t te = (v & 0x000F000Fu) ^ 0x64086408u;  // 1032 + q
-    uint32_t to = (v & 0x00F000F0u) ^ 0x64806480u;  // 1024 + 16 (q + 8)
-    __half2 he = __hsub2(*reinterpret_cast<__half2*>(&te), off);
-    __half2 ho = __hfma2(*reinterpret_cast<__half2*>(&to), sixteenth, off_hi);
-    o[2 * b] = *reinterpret_cast<uint32_t*>(&he);
-    o[2 * b + 1] = *reinterpret_cast<uint32_t*>(&ho);
+    const uint32_t te = and_xor(v, m_lo, x_lo);  // 1032 + q
+    const uint32_t to = and_xor(v, m_hi, x_hi);  // 1024 + 16 (q + 8)
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(o[2 * b]) : "r"(te), "r"(off));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(o[2 * b + 1]) : "r"(to), "r"(sixteenth), "r"(off_hi));
   }
+}
+
+// D = A B (no accumulator input) for one m16n8k16 fp16 step.
+__device__ __forceinline__ void mma_f16_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
 // ---------------------------------------------------------------- misc

@@ -13,19 +13,33 @@
 // monotonic counter) separate the phases.  Programmatic dependent launch lets
 // the next step's router rows be fetched before this step has drained.
 //
-// Single-warp serial code is slow on this part (a few cycles per dependent
-// instruction), so every phase spreads over the 16 warps:
-//   P0  router logits of this CTA's experts, K split over warps (W_r rows are
-//       fetched before the grid-dependency wait).            -- grid barrier A
-//   P1  every CTA reads all logits and selects top-k per token in parallel:
-//       the k-th largest of the 16 warp maxima bounds the k-th logit from
-//       below, so only the few logits above it are ranked.  Gates, the stable
-//       grouping and the work split follow (identical in every CTA).
+// At batch 1 every phase runs once per launch, so the time goes to dependent
+// latency (global round trips, CTA-wide barriers, instruction fetch) rather
+// than to arithmetic: the phases below keep their serial chains short and their
+// code compact.
+//   P0  router logits of this CTA's experts, one warp per (token, expert) dot
+//       product (W_r rows are fetched before the grid-dependency wait).  While
+//       the grid barrier A is pending, the staged tokens are turned into fp16
+//       scaled by a power of two per token (exact; see below).
+//                                                            -- grid barrier A
+//   P1  every CTA reads all logits and selects top-k per token: the k-th
+//       largest of the 16 warp maxima bounds the k-th logit from below, so only
+//       the few logits above it are ranked; for one token a single warp then
+//       computes the gates and the (one row per expert) grouping, for several
+//       tokens one warp per token selects and the grouping is a rank count.
 //   P2  gate/up units (expert, 16-row tile), one 128-column chunk per warp;
 //       h = silu(a) * u stored as an fp16 hi + lo pair.      -- grid barrier B
 //       (the producer streams the CTA's W_down tiles meanwhile)
 //   P3  16 output columns per CTA: four warps per expert tile (a K quarter
 //       each), then out = resid + sum_j w_j y_j in ascending j.
+//
+// Both projections dequantise int4 to fp16 (the magic-number conversion takes
+// one shift per eight weights, against three for bf16).  The gate/up inputs are
+// bf16 tokens: token t is multiplied by 2^s_t so that its largest |x| lands in
+// [2^14, 2^15), which makes every scaled value an exact fp16 (elements below
+// 2^-24 of the token's largest would round); the fp32 dot products are scaled
+// back by 2^-s_t, exactly, so the projections keep the exact products and fp32
+// sums of the bf16 arithmetic.
 #include "kernels.h"
 
 namespace bitmoe {
@@ -64,6 +78,7 @@ struct DecodeArgs {
   DevStatus* st;
   int nstages;
   int offA, offB, offR, offRing;  // shared-memory carve-up (bytes)
+  int offX16;                      // fp16 tokens, from the start of region A
   unsigned long long* trace;       // optional [grid][kTracePoints] SM-clock stamps
   int prenorm;                     // x holds the residual: route and run the experts on RMSNorm(x)
   float eps;
@@ -101,39 +116,96 @@ __device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-// Grid-wide barrier over the consumer warps of every CTA (called by all
-// consumer threads).  gb[0] is a monotonic arrival counter: every launch calls
-// each barrier once from every CTA, so a launch starts with gb[0] a multiple
-// of gridDim.x and an arrival that returns `old` waits for the next multiple.
-// (A launch that timed out can leave it misaligned; clearing the device
-// status word resets it.)  The release-add publishes the CTA's writes (made
-// CTA-visible by the preceding bar.sync); the acquire fence after the poll
-// makes the other CTAs' writes visible.  Returns false on timeout.
-__device__ bool grid_barrier(unsigned* gb, int* fail, DevStatus* st, int where, const unsigned long long* trace,
-                             int arrived_point) {
+// Grid-wide barrier over the consumer warps of every CTA, in two halves so that
+// a CTA can work between its arrival and its wait.  gb[0] is a monotonic
+// arrival counter: every launch passes each barrier once from every CTA, so a
+// launch starts with gb[0] a multiple of gridDim.x and an arrival that returns
+// `old` waits for the next multiple.  (A launch that timed out can leave it
+// misaligned; clearing the device status word resets it.)  The release-add
+// publishes the CTA's writes (made CTA-visible by the preceding bar.sync); the
+// acquire fence after the poll makes the other CTAs' writes visible.
+//
+// grid_arrive: called by every consumer thread; returns the count to wait for
+// (meaningful in thread 0 only).
+__device__ __forceinline__ unsigned grid_arrive(unsigned* gb, const unsigned long long* trace, int arrived_point) {
   consumer_sync();
+  unsigned target = 0;
   if (threadIdx.x == 0) {
     unsigned old;
     asm volatile("atom.add.release.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(gb) : "memory");
     stamp(trace, arrived_point);
-    const unsigned target = (old / gridDim.x + 1u) * gridDim.x;
-    unsigned v;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(gb) : "memory");
-    if ((int)(v - target) < 0) {
-      const uint64_t t0 = globaltimer_ns();
-      do {
-        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(gb) : "memory");
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-          record_status(st, kStatusTimeout, where, blockIdx.x);
-          *(volatile int*)fail = 1;
-          break;
-        }
-      } while ((int)(v - target) < 0);
-    }
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    target = (old / gridDim.x + 1u) * gridDim.x;
   }
+  return target;
+}
+
+// Bounded poll of thread 0 (out of line: it runs once per barrier).
+__device__ __noinline__ void grid_poll(unsigned* gb, unsigned target, int* fail, DevStatus* st, int where) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(gb) : "memory");
+  if ((int)(v - target) < 0) {
+    const uint64_t t0 = globaltimer_ns();
+    do {
+      asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(gb) : "memory");
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        record_status(st, kStatusTimeout, where, blockIdx.x);
+        *(volatile int*)fail = 1;
+        break;
+      }
+    } while ((int)(v - target) < 0);
+  }
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+// grid_wait: called by every consumer thread after grid_arrive; false on timeout.
+__device__ __forceinline__ bool grid_wait(unsigned* gb, unsigned target, int* fail, DevStatus* st, int where) {
+  if (threadIdx.x == 0) grid_poll(gb, target, fail, st, where);
   consumer_sync();
   return *(volatile int*)fail == 0;
+}
+
+__device__ __forceinline__ bool grid_barrier(unsigned* gb, int* fail, DevStatus* st, int where,
+                                             const unsigned long long* trace, int arrived_point) {
+  const unsigned target = grid_arrive(gb, trace, arrived_point);
+  return grid_wait(gb, target, fail, st, where);
+}
+
+// 2^s as a float, exactly, for |s| <= 126.
+__device__ __forceinline__ float pow2i(int s) { return __int_as_float((s + 127) << 23); }
+
+// Copies the T staged bf16 token rows into fp16 rows of dst, token t scaled by
+// 2^sexp[t] so that its largest magnitude lands in [2^14, 2^15) (exact: bf16
+// values carry 8 significant bits, fp16 holds 11).  One warp per token: warp
+// w of nw handles tokens w, w + nw, ...
+__device__ __noinline__ void stage_tokens_f16(const unsigned char* rows, unsigned char* dst, int T, int d, int xstride,
+                                              int* sexp, int w, int nw, int lane) {
+  for (int t = w; t < T; t += nw) {
+    const uint16_t* xr = reinterpret_cast<const uint16_t*>(rows + t * xstride);
+    uint16_t* xo = reinterpret_cast<uint16_t*>(dst + t * xstride);
+    uint32_t m = 0;
+    for (int c = lane * 8; c < d; c += 256) {
+      const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
+      m = max(m, max(max(v.x & 0x7fffu, v.x >> 16 & 0x7fffu), max(v.y & 0x7fffu, v.y >> 16 & 0x7fffu)));
+      m = max(m, max(max(v.z & 0x7fffu, v.z >> 16 & 0x7fffu), max(v.w & 0x7fffu, v.w >> 16 & 0x7fffu)));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+    const int ef = (int)(m >> 7);  // exponent field of the largest magnitude (0: zero / subnormal only)
+    const int sc = (ef == 0) ? 0 : min(126, max(-126, 14 - (ef - 127)));
+    if (lane == 0) sexp[t] = sc;
+    const float f = pow2i(sc);
+    for (int c = lane * 8; c < d; c += 256) {
+      const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __half2 h2 = __floats2half2_rn(__uint_as_float(w4[i] << 16) * f, __uint_as_float(w4[i] & 0xffff0000u) * f);
+        o[i] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      *reinterpret_cast<uint4*>(xo + c) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
 }
 
 // Float value of an order-preserving arg-max key (inverse of float_order_key).
@@ -168,6 +240,7 @@ struct Routing {  // shared-memory routing tables (identical in every CTA)
   unsigned long long* sel;   // [kDecMaxT][kDecMaxK]
   float* zall;   // [kDecMaxT]
   float* part;   // [kDecWarps] partial sums
+  int* sexp;     // [kDecMaxT] power-of-two scale of each staged fp16 token
   int* misc;     // [0] U, [1] fail flag, [2] candidate count, [3] tau slot
 };
 
@@ -178,7 +251,7 @@ struct Routing {  // shared-memory routing tables (identical in every CTA)
 // Writes the token's rows t*k + j of the routing tables (the shared expert's
 // row, if any, last with weight 1).
 template <int NPER>  // logits per lane: E <= 32 * NPER
-__device__ void warp_topk_token(const float* __restrict__ lrow, int E, int kr, int k, int renorm, int t, int* ids,
+__device__ __noinline__ void warp_topk_token(const float* __restrict__ lrow, int E, int kr, int k, int renorm, int t, int* ids,
                                 float* w, int lane) {
   float v[NPER];
   const int nper = (E + 31) / 32;
@@ -247,6 +320,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
   uint64_t* wrbar = xbar + 1;
   uint64_t* hbar = wrbar + 1;
   unsigned char* regA = smem + p.offA;
+  unsigned char* x16 = smem + p.offA + p.offX16;  // fp16 scaled tokens (P2), beside the bf16 ones
   unsigned char* regB = smem + p.offB;
   unsigned char* ring = smem + p.offRing;
   // kr routed experts per token; k rows per token (the shared expert's row last)
@@ -268,6 +342,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
     int* q = reinterpret_cast<int*>(q8);
     rt.zall = reinterpret_cast<float*>(q); q += kDecMaxT;
     rt.part = reinterpret_cast<float*>(q); q += kDecWarps;
+    rt.sexp = q; q += kDecMaxT;
     rt.ids = q; q += R;
     rt.w = reinterpret_cast<float*>(q); q += R;
     rt.pos = q; q += R;
@@ -311,9 +386,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
   }
   // router bias of the logit this warp's lane 0 writes first (pair = warp), read now
   const int pairs = T * nexp;
-  float bias0 = 0.f;
+  // warps per (token, expert) dot product: the largest power of two that keeps
+  // every pair covered by the 16 consumer warps at once
+  int wpp = 1;
+  while (pairs > 0 && wpp < kDecWarps && wpp * 2 * pairs <= kDecWarps) wpp *= 2;
+  float bias0 = 0.f, biasA = 0.f;
   if (routed && lane == 0 && warp < kDecWarps && warp < pairs && p.b_router != nullptr)
     bias0 = p.b_router[e_lo + warp % nexp];
+  if (routed && wpp > 1 && tid < pairs && p.b_router != nullptr) biasA = p.b_router[e_lo + tid % nexp];
   grid_dep_wait();  // the previous launch on this stream is complete and visible
   stamp(p, 1);
   // residual of this CTA's first output tile, read now so that its latency is
@@ -376,22 +456,27 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
         consumer_sync();  // the partials are read; the normalised rows are in place
       }
     }
+    {  // the zeroed pad row after the fp16 tokens (read by lanes without a token)
+      uint4* pad = reinterpret_cast<uint4*>(x16 + T * xstride);
+      for (int c = tid; c < d / 8; c += kConsumers) pad[c] = make_uint4(0, 0, 0, 0);
+    }
     if (routed && kr > 0) {  // (kr = 0: a dense layer, nothing to score)
       if (nexp > 0) ok = mbar_wait(wrbar, 0, p.st, 31) && ok;
       stamp(p, 17);
       if (!ok) *(volatile int*)fail = 1;
-      // one warp per (token, expert) pair over the whole K (two accumulators),
-      // lane 0 adds the bias and stores the logit: no cross-warp reduction
-      for (int pr = warp; pr < pairs; pr += kDecWarps) {
-        const int t = pr / nexp, el = pr % nexp;
+      // (token, expert) dot products: wpp warps per pair, each over a K slice
+      // (two accumulators per lane), then the slices are added in order
+      for (int pr = warp / wpp; pr < pairs; pr += kDecWarps / wpp) {
+        const int t = pr / nexp, el = pr % nexp, sl = warp % wpp;
         const uint16_t* xr = reinterpret_cast<const uint16_t*>(regA + t * xstride);
         const float* wrow = wr_s + (size_t)el * d;
+        const int ks = sl * (d / wpp), ke = ks + d / wpp;
         float acc0 = 0.f, acc1 = 0.f;
-        for (int i = lane * 8; i < d; i += 512) {
+        for (int i = ks + lane * 8; i < ke; i += 512) {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int ii = i + h * 256;
-            if (ii < d) {
+            if (ii < ke) {
               const uint4 xv = *reinterpret_cast<const uint4*>(xr + ii);
               const float4 w0 = *reinterpret_cast<const float4*>(wrow + ii);
               const float4 w1 = *reinterpret_cast<const float4*>(wrow + ii + 4);
@@ -412,19 +497,40 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (lane == 0) {
-          const float b = (pr == warp) ? bias0 : (p.b_router ? p.b_router[e_lo + el] : 0.f);
-          p.logits[(size_t)t * E + e_lo + el] = acc + b;
+          if (wpp == 1) {
+            const float b = (pr == warp) ? bias0 : (p.b_router ? p.b_router[e_lo + el] : 0.f);
+            p.logits[(size_t)t * E + e_lo + el] = acc + b;
+          } else {
+            rt.part[pr * wpp + sl] = acc;
+          }
+        }
+      }
+      stamp(p, 24);
+      if (wpp > 1) {
+        consumer_sync();
+        stamp(p, 25);
+        if (tid < pairs) {
+          float acc = 0.f;
+          for (int sl = 0; sl < wpp; ++sl) acc += rt.part[tid * wpp + sl];
+          p.logits[(size_t)(tid / nexp) * E + e_lo + tid % nexp] = acc + biasA;
         }
       }
       stamp(p, 18);
       stamp(p, 2);
-      grid_barrier(p.gbar, fail, p.st, 32, p.trace, 22);  // A: every logit written
+      // A: every logit written.  Between the arrival and the wait the staged
+      // tokens become scaled fp16 (the router has read them).
+      const unsigned tgt = grid_arrive(p.gbar, p.trace, 22);
+      if (ok && warp > 0) stage_tokens_f16(regA, x16, T, d, xstride, rt.sexp, warp - 1, kDecWarps - 1, lane);
+      grid_wait(p.gbar, tgt, fail, p.st, 32);
       stamp(p, 3);
-    } else if (!ok) {
-      *(volatile int*)fail = 1;
+    } else {
+      if (!ok) *(volatile int*)fail = 1;
+      consumer_sync();  // (prenorm) every normalised row is in place
+      if (ok) stage_tokens_f16(regA, x16, T, d, xstride, rt.sexp, warp, kDecWarps, lane);
     }
 
     // ---------------- P1: routing tables, replicated in every CTA
+    bool grouped = false;  // the T = 1 path builds the grouping itself
     if (*(volatile int*)fail == 0) {
       if (routed && T > 1 && kr > 0) {
         // several tokens: one warp per token, all tokens at once
@@ -435,80 +541,113 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
             warp_topk_token<kDecMaxE / 32>(p.logits + (size_t)warp * E, E, kr, k, p.renorm, warp, rt.ids, rt.w,
                                             lane);
         }
-      } else if (routed) {
-        // Per token: keys = order-preserving logit bits, then the inverted
-        // expert index (equal logits put the lower expert first).  The k-th
-        // largest of the 16 warp maxima is a lower bound tau for the k-th key
-        // (k distinct elements reach it), so only keys >= tau can be chosen and
-        // ranking those few candidates against each other gives the top-k.
-        for (int t = 0; t < T && kr > 0; ++t) {
-          const unsigned long long key =
-              (tid < E) ? (((unsigned long long)float_order_key(__ldcg(p.logits + (size_t)t * E + tid)) << 32) |
-                           (0xffffffffu - (uint32_t)tid))
-                        : 0ull;
-          unsigned long long m = key;
+      } else if (routed && kr > 0) {
+        // One token.  Keys = order-preserving logit bits, then the inverted
+        // expert index (equal logits put the lower expert first).  The kr-th
+        // largest of the 16 warp maxima is a lower bound tau for the kr-th key
+        // (kr distinct elements reach it), so only keys >= tau can be chosen;
+        // ranking those few candidates against each other gives the top-kr.
+        const unsigned long long key =
+            (tid < E) ? (((unsigned long long)float_order_key(__ldcg(p.logits + tid)) << 32) |
+                         (0xffffffffu - (uint32_t)tid))
+                      : 0ull;
+        stamp(p, 26);
+        unsigned long long m = key;
 #pragma unroll
-          for (int off = 16; off > 0; off >>= 1) m = umax64(m, __shfl_xor_sync(0xffffffffu, m, off));
-          if (lane == 0) rt.wmax[warp] = m;
-          consumer_sync();
-          if (tid < kDecWarps) {
-            const unsigned long long mw = rt.wmax[tid];
-            int rank = 0;
+        for (int off = 16; off > 0; off >>= 1) m = umax64(m, __shfl_xor_sync(0xffffffffu, m, off));
+        if (lane == 0) rt.wmax[warp] = m;
+        consumer_sync();
+        stamp(p, 27);
+        // every warp finds tau itself: lanes 0..15 rank the 16 warp maxima
+        const unsigned long long wm = (lane < kDecWarps) ? rt.wmax[lane] : 0ull;
+        int rank = 0;
 #pragma unroll
-            for (int w = 0; w < kDecWarps; ++w) {
-              const unsigned long long o = rt.wmax[w];
-              rank += (o > mw) || (o == mw && w < tid);
-            }
-            if (rank == kr - 1) rt.misc[3] = tid;
-          }
-          consumer_sync();
-          const unsigned long long tau = rt.wmax[rt.misc[3]];
-          const bool is_cand = key != 0ull && key >= tau;
-          if (is_cand) rt.cand[atomicAdd(&rt.misc[2], 1)] = key;
-          if (!p.renorm) {
-            unsigned long long top = 0ull;
-#pragma unroll
-            for (int w = 0; w < kDecWarps; ++w) top = umax64(top, rt.wmax[w]);
-            float ez = (key != 0ull) ? expf(key_value(key) - key_value(top)) : 0.f;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) ez += __shfl_xor_sync(0xffffffffu, ez, off);
-            if (lane == 0) rt.part[warp] = ez;
-          }
-          consumer_sync();
-          if (is_cand) {
-            const int nc = rt.misc[2];
-            int rank = 0;
-            for (int j = 0; j < nc; ++j) rank += rt.cand[j] > key;
-            if (rank < kr) rt.sel[t * kDecMaxK + rank] = key;
-          }
-          if (tid == 0 && !p.renorm) {
-            float z = 0.f;
-            for (int w = 0; w < kDecWarps; ++w) z += rt.part[w];
-            rt.zall[t] = z;
-          }
-          consumer_sync();
-          if (tid == 0) rt.misc[2] = 0;
+        for (int w = 0; w < kDecWarps; ++w) {
+          const unsigned long long o = __shfl_sync(0xffffffffu, wm, w);
+          rank += (o > wm) || (o == wm && w < lane);
         }
-        // gates: exp(l_j - l_max) over the chosen kr (renormalised) or over all E;
-        // the shared expert's row (j = kr) is bank entry E with weight 1
-        if (tid < R) {
-          const int t = tid / k, j = tid % k;
-          if (j >= kr) {
-            rt.ids[tid] = E;
-            rt.w[tid] = 1.0f;
-          } else {
-            const unsigned long long* sk = rt.sel + t * kDecMaxK;
-            const float vmax = key_value(sk[0]);
-            float z = 0.f;
-            if (p.renorm) {
-              for (int jj = 0; jj < kr; ++jj) z += expf(key_value(sk[jj]) - vmax);
-            } else {
-              z = rt.zall[t];
-            }
-            const int e = (int)(0xffffffffu - (uint32_t)(sk[j] & 0xffffffffull));
-            rt.ids[tid] = (sk[j] != 0ull && e < E) ? e : -1;
-            rt.w[tid] = expf(key_value(sk[j]) - vmax) / z;
+        const unsigned at_k = __ballot_sync(0xffffffffu, lane < kDecWarps && rank == kr - 1);
+        const unsigned long long tau = __shfl_sync(0xffffffffu, wm, __ffs(at_k) - 1);
+        // candidates (keys >= tau), compacted with one shared atomic per warp
+        const bool is_cand = key != 0ull && key >= tau;
+        const unsigned cb = __ballot_sync(0xffffffffu, is_cand);
+        if (cb) {
+          int base = 0;
+          if (lane == 0) base = atomicAdd(&rt.misc[2], __popc(cb));
+          base = __shfl_sync(0xffffffffu, base, 0);
+          if (is_cand) rt.cand[base + __popc(cb & ((1u << lane) - 1u))] = key;
+        }
+        if (!p.renorm) {  // gates over all E: the softmax denominator, per warp
+          const unsigned at_0 = __ballot_sync(0xffffffffu, lane < kDecWarps && rank == 0);
+          const float vtop = key_value(__shfl_sync(0xffffffffu, wm, __ffs(at_0) - 1));
+          float ez = (key != 0ull) ? expf(key_value(key) - vtop) : 0.f;
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) ez += __shfl_xor_sync(0xffffffffu, ez, off);
+          if (lane == 0) rt.part[warp] = ez;
+        }
+        stamp(p, 28);
+        consumer_sync();
+        stamp(p, 29);
+        if (is_cand) {
+          const int nc = rt.misc[2];
+          int r = 0;
+          for (int j = 0; j < nc; ++j) r += rt.cand[j] > key;
+          if (r < kr) rt.sel[r] = key;
+        }
+        consumer_sync();
+        stamp(p, 10);
+        if (warp == 0) {
+          // lane j < kr: the j-th chosen expert; lane kr (n_shared = 1): the
+          // shared expert, bank entry E, weight 1.  One row per expert, so the
+          // grouping sorts the kt = k ids (all distinct) ascending.
+          int e = 0x7fffffff;
+          float v = 0.f;
+          if (lane < kr) {
+            const unsigned long long sk = rt.sel[lane];
+            e = (int)(0xffffffffu - (uint32_t)(sk & 0xffffffffull));
+            v = key_value(sk);
+          } else if (lane < k) {
+            e = E;
           }
+          const float vmax = __shfl_sync(0xffffffffu, v, 0);
+          const float ez = (lane < kr) ? expf(v - vmax) : 0.f;
+          float z = 0.f;
+          if (p.renorm) {
+            z = ez;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+          } else {
+            for (int w = 0; w < kDecWarps; ++w) z += rt.part[w];
+          }
+          int pos = 0;
+          for (int j = 0; j < k; ++j) pos += __shfl_sync(0xffffffffu, e, j) < e;
+          if (lane < k) {
+            const float wg = (lane < kr) ? ez / z : 1.0f;
+            rt.ids[lane] = e;
+            rt.w[lane] = wg;
+            rt.pos[lane] = pos;
+            rt.sorted[pos] = lane;
+            rt.act_e[pos] = e;
+            rt.act_off[pos] = pos;
+            rt.first[lane] = pos + 1;
+            if (cta == 0) {
+              if (p.ids_out) p.ids_out[lane] = e;
+              if (p.w_out) p.w_out[lane] = wg;
+            }
+          }
+          if (lane == 0) {
+            rt.misc[0] = k;
+            rt.act_off[k] = k;
+            rt.misc[2] = 0;
+          }
+        }
+        grouped = true;
+        stamp(p, 11);
+      } else if (routed) {
+        // a dense layer (kr = 0): each token's one row is the shared expert
+        for (int r = tid; r < R; r += kConsumers) {
+          rt.ids[r] = E;
+          rt.w[r] = 1.0f;
         }
       } else {
         for (int r = tid; r < R; r += kConsumers) {
@@ -525,53 +664,55 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
           rt.w[r] = p.forced_w[r];
         }
       }
-      consumer_sync();
-      // stable grouping by ranks: row r goes to (rows of smaller experts) +
-      // (earlier rows of its own expert); the first row of each expert also
-      // places the expert in the ascending list of active experts
-      for (int r = tid; r < R; r += kConsumers) {
-        const int e = rt.ids[r];
-        int less = 0, before = 0;
-        if (e >= 0) {
-#pragma unroll 8  // eight broadcast loads in flight (R is up to 136 rows)
-          for (int rr = 0; rr < R; ++rr) {
-            const int f = rt.ids[rr];
-            less += (f >= 0 && f < e);
-            before += (rr < r && f == e);
-          }
-          rt.pos[r] = less + before;
-          rt.sorted[less + before] = r;
-        } else {
-          rt.pos[r] = -1;
-        }
-        rt.first[r] = (e >= 0 && before == 0) ? less + 1 : 0;
-      }
-      consumer_sync();
-      stamp(p, 10);
-      for (int r = tid; r < R; r += kConsumers) {
-        if (rt.first[r] > 0) {
-          const int e = rt.ids[r];
-          int a = 0;
-#pragma unroll 8
-          for (int rr = 0; rr < R; ++rr) a += (rt.first[rr] > 0 && rt.ids[rr] < e);
-          rt.act_e[a] = e;
-          rt.act_off[a] = rt.first[r] - 1;
-        }
-      }
-      {  // active experts and routed rows, counted by the barrier itself (R <= kConsumers)
-        const int U = consumer_popc(tid < R && rt.first[tid] > 0);
-        const int Rv = consumer_popc(tid < R && rt.ids[tid] >= 0);
-        if (tid == 0) {
-          rt.misc[0] = U;
-          rt.act_off[U] = Rv;
-        }
-      }
-      consumer_sync();
-      stamp(p, 11);
-      if (cta == 0) {
+      if (!grouped) {
+        consumer_sync();
+        // stable grouping by ranks: row r goes to (rows of smaller experts) +
+        // (earlier rows of its own expert); the first row of each expert also
+        // places the expert in the ascending list of active experts
         for (int r = tid; r < R; r += kConsumers) {
-          if (p.ids_out) p.ids_out[r] = rt.ids[r];
-          if (p.w_out) p.w_out[r] = rt.w[r];
+          const int e = rt.ids[r];
+          int less = 0, before = 0;
+          if (e >= 0) {
+#pragma unroll 8  // eight broadcast loads in flight (R is up to 136 rows)
+            for (int rr = 0; rr < R; ++rr) {
+              const int f = rt.ids[rr];
+              less += (f >= 0 && f < e);
+              before += (rr < r && f == e);
+            }
+            rt.pos[r] = less + before;
+            rt.sorted[less + before] = r;
+          } else {
+            rt.pos[r] = -1;
+          }
+          rt.first[r] = (e >= 0 && before == 0) ? less + 1 : 0;
+        }
+        consumer_sync();
+        stamp(p, 10);
+        for (int r = tid; r < R; r += kConsumers) {
+          if (rt.first[r] > 0) {
+            const int e = rt.ids[r];
+            int a = 0;
+#pragma unroll 8
+            for (int rr = 0; rr < R; ++rr) a += (rt.first[rr] > 0 && rt.ids[rr] < e);
+            rt.act_e[a] = e;
+            rt.act_off[a] = rt.first[r] - 1;
+          }
+        }
+        {  // active experts and routed rows, counted by the barrier itself (R <= kConsumers)
+          const int U = consumer_popc(tid < R && rt.first[tid] > 0);
+          const int Rv = consumer_popc(tid < R && rt.ids[tid] >= 0);
+          if (tid == 0) {
+            rt.misc[0] = U;
+            rt.act_off[U] = Rv;
+          }
+        }
+        consumer_sync();
+        stamp(p, 11);
+        if (cta == 0) {
+          for (int r = tid; r < R; r += kConsumers) {
+            if (p.ids_out) p.ids_out[r] = rt.ids[r];
+            if (p.w_out) p.w_out[r] = rt.w[r];
+          }
         }
       }
     }
@@ -631,8 +772,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
     const unsigned char* tg = ring + (size_t)sg * tbd;
     const unsigned char* tu = ring + (size_t)su * tbd;
     // token row of this lane's B fragment (n = g)
-    const unsigned char* xrow = nullptr;
-    if (g < na) xrow = regA + (rt.sorted[rt.act_off[a] + g] / k) * xstride;
+    // (lanes past the expert's tokens read the zeroed pad row after the tokens)
+    const unsigned char* xrow = x16 + (g < na ? rt.sorted[rt.act_off[a] + g] / k : T) * xstride;
     float ag4[4] = {0.f, 0.f, 0.f, 0.f}, au4[4] = {0.f, 0.f, 0.f, 0.f};
     for (int ch = warp; ch < d / kChunkK; ch += kDecWarps) {
       const unsigned char* cg = tg + ch * kChunkBytes;
@@ -645,31 +786,22 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
       const uint2 sg1 = *reinterpret_cast<const uint2*>(cg + kChunkQBytes + (g + 8) * 8);
       const uint2 su0 = *reinterpret_cast<const uint2*>(cu + kChunkQBytes + g * 8);
       const uint2 su1 = *reinterpret_cast<const uint2*>(cu + kChunkQBytes + (g + 8) * 8);
-#pragma unroll
+#pragma unroll 2
       for (int gg = 0; gg < 4; ++gg) {
         const int col = (ch * 4 + gg) * kGroup + c * 8;
-        uint4 xb = make_uint4(0, 0, 0, 0);
-        if (xrow) xb = *reinterpret_cast<const uint4*>(xrow + col * 2);
-        uint32_t A[2][4], B[2][4];
-        const uint32_t wg0 = word_at(qg0, gg), wg1 = word_at(qg1, gg);
-        const uint32_t wu0 = word_at(qu0, gg), wu1 = word_at(qu1, gg);
-#pragma unroll
-        for (int st = 0; st < 2; ++st) {
-          A[st][0] = nib_pair_bf16(wg0, 2 * st);
-          A[st][1] = nib_pair_bf16(wg1, 2 * st);
-          A[st][2] = nib_pair_bf16(wg0, 2 * st + 1);
-          A[st][3] = nib_pair_bf16(wg1, 2 * st + 1);
-          B[st][0] = nib_pair_bf16(wu0, 2 * st);
-          B[st][1] = nib_pair_bf16(wu1, 2 * st);
-          B[st][2] = nib_pair_bf16(wu0, 2 * st + 1);
-          B[st][3] = nib_pair_bf16(wu1, 2 * st + 1);
-        }
-        const float z[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint4 xb = *reinterpret_cast<const uint4*>(xrow + col * 2);  // fp16, scaled
+        uint32_t pg0[4], pg1[4], pu0[4], pu1[4];
+        nib_pairs4_f16(word_at(qg0, gg), pg0);
+        nib_pairs4_f16(word_at(qg1, gg), pg1);
+        nib_pairs4_f16(word_at(qu0, gg), pu0);
+        nib_pairs4_f16(word_at(qu1, gg), pu1);
+        const uint32_t A0[4] = {pg0[0], pg1[0], pg0[1], pg1[1]}, A1[4] = {pg0[2], pg1[2], pg0[3], pg1[3]};
+        const uint32_t B0[4] = {pu0[0], pu1[0], pu0[1], pu1[1]}, B1[4] = {pu0[2], pu1[2], pu0[3], pu1[3]};
         float dg[4], du[4];
-        mma_bf16(dg, A[0], xb.x, xb.y, z);
-        mma_bf16(du, B[0], xb.x, xb.y, z);
-        mma_bf16(dg, A[1], xb.z, xb.w, dg);
-        mma_bf16(du, B[1], xb.z, xb.w, du);
+        mma_f16_z(dg, A0, xb.x, xb.y);
+        mma_f16_z(du, B0, xb.x, xb.y);
+        mma_f16(dg, A1, xb.z, xb.w, dg);
+        mma_f16(du, B1, xb.z, xb.w, du);
         const float s_g0 = scale_at(sg0, gg), s_g1 = scale_at(sg1, gg);
         const float s_u0 = scale_at(su0, gg), s_u1 = scale_at(su1, gg);
         ag4[0] = fmaf(s_g0, dg[0], ag4[0]);
@@ -710,7 +842,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
           av += rb[(w * 32 + ln) * 8 + ix];
           uv += rb[(w * 32 + ln) * 8 + 4 + ix];
         }
-        const float h = silu_mul(av, uv);
+        const float un = pow2i(-rt.sexp[rt.sorted[rt.act_off[a] + tok] / k]);  // undo the token's scale
+        const float h = silu_mul(av * un, uv * un);
         const __half hi = __float2half_rn(h);
         const __half lo = __float2half_rn(h - __half2float(hi));
         const size_t o = (size_t)(rt.act_off[a] + tok) * I + r16 * kTileRows + row;
@@ -785,10 +918,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
               A[sp][3] = p1[2 * sp + 1];
             }
             // h = hi + lo: two independent chains of two MMAs, summed afterwards
-            const float z[4] = {0.f, 0.f, 0.f, 0.f};
             float dh[4], dl[4];
-            mma_f16(dh, A[0], bh.x, bh.y, z);
-            mma_f16(dl, A[0], bl.x, bl.y, z);
+            mma_f16_z(dh, A[0], bh.x, bh.y);
+            mma_f16_z(dl, A[0], bl.x, bl.y);
             mma_f16(dh, A[1], bh.z, bh.w, dh);
             mma_f16(dl, A[1], bl.z, bl.w, dl);
             const float sc0 = scale_at(s0, gg), sc1 = scale_at(s1, gg);
@@ -841,7 +973,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
 }
 
 struct DecodePlan {
-  int offA, offB, offR, offRing, nstages;
+  int offA, offB, offR, offRing, offX16, nstages;
   size_t smem;
   bool ok;
 };
@@ -855,13 +987,15 @@ DecodePlan plan(int T, int d, int E, int k, int I, int n_shared, int G) {
   if (tile_bytes(d) % tile_bytes(I)) return pl;
   const size_t xall = (size_t)T * (2 * d + kSmemRowPad);
   const size_t hall = (size_t)R * 2 * (2 * I);
-  const size_t regA = ((xall > hall ? xall : hall) + 127) / 128 * 128;
+  const size_t xall2 = (xall + 127) / 128 * 128 + (size_t)(T + 1) * (2 * d + kSmemRowPad);  // bf16, fp16 + pad
+  const size_t regA = ((xall2 > hall ? xall2 : hall) + 127) / 128 * 128;
+  pl.offX16 = (int)((xall + 127) / 128 * 128);
   const int nexp = (E + G - 1) / G;
   const size_t p0 = (size_t)nexp * d * 4 + (size_t)T * nexp * kDecWarps * 4;
   const size_t p2 = (size_t)2 * kDecWarps * 32 * 8 * 4 + (size_t)4 * R * kTileRows * 4;
   const size_t regB = ((p0 > p2 ? p0 : p2) + 127) / 128 * 128;
   const size_t regR = ((size_t)(kDecWarps + kConsumers + kDecMaxT * kDecMaxK) * 8 +
-                       (size_t)(kDecMaxT + kDecWarps + 7 * R + 1 + 4) * 4 + 127) / 128 * 128;
+                       (size_t)(2 * kDecMaxT + kDecWarps + 7 * R + 1 + 4) * 4 + 127) / 128 * 128;
   pl.offA = 1024;
   pl.offB = pl.offA + (int)regA;
   pl.offR = pl.offB + (int)regB;
@@ -947,6 +1081,7 @@ cudaError_t launch_decode_fused(const DecodeLaunch& L, cudaStream_t s) {
   a.offB = pl.offB;
   a.offR = pl.offR;
   a.offRing = pl.offRing;
+  a.offX16 = pl.offX16;
   a.prenorm = L.prenorm;
   a.eps = L.eps;
   a.xh_out = L.xh_out;

@@ -97,6 +97,8 @@ cudaError_t launch_pack_int4(const uint8_t* q, const uint16_t* scale, int64_t n_
 
 // ---------------------------------------------------------------- LM head (lmhead.cu)
 size_t lmhead_scratch_bytes(int T);
+// Whether one launch can stage min(T, 16) tokens and at least two weight tiles of width d.
+bool lmhead_supported(int d, int T);
 cudaError_t launch_lmhead(const uint16_t* h, int T, int d, int V, const uint8_t* w_packed, float* logits,
                           int32_t* argmax, void* scratch, DevStatus* st, cudaStream_t s);
 

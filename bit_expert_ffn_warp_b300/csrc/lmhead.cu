@@ -9,7 +9,8 @@
 // a weight stream that has to keep HBM busy: one CTA per SM, a producer warp
 // keeps a ring of 16-row tiles in flight with TMA bulk copies, and each
 // consumer warp owns whole tiles -- it multiplies its tile's 16 rows over the
-// full reduction on its own, so no consumer waits for another.  A warp folds
+// full reduction on its own, so no consumer waits for another -- and its own
+// ring stages.  A warp folds
 // its logits into a per-token running arg-max in registers; at the end the
 // warps' maxima meet in shared memory and one 64-bit atomicMax per token and
 // CTA (order-preserving logit bits, then the inverted row index so that the
@@ -28,7 +29,7 @@
 namespace bitmoe {
 namespace {
 
-constexpr int kLmConsumers = 8;                 // consumer warps, each owning whole tiles
+constexpr int kLmConsumers = 12;                // consumer warps, each owning whole tiles
 constexpr int kLmThreads = (kLmConsumers + 1) * 32;
 constexpr int kLmTok = 16;                      // tokens per launch (two mma n-tiles)
 constexpr int kLmMaxStages = 16;
@@ -37,6 +38,7 @@ constexpr int kLmSmemBudget = 227 * 1024;
 struct LmArgs {
   const uint16_t* h;  // [T, d] bf16, this launch's first token
   int ntok, d, V, tok0, nstages;
+  int nwarps;  // consumer warps that take tiles (nstages is a multiple of it)
   const uint8_t* w;
   float* logits;             // [T_total, V] or null
   unsigned long long* keys;  // [T_total]
@@ -63,16 +65,17 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
 __device__ __forceinline__ float pow2i(int s) { return __int_as_float((s + 127) << 23); }
 
 // Shared memory: barriers (256 B), the per-token scale exponents and arg-max
-// partials, the fp16 tokens [8 * NT][d + pad], then the tile ring.
+// partials, the fp16 tokens [8 * NT][d + pad] and one zeroed row, then the tile ring.
 struct LmSmem {
   static constexpr int kBars = 0;                                   // full[16], empty[16], xbar
   static constexpr int kExp = 384;                                  // int [16]
-  static constexpr int kBestV = kExp + 64;                          // float [8 warps][16 tokens]
-  static constexpr int kBestI = kBestV + kLmConsumers * kLmTok * 4; // int   [8 warps][16 tokens]
+  static constexpr int kBestV = kExp + 64;                          // float [warps][16 tokens]
+  static constexpr int kBestI = kBestV + kLmConsumers * kLmTok * 4; // int   [warps][16 tokens]
   static constexpr int kFail = kBestI + kLmConsumers * kLmTok * 4;  // int
-  static constexpr int kX = 2048;                                   // fp16 tokens
+  static constexpr int kX = 2304;                                   // fp16 tokens
   __host__ __device__ static int xstride(int d) { return 2 * d + kSmemRowPad; }
-  __host__ __device__ static int ring(int d, int nt) { return kX + ((8 * nt * xstride(d) + 127) / 128) * 128; }
+  // the launch's ntok token rows, then one zeroed pad row
+  __host__ __device__ static int ring(int d, int ntok) { return kX + (((ntok + 1) * xstride(d) + 127) / 128) * 128; }
 };
 static_assert((2 * kLmMaxStages + 1) * 8 <= LmSmem::kExp, "lm head barriers");
 static_assert(LmSmem::kFail + 4 <= LmSmem::kX, "lm head smem header");
@@ -90,7 +93,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_kernel(LmArgs p) {
   const int d = p.d;
   const int xstride = LmSmem::xstride(d);
   unsigned char* sx = smem + LmSmem::kX;
-  unsigned char* ring = smem + LmSmem::ring(d, NT);
+  unsigned char* ring = smem + LmSmem::ring(d, p.ntok);
   const int tbytes = (int)tile_bytes(d);
   const int NS = p.nstages;
 
@@ -149,9 +152,13 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_kernel(LmArgs p) {
   // ---------------- consumers: stage the tokens as scaled fp16
   bool ok = mbar_wait(xbar, 0, p.st, 21);
   if (!ok) atomicOr(fail_flag, 1);
+  {  // the pad row read for absent tokens
+    uint4* pad = reinterpret_cast<uint4*>(sx + p.ntok * xstride);
+    for (int c = tid; c < d / 8; c += kLmConsumers * 32) pad[c] = make_uint4(0, 0, 0, 0);
+  }
   consumer_sync();
   if (*(volatile int*)fail_flag == 0) {
-    // per token (one warp each, two passes for 16 tokens over 8 warps): largest
+    // per token (one warp each, two passes for 16 tokens over 12 warps): largest
     // |h| -> exponent e; scale 2^(14 - e) puts the largest element in [2^14, 2^15)
     for (int t = warp; t < p.ntok; t += kLmConsumers) {
       uint16_t* xr = reinterpret_cast<uint16_t*>(sx + t * xstride);
@@ -202,7 +209,19 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_kernel(LmArgs p) {
       unscale[nt][b] = (tok < p.ntok) ? pow2i(-sexp[tok]) : 0.f;
     }
 
-  for (int i = warp; i < my_tiles && *(volatile int*)fail_flag == 0; i += kLmConsumers) {
+  // the activation row of each lane's n-tile token; lanes past the last token
+  // read the zeroed pad row after the tokens, so the load needs no branch
+  const unsigned char* xrow[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int tok = nt * 8 + g;
+    xrow[nt] = sx + (tok < p.ntok ? tok : p.ntok) * xstride;
+  }
+  // Stage s always belongs to warp s % nw (the stage count is a multiple of
+  // nw), so a warp waits on a stage's phases strictly in order: a parity wait
+  // two phases ahead would alias the earlier phase and return at once.
+  const int nw = p.nwarps;
+  for (int i = warp; warp < nw && i < my_tiles && *(volatile int*)fail_flag == 0; i += nw) {
     const int s = i % NS;
     if (!mbar_wait(&full[s], (i / NS) & 1, p.st, 22)) {
       atomicOr(fail_flag, 1);
@@ -232,12 +251,9 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_kernel(LmArgs p) {
         const float sc0 = scale_at(s0, gg), sc1 = scale_at(s1, gg);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const int tok = nt * 8 + g;
-          uint4 xb = make_uint4(0, 0, 0, 0);
-          if (tok < p.ntok) xb = *reinterpret_cast<const uint4*>(sx + tok * xstride + col * 2);
-          const float z[4] = {0.f, 0.f, 0.f, 0.f};
+          const uint4 xb = *reinterpret_cast<const uint4*>(xrow[nt] + col * 2);
           float dd[4];
-          mma_f16(dd, a0, xb.x, xb.y, z);
+          mma_f16_z(dd, a0, xb.x, xb.y);
           mma_f16(dd, a1, xb.z, xb.w, dd);
           acc[nt][0] = fmaf(sc0, dd[0], acc[nt][0]);
           acc[nt][1] = fmaf(sc0, dd[1], acc[nt][1]);
@@ -313,28 +329,31 @@ __global__ void argmax_finalize_kernel(const unsigned long long* keys, int T, in
   if (t < T) argmax[t] = (int32_t)(0xffffffffu - (uint32_t)(keys[t] & 0xffffffffull));
 }
 
-int lm_stages(int d, int nt) {
-  const int n = (kLmSmemBudget - LmSmem::ring(d, nt)) / (int)tile_bytes(d);
+int lm_stages(int d, int ntok) {
+  const int n = (kLmSmemBudget - LmSmem::ring(d, ntok)) / (int)tile_bytes(d);
   return n < kLmMaxStages ? n : kLmMaxStages;
 }
 
-size_t lm_smem(int d, int nt) { return (size_t)LmSmem::ring(d, nt) + (size_t)lm_stages(d, nt) * tile_bytes(d); }
+size_t lm_smem(int d, int ntok) { return (size_t)LmSmem::ring(d, ntok) + (size_t)lm_stages(d, ntok) * tile_bytes(d); }
 
 }  // namespace
 
 size_t lmhead_scratch_bytes(int T) { return (size_t)T * sizeof(unsigned long long); }
 
+bool lmhead_supported(int d, int T) { return lm_stages(d, T < kLmTok ? T : kLmTok) >= 2; }
+
 cudaError_t launch_lmhead(const uint16_t* h, int T, int d, int V, const uint8_t* w_packed, float* logits,
                           int32_t* argmax, void* scratch, DevStatus* st, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  if (lm_stages(d, 2) < 2) return cudaErrorNotSupported;  // d too large for two tiles beside the tokens
+  if (!lmhead_supported(d, T)) return cudaErrorNotSupported;  // d too large for two tiles beside the tokens
   unsigned long long* keys = static_cast<unsigned long long*>(scratch);
   cudaError_t err = cudaMemsetAsync(keys, 0, (size_t)T * sizeof(unsigned long long), s);
   if (err != cudaSuccess) return err;
   static int attr1[64] = {}, attr2[64] = {};
-  err = ensure_smem_attr(lmhead_kernel<1>, lm_smem(d, 1), attr1);
+  // every launch fits the budget whatever its token count (the ring takes the rest)
+  err = ensure_smem_attr(lmhead_kernel<1>, (size_t)kLmSmemBudget, attr1);
   if (err != cudaSuccess) return err;
-  err = ensure_smem_attr(lmhead_kernel<2>, lm_smem(d, 2), attr2);
+  err = ensure_smem_attr(lmhead_kernel<2>, (size_t)kLmSmemBudget, attr2);
   if (err != cudaSuccess) return err;
   static int sm_count[64] = {};
   int dev = 0;
@@ -352,15 +371,17 @@ cudaError_t launch_lmhead(const uint16_t* h, int T, int d, int V, const uint8_t*
     a.V = V;
     a.tok0 = t0;
     const int nt = a.ntok <= 8 ? 1 : 2;
-    a.nstages = lm_stages(d, nt);
+    const int ns = lm_stages(d, a.ntok);
+    a.nwarps = ns < kLmConsumers ? ns : kLmConsumers;
+    a.nstages = ns / a.nwarps * a.nwarps;
     a.w = w_packed;
     a.logits = logits;
     a.keys = keys;
     a.st = st;
     if (nt == 1)
-      lmhead_kernel<1><<<grid, kLmThreads, lm_smem(d, 1), s>>>(a);
+      lmhead_kernel<1><<<grid, kLmThreads, lm_smem(d, a.ntok), s>>>(a);
     else
-      lmhead_kernel<2><<<grid, kLmThreads, lm_smem(d, 2), s>>>(a);
+      lmhead_kernel<2><<<grid, kLmThreads, lm_smem(d, a.ntok), s>>>(a);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }

@@ -63,6 +63,7 @@ bitmoe_status_t lmhead_int4_gemv_static(const uint16_t* h, int64_t T, int64_t d,
   // the scratch this call needs must fit the fixed array
   if (T > 64 || kStatusBytes + lmhead_scratch_bytes((int)T) > kStaticScratchBytes) return BITMOE_ERR_WORKSPACE;
   if (T == 0) return BITMOE_OK;
+  if (!lmhead_supported((int)d, (int)T)) return BITMOE_ERR_UNSUPPORTED;
   const uintptr_t a16 = 15u;
   if (!h || !w_packed || !argmax || (reinterpret_cast<uintptr_t>(h) & a16) ||
       (reinterpret_cast<uintptr_t>(w_packed) & a16))

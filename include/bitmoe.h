@@ -263,7 +263,10 @@ size_t lmhead_workspace_size(int64_t T, int64_t d, int64_t V);
 /*
  * 4-bit output projection: logits[t,v] = sum_i Wlm[v,i] h[t,i] (fp32) and
  * argmax[t] = the lowest v reaching the maximum.  h [T, d] bf16; w_packed is
- * the packed [V, d] bank; logits [T, V] may be NULL.  V % 16 == 0, T <= 64.
+ * the packed [V, d] bank; logits [T, V] may be NULL.  V % 16 == 0, T <= 64,
+ * d % 128 == 0 and small enough that a CTA stages min(T, 16) tokens beside two
+ * 16-row weight tiles in shared memory (d = 2048: any T; d = 8192: T <= 4),
+ * else BITMOE_ERR_UNSUPPORTED.
  * Source: "Flint 40B : Best Mid Sized LLM", transcript 03:36 and 05:39.
  */
 bitmoe_status_t lmhead_int4_gemv(const uint16_t* h, int64_t T, int64_t d, int64_t V, int64_t group,

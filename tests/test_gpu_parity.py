@@ -150,6 +150,69 @@ def test_route_parity(T, bias):
     assert np.allclose(w.cpu().numpy()[ok], w_ref[ok], rtol=2e-5, atol=1e-6)
 
 
+def tie_layer(E, d, tied, top_bias=20.0, seed=3):
+    """A router whose logits are l_e = x_e + b_e exactly (W_r is the identity on the
+    first E columns), with the experts in `tied` sharing one bias well above the
+    rest: with x equal on those columns their logits tie bit for bit, whatever
+    the summation order."""
+    rng = np.random.default_rng(seed)
+    wr = np.zeros((E, d), np.float32)
+    wr[np.arange(E), np.arange(E)] = 1.0
+    b = rng.normal(0, 1, E).astype(np.float32)
+    b[list(tied)] = top_bias
+    return wr, b
+
+
+def tie_tokens(T, d, tied, seed=4):
+    rng = np.random.default_rng(seed)
+    x = synth.f64_to_bf16_bits(rng.normal(0, 1, (T, d)))
+    x[:, list(tied)] = x[:, [tied[0]]]
+    return x
+
+
+@pytest.mark.parametrize("k", [1, 2, 3])
+def test_route_exact_ties_pick_the_lower_expert(k):
+    """Exactly equal logits: the lower expert index is chosen and listed first
+    (no near-tie feed -- the GPU's own tie-break against the oracle's)."""
+    E, d, T = 16, 256, 5
+    tied = (3, 7, 11)
+    wr, b = tie_layer(E, d, tied)
+    x_bits = tie_tokens(T, d, tied)
+    ids_ref, w_ref, _, gap = oracle.route(x_bits, wr, b, k)
+    assert np.all(ids_ref[:, 0] == 3)
+    tensors = layer_tensors(0, d, E, TINY["I"], bias="zero")
+    tensors["w_router"], tensors["b_router"] = wr, b
+    lay = device_layer(tensors, k)
+    ws = bm.moe_workspace(lay, T)
+    ids, w = bm.moe_route(torch_bf16_from_bits(x_bits), lay, ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+    assert np.allclose(w.cpu().numpy(), w_ref, rtol=1e-5, atol=1e-6)
+
+
+@pytest.mark.parametrize("T,k", [(1, 8), (1, 2), (4, 8)])
+def test_fused_decode_exact_ties_pick_the_lower_expert(T, k):
+    """The fused decode kernel's top-k on exactly tied logits (the top three
+    experts tie; with k = 2 the tie straddles the k-th place)."""
+    E, d, I = 256, 2048, 512
+    tied = (40, 41, 200)
+    wr, b = tie_layer(E, d, tied)
+    x_bits = tie_tokens(T, d, tied)
+    tensors = layer_tensors(9, d, E, I, bias="zero")
+    tensors["w_router"], tensors["b_router"] = wr, b
+    ref = oracle.moe_forward(x_bits, tensors, k)
+    assert np.all(ref["ids"][:, :2] == [40, 41])
+    lay = device_layer(tensors, k)
+    ws = bm.moe_workspace(lay, T)
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    out_f32 = torch.empty((T, d), dtype=torch.float32, device="cuda")
+    out, _, _, _ = bm.moe_forward(torch_bf16_from_bits(x_bits), lay, ws, out_f32=out_f32, ids_out=ids)
+    torch.cuda.synchronize()
+    assert bm.bitmoe_get_device_status(ws) == 0
+    assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+    check_layer_output(out, out_f32, ref["out"], f"ties T={T} k={k}")
+
+
 def test_route_tiny_unrenormalised_gates():
     tensors, lay = tiny_layer(renorm=False)
     x_bits = synth.activations(1, 4, TINY["d"])
@@ -273,6 +336,23 @@ def test_layer_forced_invalid_ids_flag_and_skip():
     fw = torch.full((2, 2), 0.5, dtype=torch.float32, device="cuda")
     bm.moe_forward(x, lay, ws, forced_ids=fi, forced_w=fw)
     assert bm.bitmoe_get_device_status(ws, clear=True) == bm.ERR_DEVICE_CHECK
+
+
+@pytest.mark.parametrize("T", [2, 12])
+def test_layer_forced_duplicate_id_alone_flags(T):
+    """A token whose forced ids repeat an expert (all ids in range) sets the
+    device check, on the fused kernel (T = 2) and the unfused path (T = 12)."""
+    tensors, lay = tiny_layer()
+    x = torch_bf16_from_bits(synth.activations(3, T, TINY["d"]))
+    ws = bm.moe_workspace(lay, T)
+    fi = np.tile(np.array([[1, 2]], np.int32), (T, 1))
+    fi[T - 1] = [5, 5]
+    fw = torch.full((T, 2), 0.5, dtype=torch.float32, device="cuda")
+    bm.moe_forward(x, lay, ws, forced_ids=torch.from_numpy(fi).cuda(), forced_w=fw)
+    assert bm.bitmoe_get_device_status(ws, clear=True) == bm.ERR_DEVICE_CHECK
+    fi[T - 1] = [5, 6]  # the same call without the duplicate is clean
+    bm.moe_forward(x, lay, ws, forced_ids=torch.from_numpy(fi).cuda(), forced_w=fw)
+    assert bm.bitmoe_get_device_status(ws) == 0
 
 
 def test_zero_tokens_is_a_no_op():
