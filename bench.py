@@ -672,15 +672,28 @@ def bench_stack(args, world, rank):
     am = torch.empty(T, dtype=torch.int32, device="cuda")
     ids = torch.empty((N_LAYERS, T, K_TOP), dtype=torch.int32, device="cuda")
 
-    def layers_and_head():
+    def layer_steps():
         for l in range(N_LAYERS):  # RMSNorm inside the layer step, residual updated in place
             bm.moe_forward_prenorm(resid, layers[l], ws, out=resid, ids_out=ids[l])
         bm.bitmoe_rmsnorm(resid, out=xh)
         bm.lmhead_int4_gemv(xh, lm, V, lm_ws, want_logits=False, argmax=am)
 
+    # the whole step in one launch where the fused decode kernel covers T
+    fused = T <= 8
+    ws_stack = bm.moe_stack_workspace(layers[0], T) if fused else None
+
+    def one_launch():
+        bm.moe_stack_decode(resid, layers, ws_stack, lm_w=lm, V=V, argmax=am, ids_out=ids)
+
+    layers_and_head = one_launch if fused else layer_steps
+
     def step(s):
         resid.copy_(xs[s % n_pool])
         layers_and_head()
+
+    def step_layers(s):
+        resid.copy_(xs[s % n_pool])
+        layer_steps()
 
     with ClockSampler(torch.cuda.current_device()) as clk:
         run_warmup(step, W)
@@ -688,6 +701,12 @@ def bench_stack(args, world, rank):
     ms_local = statistics.median(times)
     ms = max_over_ranks(ms_local, world) / K
     launches_per_step = count_kernels(layers_and_head)
+    compare = None
+    if fused:  # the same step as 49 layer launches + RMSNorm + LM head, for comparison
+        run_warmup(step_layers, 3)
+        lt = time_regions(region_graphs(step_layers, K, 1), world, min_total_s=0.2)
+        compare = {"ms_per_step": round(max_over_ranks(statistics.median(lt), world) / K, 5),
+                   "launches_per_step": count_kernels(layer_steps), "regions": len(lt)}
 
     # bytes touched per step: the unique experts of every layer (last step), routers, LM head
     ids_np = ids.cpu().numpy()
@@ -720,9 +739,11 @@ def bench_stack(args, world, rank):
                          f" GB) + LM head {LM_BYTES / 1e6:.0f} MB per step",
                    "parallelism": f"replicas x{world}"},
         "timing": timing_record(times, K, f"CUDA graph of {K} stack steps"),
+        "per_layer_launches": compare,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "traffic": None,
-                     "kernel": "whole stack step (49 x pre-norm decode layer, RMSNorm, LM head)",
+                     "kernel": ("decode_stack_kernel (49 pre-norm layers, RMSNorm, LM head: one launch)" if fused
+                                else "whole stack step (49 x pre-norm decode layer, RMSNorm, LM head)"),
                      "bytes_per_step": int(step_bytes), "unique_experts_per_layer_mean": float(np.mean(uniq)),
                      "peak_source": which + " (copy, burst)"},
         "gpu_launches": launches_per_step * K if launches_per_step else None,

@@ -72,6 +72,9 @@ _SIGS = {
                                    _P, _P, _P, _P, _SZ, _P]),
     "moe_forward_prenorm": (ctypes.c_int, [_P, _I64, _P, _P, ctypes.c_float, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                                            _P]),
+    "moe_stack_workspace_size": (_SZ, [ctypes.POINTER(MoeShape), _I64]),
+    "moe_stack_decode": (ctypes.c_int, [_P, _I64, ctypes.POINTER(MoeShape), _P, _I64, ctypes.c_float, _P, _I64, _P,
+                                        _P, _P, _P, _SZ, _P]),
     "lmhead_workspace_size": (_SZ, [_I64, _I64, _I64]),
     "lmhead_int4_gemv": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _SZ, _P]),
     "lmhead_static_scratch_bytes": (_SZ, []),
@@ -327,6 +330,39 @@ def moe_forward_prenorm(residual, layer: MoeLayer, workspace, eps: float = 1e-6,
                                     _ptr(forced_ids), _ptr(forced_w), _ptr(ids_out), _ptr(w_out), _ptr(xh_out),
                                     _ptr(out), _ptr(out_f32), _ptr(workspace), workspace.numel(), _stream()))
     return out
+
+
+def moe_stack_workspace(layer: MoeLayer, T: int) -> torch.Tensor:
+    """A zero-filled workspace for moe_stack_decode on T tokens of this layer shape."""
+    n = int(_lib.moe_stack_workspace_size(ctypes.byref(layer.shape), T))
+    if n == 0:
+        raise BitmoeError("moe_stack_workspace_size", 2)
+    return torch.zeros(n, dtype=torch.uint8, device=layer.gate.device)
+
+
+def moe_stack_decode(residual, layers, workspace, eps: float = 1e-6, lm_w=None, V: int = 0, argmax=None,
+                     logits=None, ids_out=None):
+    """One decode step of a stack of pre-norm MoE layers (and, with lm_w, the LM head's
+    arg-max) in a single launch.  residual [T, d] bf16 is updated in place."""
+    T = residual.shape[0]
+    lay0 = layers[0]
+    _need(residual, torch.bfloat16, (T, lay0.d), "residual")
+    if any(l.shape.d != lay0.d or l.k != lay0.k or l.E != lay0.E or l.I != lay0.I or l.n_shared != lay0.n_shared
+           for l in layers):
+        raise ValueError("every layer of a stack shares one shape")
+    arr = (MoeWeights * len(layers))(*[l.weights for l in layers])
+    if lm_w is not None:
+        argmax = torch.empty(T, dtype=torch.int32, device=residual.device) if argmax is None else argmax
+        _need(argmax, torch.int32, (T,), "argmax")
+        if logits is not None:
+            _need(logits, torch.float32, (T, V), "logits")
+    if ids_out is not None:
+        _need(ids_out, torch.int32, (len(layers), T, lay0.kt), "ids_out")
+    sh = lay0.shape
+    _check("moe_stack_decode", _lib.moe_stack_decode(_ptr(residual), T, ctypes.byref(sh), arr, len(layers),
+                                                     float(eps), _ptr(lm_w), V, _ptr(logits), _ptr(argmax),
+                                                     _ptr(ids_out), _ptr(workspace), workspace.numel(), _stream()))
+    return residual, argmax
 
 
 # ---------------------------------------------------------------- LM head and norm

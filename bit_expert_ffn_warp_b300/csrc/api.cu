@@ -383,6 +383,59 @@ bitmoe_status_t moe_forward_prenorm(const uint16_t* residual, int64_t T, const b
                       out_f32, workspace, workspace_bytes, stream, 1, eps, xh_out);
 }
 
+size_t moe_stack_workspace_size(const bitmoe_moe_shape_t* shape, int64_t T) {
+  if (check_shape(shape, T) != BITMOE_OK) return 0;
+  return moe_layout(shape, T, nullptr).total + 256;  // + the arg-max keys
+}
+
+bitmoe_status_t moe_stack_decode(uint16_t* residual, int64_t T, const bitmoe_moe_shape_t* shape,
+                                 const bitmoe_moe_weights_t* layers, int64_t n_layers, float eps,
+                                 const uint8_t* lm_packed, int64_t V, float* logits, int32_t* argmax,
+                                 int32_t* topk_ids_out, void* workspace, size_t workspace_bytes, void* stream) {
+  bitmoe_status_t st = check_shape(shape, T);
+  if (st != BITMOE_OK) return st;
+  if (!layers || n_layers < 1 || !(eps >= 0.f) || V < 0) return BITMOE_ERR_INVALID_ARG;
+  if (T == 0) return BITMOE_OK;
+  if (!residual || !aligned16(residual)) return BITMOE_ERR_INVALID_ARG;
+  for (int64_t l = 0; l < n_layers; ++l)
+    if ((st = check_weights(&layers[l], shape->k > 0)) != BITMOE_OK) return st;
+  if (lm_packed && (!argmax || !aligned16(lm_packed) || V <= 0 || (logits && !aligned16(logits))))
+    return BITMOE_ERR_INVALID_ARG;
+  if (!decode_stack_eligible((int)T, (int)shape->d, (int)shape->E, (int)shape->k, (int)shape->I,
+                             (int)shape->n_shared, (int)n_layers, lm_packed ? (int)V : 0) ||
+      V > (int64_t(1) << 30))
+    return BITMOE_ERR_UNSUPPORTED;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < moe_stack_workspace_size(shape, T))
+    return BITMOE_ERR_WORKSPACE;
+  const MoeWs w = moe_layout(shape, T, workspace);
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + w.total);
+  StackLayer tab[64];
+  for (int64_t l = 0; l < n_layers; ++l)
+    tab[l] = StackLayer{layers[l].gate, layers[l].up, layers[l].down, layers[l].w_router, layers[l].b_router};
+  DecodeLaunch L = {};
+  L.x = residual;
+  L.resid = residual;
+  L.out = residual;
+  L.T = (int)T;
+  L.d = (int)shape->d;
+  L.E = (int)shape->E;
+  L.k = (int)shape->k;
+  L.I = (int)shape->I;
+  L.renorm = shape->renormalize;
+  L.n_shared = (int)shape->n_shared;
+  L.ids_out = topk_ids_out;
+  L.logits = w.logits;
+  L.h_hi = w.h_hi;
+  L.h_lo = w.h_lo;
+  L.gbar = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(w.st) + 64);
+  L.st = w.st;
+  L.pdl = 1;
+  L.prenorm = 1;
+  L.eps = eps;
+  return cuda_status(launch_decode_stack(L, tab, (int)n_layers, lm_packed, (int)V, logits, keys, argmax,
+                                         (cudaStream_t)stream));
+}
+
 size_t lmhead_workspace_size(int64_t T, int64_t d, int64_t V) {
   if (T < 0 || d <= 0 || V <= 0) return 0;
   return 256 + align256(lmhead_scratch_bytes((int)T));

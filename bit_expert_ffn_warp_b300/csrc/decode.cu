@@ -83,6 +83,27 @@ struct DecodeArgs {
   int prenorm;                     // x holds the residual: route and run the experts on RMSNorm(x)
   float eps;
   uint16_t* xh_out;                // optional [T, d] copy of RMSNorm(x) (CTA 0 writes it)
+  // stack launches only
+  int n_layers;                    // layers in the table
+  const uint8_t* lm_w;             // packed LM head [V, d] after the layers (null: none)
+  int lm_V;
+  float* lm_logits;                // optional [T, V]
+  unsigned long long* lm_keys;     // [T] arg-max keys (global scratch)
+  int32_t* lm_argmax;              // [T]
+};
+
+struct LayerPtrs {  // one layer's weights
+  const uint8_t* gate;
+  const uint8_t* up;
+  const uint8_t* down;
+  const float* w_router;
+  const float* b_router;
+};
+
+constexpr int kMaxStackLayers = 64;
+struct StackArgs {
+  DecodeArgs base;
+  LayerPtrs tab[kMaxStackLayers];
 };
 
 // Phase timestamps for the optional trace buffer (thread 0 of each CTA): the
@@ -95,7 +116,6 @@ __device__ __forceinline__ void stamp(const unsigned long long* trace, int point
     if (point == 0) row[kTracePoints - 1] = globaltimer_ns();
   }
 }
-__device__ __forceinline__ void stamp(const DecodeArgs& p, int point) { stamp(p.trace, point); }
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers)); }
 
@@ -312,7 +332,200 @@ __device__ __noinline__ void warp_topk_token(const float* __restrict__ lrow, int
   }
 }
 
-__global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs p) {
+// RMSNorm of the T staged bf16 rows in place (unit gain, eps), by the 512
+// consumer threads: reduced exactly as the standalone RMSNorm kernel does (256
+// threads per token, fp32 FMA chains, then eight warp partials in order), so
+// both give the same bits; two tokens at a time.  xh_out (optional) receives a
+// copy of the normalised rows.
+__device__ __noinline__ void rmsnorm_rows(unsigned char* rows, int T, int d, int xstride, float eps, float* part,
+                                          uint16_t* xh_out) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int half = tid >> 8, lt = tid & 255;
+  for (int t0 = 0; t0 < T; t0 += 2) {
+    const int t = t0 + half;
+    uint16_t* xr = reinterpret_cast<uint16_t*>(rows + t * xstride);
+    float ss = 0.f;
+    if (t < T) {
+      for (int c8 = lt * 8; c8 < d; c8 += 256 * 8) {
+        const uint4 r = *reinterpret_cast<const uint4*>(xr + c8);
+        const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float a = __uint_as_float(rw[i] << 16), b = __uint_as_float(rw[i] & 0xffff0000u);
+          ss = fmaf(a, a, ss);
+          ss = fmaf(b, b, ss);
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if (lane == 0) part[warp] = ss;
+    consumer_sync();
+    float tot = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) tot += part[half * 8 + i];
+    const float inv = 1.0f / sqrtf(tot / (float)d + eps);
+    if (t < T) {
+      for (int c8 = lt * 8; c8 < d; c8 += 256 * 8) {
+        const uint4 r = *reinterpret_cast<const uint4*>(xr + c8);
+        const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+        uint32_t ob[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float a = __uint_as_float(rw[i] << 16) * inv, b = __uint_as_float(rw[i] & 0xffff0000u) * inv;
+          ob[i] = (uint32_t)float_to_bf16_bits(a) | ((uint32_t)float_to_bf16_bits(b) << 16);
+        }
+        const uint4 o = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+        *reinterpret_cast<uint4*>(xr + c8) = o;
+        if (xh_out) *reinterpret_cast<uint4*>(xh_out + (size_t)t * d + c8) = o;
+      }
+    }
+    consumer_sync();  // the partials are read; the normalised rows are in place
+  }
+}
+
+__device__ __forceinline__ void mbar_arrive_n(uint64_t* bar, uint32_t n) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(n) : "memory");
+}
+
+// After the last layer of a stack: RMSNorm of the residual rows, then the LM
+// head over all V rows and the arg-max (the arithmetic of lmhead.cu: fp16
+// weights, tokens scaled by 2^s exactly, fp32 sums, lowest row wins ties).
+// Tiles go to CTAs as in lmhead.cu (tile c, c + G, ...) and through the ring in
+// the order of the layers' uses (ring_i onward); a stage belongs to one
+// consumer warp here (nw = the stage count), so every warp waits on its own
+// stage's phases in order, and releases it for all 16 layer-phase arrivals.
+__device__ __noinline__ void lm_phase(const DecodeArgs& p, unsigned char* regA, unsigned char* x16,
+                                      unsigned char* ring, uint64_t* full, uint64_t* empty, float* part,
+                                      int* sexp, unsigned long long* wkey, int ring_i, int* fail) {
+  const int T = p.T, d = p.d, V = p.lm_V, NS = p.nstages;
+  const int G = gridDim.x, cta = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tbd = (int)tile_bytes(d), xstride = 2 * d + kSmemRowPad;
+  const int VT = V / kTileRows;
+  const int my_tiles = (VT > cta) ? (VT - 1 - cta) / G + 1 : 0;
+  if (warp == kDecWarps) {
+    if (lane == 0) {
+      for (int j = 0; j < my_tiles; ++j) {
+        const int i = ring_i + j, s = i % NS;
+        if (i >= NS && !mbar_wait(&empty[s], ((i / NS) - 1) & 1, p.st, 44)) {
+          *(volatile int*)fail = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], (uint32_t)tbd);
+        bulk_g2s(ring + (size_t)s * tbd, p.lm_w + ((size_t)cta + (size_t)j * G) * tbd, (uint32_t)tbd, &full[s]);
+      }
+    }
+    return;
+  }
+  // the final residual rows (written before barrier C), normalised, as scaled fp16
+  for (int c8 = tid * 8; c8 < T * d; c8 += kConsumers * 8) {
+    const int t = c8 / d, col = c8 - t * d;
+    *reinterpret_cast<uint4*>(regA + t * xstride + col * 2) = __ldcg(reinterpret_cast<const uint4*>(p.x + c8));
+  }
+  {
+    uint4* pad = reinterpret_cast<uint4*>(x16 + T * xstride);
+    for (int c = tid; c < d / 8; c += kConsumers) pad[c] = make_uint4(0, 0, 0, 0);
+  }
+  consumer_sync();
+  rmsnorm_rows(regA, T, d, xstride, p.eps, part, nullptr);
+  stage_tokens_f16(regA, x16, T, d, xstride, sexp, warp, kDecWarps, lane);
+  consumer_sync();
+
+  const int g = lane >> 2, c = lane & 3;
+  const int nw = NS;  // one stage per consumer warp (NS <= 16)
+  const unsigned char* xrow = x16 + (g < T ? g : T) * xstride;
+  const float un0 = (2 * c < T) ? pow2i(-sexp[2 * c]) : 0.f;
+  const float un1 = (2 * c + 1 < T) ? pow2i(-sexp[2 * c + 1]) : 0.f;
+  float best_v[2] = {-INFINITY, -INFINITY};
+  int best_i[2] = {0x7fffffff, 0x7fffffff};
+  bool ok = true;
+  if (warp < nw) {
+    const int j0 = ((warp - ring_i) % nw + nw) % nw;
+    for (int j = j0; j < my_tiles && ok; j += nw) {
+      const int i = ring_i + j, s = i % NS;
+      ok = mbar_wait(&full[s], (i / NS) & 1, p.st, 45);
+      if (!ok) break;
+      const unsigned char* tile = ring + (size_t)s * tbd;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int ch = 0; ch < d / kChunkK; ++ch) {
+        const unsigned char* cw = tile + ch * kChunkBytes;
+        const uint4 q0 = *reinterpret_cast<const uint4*>(cw + (g * 4 + c) * 16);
+        const uint4 q1 = *reinterpret_cast<const uint4*>(cw + ((g + 8) * 4 + c) * 16);
+        const uint2 s0 = *reinterpret_cast<const uint2*>(cw + kChunkQBytes + g * 8);
+        const uint2 s1 = *reinterpret_cast<const uint2*>(cw + kChunkQBytes + (g + 8) * 8);
+#pragma unroll 2
+        for (int gg = 0; gg < 4; ++gg) {
+          const int col = (ch * 4 + gg) * kGroup + c * 8;
+          uint32_t p0[4], p1[4];
+          nib_pairs4_f16(word_at(q0, gg), p0);
+          nib_pairs4_f16(word_at(q1, gg), p1);
+          const uint32_t a0[4] = {p0[0], p1[0], p0[1], p1[1]}, a1[4] = {p0[2], p1[2], p0[3], p1[3]};
+          const uint4 xb = *reinterpret_cast<const uint4*>(xrow + col * 2);
+          float dd[4];
+          mma_f16_z(dd, a0, xb.x, xb.y);
+          mma_f16(dd, a1, xb.z, xb.w, dd);
+          const float sc0 = scale_at(s0, gg), sc1 = scale_at(s1, gg);
+          acc[0] = fmaf(sc0, dd[0], acc[0]);
+          acc[1] = fmaf(sc0, dd[1], acc[1]);
+          acc[2] = fmaf(sc1, dd[2], acc[2]);
+          acc[3] = fmaf(sc1, dd[3], acc[3]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_n(&empty[s], kDecWarps);
+      const int vrow0 = (cta + j * G) * kTileRows;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int b = q & 1, tok = 2 * c + b, vrow = vrow0 + g + ((q >= 2) ? 8 : 0);
+        if (tok < T) {
+          const float v = acc[q] * (b ? un1 : un0);
+          if (p.lm_logits) p.lm_logits[(size_t)tok * V + vrow] = v;
+          if (v > best_v[b] || (v == best_v[b] && vrow < best_i[b])) {
+            best_v[b] = v;
+            best_i[b] = vrow;
+          }
+        }
+      }
+    }
+  }
+  if (!ok) *(volatile int*)fail = 1;
+  // per token: the warp's best over its rows (lanes with the same c), then over
+  // the warps as 64-bit keys (logit order, then the inverted row: lowest wins)
+  // wkey: [16 warps][8 tokens]
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    float v = best_v[b];
+    int ix = best_i[b];
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, ix, off);
+      if (ov > v || (ov == v && oi < ix)) {
+        v = ov;
+        ix = oi;
+      }
+    }
+    if (g == 0 && 2 * c + b < kDecMaxT)
+      wkey[warp * kDecMaxT + 2 * c + b] =
+          (ix == 0x7fffffff) ? 0ull : (((unsigned long long)float_order_key(v) << 32) | (0xffffffffu - (uint32_t)ix));
+  }
+  consumer_sync();
+  if (tid < T && *(volatile int*)fail == 0) {
+    unsigned long long key = 0ull;
+    for (int w = 0; w < kDecWarps; ++w) key = umax64(key, wkey[w * kDecMaxT + tid]);
+    if (key != 0ull) atomicMax(&p.lm_keys[tid], key);
+  }
+  // D: every CTA's keys folded; CTA 0 publishes the arg-max
+  if (grid_barrier(p.gbar, fail, p.st, 43, nullptr, 0) && cta == 0 && tid < T)
+    p.lm_argmax[tid] = (int32_t)(0xffffffffu - (uint32_t)(__ldcg(p.lm_keys + tid) & 0xffffffffull));
+}
+
+// The kernel body, one layer (kStack = false) or a stack of pre-norm layers
+// followed by RMSNorm, the LM head and the arg-max (kStack = true; layer l's
+// weights from tab[l], the residual updated in place).
+template <bool kStack>
+__device__ __forceinline__ void decode_body(const DecodeArgs& p, const LayerPtrs* tab) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxStages;
@@ -360,6 +573,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
   float* wr_s = reinterpret_cast<float*>(regB);
   const bool routed = (p.forced_ids == nullptr);
 
+  const bool lm = kStack && p.lm_w != nullptr;  // RMSNorm + LM head + arg-max after the layers
   if (tid == 0) {
     for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(&full[s], 1);
@@ -374,95 +588,66 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
     fence_mbar_init();
   }
   __syncthreads();
-  stamp(p, 0);
+  const unsigned long long* trace = p.trace;  // layer 0 only
+  stamp(trace, 0);
   if (tid == 0) grid_dep_launch();  // the next launch may be scheduled as SMs free up
 
-  // ---------------- P0: router rows (independent of the previous step) then x
-  if (warp == kDecWarps && lane == 0) {
-    if (routed && nexp > 0) {
-      mbar_arrive_expect_tx(wrbar, (uint32_t)nexp * d * 4u);
-      bulk_g2s(wr_s, p.w_router + (size_t)e_lo * d, (uint32_t)nexp * d * 4u, wrbar);
-    }
+  // router rows of the first layer (independent of the previous step)
+  if (warp == kDecWarps && lane == 0 && routed && kr > 0 && nexp > 0) {
+    const float* wr0 = kStack ? tab[0].w_router : p.w_router;
+    mbar_arrive_expect_tx(wrbar, (uint32_t)nexp * d * 4u);
+    bulk_g2s(wr_s, wr0 + (size_t)e_lo * d, (uint32_t)nexp * d * 4u, wrbar);
   }
-  // router bias of the logit this warp's lane 0 writes first (pair = warp), read now
   const int pairs = T * nexp;
   // warps per (token, expert) dot product: the largest power of two that keeps
   // every pair covered by the 16 consumer warps at once
   int wpp = 1;
   while (pairs > 0 && wpp < kDecWarps && wpp * 2 * pairs <= kDecWarps) wpp *= 2;
+  int ring_i = 0;  // ring uses so far (the producer and the consumers count alike)
+  const int L = kStack ? p.n_layers : 1;
+  for (int l = 0; l < L; ++l) {
+  const LayerPtrs lp = kStack ? tab[l] : LayerPtrs{p.gate, p.up, p.down, p.w_router, p.b_router};
+  int32_t* ids_out = (kStack && p.ids_out) ? p.ids_out + (size_t)l * R : p.ids_out;
+  float* w_out = (kStack && p.w_out) ? p.w_out + (size_t)l * R : p.w_out;
+  if (l > 0) trace = nullptr;
+  const uint32_t lpar = (uint32_t)(l & 1);  // phase parity of the layer's single-use barriers
+  // router bias of the logit this warp's lane 0 writes first (pair = warp), read now
   float bias0 = 0.f, biasA = 0.f;
-  if (routed && lane == 0 && warp < kDecWarps && warp < pairs && p.b_router != nullptr)
-    bias0 = p.b_router[e_lo + warp % nexp];
-  if (routed && wpp > 1 && tid < pairs && p.b_router != nullptr) biasA = p.b_router[e_lo + tid % nexp];
-  grid_dep_wait();  // the previous launch on this stream is complete and visible
-  stamp(p, 1);
+  if (routed && lane == 0 && warp < kDecWarps && warp < pairs && lp.b_router != nullptr)
+    bias0 = lp.b_router[e_lo + warp % nexp];
+  if (routed && wpp > 1 && tid < pairs && lp.b_router != nullptr) biasA = lp.b_router[e_lo + tid % nexp];
+  if (l == 0) {
+    grid_dep_wait();  // the previous launch on this stream is complete and visible
+    // arg-max keys: cleared once the previous launch (which may fold into them)
+    // is done, before this launch's first grid barrier; read after its last
+    if (lm && cta == 0 && tid < T) p.lm_keys[tid] = 0ull;
+  }
+  stamp(trace, 1);
   // residual of this CTA's first output tile, read now so that its latency is
   // off the combine at the end (one value per combine thread)
   uint16_t resid0 = 0;
   if (tid < T * kTileRows && cta < CT) resid0 = p.resid[(size_t)(tid >> 4) * d + (size_t)cta * kTileRows + (tid & 15)];
-  if (warp == kDecWarps && lane == 0) {
+  if (tid == 0) {  // the layer's input rows (later layers: written by the combines before barrier C)
+    if (l > 0) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      fence_proxy_async_smem();
+    }
     mbar_arrive_expect_tx(xbar, (uint32_t)T * 2u * d);
     for (int t = 0; t < T; ++t) bulk_g2s(regA + t * xstride, p.x + (size_t)t * d, 2u * d, xbar);
   }
 
   if (warp < kDecWarps) {
-    bool ok = mbar_wait(xbar, 0, p.st, 30);
-    stamp(p, 16);
-    if (p.prenorm) {  // taken by every consumer thread alike (the block has barriers)
-      // the staged rows are the residual: replace them in place by RMSNorm(x) with unit
-      // gain, reduced exactly as the standalone RMSNorm kernel does (256 threads per token,
-      // fp32 FMA chains, then eight warp partials in order), so both give the same bits;
-      // two tokens at a time
-      const int half = tid >> 8, lt = tid & 255;
-      for (int t0 = 0; t0 < T; t0 += 2) {
-        const int t = t0 + half;
-        uint16_t* xr = reinterpret_cast<uint16_t*>(regA + t * xstride);
-        float ss = 0.f;
-        if (t < T) {
-          for (int c8 = lt * 8; c8 < d; c8 += 256 * 8) {
-            const uint4 r = *reinterpret_cast<const uint4*>(xr + c8);
-            const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float a = __uint_as_float(rw[i] << 16), b = __uint_as_float(rw[i] & 0xffff0000u);
-              ss = fmaf(a, a, ss);
-              ss = fmaf(b, b, ss);
-            }
-          }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        if (lane == 0) rt.part[warp] = ss;
-        consumer_sync();
-        float tot = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) tot += rt.part[half * 8 + i];
-        const float inv = 1.0f / sqrtf(tot / (float)d + p.eps);
-        if (t < T) {
-          for (int c8 = lt * 8; c8 < d; c8 += 256 * 8) {
-            const uint4 r = *reinterpret_cast<const uint4*>(xr + c8);
-            const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
-            uint32_t ob[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float a = __uint_as_float(rw[i] << 16) * inv, b = __uint_as_float(rw[i] & 0xffff0000u) * inv;
-              ob[i] = (uint32_t)float_to_bf16_bits(a) | ((uint32_t)float_to_bf16_bits(b) << 16);
-            }
-            const uint4 o = make_uint4(ob[0], ob[1], ob[2], ob[3]);
-            *reinterpret_cast<uint4*>(xr + c8) = o;
-            if (p.xh_out && cta == 0) *reinterpret_cast<uint4*>(p.xh_out + (size_t)t * d + c8) = o;
-          }
-        }
-        consumer_sync();  // the partials are read; the normalised rows are in place
-      }
-    }
+    bool ok = mbar_wait(xbar, lpar, p.st, 30);
+    stamp(trace, 16);
+    if (p.prenorm)  // taken by every consumer thread alike (the function has barriers)
+      rmsnorm_rows(regA, T, d, xstride, p.eps, rt.part, cta == 0 ? p.xh_out : nullptr);
     {  // the zeroed pad row after the fp16 tokens (read by lanes without a token)
       uint4* pad = reinterpret_cast<uint4*>(x16 + T * xstride);
       for (int c = tid; c < d / 8; c += kConsumers) pad[c] = make_uint4(0, 0, 0, 0);
     }
     if (routed && kr > 0) {  // (kr = 0: a dense layer, nothing to score)
-      if (nexp > 0) ok = mbar_wait(wrbar, 0, p.st, 31) && ok;
-      stamp(p, 17);
+      if (nexp > 0) ok = mbar_wait(wrbar, lpar, p.st, 31) && ok;
+      stamp(trace, 17);
       if (!ok) *(volatile int*)fail = 1;
       // (token, expert) dot products: wpp warps per pair, each over a K slice
       // (two accumulators per lane), then the slices are added in order
@@ -498,31 +683,31 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (lane == 0) {
           if (wpp == 1) {
-            const float b = (pr == warp) ? bias0 : (p.b_router ? p.b_router[e_lo + el] : 0.f);
+            const float b = (pr == warp) ? bias0 : (lp.b_router ? lp.b_router[e_lo + el] : 0.f);
             p.logits[(size_t)t * E + e_lo + el] = acc + b;
           } else {
             rt.part[pr * wpp + sl] = acc;
           }
         }
       }
-      stamp(p, 24);
+      stamp(trace, 24);
       if (wpp > 1) {
         consumer_sync();
-        stamp(p, 25);
+        stamp(trace, 25);
         if (tid < pairs) {
           float acc = 0.f;
           for (int sl = 0; sl < wpp; ++sl) acc += rt.part[tid * wpp + sl];
           p.logits[(size_t)(tid / nexp) * E + e_lo + tid % nexp] = acc + biasA;
         }
       }
-      stamp(p, 18);
-      stamp(p, 2);
+      stamp(trace, 18);
+      stamp(trace, 2);
       // A: every logit written.  Between the arrival and the wait the staged
       // tokens become scaled fp16 (the router has read them).
-      const unsigned tgt = grid_arrive(p.gbar, p.trace, 22);
+      const unsigned tgt = grid_arrive(p.gbar, trace, 22);
       if (ok && warp > 0) stage_tokens_f16(regA, x16, T, d, xstride, rt.sexp, warp - 1, kDecWarps - 1, lane);
       grid_wait(p.gbar, tgt, fail, p.st, 32);
-      stamp(p, 3);
+      stamp(trace, 3);
     } else {
       if (!ok) *(volatile int*)fail = 1;
       consumer_sync();  // (prenorm) every normalised row is in place
@@ -551,19 +736,20 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
             (tid < E) ? (((unsigned long long)float_order_key(__ldcg(p.logits + tid)) << 32) |
                          (0xffffffffu - (uint32_t)tid))
                       : 0ull;
-        stamp(p, 26);
+        stamp(trace, 26);
         unsigned long long m = key;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) m = umax64(m, __shfl_xor_sync(0xffffffffu, m, off));
         if (lane == 0) rt.wmax[warp] = m;
         consumer_sync();
-        stamp(p, 27);
+        stamp(trace, 27);
         // every warp finds tau itself: lanes 0..15 rank the 16 warp maxima
+        // (independent shared-memory loads, no shuffle chain)
         const unsigned long long wm = (lane < kDecWarps) ? rt.wmax[lane] : 0ull;
         int rank = 0;
 #pragma unroll
         for (int w = 0; w < kDecWarps; ++w) {
-          const unsigned long long o = __shfl_sync(0xffffffffu, wm, w);
+          const unsigned long long o = rt.wmax[w];
           rank += (o > wm) || (o == wm && w < lane);
         }
         const unsigned at_k = __ballot_sync(0xffffffffu, lane < kDecWarps && rank == kr - 1);
@@ -585,9 +771,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
           for (int off = 16; off > 0; off >>= 1) ez += __shfl_xor_sync(0xffffffffu, ez, off);
           if (lane == 0) rt.part[warp] = ez;
         }
-        stamp(p, 28);
+        stamp(trace, 28);
         consumer_sync();
-        stamp(p, 29);
+        stamp(trace, 29);
         if (is_cand) {
           const int nc = rt.misc[2];
           int r = 0;
@@ -595,7 +781,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
           if (r < kr) rt.sel[r] = key;
         }
         consumer_sync();
-        stamp(p, 10);
+        stamp(trace, 10);
         if (warp == 0) {
           // lane j < kr: the j-th chosen expert; lane kr (n_shared = 1): the
           // shared expert, bank entry E, weight 1.  One row per expert, so the
@@ -619,8 +805,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
           } else {
             for (int w = 0; w < kDecWarps; ++w) z += rt.part[w];
           }
+          // rank of this lane's id among the k ids (all distinct), counted from
+          // shared memory with independent loads (a loop of shuffles with a
+          // varying source lane is a long serial chain here)
+          if (lane < k) rt.act_e[lane] = e;
+          __syncwarp();
           int pos = 0;
-          for (int j = 0; j < k; ++j) pos += __shfl_sync(0xffffffffu, e, j) < e;
+#pragma unroll 8
+          for (int j = 0; j < k; ++j) pos += rt.act_e[j] < e;
+          __syncwarp();
           if (lane < k) {
             const float wg = (lane < kr) ? ez / z : 1.0f;
             rt.ids[lane] = e;
@@ -631,8 +824,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
             rt.act_off[pos] = pos;
             rt.first[lane] = pos + 1;
             if (cta == 0) {
-              if (p.ids_out) p.ids_out[lane] = e;
-              if (p.w_out) p.w_out[lane] = wg;
+              if (ids_out) ids_out[lane] = e;
+              if (w_out) w_out[lane] = wg;
             }
           }
           if (lane == 0) {
@@ -642,7 +835,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
           }
         }
         grouped = true;
-        stamp(p, 11);
+        stamp(trace, 11);
       } else if (routed) {
         // a dense layer (kr = 0): each token's one row is the shared expert
         for (int r = tid; r < R; r += kConsumers) {
@@ -687,7 +880,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
           rt.first[r] = (e >= 0 && before == 0) ? less + 1 : 0;
         }
         consumer_sync();
-        stamp(p, 10);
+        stamp(trace, 10);
         for (int r = tid; r < R; r += kConsumers) {
           if (rt.first[r] > 0) {
             const int e = rt.ids[r];
@@ -707,19 +900,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
           }
         }
         consumer_sync();
-        stamp(p, 11);
+        stamp(trace, 11);
         if (cta == 0) {
           for (int r = tid; r < R; r += kConsumers) {
-            if (p.ids_out) p.ids_out[r] = rt.ids[r];
-            if (p.w_out) p.w_out[r] = rt.w[r];
+            if (ids_out) ids_out[r] = rt.ids[r];
+            if (w_out) w_out[r] = rt.w[r];
           }
         }
       }
     }
   }
   __syncthreads();  // routing tables visible to the producer warp
-  stamp(p, 4);
-  if (*(volatile int*)fail) return;
+  stamp(trace, 4);
+  if (*(volatile int*)fail) break;
 
   const int U = rt.misc[0];
   const int n_up = U * RT;
@@ -727,38 +920,50 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
 
   // ---------------- producer: this CTA's tiles, in consumption order
   if (warp == kDecWarps) {
+    int i = ring_i;
     if (lane == 0) {
-      int i = 0;
-      for (int u = u_lo; u < u_hi; ++u) {
+      bool pok = true;  // a wait that ran out stops the issue (consumers then time out too)
+#pragma unroll 1
+      for (int u = u_lo; u < u_hi && pok; ++u) {
         const int a = u / RT, r16 = u - a * RT;
         const size_t toff = ((size_t)rt.act_e[a] * RT + r16) * tbd;
+#pragma unroll 1
         for (int m = 0; m < 2; ++m, ++i) {
           const int s = i % NS;
-          if (i >= NS && !mbar_wait(&empty[s], ((i / NS) - 1) & 1, p.st, 35)) return;
+          if (i >= NS && !mbar_wait(&empty[s], ((i / NS) - 1) & 1, p.st, 35)) {
+            pok = false;
+            break;
+          }
           mbar_arrive_expect_tx(&full[s], (uint32_t)tbd);
-          bulk_g2s(ring + (size_t)s * tbd, (m == 0 ? p.gate : p.up) + toff, (uint32_t)tbd, &full[s]);
+          bulk_g2s(ring + (size_t)s * tbd, (m == 0 ? lp.gate : lp.up) + toff, (uint32_t)tbd, &full[s]);
         }
       }
-      for (int ct = cta; ct < CT; ct += G) {
+#pragma unroll 1
+      for (int ct = cta; ct < CT && pok; ct += G) {
+#pragma unroll 1
         for (int a0 = 0; a0 < U; a0 += dps, ++i) {
           const int s = i % NS;
-          if (i >= NS && !mbar_wait(&empty[s], ((i / NS) - 1) & 1, p.st, 36)) return;
+          if (i >= NS && !mbar_wait(&empty[s], ((i / NS) - 1) & 1, p.st, 36)) {
+            pok = false;
+            break;
+          }
           const int n = min(dps, U - a0);
           mbar_arrive_expect_tx(&full[s], (uint32_t)n * tbi);
+#pragma unroll 1
           for (int j = 0; j < n; ++j)
             bulk_g2s(ring + (size_t)s * tbd + (size_t)j * tbi,
-                     p.down + ((size_t)rt.act_e[a0 + j] * CT + ct) * tbi, (uint32_t)tbi, &full[s]);
+                     lp.down + ((size_t)rt.act_e[a0 + j] * CT + ct) * tbi, (uint32_t)tbi, &full[s]);
         }
       }
+      if (!pok) *(volatile int*)fail = 1;
     }
-    return;
-  }
-
+    ring_i = __shfl_sync(0xffffffffu, i, 0);
+  } else {
   // ---------------- consumers
   const int g = lane >> 2, c = lane & 3;
   float* red = reinterpret_cast<float*>(regB);            // [2][16 warps][32][8]
   float* ypart = red + 2 * kDecWarps * 32 * 8;            // [4][R][16]
-  int i = 0;
+  int i = ring_i;
   bool ok = true;
 
   // P2: gate/up units, one 128-column chunk per warp
@@ -767,8 +972,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
     const int na = rt.act_off[a + 1] - rt.act_off[a];
     const int sg = i % NS, su = (i + 1) % NS;
     if (ok) ok = mbar_wait(&full[sg], (i / NS) & 1, p.st, 37) && mbar_wait(&full[su], ((i + 1) / NS) & 1, p.st, 38);
-    if (u == u_lo) stamp(p, 12);
-    if (u == u_lo + 1) stamp(p, 9);
+    if (u == u_lo) stamp(trace, 12);
+    if (u == u_lo + 1) stamp(trace, 9);
     const unsigned char* tg = ring + (size_t)sg * tbd;
     const unsigned char* tu = ring + (size_t)su * tbd;
     // token row of this lane's B fragment (n = g)
@@ -827,7 +1032,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
       my[4 + j] = au4[j];
     }
     if (!ok) *(volatile int*)fail = 1;
-    if (u == u_lo) stamp(p, 8);
+    if (u == u_lo) stamp(trace, 8);
     consumer_sync();
     // one thread per (row, token) output of the 16 x 8 tile
     if (tid < kTileRows * 8) {
@@ -851,11 +1056,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
         p.h_lo[o] = lo;
       }
     }
-    if (u == u_lo) stamp(p, 15);
+    if (u == u_lo) stamp(trace, 15);
   }
-  stamp(p, 5);
-  if (!grid_barrier(p.gbar, fail, p.st, 39, p.trace, 23)) return;  // B: every h written
-  stamp(p, 6);
+  stamp(trace, 5);
+  const bool passed_b = grid_barrier(p.gbar, fail, p.st, 39, trace, 23);  // B: every h written
+  stamp(trace, 6);
+  if (passed_b) {
+  // the next layer's router rows, into region B while P3 runs (the P2 partials
+  // there are dead; P3's partials sit above them)
+  if (kStack && tid == 0 && l + 1 < L && routed && kr > 0 && nexp > 0) {
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(wrbar, (uint32_t)nexp * d * 4u);
+    bulk_g2s(wr_s, tab[l + 1].w_router + (size_t)e_lo * d, (uint32_t)nexp * d * 4u, wrbar);
+  }
 
   // P3: down projection of this CTA's 16-column tiles, then the combine
   const int Rv = rt.act_off[U];  // rows that reached an expert
@@ -872,9 +1085,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
         bulk_g2s(hhi, p.h_hi, (uint32_t)Rv * hstride, hbar);
         bulk_g2s(hlo, p.h_lo, (uint32_t)Rv * hstride, hbar);
       }
-      if (ok) ok = mbar_wait(hbar, 0, p.st, 40);
+      if (ok) ok = mbar_wait(hbar, lpar, p.st, 40);
       h_loaded = true;
-      stamp(p, 13);
+      stamp(trace, 13);
     }
     // W_down stages of this output tile in ring order; four warps per expert
     // tile, a quarter of the reduction each.  A warp releases a stage as soon
@@ -884,7 +1097,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
     for (int st = 0; st < nst; ++st) {
       const int s = (i + st) % NS;
       if (ok) ok = mbar_wait(&full[s], ((i + st) / NS) & 1, p.st, 41);
-      if (st == 0 && ct == cta) stamp(p, 19);
+      if (st == 0 && ct == cta) stamp(trace, 19);
       for (int j = warp >> 2; j < dps; j += kDecWarps / 4) {
         const int a = st * dps + j;
         if (a >= U) break;
@@ -941,12 +1154,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
       }
       __syncwarp();
       if (lane == 0) mbar_arrive1(&empty[s]);
-      if (st == 0 && ct == cta) stamp(p, 20);
+      if (st == 0 && ct == cta) stamp(trace, 20);
     }
     i += nst;
     if (!ok) *(volatile int*)fail = 1;
     consumer_sync();
-    stamp(p, 14);
+    stamp(trace, 14);
     // combine: out[t, ct*16 + col] = resid + sum_j w_j * y_j (ascending j)
     if (tid < T * kTileRows) {
       const int t = tid >> 4, col = tid & 15;
@@ -969,7 +1182,26 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(DecodeArgs
     }
     consumer_sync();
   }
-  stamp(p, 7);
+  stamp(trace, 7);
+  }  // passed_b
+  ring_i = i;
+  // C: every output column of the layer written before the next layer (or the
+  // LM head) reads whole rows
+  if (kStack && (l + 1 < L || lm)) grid_barrier(p.gbar, fail, p.st, 42, nullptr, 0);
+  }  // consumers
+  __syncthreads();
+  if (*(volatile int*)fail) break;
+  }  // layers
+  if (lm && *(volatile int*)fail == 0)
+    lm_phase(p, regA, x16, ring, full, empty, rt.part, rt.sexp, rt.cand, ring_i, fail);
+}
+
+__global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const __grid_constant__ DecodeArgs p) {
+  decode_body<false>(p, nullptr);
+}
+
+__global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __grid_constant__ StackArgs a) {
+  decode_body<true>(a.base, a.tab);
 }
 
 struct DecodePlan {
@@ -1028,29 +1260,32 @@ bool decode_fused_eligible(int T, int d, int E, int k, int I, int n_shared) {
   return plan(T, d, E, k, I, n_shared, sm_count()).ok;
 }
 
-cudaError_t launch_decode_fused(const DecodeLaunch& L, cudaStream_t s) {
-  const int G = sm_count();
-  const DecodePlan pl = plan(L.T, L.d, L.E, L.k, L.I, L.n_shared, G);
-  if (!pl.ok) return cudaErrorNotSupported;
-  static int attr_set[64] = {};
-  cudaError_t err = ensure_smem_attr(decode_layer_kernel, pl.smem, attr_set);
+namespace {
+
+// Shared-memory attribute and the one-CTA-per-SM residency check of a fused
+// kernel, once per device and size.
+template <typename K>
+cudaError_t prepare_fused(K* kernel, size_t smem, int* attr_set, size_t* occ_ok) {
+  cudaError_t err = ensure_smem_attr(kernel, smem, attr_set);
   if (err != cudaSuccess) return err;
   // The CTAs wait on each other at the grid barriers, so all G of them must be
-  // resident at once: one per SM.  Checked once per device and shared-memory
-  // size; a device where they do not fit takes the unfused kernels.
-  static size_t occ_ok[64] = {};
+  // resident at once: one per SM.  A device where they do not fit takes the
+  // unfused kernels.
   int dev = 0;
   if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
   if (dev < 0 || dev >= 64) return cudaErrorNotSupported;
-  if (occ_ok[dev] < pl.smem) {
+  if (occ_ok[dev] < smem) {
     int per_sm = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_layer_kernel, kDecThreads, pl.smem);
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kDecThreads, smem);
     if (err != cudaSuccess) return err;
-    if ((long)per_sm * sm_count() < G) return cudaErrorNotSupported;
-    occ_ok[dev] = pl.smem;
+    if (per_sm < 1) return cudaErrorNotSupported;
+    occ_ok[dev] = smem;
   }
+  return cudaSuccess;
+}
 
-  DecodeArgs a;
+DecodeArgs fill_args(const DecodeLaunch& L, const DecodePlan& pl, int G) {
+  DecodeArgs a = {};
   a.x = L.x;
   a.resid = L.resid;
   a.T = L.T;
@@ -1085,20 +1320,72 @@ cudaError_t launch_decode_fused(const DecodeLaunch& L, cudaStream_t s) {
   a.prenorm = L.prenorm;
   a.eps = L.eps;
   a.xh_out = L.xh_out;
+  a.n_layers = 1;
   a.trace = static_cast<unsigned long long*>(g_trace_buf);
   if (a.trace && g_trace_bytes < (size_t)G * kTracePoints * sizeof(unsigned long long)) a.trace = nullptr;
+  return a;
+}
 
+template <typename K, typename A>
+cudaError_t launch_fused(K* kernel, const A& args, int G, size_t smem, int pdl, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(G);
   cfg.blockDim = dim3(kDecThreads);
-  cfg.dynamicSmemBytes = pl.smem;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = L.pdl ? 1 : 0;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_layer_kernel, a);
+  return cudaLaunchKernelEx(&cfg, kernel, args);
+}
+
+}  // namespace
+
+cudaError_t launch_decode_fused(const DecodeLaunch& L, cudaStream_t s) {
+  const int G = sm_count();
+  const DecodePlan pl = plan(L.T, L.d, L.E, L.k, L.I, L.n_shared, G);
+  if (!pl.ok) return cudaErrorNotSupported;
+  static int attr_set[64] = {};
+  static size_t occ_ok[64] = {};
+  cudaError_t err = prepare_fused(decode_layer_kernel, pl.smem, attr_set, occ_ok);
+  if (err != cudaSuccess) return err;
+  return launch_fused(decode_layer_kernel, fill_args(L, pl, G), G, pl.smem, L.pdl, s);
+}
+
+bool decode_stack_eligible(int T, int d, int E, int k, int I, int n_shared, int n_layers, int V) {
+  const int G = sm_count();
+  const DecodePlan pl = plan(T, d, E, k, I, n_shared, G);
+  const int nexp = (E + G - 1) / G;
+  // the next layer's router rows go below the down projection's partials in region B
+  return pl.ok && n_layers >= 1 && n_layers <= kMaxStackLayers && (size_t)nexp * d * 4 <= (size_t)2 * kDecWarps * 32 * 8 * 4 &&
+         (V == 0 || V % kTileRows == 0);
+}
+
+cudaError_t launch_decode_stack(const DecodeLaunch& L, const StackLayer* layers, int n_layers, const uint8_t* lm_w,
+                                int V, float* lm_logits, unsigned long long* lm_keys, int32_t* lm_argmax,
+                                cudaStream_t s) {
+  const int G = sm_count();
+  if (!decode_stack_eligible(L.T, L.d, L.E, L.k, L.I, L.n_shared, n_layers, V)) return cudaErrorNotSupported;
+  const DecodePlan pl = plan(L.T, L.d, L.E, L.k, L.I, L.n_shared, G);
+  static int attr_set[64] = {};
+  static size_t occ_ok[64] = {};
+  cudaError_t err = prepare_fused(decode_stack_kernel, pl.smem, attr_set, occ_ok);
+  if (err != cudaSuccess) return err;
+  StackArgs a;
+  a.base = fill_args(L, pl, G);
+  a.base.n_layers = n_layers;
+  a.base.lm_w = lm_w;
+  a.base.lm_V = V;
+  a.base.lm_logits = lm_logits;
+  a.base.lm_keys = lm_keys;
+  a.base.lm_argmax = lm_argmax;
+  for (int l = 0; l < kMaxStackLayers; ++l) {
+    const StackLayer& w = layers[l < n_layers ? l : 0];
+    a.tab[l] = LayerPtrs{w.gate, w.up, w.down, w.w_router, w.b_router};
+  }
+  return launch_fused(decode_stack_kernel, a, G, pl.smem, L.pdl, s);
 }
 
 }  // namespace bitmoe

@@ -87,6 +87,21 @@ bool decode_fused_eligible(int T, int d, int E, int k, int I, int n_shared);
 extern void* g_trace_buf;
 extern size_t g_trace_bytes;
 cudaError_t launch_decode_fused(const DecodeLaunch& L, cudaStream_t s);
+// Whole decode stack in one launch: n_layers pre-norm layers (L.prenorm = 1, x,
+// resid and out all the residual, updated in place), then (lm_w != null)
+// RMSNorm, the LM head over V rows and the arg-max.  The weights of L are unused;
+// layer l's come from layers[l].
+struct StackLayer {
+  const uint8_t* gate;
+  const uint8_t* up;
+  const uint8_t* down;
+  const float* w_router;
+  const float* b_router;
+};
+bool decode_stack_eligible(int T, int d, int E, int k, int I, int n_shared, int n_layers, int V);
+cudaError_t launch_decode_stack(const DecodeLaunch& L, const StackLayer* layers, int n_layers, const uint8_t* lm_w,
+                                int V, float* lm_logits, unsigned long long* lm_keys, int32_t* lm_argmax,
+                                cudaStream_t s);
 
 // ---------------------------------------------------------------- combine / norm / pack (misc.cu)
 cudaError_t launch_combine(const float* y_rows, const int32_t* inv, const float* w, const uint16_t* resid, int T,

@@ -256,6 +256,39 @@ bitmoe_status_t moe_forward_prenorm(const uint16_t* residual, int64_t T, const b
                                     uint16_t* out, float* out_f32, void* workspace, size_t workspace_bytes,
                                     void* stream);
 
+/*
+ * A whole decode step of a stack of pre-norm MoE layers in ONE launch:
+ *   for l = 0 .. n_layers-1:  residual = residual + MoE_l(RMSNorm(residual))
+ * (each layer exactly as moe_forward_prenorm computes it, the residual kept in
+ * bf16 and updated in place), then, when lm_packed is given,
+ *   argmax[t] = the lowest v maximising (RMSNorm(residual) Wlm^T)[t, v]
+ * with the LM head of lmhead_int4_gemv (logits [T, V] written when not NULL).
+ * One persistent kernel: the layers follow each other through grid-wide
+ * barriers instead of kernel boundaries, and each layer's router rows are
+ * fetched while the previous layer's down projection runs.
+ * residual [T, d] bf16 (in/out).  layers: a HOST array of n_layers weight sets
+ * (each as moe_forward's; all layers share `shape`).  topk_ids_out (nullable)
+ * [n_layers, T, kt] int32.  lm_packed: the packed [V, d] LM head or NULL (then
+ * argmax / logits are unused).  The workspace is moe_stack_workspace_size()
+ * bytes, zero-filled before its first use, as for moe_forward.
+ * Supported: T <= 8, n_layers <= 64, the fused decode kernel's shapes (those
+ * of moe_forward's batch <= 8 path), V % 16 == 0; otherwise
+ * BITMOE_ERR_UNSUPPORTED, and the caller steps the layers with
+ * moe_forward_prenorm, then bitmoe_rmsnorm and lmhead_int4_gemv, which compute
+ * the same bits.  Its CTAs wait on each other across all layers, so it should
+ * not share the device with concurrent kernels that occupy SMs for long.
+ * Source: "Flint 40B : Best Mid Sized LLM", transcript 06:43 (a kernel that
+ * fuses the entire decode pass into a single launch, written there for Apple
+ * GPUs; here the 49-layer MoE stack and the output layer on B300) and 02:35
+ * (the 49-layer decoder); "Recursive_SI's First Model Unveiled!", section
+ * "Inference Kernel".
+ */
+size_t moe_stack_workspace_size(const bitmoe_moe_shape_t* shape, int64_t T);
+bitmoe_status_t moe_stack_decode(uint16_t* residual, int64_t T, const bitmoe_moe_shape_t* shape,
+                                 const bitmoe_moe_weights_t* layers, int64_t n_layers, float eps,
+                                 const uint8_t* lm_packed, int64_t V, float* logits, int32_t* argmax,
+                                 int32_t* topk_ids_out, void* workspace, size_t workspace_bytes, void* stream);
+
 /* ------------------------------------------------------------ LM head */
 
 size_t lmhead_workspace_size(int64_t T, int64_t d, int64_t V);

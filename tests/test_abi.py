@@ -96,3 +96,27 @@ def test_host_side_validation_without_gpu(built):
                            None, 0, None) == 0
     for code in range(7):
         assert lib.bitmoe_status_string(code)
+
+
+def test_stack_call_rejects_on_the_host_without_gpu(built):
+    """moe_stack_decode: argument and shape checks that return before any launch."""
+    import bit_expert_ffn_warp_b300 as bm
+    lib = bm._lib
+    sh = bm.MoeShape(2048, 256, 8, 512, 32, 1)
+    ws_bytes = lib.moe_stack_workspace_size(ctypes.byref(sh), 1)
+    assert ws_bytes == lib.moe_workspace_size(ctypes.byref(sh), 1) + 256
+    fake = ctypes.c_void_p(1 << 20)  # 16-byte aligned stand-in, never dereferenced on these paths
+    w = bm.MoeWeights(1 << 20, 1 << 20, 1 << 20, 1 << 20, None)
+    arr = (bm.MoeWeights * 65)(*([w] * 65))
+    call = lambda T, n, ws=fake, nb=ws_bytes, V=0, lm=None, am=None: lib.moe_stack_decode(
+        fake, T, ctypes.byref(sh), arr, n, 1e-6, lm, V, None, am, None, ws, nb, None)
+    assert call(0, 1) == 0                   # no tokens: nothing to do
+    assert call(1, 0) == 1                   # no layers
+    assert call(9, 2) == 2                   # T > 8: not the fused decode kernel's shapes
+    assert call(1, 65) == 2                  # more layers than the launch carries
+    assert call(1, 2, V=100, lm=fake, am=fake) == 2  # V % 16 != 0
+    assert call(1, 2, lm=fake, am=None, V=4096) == 1  # an LM head needs the arg-max output
+    assert call(1, 2, nb=ws_bytes - 1) == 3  # workspace too small
+    bad = (bm.MoeWeights * 2)(w, bm.MoeWeights(1 << 20, None, 1 << 20, 1 << 20, None))
+    assert lib.moe_stack_decode(fake, 1, ctypes.byref(sh), bad, 2, 1e-6, None, 0, None, None, None, fake,
+                                ws_bytes, None) == 1

@@ -58,6 +58,7 @@ def run_stack(x_bits):
     _, am = bm.lmhead_int4_gemv(xh, lm, V, bm.lmhead_workspace(T, D, V), want_logits=False)
     torch.cuda.synchronize()
     assert bm.bitmoe_get_device_status(ws) == 0
+    _STACK["last_resid"] = resid.clone()
     return rec, xh.clone(), am
 
 
@@ -120,3 +121,54 @@ def test_prenorm_step_equals_rmsnorm_then_layer(T):
     assert bm.bitmoe_get_device_status(ws) == 0
     assert torch.equal(xh_a, xh_b)
     assert torch.equal(out_a, out_b) and torch.equal(o_a, o_b)
+
+
+# ------------------------------------------------------------------ one launch for the whole stack
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_fused_stack_kernel_equals_layer_steps(T):
+    """moe_stack_decode (49 layers + RMSNorm + LM head in one launch) gives the bits
+    of the per-layer calls: every layer's expert ids, the final residual and the
+    arg-max -- the per-layer path being the one checked against the oracle above."""
+    layers, lm = stack()
+    x0 = synth.activations(SEED + 11, T, D, step=T)
+    rec, _, am_ref = run_stack(x0)
+    resid_ref = _STACK["last_resid"]
+    resid = torch_bf16_from_bits(x0)
+    ws = bm.moe_stack_workspace(layers[0], T)
+    ids = torch.full((N_LAYERS, T, K), -7, dtype=torch.int32, device="cuda")
+    logits = torch.empty((T, V), dtype=torch.float32, device="cuda")
+    _, am = bm.moe_stack_decode(resid, layers, ws, lm_w=lm, V=V, ids_out=ids, logits=logits)
+    torch.cuda.synchronize()
+    assert bm.bitmoe_get_device_status(ws) == 0
+    for l in range(N_LAYERS):
+        assert torch.equal(ids[l], rec[l][3]), f"layer {l}: expert ids"
+    assert torch.equal(resid, resid_ref)
+    assert torch.equal(am, am_ref)
+    # the logits it wrote are the LM head's on the final normalised residual
+    xh = bm.bitmoe_rmsnorm(resid_ref)
+    ref_logits, _ = bm.lmhead_int4_gemv(xh, lm, V, bm.lmhead_workspace(T, D, V))
+    torch.cuda.synchronize()
+    assert torch.equal(logits, ref_logits)
+
+
+def test_fused_stack_kernel_few_layers_repeated_without_lm_head():
+    """Three layers, no LM head, two calls in a row on one workspace (the grid-barrier
+    counter and the barriers' phases carry over): the residual of each call equals
+    the per-layer steps'."""
+    layers, _ = stack()
+    sub = layers[10:13]
+    T = 2
+    ws = bm.moe_stack_workspace(sub[0], T)
+    ws_l = bm.moe_workspace(sub[0], T)
+    for call in range(2):
+        x0 = synth.activations(SEED + 20 + call, T, D, step=call)
+        ref = torch_bf16_from_bits(x0)
+        for lay in sub:
+            bm.moe_forward_prenorm(ref, lay, ws_l, out=ref)
+        resid = torch_bf16_from_bits(x0)
+        bm.moe_stack_decode(resid, sub, ws)
+        torch.cuda.synchronize()
+        assert bm.bitmoe_get_device_status(ws) == 0
+        assert torch.equal(resid, ref), f"call {call}"
