@@ -1,4 +1,4 @@
-"""fp64 CPU oracle of the int4 MoE layer and int4 LM head (ctypes front end).
+"""fp64 CPU oracle of the 4-bit (int4 or NVFP4) MoE layer and LM head (ctypes front end).
 
 TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by ``__graft_entry__.smoke()``
 and by the CPU-baseline leg of ``bench.py``; never by the product package.
@@ -61,6 +61,14 @@ def _lib():
             "oracle_rmsnorm": (ctypes.c_int, [P, I64, I64, ctypes.c_double, P]),
             "oracle_lmhead": (ctypes.c_int, [P, I64, I64, I64, I64, P, P, P, P, P]),
             "oracle_num_threads": (ctypes.c_int, []),
+            "oracle_e2m1_to_f64": (ctypes.c_double, [ctypes.c_uint8]),
+            "oracle_e4m3_to_f64": (ctypes.c_double, [ctypes.c_uint8]),
+            "oracle_dequant_nvfp4": (ctypes.c_int, [P, P, ctypes.c_float, I64, I64, P]),
+            "oracle_expert_ffn_nvfp4": (ctypes.c_int, [P, I64, I64, I64, I64, I64, P, P, P, P, P, P, P, P, P, P,
+                                                       P, P]),
+            "oracle_moe_forward_nvfp4": (ctypes.c_int, [P, P, I64, I64, I64, I64, I64, I64, ctypes.c_int, P, P,
+                                                        P, P, P, P, P, P, P, P, P, P, P, P, P, P, P]),
+            "oracle_lmhead_nvfp4": (ctypes.c_int, [P, I64, I64, I64, P, P, ctypes.c_float, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -115,6 +123,40 @@ def dequant_int4(q: np.ndarray, s: np.ndarray, group: int = 32) -> np.ndarray:
     out = np.empty((rows, K), np.float64)
     _check(_lib().oracle_dequant_int4(_p(q), _p(s), rows, K, group, _p(out)), "dequant_int4")
     return out.reshape(q.shape[:-1] + (K,))
+
+
+def e2m1_to_f64(codes: np.ndarray) -> np.ndarray:
+    """Values of FP4 E2M1 codes (the low nibble of each uint8)."""
+    f = np.vectorize(_lib().oracle_e2m1_to_f64, otypes=[np.float64])
+    return f(np.asarray(codes, np.uint8) & np.uint8(15))
+
+
+def e4m3_to_f64(b: np.ndarray) -> np.ndarray:
+    """Values of FP8 E4M3 bytes (NaN for the two NaN codes)."""
+    f = np.vectorize(_lib().oracle_e4m3_to_f64, otypes=[np.float64])
+    return f(np.asarray(b, np.uint8))
+
+
+def dequant_nvfp4(q: np.ndarray, s: np.ndarray, ts: float) -> np.ndarray:
+    """One NVFP4 matrix: q [rows, K/2] codes, s [rows, K/16] E4M3 bytes, ts fp32."""
+    q = _c(q, np.uint8)
+    s = _c(s, np.uint8)
+    rows, K = q.shape[0], q.shape[1] * 2
+    out = np.empty((rows, K), np.float64)
+    _check(_lib().oracle_dequant_nvfp4(_p(q), _p(s), float(np.float32(ts)), rows, K, _p(out)), "dequant_nvfp4")
+    return out
+
+
+def is_nvfp4(layer: dict) -> bool:
+    """A layer dict whose expert banks are NVFP4 (codes *_q, E4M3 *_s, fp32 tensor scales *_ts)."""
+    return "gate_ts" in layer
+
+
+def _nvfp4_args(layer):
+    out = []
+    for n in ("gate", "up", "down"):
+        out += [_c(layer[n + "_q"], np.uint8), _c(layer[n + "_s"], np.uint8), _c(layer[n + "_ts"], np.float32)]
+    return out
 
 
 # ---------------------------------------------------------------- routing
@@ -196,10 +238,15 @@ def expert_ffn(x, layer, ids, group=32, want_h=False):
     k = ids.shape[1]
     gq = _c(layer["gate_q"], np.uint8)
     E, I = gq.shape[0], gq.shape[1]
-    args = [_c(layer[n], np.uint8 if n.endswith("_q") else np.uint16)
-            for n in ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")]
     y = np.empty((T * k, d), np.float64)
     h = np.empty((T * k, I), np.float64) if want_h else None
+    if is_nvfp4(layer):
+        args = _nvfp4_args(layer)
+        _check(_lib().oracle_expert_ffn_nvfp4(_p(x), T, d, I, E, k, *[_p(a) for a in args], _p(ids), _p(y), _p(h)),
+               "expert_ffn_nvfp4")
+        return (y, h) if want_h else y
+    args = [_c(layer[n], np.uint8 if n.endswith("_q") else np.uint16)
+            for n in ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")]
     _check(_lib().oracle_expert_ffn(_p(x), T, d, I, E, k, group, *[_p(a) for a in args], _p(ids), _p(y), _p(h)),
            "expert_ffn")
     return (y, h) if want_h else y
@@ -229,8 +276,6 @@ def moe_forward(x, layer, k, resid=None, group=32, renorm=True, forced_ids=None,
     T, d = x.shape
     gq = layer["gate_q"]
     E, I = gq.shape[0] - n_shared, gq.shape[1]
-    args = [_c(layer[n], np.uint8 if n.endswith("_q") else np.uint16)
-            for n in ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")]
     Wr = _c(layer.get("w_router"), np.float32)
     b = _c(layer.get("b_router"), np.float32)
     if Wr is None and forced_ids is None and k > 0:
@@ -241,9 +286,17 @@ def moe_forward(x, layer, k, resid=None, group=32, renorm=True, forced_ids=None,
     w = np.empty((T, k + n_shared), np.float64)
     gap = np.empty(T, np.float64)
     out = np.empty((T, d), np.float64)
-    _check(_lib().oracle_moe_forward(_p(x), _p(resid), T, d, E, k, n_shared, I, group, int(renorm), _p(Wr), _p(b),
-                                     *[_p(a) for a in args], _p(fi), _p(fw), _p(ids), _p(w), _p(gap), _p(out)),
-           "moe_forward")
+    if is_nvfp4(layer):
+        args = _nvfp4_args(layer)
+        _check(_lib().oracle_moe_forward_nvfp4(_p(x), _p(resid), T, d, E, k, n_shared, I, int(renorm), _p(Wr), _p(b),
+                                               *[_p(a) for a in args], _p(fi), _p(fw), _p(ids), _p(w), _p(gap),
+                                               _p(out)), "moe_forward_nvfp4")
+    else:
+        args = [_c(layer[n], np.uint8 if n.endswith("_q") else np.uint16)
+                for n in ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")]
+        _check(_lib().oracle_moe_forward(_p(x), _p(resid), T, d, E, k, n_shared, I, group, int(renorm), _p(Wr),
+                                         _p(b), *[_p(a) for a in args], _p(fi), _p(fw), _p(ids), _p(w), _p(gap),
+                                         _p(out)), "moe_forward")
     return {"out": out, "ids": ids, "w": w, "gap": gap}
 
 
@@ -266,6 +319,21 @@ def lmhead(h, q, s, group=32, want_logits=True):
     am = np.empty(T, np.int32)
     gap = np.empty(T, np.float64)
     _check(_lib().oracle_lmhead(_p(h), T, d, V, group, _p(q), _p(s), _p(logits), _p(am), _p(gap)), "lmhead")
+    return logits, am, gap
+
+
+def lmhead_nvfp4(h, q, s, ts, want_logits=True):
+    """NVFP4 LM head: q [V, d/2] codes, s [V, d/16] E4M3, ts fp32.  Returns (logits, argmax, gap)."""
+    h = _c(h, np.uint16)
+    q = _c(q, np.uint8)
+    s = _c(s, np.uint8)
+    T, d = h.shape
+    V = q.shape[0]
+    logits = np.empty((T, V), np.float64) if want_logits else None
+    am = np.empty(T, np.int32)
+    gap = np.empty(T, np.float64)
+    _check(_lib().oracle_lmhead_nvfp4(_p(h), T, d, V, _p(q), _p(s), float(np.float32(ts)), _p(logits), _p(am),
+                                      _p(gap)), "lmhead_nvfp4")
     return logits, am, gap
 
 

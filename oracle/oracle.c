@@ -1,6 +1,6 @@
 /*
- * oracle.c -- plain fp64 CPU oracle of the int4 mixture-of-experts layer and
- * the int4 LM-head projection.
+ * oracle.c -- plain fp64 CPU oracle of the 4-bit (int4 or NVFP4)
+ * mixture-of-experts layer and the 4-bit LM-head projection.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link or call
  * this file; only the tests, the smoke check and the CPU-baseline leg of the
@@ -17,7 +17,8 @@
  *   combine         out[t] = resid[t] + sum_j w[t,j] * y[t,j]   (j ascending)
  *   RMSNorm         xh = x / sqrt(mean(x^2) + eps)               (gain 1)
  *   LM head         z[t,v] = sum_i Wlm[v,i] * xh[t,i];  argmax, lowest v on ties
- * with every int4 weight dequantised exactly: W[n,i] = q[n,i] * s[n, i/32].
+ * with every int4 weight dequantised exactly: W[n,i] = q[n,i] * s[n, i/32],
+ * or, for NVFP4 banks, W[n,i] = e2m1(q[n,i]) * e4m3(s[n, i/16]) * ts (below).
  *
  * Sources.  "Flint 40B : Best Mid Sized LLM" (video transcript): 02:35 -- 256
  * routed experts per mixture layer, a small router picks a few per token;
@@ -119,6 +120,116 @@ static double int4_row_dot(const uint8_t* qrow, const uint16_t* srow, int64_t K,
     acc += w * v[i];
   }
   return acc;
+}
+
+/* ------------------------------------------------------------ NVFP4 */
+
+/*
+ * NVFP4, the "four-bit NVFP" builds of the model ("Flint 40B : Best Mid Sized
+ * LLM", transcript 07:15; "Recursive_SI's First Model Unveiled!", section
+ * "Quantization": the final NVFP4 model).  The pages name the format without
+ * defining it; this is its public definition (4-bit floating-point elements in
+ * 16-element blocks with an 8-bit floating-point scale, plus one fp32 scale
+ * per tensor):
+ *   element  FP4 E2M1: bit 3 sign, bits 2..1 exponent (bias 1), bit 0
+ *            mantissa; exponent 0 is subnormal (0 or 0.5); no Inf or NaN, so
+ *            the magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4, 6;
+ *   scale    FP8 E4M3 for every 16 consecutive elements along the reduction
+ *            dimension: bit 7 sign, bits 6..3 exponent (bias 7), bits 2..0
+ *            mantissa; exponent 0 is subnormal; exponent 15 with mantissa 7 is
+ *            NaN; no Inf (largest 448);
+ *   tensor   one fp32 scale per matrix;
+ *   W[n,i] = e2m1(q[n,i]) * e4m3(s[n, i/16]) * ts.
+ * Codes are stored two per byte like the int4 values: element 2b in the low
+ * nibble of byte b.
+ */
+double oracle_e2m1_to_f64(uint8_t code) {
+  int sign = (code >> 3) & 1;
+  int ex = (code >> 1) & 3;
+  int m = code & 1;
+  double v = (ex == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, ex - 1);
+  return sign ? -v : v;
+}
+
+double oracle_e4m3_to_f64(uint8_t b) {
+  int sign = (b >> 7) & 1;
+  int ex = (b >> 3) & 15;
+  int m = b & 7;
+  double v;
+  if (ex == 15 && m == 7)
+    v = NAN;
+  else if (ex == 0)
+    v = ldexp((double)m, -9); /* subnormal: m/8 * 2^-6 */
+  else
+    v = ldexp(8.0 + m, ex - 10); /* (1 + m/8) * 2^(ex-7) */
+  return sign ? -v : v;
+}
+
+#define NVFP4_BLOCK 16
+
+static uint8_t nib_at(const uint8_t* row, int64_t i) {
+  uint8_t byte = row[i >> 1];
+  return (i & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0x0f);
+}
+
+/* Dequantise one NVFP4 matrix rows x K: out[n,i] = e2m1(q) * e4m3(s[n, i/16]) * ts. */
+int oracle_dequant_nvfp4(const uint8_t* q, const uint8_t* s, float ts, int64_t rows, int64_t K, double* out) {
+  if (!q || !s || !out || K % NVFP4_BLOCK) return ORACLE_EINVAL;
+  for (int64_t n = 0; n < rows; ++n)
+    for (int64_t i = 0; i < K; ++i)
+      out[n * K + i] = oracle_e2m1_to_f64(nib_at(q + n * (K / 2), i)) *
+                       oracle_e4m3_to_f64(s[n * (K / NVFP4_BLOCK) + i / NVFP4_BLOCK]) * (double)ts;
+  return ORACLE_OK;
+}
+
+/* sum_i W[n,i] * v[i] for one NVFP4 row, i ascending. */
+static double nvfp4_row_dot(const uint8_t* qrow, const uint8_t* srow, double ts, int64_t K, const double* v) {
+  double acc = 0.0;
+  for (int64_t i = 0; i < K; ++i) {
+    double w = oracle_e2m1_to_f64(nib_at(qrow, i)) * oracle_e4m3_to_f64(srow[i / NVFP4_BLOCK]) * ts;
+    acc += w * v[i];
+  }
+  return acc;
+}
+
+/* ------------------------------------------------------------ weight banks */
+
+/*
+ * A bank of n matrices of rows x K in one of the two 4-bit formats, so that
+ * the layer and the LM head below are written once for both.
+ *   int4:  q [n, rows, K/2], s16 [n, rows, K/group] fp16
+ *   NVFP4: q [n, rows, K/2], s8 [n, rows, K/16] E4M3, ts [n] fp32
+ */
+typedef struct {
+  int nvfp4;
+  const uint8_t* q;
+  const uint16_t* s16;
+  const uint8_t* s8;
+  const float* ts;
+  int64_t rows, K, group;
+} wbank;
+
+static wbank int4_bank(const uint8_t* q, const uint16_t* s, int64_t rows, int64_t K, int64_t group) {
+  wbank b = {0, q, s, NULL, NULL, rows, K, group};
+  return b;
+}
+
+static wbank nvfp4_bank(const uint8_t* q, const uint8_t* s, const float* ts, int64_t rows, int64_t K) {
+  wbank b = {1, q, NULL, s, ts, rows, K, NVFP4_BLOCK};
+  return b;
+}
+
+static int bank_ok(const wbank* b) {
+  if (!b->q || b->K % 2 || b->group <= 0 || b->K % b->group) return 0;
+  return b->nvfp4 ? (b->s8 && b->ts) : (b->s16 != NULL);
+}
+
+/* sum_i W[row,i] * v[i] for row `row` of the bank (counted over all matrices). */
+static double bank_row_dot(const wbank* b, int64_t row, const double* v) {
+  if (b->nvfp4)
+    return nvfp4_row_dot(b->q + row * (b->K / 2), b->s8 + row * (b->K / NVFP4_BLOCK), (double)b->ts[row / b->rows],
+                         b->K, v);
+  return int4_row_dot(b->q + row * (b->K / 2), b->s16 + row * (b->K / b->group), b->K, b->group, v);
 }
 
 /* ------------------------------------------------------------ routing */
@@ -256,11 +367,12 @@ int oracle_permute(const int32_t* ids, int64_t T, int64_t E, int64_t k, int32_t*
  * Weight banks: gate/up q [E, I, d/2], s [E, I, d/group]; down q [E, d, I/2],
  * s [E, d, I/group].  y is [T*k, d] in (t, j) order; h [T*k, I] may be NULL.
  */
-int oracle_expert_ffn(const uint16_t* x, int64_t T, int64_t d, int64_t I, int64_t E, int64_t k, int64_t group,
-                      const uint8_t* gq, const uint16_t* gs, const uint8_t* uq, const uint16_t* us,
-                      const uint8_t* dq, const uint16_t* ds, const int32_t* ids, double* y, double* h_out) {
-  if (d % group || I % group || d % 2 || I % 2 || k <= 0 || E <= 0) return ORACLE_EINVAL;
-  if (T && (!x || !gq || !gs || !uq || !us || !dq || !ds || !ids || !y)) return ORACLE_EINVAL;
+static int expert_ffn_banks(const uint16_t* x, int64_t T, int64_t d, int64_t I, int64_t E, int64_t k,
+                            const wbank* gb, const wbank* ub, const wbank* db, const int32_t* ids, double* y,
+                            double* h_out) {
+  if (d % 2 || I % 2 || k <= 0 || E <= 0) return ORACLE_EINVAL;
+  if (T && (!x || !bank_ok(gb) || !bank_ok(ub) || !bank_ok(db) || !ids || !y)) return ORACLE_EINVAL;
+  if (gb->K != d || ub->K != d || db->K != I || gb->rows != I || ub->rows != I || db->rows != d) return ORACLE_EINVAL;
   int64_t R = T * k;
   for (int64_t r = 0; r < R; ++r)
     if (ids[r] < 0 || ids[r] >= E) return ORACLE_EINVAL;
@@ -280,21 +392,37 @@ int oracle_expert_ffn(const uint16_t* x, int64_t T, int64_t d, int64_t I, int64_
         for (int64_t i = 0; i < d; ++i) xv[i] = oracle_bf16_to_f64(x[t * d + i]);
         for (int64_t n = 0; n < I; ++n) {
           int64_t row = e * I + n;
-          double a = int4_row_dot(gq + row * (d / 2), gs + row * (d / group), d, group, xv);
-          double u = int4_row_dot(uq + row * (d / 2), us + row * (d / group), d, group, xv);
+          double a = bank_row_dot(gb, row, xv);
+          double u = bank_row_dot(ub, row, xv);
           hv[n] = a / (1.0 + exp(-a)) * u;
         }
         if (h_out) memcpy(h_out + r * I, hv, sizeof(double) * (size_t)I);
-        for (int64_t c = 0; c < d; ++c) {
-          int64_t row = e * d + c;
-          y[r * d + c] = int4_row_dot(dq + row * (I / 2), ds + row * (I / group), I, group, hv);
-        }
+        for (int64_t c = 0; c < d; ++c) y[r * d + c] = bank_row_dot(db, e * d + c, hv);
       }
     }
     free(xv);
     free(hv);
   }
   return bad ? ORACLE_EINVAL : ORACLE_OK;
+}
+
+int oracle_expert_ffn(const uint16_t* x, int64_t T, int64_t d, int64_t I, int64_t E, int64_t k, int64_t group,
+                      const uint8_t* gq, const uint16_t* gs, const uint8_t* uq, const uint16_t* us,
+                      const uint8_t* dq, const uint16_t* ds, const int32_t* ids, double* y, double* h_out) {
+  if (group <= 0 || d % group || I % group) return ORACLE_EINVAL;
+  wbank gb = int4_bank(gq, gs, I, d, group), ub = int4_bank(uq, us, I, d, group), db = int4_bank(dq, ds, d, I, group);
+  return expert_ffn_banks(x, T, d, I, E, k, &gb, &ub, &db, ids, y, h_out);
+}
+
+/* The same with NVFP4 banks: gate/up q [E, I, d/2], s [E, I, d/16], ts [E];
+ * down q [E, d, I/2], s [E, d, I/16], ts [E]. */
+int oracle_expert_ffn_nvfp4(const uint16_t* x, int64_t T, int64_t d, int64_t I, int64_t E, int64_t k,
+                            const uint8_t* gq, const uint8_t* gs, const float* gts, const uint8_t* uq,
+                            const uint8_t* us, const float* uts, const uint8_t* dq, const uint8_t* ds,
+                            const float* dts, const int32_t* ids, double* y, double* h_out) {
+  if (d % NVFP4_BLOCK || I % NVFP4_BLOCK) return ORACLE_EINVAL;
+  wbank gb = nvfp4_bank(gq, gs, gts, I, d), ub = nvfp4_bank(uq, us, uts, I, d), db = nvfp4_bank(dq, ds, dts, d, I);
+  return expert_ffn_banks(x, T, d, I, E, k, &gb, &ub, &db, ids, y, h_out);
 }
 
 /* out[t,c] = resid[t,c] + sum_{j=0}^{k-1} w[t,j] * y[t*k+j, c]. */
@@ -322,11 +450,10 @@ int oracle_combine(const double* y, const double* w, const uint16_t* resid, int6
  * forced_ids / forced_w ([T, k + n_shared]) may be NULL (then both must be
  * NULL).  ids_out, w_out ([T, k + n_shared]), gap_out may be NULL.  out [T, d].
  */
-int oracle_moe_forward(const uint16_t* x, const uint16_t* resid, int64_t T, int64_t d, int64_t E, int64_t k,
-                       int64_t n_shared, int64_t I, int64_t group, int renorm, const float* Wr, const float* b,
-                       const uint8_t* gq, const uint16_t* gs, const uint8_t* uq, const uint16_t* us,
-                       const uint8_t* dq, const uint16_t* ds, const int32_t* forced_ids, const double* forced_w,
-                       int32_t* ids_out, double* w_out, double* gap_out, double* out) {
+static int moe_forward_banks(const uint16_t* x, const uint16_t* resid, int64_t T, int64_t d, int64_t E, int64_t k,
+                             int64_t n_shared, int64_t I, int renorm, const float* Wr, const float* b,
+                             const wbank* gb, const wbank* ub, const wbank* db, const int32_t* forced_ids,
+                             const double* forced_w, int32_t* ids_out, double* w_out, double* gap_out, double* out) {
   if ((forced_ids == NULL) != (forced_w == NULL)) return ORACLE_EINVAL;
   if (n_shared < 0 || n_shared > 1 || k < 0 || (k == 0 && n_shared == 0)) return ORACLE_EINVAL;
   const int64_t kt = k + n_shared;  // rows per token
@@ -363,7 +490,7 @@ int oracle_moe_forward(const uint16_t* x, const uint16_t* resid, int64_t T, int6
         }
       }
     }
-    if (!rc) rc = oracle_expert_ffn(x, T, d, I, E + n_shared, kt, group, gq, gs, uq, us, dq, ds, ids, y, NULL);
+    if (!rc) rc = expert_ffn_banks(x, T, d, I, E + n_shared, kt, gb, ub, db, ids, y, NULL);
     if (!rc) rc = oracle_combine(y, w, resid, T, d, kt, out);
     if (!rc && ids_out) memcpy(ids_out, ids, sizeof(int32_t) * (size_t)R);
     if (!rc && w_out) memcpy(w_out, w, sizeof(double) * (size_t)R);
@@ -374,6 +501,30 @@ int oracle_moe_forward(const uint16_t* x, const uint16_t* resid, int64_t T, int6
   free(rids);
   free(rw);
   return rc;
+}
+
+int oracle_moe_forward(const uint16_t* x, const uint16_t* resid, int64_t T, int64_t d, int64_t E, int64_t k,
+                       int64_t n_shared, int64_t I, int64_t group, int renorm, const float* Wr, const float* b,
+                       const uint8_t* gq, const uint16_t* gs, const uint8_t* uq, const uint16_t* us,
+                       const uint8_t* dq, const uint16_t* ds, const int32_t* forced_ids, const double* forced_w,
+                       int32_t* ids_out, double* w_out, double* gap_out, double* out) {
+  if (group <= 0 || d % group || I % group) return ORACLE_EINVAL;
+  wbank gb = int4_bank(gq, gs, I, d, group), ub = int4_bank(uq, us, I, d, group), db = int4_bank(dq, ds, d, I, group);
+  return moe_forward_banks(x, resid, T, d, E, k, n_shared, I, renorm, Wr, b, &gb, &ub, &db, forced_ids, forced_w,
+                           ids_out, w_out, gap_out, out);
+}
+
+/* The same layer with NVFP4 expert banks (tensor scales gts/uts/dts [E + n_shared]). */
+int oracle_moe_forward_nvfp4(const uint16_t* x, const uint16_t* resid, int64_t T, int64_t d, int64_t E, int64_t k,
+                             int64_t n_shared, int64_t I, int renorm, const float* Wr, const float* b,
+                             const uint8_t* gq, const uint8_t* gs, const float* gts, const uint8_t* uq,
+                             const uint8_t* us, const float* uts, const uint8_t* dq, const uint8_t* ds,
+                             const float* dts, const int32_t* forced_ids, const double* forced_w, int32_t* ids_out,
+                             double* w_out, double* gap_out, double* out) {
+  if (d % NVFP4_BLOCK || I % NVFP4_BLOCK) return ORACLE_EINVAL;
+  wbank gb = nvfp4_bank(gq, gs, gts, I, d), ub = nvfp4_bank(uq, us, uts, I, d), db = nvfp4_bank(dq, ds, dts, d, I);
+  return moe_forward_banks(x, resid, T, d, E, k, n_shared, I, renorm, Wr, b, &gb, &ub, &db, forced_ids, forced_w,
+                           ids_out, w_out, gap_out, out);
 }
 
 /* ------------------------------------------------------------ stack helpers */
@@ -398,9 +549,9 @@ int oracle_rmsnorm(const uint16_t* x, int64_t T, int64_t d, double eps, double* 
  * q [V, d/2], s [V, d/group]; argmax[t] = lowest v reaching max_v z[t,v];
  * gap[t] = top-1 minus top-2 logit.  logits [T, V] and gap may be NULL.
  */
-int oracle_lmhead(const uint16_t* h, int64_t T, int64_t d, int64_t V, int64_t group, const uint8_t* q,
-                  const uint16_t* s, double* logits, int32_t* argmax, double* gap) {
-  if (d % group || d % 2 || V <= 0 || (T && (!h || !q || !s || !argmax))) return ORACLE_EINVAL;
+static int lmhead_bank(const uint16_t* h, int64_t T, int64_t d, int64_t V, const wbank* wb, double* logits,
+                       int32_t* argmax, double* gap) {
+  if (d % 2 || V <= 0 || wb->K != d || (T && (!h || !bank_ok(wb) || !argmax))) return ORACLE_EINVAL;
   double* hv = (double*)malloc(sizeof(double) * (size_t)(T * d + 1));
   double* z = (double*)malloc(sizeof(double) * (size_t)(T * V + 1));
   if (!hv || !z) {
@@ -412,7 +563,7 @@ int oracle_lmhead(const uint16_t* h, int64_t T, int64_t d, int64_t V, int64_t gr
 #pragma omp parallel for schedule(static)
   for (int64_t v = 0; v < V; ++v)
     for (int64_t t = 0; t < T; ++t)
-      z[t * V + v] = int4_row_dot(q + v * (d / 2), s + v * (d / group), d, group, hv + t * d);
+      z[t * V + v] = bank_row_dot(wb, v, hv + t * d);
   for (int64_t t = 0; t < T; ++t) {
     int64_t best = 0;
     for (int64_t v = 1; v < V; ++v)
@@ -427,6 +578,21 @@ int oracle_lmhead(const uint16_t* h, int64_t T, int64_t d, int64_t V, int64_t gr
   free(hv);
   free(z);
   return ORACLE_OK;
+}
+
+int oracle_lmhead(const uint16_t* h, int64_t T, int64_t d, int64_t V, int64_t group, const uint8_t* q,
+                  const uint16_t* s, double* logits, int32_t* argmax, double* gap) {
+  if (group <= 0 || d % group) return ORACLE_EINVAL;
+  wbank wb = int4_bank(q, s, V, d, group);
+  return lmhead_bank(h, T, d, V, &wb, logits, argmax, gap);
+}
+
+/* The LM head with an NVFP4 matrix: q [V, d/2], s [V, d/16] E4M3, tensor scale ts. */
+int oracle_lmhead_nvfp4(const uint16_t* h, int64_t T, int64_t d, int64_t V, const uint8_t* q, const uint8_t* s,
+                        float ts, double* logits, int32_t* argmax, double* gap) {
+  if (d % NVFP4_BLOCK) return ORACLE_EINVAL;
+  wbank wb = nvfp4_bank(q, s, &ts, V, d);
+  return lmhead_bank(h, T, d, V, &wb, logits, argmax, gap);
 }
 
 int oracle_num_threads(void) {

@@ -24,7 +24,11 @@ layer as described on the Flint model pages):
 * fp16 scales: ``RNE_fp16(0.005 + 0.015 * u)``, u uniform in [0, 1) with 53 bits;
 * activations: N(0, 1) rounded to bf16 (nearest-even);
 * router weights: N(0, 1/d) in fp32; router bias: N(0, 1) in fp32, or the
-  Zipf(s) bias ``b[pi(r)] = ln(r^-s / H)`` over a seeded permutation pi.
+  Zipf(s) bias ``b[pi(r)] = ln(r^-s / H)`` over a seeded permutation pi;
+* NVFP4 banks: E2M1 codes uniform over the 16 codes (two per byte, drawn as the
+  int4 bytes are), E4M3 block scales uniform over the codes 0x58..0x67 (16..60),
+  fp32 tensor scales ``RN_fp32((1 + u) * 2^-12)``, so that the weights have
+  the int4 banks' magnitude (mean |w| near 0.03 against 0.05).
 """
 from __future__ import annotations
 
@@ -43,7 +47,14 @@ _MASK64 = (1 << 64) - 1
 TAG = {
     "gate_q": 1, "gate_s": 2, "up_q": 3, "up_s": 4, "down_q": 5, "down_s": 6,
     "router_w": 7, "router_b": 8, "x": 9, "lm_q": 10, "lm_s": 11, "zipf": 12,
+    # NVFP4 banks: E2M1 codes, E4M3 block scales, fp32 tensor scales
+    "gate_fq": 13, "gate_fs": 14, "gate_ts": 15, "up_fq": 16, "up_fs": 17, "up_ts": 18,
+    "down_fq": 19, "down_fs": 20, "down_ts": 21, "lm_fq": 22, "lm_fs": 23, "lm_ts": 24,
 }
+
+# E4M3 block scales are drawn uniformly among the 16 byte codes 0x58 .. 0x67,
+# the E4M3 numbers 16, 18, ..., 30, 32, 36, ..., 60.
+E4M3_SCALE_CODE0 = 0x58
 
 
 def _mix64_int(z: int) -> int:
@@ -101,6 +112,23 @@ def f16_scales(key: int, start: int, count: int) -> np.ndarray:
     u = (h >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
     v = 0.005 + 0.015 * u
     return v.astype(np.float16).view(np.uint16)
+
+
+def e4m3_scale_bytes(key: int, start: int, count: int) -> np.ndarray:
+    """E4M3 block-scale bytes: 0x58 + (h >> 60), one hash word per byte."""
+    if count == 0:
+        return np.zeros(0, np.uint8)
+    h = hash_words(key, start, count)
+    return (np.uint64(E4M3_SCALE_CODE0) + (h >> np.uint64(60))).astype(np.uint8)
+
+
+def f32_tensor_scales(key: int, start: int, count: int) -> np.ndarray:
+    """fp32 tensor scales RN_fp32((1 + u) * 2^-12), u = (h >> 11) * 2^-53."""
+    if count == 0:
+        return np.zeros(0, np.float32)
+    h = hash_words(key, start, count)
+    u = (h >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+    return ((1.0 + u) * 2.0 ** -12).astype(np.float32)
 
 
 def f64_to_bf16_bits(v: np.ndarray) -> np.ndarray:
@@ -221,6 +249,49 @@ def lm_head(seed: int, V: int, d: int, group: int = 32, rows: tuple[int, int] | 
     return q, s
 
 
+# ---------------------------------------------------------------- NVFP4 weights
+
+
+def nvfp4_matrix(seed: int, name: str, layer: int, n_mats: int, rows: int, K: int, mat0: int = 0,
+                 mat1: int | None = None):
+    """NVFP4 bank [n_mats, rows, K]: codes q [m, rows, K/2] (two E2M1 codes per
+    byte, uniform over all 16), E4M3 block scales s [m, rows, K/16] and fp32
+    tensor scales ts [m], for matrices mat0 .. mat1-1 of the full bank."""
+    if mat1 is None:
+        mat1 = n_mats
+    m = mat1 - mat0
+    qb = rows * K // 2
+    sb = rows * K // 16
+    q = int4_bytes(stream_key(seed, TAG[name + "_fq"], layer), mat0 * qb, m * qb).reshape(m, rows, K // 2)
+    s = e4m3_scale_bytes(stream_key(seed, TAG[name + "_fs"], layer), mat0 * sb, m * sb).reshape(m, rows, K // 16)
+    ts = f32_tensor_scales(stream_key(seed, TAG[name + "_ts"], layer), mat0, m)
+    return q, s, ts
+
+
+def moe_layer_nvfp4(seed: int, d: int, E: int, I: int, layer: int = 0, bias: str = "normal",
+                    experts: tuple[int, int] | None = None, n_shared: int = 0) -> dict:
+    """An MoE layer with NVFP4 expert banks (E + n_shared entries; the router
+    scores E) and the same router as moe_layer."""
+    Et = E + n_shared
+    e0, e1 = experts if experts is not None else (0, Et)
+    t = {}
+    for name, rows, K in (("gate", I, d), ("up", I, d), ("down", d, I)):
+        q, s, ts = nvfp4_matrix(seed, name, layer, Et, rows, K, e0, e1)
+        t[name + "_q"], t[name + "_s"], t[name + "_ts"] = q, s, ts
+    t["w_router"] = router_weight(seed, E, d, layer)
+    t["b_router"] = router_bias(seed, E, bias, layer)
+    return t
+
+
+def lm_head_nvfp4(seed: int, V: int, d: int, rows: tuple[int, int] | None = None):
+    """NVFP4 LM head: q [V, d/2], s [V, d/16] (or rows [r0, r1)), ts (fp32 scalar)."""
+    r0, r1 = rows if rows is not None else (0, V)
+    q = int4_bytes(stream_key(seed, TAG["lm_fq"], 0), r0 * (d // 2), (r1 - r0) * (d // 2)).reshape(r1 - r0, d // 2)
+    s = e4m3_scale_bytes(stream_key(seed, TAG["lm_fs"], 0), r0 * (d // 16), (r1 - r0) * (d // 16))
+    ts = f32_tensor_scales(stream_key(seed, TAG["lm_ts"], 0), 0, 1)[0]
+    return q, s.reshape(r1 - r0, d // 16), ts
+
+
 # ---------------------------------------------------------------- device twin
 
 _DEV = None
@@ -233,7 +304,7 @@ def _dev_lib():
         if not os.path.exists(path):
             raise RuntimeError(f"device generator not built: {path} (run __graft_entry__.build())")
         lib = ctypes.CDLL(path)
-        for name in ("synth_fill_int4_bytes", "synth_fill_f16_scales"):
+        for name in ("synth_fill_int4_bytes", "synth_fill_f16_scales", "synth_fill_e4m3_scales"):
             fn = getattr(lib, name)
             fn.restype = ctypes.c_int
             fn.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_void_p]
@@ -253,3 +324,10 @@ def device_fill_scales(dst_ptr: int, count: int, key: int, start: int = 0, strea
     rc = _dev_lib().synth_fill_f16_scales(dst_ptr, count, key, start, stream)
     if rc != 0:
         raise RuntimeError(f"synth_fill_f16_scales failed: cuda error {rc}")
+
+
+def device_fill_e4m3(dst_ptr: int, count: int, key: int, start: int = 0, stream: int = 0) -> None:
+    """Write E4M3 block-scale bytes start .. start+count-1 of stream ``key`` to device memory."""
+    rc = _dev_lib().synth_fill_e4m3_scales(dst_ptr, count, key, start, stream)
+    if rc != 0:
+        raise RuntimeError(f"synth_fill_e4m3_scales failed: cuda error {rc}")

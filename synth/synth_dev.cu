@@ -2,7 +2,8 @@
 //
 // Draws the same bits as the numpy code: the i-th SplitMix64 output from a
 // stream key (Steele, Lea and Flood, OOPSLA 2014), mapped to packed int4
-// bytes or to fp16 scales RNE_fp16(0.005 + 0.015 * u).  It exists so that the
+// bytes, to fp16 scales RNE_fp16(0.005 + 0.015 * u) or to E4M3 block-scale
+// bytes 0x58 + (h >> 60).  It exists so that the
 // multi-GB weight banks can be written straight into HBM; it holds none of the
 // MoE layer's arithmetic.
 #include <cuda_runtime.h>
@@ -41,6 +42,13 @@ __global__ void fill_scales_kernel(uint16_t* dst, uint64_t count, uint64_t key, 
   }
 }
 
+// E4M3 block-scale bytes: 0x58 + (h >> 60).
+__global__ void fill_e4m3_kernel(uint8_t* dst, uint64_t count, uint64_t key, uint64_t start) {
+  uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += stride)
+    dst[i] = (uint8_t)(0x58u + (uint32_t)(hash_word(key, start + i) >> 60));
+}
+
 int grid_for(uint64_t n) {
   uint64_t g = (n + 255) / 256;
   if (g > 148ull * 32) g = 148ull * 32;
@@ -61,5 +69,12 @@ extern "C" int synth_fill_f16_scales(void* dst, uint64_t count, uint64_t key, ui
   if (count == 0) return 0;
   if (dst == nullptr) return (int)cudaErrorInvalidValue;
   fill_scales_kernel<<<grid_for(count), 256, 0, (cudaStream_t)stream>>>((uint16_t*)dst, count, key, start);
+  return (int)cudaGetLastError();
+}
+
+extern "C" int synth_fill_e4m3_scales(void* dst, uint64_t count, uint64_t key, uint64_t start, void* stream) {
+  if (count == 0) return 0;
+  if (dst == nullptr) return (int)cudaErrorInvalidValue;
+  fill_e4m3_kernel<<<grid_for(count), 256, 0, (cudaStream_t)stream>>>((uint8_t*)dst, count, key, start);
   return (int)cudaGetLastError();
 }

@@ -357,6 +357,128 @@ def test_combine_constant_rows():
     assert np.allclose(oracle.combine(y, w, x), bf16_to_np(x) + 0.75, rtol=1e-15, atol=1e-15)
 
 
+# ------------------------------------------------------------------ NVFP4
+
+
+def e2m1_table():
+    with open(os.path.join(GOLDEN, "nvfp4_e2m1.json")) as f:
+        return np.array(json.load(f)["values"], np.float64)
+
+
+def np_e4m3(b):
+    """E4M3 bytes through torch's float8_e4m3fn conversion (a library routine)."""
+    import torch
+    return torch.from_numpy(np.asarray(b, np.uint8).copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def np_dequant_nvfp4(q, s, ts):
+    """Independent NVFP4 dequantisation: low nibble first, the golden E2M1
+    table, torch's E4M3 decoding, one scale per 16 columns."""
+    q = np.asarray(q, np.uint8)
+    codes = np.stack([q & 0x0F, q >> 4], axis=-1).reshape(q.shape[:-1] + (q.shape[-1] * 2,))
+    return e2m1_table()[codes] * np.repeat(np_e4m3(s), 16, axis=-1) * float(np.float32(ts))
+
+
+def np_pack_codes(codes):
+    c = np.asarray(codes, np.int64) & 0xF
+    return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+
+
+def test_e2m1_codes_match_the_format_table():
+    table = e2m1_table()
+    got = oracle.e2m1_to_f64(np.arange(16))
+    assert np.array_equal(got, table)
+    assert np.array_equal(np.signbit(got), np.signbit(table))  # code 8 is -0
+    # only the low nibble of a byte is a code
+    assert np.array_equal(oracle.e2m1_to_f64(np.arange(16) + 0x30), table)
+
+
+def test_e4m3_bytes_match_torch_float8_e4m3fn():
+    b = np.arange(256)
+    got = oracle.e4m3_to_f64(b)
+    want = np_e4m3(b)
+    assert np.array_equal(np.isnan(got), np.isnan(want)) and int(np.isnan(got).sum()) == 2
+    fin = ~np.isnan(want)
+    assert np.array_equal(got[fin], want[fin])
+    assert np.array_equal(np.signbit(got[fin]), np.signbit(want[fin]))
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9
+
+
+def test_dequant_nvfp4_matches_an_independent_decoding():
+    q, s, ts = synth.nvfp4_matrix(30, "gate", 0, 1, 32, 256)
+    got = oracle.dequant_nvfp4(q[0], s[0], ts[0])
+    assert np.array_equal(got, np_dequant_nvfp4(q[0], s[0], ts[0]))
+
+
+def test_dequant_nvfp4_block_index_is_column_over_16():
+    rows, K = 3, 64
+    q = np_pack_codes(np.full((rows, K), 2))  # every element 1.0
+    s = (0x38 + np.arange(rows * K // 16).reshape(rows, K // 16)).astype(np.uint8)  # distinct scales 1, 1.125, ...
+    got = oracle.dequant_nvfp4(q, s, 0.5)
+    want = 0.5 * np.repeat(np_e4m3(s), 16, axis=1)
+    assert np.array_equal(got, want)
+    # the sign is bit 3 of the code, the tensor scale multiplies every element
+    q = np_pack_codes(np.tile([7, 15], (rows, K // 2)))
+    got = oracle.dequant_nvfp4(q, np.full((rows, K // 16), 0x38, np.uint8), 2.0)
+    assert np.array_equal(got, np.tile([12.0, -12.0], (rows, K // 2)))
+
+
+def test_lmhead_nvfp4_planted_row_and_ties():
+    d, V = 64, 48
+    rng = np.random.default_rng(31)
+    codes = rng.integers(0, 16, (V, d)) & 0b1011  # magnitudes up to 1.5, either sign
+    hx = synth.f64_to_bf16_bits(rng.normal(size=(2, d)))
+    hv = bf16_to_np(hx)
+    codes[17] = np.where(hv[0] > 0, 7, 15)  # planted: +-6 aligned with sign(h[0])
+    codes[30] = np.where(hv[1] > 0, 7, 15)
+    s = rng.integers(0x30, 0x40, (V, d // 16)).astype(np.uint8)
+    s[17] = s[30] = 0x3F  # the largest scale drawn
+    q = np_pack_codes(codes)
+    ts = np.float32(0.0625)
+    logits, am, gap = oracle.lmhead_nvfp4(hx, q, s, ts)
+    W = np_dequant_nvfp4(q, s, ts)
+    assert np.allclose(logits, hv @ W.T, rtol=1e-13, atol=1e-13)
+    assert am.tolist() == [17, 30] and np.all(gap > 0)
+    codes[5] = codes[17]
+    s[5] = s[17]
+    _, am, gap = oracle.lmhead_nvfp4(hx, np_pack_codes(codes), s, ts)
+    assert am[0] == 5 and gap[0] == 0.0
+
+
+def test_expert_ffn_nvfp4_matches_numpy_per_row():
+    d, E, I, T, k = 128, 6, 64, 4, 3
+    lay = synth.moe_layer_nvfp4(32, d, E, I, bias="normal")
+    x = synth.activations(32, T, d)
+    ids, w, _, _ = oracle.route(x, lay["w_router"], lay["b_router"], k)
+    y, h = oracle.expert_ffn(x, lay, ids, want_h=True)
+    xv = bf16_to_np(x)
+    for t in range(T):
+        for j in range(k):
+            e = ids[t, j]
+            Wg, Wu, Wd = (np_dequant_nvfp4(lay[n + "_q"][e], lay[n + "_s"][e], lay[n + "_ts"][e])
+                          for n in ("gate", "up", "down"))
+            hh = silu(Wg @ xv[t]) * (Wu @ xv[t])
+            assert np.allclose(h[t * k + j], hh, rtol=1e-12, atol=1e-12)
+            assert np.allclose(y[t * k + j], Wd @ hh, rtol=1e-12, atol=1e-12)
+    res = oracle.moe_forward(x, lay, k)
+    assert np.array_equal(res["ids"], ids)
+    want = xv + np.einsum("tj,tjc->tc", w, y.reshape(T, k, d))
+    assert np.allclose(res["out"], want, rtol=1e-13, atol=1e-13)
+
+
+def test_nvfp4_single_expert_top1_is_a_dense_swiglu_ffn():
+    d, I, T = 64, 32, 3
+    lay = synth.moe_layer_nvfp4(33, d, 1, I, bias="zero")
+    x = synth.activations(33, T, d)
+    res = oracle.moe_forward(x, lay, 1)
+    assert np.all(res["ids"] == 0) and np.allclose(res["w"], 1.0)
+    Wg, Wu, Wd = (np_dequant_nvfp4(lay[n + "_q"][0], lay[n + "_s"][0], lay[n + "_ts"][0])
+                  for n in ("gate", "up", "down"))
+    xv = bf16_to_np(x)
+    want = xv + (silu(xv @ Wg.T) * (xv @ Wu.T)) @ Wd.T
+    assert np.allclose(res["out"], want, rtol=1e-12, atol=1e-12)
+
+
 # ------------------------------------------------------------------ stack pieces
 
 

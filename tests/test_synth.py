@@ -60,3 +60,21 @@ def test_zipf_bias_is_a_permuted_log_zipf_law():
     r = np.arange(1, E + 1)
     assert abs(p.sum() - 1) < 1e-5
     assert np.allclose(p[0] / p, r ** 1.1, rtol=1e-5)
+
+
+def test_nvfp4_draws_codes_scales_and_tensor_scales():
+    key = synth.stream_key(4, synth.TAG["down_fs"], 1)
+    s = synth.e4m3_scale_bytes(key, 0, 1 << 15)
+    counts = np.bincount(s, minlength=256)[0x58:0x68]
+    assert counts.sum() == len(s) and counts.min() > 0.9 * len(s) / 16
+    assert np.array_equal(synth.e4m3_scale_bytes(key, 100, 50), s[100:150])
+    ts = synth.f32_tensor_scales(synth.stream_key(4, synth.TAG["gate_ts"], 0), 0, 4096)
+    assert ts.dtype == np.float32 and ts.min() >= 2.0 ** -12 and ts.max() <= 2.0 ** -11
+    full = synth.moe_layer_nvfp4(5, 256, 8, 128)
+    part = synth.moe_layer_nvfp4(5, 256, 8, 128, experts=(2, 7))
+    for n in ("gate_q", "gate_s", "gate_ts", "up_q", "up_s", "up_ts", "down_q", "down_s", "down_ts"):
+        assert np.array_equal(part[n], full[n][2:7])
+    assert full["gate_s"].shape == (8, 128, 16) and full["down_s"].shape == (8, 256, 8)
+    q, s2, t = synth.lm_head_nvfp4(5, 64, 256)
+    q2, s3, t2 = synth.lm_head_nvfp4(5, 64, 256, rows=(16, 48))
+    assert np.array_equal(q2, q[16:48]) and np.array_equal(s3, s2[16:48]) and t == t2
