@@ -23,8 +23,10 @@ Other workloads (``--workload``): ``batch`` (T tokens per step, Zipf(1.1)
 router skew), ``prefill`` (T=4096 chunk, Zipf skew), ``stack`` (49 layers +
 RMSNorm + int4 LM head + argmax), ``shared`` (the pages' routing: top-6 of 256
 plus one shared expert), ``lmhead`` (the int4 LM head alone, V = 131072).
-``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same
-workload.
+``--format nvfp4`` runs the decode, batch, prefill and LM-head workloads with
+NVFP4 weights (E2M1 codes, an E4M3 scale per 16 weights, an fp32 scale per
+matrix; the same 4.5 bits per weight).  ``--impl reference`` times the fp64 CPU
+oracle on a bounded sample of the same workload.
 """
 from __future__ import annotations
 
@@ -66,6 +68,8 @@ def parse():
                    choices=["decode", "batch", "prefill", "stack", "shared", "lmhead"],
                    help="shared: batch-1 decode with the pages' routing, top-6 of 256 plus one shared expert")
     p.add_argument("--T", type=int, default=None, help="tokens per step (batch / prefill / stack / lmhead)")
+    p.add_argument("--format", default="int4", choices=["int4", "nvfp4"],
+                   help="weight format of the experts and the LM head (not the stack)")
     p.add_argument("--copies", type=int, default=64, help="independent layer copies cycled per step")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -76,7 +80,13 @@ def parse():
         a.warmup = DEFAULT_WARMUP[a.workload]
     a.steps = max(1, a.steps)
     a.warmup = max(3, a.warmup)
+    if a.format == "nvfp4" and a.workload in ("stack", "shared"):
+        p.error("--format nvfp4 covers the decode, batch, prefill and lmhead workloads")
     return a
+
+
+def fmt_suffix(fmt):
+    return "_nvfp4" if fmt == "nvfp4" else ""
 
 
 # ---------------------------------------------------------------- helpers
@@ -329,7 +339,7 @@ def count_kernels(fn):
 # ---------------------------------------------------------------- device weights
 
 
-def make_device_layers(n_layers, seed, bias, device="cuda", k=K_TOP, n_shared=0):
+def make_device_layers(n_layers, seed, bias, device="cuda", k=K_TOP, n_shared=0, fmt="int4"):
     """n independently seeded layers, drawn on the device and packed (with
     n_shared = 1 the banks hold E + 1 experts, the last one shared)."""
     import torch
@@ -340,9 +350,17 @@ def make_device_layers(n_layers, seed, bias, device="cuda", k=K_TOP, n_shared=0)
     Et = E + n_shared
     qbuf = torch.empty(Et * I_FF * D // 2, dtype=torch.uint8, device=device)
     sbuf = torch.empty(Et * I_FF * D // 32, dtype=torch.float16, device=device)
+    fbuf = torch.empty(Et * I_FF * D // 16, dtype=torch.uint8, device=device)
     for l in range(n_layers):
-        banks = {}
+        banks, ts = {}, {}
         for name, (rows, K) in {"gate": (I_FF, D), "up": (I_FF, D), "down": (D, I_FF)}.items():
+            if fmt == "nvfp4":  # same bits as synth.moe_layer_nvfp4(seed, ..., layer=l)
+                synth.device_fill_int4(qbuf.data_ptr(), qbuf.numel(), synth.stream_key(seed, synth.TAG[name + "_fq"], l))
+                synth.device_fill_e4m3(fbuf.data_ptr(), fbuf.numel(), synth.stream_key(seed, synth.TAG[name + "_fs"], l))
+                banks[name] = bm.bitmoe_pack_nvfp4(qbuf.view(Et, rows, K // 2), fbuf.view(Et, rows, K // 16))
+                ts[name] = torch.from_numpy(
+                    synth.f32_tensor_scales(synth.stream_key(seed, synth.TAG[name + "_ts"], l), 0, Et)).to(device)
+                continue
             kq = synth.stream_key(seed, synth.TAG[name + "_q"], l)
             ks = synth.stream_key(seed, synth.TAG[name + "_s"], l)
             synth.device_fill_int4(qbuf.data_ptr(), qbuf.numel(), kq)
@@ -351,17 +369,28 @@ def make_device_layers(n_layers, seed, bias, device="cuda", k=K_TOP, n_shared=0)
         wr = torch.from_numpy(synth.router_weight(seed, E, D, l)).to(device)
         br = torch.from_numpy(synth.router_bias(seed, E, bias, l)).to(device)
         layers.append(bm.MoeLayer(d=D, E=E, k=k, I=I_FF, gate=banks["gate"], up=banks["up"],
-                                  down=banks["down"], w_router=wr, b_router=br, n_shared=n_shared))
+                                  down=banks["down"], w_router=wr, b_router=br, n_shared=n_shared,
+                                  gate_ts=ts.get("gate"), up_ts=ts.get("up"), down_ts=ts.get("down")))
     torch.cuda.synchronize()
     return layers
 
 
-def make_device_lm_head(seed, device="cuda"):
-    """The int4 LM head [V, D] drawn on the device and packed."""
+def make_device_lm_head(seed, device="cuda", fmt="int4"):
+    """The int4 LM head [V, D] drawn on the device and packed (NVFP4: the packed
+    bank and its tensor scale, the bits of synth.lm_head_nvfp4)."""
     import torch
 
     import bit_expert_ffn_warp_b300 as bm
     import synth
+    if fmt == "nvfp4":
+        q = torch.empty(V * D // 2, dtype=torch.uint8, device=device)
+        sc = torch.empty(V * D // 16, dtype=torch.uint8, device=device)
+        synth.device_fill_int4(q.data_ptr(), q.numel(), synth.stream_key(seed, synth.TAG["lm_fq"], 0))
+        synth.device_fill_e4m3(sc.data_ptr(), sc.numel(), synth.stream_key(seed, synth.TAG["lm_fs"], 0))
+        packed = bm.bitmoe_pack_nvfp4(q.view(V, D // 2), sc.view(V, D // 16))
+        ts = float(synth.f32_tensor_scales(synth.stream_key(seed, synth.TAG["lm_ts"], 0), 0, 1)[0])
+        torch.cuda.synchronize()
+        return packed, ts
     q = torch.empty(V * D // 2, dtype=torch.uint8, device=device)
     sc = torch.empty(V * D // 32, dtype=torch.float16, device=device)
     synth.device_fill_int4(q.data_ptr(), q.numel(), synth.stream_key(seed, synth.TAG["lm_q"], 0))
@@ -386,7 +415,7 @@ def to_bf16(host_bits, pin=False, device="cuda"):
 # ---------------------------------------------------------------- CPU oracle leg
 
 
-def cpu_oracle_sample(workload, T, seconds, seed=0):
+def cpu_oracle_sample(workload, T, seconds, seed=0, fmt="int4"):
     """Time the fp64 oracle on a bounded sample of the workload; returns dict."""
     import oracle
     import synth
@@ -394,7 +423,10 @@ def cpu_oracle_sample(workload, T, seconds, seed=0):
     bias = "normal" if one else "zipf"
     shared = workload == "shared"
     k = K_SHARED if shared else K_TOP
-    tensors = (synth.moe_layer_shared if shared else synth.moe_layer)(seed, D, E, I_FF, bias=bias, layer=0)
+    if fmt == "nvfp4":
+        tensors = synth.moe_layer_nvfp4(seed, D, E, I_FF, bias=bias, layer=0)
+    else:
+        tensors = (synth.moe_layer_shared if shared else synth.moe_layer)(seed, D, E, I_FF, bias=bias, layer=0)
     cores = oracle.num_threads()
     done, t0, step = 0, time.perf_counter(), 0
     # decode: one token per call (batch 1, as the workload), until the time budget is spent
@@ -410,17 +442,22 @@ def cpu_oracle_sample(workload, T, seconds, seed=0):
                       f"OpenMP over the {per_call * (k + int(shared))} rows of each call)"}
 
 
-def cpu_lmhead_sample(T, seconds, seed=0):
+def cpu_lmhead_sample(T, seconds, seed=0, fmt="int4"):
     """Oracle LM head on a row sample of the V = 131072 bank, scaled to all rows."""
     import oracle
     import synth
     cores = oracle.num_threads()
     h = synth.activations(seed, T, D)
     rows, el, n = 4096, 0.0, 0
-    q, s = synth.lm_head(seed, rows, D)
+    if fmt == "nvfp4":
+        q, s, ts = synth.lm_head_nvfp4(seed, rows, D)
+        run = lambda: oracle.lmhead_nvfp4(h, q, s, ts, want_logits=False)  # noqa: E731
+    else:
+        q, s = synth.lm_head(seed, rows, D)
+        run = lambda: oracle.lmhead(h, q, s, want_logits=False)  # noqa: E731
     t0 = time.perf_counter()
     while time.perf_counter() - t0 < seconds or n == 0:
-        oracle.lmhead(h, q, s, want_logits=False)
+        run()
         n += 1
     el = time.perf_counter() - t0
     per_call = el / n * (V / rows)
@@ -469,7 +506,7 @@ def bench_decode(args, world, rank):
     G = args.copies
     k = K_SHARED if shared else K_TOP
     K, W = args.steps, args.warmup
-    layers = make_device_layers(G, seed=1 + rank, bias=bias, k=k, n_shared=int(shared))
+    layers = make_device_layers(G, seed=1 + rank, bias=bias, k=k, n_shared=int(shared), fmt=args.format)
     ws = bm.moe_workspace(layers[0], T)
     kt = layers[0].kt
 
@@ -503,14 +540,16 @@ def bench_decode(args, world, rank):
     hbm, _, _, which = peaks()
     achieved = step_bytes / (per_step_us * 1e-6) / 1e9
     name = ("moe_layer_shared_decode_batch1" if shared else
-            f"moe_layer_decode_T{T}" if T > 1 else "moe_layer_decode_batch1")
+            f"moe_layer_decode_T{T}" if T > 1 else "moe_layer_decode_batch1") + fmt_suffix(args.format)
     fused = T <= 8
     return {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": per_step_us / 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int4xbf16->fp32", "data": "synthetic (seeded; weights drawn on device)",
+        "vs_baseline": None, "dtype": "nvfp4xbf16->fp32" if args.format == "nvfp4" else "int4xbf16->fp32",
+        "data": "synthetic (seeded; weights drawn on device)",
         "config": {"workload": name, "T": T, "d": D, "E": E, "top_k": k, "n_shared": int(shared), "I": I_FF,
-                   "group": 32, "router_bias": bias, "layer_copies": G,
+                   "format": args.format, "group": 16 if args.format == "nvfp4" else 32, "router_bias": bias,
+                   "layer_copies": G,
                    "l2": f"inputs larger than L2: {G} independently seeded layer copies "
                          f"({G * ((E + int(shared)) * EXPERT_BYTES + ROUTER_BYTES) / 1e9:.1f} GB) cycled step by step",
                    "parallelism": f"replicas x{world}"},
@@ -567,7 +606,7 @@ def bench_prefill(args, world, rank):
     T = args.T or 4096
     G = min(args.copies, 4)
     K, W = args.steps, args.warmup
-    layers = make_device_layers(G, seed=1 + rank, bias="zipf")
+    layers = make_device_layers(G, seed=1 + rank, bias="zipf", fmt=args.format)
     xs_host = token_pool(rank, G, T)
     xs = to_bf16(xs_host)
     ws = bm.moe_workspace(layers[0], T)
@@ -587,7 +626,8 @@ def bench_prefill(args, world, rank):
 
     def ffn_step(s):
         off, rows = groups[s % G]
-        bm.moe_expert_ffn_int4(xs[s % G], layers[s % G], off, rows, ws, y_out=y_rows)
+        (bm.moe_expert_ffn_nvfp4 if args.format == "nvfp4" else bm.moe_expert_ffn_int4)(
+            xs[s % G], layers[s % G], off, rows, ws, y_out=y_rows)
 
     with ClockSampler(torch.cuda.current_device()) as clk:
         run_warmup(step, W)
@@ -623,16 +663,18 @@ def bench_prefill(args, world, rank):
         "metric": PREFILL_METRIC,
         "value": round(job_throughput(K * T, ms_local, world), 1), "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int4->f16 x f16 -> f32", "data": "synthetic (seeded; weights drawn on device)",
-        "config": {"workload": f"moe_layer_prefill_T{T}", "T": T, "d": D, "E": E, "top_k": K_TOP, "I": I_FF,
-                   "router_bias": "zipf(1.1)", "layer_copies": G,
+        "vs_baseline": None, "dtype": ("nvfp4" if args.format == "nvfp4" else "int4") + "->f16 x f16 -> f32",
+        "data": "synthetic (seeded; weights drawn on device)",
+        "config": {"workload": f"moe_layer_prefill_T{T}" + fmt_suffix(args.format), "T": T, "d": D, "E": E,
+                   "top_k": K_TOP, "I": I_FF, "format": args.format, "router_bias": "zipf(1.1)", "layer_copies": G,
                    "l2": f"inputs larger than L2: {G} layer copies of {E * EXPERT_BYTES / 1e6:.0f} MB cycled",
                    "active_experts_mean": float(np.mean([(c > 0).sum() for c in cnt])),
                    "parallelism": f"replicas x{world}"},
         "timing": timing_record(times, K, f"CUDA graph of {K} moe_forward steps"),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16_peak, "unit": "TFLOP/s",
                      "frac": round(achieved / bf16_peak, 4),
-                     "traffic": profiled_traffic("prefill_gemm_kernel", workload=f"moe_layer_prefill_T{T}"),
+                     "traffic": profiled_traffic("prefill_gemm_kernel",
+                                                 workload=f"moe_layer_prefill_T{T}" + fmt_suffix(args.format)),
                      "kernel": "expert FFN grouped GEMMs (gate/up+SwiGLU, down)",
                      "flops_per_launch": flops, "ms_per_launch": gemm_ms,
                      "launch_timing": timing_record(ffn_times, K, f"CUDA graph of {K} moe_expert_ffn_int4 calls"),
@@ -767,7 +809,14 @@ def bench_lmhead(args, world, rank):
     T = args.T or 1
     K, W = args.steps, args.warmup
     n_heads = 4   # 604 MB of LM-head copies cycled: each call streams its 151 MB from HBM
-    heads = [make_device_lm_head(seed=1 + rank + 1000 * c) for c in range(n_heads)]
+    fp4 = args.format == "nvfp4"
+    heads = [make_device_lm_head(seed=1 + rank + 1000 * c, fmt=args.format) for c in range(n_heads)]
+
+    def lm_call(c, x):
+        if fp4:
+            bm.lmhead_nvfp4_gemv(x, heads[c][0], heads[c][1], V, lm_ws, want_logits=False, argmax=am[c])
+        else:
+            bm.lmhead_int4_gemv(x, heads[c], V, lm_ws, want_logits=False, argmax=am[c])
     lm_ws = bm.lmhead_workspace(T, D, V)
     n_pool = 256
     xs_host = token_pool(rank, n_pool, T)
@@ -775,8 +824,7 @@ def bench_lmhead(args, world, rank):
     am = torch.empty((n_heads, T), dtype=torch.int32, device="cuda")
 
     def step(s):
-        c = s % n_heads
-        bm.lmhead_int4_gemv(xs[s % n_pool], heads[c], V, lm_ws, want_logits=False, argmax=am[c])
+        lm_call(s % n_heads, xs[s % n_pool])
 
     with ClockSampler(torch.cuda.current_device()) as clk:
         run_warmup(step, W)
@@ -795,18 +843,20 @@ def bench_lmhead(args, world, rank):
     def e2e_step(s):
         c = s % n_heads
         xd.copy_(x_pin[s % n_pool], non_blocking=True)
-        bm.lmhead_int4_gemv(xd, heads[c], V, lm_ws, want_logits=False, argmax=am[c])
+        lm_call(c, xd)
         am_pin[s % n_pool].copy_(am[c], non_blocking=True)
 
     run_warmup(e2e_step, 3)
     e_times = time_regions(region_graphs(e2e_step, K, 1), world)
-    name = f"lmhead_V{V}_T{T}"
+    name = f"lmhead_V{V}_T{T}" + fmt_suffix(args.format)
     return {
         "metric": LMHEAD_METRIC,
         "value": round(job_throughput(K * T, ms_local, world), 1), "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int4xbf16->fp32", "data": "synthetic (seeded; weights drawn on device)",
-        "config": {"workload": name, "T": T, "d": D, "V": V, "group": 32, "lm_head_copies": n_heads,
+        "vs_baseline": None, "dtype": "nvfp4xbf16->fp32" if fp4 else "int4xbf16->fp32",
+        "data": "synthetic (seeded; weights drawn on device)",
+        "config": {"workload": name, "T": T, "d": D, "V": V, "format": args.format, "group": 16 if fp4 else 32,
+                   "lm_head_copies": n_heads,
                    "l2": f"inputs larger than L2: {n_heads} LM-head copies ({n_heads * LM_BYTES / 1e6:.0f} MB) cycled",
                    "parallelism": f"replicas x{world}"},
         "timing": timing_record(times, K, f"CUDA graph of {K} lmhead_int4_gemv calls"),
@@ -897,9 +947,9 @@ def main():
             if args.workload == "stack":
                 res["cpu_baseline"] = cpu_stack_sample(T, args.cpu_seconds)
             elif args.workload == "lmhead":
-                res["cpu_baseline"] = cpu_lmhead_sample(T, args.cpu_seconds)
+                res["cpu_baseline"] = cpu_lmhead_sample(T, args.cpu_seconds, fmt=args.format)
             else:
-                res["cpu_baseline"] = cpu_oracle_sample(args.workload, T, args.cpu_seconds)
+                res["cpu_baseline"] = cpu_oracle_sample(args.workload, T, args.cpu_seconds, fmt=args.format)
         print(json.dumps(res))
     if world > 1:
         import torch.distributed as dist

@@ -51,6 +51,15 @@ class MoeWeights(ctypes.Structure):
                 ("w_router", ctypes.c_void_p), ("b_router", ctypes.c_void_p)]
 
 
+class MoeWeightsNvfp4(ctypes.Structure):
+    _fields_ = [("gate", ctypes.c_void_p), ("up", ctypes.c_void_p), ("down", ctypes.c_void_p),
+                ("gate_scale", ctypes.c_void_p), ("up_scale", ctypes.c_void_p), ("down_scale", ctypes.c_void_p),
+                ("w_router", ctypes.c_void_p), ("b_router", ctypes.c_void_p)]
+
+
+FP4_BLOCK = 16
+
+
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
 _SZ = ctypes.c_size_t
@@ -61,6 +70,8 @@ _SIGS = {
     "bitmoe_set_trace_buffer": (ctypes.c_int, [_P, _SZ]),
     "bitmoe_packed_int4_bytes": (_SZ, [_I64, _I64, _I64, _I64]),
     "bitmoe_pack_int4": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I64, _P, _P]),
+    "bitmoe_packed_nvfp4_bytes": (_SZ, [_I64, _I64, _I64]),
+    "bitmoe_pack_nvfp4": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P, _P]),
     "bitmoe_get_device_status": (ctypes.c_int, [_P, ctypes.c_int, ctypes.POINTER(ctypes.c_int32), _P]),
     "moe_workspace_size": (_SZ, [ctypes.POINTER(MoeShape), _I64]),
     "moe_route": (ctypes.c_int, [_P, _I64, ctypes.POINTER(MoeShape), _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -70,6 +81,10 @@ _SIGS = {
     "moe_combine": (ctypes.c_int, [_P, _P, _P, _P, _I64, ctypes.POINTER(MoeShape), _P, _P, _P]),
     "moe_forward": (ctypes.c_int, [_P, _P, _I64, ctypes.POINTER(MoeShape), ctypes.POINTER(MoeWeights), _P, _P, _P,
                                    _P, _P, _P, _P, _SZ, _P]),
+    "moe_forward_nvfp4": (ctypes.c_int, [_P, _P, _I64, ctypes.POINTER(MoeShape), ctypes.POINTER(MoeWeightsNvfp4), _P,
+                                         _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_expert_ffn_nvfp4": (ctypes.c_int, [_P, _I64, ctypes.POINTER(MoeShape), ctypes.POINTER(MoeWeightsNvfp4), _P,
+                                            _P, _P, _P, _SZ, _P]),
     "moe_forward_prenorm": (ctypes.c_int, [_P, _I64, _P, _P, ctypes.c_float, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                                            _P]),
     "moe_stack_workspace_size": (_SZ, [ctypes.POINTER(MoeShape), _I64]),
@@ -77,6 +92,7 @@ _SIGS = {
                                         _P, _P, _P, _SZ, _P]),
     "lmhead_workspace_size": (_SZ, [_I64, _I64, _I64]),
     "lmhead_int4_gemv": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _SZ, _P]),
+    "lmhead_nvfp4_gemv": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, ctypes.c_float, _P, _P, _P, _SZ, _P]),
     "lmhead_static_scratch_bytes": (_SZ, []),
     "lmhead_int4_gemv_static": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P, _P, _P]),
     "bitmoe_rmsnorm": (ctypes.c_int, [_P, _I64, _I64, ctypes.c_float, _P, _P]),
@@ -151,6 +167,23 @@ def bitmoe_pack_int4(q: torch.Tensor, scale: torch.Tensor, group: int = GROUP) -
     return out
 
 
+def bitmoe_pack_nvfp4(q: torch.Tensor, scale: torch.Tensor) -> torch.Tensor:
+    """Canonical NVFP4 bank q uint8 [n, rows, K/2] (E2M1 codes) + scale uint8
+    [n, rows, K/16] (E4M3 bytes) -> packed uint8 tiles."""
+    if q.dim() == 2:
+        q, scale = q.unsqueeze(0), scale.unsqueeze(0)
+    n, rows, kh = q.shape
+    K = kh * 2
+    _need(q, torch.uint8, (n, rows, kh), "q")
+    _need(scale, torch.uint8, (n, rows, K // 16), "scale")
+    nbytes = int(_lib.bitmoe_packed_nvfp4_bytes(n, rows, K))
+    if nbytes == 0:
+        raise BitmoeError("bitmoe_pack_nvfp4", 2)
+    out = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    _check("bitmoe_pack_nvfp4", _lib.bitmoe_pack_nvfp4(_ptr(q), _ptr(scale), n, rows, K, _ptr(out), _stream()))
+    return out
+
+
 @dataclass
 class MoeLayer:
     """Device-resident weights of one MoE layer (packed banks + fp32 router).
@@ -171,6 +204,14 @@ class MoeLayer:
     b_router: torch.Tensor | None
     renormalize: bool = True
     n_shared: int = 0
+    # NVFP4 banks: fp32 tensor scales [Et] (device); None for int4 banks
+    gate_ts: torch.Tensor | None = None
+    up_ts: torch.Tensor | None = None
+    down_ts: torch.Tensor | None = None
+
+    @property
+    def nvfp4(self) -> bool:
+        return self.gate_ts is not None
 
     @property
     def kt(self) -> int:
@@ -184,17 +225,25 @@ class MoeLayer:
 
     @property
     def shape(self) -> MoeShape:
-        return MoeShape(self.d, self.E, self.k, self.I, GROUP, int(self.renormalize), int(self.n_shared))
+        return MoeShape(self.d, self.E, self.k, self.I, FP4_BLOCK if self.nvfp4 else GROUP, int(self.renormalize),
+                        int(self.n_shared))
 
     @property
-    def weights(self) -> MoeWeights:
-        return MoeWeights(self.gate.data_ptr(), self.up.data_ptr(), self.down.data_ptr(),
-                          None if self.w_router is None else self.w_router.data_ptr(),
-                          None if self.b_router is None else self.b_router.data_ptr())
+    def weights(self):
+        wr = None if self.w_router is None else self.w_router.data_ptr()
+        br = None if self.b_router is None else self.b_router.data_ptr()
+        if self.nvfp4:
+            return MoeWeightsNvfp4(self.gate.data_ptr(), self.up.data_ptr(), self.down.data_ptr(),
+                                   self.gate_ts.data_ptr(), self.up_ts.data_ptr(), self.down_ts.data_ptr(), wr, br)
+        return MoeWeights(self.gate.data_ptr(), self.up.data_ptr(), self.down.data_ptr(), wr, br)
 
     @classmethod
     def from_canonical(cls, tensors: dict, k: int, device="cuda", renormalize: bool = True) -> "MoeLayer":
-        """Build from host/device canonical tensors (gate_q/gate_s/.../w_router/b_router)."""
+        """Build from host/device canonical tensors (gate_q/gate_s/.../w_router/b_router);
+        NVFP4 banks when the tensors carry gate_ts/up_ts/down_ts (then *_s are E4M3 bytes)."""
+        if "gate_ts" in tensors:
+            return cls._from_canonical_nvfp4(tensors, k, device, renormalize)
+
         def dev(name, dtype):
             t = tensors[name]
             if not isinstance(t, torch.Tensor):
@@ -221,6 +270,27 @@ class MoeLayer:
             w_router=None if wr is None else dev("w_router", torch.float32),
             b_router=None if b is None else dev("b_router", torch.float32),
             renormalize=renormalize)
+
+    @classmethod
+    def _from_canonical_nvfp4(cls, tensors: dict, k: int, device, renormalize: bool) -> "MoeLayer":
+        def dev(name, dtype):
+            t = tensors[name]
+            if not isinstance(t, torch.Tensor):
+                t = torch.as_tensor(t)
+            return t.to(device=device, dtype=dtype).contiguous()
+        packed, ts = {}, {}
+        for n in ("gate", "up", "down"):
+            packed[n] = bitmoe_pack_nvfp4(dev(n + "_q", torch.uint8), dev(n + "_s", torch.uint8))
+            ts[n] = dev(n + "_ts", torch.float32)
+        Et, I, dh = tensors["gate_q"].shape
+        wr, b = tensors.get("w_router"), tensors.get("b_router")
+        E = Et - 1 if k == 0 else (wr.shape[0] if wr is not None else Et)
+        if Et - E not in (0, 1):
+            raise ValueError("the banks hold the routed experts plus at most one shared expert")
+        return cls(d=dh * 2, E=E, k=k, I=I, n_shared=Et - E, gate=packed["gate"], up=packed["up"],
+                   down=packed["down"], w_router=None if wr is None else dev("w_router", torch.float32),
+                   b_router=None if b is None else dev("b_router", torch.float32), renormalize=renormalize,
+                   gate_ts=ts["gate"], up_ts=ts["up"], down_ts=ts["down"])
 
 
 def moe_workspace_size(layer_or_shape, T: int) -> int:
@@ -273,6 +343,18 @@ def moe_permute(ids, layer: MoeLayer, workspace):
 
 
 def moe_expert_ffn_int4(x, layer: MoeLayer, offsets, sorted_rows, workspace, y_out=None):
+    """Expert FFNs of the grouped rows (int4 banks; NVFP4 layers go to moe_expert_ffn_nvfp4)."""
+    return _expert_ffn(x, layer, offsets, sorted_rows, workspace, y_out, False)
+
+
+def moe_expert_ffn_nvfp4(x, layer: MoeLayer, offsets, sorted_rows, workspace, y_out=None):
+    """Expert FFNs of the grouped rows over NVFP4 banks."""
+    return _expert_ffn(x, layer, offsets, sorted_rows, workspace, y_out, True)
+
+
+def _expert_ffn(x, layer, offsets, sorted_rows, workspace, y_out, nvfp4):
+    if layer.nvfp4 != nvfp4:
+        raise ValueError("the layer's banks are " + ("NVFP4" if layer.nvfp4 else "int4"))
     T = x.shape[0]
     _need(x, torch.bfloat16, (T, layer.d), "x")
     _need(offsets, torch.int32, (layer.Et + 1,), "offsets")
@@ -282,9 +364,9 @@ def moe_expert_ffn_int4(x, layer: MoeLayer, offsets, sorted_rows, workspace, y_o
     else:
         y = _need(y_out, torch.float32, (T * layer.kt, layer.d), "y_out")
     sh, wt = layer.shape, layer.weights
-    _check("moe_expert_ffn_int4", _lib.moe_expert_ffn_int4(_ptr(x), T, ctypes.byref(sh), ctypes.byref(wt),
-                                                           _ptr(offsets), _ptr(sorted_rows), _ptr(y),
-                                                           _ptr(workspace), workspace.numel(), _stream()))
+    name = "moe_expert_ffn_nvfp4" if layer.nvfp4 else "moe_expert_ffn_int4"
+    _check(name, getattr(_lib, name)(_ptr(x), T, ctypes.byref(sh), ctypes.byref(wt), _ptr(offsets),
+                                     _ptr(sorted_rows), _ptr(y), _ptr(workspace), workspace.numel(), _stream()))
     return y
 
 
@@ -299,9 +381,17 @@ def moe_combine(y_rows, inv_rows, topk_w, residual, layer: MoeLayer, out=None, w
     return out, out_f32
 
 
+def moe_forward_nvfp4(x, layer: MoeLayer, workspace, **kw):
+    """moe_forward of a layer with NVFP4 banks (moe_forward itself dispatches on the layer)."""
+    if not layer.nvfp4:
+        raise ValueError("the layer's banks are int4")
+    return moe_forward(x, layer, workspace, **kw)
+
+
 def moe_forward(x, layer: MoeLayer, workspace, residual=None, forced_ids=None, forced_w=None, out=None,
                 out_f32=None, ids_out=None, w_out=None):
-    """One MoE layer: returns (out bf16 [T,d], out_f32 or None, ids or None, w or None)."""
+    """One MoE layer: returns (out bf16 [T,d], out_f32 or None, ids or None, w or None).
+    Calls moe_forward_nvfp4 of the C ABI for a layer with NVFP4 banks."""
     T = x.shape[0]
     _need(x, torch.bfloat16, (T, layer.d), "x")
     residual = x if residual is None else residual
@@ -311,15 +401,18 @@ def moe_forward(x, layer: MoeLayer, workspace, residual=None, forced_ids=None, f
         _need(forced_w, torch.float32, (T, layer.kt), "forced_w")
     out = torch.empty_like(x) if out is None else out
     sh, wt = layer.shape, layer.weights
-    _check("moe_forward", _lib.moe_forward(_ptr(x), _ptr(residual), T, ctypes.byref(sh), ctypes.byref(wt),
-                                           _ptr(forced_ids), _ptr(forced_w), _ptr(ids_out), _ptr(w_out), _ptr(out),
-                                           _ptr(out_f32), _ptr(workspace), workspace.numel(), _stream()))
+    name = "moe_forward_nvfp4" if layer.nvfp4 else "moe_forward"
+    _check(name, getattr(_lib, name)(_ptr(x), _ptr(residual), T, ctypes.byref(sh), ctypes.byref(wt),
+                                     _ptr(forced_ids), _ptr(forced_w), _ptr(ids_out), _ptr(w_out), _ptr(out),
+                                     _ptr(out_f32), _ptr(workspace), workspace.numel(), _stream()))
     return out, out_f32, ids_out, w_out
 
 
 def moe_forward_prenorm(residual, layer: MoeLayer, workspace, eps: float = 1e-6, out=None, out_f32=None,
                         xh_out=None, ids_out=None, w_out=None, forced_ids=None, forced_w=None):
     """out = residual + MoE(RMSNorm(residual)); out may be residual itself (in place)."""
+    if layer.nvfp4:
+        raise ValueError("moe_forward_prenorm takes int4 banks")
     T = residual.shape[0]
     _need(residual, torch.bfloat16, (T, layer.d), "residual")
     out = torch.empty_like(residual) if out is None else out
@@ -350,6 +443,8 @@ def moe_stack_decode(residual, layers, workspace, eps: float = 1e-6, lm_w=None, 
     if any(l.shape.d != lay0.d or l.k != lay0.k or l.E != lay0.E or l.I != lay0.I or l.n_shared != lay0.n_shared
            for l in layers):
         raise ValueError("every layer of a stack shares one shape")
+    if any(l.nvfp4 for l in layers):
+        raise ValueError("moe_stack_decode takes int4 banks")
     arr = (MoeWeights * len(layers))(*[l.weights for l in layers])
     if lm_w is not None:
         argmax = torch.empty(T, dtype=torch.int32, device=residual.device) if argmax is None else argmax
@@ -380,6 +475,20 @@ def lmhead_int4_gemv(h, w_packed, V: int, workspace, want_logits: bool = True, l
     argmax = torch.empty(T, dtype=torch.int32, device=h.device) if argmax is None else argmax
     _check("lmhead_int4_gemv", _lib.lmhead_int4_gemv(_ptr(h), T, d, V, GROUP, _ptr(w_packed), _ptr(logits),
                                                      _ptr(argmax), _ptr(workspace), workspace.numel(), _stream()))
+    return logits, argmax
+
+
+def lmhead_nvfp4_gemv(h, w_packed, tensor_scale: float, V: int, workspace, want_logits: bool = True, logits=None,
+                      argmax=None):
+    """LM head over a packed NVFP4 [V, d] bank with its fp32 tensor scale."""
+    T, d = h.shape
+    _need(h, torch.bfloat16, (T, d), "h")
+    logits = (torch.empty((T, V), dtype=torch.float32, device=h.device) if want_logits else None) \
+        if logits is None else logits
+    argmax = torch.empty(T, dtype=torch.int32, device=h.device) if argmax is None else argmax
+    _check("lmhead_nvfp4_gemv", _lib.lmhead_nvfp4_gemv(_ptr(h), T, d, V, _ptr(w_packed), float(tensor_scale),
+                                                       _ptr(logits), _ptr(argmax), _ptr(workspace), workspace.numel(),
+                                                       _stream()))
     return logits, argmax
 
 

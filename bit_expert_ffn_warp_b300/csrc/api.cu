@@ -2,6 +2,8 @@
 // and the launch sequence of each entry point.  See include/bitmoe.h.
 #include <string.h>
 
+#include <cmath>
+
 #include "kernels.h"
 
 using namespace bitmoe;
@@ -84,7 +86,7 @@ bitmoe_status_t check_shape(const bitmoe_moe_shape_t* sh, int64_t T) {
   if (sh->k > 0 && sh->E == 0) return BITMOE_ERR_INVALID_ARG;
   if (sh->n_shared < 0 || sh->n_shared > 1) return BITMOE_ERR_INVALID_ARG;
   if (sh->k > sh->E || rows_per_token(sh) > kMaxK) return BITMOE_ERR_INVALID_ARG;
-  if (sh->group != kGroup) return BITMOE_ERR_UNSUPPORTED;
+  if (sh->group != kGroup && sh->group != kFp4Block) return BITMOE_ERR_UNSUPPORTED;  // int4 or NVFP4 banks
   if (sh->d % kChunkK || sh->I % kChunkK) return BITMOE_ERR_UNSUPPORTED;
   if (bank_experts(sh) > kMaxE || sh->d > 16384 || sh->I > 16384) return BITMOE_ERR_UNSUPPORTED;
   if (T * rows_per_token(sh) > kMaxRows) return BITMOE_ERR_UNSUPPORTED;
@@ -97,15 +99,47 @@ bitmoe_status_t check_ws(const bitmoe_moe_shape_t* sh, int64_t T, void* ws, size
   return BITMOE_OK;
 }
 
-bitmoe_status_t check_weights(const bitmoe_moe_weights_t* wt, bool need_router) {
-  if (wt == nullptr) return BITMOE_ERR_INVALID_ARG;
-  if (!wt->gate || !wt->up || !wt->down) return BITMOE_ERR_INVALID_ARG;
-  if (!aligned16(wt->gate) || !aligned16(wt->up) || !aligned16(wt->down)) return BITMOE_ERR_INVALID_ARG;
-  if (need_router && (!wt->w_router || !aligned16(wt->w_router))) return BITMOE_ERR_INVALID_ARG;
+
+// A layer's weights in either format (tensor scales null: int4 banks).
+struct LayerW {
+  const uint8_t* gate;
+  const uint8_t* up;
+  const uint8_t* down;
+  const float* w_router;
+  const float* b_router;
+  const float* gate_ts;
+  const float* up_ts;
+  const float* down_ts;
+  bool nvfp4() const { return gate_ts != nullptr; }
+};
+
+LayerW layer_w(const bitmoe_moe_weights_t* wt) {
+  return LayerW{wt->gate, wt->up, wt->down, wt->w_router, wt->b_router, nullptr, nullptr, nullptr};
+}
+
+LayerW layer_w(const bitmoe_moe_weights_nvfp4_t* wt) {
+  return LayerW{wt->gate, wt->up, wt->down, wt->w_router, wt->b_router, wt->gate_scale, wt->up_scale, wt->down_scale};
+}
+
+// The shape's scale group names the format: 32 for int4 calls, 16 for NVFP4 ones.
+bitmoe_status_t check_format(const bitmoe_moe_shape_t* sh, bool nvfp4) {
+  return sh->group == (nvfp4 ? kFp4Block : kGroup) ? BITMOE_OK : BITMOE_ERR_UNSUPPORTED;
+}
+
+// nvfp4: the call takes NVFP4 banks, whose three tensor-scale arrays must be given.
+bitmoe_status_t check_layer(const LayerW& wt, bool need_router, bool nvfp4) {
+  if (!wt.gate || !wt.up || !wt.down) return BITMOE_ERR_INVALID_ARG;
+  if (!aligned16(wt.gate) || !aligned16(wt.up) || !aligned16(wt.down)) return BITMOE_ERR_INVALID_ARG;
+  if (need_router && (!wt.w_router || !aligned16(wt.w_router))) return BITMOE_ERR_INVALID_ARG;
+  if (nvfp4 && (!wt.gate_ts || !wt.up_ts || !wt.down_ts)) return BITMOE_ERR_INVALID_ARG;
   return BITMOE_OK;
 }
 
-FfnArgs ffn_args(const uint16_t* x, int64_t T, const bitmoe_moe_shape_t* sh, const bitmoe_moe_weights_t* wt,
+bitmoe_status_t check_weights(const bitmoe_moe_weights_t* wt, bool need_router) {
+  return wt ? check_layer(layer_w(wt), need_router, false) : BITMOE_ERR_INVALID_ARG;
+}
+
+FfnArgs ffn_args(const uint16_t* x, int64_t T, const bitmoe_moe_shape_t* sh, const LayerW& wt,
                  const int32_t* offsets, const int32_t* sorted_rows, const int32_t* blk_prefix, const MoeWs& w,
                  float* y_rows) {
   FfnArgs a;
@@ -115,9 +149,12 @@ FfnArgs ffn_args(const uint16_t* x, int64_t T, const bitmoe_moe_shape_t* sh, con
   a.I = (int)sh->I;
   a.E = (int)bank_experts(sh);
   a.k = (int)rows_per_token(sh);
-  a.gate = wt->gate;
-  a.up = wt->up;
-  a.down = wt->down;
+  a.gate = wt.gate;
+  a.up = wt.up;
+  a.down = wt.down;
+  a.gate_ts = wt.gate_ts;
+  a.up_ts = wt.up_ts;
+  a.down_ts = wt.down_ts;
   a.offsets = offsets;
   a.sorted_rows = sorted_rows;
   a.blk_prefix = blk_prefix;
@@ -152,15 +189,16 @@ namespace {
 // One layer step.  prenorm: x is the residual and the layer runs on RMSNorm(x) (unit gain,
 // eps), optionally copied to xh_out.
 bitmoe_status_t forward_impl(const uint16_t* x, const uint16_t* residual, int64_t T, const bitmoe_moe_shape_t* shape,
-                             const bitmoe_moe_weights_t* weights, const int32_t* forced_ids, const float* forced_w,
+                             const LayerW& weights, const int32_t* forced_ids, const float* forced_w,
                              int32_t* topk_ids_out, float* topk_w_out, uint16_t* out, float* out_f32,
                              void* workspace, size_t workspace_bytes, void* stream, int prenorm, float eps,
-                             uint16_t* xh_out) {
+                             uint16_t* xh_out, bool nvfp4) {
   bitmoe_status_t st = check_shape(shape, T);
   if (st != BITMOE_OK) return st;
+  if ((st = check_format(shape, nvfp4)) != BITMOE_OK) return st;
   if (T == 0) return BITMOE_OK;
   if ((forced_ids == nullptr) != (forced_w == nullptr)) return BITMOE_ERR_INVALID_ARG;
-  if ((st = check_weights(weights, forced_ids == nullptr && shape->k > 0)) != BITMOE_OK) return st;
+  if ((st = check_layer(weights, forced_ids == nullptr && shape->k > 0, nvfp4)) != BITMOE_OK) return st;
   if (!x || !residual || !out || !aligned16(x) || !aligned16(residual) || !aligned16(out) ||
       (out_f32 && !aligned16(out_f32)) || (xh_out && !aligned16(xh_out)) || !(eps >= 0.f))
     return BITMOE_ERR_INVALID_ARG;
@@ -181,11 +219,14 @@ bitmoe_status_t forward_impl(const uint16_t* x, const uint16_t* residual, int64_
     L.I = (int)shape->I;
     L.renorm = shape->renormalize;
     L.n_shared = ns;
-    L.gate = weights->gate;
-    L.up = weights->up;
-    L.down = weights->down;
-    L.w_router = weights->w_router;
-    L.b_router = weights->b_router;
+    L.gate = weights.gate;
+    L.up = weights.up;
+    L.down = weights.down;
+    L.w_router = weights.w_router;
+    L.b_router = weights.b_router;
+    L.gate_ts = weights.gate_ts;
+    L.up_ts = weights.up_ts;
+    L.down_ts = weights.down_ts;
     L.forced_ids = forced_ids;
     L.forced_w = forced_w;
     L.out = out;
@@ -214,7 +255,7 @@ bitmoe_status_t forward_impl(const uint16_t* x, const uint16_t* residual, int64_
   if (forced_ids) {
     e = launch_forced_select(forced_ids, forced_w, Ti, Et, kt, w.ids, w.w, w.st, s);
   } else {
-    e = k > 0 ? launch_router_logits(x, Ti, d, E, weights->w_router, weights->b_router, w.logits, s) : cudaSuccess;
+    e = k > 0 ? launch_router_logits(x, Ti, d, E, weights.w_router, weights.b_router, w.logits, s) : cudaSuccess;
     if (e == cudaSuccess) e = launch_topk_gates(w.logits, Ti, E, k, shape->renormalize, ns, w.ids, w.w, s);
   }
   if (e == cudaSuccess)
@@ -234,6 +275,21 @@ bitmoe_status_t forward_impl(const uint16_t* x, const uint16_t* residual, int64_
     e = cudaMemcpyAsync(topk_ids_out, w.ids, (size_t)T * kt * 4, cudaMemcpyDeviceToDevice, s);
   if (e == cudaSuccess && topk_w_out)
     e = cudaMemcpyAsync(topk_w_out, w.w, (size_t)T * kt * 4, cudaMemcpyDeviceToDevice, s);
+  return cuda_status(e);
+}
+
+bitmoe_status_t expert_ffn_impl(const uint16_t* x, int64_t T, const bitmoe_moe_shape_t* shape, const LayerW& weights,
+                                const int32_t* expert_offsets, const int32_t* sorted_rows, float* y_rows,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  if (!x || !expert_offsets || !sorted_rows || !y_rows || !aligned16(x) || !aligned16(y_rows))
+    return BITMOE_ERR_INVALID_ARG;
+  bitmoe_status_t st = check_ws(shape, T, workspace, workspace_bytes);
+  if (st != BITMOE_OK) return st;
+  const MoeWs w = moe_layout(shape, T, workspace);
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = launch_blk_prefix(expert_offsets, (int)bank_experts(shape), w.blk_prefix, s);
+  const FfnArgs a = ffn_args(x, T, shape, weights, expert_offsets, sorted_rows, w.blk_prefix, w, y_rows);
+  if (e == cudaSuccess) e = run_expert_ffn(a, w, nullptr, s);
   return cuda_status(e);
 }
 
@@ -278,6 +334,18 @@ bitmoe_status_t bitmoe_pack_int4(const uint8_t* q, const uint16_t* scale, int64_
   if (!aligned16(packed) || (reinterpret_cast<uintptr_t>(q) & 3u) || (reinterpret_cast<uintptr_t>(scale) & 1u))
     return BITMOE_ERR_INVALID_ARG;
   return cuda_status(launch_pack_int4(q, scale, n_mats, rows, K, packed, (cudaStream_t)stream));
+}
+
+size_t bitmoe_packed_nvfp4_bytes(int64_t n_mats, int64_t rows, int64_t K) {
+  return bitmoe_packed_int4_bytes(n_mats, rows, K, kGroup);  // same geometry: 4.5 bits per weight
+}
+
+bitmoe_status_t bitmoe_pack_nvfp4(const uint8_t* q, const uint8_t* scale, int64_t n_mats, int64_t rows, int64_t K,
+                                  uint8_t* packed, void* stream) {
+  if (!q || !scale || !packed) return BITMOE_ERR_INVALID_ARG;
+  if (bitmoe_packed_nvfp4_bytes(n_mats, rows, K) == 0) return BITMOE_ERR_UNSUPPORTED;
+  if (!aligned16(packed) || (reinterpret_cast<uintptr_t>(q) & 3u)) return BITMOE_ERR_INVALID_ARG;
+  return cuda_status(launch_pack_nvfp4(q, scale, n_mats, rows, K, packed, (cudaStream_t)stream));
 }
 
 bitmoe_status_t bitmoe_get_device_status(void* workspace, int clear, int32_t* status_out, void* stream) {
@@ -340,17 +408,24 @@ bitmoe_status_t moe_expert_ffn_int4(const uint16_t* x, int64_t T, const bitmoe_m
                                     size_t workspace_bytes, void* stream) {
   bitmoe_status_t st = check_shape(shape, T);
   if (st != BITMOE_OK) return st;
+  if ((st = check_format(shape, false)) != BITMOE_OK) return st;
   if (T == 0) return BITMOE_OK;
   if ((st = check_weights(weights, false)) != BITMOE_OK) return st;
-  if (!x || !expert_offsets || !sorted_rows || !y_rows || !aligned16(x) || !aligned16(y_rows))
-    return BITMOE_ERR_INVALID_ARG;
-  if ((st = check_ws(shape, T, workspace, workspace_bytes)) != BITMOE_OK) return st;
-  const MoeWs w = moe_layout(shape, T, workspace);
-  cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = launch_blk_prefix(expert_offsets, (int)bank_experts(shape), w.blk_prefix, s);
-  const FfnArgs a = ffn_args(x, T, shape, weights, expert_offsets, sorted_rows, w.blk_prefix, w, y_rows);
-  if (e == cudaSuccess) e = run_expert_ffn(a, w, nullptr, s);
-  return cuda_status(e);
+  return expert_ffn_impl(x, T, shape, layer_w(weights), expert_offsets, sorted_rows, y_rows, workspace,
+                         workspace_bytes, stream);
+}
+
+bitmoe_status_t moe_expert_ffn_nvfp4(const uint16_t* x, int64_t T, const bitmoe_moe_shape_t* shape,
+                                     const bitmoe_moe_weights_nvfp4_t* weights, const int32_t* expert_offsets,
+                                     const int32_t* sorted_rows, float* y_rows, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  bitmoe_status_t st = check_shape(shape, T);
+  if (st != BITMOE_OK) return st;
+  if ((st = check_format(shape, true)) != BITMOE_OK) return st;
+  if (T == 0) return BITMOE_OK;
+  if (!weights || (st = check_layer(layer_w(weights), false, true)) != BITMOE_OK) return BITMOE_ERR_INVALID_ARG;
+  return expert_ffn_impl(x, T, shape, layer_w(weights), expert_offsets, sorted_rows, y_rows, workspace,
+                         workspace_bytes, stream);
 }
 
 bitmoe_status_t moe_combine(const float* y_rows, const int32_t* inv_rows, const float* topk_w,
@@ -370,8 +445,17 @@ bitmoe_status_t moe_forward(const uint16_t* x, const uint16_t* residual, int64_t
                             const bitmoe_moe_weights_t* weights, const int32_t* forced_ids, const float* forced_w,
                             int32_t* topk_ids_out, float* topk_w_out, uint16_t* out, float* out_f32,
                             void* workspace, size_t workspace_bytes, void* stream) {
-  return forward_impl(x, residual, T, shape, weights, forced_ids, forced_w, topk_ids_out, topk_w_out, out, out_f32,
-                      workspace, workspace_bytes, stream, 0, 0.f, nullptr);
+  return forward_impl(x, residual, T, shape, weights ? layer_w(weights) : LayerW{}, forced_ids, forced_w, topk_ids_out,
+                      topk_w_out, out, out_f32, workspace, workspace_bytes, stream, 0, 0.f, nullptr, false);
+}
+
+bitmoe_status_t moe_forward_nvfp4(const uint16_t* x, const uint16_t* residual, int64_t T,
+                                  const bitmoe_moe_shape_t* shape, const bitmoe_moe_weights_nvfp4_t* weights,
+                                  const int32_t* forced_ids, const float* forced_w, int32_t* topk_ids_out,
+                                  float* topk_w_out, uint16_t* out, float* out_f32, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  return forward_impl(x, residual, T, shape, weights ? layer_w(weights) : LayerW{}, forced_ids, forced_w, topk_ids_out,
+                      topk_w_out, out, out_f32, workspace, workspace_bytes, stream, 0, 0.f, nullptr, true);
 }
 
 bitmoe_status_t moe_forward_prenorm(const uint16_t* residual, int64_t T, const bitmoe_moe_shape_t* shape,
@@ -379,8 +463,9 @@ bitmoe_status_t moe_forward_prenorm(const uint16_t* residual, int64_t T, const b
                                     const float* forced_w, int32_t* topk_ids_out, float* topk_w_out, uint16_t* xh_out,
                                     uint16_t* out, float* out_f32, void* workspace, size_t workspace_bytes,
                                     void* stream) {
-  return forward_impl(residual, residual, T, shape, weights, forced_ids, forced_w, topk_ids_out, topk_w_out, out,
-                      out_f32, workspace, workspace_bytes, stream, 1, eps, xh_out);
+  return forward_impl(residual, residual, T, shape, weights ? layer_w(weights) : LayerW{}, forced_ids, forced_w,
+                      topk_ids_out, topk_w_out, out, out_f32, workspace, workspace_bytes, stream, 1, eps, xh_out,
+                      false);
 }
 
 size_t moe_stack_workspace_size(const bitmoe_moe_shape_t* shape, int64_t T) {
@@ -394,6 +479,7 @@ bitmoe_status_t moe_stack_decode(uint16_t* residual, int64_t T, const bitmoe_moe
                                  int32_t* topk_ids_out, void* workspace, size_t workspace_bytes, void* stream) {
   bitmoe_status_t st = check_shape(shape, T);
   if (st != BITMOE_OK) return st;
+  if ((st = check_format(shape, false)) != BITMOE_OK) return st;
   if (!layers || n_layers < 1 || !(eps >= 0.f) || V < 0) return BITMOE_ERR_INVALID_ARG;
   if (T == 0) return BITMOE_OK;
   if (!residual || !aligned16(residual)) return BITMOE_ERR_INVALID_ARG;
@@ -456,6 +542,22 @@ bitmoe_status_t lmhead_int4_gemv(const uint16_t* h, int64_t T, int64_t d, int64_
   void* keys = static_cast<char*>(workspace) + 256;
   return cuda_status(launch_lmhead(h, (int)T, (int)d, (int)V, w_packed, logits, argmax, keys, st,
                                    (cudaStream_t)stream));
+}
+
+bitmoe_status_t lmhead_nvfp4_gemv(const uint16_t* h, int64_t T, int64_t d, int64_t V, const uint8_t* w_packed,
+                                  float tensor_scale, float* logits, int32_t* argmax, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  if (T < 0 || d <= 0 || V <= 0 || !std::isfinite(tensor_scale)) return BITMOE_ERR_INVALID_ARG;
+  if (d % kChunkK || V % kTileRows || T > 64 || d > 16384 || V > (int64_t(1) << 30)) return BITMOE_ERR_UNSUPPORTED;
+  if (T == 0) return BITMOE_OK;
+  if (!lmhead_supported((int)d, (int)T)) return BITMOE_ERR_UNSUPPORTED;
+  if (!h || !w_packed || !argmax || !aligned16(h) || !aligned16(w_packed)) return BITMOE_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < lmhead_workspace_size(T, d, V))
+    return BITMOE_ERR_WORKSPACE;
+  DevStatus* st = static_cast<DevStatus*>(workspace);
+  void* keys = static_cast<char*>(workspace) + 256;
+  return cuda_status(launch_lmhead_nvfp4(h, (int)T, (int)d, (int)V, w_packed, tensor_scale, logits, argmax, keys,
+                                         st, (cudaStream_t)stream));
 }
 
 bitmoe_status_t bitmoe_rmsnorm(const uint16_t* x, int64_t T, int64_t d, float eps, uint16_t* y, void* stream) {

@@ -146,27 +146,10 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], u
 //
 // A packed word holds the 8 nibbles one thread feeds to two k16 mma steps:
 // pair p (p = 0..3) sits at bits [4p, 4p+4) (first element) and
-// [16+4p, 20+4p) (second element).  Masking with 0x000F000F after a shift by
-// 4p puts the two nibbles in the low bits of each 16-bit half; XOR with 8
-// turns the two's-complement nibble n into q + 8, and OR-ing an exponent
-// pattern makes each half the float B + q + 8 with B = 128 (bf16) or 1024
-// (fp16), whose spacing is 1.  Subtracting B + 8 leaves q exactly.
-
-__device__ __forceinline__ uint32_t nib_pair_bf16(uint32_t w, int p) {
-  uint32_t t = ((w >> (4 * p)) & 0x000F000Fu) ^ 0x43084308u;  // 136 + q in each half
-  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&t);
-  const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
-  v = __hsub2(v, off);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ uint32_t nib_pair_f16(uint32_t w, int p) {
-  uint32_t t = ((w >> (4 * p)) & 0x000F000Fu) ^ 0x64086408u;  // 1032 + q in each half
-  __half2 v = *reinterpret_cast<__half2*>(&t);
-  const __half2 off = __floats2half2_rn(1032.0f, 1032.0f);
-  v = __hsub2(v, off);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
+// [16+4p, 20+4p) (second element).  Masking puts two nibbles in each 16-bit
+// half; XOR with 8 turns the two's-complement nibble n into q + 8, and the
+// fp16 exponent pattern of 1024 (whose spacing is 1) makes each half the
+// float 1024 + q + 8.  Subtracting 1032 leaves q exactly.
 
 // (a & b) ^ c in one LOP3 (truth table 0x6A for the operand order a, b, c).
 // The compiler otherwise splits a mask-and-flip into two logic instructions;
@@ -180,8 +163,7 @@ __device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t b, uint32_t c) 
 // All four fp16 pairs of a word, p = 0..3, with one shift instead of three:
 // an odd pair (nibbles at bits 4..7 of each half) is read in place as
 // 1024 + 16 (q + 8), which fits fp16's 10-bit mantissa, and one fused
-// multiply-add by 1/16 minus 72 leaves q (every step exact).  bf16 has only 7
-// mantissa bits, so it keeps the shifted form of nib_pair_bf16.  The f16x2
+// multiply-add by 1/16 minus 72 leaves q (every step exact).  The f16x2
 // constants are bit patterns held in registers (1032 = 0x6408, 1/16 = 0x2C00,
 // -72 = 0xD480), so each step is a single instruction: per 8 weights one
 // shift, four logic ops, two subtracts and two fused multiply-adds.
@@ -196,6 +178,68 @@ __device__ __forceinline__ void nib_pairs4_f16(uint32_t w, uint32_t (&o)[4]) {
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(o[2 * b]) : "r"(te), "r"(off));
     asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(o[2 * b + 1]) : "r"(to), "r"(sixteenth), "r"(off_hi));
   }
+}
+
+// 2^s as a float, exactly, for |s| <= 126.
+__device__ __forceinline__ float pow2i(int s) { return __int_as_float((s + 127) << 23); }
+
+// Exponent s that puts a bf16 row's largest magnitude (bits m, sign cleared)
+// in [2^14, 2^15): multiplying the row by 2^s makes every element an exact
+// fp16 value (bf16 carries 8 significant bits, fp16 11; only elements below
+// 2^-24 of the largest would round).  0 for an all-zero or subnormal-only row.
+__device__ __forceinline__ int f16_row_exponent(uint32_t m) {
+  const int ef = (int)(m >> 7);
+  return (ef == 0) ? 0 : min(126, max(-126, 14 - (ef - 127)));
+}
+
+// ---------------------------------------------------------------- NVFP4
+
+// NVFP4 weights: FP4 E2M1 codes, one FP8 E4M3 scale per 16 consecutive
+// weights of a row, one fp32 scale per matrix (the "four-bit NVFP" builds of
+// "Flint 40B : Best Mid Sized LLM", transcript 07:15).  The packed layout has
+// the int4 layout's geometry: a 128-column chunk of a 16-row tile holds the
+// 16 x 128 codes (1024 bytes, each 32-bit word the 8 codes of one lane's
+// fragment, byte j the pair that fragment register j takes, low nibble first)
+// and then 16 rows x 8 block scales (128 bytes).
+constexpr int kFp4Block = 16;
+
+// Block scale s (an E4M3 byte) as the fp16 pair (s, s), exactly (E4M3 is a
+// subset of fp16).
+__device__ __forceinline__ uint32_t e4m3_pair_f16(uint32_t byte) {
+  uint32_t d;
+  const uint16_t v = (uint16_t)(byte * 0x0101u);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(v));
+  return d;
+}
+
+// The eight E2M1 codes of a packed word as four fp16 pairs (hardware
+// conversion), each multiplied by the block scale pair sc.  Exact: a code has
+// at most 2 significant bits and a scale 4, so every product is an fp16 value
+// (|product| between 2^-10 and 2688, never below fp16's subnormal step).
+__device__ __forceinline__ void e2m1x8_f16_scaled(uint32_t w, uint32_t sc, uint32_t (&o)[4]) {
+  uint32_t c0, c1, c2, c3;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(c0), "=r"(c1), "=r"(c2), "=r"(c3)
+      : "r"(w));
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[0]) : "r"(c0), "r"(sc));
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[1]) : "r"(c1), "r"(sc));
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[2]) : "r"(c2), "r"(sc));
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[3]) : "r"(c3), "r"(sc));
+}
+
+// The four block-scale bytes a lane needs from one row's 8 scales of a chunk
+// (lane quarter c covers columns 8c .. 8c+7 of every 32-column group, which
+// lie in block 2 gg + c / 2 of the chunk for group gg): byte gg of the result
+// is the scale of group gg.
+__device__ __forceinline__ uint32_t fp4_lane_scales(uint2 s8, int c) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(s8.x), "r"(s8.y), "r"((c >> 1) ? 0x7531u : 0x6420u));
+  return d;
 }
 
 // D = A B (no accumulator input) for one m16n8k16 fp16 step.

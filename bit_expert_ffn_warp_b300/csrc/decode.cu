@@ -65,6 +65,9 @@ struct DecodeArgs {
   const uint8_t* down;
   const float* w_router;
   const float* b_router;
+  const float* gate_ts;  // NVFP4 banks: fp32 tensor scale per bank entry (null: int4 banks)
+  const float* up_ts;
+  const float* down_ts;
   const int32_t* forced_ids;
   const float* forced_w;
   uint16_t* out;
@@ -98,6 +101,9 @@ struct LayerPtrs {  // one layer's weights
   const uint8_t* down;
   const float* w_router;
   const float* b_router;
+  const float* gate_ts;  // NVFP4 tensor scales (null for int4 banks)
+  const float* up_ts;
+  const float* down_ts;
 };
 
 constexpr int kMaxStackLayers = 64;
@@ -190,8 +196,6 @@ __device__ __forceinline__ bool grid_barrier(unsigned* gb, int* fail, DevStatus*
   return grid_wait(gb, target, fail, st, where);
 }
 
-// 2^s as a float, exactly, for |s| <= 126.
-__device__ __forceinline__ float pow2i(int s) { return __int_as_float((s + 127) << 23); }
 
 // Copies the T staged bf16 token rows into fp16 rows of dst, token t scaled by
 // 2^sexp[t] so that its largest magnitude lands in [2^14, 2^15) (exact: bf16
@@ -262,6 +266,7 @@ struct Routing {  // shared-memory routing tables (identical in every CTA)
   float* part;   // [kDecWarps] partial sums
   int* sexp;     // [kDecMaxT] power-of-two scale of each staged fp16 token
   int* misc;     // [0] U, [1] fail flag, [2] candidate count, [3] tau slot
+  float* tsd;    // [R] NVFP4: W_down tensor scale of active expert a
 };
 
 // Top-k of one token by one warp, for batches of several tokens (one warp per
@@ -524,7 +529,10 @@ __device__ __noinline__ void lm_phase(const DecodeArgs& p, unsigned char* regA, 
 // The kernel body, one layer (kStack = false) or a stack of pre-norm layers
 // followed by RMSNorm, the LM head and the arg-max (kStack = true; layer l's
 // weights from tab[l], the residual updated in place).
-template <bool kStack>
+// kFp4: the expert banks are NVFP4 (each code times its E4M3 block scale is an
+// exact fp16 weight, the MMAs accumulate a whole row in fp32, and the tensor
+// scale multiplies the sums); else int4 with fp16 scales applied per group.
+template <bool kStack, bool kFp4>
 __device__ __forceinline__ void decode_body(const DecodeArgs& p, const LayerPtrs* tab) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -563,7 +571,8 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& p, const LayerPtrs
     rt.first = q; q += R;
     rt.act_e = q; q += R;
     rt.act_off = q; q += R + 1;
-    rt.misc = q;
+    rt.misc = q; q += 4;
+    rt.tsd = reinterpret_cast<float*>(q);
   }
   int* fail = rt.misc + 1;
 
@@ -606,7 +615,8 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& p, const LayerPtrs
   int ring_i = 0;  // ring uses so far (the producer and the consumers count alike)
   const int L = kStack ? p.n_layers : 1;
   for (int l = 0; l < L; ++l) {
-  const LayerPtrs lp = kStack ? tab[l] : LayerPtrs{p.gate, p.up, p.down, p.w_router, p.b_router};
+  const LayerPtrs lp = kStack ? tab[l]
+                              : LayerPtrs{p.gate, p.up, p.down, p.w_router, p.b_router, p.gate_ts, p.up_ts, p.down_ts};
   int32_t* ids_out = (kStack && p.ids_out) ? p.ids_out + (size_t)l * R : p.ids_out;
   float* w_out = (kStack && p.w_out) ? p.w_out + (size_t)l * R : p.w_out;
   if (l > 0) trace = nullptr;
@@ -966,10 +976,14 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& p, const LayerPtrs
   int i = ring_i;
   bool ok = true;
 
+  // NVFP4: this thread's active expert's W_down tensor scale, read now and
+  // kept in shared memory for P3 (the load's latency hides behind P2)
+  const float tsd_r = (kFp4 && tid < U) ? lp.down_ts[rt.act_e[tid]] : 1.0f;
   // P2: gate/up units, one 128-column chunk per warp
   for (int u = u_lo; u < u_hi; ++u) {
     const int a = u / RT, r16 = u - a * RT;
     const int na = rt.act_off[a + 1] - rt.act_off[a];
+    const float tsg = kFp4 ? lp.gate_ts[rt.act_e[a]] : 1.0f, tsu = kFp4 ? lp.up_ts[rt.act_e[a]] : 1.0f;
     const int sg = i % NS, su = (i + 1) % NS;
     if (ok) ok = mbar_wait(&full[sg], (i / NS) & 1, p.st, 37) && mbar_wait(&full[su], ((i + 1) / NS) & 1, p.st, 38);
     if (u == u_lo) stamp(trace, 12);
@@ -991,6 +1005,38 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& p, const LayerPtrs
       const uint2 sg1 = *reinterpret_cast<const uint2*>(cg + kChunkQBytes + (g + 8) * 8);
       const uint2 su0 = *reinterpret_cast<const uint2*>(cu + kChunkQBytes + g * 8);
       const uint2 su1 = *reinterpret_cast<const uint2*>(cu + kChunkQBytes + (g + 8) * 8);
+      if constexpr (kFp4) {
+        const uint32_t lg0 = fp4_lane_scales(sg0, c), lg1 = fp4_lane_scales(sg1, c);
+        const uint32_t lu0 = fp4_lane_scales(su0, c), lu1 = fp4_lane_scales(su1, c);
+        float dg[4], du[4];
+#pragma unroll
+        for (int gg = 0; gg < 4; ++gg) {
+          const int col = (ch * 4 + gg) * kGroup + c * 8;
+          const uint4 xb = *reinterpret_cast<const uint4*>(xrow + col * 2);
+          uint32_t pg0[4], pg1[4], pu0[4], pu1[4];
+          e2m1x8_f16_scaled(word_at(qg0, gg), e4m3_pair_f16((lg0 >> (8 * gg)) & 0xffu), pg0);
+          e2m1x8_f16_scaled(word_at(qg1, gg), e4m3_pair_f16((lg1 >> (8 * gg)) & 0xffu), pg1);
+          e2m1x8_f16_scaled(word_at(qu0, gg), e4m3_pair_f16((lu0 >> (8 * gg)) & 0xffu), pu0);
+          e2m1x8_f16_scaled(word_at(qu1, gg), e4m3_pair_f16((lu1 >> (8 * gg)) & 0xffu), pu1);
+          const uint32_t A0[4] = {pg0[0], pg1[0], pg0[1], pg1[1]}, A1[4] = {pg0[2], pg1[2], pg0[3], pg1[3]};
+          const uint32_t B0[4] = {pu0[0], pu1[0], pu0[1], pu1[1]}, B1[4] = {pu0[2], pu1[2], pu0[3], pu1[3]};
+          if (gg == 0) {  // a chunk's MMAs chain in the accumulator; chunks add in fp32
+            mma_f16_z(dg, A0, xb.x, xb.y);
+            mma_f16_z(du, B0, xb.x, xb.y);
+          } else {
+            mma_f16(dg, A0, xb.x, xb.y, dg);
+            mma_f16(du, B0, xb.x, xb.y, du);
+          }
+          mma_f16(dg, A1, xb.z, xb.w, dg);
+          mma_f16(du, B1, xb.z, xb.w, du);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          ag4[j] += dg[j];
+          au4[j] += du[j];
+        }
+        continue;
+      }
 #pragma unroll 2
       for (int gg = 0; gg < 4; ++gg) {
         const int col = (ch * 4 + gg) * kGroup + c * 8;
@@ -1048,7 +1094,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& p, const LayerPtrs
           uv += rb[(w * 32 + ln) * 8 + 4 + ix];
         }
         const float un = pow2i(-rt.sexp[rt.sorted[rt.act_off[a] + tok] / k]);  // undo the token's scale
-        const float h = silu_mul(av * un, uv * un);
+        const float h = silu_mul(av * (un * tsg), uv * (un * tsu));
         const __half hi = __float2half_rn(h);
         const __half lo = __float2half_rn(h - __half2float(hi));
         const size_t o = (size_t)(rt.act_off[a] + tok) * I + r16 * kTileRows + row;
@@ -1058,6 +1104,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& p, const LayerPtrs
     }
     if (u == u_lo) stamp(trace, 15);
   }
+  if (kFp4 && tid < U) rt.tsd[tid] = tsd_r;  // read in P3, after the barrier's CTA-wide sync
   stamp(trace, 5);
   const bool passed_b = grid_barrier(p.gbar, fail, p.st, 39, trace, 23);  // B: every h written
   stamp(trace, 6);
@@ -1106,6 +1153,47 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& p, const LayerPtrs
         const int p0 = rt.act_off[a];
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         const bool has = g < na;
+        if constexpr (kFp4) {
+          float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int ch = quarter; ch < I / kChunkK; ch += 4) {
+            float dh[4], dl[4];  // a chunk's MMAs chain in the accumulator; chunks add in fp32
+            const unsigned char* cw = tw + ch * kChunkBytes;
+            const uint4 q0 = *reinterpret_cast<const uint4*>(cw + (g * 4 + c) * 16);
+            const uint4 q1 = *reinterpret_cast<const uint4*>(cw + ((g + 8) * 4 + c) * 16);
+            const uint32_t l0 = fp4_lane_scales(*reinterpret_cast<const uint2*>(cw + kChunkQBytes + g * 8), c);
+            const uint32_t l1 = fp4_lane_scales(*reinterpret_cast<const uint2*>(cw + kChunkQBytes + (g + 8) * 8), c);
+#pragma unroll
+            for (int gg = 0; gg < 4; ++gg) {
+              const int col = (ch * 4 + gg) * kGroup + c * 8;
+              uint4 bh = make_uint4(0, 0, 0, 0), bl = make_uint4(0, 0, 0, 0);
+              if (has) {
+                bh = *reinterpret_cast<const uint4*>(hhi + (size_t)(p0 + g) * hstride + col * 2);
+                bl = *reinterpret_cast<const uint4*>(hlo + (size_t)(p0 + g) * hstride + col * 2);
+              }
+              uint32_t w0[4], w1[4];
+              e2m1x8_f16_scaled(word_at(q0, gg), e4m3_pair_f16((l0 >> (8 * gg)) & 0xffu), w0);
+              e2m1x8_f16_scaled(word_at(q1, gg), e4m3_pair_f16((l1 >> (8 * gg)) & 0xffu), w1);
+              const uint32_t A0[4] = {w0[0], w1[0], w0[1], w1[1]}, A1[4] = {w0[2], w1[2], w0[3], w1[3]};
+              if (gg == 0) {
+                mma_f16_z(dh, A0, bh.x, bh.y);
+                mma_f16_z(dl, A0, bl.x, bl.y);
+              } else {
+                mma_f16(dh, A0, bh.x, bh.y, dh);
+                mma_f16(dl, A0, bl.x, bl.y, dl);
+              }
+              mma_f16(dh, A1, bh.z, bh.w, dh);
+              mma_f16(dl, A1, bl.z, bl.w, dl);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              sh[q] += dh[q];
+              sl[q] += dl[q];
+            }
+          }
+          const float tsd = rt.tsd[a];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[q] = (sh[q] + sl[q]) * tsd;
+        } else
         for (int ch = quarter; ch < I / kChunkK; ch += 4) {
           const unsigned char* cw = tw + ch * kChunkBytes;
           const uint4 q0 = *reinterpret_cast<const uint4*>(cw + (g * 4 + c) * 16);
@@ -1196,12 +1284,13 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& p, const LayerPtrs
     lm_phase(p, regA, x16, ring, full, empty, rt.part, rt.sexp, rt.cand, ring_i, fail);
 }
 
+template <bool kFp4>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const __grid_constant__ DecodeArgs p) {
-  decode_body<false>(p, nullptr);
+  decode_body<false, kFp4>(p, nullptr);
 }
 
 __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __grid_constant__ StackArgs a) {
-  decode_body<true>(a.base, a.tab);
+  decode_body<true, false>(a.base, a.tab);
 }
 
 struct DecodePlan {
@@ -1227,7 +1316,7 @@ DecodePlan plan(int T, int d, int E, int k, int I, int n_shared, int G) {
   const size_t p2 = (size_t)2 * kDecWarps * 32 * 8 * 4 + (size_t)4 * R * kTileRows * 4;
   const size_t regB = ((p0 > p2 ? p0 : p2) + 127) / 128 * 128;
   const size_t regR = ((size_t)(kDecWarps + kConsumers + kDecMaxT * kDecMaxK) * 8 +
-                       (size_t)(2 * kDecMaxT + kDecWarps + 7 * R + 1 + 4) * 4 + 127) / 128 * 128;
+                       (size_t)(2 * kDecMaxT + kDecWarps + 8 * R + 1 + 4) * 4 + 127) / 128 * 128;
   pl.offA = 1024;
   pl.offB = pl.offA + (int)regA;
   pl.offR = pl.offB + (int)regB;
@@ -1300,6 +1389,9 @@ DecodeArgs fill_args(const DecodeLaunch& L, const DecodePlan& pl, int G) {
   a.down = L.down;
   a.w_router = L.w_router;
   a.b_router = L.b_router;
+  a.gate_ts = L.gate_ts;
+  a.up_ts = L.up_ts;
+  a.down_ts = L.down_ts;
   a.forced_ids = L.forced_ids;
   a.forced_w = L.forced_w;
   a.out = L.out;
@@ -1347,11 +1439,18 @@ cudaError_t launch_decode_fused(const DecodeLaunch& L, cudaStream_t s) {
   const int G = sm_count();
   const DecodePlan pl = plan(L.T, L.d, L.E, L.k, L.I, L.n_shared, G);
   if (!pl.ok) return cudaErrorNotSupported;
+  if (L.gate_ts != nullptr) {  // NVFP4 banks
+    static int attr_set[64] = {};
+    static size_t occ_ok[64] = {};
+    cudaError_t err = prepare_fused(decode_layer_kernel<true>, pl.smem, attr_set, occ_ok);
+    if (err != cudaSuccess) return err;
+    return launch_fused(decode_layer_kernel<true>, fill_args(L, pl, G), G, pl.smem, L.pdl, s);
+  }
   static int attr_set[64] = {};
   static size_t occ_ok[64] = {};
-  cudaError_t err = prepare_fused(decode_layer_kernel, pl.smem, attr_set, occ_ok);
+  cudaError_t err = prepare_fused(decode_layer_kernel<false>, pl.smem, attr_set, occ_ok);
   if (err != cudaSuccess) return err;
-  return launch_fused(decode_layer_kernel, fill_args(L, pl, G), G, pl.smem, L.pdl, s);
+  return launch_fused(decode_layer_kernel<false>, fill_args(L, pl, G), G, pl.smem, L.pdl, s);
 }
 
 bool decode_stack_eligible(int T, int d, int E, int k, int I, int n_shared, int n_layers, int V) {

@@ -7,13 +7,22 @@
 // tiles in the packed layout and the unit's activation rows) on an mbarrier;
 // four warps split the reduction dimension by 128-column chunks.
 //
-// Arithmetic.  The int4 values are turned into exact 16-bit integers (bf16 for
-// the bf16 activations, fp16 for h) and multiplied on the tensor cores with
-// mma.sync m16n8k16 (weights = A, up to 8 tokens = B).  Each mma pair covers
+// Arithmetic.  The int4 values are turned into exact fp16 integers (one shift
+// per 8 nibbles with the magic-number conversion) and multiplied on the tensor
+// cores with mma.sync m16n8k16 (weights = A, up to 8 tokens = B).  The bf16
+// activation rows are staged as fp16 scaled by a power of two per row, which
+// is exact (the largest |x| lands in [2^14, 2^15)) and undone on the sums.  Each mma pair covers
 // exactly one 32-column group, so its fp32 result is the group's exact-input
 // partial sum, which is then scaled by the group's fp16 scale in fp32: the
 // dequantised weight q*s is never rounded.  h enters the down projection as
 // an fp16 pair hi + lo (about 22 significant bits).
+//
+// NVFP4 banks (kFp4): each E2M1 code times its E4M3 block scale is an exact
+// fp16 weight, so the weights enter the MMAs in fp16 with the scale already
+// applied, a 128-column chunk's MMAs chain in the accumulator and the chunks
+// add in fp32; the activation rows are turned into fp16 scaled by a power of
+// two per row (exact, undone on the sums) and the tensor scale multiplies the
+// result.
 #include "kernels.h"
 
 namespace bitmoe {
@@ -27,21 +36,25 @@ __device__ __forceinline__ float scale_at(uint2 s, int gg) {
   return __half2float(__ushort_as_half(b));
 }
 
-// A fragments of two k16 steps for rows g (word w0) and g+8 (word w1).
-__device__ __forceinline__ void frag_bf16(uint32_t w0, uint32_t w1, uint32_t (&a)[2][4]) {
-#pragma unroll
-  for (int s = 0; s < 2; ++s) {
-    a[s][0] = nib_pair_bf16(w0, 2 * s);
-    a[s][1] = nib_pair_bf16(w1, 2 * s);
-    a[s][2] = nib_pair_bf16(w0, 2 * s + 1);
-    a[s][3] = nib_pair_bf16(w1, 2 * s + 1);
-  }
-}
-
 __device__ __forceinline__ void frag_f16(uint32_t w0, uint32_t w1, uint32_t (&a)[2][4]) {
   uint32_t p0[4], p1[4];
   nib_pairs4_f16(w0, p0);
   nib_pairs4_f16(w1, p1);
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    a[s][0] = p0[2 * s];
+    a[s][1] = p1[2 * s];
+    a[s][2] = p0[2 * s + 1];
+    a[s][3] = p1[2 * s + 1];
+  }
+}
+
+// NVFP4: A fragments of two k16 steps for rows g (word w0, block scale byte s0)
+// and g+8 (w1, s1), each weight the exact fp16 code times its block scale.
+__device__ __forceinline__ void frag_fp4(uint32_t w0, uint32_t w1, uint32_t s0, uint32_t s1, uint32_t (&a)[2][4]) {
+  uint32_t p0[4], p1[4];
+  e2m1x8_f16_scaled(w0, e4m3_pair_f16(s0), p0);
+  e2m1x8_f16_scaled(w1, e4m3_pair_f16(s1), p1);
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
     a[s][0] = p0[2 * s];
@@ -152,6 +165,39 @@ struct Blk {
   int e, p0, nval;
 };
 
+// NVFP4 path: the block's bf16 activation rows, in place, as fp16 scaled by
+// 2^sexp[r] (the largest |x| of row r in [2^14, 2^15), exact); consumer warp w
+// takes rows w, w + 8.
+__device__ __forceinline__ void rows_to_scaled_f16(unsigned char* sx, int nval, int d, int xstride, int* sexp,
+                                                   int warp, int lane) {
+  for (int r = warp; r < nval; r += kConsWarps) {
+    uint16_t* xr = reinterpret_cast<uint16_t*>(sx + r * xstride);
+    uint32_t m = 0;
+    for (int c = lane * 8; c < d; c += 256) {
+      const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) m = max(m, max(w4[i] & 0x7fffu, (w4[i] >> 16) & 0x7fffu));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+    const int sc = f16_row_exponent(m);
+    if (lane == 0) sexp[r] = sc;
+    const float f = pow2i(sc);
+    for (int c = lane * 8; c < d; c += 256) {
+      const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __half2 h2 = __floats2half2_rn(__uint_as_float(w4[i] << 16) * f, __uint_as_float(w4[i] & 0xffff0000u) * f);
+        o[i] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      *reinterpret_cast<uint4*>(xr + c) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
 __device__ __forceinline__ Blk block_info(const FfnArgs& p, int b) {
   Blk k;
   k.e = expert_of_block(p.blk_prefix, p.E, b);
@@ -167,6 +213,7 @@ __device__ __forceinline__ Blk block_info(const FfnArgs& p, int b) {
 // warp w takes the 128-column chunks w, w + 8, ...; partial sums meet in a
 // double-buffered shared array and one thread per (row, token) applies SwiGLU.
 
+template <bool kFp4>
 __global__ void __launch_bounds__(kPipeThreads, 1) ffn_up_kernel(FfnArgs p, int ns) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int d = p.d, I = p.I;
@@ -176,6 +223,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) ffn_up_kernel(FfnArgs p, int 
   float* red = reinterpret_cast<float*>(sx + kTokBlock * xstride);        // [2][8 warps][32][8 * kNT]
   unsigned char* ring = reinterpret_cast<unsigned char*>(red + 2 * kConsWarps * 32 * 8 * kNT);
   const Pipe pp = pipe_init(smem, ns);
+  int* sexp = reinterpret_cast<int*>(smem + 512);  // [16] NVFP4: the rows' power-of-two scales
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
   const int RT = I / kTileRows;
   int u_lo, u_hi;
@@ -223,6 +271,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) ffn_up_kernel(FfnArgs p, int 
   const int nch = d / kChunkK;
   int cur_b = -1, j = 0, i = 0;
   Blk k{};
+  float tsg = 1.f, tsu = 1.f;
   for (int u = u_lo; u < u_hi; ++u, ++i) {
     const int b = u / RT, rt = u - b * RT;
     bool ok = true;
@@ -235,6 +284,12 @@ __global__ void __launch_bounds__(kPipeThreads, 1) ffn_up_kernel(FfnArgs p, int 
       ++j;
       cur_b = b;
       k = block_info(p, b);
+      if constexpr (kFp4) {
+        tsg = p.gate_ts[k.e];
+        tsu = p.up_ts[k.e];
+      }
+      if (ok) rows_to_scaled_f16(sx, k.nval, d, xstride, sexp, warp, lane);
+      if (cons_sync_or(!ok)) ok = false;  // every row converted before any warp reads one
     }
     const int s = i % ns;
     ok = ok && pwait(&pp.full[s], (i / ns) & 1, pp, p.st, 16);
@@ -259,12 +314,61 @@ __global__ void __launch_bounds__(kPipeThreads, 1) ffn_up_kernel(FfnArgs p, int 
         const uint2 sg1 = *reinterpret_cast<const uint2*>(cg + kChunkQBytes + (g + 8) * 8);
         const uint2 su0 = *reinterpret_cast<const uint2*>(cu + kChunkQBytes + g * 8);
         const uint2 su1 = *reinterpret_cast<const uint2*>(cu + kChunkQBytes + (g + 8) * 8);
+        if constexpr (kFp4) {
+          const uint32_t lg0 = fp4_lane_scales(sg0, c), lg1 = fp4_lane_scales(sg1, c);
+          const uint32_t lu0 = fp4_lane_scales(su0, c), lu1 = fp4_lane_scales(su1, c);
+          float dg[kNT][4], du[kNT][4];
+#pragma unroll
+          for (int gg = 0; gg < 4; ++gg) {
+            const int col = (ch * 4 + gg) * kGroup + c * 8;
+            uint32_t ag[2][4], au[2][4];
+            frag_fp4(word_at(qg0, gg), word_at(qg1, gg), (lg0 >> (8 * gg)) & 0xffu, (lg1 >> (8 * gg)) & 0xffu, ag);
+            frag_fp4(word_at(qu0, gg), word_at(qu1, gg), (lu0 >> (8 * gg)) & 0xffu, (lu1 >> (8 * gg)) & 0xffu, au);
+            uint4 xb[kNT];
+#pragma unroll
+            for (int nt = 0; nt < kNT; ++nt) {
+              const int tok = nt * 8 + g;
+              xb[nt] = make_uint4(0, 0, 0, 0);
+              if (nt < nt_lim && tok < k.nval) xb[nt] = *reinterpret_cast<const uint4*>(sx + tok * xstride + col * 2);
+            }
+            const float z[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int nt = 0; nt < kNT; ++nt) {
+              if (nt < nt_lim) {  // a chunk's MMAs chain in the accumulator; chunks add in fp32
+                if (gg == 0) {
+                  mma_f16(dg[nt], ag[0], xb[nt].x, xb[nt].y, z);
+                  mma_f16(du[nt], au[0], xb[nt].x, xb[nt].y, z);
+                } else {
+                  mma_f16(dg[nt], ag[0], xb[nt].x, xb[nt].y, dg[nt]);
+                  mma_f16(du[nt], au[0], xb[nt].x, xb[nt].y, du[nt]);
+                }
+              }
+            }
+#pragma unroll
+            for (int nt = 0; nt < kNT; ++nt) {
+              if (nt < nt_lim) {
+                mma_f16(dg[nt], ag[1], xb[nt].z, xb[nt].w, dg[nt]);
+                mma_f16(du[nt], au[1], xb[nt].z, xb[nt].w, du[nt]);
+              }
+            }
+          }
+#pragma unroll
+          for (int nt = 0; nt < kNT; ++nt) {
+            if (nt >= nt_lim) continue;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              acc_g[nt][q] += dg[nt][q];
+              acc_u[nt][q] += du[nt][q];
+            }
+          }
+          continue;
+        }
 #pragma unroll
         for (int gg = 0; gg < 4; ++gg) {
           const int col = (ch * 4 + gg) * kGroup + c * 8;
           uint32_t ag[2][4], au[2][4];
-          frag_bf16(word_at(qg0, gg), word_at(qg1, gg), ag);
-          frag_bf16(word_at(qu0, gg), word_at(qu1, gg), au);
+          frag_f16(word_at(qg0, gg), word_at(qg1, gg), ag);
+          frag_f16(word_at(qu0, gg), word_at(qu1, gg), au);
           const float s_g0 = scale_at(sg0, gg), s_g1 = scale_at(sg1, gg);
           const float s_u0 = scale_at(su0, gg), s_u1 = scale_at(su1, gg);
           uint4 xb[kNT];
@@ -280,15 +384,15 @@ __global__ void __launch_bounds__(kPipeThreads, 1) ffn_up_kernel(FfnArgs p, int 
 #pragma unroll
           for (int nt = 0; nt < kNT; ++nt) {
             if (nt < nt_lim) {
-              mma_bf16(dg[nt], ag[0], xb[nt].x, xb[nt].y, z);
-              mma_bf16(du[nt], au[0], xb[nt].x, xb[nt].y, z);
+              mma_f16(dg[nt], ag[0], xb[nt].x, xb[nt].y, z);
+              mma_f16(du[nt], au[0], xb[nt].x, xb[nt].y, z);
             }
           }
 #pragma unroll
           for (int nt = 0; nt < kNT; ++nt) {
             if (nt < nt_lim) {
-              mma_bf16(dg[nt], ag[1], xb[nt].z, xb[nt].w, dg[nt]);
-              mma_bf16(du[nt], au[1], xb[nt].z, xb[nt].w, du[nt]);
+              mma_f16(dg[nt], ag[1], xb[nt].z, xb[nt].w, dg[nt]);
+              mma_f16(du[nt], au[1], xb[nt].z, xb[nt].w, du[nt]);
             }
           }
 #pragma unroll
@@ -328,6 +432,11 @@ __global__ void __launch_bounds__(kPipeThreads, 1) ffn_up_kernel(FfnArgs p, int 
         for (int w = 0; w < kConsWarps; ++w) {
           a += rb[((size_t)w * (8 * kNT) + nt * 4 + q) * 32 + ln];
           uu += rb[((size_t)w * (8 * kNT) + 4 * kNT + nt * 4 + q) * 32 + ln];
+        }
+        {  // undo the row's power of two (and apply NVFP4 tensor scales)
+          const float un = pow2i(-sexp[tok]);
+          a *= un * tsg;
+          uu *= un * tsu;
         }
         const float h = silu_mul(a, uu);
         const __half hi = __float2half_rn(h);
@@ -396,6 +505,36 @@ __device__ __forceinline__ void down_chunk(const unsigned char* cw, const unsign
   }
 }
 
+// NVFP4 form of down_chunk: the chunk's MMAs chain in the accumulator (exact
+// fp16 weights), then the hi and lo sums add into acc in fp32.
+__device__ __forceinline__ void down_chunk_fp4(const unsigned char* cw, const unsigned char* hh,
+                                               const unsigned char* hl, bool has, int ch, int g, int c,
+                                               float (&acc)[4]) {
+  const uint4 q0 = *reinterpret_cast<const uint4*>(cw + (g * 4 + c) * 16);
+  const uint4 q1 = *reinterpret_cast<const uint4*>(cw + ((g + 8) * 4 + c) * 16);
+  const uint32_t l0 = fp4_lane_scales(*reinterpret_cast<const uint2*>(cw + kChunkQBytes + g * 8), c);
+  const uint32_t l1 = fp4_lane_scales(*reinterpret_cast<const uint2*>(cw + kChunkQBytes + (g + 8) * 8), c);
+  float dh[4] = {0.f, 0.f, 0.f, 0.f}, dl[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int gg = 0; gg < 4; ++gg) {
+    const int col = (ch * 4 + gg) * kGroup + c * 8;
+    uint32_t a[2][4];
+    frag_fp4(word_at(q0, gg), word_at(q1, gg), (l0 >> (8 * gg)) & 0xffu, (l1 >> (8 * gg)) & 0xffu, a);
+    uint4 bh = make_uint4(0, 0, 0, 0), bl = make_uint4(0, 0, 0, 0);
+    if (has) {
+      bh = *reinterpret_cast<const uint4*>(hh + col * 2);
+      bl = *reinterpret_cast<const uint4*>(hl + col * 2);
+    }
+    mma_f16(dh, a[0], bh.x, bh.y, dh);
+    mma_f16(dl, a[0], bl.x, bl.y, dl);
+    mma_f16(dh, a[1], bh.z, bh.w, dh);
+    mma_f16(dl, a[1], bl.z, bl.w, dl);
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) acc[q] += dh[q] + dl[q];
+}
+
+template <bool kFp4>
 __global__ void __launch_bounds__(kPipeThreads, 1) ffn_down_kernel(FfnArgs p, int ns) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int d = p.d, I = p.I;
@@ -473,18 +612,27 @@ __global__ void __launch_bounds__(kPipeThreads, 1) ffn_down_kernel(FfnArgs p, in
     if (ok) {
       if (small) {
         const bool has = g < k.nval;
-        for (int ch = warp & 3; ch < nch; ch += 4)
-          down_chunk(sw + ch * kChunkBytes, shh + g * hstride, shl + g * hstride, has, ch, g, c, acc);
+        for (int ch = warp & 3; ch < nch; ch += 4) {
+          if constexpr (kFp4)
+            down_chunk_fp4(sw + ch * kChunkBytes, shh + g * hstride, shl + g * hstride, has, ch, g, c, acc);
+          else
+            down_chunk(sw + ch * kChunkBytes, shh + g * hstride, shl + g * hstride, has, ch, g, c, acc);
+        }
       } else {
         const int nt = warp & 1, tok = nt * 8 + g;
         const bool has = tok < k.nval;
         for (int ch0 = 2 * ((warp >> 1) & 1); ch0 < nch; ch0 += 4)
-          for (int ch = ch0; ch < ch0 + 2 && ch < nch; ++ch)
-            down_chunk(sw + ch * kChunkBytes, shh + tok * hstride, shl + tok * hstride, has, ch, g, c, acc);
+          for (int ch = ch0; ch < ch0 + 2 && ch < nch; ++ch) {
+            if constexpr (kFp4)
+              down_chunk_fp4(sw + ch * kChunkBytes, shh + tok * hstride, shl + tok * hstride, has, ch, g, c, acc);
+            else
+              down_chunk(sw + ch * kChunkBytes, shh + tok * hstride, shl + tok * hstride, has, ch, g, c, acc);
+          }
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive_one(&pp.empty[s]);
+    const float tsd = kFp4 ? p.down_ts[k.e] : 1.f;
     float* rb = red + (size_t)(i & 1) * kConsWarps * 32 * 4;  // [warp][value][lane]
 #pragma unroll
     for (int q = 0; q < 4; ++q) rb[((size_t)warp * 4 + q) * 32 + lane] = acc[q];
@@ -498,7 +646,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) ffn_down_kernel(FfnArgs p, in
           float v = 0.f;
 #pragma unroll
           for (int w = 0; w < 4; ++w) v += rb[((size_t)(tl * 4 + w) * 4 + q) * 32 + ln];
-          p.y_rows[(size_t)(k.p0 + t8) * d + ybase] = v;
+          p.y_rows[(size_t)(k.p0 + t8) * d + ybase] = kFp4 ? v * tsd : v;
         }
       } else {
 #pragma unroll
@@ -506,7 +654,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) ffn_down_kernel(FfnArgs p, in
           const int tk = nt * 8 + t8;
           if (tk < k.nval) {
             const float v = rb[((size_t)(tl * 4 + nt) * 4 + q) * 32 + ln] + rb[((size_t)(tl * 4 + 2 + nt) * 4 + q) * 32 + ln];
-            p.y_rows[(size_t)(k.p0 + tk) * d + ybase] = v;
+            p.y_rows[(size_t)(k.p0 + tk) * d + ybase] = kFp4 ? v * tsd : v;
           }
         }
       }
@@ -546,12 +694,17 @@ cudaError_t launch_ffn_up(const FfnArgs& a, cudaStream_t s) {
   int ns = (int)((kFfnSmemBudget - fixed) / stage);
   if (ns > kMaxRing) ns = kMaxRing;
   const size_t sm = fixed + (size_t)ns * stage;
-  static int attr_set[64] = {};
-  cudaError_t err = ensure_smem_attr(ffn_up_kernel, sm, attr_set);
-  if (err != cudaSuccess) return err;
   const long units = (long)(a.I / kTileRows) * max_blocks(R, a.E);
   const int grid = (int)(units < num_sms() ? units : num_sms());
-  ffn_up_kernel<<<grid, kPipeThreads, sm, s>>>(a, ns);
+  static int attr_set[64] = {}, attr_fp4[64] = {};
+  cudaError_t err;
+  if (a.gate_ts != nullptr) {
+    if ((err = ensure_smem_attr(ffn_up_kernel<true>, sm, attr_fp4)) != cudaSuccess) return err;
+    ffn_up_kernel<true><<<grid, kPipeThreads, sm, s>>>(a, ns);
+  } else {
+    if ((err = ensure_smem_attr(ffn_up_kernel<false>, sm, attr_set)) != cudaSuccess) return err;
+    ffn_up_kernel<false><<<grid, kPipeThreads, sm, s>>>(a, ns);
+  }
   return cudaGetLastError();
 }
 
@@ -564,12 +717,17 @@ cudaError_t launch_ffn_down(const FfnArgs& a, cudaStream_t s) {
   int ns = (int)((kFfnSmemBudget - fixed) / stage);
   if (ns > kMaxRing) ns = kMaxRing;
   const size_t sm = fixed + (size_t)ns * stage;
-  static int attr_set[64] = {};
-  cudaError_t err = ensure_smem_attr(ffn_down_kernel, sm, attr_set);
-  if (err != cudaSuccess) return err;
   const long units = (long)(a.d / kTileRows / 2) * max_blocks(R, a.E);
   const int grid = (int)(units < num_sms() ? units : num_sms());
-  ffn_down_kernel<<<grid, kPipeThreads, sm, s>>>(a, ns);
+  static int attr_set[64] = {}, attr_fp4[64] = {};
+  cudaError_t err;
+  if (a.down_ts != nullptr) {
+    if ((err = ensure_smem_attr(ffn_down_kernel<true>, sm, attr_fp4)) != cudaSuccess) return err;
+    ffn_down_kernel<true><<<grid, kPipeThreads, sm, s>>>(a, ns);
+  } else {
+    if ((err = ensure_smem_attr(ffn_down_kernel<false>, sm, attr_set)) != cudaSuccess) return err;
+    ffn_down_kernel<false><<<grid, kPipeThreads, sm, s>>>(a, ns);
+  }
   return cudaGetLastError();
 }
 

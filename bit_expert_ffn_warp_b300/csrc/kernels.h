@@ -35,6 +35,9 @@ struct FfnArgs {
   const uint8_t* gate;  // packed banks
   const uint8_t* up;
   const uint8_t* down;
+  const float* gate_ts;        // NVFP4 banks: tensor scale per bank entry; null = int4 banks
+  const float* up_ts;
+  const float* down_ts;
   const int32_t* offsets;      // [E+1]
   const int32_t* sorted_rows;  // [R]
   const int32_t* blk_prefix;   // [E+1]
@@ -66,6 +69,9 @@ struct DecodeLaunch {
   const uint8_t* down;
   const float* w_router;
   const float* b_router;
+  const float* gate_ts;       // NVFP4 banks: tensor scale per bank entry; null = int4 banks
+  const float* up_ts;
+  const float* down_ts;
   const int32_t* forced_ids;  // null = route; else [T, k + n_shared]
   const float* forced_w;
   uint16_t* out;
@@ -109,6 +115,8 @@ cudaError_t launch_combine(const float* y_rows, const int32_t* inv, const float*
 cudaError_t launch_rmsnorm(const uint16_t* x, int T, int d, float eps, uint16_t* y, cudaStream_t s);
 cudaError_t launch_pack_int4(const uint8_t* q, const uint16_t* scale, int64_t n_mats, int64_t rows, int64_t K,
                              uint8_t* packed, cudaStream_t s);
+cudaError_t launch_pack_nvfp4(const uint8_t* q, const uint8_t* scale, int64_t n_mats, int64_t rows, int64_t K,
+                              uint8_t* packed, cudaStream_t s);
 
 // ---------------------------------------------------------------- LM head (lmhead.cu)
 size_t lmhead_scratch_bytes(int T);
@@ -116,6 +124,9 @@ size_t lmhead_scratch_bytes(int T);
 bool lmhead_supported(int d, int T);
 cudaError_t launch_lmhead(const uint16_t* h, int T, int d, int V, const uint8_t* w_packed, float* logits,
                           int32_t* argmax, void* scratch, DevStatus* st, cudaStream_t s);
+// The same over a packed NVFP4 bank with tensor scale ts.
+cudaError_t launch_lmhead_nvfp4(const uint16_t* h, int T, int d, int V, const uint8_t* w_packed, float ts,
+                                float* logits, int32_t* argmax, void* scratch, DevStatus* st, cudaStream_t s);
 
 // ---------------------------------------------------------------- C-ABI helpers (api.cu)
 // Records e as the thread's last CUDA error (read by bitmoe_last_cuda_error) and maps it to a status.

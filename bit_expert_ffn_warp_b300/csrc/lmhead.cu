@@ -1,4 +1,6 @@
-// 4-bit LM head: logits = h Wlm^T and the argmax over the vocabulary.
+// 4-bit LM head: logits = h Wlm^T and the argmax over the vocabulary, with
+// int4 (fp16 scale per 32 weights) or NVFP4 (E2M1 codes, E4M3 scale per 16
+// weights, fp32 tensor scale) weights.
 //
 // "Flint 40B : Best Mid Sized LLM", transcript 03:36 (the output layer maps
 // hidden states to a ~150k-token vocabulary) and 05:39 (it is quantised to
@@ -40,6 +42,7 @@ struct LmArgs {
   int ntok, d, V, tok0, nstages;
   int nwarps;  // consumer warps that take tiles (nstages is a multiple of it)
   const uint8_t* w;
+  float ts;                  // NVFP4: the matrix's tensor scale
   float* logits;             // [T_total, V] or null
   unsigned long long* keys;  // [T_total]
   DevStatus* st;
@@ -61,8 +64,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kLmConsumers * 32)); }
 
-// 2^s as a float, exactly, for |s| <= 126.
-__device__ __forceinline__ float pow2i(int s) { return __int_as_float((s + 127) << 23); }
 
 // Shared memory: barriers (256 B), the per-token scale exponents and arg-max
 // partials, the fp16 tokens [8 * NT][d + pad] and one zeroed row, then the tile ring.
@@ -80,7 +81,10 @@ struct LmSmem {
 static_assert((2 * kLmMaxStages + 1) * 8 <= LmSmem::kExp, "lm head barriers");
 static_assert(LmSmem::kFail + 4 <= LmSmem::kX, "lm head smem header");
 
-template <int NT>
+// kFp4: the bank is NVFP4 (codes times block scale become exact fp16 weights
+// before the MMA, whose fp32 sums run over the whole row; the tensor scale
+// multiplies the logit); else int4 with fp16 group scales applied per group.
+template <int NT, bool kFp4>
 __global__ void __launch_bounds__(kLmThreads, 1) lmhead_kernel(LmArgs p) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + LmSmem::kBars);
@@ -240,6 +244,36 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_kernel(LmArgs p) {
       const uint4 q1 = *reinterpret_cast<const uint4*>(cw + ((g + 8) * 4 + c) * 16);
       const uint2 s0 = *reinterpret_cast<const uint2*>(cw + kChunkQBytes + g * 8);
       const uint2 s1 = *reinterpret_cast<const uint2*>(cw + kChunkQBytes + (g + 8) * 8);
+      if constexpr (kFp4) {
+        // the chunk's 8 MMA steps chain in the tensor core's accumulator; the
+        // chunks are then added in fp32 (a chain over the whole row would
+        // drift: the tensor core does not round its additions to nearest)
+        const uint32_t sl0 = fp4_lane_scales(s0, c), sl1 = fp4_lane_scales(s1, c);
+        float dd[NT][4];
+#pragma unroll
+        for (int gg = 0; gg < 4; ++gg) {
+          const int col = (ch * 4 + gg) * kGroup + c * 8;
+          uint32_t p0[4], p1[4];
+          e2m1x8_f16_scaled(word_at(q0, gg), e4m3_pair_f16((sl0 >> (8 * gg)) & 0xffu), p0);
+          e2m1x8_f16_scaled(word_at(q1, gg), e4m3_pair_f16((sl1 >> (8 * gg)) & 0xffu), p1);
+          const uint32_t a0[4] = {p0[0], p1[0], p0[1], p1[1]};
+          const uint32_t a1[4] = {p0[2], p1[2], p0[3], p1[3]};
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const uint4 xb = *reinterpret_cast<const uint4*>(xrow[nt] + col * 2);
+            if (gg == 0)
+              mma_f16_z(dd[nt], a0, xb.x, xb.y);
+            else
+              mma_f16(dd[nt], a0, xb.x, xb.y, dd[nt]);
+            mma_f16(dd[nt], a1, xb.z, xb.w, dd[nt]);
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[nt][j] += dd[nt][j];
+        continue;
+      }
 #pragma unroll
       for (int gg = 0; gg < 4; ++gg) {
         const int col = (ch * 4 + gg) * kGroup + c * 8;
@@ -273,7 +307,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_kernel(LmArgs p) {
         const int tok = nt * 8 + 2 * c + b;
         const int vrow = vrow0 + g + ((j >= 2) ? 8 : 0);
         if (tok < p.ntok) {
-          const float v = acc[nt][j] * unscale[nt][b];
+          const float v = kFp4 ? acc[nt][j] * (unscale[nt][b] * p.ts) : acc[nt][j] * unscale[nt][b];
           if (p.logits) p.logits[(size_t)(p.tok0 + tok) * p.V + vrow] = v;
           if (v > best_v[nt][b] || (v == best_v[nt][b] && vrow < best_i[nt][b])) {
             best_v[nt][b] = v;
@@ -342,8 +376,9 @@ size_t lmhead_scratch_bytes(int T) { return (size_t)T * sizeof(unsigned long lon
 
 bool lmhead_supported(int d, int T) { return lm_stages(d, T < kLmTok ? T : kLmTok) >= 2; }
 
-cudaError_t launch_lmhead(const uint16_t* h, int T, int d, int V, const uint8_t* w_packed, float* logits,
-                          int32_t* argmax, void* scratch, DevStatus* st, cudaStream_t s) {
+template <bool kFp4>
+cudaError_t launch_lmhead_fmt(const uint16_t* h, int T, int d, int V, const uint8_t* w_packed, float ts,
+                              float* logits, int32_t* argmax, void* scratch, DevStatus* st, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   if (!lmhead_supported(d, T)) return cudaErrorNotSupported;  // d too large for two tiles beside the tokens
   unsigned long long* keys = static_cast<unsigned long long*>(scratch);
@@ -351,9 +386,9 @@ cudaError_t launch_lmhead(const uint16_t* h, int T, int d, int V, const uint8_t*
   if (err != cudaSuccess) return err;
   static int attr1[64] = {}, attr2[64] = {};
   // every launch fits the budget whatever its token count (the ring takes the rest)
-  err = ensure_smem_attr(lmhead_kernel<1>, (size_t)kLmSmemBudget, attr1);
+  err = ensure_smem_attr(lmhead_kernel<1, kFp4>, (size_t)kLmSmemBudget, attr1);
   if (err != cudaSuccess) return err;
-  err = ensure_smem_attr(lmhead_kernel<2>, (size_t)kLmSmemBudget, attr2);
+  err = ensure_smem_attr(lmhead_kernel<2, kFp4>, (size_t)kLmSmemBudget, attr2);
   if (err != cudaSuccess) return err;
   static int sm_count[64] = {};
   int dev = 0;
@@ -375,18 +410,29 @@ cudaError_t launch_lmhead(const uint16_t* h, int T, int d, int V, const uint8_t*
     a.nwarps = ns < kLmConsumers ? ns : kLmConsumers;
     a.nstages = ns / a.nwarps * a.nwarps;
     a.w = w_packed;
+    a.ts = ts;
     a.logits = logits;
     a.keys = keys;
     a.st = st;
     if (nt == 1)
-      lmhead_kernel<1><<<grid, kLmThreads, lm_smem(d, a.ntok), s>>>(a);
+      lmhead_kernel<1, kFp4><<<grid, kLmThreads, lm_smem(d, a.ntok), s>>>(a);
     else
-      lmhead_kernel<2><<<grid, kLmThreads, lm_smem(d, a.ntok), s>>>(a);
+      lmhead_kernel<2, kFp4><<<grid, kLmThreads, lm_smem(d, a.ntok), s>>>(a);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
   argmax_finalize_kernel<<<ceil_div(T, 128), 128, 0, s>>>(keys, T, argmax);
   return cudaGetLastError();
+}
+
+cudaError_t launch_lmhead(const uint16_t* h, int T, int d, int V, const uint8_t* w_packed, float* logits,
+                          int32_t* argmax, void* scratch, DevStatus* st, cudaStream_t s) {
+  return launch_lmhead_fmt<false>(h, T, d, V, w_packed, 1.0f, logits, argmax, scratch, st, s);
+}
+
+cudaError_t launch_lmhead_nvfp4(const uint16_t* h, int T, int d, int V, const uint8_t* w_packed, float ts,
+                                float* logits, int32_t* argmax, void* scratch, DevStatus* st, cudaStream_t s) {
+  return launch_lmhead_fmt<true>(h, T, d, V, w_packed, ts, logits, argmax, scratch, st, s);
 }
 
 }  // namespace bitmoe

@@ -194,6 +194,39 @@ __global__ void pack_int4_kernel(const uint8_t* __restrict__ q, const uint16_t* 
   }
 }
 
+// NVFP4 bank -> packed tiles: the same geometry as the int4 tiles.  A lane's
+// word holds the 8 codes of columns 8c .. 8c+7 of a 32-column group in their
+// canonical byte order (byte j = columns 8c+2j and 8c+2j+1, low nibble first),
+// which is the pair order the hardware E2M1 conversion gives fragment register
+// j; the chunk's scale block is each row's 8 E4M3 bytes.
+__global__ void pack_nvfp4_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ scale, int64_t n_mats,
+                                  int64_t rows, int64_t K, uint8_t* __restrict__ packed) {
+  const int64_t nch = K / kChunkK;
+  const int64_t tiles = n_mats * (rows / kTileRows);
+  const int64_t items = tiles * nch * kTileRows;
+  for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < items;
+       it += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(it % kTileRows);
+    const int64_t ch = (it / kTileRows) % nch;
+    const int64_t tile = it / (kTileRows * nch);
+    const int64_t grow = tile * kTileRows + r;
+    const uint8_t* qrow = q + grow * (K / 2);
+    const uint8_t* srow = scale + grow * (K / kFp4Block);
+    uint8_t* chunk = packed + tile * tile_bytes(K) + ch * kChunkBytes;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t words[4];
+#pragma unroll
+      for (int gg = 0; gg < 4; ++gg)
+        words[gg] = *reinterpret_cast<const uint32_t*>(qrow + ((ch * 4 + gg) * kGroup + c * 8) / 2);
+      *reinterpret_cast<uint4*>(chunk + (r * 4 + c) * 16) = make_uint4(words[0], words[1], words[2], words[3]);
+    }
+    uint8_t* sdst = chunk + kChunkQBytes + r * 8;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) sdst[b] = srow[ch * 8 + b];
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_combine(const float* y_rows, const int32_t* inv, const float* w, const uint16_t* resid, int T,
@@ -234,6 +267,19 @@ cudaError_t launch_pack_int4(const uint8_t* q, const uint16_t* scale, int64_t n_
   if (items == 0) return cudaSuccess;
   const int grid = (int)(ceil_div<int64_t>(items, 256) < 148 * 64 ? ceil_div<int64_t>(items, 256) : 148 * 64);
   pack_int4_kernel<<<grid, 256, 0, s>>>(q, scale, n_mats, rows, K, packed);
+  return cudaGetLastError();
+}
+
+}  // namespace bitmoe
+
+namespace bitmoe {
+
+cudaError_t launch_pack_nvfp4(const uint8_t* q, const uint8_t* scale, int64_t n_mats, int64_t rows, int64_t K,
+                              uint8_t* packed, cudaStream_t s) {
+  const int64_t items = n_mats * (rows / kTileRows) * (K / kChunkK) * kTileRows;
+  if (items == 0) return cudaSuccess;
+  const int grid = (int)(ceil_div<int64_t>(items, 256) < 148 * 64 ? ceil_div<int64_t>(items, 256) : 148 * 64);
+  pack_nvfp4_kernel<<<grid, 256, 0, s>>>(q, scale, n_mats, rows, K, packed);
   return cudaGetLastError();
 }
 

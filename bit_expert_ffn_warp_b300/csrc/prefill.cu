@@ -61,6 +61,8 @@ struct PrefillArgs {
   int FB;              // weight tiles per expert (I/128 for mode 1, d/256 for mode 2)
   const uint8_t* wa;   // packed bank (gate for mode 1, down for mode 2)
   const uint8_t* wb;   // packed bank (up for mode 1)
+  const float* tsa;    // NVFP4 banks: tensor scales per expert of wa and wb (null: int4 banks)
+  const float* tsb;
   int wrows;           // rows per expert in the packed banks (I or d)
   const int32_t* offsets;      // [E+1]
   const int32_t* nb_prefix;    // [E+1] prefix of ceil(n_e / 128)
@@ -208,10 +210,21 @@ __device__ __forceinline__ uint4 dequant_word_f16(uint32_t w, __half2 s2) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// NVFP4: the 8 E2M1 codes of one packed word times their E4M3 block scale
+// (byte sb) as 16 bytes of fp16 -- exact, so nothing is rounded here.
+__device__ __forceinline__ uint4 dequant_word_fp4(uint32_t w, uint32_t sb) {
+  uint32_t o[4];
+  e2m1x8_f16_scaled(w, e4m3_pair_f16(sb), o);
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
+// kFp4: NVFP4 banks (codes times block scale, exact fp16 weights; the tensor
+// scales multiply the accumulators in the epilogue); else int4, RNE(q * s).
+template <bool kFp4>
 __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid_constant__ PrefillArgs p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // the swizzled operand tiles need a 1024-byte aligned base; the dynamic shared memory
@@ -230,7 +243,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
   uint64_t* s_empty = w_full + kPStages;       // [kPStages] MMA commit
   uint64_t* acc_full = s_empty + kPStages;     // [2] MMA commit
   uint64_t* acc_empty = acc_full + 2;          // [2] one arrival per epilogue warp
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint64_t* drain = acc_empty + 2;             // MMA commit: every MMA of this CTA done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr uint32_t kTmemCols = 2 * kPN;  // two 256-column accumulators
@@ -249,6 +263,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], kEpiWarps);
     }
+    mbar_init(drain, 1);
     fence_mbar_init();
   }
   if (warp == kWarpMMA) {
@@ -345,10 +360,18 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
               const int row = 16 * (w + 8 * st) + 8 * u + (lane >> 2);
               const uint32_t wg0 = h ? q[st][u].z : q[st][u].x;  // group 2h
               const uint32_t wg1 = h ? q[st][u].w : q[st][u].y;  // group 2h+1
-              const uint32_t s01 = h ? sc[st][u].y : sc[st][u].x;
-              const __half2 s0 = __half2half2(__ushort_as_half((uint16_t)(s01 & 0xffffu)));
-              const __half2 s1 = __half2half2(__ushort_as_half((uint16_t)(s01 >> 16)));
-              const uint4 d0 = dequant_word_f16(wg0, s0), d1 = dequant_word_f16(wg1, s1);
+              uint4 d0, d1;
+              if constexpr (kFp4) {  // block 2 gg + cq / 2 of the chunk holds this lane's 8 columns
+                const uint32_t ls = fp4_lane_scales(sc[st][u], cq);
+                d0 = dequant_word_fp4(wg0, (ls >> (16 * h)) & 0xffu);
+                d1 = dequant_word_fp4(wg1, (ls >> (16 * h + 8)) & 0xffu);
+              } else {
+                const uint32_t s01 = h ? sc[st][u].y : sc[st][u].x;
+                const __half2 s0 = __half2half2(__ushort_as_half((uint16_t)(s01 & 0xffffu)));
+                const __half2 s1 = __half2half2(__ushort_as_half((uint16_t)(s01 >> 16)));
+                d0 = dequant_word_f16(wg0, s0);
+                d1 = dequant_word_f16(wg1, s1);
+              }
               // a 128-bit store goes out in phases of 8 lanes = rows r, r+1 of the same
               // 4-chunk swizzle group; odd rows store their second chunk first so that each
               // phase covers all 8 chunk positions (no bank conflict)
@@ -448,6 +471,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
         if (!ok) break;
         umma_commit(&acc_full[buf]);
       }
+      // every MMA this thread issued has finished writing TMEM before the CTA
+      // deallocates it, also when a wait ran out above (bounded)
+      umma_commit(drain);
+      mbar_wait(drain, 0, p.st, 71);
       ptrace(p, 0, t_a);
       ptrace(p, 1, t_b);
       ptrace(p, 2, t_acc);
@@ -477,6 +504,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
       const TileInfo ti = tile_info(p, tile);
       const bool valid = n < ti.nval;
       const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kPN);
+      const float ta = kFp4 ? p.tsa[ti.e] : 1.f, tb = (kFp4 && p.mode == 1) ? p.tsb[ti.e] : 1.f;
       if (p.mode == 1) {
         __half* hrow = p.hout + (size_t)(ti.p0 + (valid ? n : 0)) * p.I + ti.f * 128;
         for (int c0 = hf * 64; c0 < hf * 64 + 64; c0 += 16) {
@@ -488,8 +516,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
           uint32_t hv[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            __half2 h2 = __floats2half2_rn(silu_mul(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
-                                           silu_mul(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1])));
+            __half2 h2 = __floats2half2_rn(
+                silu_mul(__uint_as_float(g[2 * i]) * ta, __uint_as_float(u[2 * i]) * tb),
+                silu_mul(__uint_as_float(g[2 * i + 1]) * ta, __uint_as_float(u[2 * i + 1]) * tb));
             hv[i] = *reinterpret_cast<uint32_t*>(&h2);
           }
           *reinterpret_cast<uint4*>(hrow + c0) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
@@ -503,6 +532,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
         for (int c0 = hf * 128; c0 < hf * 128 + 128; c0 += 16) {
           const bool more = c0 + 16 < hf * 128 + 128;
           if (more) tmem_ld16(tq + (uint32_t)(c0 + 16), nxt);
+          if (kFp4) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) cur[i] = __float_as_uint(__uint_as_float(cur[i]) * ta);
+          }
           if (valid) {
             if (p.y16) {
               uint32_t hv[8];
@@ -664,8 +697,12 @@ cudaError_t launch_prefill_ffn(const FfnArgs& a, int32_t* nb_prefix, __half* xs,
   const int gw = (R + 7) / 8;  // blocks of 8 warps
   gather_f16_kernel<<<gw < 148 * 8 ? gw : 148 * 8, 256, 0, s>>>(a.x, a.sorted_rows, R, a.k, a.d, xs);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  static int attr1[64] = {};
-  if ((err = ensure_smem_attr(prefill_gemm_kernel, kPSmem, attr1)) != cudaSuccess) return err;
+  const bool fp4 = a.gate_ts != nullptr;
+  static int attr1[64] = {}, attr_fp4[64] = {};
+  if ((err = fp4 ? ensure_smem_attr(prefill_gemm_kernel<true>, kPSmem, attr_fp4)
+                 : ensure_smem_attr(prefill_gemm_kernel<false>, kPSmem, attr1)) != cudaSuccess)
+    return err;
+  auto kern = fp4 ? prefill_gemm_kernel<true> : prefill_gemm_kernel<false>;
   const int G = sm_count_prefill();
   // upper bound on the 128-row expert blocks, for the grid size
   const long blocks = (long)R / kRowsPerBlock + (R < a.E ? R : a.E) + 1;
@@ -682,6 +719,8 @@ cudaError_t launch_prefill_ffn(const FfnArgs& a, int32_t* nb_prefix, __half* xs,
   p1.FB = a.I / 128;
   p1.wa = a.gate;
   p1.wb = a.up;
+  p1.tsa = a.gate_ts;
+  p1.tsb = a.up_ts;
   p1.wrows = a.I;
   p1.offsets = a.offsets;
   p1.nb_prefix = nb_prefix;
@@ -690,7 +729,7 @@ cudaError_t launch_prefill_ffn(const FfnArgs& a, int32_t* nb_prefix, __half* xs,
   p1.st = a.st;
   p1.trace = tr;
   const long g1 = blocks * p1.FB;
-  prefill_gemm_kernel<<<(int)(g1 < G ? g1 : G), kPThreads, kPSmem, s>>>(p1);
+  kern<<<(int)(g1 < G ? g1 : G), kPThreads, kPSmem, s>>>(p1);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
   p2.mode = 2;
@@ -703,6 +742,8 @@ cudaError_t launch_prefill_ffn(const FfnArgs& a, int32_t* nb_prefix, __half* xs,
   p2.FB = a.d / kPN;
   p2.wa = a.down;
   p2.wb = nullptr;
+  p2.tsa = a.down_ts;
+  p2.tsb = nullptr;
   p2.wrows = a.d;
   p2.offsets = a.offsets;
   p2.nb_prefix = nb_prefix;
@@ -713,7 +754,7 @@ cudaError_t launch_prefill_ffn(const FfnArgs& a, int32_t* nb_prefix, __half* xs,
   p2.st = a.st;
   p2.trace = tr ? tr + (size_t)G * 16 : nullptr;
   const long g2 = blocks * p2.FB;
-  prefill_gemm_kernel<<<(int)(g2 < G ? g2 : G), kPThreads, kPSmem, s>>>(p2);
+  kern<<<(int)(g2 < G ? g2 : G), kPThreads, kPSmem, s>>>(p2);
   return cudaGetLastError();
 }
 

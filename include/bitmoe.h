@@ -60,8 +60,9 @@ typedef enum bitmoe_status {
 } bitmoe_status_t;
 
 /* Shape of one MoE layer.  d: hidden size; E: routed experts; k: routed
- * experts per token; I: expert intermediate size; group: int4 scale group
- * (32); renormalize: 1 = gates are the chosen softmax probabilities rescaled
+ * experts per token; I: expert intermediate size; group: the weights' scale
+ * group (32 for the int4 calls, 16 for the NVFP4 ones); renormalize: 1 = gates
+ * are the chosen softmax probabilities rescaled
  * to sum 1, 0 = the raw probabilities; n_shared: 0, or 1 for a shared expert
  * that every token uses with gate weight 1 besides its k routed ones ("Flint
  * 40B : Best Mid Sized LLM", transcript 02:35: six routed experts of 256 plus
@@ -73,7 +74,7 @@ typedef enum bitmoe_status {
  * n_shared = 1 is a dense SwiGLU layer (the stack's two leading layers in the
  * same transcript): the bank's one entry serves every token with weight 1 and
  * there is no router (w_router may be NULL; E is normally 0).  Supported: d and
- * I multiples of 128, group == 32, 1 <= k <= E or k = 0 with n_shared = 1,
+ * I multiples of 128, group == 32 (int4) or 16 (NVFP4), 1 <= k <= E or k = 0 with n_shared = 1,
  * k + n_shared <= 32, E + n_shared <= 1024.  (n_shared fills what was padding: the struct's size
  * is that of the version without it, where it read as 0 when zero-filled.) */
 typedef struct bitmoe_moe_shape {
@@ -91,6 +92,20 @@ typedef struct bitmoe_moe_weights {
   const float* w_router;
   const float* b_router;
 } bitmoe_moe_weights_t;
+
+/* NVFP4 expert banks (bitmoe_pack_nvfp4 output, 16-byte aligned), their fp32
+ * tensor scales gate_scale / up_scale / down_scale [E + n_shared] (device, one
+ * per bank entry, finite) and the router as in bitmoe_moe_weights_t. */
+typedef struct bitmoe_moe_weights_nvfp4 {
+  const uint8_t* gate;
+  const uint8_t* up;
+  const uint8_t* down;
+  const float* gate_scale;
+  const float* up_scale;
+  const float* down_scale;
+  const float* w_router;
+  const float* b_router;
+} bitmoe_moe_weights_nvfp4_t;
 
 /* ------------------------------------------------------------ utilities */
 
@@ -137,6 +152,37 @@ bitmoe_status_t bitmoe_pack_int4(const uint8_t* q, const uint16_t* scale, int64_
  * Synchronises `stream`.  *status_out receives BITMOE_OK, BITMOE_ERR_TIMEOUT
  * or BITMOE_ERR_DEVICE_CHECK. */
 bitmoe_status_t bitmoe_get_device_status(void* workspace, int clear, int32_t* status_out, void* stream);
+
+/* ------------------------------------------------------------ NVFP4 weights
+ *
+ * The pages name "four-bit NVFP" builds of the model beside the integer-four
+ * ones and an NVFP4 final model ("Flint 40B : Best Mid Sized LLM", transcript
+ * 07:15; "Recursive_SI's First Model Unveiled!", section "Quantization") but do
+ * not define the format; this library takes its public definition:
+ *   W[n,i] = e2m1(q[n,i]) * e4m3(s[n, i/16]) * ts
+ * with q an FP4 E2M1 code (bit 3 sign, 2 exponent bits with bias 1, 1 mantissa
+ * bit: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), s an FP8 E4M3 scale byte for
+ * every 16 consecutive weights of a row (finite; NVFP4 scales are >= 0), and ts
+ * one fp32 tensor scale per matrix.
+ * Canonical NVFP4 layout (input of bitmoe_pack_nvfp4): q [n_mats, rows, K/2]
+ * bytes, element 2b in the low nibble of byte b; s [n_mats, rows, K/16] bytes.
+ * The packed bank has the int4 bank's tile geometry and size (4.5 bits per
+ * weight); tensor scales are passed to the compute calls, not packed.
+ */
+
+/* Bytes of a packed NVFP4 bank (rows % 16 == 0, K % 128 == 0; else 0):
+ * n_mats * rows * K * 9 / 16. */
+size_t bitmoe_packed_nvfp4_bytes(int64_t n_mats, int64_t rows, int64_t K);
+
+/* Reorder a canonical NVFP4 bank (device q, s) into the packed tile layout:
+ * 16-row tiles of 128-column chunks, each chunk the 16 x 128 codes in the
+ * order one mma fragment takes them (a 32-bit word per lane and 32-column
+ * group, byte j holding the two codes of fragment register j) and then the 16
+ * rows' 8 block-scale bytes.  q 4-byte aligned; packed 16-byte aligned, of
+ * bitmoe_packed_nvfp4_bytes().  Off the timed path.
+ * Source: "Flint 40B : Best Mid Sized LLM", transcript 07:15. */
+bitmoe_status_t bitmoe_pack_nvfp4(const uint8_t* q, const uint8_t* scale, int64_t n_mats, int64_t rows, int64_t K,
+                                  uint8_t* packed, void* stream);
 
 /* ------------------------------------------------------------ MoE layer */
 
@@ -239,6 +285,32 @@ bitmoe_status_t moe_forward(const uint16_t* x, const uint16_t* residual, int64_t
                             void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * moe_forward with NVFP4 expert banks (see the NVFP4 section above):
+ * shape->group must be 16 (the NVFP4 block), weights the packed NVFP4 banks
+ * with their per-expert tensor scales; everything else as moe_forward.  Each
+ * code times its E4M3 block scale is an exact fp16 weight, so the projections
+ * keep exact products and fp32 sums; the tensor scale multiplies each
+ * projection's fp32 result.  The kernels are those of moe_forward (fused
+ * decode for T <= 8, streaming, tcgen05 grouped GEMM), each with an NVFP4
+ * dequantisation step.
+ * Source: "Flint 40B : Best Mid Sized LLM", transcript 02:35, 06:43 and 07:15
+ * (the four-bit NVFP builds); "Recursive_SI's First Model Unveiled!", section
+ * "Quantization" (the NVFP4 model).
+ */
+bitmoe_status_t moe_forward_nvfp4(const uint16_t* x, const uint16_t* residual, int64_t T,
+                                  const bitmoe_moe_shape_t* shape, const bitmoe_moe_weights_nvfp4_t* weights,
+                                  const int32_t* forced_ids, const float* forced_w, int32_t* topk_ids_out,
+                                  float* topk_w_out, uint16_t* out, float* out_f32, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/* moe_expert_ffn_int4 over NVFP4 banks (shape->group == 16).  Source as
+ * moe_forward_nvfp4. */
+bitmoe_status_t moe_expert_ffn_nvfp4(const uint16_t* x, int64_t T, const bitmoe_moe_shape_t* shape,
+                                     const bitmoe_moe_weights_nvfp4_t* weights, const int32_t* expert_offsets,
+                                     const int32_t* sorted_rows, float* y_rows, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
+/*
  * One pre-norm layer step of a decode stack: xh = RMSNorm(residual) with unit
  * gain (y = x / sqrt(mean(x^2) + eps), fp32, rounded to bf16), then
  * out = residual + MoE(xh), as moe_forward(xh, residual, ...) computes it.
@@ -307,7 +379,22 @@ bitmoe_status_t lmhead_int4_gemv(const uint16_t* h, int64_t T, int64_t d, int64_
                                  size_t workspace_bytes, void* stream);
 
 /*
- * lmhead_int4_gemv_static: the LM head above without a workspace argument.
+ * The LM head over an NVFP4 matrix: logits[t,v] = sum_i Wlm[v,i] h[t,i] with
+ * Wlm = e2m1(q) * e4m3(s) * tensor_scale (see the NVFP4 section above), fp32
+ * sums, argmax as lmhead_int4_gemv.  w_packed is bitmoe_pack_nvfp4's [V, d]
+ * bank; tensor_scale must be finite.  Shapes, workspace and errors as
+ * lmhead_int4_gemv.  Each code times its block scale is an exact fp16 value,
+ * so the products with the (exactly scaled) fp16 tokens are exact.
+ * Source: "Flint 40B : Best Mid Sized LLM", transcript 03:36, 05:39 (the 4-bit
+ * output layer) and 07:15 (the NVFP4 builds); "Recursive_SI's First Model
+ * Unveiled!", section "Quantization".
+ */
+bitmoe_status_t lmhead_nvfp4_gemv(const uint16_t* h, int64_t T, int64_t d, int64_t V, const uint8_t* w_packed,
+                                  float tensor_scale, float* logits, int32_t* argmax, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/*
+ * lmhead_int4_gemv_static: the int4 LM head (lmhead_int4_gemv) without a workspace argument.
  * For callers that cannot allocate device memory: code embedded in another
  * runtime that owns all device memory through its own pool and hands this
  * library only the pointers of its inputs and outputs, or a per-token loop

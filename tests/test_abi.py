@@ -98,6 +98,33 @@ def test_host_side_validation_without_gpu(built):
         assert lib.bitmoe_status_string(code)
 
 
+def test_nvfp4_host_side_validation_without_gpu(built):
+    import bit_expert_ffn_warp_b300 as bm
+    lib = bm._lib
+    assert lib.bitmoe_packed_nvfp4_bytes(256, 512, 2048) == 256 * 512 * 2048 * 9 // 16
+    assert lib.bitmoe_packed_nvfp4_bytes(1, 15, 2048) == 0 and lib.bitmoe_packed_nvfp4_bytes(1, 16, 2000) == 0
+    assert lib.bitmoe_pack_nvfp4(None, None, 1, 16, 128, None, None) == 1
+    sh16 = bm.MoeShape(2048, 256, 8, 512, 16, 1)  # the NVFP4 block as the scale group
+    sh32 = bm.MoeShape(2048, 256, 8, 512, 32, 1)
+    assert lib.moe_workspace_size(ctypes.byref(sh16), 8) == lib.moe_workspace_size(ctypes.byref(sh32), 8)
+    w4 = bm.MoeWeightsNvfp4(None, None, None, None, None, None, None, None)
+    wi = bm.MoeWeights(None, None, None, None, None)
+    args = (None, None, None, None, None, None, None, 0, None)
+    # each format's calls take only their own scale group
+    assert lib.moe_forward_nvfp4(None, None, 1, ctypes.byref(sh32), ctypes.byref(w4), *args) == 2
+    assert lib.moe_forward(None, None, 1, ctypes.byref(sh16), ctypes.byref(wi), *args) == 2
+    assert lib.moe_forward_nvfp4(None, None, 1, ctypes.byref(sh16), ctypes.byref(w4), *args) == 1
+    assert lib.moe_expert_ffn_nvfp4(None, 1, ctypes.byref(sh16), ctypes.byref(w4), None, None, None, None, 0,
+                                    None) == 1
+    assert lib.moe_expert_ffn_int4(None, 1, ctypes.byref(sh16), ctypes.byref(wi), None, None, None, None, 0,
+                                   None) == 2
+    assert lib.moe_forward_nvfp4(None, None, 0, ctypes.byref(sh16), ctypes.byref(w4), *args) == 0
+    # the NVFP4 LM head: T and shape limits as the int4 one, a finite tensor scale
+    assert lib.lmhead_nvfp4_gemv(None, 65, 2048, 131072, None, 1.0, None, None, None, 0, None) == 2
+    assert lib.lmhead_nvfp4_gemv(None, 1, 2048, 131072, None, float("nan"), None, None, None, 0, None) == 1
+    assert lib.lmhead_nvfp4_gemv(None, 0, 2048, 131072, None, 1.0, None, None, None, 0, None) == 0
+
+
 def test_stack_call_rejects_on_the_host_without_gpu(built):
     """moe_stack_decode: argument and shape checks that return before any launch."""
     import bit_expert_ffn_warp_b300 as bm
