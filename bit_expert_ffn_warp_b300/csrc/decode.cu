@@ -1200,7 +1200,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& p, const LayerPtrs
           const uint4 q1 = *reinterpret_cast<const uint4*>(cw + ((g + 8) * 4 + c) * 16);
           const uint2 s0 = *reinterpret_cast<const uint2*>(cw + kChunkQBytes + g * 8);
           const uint2 s1 = *reinterpret_cast<const uint2*>(cw + kChunkQBytes + (g + 8) * 8);
-#pragma unroll
+#pragma unroll 2  // (full unrolling spills at the 96-register cap)
           for (int gg = 0; gg < 4; ++gg) {
             const int col = (ch * 4 + gg) * kGroup + c * 8;
             uint4 bh = make_uint4(0, 0, 0, 0), bl = make_uint4(0, 0, 0, 0);
