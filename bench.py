@@ -59,6 +59,7 @@ DEFAULT_WARMUP = {"decode": 200, "shared": 200, "batch": 50, "prefill": 5, "stac
 
 
 def parse():
+    global MIN_TIMED_S
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=None, help="steps in one timed region (per-workload default)")
@@ -73,6 +74,8 @@ def parse():
     p.add_argument("--copies", type=int, default=64, help="independent layer copies cycled per step")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
+    p.add_argument("--min-timed-s", type=float, default=MIN_TIMED_S,
+                   help="GPU time the repeated timed region adds up to, at least (short profiling runs)")
     a = p.parse_args()
     if a.steps is None:
         a.steps = DEFAULT_STEPS[a.workload]
@@ -80,6 +83,7 @@ def parse():
         a.warmup = DEFAULT_WARMUP[a.workload]
     a.steps = max(1, a.steps)
     a.warmup = max(3, a.warmup)
+    MIN_TIMED_S = max(0.0, a.min_timed_s)
     if a.format == "nvfp4" and a.workload in ("stack", "shared"):
         p.error("--format nvfp4 covers the decode, batch, prefill and lmhead workloads")
     return a
@@ -269,12 +273,14 @@ def run_warmup(step, W):
     torch.cuda.synchronize()
 
 
-def time_regions(graphs, world, min_total_s=MIN_TIMED_S, min_regions=5, max_regions=20000):
+def time_regions(graphs, world, min_total_s=None, min_regions=5, max_regions=20000):
     """Replays the K-step region graphs (cycling through them) back to back, each
     replay between two CUDA events on the current stream, until at least
     min_total_s of GPU time is timed.  Barrier + synchronize on both sides.
     Returns the per-region times (ms)."""
     import torch
+    if min_total_s is None:
+        min_total_s = MIN_TIMED_S
     stream = torch.cuda.current_stream()
     torch.cuda.synchronize()
     barrier(world)
