@@ -578,6 +578,422 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
   }
 }
 
+// ---------------------------------------------------------------- weights in tensor memory
+//
+// The grouped GEMM with the roles of the operands swapped: the MMA's A side (M = 128)
+// is 128 weight rows held in tensor memory, its B side (N = the routed rows of one
+// 128-row expert block, rounded up to 16) the activation rows in shared memory, so
+// that the dequantised weights never pass through shared memory (they go from the
+// dequantising warps' registers to tensor memory with tcgen05.st) and an expert block
+// with few rows costs an MMA of that width.  Each B stage feeds two M tiles (GEMM 1:
+// 128 gate rows and the same 128 up rows; GEMM 2: 256 rows of W_down), two
+// accumulators D0, D1 of N columns.  Per 64-column k-block the CTA's shared memory
+// sees the 16 KB B stage written by TMA and read twice by the MMAs, against 512 MMA
+// cycles at N = 128.
+//
+// K order.  The dequantising warps read the packed tiles in the mma-fragment order
+// (lane (g, c) holds rows g and g+8, columns 8c .. 8c+7 of every 32-column group) and
+// store them with tcgen05.st.16x256b, whose thread t writes lanes t/4 and t/4 + 8,
+// columns 2(t%4) and 2(t%4)+1 of each 8-column block.  So column p of a 16-column
+// group (one 32-element K group, two K elements per column) holds the K pair
+// P(p) = 4 ((p % 8) / 2) + p % 2 + 2 (p / 8); the B rows are stored with the same
+// permutation inside every 32-element group (the gathered activations, and the h rows
+// GEMM 1 writes for GEMM 2), so every product pairs the right elements.
+// Warps: 1 B rows, 2 MMA issuer + TMEM owner (on the third SM sub-partition, which the
+// other roles load least), 4-11 dequantisation, 12-15 epilogue.
+constexpr int kQThreads = 16 * 32;
+constexpr int kQWarpMMA = 2, kQWarpB = 1, kQWarpDq0 = 4, kQWarpEpi0 = 12;
+constexpr int kQBStages = 4;                      // B ring (128 rows x 64 K fp16 = 16 KB each)
+constexpr int kQAStages = kQBStages;              // A ring in tensor memory (2 tiles x 32 columns each):
+                                                  // the same depth, so one MMA commit frees both
+constexpr int kQBBytes = kPM * kPK * 2;
+constexpr uint32_t kQTmemCols = 512;              // D0, D1 (128 columns each), then the A ring
+constexpr int kQEpiBytes = 16 * 32 * 4;          // per epilogue warp: 16 routed rows x 32 values (fp32 at most)
+constexpr int kQTileCache = 128;                  // tiles of a CTA whose TileInfo is computed once, up front
+constexpr size_t kQSmem =
+    (size_t)kQBStages * kQBBytes + 4 * kQEpiBytes + (size_t)kQTileCache * sizeof(TileInfo) + 1024 + 256;
+static_assert(kQSmem <= 227 * 1024, "shared memory budget");
+static_assert(256 + kQAStages * 2 * 32 <= (int)kQTmemCols, "tensor memory budget");
+
+// Position of K pair P (0..15) inside its 32-element group (inverse of P(p) above).
+__host__ __device__ constexpr int kpair_pos(int P) { return 2 * (P >> 2) + (P & 1) + 8 * ((P >> 1) & 1); }
+// Column of element f of a row stored in that order.
+__host__ __device__ constexpr int kperm(int f) { return (f & ~31) + 2 * kpair_pos((f & 31) >> 1) + (f & 1); }
+
+__device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                            uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16x256b_x4(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t word_at(const uint4& q, int gg) {
+  return gg == 0 ? q.x : gg == 1 ? q.y : gg == 2 ? q.z : q.w;
+}
+
+// The eight weights of one packed word as fp16 pairs o[j] = columns 2j, 2j+1 of the lane's octet:
+// int4: RNE(q * s) with the group's fp16 scale; NVFP4: code times block scale, exact.
+template <bool kFp4>
+__device__ __forceinline__ void dq_word(uint32_t w, uint32_t scale_bits, uint32_t (&o)[4]) {
+  if constexpr (kFp4) {
+    e2m1x8_f16_scaled(w, e4m3_pair_f16(scale_bits), o);
+  } else {
+    uint32_t q[4];
+    nib_pairs4_f16(w, q);
+    const __half2 s2 = __half2half2(__ushort_as_half((uint16_t)scale_bits));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&q[j]), s2);
+      o[j] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+  }
+}
+
+template <bool kFp4>
+__global__ void __launch_bounds__(kQThreads, 1) prefill_wa_kernel(const __grid_constant__ PrefillArgs p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  if ((smem_u32(smem_raw) & 1023u) != 0) {  // the swizzled B tiles need a 1024-byte aligned base
+    if (threadIdx.x == 0) record_status(p.st, kStatusCheck, 80, (int)(smem_u32(smem_raw) & 1023u));
+    return;
+  }
+  unsigned char* bst = smem_raw;  // [kQBStages] B stages
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + (size_t)kQBStages * kQBBytes);
+  // stage s is full once its B rows have landed (TMA transaction count, armed by the B
+  // loader's arrival) and the eight dequantising warps have stored its A (eight more
+  // arrivals): one barrier, so the MMA thread waits once per stage
+  uint64_t* b_full = bars;                     // [kQBStages] 1 + 8 arrivals + B bytes
+  uint64_t* b_empty = b_full + kQBStages;      // [kQBStages] MMA commit: B and A stage s free again
+  uint64_t* a_full = b_full;                   // (the same barriers)
+  uint64_t* a_empty = b_empty;
+  uint64_t* d_full = b_empty + kQBStages;      // MMA commit: the tile's accumulators are complete
+  uint64_t* d_empty = d_full + 1;              // one arrival per epilogue warp
+  uint64_t* drain = d_empty + 1;               // MMA commit: every MMA of this CTA done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  unsigned char* epi_tile = smem_raw + (size_t)kQBStages * kQBBytes + 1024;  // [4 warps][kQEpiBytes]
+  TileInfo* tcache = reinterpret_cast<TileInfo*>(epi_tile + 4 * kQEpiBytes);  // [kQTileCache]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < kQBStages; ++s) {
+      mbar_init(&b_full[s], 1 + 8);
+      mbar_init(&b_empty[s], 1);
+    }
+    mbar_init(d_full, 1);
+    mbar_init(d_empty, 4);
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == kQWarpMMA) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kQTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  const int n_tiles = p.nb_prefix[p.E] * p.FB;
+  // every role walks the same tiles: their (expert, block, rows) are looked up once here,
+  // in parallel, instead of by each role's single thread on its critical path
+  for (int j = tid; j < kQTileCache; j += kQThreads) {
+    const int tile = snake_tile(j);
+    if (tile < n_tiles) tcache[j] = tile_info(p, tile);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  auto a_col = [](int s, int t) { return (uint32_t)(256 + (s * 2 + t) * 32); };
+  auto tinfo = [&](int j, int tile) { return j < kQTileCache ? tcache[j] : tile_info(p, tile); };
+
+  const int nchunks = p.Kdim / kChunkK;
+  const int nkb = 2 * nchunks;  // 64-K stages per tile
+
+  if (warp == kQWarpB) {
+    // ---------------- B: the tile's routed rows, 64-row TMA boxes of 64 K (two per full block)
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_a)) : "memory");
+      int it = 0;
+      bool ok = true;
+      // the dequantising warps read the packed weights straight from global memory, a
+      // chunk ahead: pull each tile's weights into L2 one tile earlier, so that those
+      // loads meet L2 rather than HBM
+      auto prefetch_tile = [&](int jn, int tile) {
+        if (tile >= n_tiles) return;
+        const TileInfo tn = tinfo(jn, tile);
+        for (int i = 0; i < kSubTiles; ++i)
+          bulk_prefetch_l2(subtile_base(p, tn, i), (uint32_t)tile_bytes(p.Kdim));
+      };
+      prefetch_tile(0, snake_tile(0));
+      for (int j = 0, tile = snake_tile(0); tile < n_tiles && ok; tile = snake_tile(++j)) {
+        const TileInfo ti = tinfo(j, tile);
+        prefetch_tile(j + 1, snake_tile(j + 1));
+        const int nbox = (ti.nval + kBoxRows - 1) / kBoxRows;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % kQBStages;
+          if (it >= kQBStages && !mbar_wait(&b_empty[s], ((it / kQBStages) - 1) & 1, p.st, 81)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&b_full[s], (uint32_t)nbox * kBoxRows * kPK * 2);
+          const uint32_t dst = smem_u32(bst + (size_t)s * kQBBytes);
+          for (int i = 0; i < nbox; ++i)
+            asm volatile(
+                "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+                    dst + (uint32_t)(i * kBoxRows * kPK * 2)),
+                "l"(reinterpret_cast<uint64_t>(&p.tmap_a)), "r"(kb * kPK), "r"(ti.p0 + i * kBoxRows),
+                "r"(smem_u32(&b_full[s]))
+                : "memory");
+        }
+      }
+      for (int n = (it > kQBStages ? it - kQBStages : 0); n < it; ++n)
+        mbar_wait(&b_full[n % kQBStages], (n / kQBStages) & 1, p.st, 82);
+    }
+  } else if (warp >= kQWarpDq0 && warp < kQWarpDq0 + 8) {
+    // ---------------- dequantisation: warp (t, q) writes rows 32q .. 32q+31 of M tile t, that is
+    // packed sub-tiles 8t + 2q and 8t + 2q + 1, into its own TMEM lane quarter q; the packed words
+    // come straight from global memory (L2), a chunk ahead of their use
+    const int q = warp & 3, t = (warp - kQWarpDq0) >> 2;
+    const int g = lane >> 2, cl = lane & 3;
+    uint4 w0[2], w1[2], n0[2], n1[2];  // rows g, g+8 of sub-tiles k = 0, 1: this chunk and the next
+    uint2 s0[2], s1[2], m0[2], m1[2];
+    TileInfo ti{};
+    const uint8_t* sb[2] = {nullptr, nullptr};
+    // the flat sequence of (tile, chunk) this CTA works through
+    int jn = 0, cn = 0, tile_n = snake_tile(0);
+    auto load = [&](int tile, int c, uint4 (&a0)[2], uint4 (&a1)[2], uint2 (&z0)[2], uint2 (&z1)[2]) {
+      if (c == 0) {
+        ti = tinfo(jn, tile);
+        sb[0] = subtile_base(p, ti, 8 * t + 2 * q);
+        sb[1] = subtile_base(p, ti, 8 * t + 2 * q + 1);
+      }
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const uint8_t* cw = sb[k] + (size_t)c * kChunkBytes;
+        a0[k] = __ldg(reinterpret_cast<const uint4*>(cw + (g * 4 + cl) * 16));
+        a1[k] = __ldg(reinterpret_cast<const uint4*>(cw + ((g + 8) * 4 + cl) * 16));
+        z0[k] = __ldg(reinterpret_cast<const uint2*>(cw + kChunkQBytes + g * 8));
+        z1[k] = __ldg(reinterpret_cast<const uint2*>(cw + kChunkQBytes + (g + 8) * 8));
+      }
+    };
+    if (tile_n < n_tiles) load(tile_n, 0, n0, n1, m0, m1);
+    int it = 0;
+    bool ok = true;
+    long long t_wait = 0;
+    const long long t_start = clock64();
+    while (tile_n < n_tiles && ok) {
+      const int c = cn;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        w0[k] = n0[k];
+        w1[k] = n1[k];
+        s0[k] = m0[k];
+        s1[k] = m1[k];
+      }
+      // advance to the next (tile, chunk) and request it now
+      if (++cn == nchunks) {
+        cn = 0;
+        tile_n = snake_tile(++jn);
+      }
+      if (tile_n < n_tiles) load(tile_n, cn, n0, n1, m0, m1);
+#pragma unroll
+      for (int h = 0; h < 2; ++h, ++it) {  // the chunk's two 64-K stages
+        const int s = it % kQAStages;
+        const long long tw = clock64();
+        if (it >= kQAStages && !mbar_wait(&a_empty[s], ((it / kQAStages) - 1) & 1, p.st, 83)) {
+          ok = false;
+          break;
+        }
+        t_wait += clock64() - tw;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          uint32_t r[16];
+#pragma unroll
+          for (int gl = 0; gl < 2; ++gl) {
+            const int gg = 2 * h + gl;
+            uint32_t sc0, sc1;
+            if constexpr (kFp4) {
+              sc0 = (fp4_lane_scales(s0[k], cl) >> (8 * gg)) & 0xffu;
+              sc1 = (fp4_lane_scales(s1[k], cl) >> (8 * gg)) & 0xffu;
+            } else {
+              sc0 = ((gg < 2 ? s0[k].x : s0[k].y) >> (16 * (gg & 1))) & 0xffffu;
+              sc1 = ((gg < 2 ? s1[k].x : s1[k].y) >> (16 * (gg & 1))) & 0xffffu;
+            }
+            uint32_t o0[4], o1[4];
+            dq_word<kFp4>(word_at(w0[k], gg), sc0, o0);
+            dq_word<kFp4>(word_at(w1[k], gg), sc1, o1);
+#pragma unroll
+            for (int jh = 0; jh < 2; ++jh) {
+              const int i = 2 * gl + jh;  // repetition: columns 8i .. 8i+7 of the stage
+              r[4 * i + 0] = o0[2 * jh];
+              r[4 * i + 1] = o0[2 * jh + 1];
+              r[4 * i + 2] = o1[2 * jh];
+              r[4 * i + 3] = o1[2 * jh + 1];
+            }
+          }
+          tmem_st16x256b_x4(tmem_base + ((uint32_t)(32 * q + 16 * k) << 16) + a_col(s, t), r);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cta(&a_full[s]);
+      }
+      (void)c;
+    }
+    if (warp == kQWarpDq0 && lane == 0) {
+      ptrace(p, 6, t_wait);
+      ptrace(p, 7, clock64() - t_start);
+    }
+  } else if (warp == kQWarpMMA) {
+    // ---------------- MMA issuer (one thread): D_t += A_t (TMEM) x B (shared memory)
+    if (lane == 0) {
+      int it = 0, lt = 0;
+      bool ok = true;
+      long long t_d = 0;
+      const long long t_start = clock64();
+      const uint64_t bdesc0 = umma_smem_desc(smem_u32(bst));
+      for (int j = 0, tile = snake_tile(0); tile < n_tiles && ok; tile = snake_tile(++j), ++lt) {
+        const TileInfo ti = tinfo(j, tile);
+        const int N = (ti.nval + 15) & ~15;
+        const uint32_t idesc = umma_idesc_f16(kPM, N);
+        const long long w0 = clock64();
+        if (lt >= 1 && !mbar_wait(d_empty, (lt - 1) & 1, p.st, 84)) break;
+        t_d += clock64() - w0;
+        tc_fence_after();
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int sbq = it % kQBStages, saq = sbq;
+          if (!mbar_wait(&b_full[sbq], (it / kQBStages) & 1, p.st, 85)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // stage sbq's descriptor is the first stage's plus its offset in 16-byte units; a 16-K
+          // step is 32 bytes further, +2 in the address field
+          const uint64_t bdesc = bdesc0 + (uint64_t)(sbq * (kQBBytes >> 4));
+          const uint32_t acol0 = tmem_base + a_col(saq, 0), acol1 = tmem_base + a_col(saq, 1);
+#pragma unroll
+          for (int ks = 0; ks < kPK / 16; ++ks) {
+            const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
+            umma_f16_ta(tmem_base, acol0 + (uint32_t)(8 * ks), bdesc + (uint64_t)(2 * ks), idesc, acc);
+            umma_f16_ta(tmem_base + 128u, acol1 + (uint32_t)(8 * ks), bdesc + (uint64_t)(2 * ks), idesc, acc);
+          }
+          umma_commit(&b_empty[sbq]);  // B and A stages are free once these MMAs have read them
+        }
+        if (!ok) break;
+        umma_commit(d_full);
+      }
+      umma_commit(drain);  // every MMA issued has finished before TMEM is released
+      mbar_wait(drain, 0, p.st, 87);
+      ptrace(p, 2, t_d);
+      ptrace(p, 3, clock64() - t_start);
+      ptrace(p, 11, lt);
+    }
+  } else if (warp >= kQWarpEpi0) {
+    // ---------------- epilogue: thread = one TMEM lane = weight row 32q + lane of both M tiles;
+    // columns = the tile's routed rows
+    const int q = warp & 3, row = 32 * q + lane;
+    int lt = 0;
+    bool dead = false;
+    long long t_wait = 0;
+    const long long t_start = clock64();
+    for (int j = 0, tile = snake_tile(0); tile < n_tiles; tile = snake_tile(++j), ++lt) {
+      const long long w0 = clock64();
+      const bool got = !dead && __all_sync(0xffffffffu, mbar_wait(d_full, lt & 1, p.st, 88));
+      t_wait += clock64() - w0;
+      dead = !got;
+      if (dead) break;
+      tc_fence_after();
+      const TileInfo ti = tinfo(j, tile);
+      const float ta = kFp4 ? p.tsa[ti.e] : 1.f, tb = (kFp4 && p.mode == 1) ? p.tsb[ti.e] : 1.f;
+      const uint32_t tq = tmem_base + ((uint32_t)(32 * q) << 16);
+      // A thread holds one weight row of 16 routed rows per step; the warp turns its
+      // 32 x 16 block around in shared memory so that each routed row's 32 values go
+      // out as 16-byte stores.
+      unsigned char* tile_s = epi_tile + (size_t)(warp - kQWarpEpi0) * kQEpiBytes;
+      for (int n0 = 0; n0 < ti.nval; n0 += 16) {
+        uint32_t d0[16], d1[16];
+        tmem_ld16(tq + (uint32_t)n0, d0);
+        tmem_ld16(tq + (uint32_t)(128 + n0), d1);
+        tmem_ld_wait();
+        const int nr = ti.nval - n0 < 16 ? ti.nval - n0 : 16;  // routed rows in this step
+        if (p.mode == 1) {  // h = silu(gate) * up of feature f, in the K order GEMM 2 reads
+          __half* ts = reinterpret_cast<__half*>(tile_s);
+          const int pos = kperm(row) - 32 * q;  // column of this feature inside its 32-group
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            ts[i * 32 + pos] = __float2half_rn(silu_mul_fast(__uint_as_float(d0[i]) * ta, __uint_as_float(d1[i]) * tb));
+          __syncwarp();
+          const int f0 = ti.f * 128 + 32 * q;
+#pragma unroll
+          for (int v = lane; v < 64; v += 32) {  // 16 rows x 4 chunks of 16 bytes
+            const int r = v >> 2, c16 = v & 3;
+            if (r < nr)
+              *reinterpret_cast<uint4*>(p.hout + (size_t)(ti.p0 + n0 + r) * p.I + f0 + 8 * c16) =
+                  *reinterpret_cast<const uint4*>(ts + r * 32 + 8 * c16);
+          }
+          __syncwarp();
+        } else {  // y rows: W_down rows f*256 + 32q + lane (tile 0) and + 128 (tile 1)
+#pragma unroll
+          for (int t2 = 0; t2 < 2; ++t2) {
+            const uint32_t(&dd)[16] = t2 ? d1 : d0;
+            const int c0 = ti.f * kPN + 128 * t2 + 32 * q;
+            if (p.y16) {
+              __half* ts = reinterpret_cast<__half*>(tile_s);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) ts[i * 32 + lane] = __float2half_rn(__uint_as_float(dd[i]) * ta);
+              __syncwarp();
+#pragma unroll
+              for (int v = lane; v < 64; v += 32) {
+                const int r = v >> 2, c16 = v & 3;
+                if (r < nr)
+                  *reinterpret_cast<uint4*>(p.y16 + (size_t)(ti.p0 + n0 + r) * p.d + c0 + 8 * c16) =
+                      *reinterpret_cast<const uint4*>(ts + r * 32 + 8 * c16);
+              }
+            } else {
+              float* ts = reinterpret_cast<float*>(tile_s);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) ts[i * 32 + lane] = __uint_as_float(dd[i]) * ta;
+              __syncwarp();
+#pragma unroll
+              for (int v = lane; v < 128; v += 32) {  // 16 rows x 8 chunks of 16 bytes
+                const int r = v >> 3, c16 = v & 7;
+                if (r < nr)
+                  *reinterpret_cast<uint4*>(p.yout + (size_t)(ti.p0 + n0 + r) * p.d + c0 + 4 * c16) =
+                      *reinterpret_cast<const uint4*>(ts + r * 32 + 4 * c16);
+              }
+            }
+            __syncwarp();
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cta(d_empty);
+    }
+    if (warp == kQWarpEpi0 && lane == 0) {
+      ptrace(p, 9, t_wait);
+      ptrace(p, 10, clock64() - t_start);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kQWarpMMA) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kQTmemCols) : "memory");
+  }
+}
+
 // pre[e] = sum over e' < e of ceil(n_e' / 128) (pre[E] = the number of 128-row expert
 // blocks), and list = those blocks ordered by width, widest first.  One CTA of 1024
 // threads, one expert per thread (E <= 1024).
@@ -644,6 +1060,32 @@ __global__ void gather_f16_kernel(const uint16_t* __restrict__ x, const int32_t*
   }
 }
 
+// The same gather with every 32-element group of a row in the K order of the weights
+// in tensor memory (kperm): the octet 8c .. 8c+7 of a group lands as two runs of four,
+// at 4c and at 4c + 16.
+__global__ void gather_f16_perm_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_rows,
+                                       int R, int k, int d, __half* __restrict__ xs) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int pos = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; pos < R; pos += warps) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(sorted_rows[pos] / k) * d);
+    uint2* dst = reinterpret_cast<uint2*>(xs + (size_t)pos * d);  // 4 fp16 per uint2
+    for (int i = lane; i < d / 8; i += 32) {
+      const uint4 v = src[i];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        __half2 h2 = __floats2half2_rn(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xffff0000u));
+        o[q] = *reinterpret_cast<uint32_t*>(&h2);
+      }
+      const int grp = i >> 2, c = i & 3;  // 32-element group, octet inside it
+      dst[grp * 8 + c] = make_uint2(o[0], o[1]);
+      dst[grp * 8 + c + 4] = make_uint2(o[2], o[3]);
+    }
+  }
+}
+
 // Tensor map of a row-major [rows, K] fp16 matrix for 64 x 16 boxes with 128-byte swizzle.
 cudaError_t encode_rows_map(CUtensorMap* map, const void* base, int rows, int K) {
   using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -695,14 +1137,14 @@ cudaError_t launch_prefill_ffn(const FfnArgs& a, int32_t* nb_prefix, __half* xs,
   int32_t* pair_list = nb_prefix + a.E + 1;  // [R/128 + E] entries after the prefix
   block_list_kernel<<<1, 1024, 0, s>>>(a.offsets, a.E, nb_prefix, pair_list);
   const int gw = (R + 7) / 8;  // blocks of 8 warps
-  gather_f16_kernel<<<gw < 148 * 8 ? gw : 148 * 8, 256, 0, s>>>(a.x, a.sorted_rows, R, a.k, a.d, xs);
+  gather_f16_perm_kernel<<<gw < 148 * 8 ? gw : 148 * 8, 256, 0, s>>>(a.x, a.sorted_rows, R, a.k, a.d, xs);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   const bool fp4 = a.gate_ts != nullptr;
   static int attr1[64] = {}, attr_fp4[64] = {};
-  if ((err = fp4 ? ensure_smem_attr(prefill_gemm_kernel<true>, kPSmem, attr_fp4)
-                 : ensure_smem_attr(prefill_gemm_kernel<false>, kPSmem, attr1)) != cudaSuccess)
+  if ((err = fp4 ? ensure_smem_attr(prefill_wa_kernel<true>, kQSmem, attr_fp4)
+                 : ensure_smem_attr(prefill_wa_kernel<false>, kQSmem, attr1)) != cudaSuccess)
     return err;
-  auto kern = fp4 ? prefill_gemm_kernel<true> : prefill_gemm_kernel<false>;
+  auto kern = fp4 ? prefill_wa_kernel<true> : prefill_wa_kernel<false>;
   const int G = sm_count_prefill();
   // upper bound on the 128-row expert blocks, for the grid size
   const long blocks = (long)R / kRowsPerBlock + (R < a.E ? R : a.E) + 1;
@@ -729,7 +1171,7 @@ cudaError_t launch_prefill_ffn(const FfnArgs& a, int32_t* nb_prefix, __half* xs,
   p1.st = a.st;
   p1.trace = tr;
   const long g1 = blocks * p1.FB;
-  kern<<<(int)(g1 < G ? g1 : G), kPThreads, kPSmem, s>>>(p1);
+  kern<<<(int)(g1 < G ? g1 : G), kQThreads, kQSmem, s>>>(p1);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
   p2.mode = 2;
@@ -754,7 +1196,7 @@ cudaError_t launch_prefill_ffn(const FfnArgs& a, int32_t* nb_prefix, __half* xs,
   p2.st = a.st;
   p2.trace = tr ? tr + (size_t)G * 16 : nullptr;
   const long g2 = blocks * p2.FB;
-  kern<<<(int)(g2 < G ? g2 : G), kPThreads, kPSmem, s>>>(p2);
+  kern<<<(int)(g2 < G ? g2 : G), kQThreads, kQSmem, s>>>(p2);
   return cudaGetLastError();
 }
 
