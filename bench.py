@@ -101,7 +101,7 @@ def fmt_suffix(fmt):
 # those sources still matches the one written beside it.
 KERNEL_SOURCES = {
     "decode_layer_kernel": ["decode.cu", "common.cuh"],
-    "prefill_gemm_kernel": ["prefill.cu", "common.cuh"],
+    "prefill_wa_kernel": ["prefill.cu", "common.cuh"],
     "lmhead_kernel": ["lmhead.cu", "common.cuh"],
 }
 
@@ -679,7 +679,7 @@ def bench_prefill(args, world, rank):
         "timing": timing_record(times, K, f"CUDA graph of {K} moe_forward steps"),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16_peak, "unit": "TFLOP/s",
                      "frac": round(achieved / bf16_peak, 4),
-                     "traffic": profiled_traffic("prefill_gemm_kernel",
+                     "traffic": profiled_traffic("prefill_wa_kernel",
                                                  workload=f"moe_layer_prefill_T{T}" + fmt_suffix(args.format)),
                      "kernel": "expert FFN grouped GEMMs (gate/up+SwiGLU, down)",
                      "flops_per_launch": flops, "ms_per_launch": gemm_ms,

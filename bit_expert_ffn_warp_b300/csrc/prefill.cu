@@ -7,28 +7,31 @@
 //   GEMM1  h = silu(Wg x) * (Wu x)   per routed row, fp16 h
 //   GEMM2  y = Wd h                  per routed row (fp16 inside the layer, fp32 standalone)
 //
-// Orientation: D[m, n] = sum_k X[m, k] * W[n, k] -- the MMA's M side is 128
-// routed rows of one expert (a 128-row block of its grouped rows), its N side
-// 256 weight rows.  For GEMM1 the 256 weight rows are 128 gate rows over the
-// same 128 up rows, so a thread of the epilogue holds gate and up of the same
-// features for its routed row and writes h directly; for GEMM2 they are 256
-// rows of W_down, so a thread writes 256 consecutive y values of its row.
-// K advances in stages of 64.  Operands live in 128-byte-swizzled K-major
-// shared memory:
-//   A  fp16 routed rows, contiguous in grouped order (GEMM1: the activations
+// Orientation: D[m, n] = sum_k W[m, k] * X[n, k].  The MMA's A side (M = 128) is 128
+// weight rows held in tensor memory, its B side (N = the routed rows of one 128-row
+// expert block, rounded up to 16) the fp16 activation rows in 128-byte-swizzled
+// K-major shared memory.  A tile is one expert block times 256 weight rows, two M
+// tiles into two accumulators D0, D1 of N columns: for GEMM1 128 gate rows and the
+// same 128 up rows, so a thread of the epilogue holds gate and up of one feature for
+// every routed row and writes h directly; for GEMM2 256 rows of W_down.
+//   B  fp16 routed rows, contiguous in grouped order (GEMM1: the activations
 //      gathered and converted once to fp16 by a small kernel; GEMM2: the h rows
-//      GEMM1 wrote), loaded by 2-D TMA boxes of 64 rows x 64 K;
-//   B  int4 weights, streamed as packed 1152-byte chunks by TMA bulk copies
-//      into a ring, then dequantised by eight warps to fp16 RNE(q * s) --
-//      the dequantised weight rounded once.
-// One thread issues tcgen05.mma (kind::f16, fp32 accumulate) into tensor
-// memory; two 256-column accumulators alternate so that the epilogue of one
-// tile runs under the MMAs of the next.  A block of an expert with fewer than
-// 128 routed rows still costs a full 128-row MMA; the tensor pipe has room for
-// that, and it keeps every tile the same cost and the epilogue a plain copy.
-// Roles per CTA (19 warps): 0 MMA issuer + TMEM owner, 1 weight-chunk TMA,
-// 2-9 dequantisation, 10 routed-row TMA, 11-18 epilogue (two per TMEM lane quarter).
+//      GEMM1 wrote), loaded by 2-D TMA boxes of 64 rows x 64 K into a 4-stage ring;
+//   A  int4 (or NVFP4) weights read by eight dequantising warps straight from global
+//      memory in the packed tile order, converted in registers to fp16 RNE(q * s)
+//      (NVFP4: code times block scale, exact) and stored into tensor memory with
+//      tcgen05.st -- the dequantised weights never pass through shared memory, and an
+//      expert block with few routed rows costs an MMA of that width only.
+// One thread issues tcgen05.mma (kind::f16, A from tensor memory, fp32 accumulate).
+// Tensor memory (512 columns): D0, D1 (128 columns each) and a 4-stage A ring
+// (2 M tiles x 32 columns per stage).  The epilogue copies both accumulators into
+// shared memory, converted and turned to row order, releases them, then writes h or y
+// with 16-byte stores while the next tile's MMAs run.
+// Roles per CTA (16 warps): 1 routed-row TMA, 2 MMA issuer + TMEM owner (on the third
+// SM sub-partition, which the other roles load least), 4-11 dequantisation,
+// 12-15 epilogue (one per TMEM lane quarter).
 // Every wait is bounded (status word + clean exit, TMEM freed).
+
 #include <cuda.h>
 
 #include "kernels.h"
@@ -36,25 +39,15 @@
 namespace bitmoe {
 namespace {
 
-constexpr int kPM = 128;                  // routed rows per tile (MMA M)
-constexpr int kPN = 256;                  // weight rows per tile (MMA N)
-constexpr int kPK = 64;                   // K per operand stage (one 128-byte swizzle row of fp16)
-constexpr int kPStages = 3;               // operand stages
-constexpr int kRawStages = 4;             // packed-weight stages
-constexpr int kSubTiles = kPN / kTileRows;            // 16 packed 16-row tiles per weight tile
-constexpr int kRawBytes = kSubTiles * kChunkBytes;    // 256 rows x 128 K packed (18432 B)
-constexpr int kABytes = kPM * kPK * 2;                // 16 KB routed-row tile
-constexpr int kBBytes = kPN * kPK * 2;                // 32 KB weight tile
-constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kPWarps = 19;
-constexpr int kPThreads = kPWarps * 32;
-constexpr int kWarpMMA = 0, kWarpRaw = 1, kWarpDq0 = 2, kWarpA = 10, kWarpEpi0 = 11;
-constexpr int kDqWarps = 8, kEpiWarps = 8;
+constexpr int kPM = 128;                  // weight rows per M tile (two M tiles per tile)
+constexpr int kPN = 256;                  // weight rows per tile (GEMM 2; GEMM 1: 128 gate + 128 up)
+constexpr int kPK = 64;                   // K per stage (one 128-byte swizzle row of fp16)
+constexpr int kSubTiles = kPN / kTileRows;  // 16 packed 16-row tiles per weight tile
 constexpr int kBoxRows = 64;              // routed rows per TMA box
-constexpr int kRowsPerBlock = kPM;        // routed rows per expert block
+constexpr int kRowsPerBlock = 128;        // routed rows per expert block (MMA N at most)
 
 struct PrefillArgs {
-  CUtensorMap tmap_a;  // routed rows [R, Kdim] fp16, box 64 x 64, 128-byte swizzle
+  CUtensorMap tmap_a;  // routed rows [R, Kdim] fp16 (the MMA's B), box 64 x 64, 128-byte swizzle
   int mode;            // 1 = gate/up + SwiGLU, 2 = down
   int T, d, I, E, k;   // shapes
   int Kdim;            // reduction length (d for mode 1, I for mode 2)
@@ -74,13 +67,11 @@ struct PrefillArgs {
   unsigned long long* trace;  // optional [grid][16] per-role cycle counters
 };
 
-// Optional per-role cycle counters (clock64) written per CTA when a trace
-// buffer is set: 0 MMA waiting on routed rows, 1 MMA waiting on weights,
-// 2 MMA waiting for a free accumulator, 3 MMA total, 4 TMA waiting for a free
-// chunk slot, 5 dequantisation waiting for chunks, 6 dequantisation waiting
-// for a free stage, 7 dequantisation total, 8 row copies waiting for a free
-// stage, 9 epilogue waiting for an accumulator, 10 epilogue total, 11 tiles,
-// 12 MMA issue (fence, four MMAs, commit), 13 sum of the tiles' N.
+// Optional per-role cycle counters (clock64) written per CTA when a trace buffer is
+// set: 2 MMA waiting for free accumulators, 3 MMA total, 4 MMA waiting for a full
+// stage, 6 dequantisation waiting for a free stage, 7 dequantisation total,
+// 9 epilogue waiting for the accumulators, 10 epilogue total, 11 tiles, 12 sum of the
+// tiles' N.
 __device__ __forceinline__ void ptrace(const PrefillArgs& p, int slot, unsigned long long v) {
   if (p.trace) p.trace[blockIdx.x * 16 + slot] = v;
 }
@@ -103,15 +94,6 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
@@ -129,22 +111,10 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 
-// 8 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-               : "r"(taddr));
-}
-
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// 16-byte chunk j (0..7) of operand row r inside a 128-byte-swizzled K-major tile.
-__device__ __forceinline__ uint32_t swz_off(int r, int j) {
-  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4));
 }
 
 __device__ __forceinline__ int expert_of(const int32_t* __restrict__ pre, int E, int b) {
@@ -198,398 +168,7 @@ __device__ __forceinline__ const uint8_t* subtile_base(const PrefillArgs& p, con
   return bank + ((size_t)ti.e * rtiles + rt) * (size_t)tile_bytes(p.Kdim);
 }
 
-// Dequantise the 8 int4 values of one packed word times scale s into 16 bytes of fp16.
-__device__ __forceinline__ uint4 dequant_word_f16(uint32_t w, __half2 s2) {
-  uint32_t q[4], o[4];
-  nib_pairs4_f16(w, q);
-#pragma unroll
-  for (int pr = 0; pr < 4; ++pr) {
-    __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&q[pr]), s2);
-    o[pr] = *reinterpret_cast<uint32_t*>(&v);
-  }
-  return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
-// NVFP4: the 8 E2M1 codes of one packed word times their E4M3 block scale
-// (byte sb) as 16 bytes of fp16 -- exact, so nothing is rounded here.
-__device__ __forceinline__ uint4 dequant_word_fp4(uint32_t w, uint32_t sb) {
-  uint32_t o[4];
-  e2m1x8_f16_scaled(w, e4m3_pair_f16(sb), o);
-  return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-// kFp4: NVFP4 banks (codes times block scale, exact fp16 weights; the tensor
-// scales multiply the accumulators in the epilogue); else int4, RNE(q * s).
-template <bool kFp4>
-__global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid_constant__ PrefillArgs p) {
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  // the swizzled operand tiles need a 1024-byte aligned base; the dynamic shared memory
-  // window starts there (checked: a misaligned base stops the kernel with a status)
-  if ((smem_u32(smem_raw) & 1023u) != 0) {
-    if (threadIdx.x == 0) record_status(p.st, kStatusCheck, 70, (int)(smem_u32(smem_raw) & 1023u));
-    return;
-  }
-  unsigned char* stages = smem_raw;  // [stage]: A routed rows (16 KB), B weights (32 KB)
-  unsigned char* raw = stages + (size_t)kPStages * kStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(raw + (size_t)kRawStages * kRawBytes);
-  uint64_t* raw_full = bars;                   // [kRawStages] TMA transaction count
-  uint64_t* raw_empty = raw_full + kRawStages; // [kRawStages] one arrival per dequantisation warp
-  uint64_t* t_full = raw_empty + kRawStages;   // [kPStages] routed rows: TMA transaction count
-  uint64_t* w_full = t_full + kPStages;        // [kPStages] weights: one arrival per dequantisation warp
-  uint64_t* s_empty = w_full + kPStages;       // [kPStages] MMA commit
-  uint64_t* acc_full = s_empty + kPStages;     // [2] MMA commit
-  uint64_t* acc_empty = acc_full + 2;          // [2] one arrival per epilogue warp
-  uint64_t* drain = acc_empty + 2;             // MMA commit: every MMA of this CTA done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  constexpr uint32_t kTmemCols = 2 * kPN;  // two 256-column accumulators
-
-  if (tid == 0) {
-    for (int s = 0; s < kRawStages; ++s) {
-      mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], kDqWarps);
-    }
-    for (int s = 0; s < kPStages; ++s) {
-      mbar_init(&t_full[s], 1);
-      mbar_init(&w_full[s], kDqWarps);
-      mbar_init(&s_empty[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], kEpiWarps);
-    }
-    mbar_init(drain, 1);
-    fence_mbar_init();
-  }
-  if (warp == kWarpMMA) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-
-  const int n_tiles = p.nb_prefix[p.E] * p.FB;
-  const int nchunks = p.Kdim / kChunkK;  // 128-K packed chunks per weight row
-  const int nkb = 2 * nchunks;           // 64-K operand stages per tile
-
-  if (warp == kWarpRaw) {
-    // ---------------- packed weight chunks: 16 sub-tiles x 1152 B per 128 K, TMA bulk copies
-    if (lane == 0) {
-      int rit = 0;
-      long long t_wait = 0;
-      bool ok = true;
-      for (int j = 0, tile = snake_tile(0); tile < n_tiles && ok; tile = snake_tile(++j)) {
-        const TileInfo ti = tile_info(p, tile);
-        const uint8_t* sb[kSubTiles];
-#pragma unroll
-        for (int i = 0; i < kSubTiles; ++i) sb[i] = subtile_base(p, ti, i);
-        for (int c = 0; c < nchunks; ++c, ++rit) {
-          const int s = rit % kRawStages;
-          const long long w0 = clock64();
-          if (rit >= kRawStages && !mbar_wait(&raw_empty[s], ((rit / kRawStages) - 1) & 1, p.st, 60)) {
-            ok = false;
-            break;
-          }
-          t_wait += clock64() - w0;
-          mbar_arrive_expect_tx(&raw_full[s], kRawBytes);
-          unsigned char* dst = raw + (size_t)s * kRawBytes;
-#pragma unroll
-          for (int i = 0; i < kSubTiles; ++i)
-            bulk_g2s(dst + i * kChunkBytes, sb[i] + (size_t)c * kChunkBytes, kChunkBytes, &raw_full[s]);
-        }
-      }
-      // copies still in flight land before this thread leaves
-      for (int n = (rit > kRawStages ? rit - kRawStages : 0); n < rit; ++n)
-        mbar_wait(&raw_full[n % kRawStages], (n / kRawStages) & 1, p.st, 61);
-      ptrace(p, 4, t_wait);
-    }
-  } else if (warp >= kWarpDq0 && warp < kWarpDq0 + kDqWarps) {
-    // ---------------- dequantisation: warp w owns sub-tiles w and w + 8 (16 weight rows each);
-    // per 128-K chunk a lane reads one 16-byte quarter (four group words) of two rows per
-    // sub-tile and writes the fp16 values of both 64-K stages
-    const int w = warp - kWarpDq0;
-    const int cq = lane & 3;  // quarter of the chunk: k = 32 g + 8 cq + m
-    int rit = 0, it = 0;
-    long long t_raw = 0, t_stage = 0;
-    const long long t_start = clock64();
-    bool ok = true;
-    for (int j = 0, tile = snake_tile(0); tile < n_tiles && ok; tile = snake_tile(++j)) {
-      for (int c = 0; c < nchunks && ok; ++c, ++rit) {
-        const int rs = rit % kRawStages;
-        const long long w0 = clock64();
-        if (!mbar_wait(&raw_full[rs], (rit / kRawStages) & 1, p.st, 62)) {
-          ok = false;
-          break;
-        }
-        t_raw += clock64() - w0;
-        uint4 q[2][2];
-        uint2 sc[2][2];
-#pragma unroll
-        for (int st = 0; st < 2; ++st) {
-          const unsigned char* src = raw + (size_t)rs * kRawBytes + (w + 8 * st) * kChunkBytes;
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int rr = 8 * u + (lane >> 2);
-            q[st][u] = *reinterpret_cast<const uint4*>(src + (rr * 4 + cq) * 16);
-            sc[st][u] = *reinterpret_cast<const uint2*>(src + kChunkQBytes + rr * 8);
-          }
-        }
-#pragma unroll
-        for (int h = 0; h < 2; ++h, ++it) {  // the two 64-K stages of this chunk
-          const int s = it % kPStages;
-          const long long w1 = clock64();
-          if (it >= kPStages && !mbar_wait(&s_empty[s], ((it / kPStages) - 1) & 1, p.st, 63)) {
-            ok = false;
-            break;
-          }
-          t_stage += clock64() - w1;
-          unsigned char* dst = stages + (size_t)s * kStageBytes + kABytes;
-#pragma unroll
-          for (int st = 0; st < 2; ++st) {
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int row = 16 * (w + 8 * st) + 8 * u + (lane >> 2);
-              const uint32_t wg0 = h ? q[st][u].z : q[st][u].x;  // group 2h
-              const uint32_t wg1 = h ? q[st][u].w : q[st][u].y;  // group 2h+1
-              uint4 d0, d1;
-              if constexpr (kFp4) {  // block 2 gg + cq / 2 of the chunk holds this lane's 8 columns
-                const uint32_t ls = fp4_lane_scales(sc[st][u], cq);
-                d0 = dequant_word_fp4(wg0, (ls >> (16 * h)) & 0xffu);
-                d1 = dequant_word_fp4(wg1, (ls >> (16 * h + 8)) & 0xffu);
-              } else {
-                const uint32_t s01 = h ? sc[st][u].y : sc[st][u].x;
-                const __half2 s0 = __half2half2(__ushort_as_half((uint16_t)(s01 & 0xffffu)));
-                const __half2 s1 = __half2half2(__ushort_as_half((uint16_t)(s01 >> 16)));
-                d0 = dequant_word_f16(wg0, s0);
-                d1 = dequant_word_f16(wg1, s1);
-              }
-              // a 128-bit store goes out in phases of 8 lanes = rows r, r+1 of the same
-              // 4-chunk swizzle group; odd rows store their second chunk first so that each
-              // phase covers all 8 chunk positions (no bank conflict)
-              const bool odd = (lane >> 2) & 1;
-              *reinterpret_cast<uint4*>(dst + swz_off(row, odd ? 4 + cq : cq)) = odd ? d1 : d0;
-              *reinterpret_cast<uint4*>(dst + swz_off(row, odd ? cq : 4 + cq)) = odd ? d0 : d1;
-            }
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive_cta(&w_full[s]);
-            // the chunk slot is free only once every lane has used what it loaded from
-            // it: the stores above consumed those registers, and the warp has synced
-            if (h == 0) mbar_arrive_cta(&raw_empty[rs]);
-          }
-        }
-      }
-    }
-    if (w == 0 && lane == 0) {
-      ptrace(p, 5, t_raw);
-      ptrace(p, 6, t_stage);
-      ptrace(p, 7, clock64() - t_start);
-    }
-  } else if (warp == kWarpA) {
-    // ---------------- routed rows: two TMA boxes of 64 rows x 64 K per stage
-    if (lane == 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_a)) : "memory");
-      int it = 0;
-      long long t_wait = 0;
-      bool ok = true;
-      for (int j = 0, tile = snake_tile(0); tile < n_tiles && ok; tile = snake_tile(++j)) {
-        const TileInfo ti = tile_info(p, tile);
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const int s = it % kPStages;
-          const long long w0 = clock64();
-          if (it >= kPStages && !mbar_wait(&s_empty[s], ((it / kPStages) - 1) & 1, p.st, 64)) {
-            ok = false;
-            break;
-          }
-          t_wait += clock64() - w0;
-          mbar_arrive_expect_tx(&t_full[s], (uint32_t)kABytes);
-          const uint32_t dst = smem_u32(stages + (size_t)s * kStageBytes);
-#pragma unroll
-          for (int i = 0; i < kPM / kBoxRows; ++i)
-            asm volatile(
-                "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-                    dst + (uint32_t)(i * kBoxRows * kPK * 2)),
-                "l"(reinterpret_cast<uint64_t>(&p.tmap_a)), "r"(kb * kPK), "r"(ti.p0 + i * kBoxRows),
-                "r"(smem_u32(&t_full[s]))
-                : "memory");
-        }
-      }
-      // boxes still in flight land before this thread leaves
-      for (int n = (it > kPStages ? it - kPStages : 0); n < it; ++n)
-        mbar_wait(&t_full[n % kPStages], (n / kPStages) & 1, p.st, 69);
-      ptrace(p, 8, t_wait);
-    }
-  } else if (warp == kWarpMMA) {
-    // ---------------- MMA issuer (one thread)
-    if (lane == 0) {
-      const uint32_t idesc = umma_idesc_f16(kPM, kPN);
-      int it = 0, lt = 0;
-      long long t_a = 0, t_b = 0, t_acc = 0, t_issue = 0;
-      const long long t_start = clock64();
-      bool ok = true;
-      for (int j = 0, tile = snake_tile(0); tile < n_tiles && ok; tile = snake_tile(++j), ++lt) {
-        const int buf = lt & 1;
-        const long long w0 = clock64();
-        if (lt >= 2 && !mbar_wait(&acc_empty[buf], ((lt >> 1) - 1) & 1, p.st, 65)) break;
-        t_acc += clock64() - w0;
-        tc_fence_after();
-        const uint32_t d0 = tmem_base + (uint32_t)(buf * kPN);
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const int s = it % kPStages;
-          const long long w1 = clock64();
-          const bool got_a = mbar_wait(&t_full[s], (it / kPStages) & 1, p.st, 66);
-          const long long w2 = clock64();
-          const bool got_b = got_a && mbar_wait(&w_full[s], (it / kPStages) & 1, p.st, 67);
-          const long long w3 = clock64();
-          t_a += w2 - w1;
-          t_b += w3 - w2;
-          if (!got_b) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t asm_ = smem_u32(stages + (size_t)s * kStageBytes);
-          const uint32_t bsm = asm_ + (uint32_t)kABytes;
-#pragma unroll
-          for (int ks = 0; ks < kPK / 16; ++ks)
-            umma_f16(d0, umma_smem_desc(asm_ + ks * 32), umma_smem_desc(bsm + ks * 32), idesc,
-                     (kb > 0 || ks > 0) ? 1u : 0u);
-          umma_commit(&s_empty[s]);  // frees the stage once these MMAs have read it
-          t_issue += clock64() - w3;
-        }
-        if (!ok) break;
-        umma_commit(&acc_full[buf]);
-      }
-      // every MMA this thread issued has finished writing TMEM before the CTA
-      // deallocates it, also when a wait ran out above (bounded)
-      umma_commit(drain);
-      mbar_wait(drain, 0, p.st, 71);
-      ptrace(p, 0, t_a);
-      ptrace(p, 1, t_b);
-      ptrace(p, 2, t_acc);
-      ptrace(p, 3, clock64() - t_start);
-      ptrace(p, 11, lt);
-      ptrace(p, 12, t_issue);
-    }
-  } else if (warp >= kWarpEpi0) {
-    // ---------------- epilogue: thread = one routed row (TMEM lane), warp (q, hf) takes half
-    // of the 256 columns; GEMM1: h = silu(gate col c) * (up col 128 + c) for its 64 features,
-    // GEMM2: its 128 y values; the next 16 columns' TMEM load is in flight meanwhile
-    const int q = warp & 3;                  // TMEM lane quarter this warp may access
-    const int hf = (warp - kWarpEpi0) >> 2;  // which half of the columns
-    const int n = q * 32 + lane;             // routed row inside the tile
-    int lt = 0;
-    long long t_wait = 0;
-    const long long t_start = clock64();
-    bool dead = false;  // a wait ran out: no more waits or stores
-    for (int j = 0, tile = snake_tile(0); tile < n_tiles; tile = snake_tile(++j), ++lt) {
-      const int buf = lt & 1;
-      const long long w0 = clock64();
-      const bool got = !dead && __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (lt >> 1) & 1, p.st, 68));
-      dead = !got;
-      t_wait += clock64() - w0;
-      if (dead) break;
-      tc_fence_after();
-      const TileInfo ti = tile_info(p, tile);
-      const bool valid = n < ti.nval;
-      const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kPN);
-      const float ta = kFp4 ? p.tsa[ti.e] : 1.f, tb = (kFp4 && p.mode == 1) ? p.tsb[ti.e] : 1.f;
-      if (p.mode == 1) {
-        __half* hrow = p.hout + (size_t)(ti.p0 + (valid ? n : 0)) * p.I + ti.f * 128;
-        for (int c0 = hf * 64; c0 < hf * 64 + 64; c0 += 16) {
-          uint32_t g[16], u[16];
-          tmem_ld16(tq + (uint32_t)c0, g);
-          tmem_ld16(tq + (uint32_t)(128 + c0), u);
-          tmem_ld_wait();
-          if (!valid) continue;
-          uint32_t hv[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            __half2 h2 = __floats2half2_rn(
-                silu_mul(__uint_as_float(g[2 * i]) * ta, __uint_as_float(u[2 * i]) * tb),
-                silu_mul(__uint_as_float(g[2 * i + 1]) * ta, __uint_as_float(u[2 * i + 1]) * tb));
-            hv[i] = *reinterpret_cast<uint32_t*>(&h2);
-          }
-          *reinterpret_cast<uint4*>(hrow + c0) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-          *reinterpret_cast<uint4*>(hrow + c0 + 8) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
-        }
-      } else {
-        const size_t rowoff = (size_t)(ti.p0 + (valid ? n : 0)) * p.d + (size_t)ti.f * kPN;
-        uint32_t cur[16], nxt[16];
-        tmem_ld16(tq + (uint32_t)(hf * 128), cur);
-        tmem_ld_wait();
-        for (int c0 = hf * 128; c0 < hf * 128 + 128; c0 += 16) {
-          const bool more = c0 + 16 < hf * 128 + 128;
-          if (more) tmem_ld16(tq + (uint32_t)(c0 + 16), nxt);
-          if (kFp4) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) cur[i] = __float_as_uint(__uint_as_float(cur[i]) * ta);
-          }
-          if (valid) {
-            if (p.y16) {
-              uint32_t hv[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                __half2 h2 = __floats2half2_rn(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1]));
-                hv[i] = *reinterpret_cast<uint32_t*>(&h2);
-              }
-              *reinterpret_cast<uint4*>(p.y16 + rowoff + c0) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-              *reinterpret_cast<uint4*>(p.y16 + rowoff + c0 + 8) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                *reinterpret_cast<uint4*>(p.yout + rowoff + c0 + 4 * i) =
-                    make_uint4(cur[4 * i], cur[4 * i + 1], cur[4 * i + 2], cur[4 * i + 3]);
-            }
-          }
-          if (more) {
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) cur[i] = nxt[i];
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cta(&acc_empty[buf]);
-    }
-    if (warp == kWarpEpi0 && lane == 0) {
-      ptrace(p, 9, t_wait);
-      ptrace(p, 10, clock64() - t_start);
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == kWarpMMA) {
-    tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols) : "memory");
-  }
-}
-
 // ---------------------------------------------------------------- weights in tensor memory
-//
-// The grouped GEMM with the roles of the operands swapped: the MMA's A side (M = 128)
-// is 128 weight rows held in tensor memory, its B side (N = the routed rows of one
-// 128-row expert block, rounded up to 16) the activation rows in shared memory, so
-// that the dequantised weights never pass through shared memory (they go from the
-// dequantising warps' registers to tensor memory with tcgen05.st) and an expert block
-// with few rows costs an MMA of that width.  Each B stage feeds two M tiles (GEMM 1:
-// 128 gate rows and the same 128 up rows; GEMM 2: 256 rows of W_down), two
-// accumulators D0, D1 of N columns.  Per 64-column k-block the CTA's shared memory
-// sees the 16 KB B stage written by TMA and read twice by the MMAs, against 512 MMA
-// cycles at N = 128.
 //
 // K order.  The dequantising warps read the packed tiles in the mma-fragment order
 // (lane (g, c) holds rows g and g+8, columns 8c .. 8c+7 of every 32-column group) and
@@ -599,8 +178,6 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
 // P(p) = 4 ((p % 8) / 2) + p % 2 + 2 (p / 8); the B rows are stored with the same
 // permutation inside every 32-element group (the gathered activations, and the h rows
 // GEMM 1 writes for GEMM 2), so every product pairs the right elements.
-// Warps: 1 B rows, 2 MMA issuer + TMEM owner (on the third SM sub-partition, which the
-// other roles load least), 4-11 dequantisation, 12-15 epilogue.
 constexpr int kQThreads = 16 * 32;
 constexpr int kQWarpMMA = 2, kQWarpB = 1, kQWarpDq0 = 4, kQWarpEpi0 = 12;
 constexpr int kQBStages = 4;                      // B ring (128 rows x 64 K fp16 = 16 KB each)
@@ -608,10 +185,10 @@ constexpr int kQAStages = kQBStages;              // A ring in tensor memory (2 
                                                   // the same depth, so one MMA commit frees both
 constexpr int kQBBytes = kPM * kPK * 2;
 constexpr uint32_t kQTmemCols = 512;              // D0, D1 (128 columns each), then the A ring
-constexpr int kQEpiBytes = 16 * 32 * 4;          // per epilogue warp: 16 routed rows x 32 values (fp32 at most)
+constexpr int kQStageWarp = 2 * 128 * 32 * 4;     // per epilogue warp: [2 M tiles][128 routed rows][32] fp32 at most
 constexpr int kQTileCache = 128;                  // tiles of a CTA whose TileInfo is computed once, up front
 constexpr size_t kQSmem =
-    (size_t)kQBStages * kQBBytes + 4 * kQEpiBytes + (size_t)kQTileCache * sizeof(TileInfo) + 1024 + 256;
+    (size_t)kQBStages * kQBBytes + 4 * (size_t)kQStageWarp + (size_t)kQTileCache * sizeof(TileInfo) + 1024 + 256;
 static_assert(kQSmem <= 227 * 1024, "shared memory budget");
 static_assert(256 + kQAStages * 2 * 32 <= (int)kQTmemCols, "tensor memory budget");
 
@@ -681,8 +258,8 @@ __global__ void __launch_bounds__(kQThreads, 1) prefill_wa_kernel(const __grid_c
   uint64_t* d_empty = d_full + 1;              // one arrival per epilogue warp
   uint64_t* drain = d_empty + 1;               // MMA commit: every MMA of this CTA done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  unsigned char* epi_tile = smem_raw + (size_t)kQBStages * kQBBytes + 1024;  // [4 warps][kQEpiBytes]
-  TileInfo* tcache = reinterpret_cast<TileInfo*>(epi_tile + 4 * kQEpiBytes);  // [kQTileCache]
+  unsigned char* epi_stage = smem_raw + (size_t)kQBStages * kQBBytes + 1024;  // [4 warps][kQStageWarp]
+  TileInfo* tcache = reinterpret_cast<TileInfo*>(epi_stage + 4 * (size_t)kQStageWarp);  // [kQTileCache]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -859,23 +436,26 @@ __global__ void __launch_bounds__(kQThreads, 1) prefill_wa_kernel(const __grid_c
     if (lane == 0) {
       int it = 0, lt = 0;
       bool ok = true;
-      long long t_d = 0;
+      long long t_d = 0, t_f = 0, n_sum = 0;
       const long long t_start = clock64();
       const uint64_t bdesc0 = umma_smem_desc(smem_u32(bst));
       for (int j = 0, tile = snake_tile(0); tile < n_tiles && ok; tile = snake_tile(++j), ++lt) {
         const TileInfo ti = tinfo(j, tile);
         const int N = (ti.nval + 15) & ~15;
         const uint32_t idesc = umma_idesc_f16(kPM, N);
+        n_sum += N;
         const long long w0 = clock64();
         if (lt >= 1 && !mbar_wait(d_empty, (lt - 1) & 1, p.st, 84)) break;
         t_d += clock64() - w0;
         tc_fence_after();
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int sbq = it % kQBStages, saq = sbq;
+          const long long w1 = clock64();
           if (!mbar_wait(&b_full[sbq], (it / kQBStages) & 1, p.st, 85)) {
             ok = false;
             break;
           }
+          t_f += clock64() - w1;
           tc_fence_after();
           // stage sbq's descriptor is the first stage's plus its offset in 16-byte units; a 16-K
           // step is 32 bytes further, +2 in the address field
@@ -896,7 +476,9 @@ __global__ void __launch_bounds__(kQThreads, 1) prefill_wa_kernel(const __grid_c
       mbar_wait(drain, 0, p.st, 87);
       ptrace(p, 2, t_d);
       ptrace(p, 3, clock64() - t_start);
+      ptrace(p, 4, t_f);
       ptrace(p, 11, lt);
+      ptrace(p, 12, n_sum);
     }
   } else if (warp >= kQWarpEpi0) {
     // ---------------- epilogue: thread = one TMEM lane = weight row 32q + lane of both M tiles;
@@ -916,69 +498,73 @@ __global__ void __launch_bounds__(kQThreads, 1) prefill_wa_kernel(const __grid_c
       const TileInfo ti = tinfo(j, tile);
       const float ta = kFp4 ? p.tsa[ti.e] : 1.f, tb = (kFp4 && p.mode == 1) ? p.tsb[ti.e] : 1.f;
       const uint32_t tq = tmem_base + ((uint32_t)(32 * q) << 16);
-      // A thread holds one weight row of 16 routed rows per step; the warp turns its
-      // 32 x 16 block around in shared memory so that each routed row's 32 values go
-      // out as 16-byte stores.
-      unsigned char* tile_s = epi_tile + (size_t)(warp - kQWarpEpi0) * kQEpiBytes;
+      // The warp copies its 32 rows of both accumulators into shared memory, already
+      // turned around (one routed row's 32 values contiguous) and converted, and releases
+      // the accumulators at once; the stores to global memory (16 bytes each) then run
+      // under the next tile's MMAs.  Staging per warp: [M tile][routed row][32 values].
+      const bool f32out = p.mode == 2 && p.y16 == nullptr;
+      unsigned char* stg = epi_stage + (size_t)q * kQStageWarp;
+      const int pos = (p.mode == 1) ? kperm(row) - 32 * q : lane;  // this thread's column in the 32
       for (int n0 = 0; n0 < ti.nval; n0 += 16) {
         uint32_t d0[16], d1[16];
         tmem_ld16(tq + (uint32_t)n0, d0);
         tmem_ld16(tq + (uint32_t)(128 + n0), d1);
         tmem_ld_wait();
-        const int nr = ti.nval - n0 < 16 ? ti.nval - n0 : 16;  // routed rows in this step
         if (p.mode == 1) {  // h = silu(gate) * up of feature f, in the K order GEMM 2 reads
-          __half* ts = reinterpret_cast<__half*>(tile_s);
-          const int pos = kperm(row) - 32 * q;  // column of this feature inside its 32-group
+          __half* hs = reinterpret_cast<__half*>(stg);
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            ts[i * 32 + pos] = __float2half_rn(silu_mul_fast(__uint_as_float(d0[i]) * ta, __uint_as_float(d1[i]) * tb));
-          __syncwarp();
-          const int f0 = ti.f * 128 + 32 * q;
+            hs[(n0 + i) * 32 + pos] =
+                __float2half_rn(silu_mul_fast(__uint_as_float(d0[i]) * ta, __uint_as_float(d1[i]) * tb));
+        } else if (!f32out) {
+          __half* ys = reinterpret_cast<__half*>(stg);
 #pragma unroll
-          for (int v = lane; v < 64; v += 32) {  // 16 rows x 4 chunks of 16 bytes
-            const int r = v >> 2, c16 = v & 3;
-            if (r < nr)
-              *reinterpret_cast<uint4*>(p.hout + (size_t)(ti.p0 + n0 + r) * p.I + f0 + 8 * c16) =
-                  *reinterpret_cast<const uint4*>(ts + r * 32 + 8 * c16);
+          for (int i = 0; i < 16; ++i) {
+            ys[(n0 + i) * 32 + pos] = __float2half_rn(__uint_as_float(d0[i]) * ta);
+            ys[(128 + n0 + i) * 32 + pos] = __float2half_rn(__uint_as_float(d1[i]) * ta);
           }
-          __syncwarp();
-        } else {  // y rows: W_down rows f*256 + 32q + lane (tile 0) and + 128 (tile 1)
+        } else {
+          float* ys = reinterpret_cast<float*>(stg);
 #pragma unroll
-          for (int t2 = 0; t2 < 2; ++t2) {
-            const uint32_t(&dd)[16] = t2 ? d1 : d0;
-            const int c0 = ti.f * kPN + 128 * t2 + 32 * q;
-            if (p.y16) {
-              __half* ts = reinterpret_cast<__half*>(tile_s);
-#pragma unroll
-              for (int i = 0; i < 16; ++i) ts[i * 32 + lane] = __float2half_rn(__uint_as_float(dd[i]) * ta);
-              __syncwarp();
-#pragma unroll
-              for (int v = lane; v < 64; v += 32) {
-                const int r = v >> 2, c16 = v & 3;
-                if (r < nr)
-                  *reinterpret_cast<uint4*>(p.y16 + (size_t)(ti.p0 + n0 + r) * p.d + c0 + 8 * c16) =
-                      *reinterpret_cast<const uint4*>(ts + r * 32 + 8 * c16);
-              }
-            } else {
-              float* ts = reinterpret_cast<float*>(tile_s);
-#pragma unroll
-              for (int i = 0; i < 16; ++i) ts[i * 32 + lane] = __uint_as_float(dd[i]) * ta;
-              __syncwarp();
-#pragma unroll
-              for (int v = lane; v < 128; v += 32) {  // 16 rows x 8 chunks of 16 bytes
-                const int r = v >> 3, c16 = v & 7;
-                if (r < nr)
-                  *reinterpret_cast<uint4*>(p.yout + (size_t)(ti.p0 + n0 + r) * p.d + c0 + 4 * c16) =
-                      *reinterpret_cast<const uint4*>(ts + r * 32 + 4 * c16);
-              }
-            }
-            __syncwarp();
+          for (int i = 0; i < 16; ++i) {
+            ys[(n0 + i) * 32 + pos] = __uint_as_float(d0[i]) * ta;
+            ys[(128 + n0 + i) * 32 + pos] = __uint_as_float(d1[i]) * ta;
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cta(d_empty);
+      if (lane == 0) mbar_arrive_cta(d_empty);  // the MMAs of the next tile may overwrite D now
+      if (p.mode == 1) {  // h rows: 32 features (64 bytes, 4 x 16) per routed row
+        const __half* hs = reinterpret_cast<const __half*>(stg);
+        const int f0 = ti.f * 128 + 32 * q;
+        for (int v = lane; v < ti.nval * 4; v += 32) {
+          const int r = v >> 2, c16 = v & 3;
+          *reinterpret_cast<uint4*>(p.hout + (size_t)(ti.p0 + r) * p.I + f0 + 8 * c16) =
+              *reinterpret_cast<const uint4*>(hs + r * 32 + 8 * c16);
+        }
+      } else {  // y rows: W_down rows f*256 + 32q + lane (M tile 0) and + 128 (M tile 1)
+#pragma unroll
+        for (int t2 = 0; t2 < 2; ++t2) {
+          const int c0 = ti.f * kPN + 128 * t2 + 32 * q;
+          if (!f32out) {  // 32 columns (64 bytes, 4 x 16) per routed row
+            const __half* ys = reinterpret_cast<const __half*>(stg) + 128 * 32 * t2;
+            for (int v = lane; v < ti.nval * 4; v += 32) {
+              const int r = v >> 2, c16 = v & 3;
+              *reinterpret_cast<uint4*>(p.y16 + (size_t)(ti.p0 + r) * p.d + c0 + 8 * c16) =
+                  *reinterpret_cast<const uint4*>(ys + r * 32 + 8 * c16);
+            }
+          } else {  // fp32: 128 bytes (8 x 16) per routed row
+            const float* ys = reinterpret_cast<const float*>(stg) + 128 * 32 * t2;
+            for (int v = lane; v < ti.nval * 8; v += 32) {
+              const int r = v >> 3, c16 = v & 7;
+              *reinterpret_cast<uint4*>(p.yout + (size_t)(ti.p0 + r) * p.d + c0 + 4 * c16) =
+                  *reinterpret_cast<const uint4*>(ys + r * 32 + 4 * c16);
+            }
+          }
+        }
+      }
+      __syncwarp();  // the staging is read before the next tile's copy overwrites it
     }
     if (warp == kQWarpEpi0 && lane == 0) {
       ptrace(p, 9, t_wait);
@@ -1038,28 +624,6 @@ __global__ void __launch_bounds__(1024) block_list_kernel(const int32_t* __restr
   }
 }
 
-// xs[pos] = fp16(x[sorted_rows[pos] / k]): the routed rows in grouped order, one warp per row.
-__global__ void gather_f16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_rows, int R,
-                                  int k, int d, __half* __restrict__ xs) {
-  const int lane = threadIdx.x & 31;
-  const int warps = (gridDim.x * blockDim.x) >> 5;
-  for (int pos = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; pos < R; pos += warps) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(sorted_rows[pos] / k) * d);
-    uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)pos * d);
-    for (int i = lane; i < d / 8; i += 32) {
-      const uint4 v = src[i];
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      uint32_t o[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        __half2 h2 = __floats2half2_rn(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xffff0000u));
-        o[q] = *reinterpret_cast<uint32_t*>(&h2);
-      }
-      dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-  }
-}
-
 // The same gather with every 32-element group of a row in the K order of the weights
 // in tensor memory (kperm): the octet 8c .. 8c+7 of a group lands as two runs of four,
 // at 4c and at 4c + 16.
@@ -1108,9 +672,6 @@ cudaError_t encode_rows_map(CUtensorMap* map, const void* base, int rows, int K)
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
-
-constexpr size_t kPSmem = (size_t)kPStages * kStageBytes + (size_t)kRawStages * kRawBytes + 256;
-static_assert(kPSmem <= 227 * 1024, "shared memory budget");
 
 int sm_count_prefill() {
   static int cnt[64] = {};
