@@ -45,6 +45,7 @@ struct MoeWs {
   __half* xs;         // [R, d] routed rows in grouped order, fp16 (grouped-GEMM path)
   int32_t* nb_prefix;  // [E+1] 128-row blocks per expert, then the block list (grouped-GEMM path)
   uint16_t* xh;        // [T, d] bf16 RMSNorm of the residual (pre-norm step, unfused path)
+  uint16_t* w_split;   // [3E, d] bf16 parts of the router rows (tcgen05 router, many tokens; else null)
   size_t total;
 };
 
@@ -74,6 +75,9 @@ MoeWs moe_layout(const bitmoe_moe_shape_t* sh, int64_t T, void* base) {
   // prefix of 128-row expert blocks [E+1], then the blocks widest first [R/128 + E]
   w.nb_prefix = reinterpret_cast<int32_t*>(take((size_t)(Et + 1) * 4 + (size_t)(R / 128 + Et + 1) * 4));
   w.xh = reinterpret_cast<uint16_t*>(take((size_t)T * sh->d * 2));
+  w.w_split = (sh->k > 0 && router_uses_tc((int)T))
+                  ? reinterpret_cast<uint16_t*>(take(router_split_bytes((int)sh->E, (int)sh->d)))
+                  : nullptr;
   w.total = off;
   return w;
 }
@@ -255,7 +259,8 @@ bitmoe_status_t forward_impl(const uint16_t* x, const uint16_t* residual, int64_
   if (forced_ids) {
     e = launch_forced_select(forced_ids, forced_w, Ti, Et, kt, w.ids, w.w, w.st, s);
   } else {
-    e = k > 0 ? launch_router_logits(x, Ti, d, E, weights.w_router, weights.b_router, w.logits, s) : cudaSuccess;
+    e = k > 0 ? launch_router_logits(x, Ti, d, E, weights.w_router, weights.b_router, w.logits, w.w_split, w.st, s)
+              : cudaSuccess;
     if (e == cudaSuccess) e = launch_topk_gates(w.logits, Ti, E, k, shape->renormalize, ns, w.ids, w.w, s);
   }
   if (e == cudaSuccess)
@@ -381,7 +386,8 @@ bitmoe_status_t moe_route(const uint16_t* x, int64_t T, const bitmoe_moe_shape_t
   const MoeWs w = moe_layout(shape, T, workspace);
   cudaStream_t s = (cudaStream_t)stream;
   float* logits = logits_out ? logits_out : w.logits;
-  cudaError_t e = scored ? launch_router_logits(x, (int)T, (int)shape->d, (int)shape->E, w_router, b_router, logits, s)
+  cudaError_t e = scored ? launch_router_logits(x, (int)T, (int)shape->d, (int)shape->E, w_router, b_router, logits,
+                                              w.w_split, w.st, s)
                          : cudaSuccess;
   if (e == cudaSuccess)
     e = launch_topk_gates(logits, (int)T, (int)shape->E, (int)shape->k, shape->renormalize, (int)shape->n_shared,

@@ -120,6 +120,18 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+//
+// Every kernel of the layer's multi-kernel paths is launched with programmatic
+// stream serialization: it may be scheduled while the previous kernel on the stream
+// drains, and its first statement waits (griddepcontrol.wait) until that kernel has
+// completed and its writes are visible, then lets the next kernel be scheduled in
+// turn.  Results are those of plain stream order; the launch gaps overlap.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mma.sync m16n8k16
 
 __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
@@ -285,6 +297,23 @@ inline cudaError_t ensure_smem_attr(F* kernel, size_t bytes, int* max_set) {
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e == cudaSuccess) max_set[dev] = (int)bytes;
   return e;
+}
+
+// Launch with programmatic stream serialization (the kernel must start with pdl_enter()).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
 template <typename T>

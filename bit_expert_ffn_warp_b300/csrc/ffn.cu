@@ -215,6 +215,7 @@ __device__ __forceinline__ Blk block_info(const FfnArgs& p, int b) {
 
 template <bool kFp4>
 __global__ void __launch_bounds__(kPipeThreads, 1) ffn_up_kernel(FfnArgs p, int ns) {
+  pdl_enter();
   extern __shared__ __align__(128) unsigned char smem[];
   const int d = p.d, I = p.I;
   const int tbytes = (int)tile_bytes(d);
@@ -536,6 +537,7 @@ __device__ __forceinline__ void down_chunk_fp4(const unsigned char* cw, const un
 
 template <bool kFp4>
 __global__ void __launch_bounds__(kPipeThreads, 1) ffn_down_kernel(FfnArgs p, int ns) {
+  pdl_enter();
   extern __shared__ __align__(128) unsigned char smem[];
   const int d = p.d, I = p.I;
   const int tbytes = (int)tile_bytes(I);
@@ -700,10 +702,10 @@ cudaError_t launch_ffn_up(const FfnArgs& a, cudaStream_t s) {
   cudaError_t err;
   if (a.gate_ts != nullptr) {
     if ((err = ensure_smem_attr(ffn_up_kernel<true>, sm, attr_fp4)) != cudaSuccess) return err;
-    ffn_up_kernel<true><<<grid, kPipeThreads, sm, s>>>(a, ns);
+    if (cudaError_t e_ = launch_pdl(ffn_up_kernel<true>, dim3(grid), dim3(kPipeThreads), sm, s, a, ns)) return e_;
   } else {
     if ((err = ensure_smem_attr(ffn_up_kernel<false>, sm, attr_set)) != cudaSuccess) return err;
-    ffn_up_kernel<false><<<grid, kPipeThreads, sm, s>>>(a, ns);
+    if (cudaError_t e_ = launch_pdl(ffn_up_kernel<false>, dim3(grid), dim3(kPipeThreads), sm, s, a, ns)) return e_;
   }
   return cudaGetLastError();
 }
@@ -723,10 +725,10 @@ cudaError_t launch_ffn_down(const FfnArgs& a, cudaStream_t s) {
   cudaError_t err;
   if (a.down_ts != nullptr) {
     if ((err = ensure_smem_attr(ffn_down_kernel<true>, sm, attr_fp4)) != cudaSuccess) return err;
-    ffn_down_kernel<true><<<grid, kPipeThreads, sm, s>>>(a, ns);
+    if (cudaError_t e_ = launch_pdl(ffn_down_kernel<true>, dim3(grid), dim3(kPipeThreads), sm, s, a, ns)) return e_;
   } else {
     if ((err = ensure_smem_attr(ffn_down_kernel<false>, sm, attr_set)) != cudaSuccess) return err;
-    ffn_down_kernel<false><<<grid, kPipeThreads, sm, s>>>(a, ns);
+    if (cudaError_t e_ = launch_pdl(ffn_down_kernel<false>, dim3(grid), dim3(kPipeThreads), sm, s, a, ns)) return e_;
   }
   return cudaGetLastError();
 }

@@ -9,8 +9,16 @@
 namespace bitmoe {
 
 // ---------------------------------------------------------------- routing (route.cu)
+// Router logits.  From kRouterTcMinT tokens on the product runs on tcgen05 and needs
+// w_split (router_split_bytes: the router rows split into three bf16 parts per call);
+// with fewer tokens, or w_split null, the mma.sync kernels run.  st: status word for
+// the tcgen05 kernel's bounded waits.
+constexpr int kRouterTcMinT = 256;
+bool router_uses_tc(int T);
+size_t router_split_bytes(int E, int d);
 cudaError_t launch_router_logits(const uint16_t* x, int T, int d, int E, const float* w_router,
-                                 const float* b_router, float* logits, cudaStream_t s);
+                                 const float* b_router, float* logits, uint16_t* w_split, DevStatus* st,
+                                 cudaStream_t s);
 // ids / w rows of k + n_shared entries: the k routed experts, then (n_shared = 1)
 // the shared expert, bank entry E, with weight 1.
 cudaError_t launch_topk_gates(const float* logits, int T, int E, int k, int renorm, int n_shared, int32_t* ids,

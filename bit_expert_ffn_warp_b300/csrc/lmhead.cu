@@ -86,6 +86,7 @@ static_assert(LmSmem::kFail + 4 <= LmSmem::kX, "lm head smem header");
 // multiplies the logit); else int4 with fp16 group scales applied per group.
 template <int NT, bool kFp4>
 __global__ void __launch_bounds__(kLmThreads, 1) lmhead_kernel(LmArgs p) {
+  pdl_enter();
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + LmSmem::kBars);
   uint64_t* empty = full + kLmMaxStages;
@@ -359,6 +360,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_kernel(LmArgs p) {
 }
 
 __global__ void argmax_finalize_kernel(const unsigned long long* keys, int T, int32_t* argmax) {
+  pdl_enter();
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t < T) argmax[t] = (int32_t)(0xffffffffu - (uint32_t)(keys[t] & 0xffffffffull));
 }
@@ -414,14 +416,14 @@ cudaError_t launch_lmhead_fmt(const uint16_t* h, int T, int d, int V, const uint
     a.logits = logits;
     a.keys = keys;
     a.st = st;
-    if (nt == 1)
-      lmhead_kernel<1, kFp4><<<grid, kLmThreads, lm_smem(d, a.ntok), s>>>(a);
-    else
-      lmhead_kernel<2, kFp4><<<grid, kLmThreads, lm_smem(d, a.ntok), s>>>(a);
+    auto* kern = (nt == 1) ? lmhead_kernel<1, kFp4> : lmhead_kernel<2, kFp4>;
+    const cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kLmThreads), lm_smem(d, a.ntok), s, a);
+    if (e != cudaSuccess) return e;
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
-  argmax_finalize_kernel<<<ceil_div(T, 128), 128, 0, s>>>(keys, T, argmax);
+  if (cudaError_t e_ = launch_pdl(argmax_finalize_kernel, dim3(ceil_div(T, 128)), dim3(128), 0, s, keys, T,
+                                  argmax)) return e_;
   return cudaGetLastError();
 }
 

@@ -9,6 +9,7 @@ namespace {
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ inv,
                                                       const float* __restrict__ w, const uint16_t* resid, int d, int k,
                                                       uint16_t* out, float* __restrict__ out_f32) {
+  pdl_enter();
   const int t = blockIdx.y;
   for (int c8 = (blockIdx.x * blockDim.x + threadIdx.x) * 8; c8 < d; c8 += gridDim.x * blockDim.x * 8) {
     // the residual, then each batch of 8 rows' positions and gates, then their y
@@ -66,6 +67,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 __global__ void __launch_bounds__(256) combine_f16_kernel(const __half* __restrict__ y, const int32_t* __restrict__ inv,
                                                           const float* __restrict__ w, const uint16_t* resid, int d,
                                                           int k, uint16_t* out, float* __restrict__ out_f32) {
+  pdl_enter();
   const int t = blockIdx.y;
   for (int c8 = (blockIdx.x * blockDim.x + threadIdx.x) * 8; c8 < d; c8 += gridDim.x * blockDim.x * 8) {
     // as combine_kernel: residual, positions and gates, then y pieces requested together
@@ -115,6 +117,7 @@ __global__ void __launch_bounds__(256) combine_f16_kernel(const __half* __restri
 
 // y = x / sqrt(mean(x^2) + eps) with unit gain; fp32 sums in a fixed tree order.
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t* x, int d, float eps, uint16_t* y) {
+  pdl_enter();
   __shared__ float part[8];
   const int t = blockIdx.x;
   const uint16_t* xr = x + (size_t)t * d;
@@ -236,8 +239,10 @@ cudaError_t launch_combine(const float* y_rows, const int32_t* inv, const float*
   for (int t0 = 0; t0 < T; t0 += 65535) {
     const int n = T - t0 < 65535 ? T - t0 : 65535;
     const size_t o = (size_t)t0 * d;
-    combine_kernel<<<dim3(ceil_div(d, 512), n), 64, 0, s>>>(y_rows, inv + (size_t)t0 * k, w + (size_t)t0 * k,
-                                                             resid + o, d, k, out + o, out_f32 ? out_f32 + o : nullptr);
+    const cudaError_t e = launch_pdl(combine_kernel, dim3(ceil_div(d, 512), n), dim3(64), 0, s, y_rows,
+                                     inv + (size_t)t0 * k, w + (size_t)t0 * k, resid + o, d, k, out + o,
+                                     out_f32 ? out_f32 + o : nullptr);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
@@ -248,16 +253,17 @@ cudaError_t launch_combine_f16(const __half* y_rows, const int32_t* inv, const f
   for (int t0 = 0; t0 < T; t0 += 65535) {
     const int n = T - t0 < 65535 ? T - t0 : 65535;
     const size_t o = (size_t)t0 * d;
-    combine_f16_kernel<<<dim3(ceil_div(d, 512), n), 64, 0, s>>>(y_rows, inv + (size_t)t0 * k, w + (size_t)t0 * k,
-                                                                 resid + o, d, k, out + o,
-                                                                 out_f32 ? out_f32 + o : nullptr);
+    const cudaError_t e = launch_pdl(combine_f16_kernel, dim3(ceil_div(d, 512), n), dim3(64), 0, s, y_rows,
+                                     inv + (size_t)t0 * k, w + (size_t)t0 * k, resid + o, d, k, out + o,
+                                     out_f32 ? out_f32 + o : nullptr);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_rmsnorm(const uint16_t* x, int T, int d, float eps, uint16_t* y, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  rmsnorm_kernel<<<T, 256, 0, s>>>(x, d, eps, y);
+  if (cudaError_t e_ = launch_pdl(rmsnorm_kernel, dim3(T), dim3(256), 0, s, x, d, eps, y)) return e_;
   return cudaGetLastError();
 }
 

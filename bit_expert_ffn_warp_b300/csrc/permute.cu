@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_single_kernel(const int3
                                                                       int32_t* __restrict__ inv,
                                                                       int32_t* __restrict__ blk_prefix,
                                                                       DevStatus* st) {
+  pdl_enter();
   extern __shared__ __align__(16) unsigned char smem[];
   int* cursor = reinterpret_cast<int*>(smem);           // [2E]
   int* hist = cursor + 2 * E;                           // [E]
@@ -128,6 +129,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_single_kernel(const int3
 // Multi-CTA path: per-chunk histograms, one scan CTA, per-chunk placement.
 __global__ void __launch_bounds__(kPermThreads) permute_hist_kernel(const int32_t* __restrict__ ids, int R, int E,
                                                                     int32_t* __restrict__ chunk_hist) {
+  pdl_enter();
   extern __shared__ __align__(16) unsigned char smem[];
   int* hist = reinterpret_cast<int*>(smem);
   const int tid = threadIdx.x;
@@ -145,6 +147,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_hist_kernel(const int32_
 __global__ void __launch_bounds__(kPermThreads) permute_scan_kernel(int32_t* __restrict__ chunk_hist, int nchunks,
                                                                     int E, int32_t* __restrict__ offsets,
                                                                     int32_t* __restrict__ blk_prefix) {
+  pdl_enter();
   __shared__ int warp_tot[34];
   const int tid = threadIdx.x;
   int tot = 0;
@@ -171,6 +174,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_place_kernel(const int32
                                                                      const int32_t* __restrict__ chunk_base,
                                                                      int32_t* __restrict__ sorted_rows,
                                                                      int32_t* __restrict__ inv, DevStatus* st) {
+  pdl_enter();
   extern __shared__ __align__(16) unsigned char smem[];
   int* cursor = reinterpret_cast<int*>(smem);                 // [2E]
   uint16_t* cnt = reinterpret_cast<uint16_t*>(cursor + 2 * E);  // [32][E]
@@ -180,6 +184,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_place_kernel(const int32
 }
 
 __global__ void blk_prefix_kernel(const int32_t* __restrict__ offsets, int E, int32_t* __restrict__ blk_prefix) {
+  pdl_enter();
   __shared__ int warp_tot[34];
   const int tid = threadIdx.x;
   const int nb = tid < E ? ceil_div(offsets[tid + 1] - offsets[tid], kTokBlock) : 0;
@@ -207,23 +212,28 @@ cudaError_t launch_permute(const int32_t* ids, int R, int E, int32_t* offsets, i
     static int attr_set[64] = {};
     cudaError_t err = ensure_smem_attr(permute_single_kernel, sm, attr_set);
     if (err != cudaSuccess) return err;
-    permute_single_kernel<<<1, kPermThreads, sm, s>>>(ids, R, E, offsets, sorted_rows, inv, blk_prefix, st);
+    if (cudaError_t e_ = launch_pdl(permute_single_kernel, dim3(1), dim3(kPermThreads), sm, s, ids, R, E, offsets,
+                                    sorted_rows, inv, blk_prefix, st)) return e_;
     return cudaGetLastError();
   }
   const int nchunks = ceil_div(R, kPermChunk);
   int32_t* chunk_hist = static_cast<int32_t*>(scratch);
-  permute_hist_kernel<<<nchunks, kPermThreads, (size_t)E * 4, s>>>(ids, R, E, chunk_hist);
-  permute_scan_kernel<<<1, kPermThreads, 0, s>>>(chunk_hist, nchunks, E, offsets, blk_prefix);
+  if (cudaError_t e_ = launch_pdl(permute_hist_kernel, dim3(nchunks), dim3(kPermThreads), (size_t)E * 4, s, ids, R, E,
+                                  chunk_hist)) return e_;
+  if (cudaError_t e_ = launch_pdl(permute_scan_kernel, dim3(1), dim3(kPermThreads), 0, s, chunk_hist, nchunks, E,
+                                  offsets, blk_prefix)) return e_;
   const size_t sm = place_smem(E);
   static int attr_set[64] = {};
   cudaError_t err = ensure_smem_attr(permute_place_kernel, sm, attr_set);
   if (err != cudaSuccess) return err;
-  permute_place_kernel<<<nchunks, kPermThreads, sm, s>>>(ids, R, E, chunk_hist, sorted_rows, inv, st);
+  if (cudaError_t e_ = launch_pdl(permute_place_kernel, dim3(nchunks), dim3(kPermThreads), sm, s, ids, R, E, chunk_hist,
+                                  sorted_rows, inv, st)) return e_;
   return cudaGetLastError();
 }
 
 cudaError_t launch_blk_prefix(const int32_t* offsets, int E, int32_t* blk_prefix, cudaStream_t s) {
-  blk_prefix_kernel<<<1, kPermThreads, 0, s>>>(offsets, E, blk_prefix);
+  if (cudaError_t e_ = launch_pdl(blk_prefix_kernel, dim3(1), dim3(kPermThreads), 0, s, offsets, E,
+                                  blk_prefix)) return e_;
   return cudaGetLastError();
 }
 

@@ -35,6 +35,7 @@
 #include <cuda.h>
 
 #include "kernels.h"
+#include "tc.cuh"
 
 namespace bitmoe {
 namespace {
@@ -74,47 +75,6 @@ struct PrefillArgs {
 // tiles' N.
 __device__ __forceinline__ void ptrace(const PrefillArgs& p, int slot, unsigned long long v) {
   if (p.trace) p.trace[blockIdx.x * 16 + slot] = v;
-}
-
-// ---------------------------------------------------------------- tcgen05 helpers
-
-__device__ __forceinline__ uint64_t umma_smem_desc(uint32_t saddr) {
-  // K-major, 128-byte swizzle: 8-row atoms of 1024 bytes (SBO), version 1.
-  uint64_t desc = 0;
-  desc |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
-  desc |= (uint64_t)1 << 16;                     // leading byte offset (unused when swizzled)
-  desc |= (uint64_t)(1024 >> 4) << 32;           // stride byte offset
-  desc |= (uint64_t)1 << 46;                     // descriptor version
-  desc |= (uint64_t)2 << 61;                     // SWIZZLE_128B
-  return desc;
-}
-
-__host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N) {
-  // kind::f16: D fp32 (bits 4-5 = 1), A fp16, B fp16 (0), K-major both, N>>3 at 17, M>>4 at 24.
-  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// 16 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
-
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-__device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ int expert_of(const int32_t* __restrict__ pre, int E, int b) {
@@ -240,6 +200,7 @@ __device__ __forceinline__ void dq_word(uint32_t w, uint32_t scale_bits, uint32_
 
 template <bool kFp4>
 __global__ void __launch_bounds__(kQThreads, 1) prefill_wa_kernel(const __grid_constant__ PrefillArgs p) {
+  pdl_enter();
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   if ((smem_u32(smem_raw) & 1023u) != 0) {  // the swizzled B tiles need a 1024-byte aligned base
     if (threadIdx.x == 0) record_status(p.st, kStatusCheck, 80, (int)(smem_u32(smem_raw) & 1023u));
@@ -585,6 +546,7 @@ __global__ void __launch_bounds__(kQThreads, 1) prefill_wa_kernel(const __grid_c
 // threads, one expert per thread (E <= 1024).
 __global__ void __launch_bounds__(1024) block_list_kernel(const int32_t* __restrict__ offsets, int E,
                                                           int32_t* __restrict__ pre, int32_t* __restrict__ list) {
+  pdl_enter();
   __shared__ int scan[1024];
   __shared__ int cnt[17], fill[17];
   const int e = threadIdx.x;
@@ -629,6 +591,7 @@ __global__ void __launch_bounds__(1024) block_list_kernel(const int32_t* __restr
 // at 4c and at 4c + 16.
 __global__ void gather_f16_perm_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_rows,
                                        int R, int k, int d, __half* __restrict__ xs) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   for (int pos = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; pos < R; pos += warps) {
@@ -650,29 +613,6 @@ __global__ void gather_f16_perm_kernel(const uint16_t* __restrict__ x, const int
   }
 }
 
-// Tensor map of a row-major [rows, K] fp16 matrix for 64 x 16 boxes with 128-byte swizzle.
-cudaError_t encode_rows_map(CUtensorMap* map, const void* base, int rows, int K) {
-  using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-  static EncodeFn encode = nullptr;
-  if (encode == nullptr) {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) return cudaErrorNotSupported;
-    encode = reinterpret_cast<EncodeFn>(fn);
-  }
-  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kPK, (cuuint32_t)kBoxRows};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 int sm_count_prefill() {
   static int cnt[64] = {};
   int dev = 0;
@@ -691,14 +631,17 @@ cudaError_t launch_prefill_ffn(const FfnArgs& a, int32_t* nb_prefix, __half* xs,
   if (R == 0) return cudaSuccess;
   if (!prefill_eligible(a.d, a.I)) return cudaErrorNotSupported;
   PrefillArgs p1 = {};
-  cudaError_t err = encode_rows_map(&p1.tmap_a, xs, R, a.d);
+  cudaError_t err = encode_rows_map(&p1.tmap_a, xs, R, a.d, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, kPK, kBoxRows);
   if (err != cudaSuccess) return err;
   PrefillArgs p2 = {};
-  if ((err = encode_rows_map(&p2.tmap_a, a.h_hi, R, a.I)) != cudaSuccess) return err;
+  err = encode_rows_map(&p2.tmap_a, a.h_hi, R, a.I, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, kPK, kBoxRows);
+  if (err != cudaSuccess) return err;
   int32_t* pair_list = nb_prefix + a.E + 1;  // [R/128 + E] entries after the prefix
-  block_list_kernel<<<1, 1024, 0, s>>>(a.offsets, a.E, nb_prefix, pair_list);
+  if (cudaError_t e_ = launch_pdl(block_list_kernel, dim3(1), dim3(1024), 0, s, a.offsets, a.E, nb_prefix,
+                                  pair_list)) return e_;
   const int gw = (R + 7) / 8;  // blocks of 8 warps
-  gather_f16_perm_kernel<<<gw < 148 * 8 ? gw : 148 * 8, 256, 0, s>>>(a.x, a.sorted_rows, R, a.k, a.d, xs);
+  if (cudaError_t e_ = launch_pdl(gather_f16_perm_kernel, dim3(gw < 148 * 8 ? gw : 148 * 8), dim3(256), 0, s, a.x,
+                                  a.sorted_rows, R, a.k, a.d, xs)) return e_;
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   const bool fp4 = a.gate_ts != nullptr;
   static int attr1[64] = {}, attr_fp4[64] = {};
@@ -732,7 +675,7 @@ cudaError_t launch_prefill_ffn(const FfnArgs& a, int32_t* nb_prefix, __half* xs,
   p1.st = a.st;
   p1.trace = tr;
   const long g1 = blocks * p1.FB;
-  kern<<<(int)(g1 < G ? g1 : G), kQThreads, kQSmem, s>>>(p1);
+  if (cudaError_t e_ = launch_pdl(kern, dim3((int)(g1 < G ? g1 : G)), dim3(kQThreads), kQSmem, s, p1)) return e_;
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
   p2.mode = 2;
@@ -757,7 +700,7 @@ cudaError_t launch_prefill_ffn(const FfnArgs& a, int32_t* nb_prefix, __half* xs,
   p2.st = a.st;
   p2.trace = tr ? tr + (size_t)G * 16 : nullptr;
   const long g2 = blocks * p2.FB;
-  kern<<<(int)(g2 < G ? g2 : G), kQThreads, kQSmem, s>>>(p2);
+  if (cudaError_t e_ = launch_pdl(kern, dim3((int)(g2 < G ? g2 : G)), dim3(kQThreads), kQSmem, s, p2)) return e_;
   return cudaGetLastError();
 }
 

@@ -150,6 +150,26 @@ def test_route_parity(T, bias):
     assert np.allclose(w.cpu().numpy()[ok], w_ref[ok], rtol=2e-5, atol=1e-6)
 
 
+@pytest.mark.parametrize("T,E,d", [(256, 64, 128), (260, 80, 256), (1000, 200, 384)])
+def test_route_many_tokens_ragged(T, E, d):
+    """The tcgen05 router (256 tokens and more) on shapes whose tokens fill no whole
+    128-token tile and whose experts fill no whole 64-expert tile: every logit within
+    2e-5 of the fp64 oracle, ids exact outside near-ties."""
+    tensors = layer_tensors(40 + T, d, E, 128, bias="normal")
+    lay = device_layer(tensors, 4)
+    x_bits = synth.activations(7 + T, T, d)
+    ids_ref, w_ref, l_ref, gap = oracle.route(x_bits, tensors["w_router"], tensors["b_router"], 4)
+    ws = bm.moe_workspace(lay, T)
+    ids, w, logits = bm.moe_route(torch_bf16_from_bits(x_bits), lay, ws, want_logits=True)
+    torch.cuda.synchronize()
+    assert bm.bitmoe_get_device_status(ws) == 0
+    l = logits.cpu().numpy().astype(np.float64)
+    assert max_abs(l, l_ref) < 2e-5
+    ok = gap >= NEAR_TIE
+    assert np.array_equal(ids.cpu().numpy()[ok], ids_ref[ok])
+    assert np.allclose(w.cpu().numpy()[ok], w_ref[ok], rtol=2e-5, atol=1e-6)
+
+
 def tie_layer(E, d, tied, top_bias=20.0, seed=3):
     """A router whose logits are l_e = x_e + b_e exactly (W_r is the identity on the
     first E columns), with the experts in `tied` sharing one bias well above the
