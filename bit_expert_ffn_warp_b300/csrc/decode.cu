@@ -553,6 +553,9 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& p, const LayerPtrs
   const int RT = I / kTileRows, CT = d / kTileRows;
   const int xstride = 2 * d + kSmemRowPad;
   const int NS = p.nstages;
+  // threads per output element in the combine: up to 8 (a power of two), all elements at once
+  int cpe = 8;
+  while (cpe > 1 && T * kTileRows * cpe > kConsumers) cpe >>= 1;
 
   Routing rt;
   {
@@ -635,8 +638,12 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& p, const LayerPtrs
   stamp(trace, 1);
   // residual of this CTA's first output tile, read now so that its latency is
   // off the combine at the end (one value per combine thread)
+  // (the combine gives each output element cpe threads; the first of them adds the residual)
   uint16_t resid0 = 0;
-  if (tid < T * kTileRows && cta < CT) resid0 = p.resid[(size_t)(tid >> 4) * d + (size_t)cta * kTileRows + (tid & 15)];
+  if (tid % cpe == 0 && tid / cpe < T * kTileRows && cta < CT) {
+    const int el = tid / cpe;
+    resid0 = p.resid[(size_t)(el >> 4) * d + (size_t)cta * kTileRows + (el & 15)];
+  }
   if (tid == 0) {  // the layer's input rows (later layers: written by the combines before barrier C)
     if (l > 0) {
       asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -1248,24 +1255,34 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& p, const LayerPtrs
     if (!ok) *(volatile int*)fail = 1;
     consumer_sync();
     stamp(trace, 14);
-    // combine: out[t, ct*16 + col] = resid + sum_j w_j * y_j (ascending j)
-    if (tid < T * kTileRows) {
-      const int t = tid >> 4, col = tid & 15;
+    // combine: out[t, ct*16 + col] = resid + sum_j w_j * y_j.  cpe neighbouring threads
+    // share an output element: thread `sub` sums rows j = sub, sub + cpe, ... in
+    // ascending order, then a fixed shuffle tree adds the cpe partial sums (no serial
+    // chain of k dependent shared-memory round trips)
+    {
+      const int el = tid / cpe, sub = tid % cpe;
+      const bool mine = el < T * kTileRows;
+      const int t = el >> 4, col = el & 15;
       float acc = 0.f;
-      for (int j = 0; j < k; ++j) {
-        const int ps = rt.pos[t * k + j];
-        if (ps >= 0) {
-          float y = 0.f;
+      if (mine) {
+        for (int j = sub; j < k; j += cpe) {
+          const int ps = rt.pos[t * k + j];
+          if (ps >= 0) {
+            float y = 0.f;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) y += ypart[((size_t)q * R + ps) * kTileRows + col];
-          acc = fmaf(rt.w[t * k + j], y, acc);
+            for (int q = 0; q < 4; ++q) y += ypart[((size_t)q * R + ps) * kTileRows + col];
+            acc = fmaf(rt.w[t * k + j], y, acc);
+          }
         }
       }
-      const size_t o = (size_t)t * d + (size_t)ct * kTileRows + col;
-      const float v = bf16_bits_to_float(ct == cta ? resid0 : p.resid[o]) + acc;
-      if (*(volatile int*)fail == 0) {
-        if (p.out_f32) p.out_f32[o] = v;
-        p.out[o] = float_to_bf16_bits(v);
+      for (int off = 1; off < cpe; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (mine && sub == 0) {
+        const size_t o = (size_t)t * d + (size_t)ct * kTileRows + col;
+        const float v = bf16_bits_to_float(ct == cta ? resid0 : p.resid[o]) + acc;
+        if (*(volatile int*)fail == 0) {
+          if (p.out_f32) p.out_f32[o] = v;
+          p.out[o] = float_to_bf16_bits(v);
+        }
       }
     }
     consumer_sync();

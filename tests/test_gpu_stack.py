@@ -91,7 +91,7 @@ def check_layer(l, resid_in, xh_gpu, o32, ids_gpu):
     return near
 
 
-@pytest.mark.parametrize("T,checked", [(1, list(range(N_LAYERS))), (16, [0, 1, 24, 47, 48])])
+@pytest.mark.parametrize("T,checked", [(1, list(range(N_LAYERS))), (16, list(range(N_LAYERS)))])
 def test_stack_teacher_forced_and_lm_head(T, checked):
     x0 = synth.activations(SEED, T, D, step=T)
     rec, xh_final, am = run_stack(x0)
