@@ -28,6 +28,12 @@ constexpr int kMaxK = 32;
 constexpr int kStatusTimeout = BITMOE_ERR_TIMEOUT;
 constexpr int kStatusCheck = BITMOE_ERR_DEVICE_CHECK;
 
+// fp16 range: a value of this magnitude or more rounds to infinity (round to nearest).
+// The expert intermediates h that the projections carry in fp16 (hi + lo pairs on the
+// exact paths, one fp16 on the grouped-GEMM path, which also keeps y in fp16) must stay
+// below it; a larger one, or a NaN, records kStatusCheck instead of passing silently.
+constexpr float kF16Overflow = 65520.0f;
+
 // A bounded wait gives up after this long and records kStatusTimeout.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 

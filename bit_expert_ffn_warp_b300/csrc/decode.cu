@@ -1105,6 +1105,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& p, const LayerPtrs
         const __half hi = __float2half_rn(h);
         const __half lo = __float2half_rn(h - __half2float(hi));
         const size_t o = (size_t)(rt.act_off[a] + tok) * I + r16 * kTileRows + row;
+        if (!(fabsf(h) < kF16Overflow)) record_status(p.st, kStatusCheck, 46, (int)o);
         p.h_hi[o] = hi;
         p.h_lo[o] = lo;
       }

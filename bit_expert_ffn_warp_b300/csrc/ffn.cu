@@ -443,6 +443,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) ffn_up_kernel(FfnArgs p, int 
         const __half hi = __float2half_rn(h);
         const __half lo = __float2half_rn(h - __half2float(hi));
         const size_t o = (size_t)(k.p0 + tok) * I + rt * kTileRows + row;
+        if (!(fabsf(h) < kF16Overflow)) record_status(p.st, kStatusCheck, 17, (int)o);
         p.h_hi[o] = hi;
         p.h_lo[o] = lo;
       }

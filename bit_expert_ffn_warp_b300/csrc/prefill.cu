@@ -473,17 +473,25 @@ __global__ void __launch_bounds__(kQThreads, 1) prefill_wa_kernel(const __grid_c
         tmem_ld_wait();
         if (p.mode == 1) {  // h = silu(gate) * up of feature f, in the K order GEMM 2 reads
           __half* hs = reinterpret_cast<__half*>(stg);
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            hs[(n0 + i) * 32 + pos] =
-                __float2half_rn(silu_mul_fast(__uint_as_float(d0[i]) * ta, __uint_as_float(d1[i]) * tb));
-        } else if (!f32out) {
-          __half* ys = reinterpret_cast<__half*>(stg);
+          bool over = false;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            ys[(n0 + i) * 32 + pos] = __float2half_rn(__uint_as_float(d0[i]) * ta);
-            ys[(128 + n0 + i) * 32 + pos] = __float2half_rn(__uint_as_float(d1[i]) * ta);
+            const float h = silu_mul_fast(__uint_as_float(d0[i]) * ta, __uint_as_float(d1[i]) * tb);
+            over |= !(fabsf(h) < kF16Overflow);
+            hs[(n0 + i) * 32 + pos] = __float2half_rn(h);
           }
+          if (over) record_status(p.st, kStatusCheck, 90, ti.p0 + n0);
+        } else if (!f32out) {
+          __half* ys = reinterpret_cast<__half*>(stg);
+          bool over = false;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float y0 = __uint_as_float(d0[i]) * ta, y1 = __uint_as_float(d1[i]) * ta;
+            over |= !(fabsf(y0) < kF16Overflow && fabsf(y1) < kF16Overflow);
+            ys[(n0 + i) * 32 + pos] = __float2half_rn(y0);
+            ys[(128 + n0 + i) * 32 + pos] = __float2half_rn(y1);
+          }
+          if (over) record_status(p.st, kStatusCheck, 91, ti.p0 + n0);
         } else {
           float* ys = reinterpret_cast<float*>(stg);
 #pragma unroll

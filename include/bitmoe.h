@@ -56,7 +56,9 @@ typedef enum bitmoe_status {
   BITMOE_ERR_WORKSPACE = 3,    /* workspace missing or smaller than *_workspace_size() */
   BITMOE_ERR_CUDA = 4,         /* a launch failed; bitmoe_last_cuda_error() has the code */
   BITMOE_ERR_TIMEOUT = 5,      /* device status: a bounded wait ran out */
-  BITMOE_ERR_DEVICE_CHECK = 6  /* device status: an input failed a device-side check */
+  BITMOE_ERR_DEVICE_CHECK = 6  /* device status: an input failed a device-side check (an
+                                  out-of-range or repeated forced expert id, or an expert
+                                  intermediate outside the fp16 range, see moe_forward) */
 } bitmoe_status_t;
 
 /* Shape of one MoE layer.  d: hidden size; E: routed experts; k: routed
@@ -267,6 +269,11 @@ bitmoe_status_t moe_combine(const float* y_rows, const int32_t* inv_rows, const 
  * not x.  Batches of T <= 8 tokens run one fused decode kernel, other batches
  * with T*k < 512 routed rows the streaming kernels (both exact int4 x bf16 with
  * fp32 sums); T*k >= 512 runs the tcgen05 grouped GEMM (fp16 operands).
+ * The projections carry the SwiGLU output h in fp16 (an exact hi + lo pair on the
+ * fused and streaming paths, one fp16 value on the grouped-GEMM path, which keeps the
+ * y rows in fp16 too): an h (or grouped-GEMM y) of magnitude 65520 or more, or a NaN,
+ * cannot be represented and flags BITMOE_ERR_DEVICE_CHECK in the device status word
+ * (inputs of the scale of a normalised residual stay far below it).
  * The fused decode kernel is one persistent launch of one CTA per SM whose
  * CTAs wait on each other; it runs only where the occupancy query says every
  * CTA of the grid can be resident at once (else the call takes the unfused

@@ -170,6 +170,24 @@ def test_route_many_tokens_ragged(T, E, d):
     assert np.allclose(w.cpu().numpy()[ok], w_ref[ok], rtol=2e-5, atol=1e-6)
 
 
+@pytest.mark.parametrize("T", [1, 16, 100])
+def test_intermediate_outside_fp16_range_is_flagged(T):
+    """Tokens 1000 times the workload's scale drive the SwiGLU output h far past the
+    fp16 range the projections carry it in: the fused (T = 1), streaming (T = 16) and
+    grouped-GEMM (T = 100) paths each report BITMOE_ERR_DEVICE_CHECK instead of
+    returning infinities silently; the status clears and the next normal step is clean."""
+    tensors, lay = flint_layer("normal")
+    big = 1000.0 * oracle.bf16_to_f64(synth.activations(300 + T, T, FLINT["d"]))
+    x = torch_bf16_from_bits(synth.f64_to_bf16_bits(big))
+    ws = bm.moe_workspace(lay, T)
+    bm.moe_forward(x, lay, ws)
+    torch.cuda.synchronize()
+    assert bm.bitmoe_get_device_status(ws, clear=True) == bm.ERR_DEVICE_CHECK
+    bm.moe_forward(torch_bf16_from_bits(synth.activations(300 + T, T, FLINT["d"])), lay, ws)
+    torch.cuda.synchronize()
+    assert bm.bitmoe_get_device_status(ws) == 0
+
+
 def tie_layer(E, d, tied, top_bias=20.0, seed=3):
     """A router whose logits are l_e = x_e + b_e exactly (W_r is the identity on the
     first E columns), with the experts in `tied` sharing one bias well above the
