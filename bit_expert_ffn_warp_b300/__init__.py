@@ -28,6 +28,9 @@ _lib = ctypes.CDLL(LIB_PATH)
 OK = 0
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE", 4: "CUDA", 5: "TIMEOUT",
                 6: "DEVICE_CHECK"}
+ERR_INVALID_ARG = 1
+ERR_UNSUPPORTED = 2
+ERR_WORKSPACE = 3
 ERR_TIMEOUT = 5
 ERR_DEVICE_CHECK = 6
 GROUP = 32
@@ -58,6 +61,16 @@ class MoeWeightsNvfp4(ctypes.Structure):
 
 
 FP4_BLOCK = 16
+
+
+class AttnShape(ctypes.Structure):
+    _fields_ = [("d", ctypes.c_int64), ("n_q_heads", ctypes.c_int64), ("n_kv_heads", ctypes.c_int64),
+                ("head_dim", ctypes.c_int64), ("max_len", ctypes.c_int64), ("window", ctypes.c_int64),
+                ("rope", ctypes.c_int32), ("eps", ctypes.c_float), ("rope_theta", ctypes.c_double)]
+
+
+class AttnWeights(ctypes.Structure):
+    _fields_ = [("wqkv", ctypes.c_void_p), ("wo", ctypes.c_void_p), ("sinks", ctypes.c_void_p)]
 
 
 _P = ctypes.c_void_p
@@ -96,6 +109,9 @@ _SIGS = {
     "lmhead_static_scratch_bytes": (_SZ, []),
     "lmhead_int4_gemv_static": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _P, _P, _P, _P]),
     "bitmoe_rmsnorm": (ctypes.c_int, [_P, _I64, _I64, ctypes.c_float, _P, _P]),
+    "attn_workspace_size": (_SZ, [ctypes.POINTER(AttnShape)]),
+    "attn_decode_step": (ctypes.c_int, [_P, _P, _I64, ctypes.POINTER(AttnShape), ctypes.POINTER(AttnWeights), _P,
+                                        _P, _P, _P, _P, _SZ, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -510,4 +526,71 @@ def bitmoe_rmsnorm(x, eps: float = 1e-6, out=None):
     _need(x, torch.bfloat16, (T, d), "x")
     out = torch.empty_like(x) if out is None else out
     _check("bitmoe_rmsnorm", _lib.bitmoe_rmsnorm(_ptr(x), T, d, eps, _ptr(out), _stream()))
+    return out
+
+
+# ------------------------------------------------------------------ attention decode step
+
+@dataclass
+class AttnLayer:
+    """Device-resident weights of one attention layer: the packed int4 banks of the stacked
+    q | k | v projection [(nq + 2 nkv) * 128, d] and of the output projection [d, nq * 128],
+    the fp32 sink logits [nq] (or None), and the layer's kind (window 0 = whole context,
+    rope 0 / 1)."""
+    d: int
+    n_q: int
+    n_kv: int
+    wqkv: torch.Tensor
+    wo: torch.Tensor
+    sinks: torch.Tensor | None
+    window: int = 513
+    rope: bool = True
+    eps: float = 1e-6
+    theta: float = 1.0e6
+
+    def shape(self, max_len: int) -> AttnShape:
+        return AttnShape(self.d, self.n_q, self.n_kv, 128, int(max_len), int(self.window), int(self.rope),
+                         float(self.eps), float(self.theta))
+
+    @property
+    def weights(self) -> AttnWeights:
+        return AttnWeights(self.wqkv.data_ptr(), self.wo.data_ptr(),
+                           None if self.sinks is None else self.sinks.data_ptr())
+
+    @classmethod
+    def from_canonical(cls, t: dict, d: int, n_q: int, n_kv: int, window: int = 513, rope: bool = True,
+                       device="cuda") -> "AttnLayer":
+        """t: numpy canonical banks wqkv_q / wqkv_s, wo_q / wo_s (int4 bytes, fp16 scale bits)
+        and sinks (fp32 or None)."""
+        def pack(q, sc):
+            return bitmoe_pack_int4(torch.from_numpy(q).to(device), torch.from_numpy(sc.view("float16")).to(device))
+        sinks = None if t.get("sinks") is None else torch.from_numpy(t["sinks"].astype("float32")).to(device)
+        return cls(d, n_q, n_kv, pack(t["wqkv_q"], t["wqkv_s"]), pack(t["wo_q"], t["wo_s"]), sinks, window, rope)
+
+
+def attn_workspace(layer: AttnLayer, max_len: int) -> torch.Tensor:
+    n = int(_lib.attn_workspace_size(ctypes.byref(layer.shape(max_len))))
+    if n == 0:
+        raise BitmoeError("attn_workspace_size", ERR_UNSUPPORTED)
+    return torch.zeros(n, dtype=torch.uint8, device="cuda")
+
+
+def attn_decode_step(x, residual, pos: int, layer: AttnLayer, k_cache, v_cache, workspace, out=None, out_f32=None):
+    """One token: x, residual [d] bf16; caches [max_len, n_kv, 128] bf16 (row pos is written).
+    Returns out [d] bf16."""
+    d = layer.d
+    _need(x, torch.bfloat16, (d,), "x")
+    _need(residual, torch.bfloat16, (d,), "residual")
+    _need(k_cache, torch.bfloat16, None, "k_cache")
+    _need(v_cache, torch.bfloat16, tuple(k_cache.shape), "v_cache")
+    if k_cache.dim() != 3 or k_cache.shape[1] != layer.n_kv or k_cache.shape[2] != 128:
+        raise ValueError("caches must be [max_len, n_kv, 128]")
+    if out is None:
+        out = torch.empty(d, dtype=torch.bfloat16, device="cuda")
+    sh = layer.shape(k_cache.shape[0])
+    wts = layer.weights
+    _check("attn_decode_step",
+           _lib.attn_decode_step(_ptr(x), _ptr(residual), int(pos), ctypes.byref(sh), ctypes.byref(wts),
+                                 _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(out_f32), _ptr(workspace),
+                                 workspace.numel(), _stream()))
     return out

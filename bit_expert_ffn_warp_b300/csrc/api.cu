@@ -300,6 +300,58 @@ bitmoe_status_t expert_ffn_impl(const uint16_t* x, int64_t T, const bitmoe_moe_s
 
 }  // namespace
 
+namespace {
+
+// Workspace carve-up of the attention decode step.
+struct AttnWs {
+  DevStatus* st;
+  void* keys;
+  int32_t* am;
+  float* qkv;
+  float* q;
+  float* part;
+  uint16_t* attn;
+  float* y;
+  size_t total;
+};
+
+bitmoe_status_t check_attn_shape(const bitmoe_attn_shape_t* sh) {
+  if (sh == nullptr || sh->d <= 0 || sh->n_q_heads <= 0 || sh->n_kv_heads <= 0 || sh->max_len <= 0 ||
+      sh->window < 0 || !(sh->eps >= 0.f) || (sh->rope && !(sh->rope_theta > 0.0)))
+    return BITMOE_ERR_INVALID_ARG;
+  if (sh->head_dim != kAttnHeadDim || sh->n_q_heads != kAttnGroup * sh->n_kv_heads || sh->d % kChunkK ||
+      sh->d > 16384 || sh->n_q_heads * kAttnHeadDim > 16384 || sh->max_len > (int64_t(1) << 31))
+    return BITMOE_ERR_UNSUPPORTED;
+  if (!lmhead_supported((int)sh->d, 1) || !lmhead_supported((int)(sh->n_q_heads * kAttnHeadDim), 1))
+    return BITMOE_ERR_UNSUPPORTED;
+  return BITMOE_OK;
+}
+
+AttnWs attn_layout(const bitmoe_attn_shape_t* sh, void* base) {
+  char* p = static_cast<char*>(base);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    char* q = p ? p + off : nullptr;
+    off += align256(bytes);
+    return q;
+  };
+  const int64_t nq = sh->n_q_heads, nkv = sh->n_kv_heads, hd = kAttnHeadDim;
+  const int64_t span = sh->window > 0 && sh->window < sh->max_len ? sh->window : sh->max_len;
+  AttnWs w;
+  w.st = reinterpret_cast<DevStatus*>(take(256));
+  w.keys = take(lmhead_scratch_bytes(1));
+  w.am = reinterpret_cast<int32_t*>(take(4));
+  w.qkv = reinterpret_cast<float*>(take((size_t)(nq + 2 * nkv) * hd * 4));
+  w.q = reinterpret_cast<float*>(take((size_t)nq * hd * 4));
+  w.part = reinterpret_cast<float*>(take((size_t)nq * attn_chunks(span) * kAttnPart * 4));
+  w.attn = reinterpret_cast<uint16_t*>(take((size_t)nq * hd * 2));
+  w.y = reinterpret_cast<float*>(take((size_t)sh->d * 4));
+  w.total = off;
+  return w;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* bitmoe_status_string(bitmoe_status_t status) {
@@ -526,6 +578,55 @@ bitmoe_status_t moe_stack_decode(uint16_t* residual, int64_t T, const bitmoe_moe
   L.eps = eps;
   return cuda_status(launch_decode_stack(L, tab, (int)n_layers, lm_packed, (int)V, logits, keys, argmax,
                                          (cudaStream_t)stream));
+}
+
+size_t attn_workspace_size(const bitmoe_attn_shape_t* shape) {
+  if (check_attn_shape(shape) != BITMOE_OK) return 0;
+  return attn_layout(shape, nullptr).total;
+}
+
+bitmoe_status_t attn_decode_step(const uint16_t* x, const uint16_t* residual, int64_t pos,
+                                 const bitmoe_attn_shape_t* shape, const bitmoe_attn_weights_t* weights,
+                                 uint16_t* k_cache, uint16_t* v_cache, uint16_t* out, float* out_f32,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  bitmoe_status_t st = check_attn_shape(shape);
+  if (st != BITMOE_OK) return st;
+  if (pos < 0 || pos >= shape->max_len || !weights) return BITMOE_ERR_INVALID_ARG;
+  if (!x || !residual || !out || !k_cache || !v_cache || !weights->wqkv || !weights->wo)
+    return BITMOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(residual) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(weights->wqkv) || !aligned16(weights->wo) || (out_f32 && !aligned16(out_f32)))
+    return BITMOE_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < attn_layout(shape, nullptr).total)
+    return BITMOE_ERR_WORKSPACE;
+  const AttnWs w = attn_layout(shape, workspace);
+  AttnLaunch L;
+  L.x = x;
+  L.resid = residual;
+  L.pos = pos;
+  L.d = (int)shape->d;
+  L.nq = (int)shape->n_q_heads;
+  L.nkv = (int)shape->n_kv_heads;
+  L.window = shape->window;
+  L.rope = shape->rope ? 1 : 0;
+  L.theta = shape->rope_theta;
+  L.eps = shape->eps;
+  L.wqkv = weights->wqkv;
+  L.wo = weights->wo;
+  L.sinks = weights->sinks;
+  L.k_cache = k_cache;
+  L.v_cache = v_cache;
+  L.out = out;
+  L.out_f32 = out_f32;
+  L.qkv = w.qkv;
+  L.q = w.q;
+  L.part = w.part;
+  L.attn = w.attn;
+  L.y = w.y;
+  L.keys_scratch = w.keys;
+  L.am_scratch = w.am;
+  L.st = w.st;
+  return cuda_status(launch_attn_decode(L, (cudaStream_t)stream));
 }
 
 size_t lmhead_workspace_size(int64_t T, int64_t d, int64_t V) {

@@ -140,4 +140,39 @@ cudaError_t launch_lmhead_nvfp4(const uint16_t* h, int T, int d, int V, const ui
 // Records e as the thread's last CUDA error (read by bitmoe_last_cuda_error) and maps it to a status.
 bitmoe_status_t api_cuda_status(cudaError_t e);
 
+// ---------------------------------------------------------------- attention decode step (attn.cu)
+constexpr int kAttnHeadDim = 128;  // head dimension the kernels are built for
+constexpr int kAttnGroup = 8;      // query heads per key/value head
+constexpr int kAttnChunk = 256;    // cache positions per CTA of the split kernel
+constexpr int kAttnPart = 4 + kAttnHeadDim;  // floats per (query head, chunk) partial result
+// chunks of the split kernel for `span` attended positions
+int attn_chunks(int64_t span);
+struct AttnLaunch {
+  const uint16_t* x;      // [d] bf16 (the normalised residual)
+  const uint16_t* resid;  // [d] bf16
+  int64_t pos;            // the token's position (its cache row)
+  int d, nq, nkv;
+  int64_t window;         // 0: the whole context
+  int rope;
+  double theta;
+  float eps;
+  const uint8_t* wqkv;    // packed int4 [(nq + 2 nkv) * 128, d]
+  const uint8_t* wo;      // packed int4 [d, nq * 128]
+  const float* sinks;     // [nq] or null
+  uint16_t* k_cache;      // [L, nkv, 128] bf16
+  uint16_t* v_cache;
+  uint16_t* out;          // [d] bf16
+  float* out_f32;         // [d] or null
+  // scratch
+  float* qkv;             // [(nq + 2 nkv) * 128]
+  float* q;               // [nq * 128]
+  float* part;            // [nq * chunks * kAttnPart]
+  uint16_t* attn;         // [nq * 128] bf16
+  float* y;               // [d]
+  void* keys_scratch;     // LM-head GEMV scratch (arg-max keys, unused here)
+  int32_t* am_scratch;    // [1]
+  DevStatus* st;
+};
+cudaError_t launch_attn_decode(const AttnLaunch& L, cudaStream_t s);
+
 }  // namespace bitmoe

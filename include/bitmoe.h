@@ -150,6 +150,53 @@ size_t bitmoe_packed_int4_bytes(int64_t n_mats, int64_t rows, int64_t K, int64_t
 bitmoe_status_t bitmoe_pack_int4(const uint8_t* q, const uint16_t* scale, int64_t n_mats, int64_t rows,
                                  int64_t K, int64_t group, uint8_t* packed, void* stream);
 
+/* ------------------------------------------------------------ attention decode step
+ *
+ * The attention layer beside each mixture layer, for one token of a decode step:
+ * grouped-query attention over a bf16 key/value cache with a sliding window or the
+ * whole context, per-head RMS norm on queries and keys, rotary encoding and learned
+ * sinks.
+ *   q | k | v = Wqkv x                    (int4 group-32, rows stacked: nq*128 | nkv*128 | nkv*128)
+ *   q_h, k_g <- RMSNorm per head (unit gain, eps), then rotated by the position when
+ *               rope: pairs (i, i + 64) by the angle pos * rope_theta^(-2i/128)
+ *   cache row pos <- bf16(k), bf16(v)
+ *   o_h = sum_j e^(s_j) v_j / (sum_j e^(s_j) + e^(sink_h)),  s_j = q_h . k_j / sqrt(128),
+ *         j over the window [max(0, pos - window + 1), pos] (window 0: [0, pos]) of key/value
+ *         head g = h / (nq / nkv); no sinks: the plain softmax
+ *   out = residual + Wo bf16(o)           (bf16 out; out_f32 the unrounded sum, nullable)
+ * Source: "Flint 40B : Best Mid Sized LLM", transcript 03:05 (32 query / 4 key-value heads of
+ * 128, a 513-token sliding window on 35 layers with rotary encoding, whole-context attention
+ * without it on the others) and 03:36 (per-head RMS norm on q and k, learned attention sinks);
+ * the pages give no formula: rope_theta, eps, the sink form and the bf16 cache are readings.
+ * Supported: head_dim 128, nq = 8 nkv, d % 128 == 0; else BITMOE_ERR_UNSUPPORTED.  x, residual,
+ * out [d] bf16 (one token); k_cache, v_cache [max_len, nkv, 128] bf16 with rows 0 .. pos - 1
+ * filled by earlier steps, row pos written by this one (0 <= pos < max_len, else
+ * BITMOE_ERR_INVALID_ARG); all 16-byte aligned.  Workspace: attn_workspace_size() bytes,
+ * zero-filled before first use. */
+typedef struct bitmoe_attn_shape {
+  int64_t d;          /* hidden size */
+  int64_t n_q_heads;  /* query heads (32) */
+  int64_t n_kv_heads; /* key/value heads (4) */
+  int64_t head_dim;   /* 128 */
+  int64_t max_len;    /* cache rows */
+  int64_t window;     /* attended tokens including the current one (513); 0: the whole context */
+  int32_t rope;       /* 1: rotary encoding of q and k; 0: none */
+  float eps;          /* RMS-norm epsilon (1e-6) */
+  double rope_theta;  /* rotary base (1e6) */
+} bitmoe_attn_shape_t;
+
+typedef struct bitmoe_attn_weights {
+  const uint8_t* wqkv; /* packed int4 [(nq + 2 nkv) * 128, d] (bitmoe_pack_int4, group 32) */
+  const uint8_t* wo;   /* packed int4 [d, nq * 128] */
+  const float* sinks;  /* [nq] fp32 sink logits, or NULL */
+} bitmoe_attn_weights_t;
+
+size_t attn_workspace_size(const bitmoe_attn_shape_t* shape);
+bitmoe_status_t attn_decode_step(const uint16_t* x, const uint16_t* residual, int64_t pos,
+                                 const bitmoe_attn_shape_t* shape, const bitmoe_attn_weights_t* weights,
+                                 uint16_t* k_cache, uint16_t* v_cache, uint16_t* out, float* out_f32,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
 /* Read (and clear, when clear != 0) the device status word of a workspace.
  * Synchronises `stream`.  *status_out receives BITMOE_OK, BITMOE_ERR_TIMEOUT
  * or BITMOE_ERR_DEVICE_CHECK. */

@@ -50,6 +50,8 @@ TAG = {
     # NVFP4 banks: E2M1 codes, E4M3 block scales, fp32 tensor scales
     "gate_fq": 13, "gate_fs": 14, "gate_ts": 15, "up_fq": 16, "up_fs": 17, "up_ts": 18,
     "down_fq": 19, "down_fs": 20, "down_ts": 21, "lm_fq": 22, "lm_fs": 23, "lm_ts": 24,
+    # attention layer: stacked q|k|v projection, output projection, sinks, key/value cache
+    "qkv_q": 25, "qkv_s": 26, "wo_q": 27, "wo_s": 28, "sinks": 29, "kcache": 30, "vcache": 31,
 }
 
 # E4M3 block scales are drawn uniformly among the 16 byte codes 0x58 .. 0x67,
@@ -203,6 +205,27 @@ def int4_matrix(seed: int, qtag: str, stag: str, layer: int, n_mats: int, rows: 
     q = int4_bytes(kq, mat0 * qb, m * qb).reshape(m, rows, K // 2)
     s = f16_scales(ks, mat0 * sb, m * sb).reshape(m, rows, K // group)
     return q, s
+
+
+def attn_layer(seed: int, d: int, n_q: int, n_kv: int, head_dim: int = 128, layer: int = 0,
+               sinks: bool = True) -> dict:
+    """Tensors of one attention layer: int4 banks of the stacked q | k | v projection
+    [(n_q + 2 n_kv) * head_dim, d] and of the output projection [d, n_q * head_dim]
+    (nibbles uniform over -8..7, fp16 scales U(0.005, 0.02)), and the sink logits
+    [n_q] ~ N(0, 1) fp32 (or None)."""
+    rows = (n_q + 2 * n_kv) * head_dim
+    wq, ws = int4_matrix(seed, "qkv_q", "qkv_s", layer, 1, rows, d)
+    oq, os_ = int4_matrix(seed, "wo_q", "wo_s", layer, 1, d, n_q * head_dim)
+    sk = _rng(seed, TAG["sinks"], layer).normal(0.0, 1.0, n_q).astype(np.float32) if sinks else None
+    return {"wqkv_q": wq[0], "wqkv_s": ws[0], "wo_q": oq[0], "wo_s": os_[0], "sinks": sk}
+
+
+def kv_cache(seed: int, L: int, n_kv: int, head_dim: int = 128, layer: int = 0):
+    """Key and value cache contents [L, n_kv, head_dim] ~ N(0, 1) as bf16 bits (keys of a
+    normalised, rotated head have unit mean square as well)."""
+    k = f64_to_bf16_bits(_rng(seed, TAG["kcache"], layer).normal(0.0, 1.0, (L, n_kv, head_dim)))
+    v = f64_to_bf16_bits(_rng(seed, TAG["vcache"], layer).normal(0.0, 1.0, (L, n_kv, head_dim)))
+    return k, v
 
 
 def moe_layer(seed: int, d: int, E: int, I: int, group: int = 32, layer: int = 0,

@@ -1,0 +1,88 @@
+"""GPU parity of the attention decode step (attn_decode_step, through the C ABI)
+against the fp64 oracle (oracle/attention.py) on seeded synthetic weights and caches.
+
+Bars: the layer output within max-abs 2e-2 and rel-L2 1e-3 on the fp32 copy, whose
+bf16 rounding is the bf16 output bit for bit; the cache rows other than pos untouched;
+the new key and value rows (fp32 on the GPU, fp64 in the oracle, both rounded once to
+bf16) equal to the oracle's except where the two sides round a value within their
+difference of a bf16 rounding boundary (at most one ulp apart, at most 1% of elements).
+"""
+import numpy as np
+import pytest
+
+import synth
+from helpers import MAX_ABS, REL_L2, bits_from_torch_bf16, max_abs, rel_l2, torch_bf16_from_bits
+from oracle import attention as A
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import bit_expert_ffn_warp_b300 as bm  # noqa: E402
+
+D, NQ, NKV, L = 2048, 32, 4, 4608
+
+
+def run_step(pos, window, rope, sinks, seed=3):
+    t = synth.attn_layer(seed, D, NQ, NKV, sinks=sinks)
+    kc, vc = synth.kv_cache(seed + 1, L, NKV)
+    x = synth.activations(seed + 2, 1, D, step=pos)[0]
+    res = synth.activations(seed + 3, 1, D, step=pos)[0]
+    ref = A.decode_step(x, res, pos, t, kc, vc, window=window, use_rope=rope)
+    lay = bm.AttnLayer.from_canonical(t, D, NQ, NKV, window=window, rope=rope)
+    kd, vd = torch_bf16_from_bits(kc).contiguous(), torch_bf16_from_bits(vc).contiguous()
+    ws = bm.attn_workspace(lay, L)
+    out_f32 = torch.empty(D, dtype=torch.float32, device="cuda")
+    out = bm.attn_decode_step(torch_bf16_from_bits(x), torch_bf16_from_bits(res), pos, lay, kd, vd, ws,
+                              out_f32=out_f32)
+    torch.cuda.synchronize()
+    assert bm.bitmoe_get_device_status(ws) == 0
+    return ref, kc, vc, out, out_f32, bits_from_torch_bf16(kd), bits_from_torch_bf16(vd)
+
+
+def close_bf16_rows(got, want):
+    ulp = np.abs(A.bf16_bits_to_f64(want)) * 2.0 ** -7 + 1e-30
+    diff = np.abs(A.bf16_bits_to_f64(got) - A.bf16_bits_to_f64(want))
+    assert np.all(diff <= ulp * 1.01)
+    assert np.mean(got != want) <= 0.01
+
+
+@pytest.mark.parametrize("pos,window,rope,sinks", [
+    (0, 513, True, True),      # one key: the current token's own
+    (7, 513, True, True),
+    (255, 0, False, True),     # chunk edges of the split kernel (256 positions)
+    (256, 0, False, True),
+    (600, 513, True, True),    # the window has left the first 88 tokens behind
+    (600, 0, False, True),
+    (1000, 513, True, False),  # no sinks: the plain softmax
+    (4500, 0, False, True),    # 18 chunks of the whole context
+])
+def test_attention_decode_step_matches_the_oracle(pos, window, rope, sinks):
+    ref, kc, vc, out, out_f32, kd, vd = run_step(pos, window, rope, sinks)
+    o32 = out_f32.cpu().numpy().astype(np.float64)
+    ma, rl = max_abs(o32, ref["out"]), rel_l2(o32, ref["out"])
+    assert ma <= MAX_ABS and rl <= REL_L2, f"max-abs {ma:.3g} rel-L2 {rl:.3g}"
+    assert np.array_equal(bits_from_torch_bf16(out), bits_from_torch_bf16(out_f32.to(torch.bfloat16)))
+    keep = np.ones(L, bool)
+    keep[pos] = False
+    assert np.array_equal(kd[keep], kc[keep]) and np.array_equal(vd[keep], vc[keep])
+    close_bf16_rows(kd[pos], ref["k_bits"])
+    close_bf16_rows(vd[pos], ref["v_bits"])
+
+
+def test_attention_step_rejects_positions_outside_the_cache():
+    t = synth.attn_layer(3, D, NQ, NKV)
+    lay = bm.AttnLayer.from_canonical(t, D, NQ, NKV)
+    kd = torch.zeros((64, NKV, 128), dtype=torch.bfloat16, device="cuda")
+    vd = torch.zeros_like(kd)
+    ws = bm.attn_workspace(lay, 64)
+    x = torch.zeros(D, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(bm.BitmoeError) as e:
+        bm.attn_decode_step(x, x, 64, lay, kd, vd, ws)
+    assert e.value.code == bm.ERR_INVALID_ARG
+    small = bm.attn_workspace(lay, 64)[:128]
+    with pytest.raises(bm.BitmoeError) as e:
+        bm.attn_decode_step(x, x, 3, lay, kd, vd, small)
+    assert e.value.code == bm.ERR_WORKSPACE
