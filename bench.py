@@ -23,6 +23,10 @@ Other workloads (``--workload``): ``batch`` (T tokens per step, Zipf(1.1)
 router skew), ``prefill`` (T=4096 chunk, Zipf skew), ``stack`` (49 layers +
 RMSNorm + int4 LM head + argmax), ``shared`` (the pages' routing: top-6 of 256
 plus one shared expert), ``lmhead`` (the int4 LM head alone, V = 131072).
+``attn`` (one token through one attention layer beside the MoE layer: int4
+q|k|v and output projections, grouped-query attention of 32 query / 4 key-value
+heads of 128 over a bf16 cache of ``--ctx`` positions, whole context or a
+``--window``, with sinks).
 ``--format nvfp4`` runs the decode, batch, prefill and LM-head workloads with
 NVFP4 weights (E2M1 codes, an E4M3 scale per 16 weights, an fp32 scale per
 matrix; the same 4.5 bits per weight).  ``--impl reference`` times the fp64 CPU
@@ -48,14 +52,19 @@ METRIC = "MoE-layer decode tokens/s on 1 B300; achieved HBM GB/s vs ~8 TB/s roof
 PREFILL_METRIC = "MoE-layer prefill tokens/s on 1 B300; grouped-GEMM TFLOP/s vs dense 16-bit tensor peak"
 STACK_METRIC = "49-layer MoE stack + int4 LM head decode tokens/s on 1 B300; achieved HBM GB/s"
 LMHEAD_METRIC = "int4 LM-head GEMV + argmax tokens/s on 1 B300; achieved HBM GB/s"
+ATTN_METRIC = "attention-layer decode tokens/s on 1 B300 (GQA 32/4 x 128, int4 projections); achieved HBM GB/s"
 D, E, K_TOP, I_FF, V = 2048, 256, 8, 512, 131072
 EXPERT_BYTES = 3 * I_FF * D * 9 // 16          # int4 + fp16 group scales of one expert (gate, up, down)
 ROUTER_BYTES = E * D * 4 + E * 4               # fp32 router weight + bias
 LM_BYTES = V * D * 9 // 16
 K_SHARED = 6                                   # routed experts per token beside the shared expert
+NQ, NKV, HD = 32, 4, 128                       # attention heads: query, key/value, head size
+WQKV_BYTES = (NQ + 2 * NKV) * HD * D * 9 // 16  # int4 + fp16 group scales of the stacked q|k|v projection
+WO_BYTES = D * NQ * HD * 9 // 16
 MIN_TIMED_S = 0.4                              # GPU time the repeated timed region adds up to, at least
-DEFAULT_STEPS = {"decode": 2000, "shared": 2000, "batch": 500, "prefill": 20, "stack": 50, "lmhead": 500}
-DEFAULT_WARMUP = {"decode": 200, "shared": 200, "batch": 50, "prefill": 5, "stack": 5, "lmhead": 50}
+DEFAULT_STEPS = {"decode": 2000, "shared": 2000, "batch": 500, "prefill": 20, "stack": 50, "lmhead": 500,
+                 "attn": 500}
+DEFAULT_WARMUP = {"decode": 200, "shared": 200, "batch": 50, "prefill": 5, "stack": 5, "lmhead": 50, "attn": 50}
 
 
 def parse():
@@ -66,12 +75,14 @@ def parse():
     p.add_argument("--warmup", type=int, default=None, help="untimed warm-up steps (per-workload default, >= 3)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="decode",
-                   choices=["decode", "batch", "prefill", "stack", "shared", "lmhead"],
+                   choices=["decode", "batch", "prefill", "stack", "shared", "lmhead", "attn"],
                    help="shared: batch-1 decode with the pages' routing, top-6 of 256 plus one shared expert")
     p.add_argument("--T", type=int, default=None, help="tokens per step (batch / prefill / stack / lmhead)")
     p.add_argument("--format", default="int4", choices=["int4", "nvfp4"],
                    help="weight format of the experts and the LM head (not the stack)")
     p.add_argument("--copies", type=int, default=64, help="independent layer copies cycled per step")
+    p.add_argument("--ctx", type=int, default=32768, help="attn: context length (the token attends at ctx - 1)")
+    p.add_argument("--window", type=int, default=0, help="attn: sliding window (0 = whole context; 513 with rotary)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--min-timed-s", type=float, default=MIN_TIMED_S,
@@ -84,7 +95,7 @@ def parse():
     a.steps = max(1, a.steps)
     a.warmup = max(3, a.warmup)
     MIN_TIMED_S = max(0.0, a.min_timed_s)
-    if a.format == "nvfp4" and a.workload in ("stack", "shared"):
+    if a.format == "nvfp4" and a.workload in ("stack", "shared", "attn"):
         p.error("--format nvfp4 covers the decode, batch, prefill and lmhead workloads")
     return a
 
@@ -880,6 +891,127 @@ def bench_lmhead(args, world, rank):
     }
 
 
+# ---------------------------------------------------------------- attention layer
+
+
+def attn_name(ctx, window):
+    return f"attn_decode_ctx{ctx}_" + (f"swa{window}" if window else "full")
+
+
+def attn_keys(ctx, window):
+    return min(ctx, window) if window else ctx
+
+
+def attn_step_bytes(ctx, window):
+    """Bytes one step must move: both projections' int4 banks, the attended keys and
+    values, the new cache rows, and x, the residual and the output."""
+    return WQKV_BYTES + WO_BYTES + attn_keys(ctx, window) * NKV * HD * 2 * 2 + NKV * HD * 2 * 2 + 3 * D * 2
+
+
+def bench_attn(args, world, rank):
+    """One token through one attention layer at position ctx - 1 (the cache holds ctx rows)."""
+    import torch
+
+    import bit_expert_ffn_warp_b300 as bm
+    import synth
+
+    ctx, window = args.ctx, args.window
+    if ctx < 1:
+        raise SystemExit("--ctx must be >= 1")
+    K, W = args.steps, args.warmup
+    rope = window > 0   # rotary encoding on the sliding-window layers, none on the whole-context ones
+    step_bytes = attn_step_bytes(ctx, window)
+    G = max(1, min(args.copies, math.ceil(3 * 126e6 / step_bytes)))   # copies cycled: 3x L2 of inputs
+    layers, kcs, vcs = [], [], []
+    gen = torch.Generator(device="cuda")
+    for c in range(G):
+        t = synth.attn_layer(1 + rank + 1000 * c, D, NQ, NKV)
+        layers.append(bm.AttnLayer.from_canonical(t, D, NQ, NKV, window=window, rope=rope))
+        gen.manual_seed(7 + rank + 1000 * c)
+        kcs.append(torch.randn((NKV, ctx, HD), generator=gen, device="cuda").to(torch.bfloat16))
+        vcs.append(torch.randn((NKV, ctx, HD), generator=gen, device="cuda").to(torch.bfloat16))
+    ws = bm.attn_workspace(layers[0], ctx)
+    pos = ctx - 1
+    n_pool = 256
+    xs_host = token_pool(rank, n_pool, 2)   # [P, 2, D]: x and the residual of each step
+    xs = to_bf16(xs_host)
+    outs = torch.empty((G, D), dtype=torch.bfloat16, device="cuda")
+
+    def step(s):
+        g = s % G
+        bm.attn_decode_step(xs[s % n_pool, 0], xs[s % n_pool, 1], pos, layers[g], kcs[g], vcs[g], ws, out=outs[g])
+
+    ng = n_region_graphs(K, G)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        run_warmup(step, W)
+        times = time_regions(region_graphs(step, K, ng), world)
+    ms_local = statistics.median(times)
+    per_step_us = max_over_ranks(ms_local, world) * 1e3 / K
+    launches_per_step = count_kernels(lambda: step(0))
+    hbm, _, _, which = peaks()
+    achieved = step_bytes / (per_step_us * 1e-6) / 1e9
+
+    x_pin = to_bf16(xs_host, pin=True)
+    out_pin = torch.empty((n_pool, D), dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty((G, 2, D), dtype=torch.bfloat16, device="cuda")
+
+    def e2e_step(s):
+        g = s % G
+        xd[g].copy_(x_pin[s % n_pool], non_blocking=True)
+        bm.attn_decode_step(xd[g, 0], xd[g, 1], pos, layers[g], kcs[g], vcs[g], ws, out=outs[g])
+        out_pin[s % n_pool].copy_(outs[g], non_blocking=True)
+
+    run_warmup(e2e_step, 3)
+    e_times = time_regions(region_graphs(e2e_step, K, ng), world)
+    name = attn_name(ctx, window)
+    return {
+        "metric": ATTN_METRIC,
+        "value": round(job_throughput(K, ms_local, world), 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": per_step_us / 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int4xbf16->fp32; bf16 cache, fp32 softmax",
+        "data": "synthetic (seeded; weights packed from host draws, caches N(0,1) drawn on device)",
+        "config": {"workload": name, "T": 1, "d": D, "n_q_heads": NQ, "n_kv_heads": NKV, "head_dim": HD,
+                   "ctx": ctx, "window": window, "rope": rope, "sinks": True, "keys_attended": attn_keys(ctx, window),
+                   "layer_copies": G,
+                   "l2": f"inputs larger than L2: {G} layer copies with their caches "
+                         f"({G * (WQKV_BYTES + WO_BYTES + 2 * ctx * NKV * HD * 2) / 1e6:.0f} MB) cycled step by step",
+                   "parallelism": f"replicas x{world}"},
+        "timing": timing_record(times, K, f"CUDA graphs of {K} attn_decode_step calls, {ng} graph(s) in rotation"),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "kernel": "whole attention step (qkv GEMV, prep, split-KV attention, combine, Wo GEMV, "
+                               "residual)", "bytes_per_step": step_bytes,
+                     "peak_source": which + " (copy, burst)"},
+        "gpu_launches": launches_per_step * K if launches_per_step else None,
+        "e2e": {"value": round(job_throughput(K, statistics.median(e_times), world), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": 2 * D * 2, "d2h_bytes_per_step": D * 2,
+                "how": "every step: pinned host x and residual -> device, attn_decode_step, output -> pinned host",
+                "regions": len(e_times)},
+        "clocks": clk.summary(),
+    }
+
+
+def cpu_attn_sample(ctx, window, seconds, seed=0):
+    """The oracle's attention step on one layer at the same context, repeated until the
+    time budget is spent (the cache draw is outside the timed part)."""
+    import oracle
+    import synth
+    from oracle import attention as A
+    t = synth.attn_layer(seed, D, NQ, NKV)
+    kc, vc = synth.kv_cache(seed + 1, ctx, NKV)
+    cores = oracle.num_threads()
+    n, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds or n == 0:
+        x = synth.activations(seed + 2, 1, D, step=n)[0]
+        r = synth.activations(seed + 3, 1, D, step=n)[0]
+        A.decode_step(x, r, ctx - 1, t, kc, vc, window=window, use_rope=window > 0)
+        n += 1
+    el = time.perf_counter() - t0
+    return {"value": n / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} attention steps at position {ctx - 1} ({el:.1f} s, fp64 numpy; projections dequantised "
+                      f"by the oracle's C routine)"}
+
+
 # ---------------------------------------------------------------- main
 
 
@@ -903,6 +1035,9 @@ def reference_arm(args):
     elif wl == "lmhead":
         T = args.T or 1
         name, metric = f"lmhead_V{V}_T{T}", LMHEAD_METRIC
+    elif wl == "attn":
+        T = 1
+        name, metric = attn_name(args.ctx, args.window), ATTN_METRIC
     else:
         T = args.T or 1
         name, metric = f"moe_stack49_lmhead_T{T}", STACK_METRIC
@@ -913,12 +1048,17 @@ def reference_arm(args):
         cb = cpu_stack_sample(T, budget)
     elif wl == "lmhead":
         cb = cpu_lmhead_sample(T, budget)
+    elif wl == "attn":
+        cb = cpu_attn_sample(args.ctx, args.window, budget)
     else:
         cb = cpu_oracle_sample(wl, T, budget)
     el = time.perf_counter() - t0
     cfg = {"workload": name, "T": T, "d": D}
     if wl == "lmhead":
         cfg["V"] = V
+    elif wl == "attn":
+        cfg.update({"n_q_heads": NQ, "n_kv_heads": NKV, "head_dim": HD, "ctx": args.ctx, "window": args.window,
+                    "rope": args.window > 0, "sinks": True})
     else:
         cfg.update({"E": E, "top_k": K_SHARED if wl == "shared" else K_TOP, "n_shared": int(wl == "shared"),
                     "I": I_FF})
@@ -945,6 +1085,8 @@ def main():
         res = bench_prefill(args, world, rank)
     elif args.workload == "lmhead":
         res = bench_lmhead(args, world, rank)
+    elif args.workload == "attn":
+        res = bench_attn(args, world, rank)
     else:
         res = bench_stack(args, world, rank)
     if rank == 0:
@@ -954,6 +1096,8 @@ def main():
                 res["cpu_baseline"] = cpu_stack_sample(T, args.cpu_seconds)
             elif args.workload == "lmhead":
                 res["cpu_baseline"] = cpu_lmhead_sample(T, args.cpu_seconds, fmt=args.format)
+            elif args.workload == "attn":
+                res["cpu_baseline"] = cpu_attn_sample(args.ctx, args.window, args.cpu_seconds)
             else:
                 res["cpu_baseline"] = cpu_oracle_sample(args.workload, T, args.cpu_seconds, fmt=args.format)
         print(json.dumps(res))

@@ -576,18 +576,19 @@ def attn_workspace(layer: AttnLayer, max_len: int) -> torch.Tensor:
 
 
 def attn_decode_step(x, residual, pos: int, layer: AttnLayer, k_cache, v_cache, workspace, out=None, out_f32=None):
-    """One token: x, residual [d] bf16; caches [max_len, n_kv, 128] bf16 (row pos is written).
+    """One token: x, residual [d] bf16; caches [n_kv, max_len, 128] bf16, head-major (row pos
+    of every head is written).
     Returns out [d] bf16."""
     d = layer.d
     _need(x, torch.bfloat16, (d,), "x")
     _need(residual, torch.bfloat16, (d,), "residual")
     _need(k_cache, torch.bfloat16, None, "k_cache")
     _need(v_cache, torch.bfloat16, tuple(k_cache.shape), "v_cache")
-    if k_cache.dim() != 3 or k_cache.shape[1] != layer.n_kv or k_cache.shape[2] != 128:
-        raise ValueError("caches must be [max_len, n_kv, 128]")
+    if k_cache.dim() != 3 or k_cache.shape[0] != layer.n_kv or k_cache.shape[2] != 128:
+        raise ValueError("caches must be [n_kv, max_len, 128] (head-major)")
     if out is None:
         out = torch.empty(d, dtype=torch.bfloat16, device="cuda")
-    sh = layer.shape(k_cache.shape[0])
+    sh = layer.shape(k_cache.shape[1])
     wts = layer.weights
     _check("attn_decode_step",
            _lib.attn_decode_step(_ptr(x), _ptr(residual), int(pos), ctypes.byref(sh), ctypes.byref(wts),

@@ -305,13 +305,9 @@ namespace {
 // Workspace carve-up of the attention decode step.
 struct AttnWs {
   DevStatus* st;
-  void* keys;
-  int32_t* am;
   float* qkv;
-  float* q;
   float* part;
   uint16_t* attn;
-  float* y;
   size_t total;
 };
 
@@ -321,8 +317,6 @@ bitmoe_status_t check_attn_shape(const bitmoe_attn_shape_t* sh) {
     return BITMOE_ERR_INVALID_ARG;
   if (sh->head_dim != kAttnHeadDim || sh->n_q_heads != kAttnGroup * sh->n_kv_heads || sh->d % kChunkK ||
       sh->d > 16384 || sh->n_q_heads * kAttnHeadDim > 16384 || sh->max_len > (int64_t(1) << 31))
-    return BITMOE_ERR_UNSUPPORTED;
-  if (!lmhead_supported((int)sh->d, 1) || !lmhead_supported((int)(sh->n_q_heads * kAttnHeadDim), 1))
     return BITMOE_ERR_UNSUPPORTED;
   return BITMOE_OK;
 }
@@ -336,16 +330,11 @@ AttnWs attn_layout(const bitmoe_attn_shape_t* sh, void* base) {
     return q;
   };
   const int64_t nq = sh->n_q_heads, nkv = sh->n_kv_heads, hd = kAttnHeadDim;
-  const int64_t span = sh->window > 0 && sh->window < sh->max_len ? sh->window : sh->max_len;
   AttnWs w;
   w.st = reinterpret_cast<DevStatus*>(take(256));
-  w.keys = take(lmhead_scratch_bytes(1));
-  w.am = reinterpret_cast<int32_t*>(take(4));
   w.qkv = reinterpret_cast<float*>(take((size_t)(nq + 2 * nkv) * hd * 4));
-  w.q = reinterpret_cast<float*>(take((size_t)nq * hd * 4));
-  w.part = reinterpret_cast<float*>(take((size_t)nq * attn_chunks(span) * kAttnPart * 4));
+  w.part = reinterpret_cast<float*>(take((size_t)nq * kAttnMaxSplits * kAttnPart * 4));
   w.attn = reinterpret_cast<uint16_t*>(take((size_t)nq * hd * 2));
-  w.y = reinterpret_cast<float*>(take((size_t)sh->d * 4));
   w.total = off;
   return w;
 }
@@ -616,16 +605,12 @@ bitmoe_status_t attn_decode_step(const uint16_t* x, const uint16_t* residual, in
   L.sinks = weights->sinks;
   L.k_cache = k_cache;
   L.v_cache = v_cache;
+  L.max_len = shape->max_len;
   L.out = out;
   L.out_f32 = out_f32;
   L.qkv = w.qkv;
-  L.q = w.q;
   L.part = w.part;
   L.attn = w.attn;
-  L.y = w.y;
-  L.keys_scratch = w.keys;
-  L.am_scratch = w.am;
-  L.st = w.st;
   return cuda_status(launch_attn_decode(L, (cudaStream_t)stream));
 }
 

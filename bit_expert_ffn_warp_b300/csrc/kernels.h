@@ -143,10 +143,16 @@ bitmoe_status_t api_cuda_status(cudaError_t e);
 // ---------------------------------------------------------------- attention decode step (attn.cu)
 constexpr int kAttnHeadDim = 128;  // head dimension the kernels are built for
 constexpr int kAttnGroup = 8;      // query heads per key/value head
-constexpr int kAttnChunk = 256;    // cache positions per CTA of the split kernel
-constexpr int kAttnPart = 4 + kAttnHeadDim;  // floats per (query head, chunk) partial result
-// chunks of the split kernel for `span` attended positions
-int attn_chunks(int64_t span);
+constexpr int kAttnPart = 4 + kAttnHeadDim;  // floats per (query head, split) partial result
+constexpr int kAttnMaxSplits = 128;          // splits of the attended span per key/value head, at most
+// How the split kernel cuts `span` attended positions for nkv key/value heads: `chunk`
+// positions per CTA (a multiple of 64) and `nsplit` <= kAttnMaxSplits CTAs per head,
+// about two CTAs per SM in all.
+struct AttnPlan {
+  int64_t chunk;
+  int nsplit;
+};
+AttnPlan attn_plan(int64_t span, int nkv);
 struct AttnLaunch {
   const uint16_t* x;      // [d] bf16 (the normalised residual)
   const uint16_t* resid;  // [d] bf16
@@ -159,19 +165,15 @@ struct AttnLaunch {
   const uint8_t* wqkv;    // packed int4 [(nq + 2 nkv) * 128, d]
   const uint8_t* wo;      // packed int4 [d, nq * 128]
   const float* sinks;     // [nq] or null
-  uint16_t* k_cache;      // [L, nkv, 128] bf16
+  uint16_t* k_cache;      // [nkv, max_len, 128] bf16
   uint16_t* v_cache;
+  int64_t max_len;
   uint16_t* out;          // [d] bf16
   float* out_f32;         // [d] or null
   // scratch
   float* qkv;             // [(nq + 2 nkv) * 128]
-  float* q;               // [nq * 128]
-  float* part;            // [nq * chunks * kAttnPart]
+  float* part;            // [nq * kAttnMaxSplits * kAttnPart]
   uint16_t* attn;         // [nq * 128] bf16
-  float* y;               // [d]
-  void* keys_scratch;     // LM-head GEMV scratch (arg-max keys, unused here)
-  int32_t* am_scratch;    // [1]
-  DevStatus* st;
 };
 cudaError_t launch_attn_decode(const AttnLaunch& L, cudaStream_t s);
 

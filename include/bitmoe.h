@@ -169,9 +169,10 @@ bitmoe_status_t bitmoe_pack_int4(const uint8_t* q, const uint16_t* scale, int64_
  * without it on the others) and 03:36 (per-head RMS norm on q and k, learned attention sinks);
  * the pages give no formula: rope_theta, eps, the sink form and the bf16 cache are readings.
  * Supported: head_dim 128, nq = 8 nkv, d % 128 == 0; else BITMOE_ERR_UNSUPPORTED.  x, residual,
- * out [d] bf16 (one token); k_cache, v_cache [max_len, nkv, 128] bf16 with rows 0 .. pos - 1
- * filled by earlier steps, row pos written by this one (0 <= pos < max_len, else
- * BITMOE_ERR_INVALID_ARG); all 16-byte aligned.  Workspace: attn_workspace_size() bytes,
+ * out [d] bf16 (one token); k_cache, v_cache [nkv, max_len, 128] bf16, head-major (each
+ * head's rows contiguous, so a span of positions is one run of memory), with rows 0 .. pos - 1
+ * of every head filled by earlier steps and row pos written by this one (0 <= pos < max_len,
+ * else BITMOE_ERR_INVALID_ARG); all 16-byte aligned.  d and nq * 128 at most 16384.  Workspace: attn_workspace_size() bytes,
  * zero-filled before first use. */
 typedef struct bitmoe_attn_shape {
   int64_t d;          /* hidden size */

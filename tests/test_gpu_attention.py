@@ -25,21 +25,24 @@ import bit_expert_ffn_warp_b300 as bm  # noqa: E402
 D, NQ, NKV, L = 2048, 32, 4, 4608
 
 
-def run_step(pos, window, rope, sinks, seed=3):
+def run_step(pos, window, rope, sinks, seed=3, L=L):
     t = synth.attn_layer(seed, D, NQ, NKV, sinks=sinks)
     kc, vc = synth.kv_cache(seed + 1, L, NKV)
     x = synth.activations(seed + 2, 1, D, step=pos)[0]
     res = synth.activations(seed + 3, 1, D, step=pos)[0]
     ref = A.decode_step(x, res, pos, t, kc, vc, window=window, use_rope=rope)
     lay = bm.AttnLayer.from_canonical(t, D, NQ, NKV, window=window, rope=rope)
-    kd, vd = torch_bf16_from_bits(kc).contiguous(), torch_bf16_from_bits(vc).contiguous()
+    # the oracle keeps [position, head, 128]; the library's cache is head-major
+    kd = torch_bf16_from_bits(np.ascontiguousarray(kc.transpose(1, 0, 2))).contiguous()
+    vd = torch_bf16_from_bits(np.ascontiguousarray(vc.transpose(1, 0, 2))).contiguous()
     ws = bm.attn_workspace(lay, L)
     out_f32 = torch.empty(D, dtype=torch.float32, device="cuda")
     out = bm.attn_decode_step(torch_bf16_from_bits(x), torch_bf16_from_bits(res), pos, lay, kd, vd, ws,
                               out_f32=out_f32)
     torch.cuda.synchronize()
     assert bm.bitmoe_get_device_status(ws) == 0
-    return ref, kc, vc, out, out_f32, bits_from_torch_bf16(kd), bits_from_torch_bf16(vd)
+    return (ref, kc, vc, out, out_f32, bits_from_torch_bf16(kd).transpose(1, 0, 2),
+            bits_from_torch_bf16(vd).transpose(1, 0, 2))
 
 
 def close_bf16_rows(got, want):
@@ -47,6 +50,19 @@ def close_bf16_rows(got, want):
     diff = np.abs(A.bf16_bits_to_f64(got) - A.bf16_bits_to_f64(want))
     assert np.all(diff <= ulp * 1.01)
     assert np.mean(got != want) <= 0.01
+
+
+def check_step(pos, window, rope, sinks, L=L):
+    ref, kc, vc, out, out_f32, kd, vd = run_step(pos, window, rope, sinks, L=L)
+    o32 = out_f32.cpu().numpy().astype(np.float64)
+    ma, rl = max_abs(o32, ref["out"]), rel_l2(o32, ref["out"])
+    assert ma <= MAX_ABS and rl <= REL_L2, f"max-abs {ma:.3g} rel-L2 {rl:.3g}"
+    assert np.array_equal(bits_from_torch_bf16(out), bits_from_torch_bf16(out_f32.to(torch.bfloat16)))
+    keep = np.ones(L, bool)
+    keep[pos] = False
+    assert np.array_equal(kd[keep], kc[keep]) and np.array_equal(vd[keep], vc[keep])
+    close_bf16_rows(kd[pos], ref["k_bits"])
+    close_bf16_rows(vd[pos], ref["v_bits"])
 
 
 @pytest.mark.parametrize("pos,window,rope,sinks", [
@@ -60,22 +76,20 @@ def close_bf16_rows(got, want):
     (4500, 0, False, True),    # 18 chunks of the whole context
 ])
 def test_attention_decode_step_matches_the_oracle(pos, window, rope, sinks):
-    ref, kc, vc, out, out_f32, kd, vd = run_step(pos, window, rope, sinks)
-    o32 = out_f32.cpu().numpy().astype(np.float64)
-    ma, rl = max_abs(o32, ref["out"]), rel_l2(o32, ref["out"])
-    assert ma <= MAX_ABS and rl <= REL_L2, f"max-abs {ma:.3g} rel-L2 {rl:.3g}"
-    assert np.array_equal(bits_from_torch_bf16(out), bits_from_torch_bf16(out_f32.to(torch.bfloat16)))
-    keep = np.ones(L, bool)
-    keep[pos] = False
-    assert np.array_equal(kd[keep], kc[keep]) and np.array_equal(vd[keep], vc[keep])
-    close_bf16_rows(kd[pos], ref["k_bits"])
-    close_bf16_rows(vd[pos], ref["v_bits"])
+    check_step(pos, window, rope, sinks)
+
+
+@pytest.mark.parametrize("window,rope", [(0, False), (513, True)])
+def test_attention_at_long_context(window, rope):
+    """40001 positions: each warp of the split kernel runs nine 16-position tiles through
+    its three-stage ring (the wrap-around), and the rotation angle reaches 4e4 radians."""
+    check_step(40000, window, rope, True, L=40960)
 
 
 def test_attention_step_rejects_positions_outside_the_cache():
     t = synth.attn_layer(3, D, NQ, NKV)
     lay = bm.AttnLayer.from_canonical(t, D, NQ, NKV)
-    kd = torch.zeros((64, NKV, 128), dtype=torch.bfloat16, device="cuda")
+    kd = torch.zeros((NKV, 64, 128), dtype=torch.bfloat16, device="cuda")
     vd = torch.zeros_like(kd)
     ws = bm.attn_workspace(lay, 64)
     x = torch.zeros(D, dtype=torch.bfloat16, device="cuda")
