@@ -114,6 +114,7 @@ KERNEL_SOURCES = {
     "decode_layer_kernel": ["decode.cu", "common.cuh"],
     "prefill_wa_kernel": ["prefill.cu", "common.cuh"],
     "lmhead_kernel": ["lmhead.cu", "common.cuh"],
+    "attn_split_kernel": ["attn.cu", "common.cuh"],
 }
 
 
@@ -979,8 +980,9 @@ def bench_attn(args, world, rank):
         "timing": timing_record(times, K, f"CUDA graphs of {K} attn_decode_step calls, {ng} graph(s) in rotation"),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "traffic": None,
-                     "kernel": "whole attention step (qkv GEMV, prep, split-KV attention, combine, Wo GEMV, "
-                               "residual)", "bytes_per_step": step_bytes,
+                     "kernel": "whole attention step (q|k|v projection, split-KV attention, combine, "
+                               "Wo projection + residual; 4 launches)", "bytes_per_step": step_bytes,
+                     "split_kernel_dram_bytes": profiled_traffic("attn_split_kernel", workload=name),
                      "peak_source": which + " (copy, burst)"},
         "gpu_launches": launches_per_step * K if launches_per_step else None,
         "e2e": {"value": round(job_throughput(K, statistics.median(e_times), world), 1), "unit": "tokens/s",
