@@ -27,6 +27,9 @@ plus one shared expert), ``lmhead`` (the int4 LM head alone, V = 131072).
 q|k|v and output projections, grouped-query attention of 32 query / 4 key-value
 heads of 128 over a bf16 cache of ``--ctx`` positions, whole context or a
 ``--window``, with sinks).
+``decoder`` (one token through 49 decoder layers -- pre-norm attention at ``--ctx``
+positions, 35 window layers with rotary and 14 whole-context ones, then the pre-norm
+MoE block -- and RMSNorm, the int4 LM head and the arg-max).
 ``--format nvfp4`` runs the decode, batch, prefill and LM-head workloads with
 NVFP4 weights (E2M1 codes, an E4M3 scale per 16 weights, an fp32 scale per
 matrix; the same 4.5 bits per weight).  ``--impl reference`` times the fp64 CPU
@@ -53,6 +56,7 @@ PREFILL_METRIC = "MoE-layer prefill tokens/s on 1 B300; grouped-GEMM TFLOP/s vs 
 STACK_METRIC = "49-layer MoE stack + int4 LM head decode tokens/s on 1 B300; achieved HBM GB/s"
 LMHEAD_METRIC = "int4 LM-head GEMV + argmax tokens/s on 1 B300; achieved HBM GB/s"
 ATTN_METRIC = "attention-layer decode tokens/s on 1 B300 (GQA 32/4 x 128, int4 projections); achieved HBM GB/s"
+DECODER_METRIC = "49-layer decoder (attention + MoE) + int4 LM head decode tokens/s on 1 B300; achieved HBM GB/s"
 D, E, K_TOP, I_FF, V = 2048, 256, 8, 512, 131072
 EXPERT_BYTES = 3 * I_FF * D * 9 // 16          # int4 + fp16 group scales of one expert (gate, up, down)
 ROUTER_BYTES = E * D * 4 + E * 4               # fp32 router weight + bias
@@ -63,8 +67,9 @@ WQKV_BYTES = (NQ + 2 * NKV) * HD * D * 9 // 16  # int4 + fp16 group scales of th
 WO_BYTES = D * NQ * HD * 9 // 16
 MIN_TIMED_S = 0.4                              # GPU time the repeated timed region adds up to, at least
 DEFAULT_STEPS = {"decode": 2000, "shared": 2000, "batch": 500, "prefill": 20, "stack": 50, "lmhead": 500,
-                 "attn": 500}
-DEFAULT_WARMUP = {"decode": 200, "shared": 200, "batch": 50, "prefill": 5, "stack": 5, "lmhead": 50, "attn": 50}
+                 "attn": 500, "decoder": 30}
+DEFAULT_WARMUP = {"decode": 200, "shared": 200, "batch": 50, "prefill": 5, "stack": 5, "lmhead": 50, "attn": 50,
+                  "decoder": 3}
 
 
 def parse():
@@ -75,13 +80,14 @@ def parse():
     p.add_argument("--warmup", type=int, default=None, help="untimed warm-up steps (per-workload default, >= 3)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="decode",
-                   choices=["decode", "batch", "prefill", "stack", "shared", "lmhead", "attn"],
+                   choices=["decode", "batch", "prefill", "stack", "shared", "lmhead", "attn", "decoder"],
                    help="shared: batch-1 decode with the pages' routing, top-6 of 256 plus one shared expert")
     p.add_argument("--T", type=int, default=None, help="tokens per step (batch / prefill / stack / lmhead)")
     p.add_argument("--format", default="int4", choices=["int4", "nvfp4"],
                    help="weight format of the experts and the LM head (not the stack)")
     p.add_argument("--copies", type=int, default=64, help="independent layer copies cycled per step")
-    p.add_argument("--ctx", type=int, default=32768, help="attn: context length (the token attends at ctx - 1)")
+    p.add_argument("--ctx", type=int, default=None,
+                   help="attn / decoder: context length, the token attends at ctx - 1 (32768 / 4096)")
     p.add_argument("--window", type=int, default=0, help="attn: sliding window (0 = whole context; 513 with rotary)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -95,7 +101,9 @@ def parse():
     a.steps = max(1, a.steps)
     a.warmup = max(3, a.warmup)
     MIN_TIMED_S = max(0.0, a.min_timed_s)
-    if a.format == "nvfp4" and a.workload in ("stack", "shared", "attn"):
+    if a.ctx is None:
+        a.ctx = 4096 if a.workload == "decoder" else 32768
+    if a.format == "nvfp4" and a.workload in ("stack", "shared", "attn", "decoder"):
         p.error("--format nvfp4 covers the decode, batch, prefill and lmhead workloads")
     return a
 
@@ -1014,6 +1022,171 @@ def cpu_attn_sample(ctx, window, seconds, seed=0):
                       f"by the oracle's C routine)"}
 
 
+# ---------------------------------------------------------------- decoder: attention + MoE per layer
+
+
+def decoder_kinds(n_layers):
+    """(window, rotary) of each layer: 14 of 49 attend over the whole context without
+    rotary encoding (layers l with l % 7 in {3, 6}), the others over 513 tokens with it."""
+    return [(0, False) if l % 7 in (3, 6) else (513, True) for l in range(n_layers)]
+
+
+def make_device_attn(n_layers, seed, ctx, device="cuda"):
+    """n attention layers (int4 banks drawn on the device, sinks N(0, 1)) and their
+    head-major caches of ctx rows (N(0, 1) bf16)."""
+    import torch
+
+    import bit_expert_ffn_warp_b300 as bm
+    import synth
+    rows = (NQ + 2 * NKV) * HD
+    out, gen = [], torch.Generator(device=device)
+    for l, (window, rope) in enumerate(decoder_kinds(n_layers)):
+        banks = {}
+        for name, (r, K) in {"qkv": (rows, D), "wo": (D, NQ * HD)}.items():
+            q = torch.empty(r * K // 2, dtype=torch.uint8, device=device)
+            s = torch.empty(r * K // 32, dtype=torch.float16, device=device)
+            synth.device_fill_int4(q.data_ptr(), q.numel(), synth.stream_key(seed, synth.TAG[name + "_q"], l))
+            synth.device_fill_scales(s.data_ptr(), s.numel(), synth.stream_key(seed, synth.TAG[name + "_s"], l))
+            banks[name] = bm.bitmoe_pack_int4(q.view(r, K // 2), s.view(r, K // 32))
+        gen.manual_seed(seed * 1000 + l)
+        sinks = torch.randn(NQ, generator=gen, device=device)
+        kc = torch.randn((NKV, ctx, HD), generator=gen, device=device).to(torch.bfloat16)
+        vc = torch.randn((NKV, ctx, HD), generator=gen, device=device).to(torch.bfloat16)
+        out.append((bm.AttnLayer(D, NQ, NKV, banks["qkv"], banks["wo"], sinks, window=window, rope=rope), kc, vc))
+    torch.cuda.synchronize()
+    return out
+
+
+def bench_decoder(args, world, rank):
+    """One token through 49 decoder layers at position ctx - 1: per layer the pre-norm
+    attention block then the pre-norm MoE block, the bf16 residual updated in place; then
+    RMSNorm, the int4 LM head and the arg-max."""
+    import torch
+
+    import bit_expert_ffn_warp_b300 as bm
+
+    ctx, K, W = args.ctx, args.steps, args.warmup
+    if ctx < 1:
+        raise SystemExit("--ctx must be >= 1")
+    moe = make_device_layers(N_LAYERS, seed=1 + rank, bias="normal")
+    attn = make_device_attn(N_LAYERS, 1 + rank, ctx)
+    lm = make_device_lm_head(seed=1 + rank)
+    mws = bm.moe_workspace(moe[0], 1)
+    aws = bm.attn_workspace(attn[0][0], ctx)
+    lm_ws = bm.lmhead_workspace(1, D, V)
+    pos = ctx - 1
+    n_pool = max(8, min(K + W, 1024))
+    xs_host = token_pool(rank, n_pool, 1)
+    xs = to_bf16(xs_host)
+    resid = torch.empty((1, D), dtype=torch.bfloat16, device="cuda")
+    xh = torch.empty_like(resid)
+    am = torch.empty(1, dtype=torch.int32, device="cuda")
+    ids = torch.empty((N_LAYERS, 1, K_TOP), dtype=torch.int32, device="cuda")
+
+    def layers_and_head():
+        for l in range(N_LAYERS):
+            lay, kc, vc = attn[l]
+            bm.attn_decode_step_prenorm(resid[0], pos, lay, kc, vc, aws, out=resid[0])
+            bm.moe_forward_prenorm(resid, moe[l], mws, out=resid, ids_out=ids[l])
+        bm.bitmoe_rmsnorm(resid, out=xh)
+        bm.lmhead_int4_gemv(xh, lm, V, lm_ws, want_logits=False, argmax=am)
+
+    def step(s):
+        resid.copy_(xs[s % n_pool])
+        layers_and_head()
+
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        run_warmup(step, W)
+        times = time_regions(region_graphs(step, K, 1), world)
+    ms_local = statistics.median(times)
+    ms = max_over_ranks(ms_local, world) / K
+    launches_per_step = count_kernels(layers_and_head)
+    ids_np = ids.cpu().numpy()
+    moe_bytes = sum(len(np.unique(ids_np[l])) * EXPERT_BYTES + ROUTER_BYTES + 2 * D * 2 for l in range(N_LAYERS))
+    attn_bytes = sum(attn_step_bytes(ctx, w) for w, _ in decoder_kinds(N_LAYERS))
+    step_bytes = moe_bytes + attn_bytes + LM_BYTES + D * 2 + 4
+    hbm, _, _, which = peaks()
+    achieved = step_bytes / (ms * 1e-3) / 1e9
+
+    x_pin = to_bf16(xs_host, pin=True)
+    am_pin = torch.empty((n_pool, 1), dtype=torch.int32).pin_memory()
+
+    def e2e_step(s):
+        resid.copy_(x_pin[s % n_pool], non_blocking=True)
+        layers_and_head()
+        am_pin[s % n_pool].copy_(am, non_blocking=True)
+
+    run_warmup(e2e_step, 3)
+    e_times = time_regions(region_graphs(e2e_step, K, 1), world)
+    n_full = sum(1 for w, _ in decoder_kinds(N_LAYERS) if w == 0)
+    return {
+        "metric": DECODER_METRIC,
+        "value": round(job_throughput(K, ms_local, world), 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int4xbf16->fp32; bf16 cache, fp32 softmax",
+        "data": "synthetic (seeded; weights drawn on device, caches N(0,1))",
+        "config": {"workload": f"decoder49_lmhead_ctx{ctx}", "T": 1, "layers": N_LAYERS, "d": D, "E": E,
+                   "top_k": K_TOP, "I": I_FF, "V": V, "n_q_heads": NQ, "n_kv_heads": NKV, "head_dim": HD,
+                   "ctx": ctx, "whole_context_layers": n_full, "window_layers": N_LAYERS - n_full, "window": 513,
+                   "l2": f"inputs larger than L2: {N_LAYERS} MoE layers ({N_LAYERS * E * EXPERT_BYTES / 1e9:.1f} GB), "
+                         f"attention weights and caches, LM head {LM_BYTES / 1e6:.0f} MB per step",
+                   "parallelism": f"replicas x{world}"},
+        "timing": timing_record(times, K, f"CUDA graph of {K} decoder steps"),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "kernel": "whole decoder step (49 x (attention block: 4 launches, MoE block: 1 launch), "
+                               "RMSNorm, LM head)",
+                     "bytes_per_step": int(step_bytes), "moe_bytes": int(moe_bytes), "attention_bytes": int(attn_bytes),
+                     "peak_source": which + " (copy, burst)"},
+        "gpu_launches": launches_per_step * K if launches_per_step else None,
+        "e2e": {"value": round(job_throughput(K, statistics.median(e_times), world), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": D * 2, "d2h_bytes_per_step": 4,
+                "how": "every step: pinned host token -> device, 49 decoder layers, LM head, arg-max -> pinned host",
+                "regions": len(e_times)},
+        "clocks": clk.summary(),
+    }
+
+
+def cpu_decoder_sample(ctx, seconds, seed=0):
+    """Oracle time of one decoder step from a bounded sample: whole attention blocks (window
+    and whole-context) and MoE blocks on one layer each, weighted by the layer counts, plus
+    one LM-head pass over a row sample."""
+    import oracle
+    import synth
+    from oracle import attention as A
+    kinds = decoder_kinds(N_LAYERS)
+    n_full = sum(1 for w, _ in kinds if w == 0)
+    t = synth.attn_layer(seed, D, NQ, NKV)
+    kc, vc = synth.kv_cache(seed + 1, ctx, NKV)
+    tensors = synth.moe_layer(seed, D, E, I_FF, bias="normal", layer=0)
+    cores = oracle.num_threads()
+    resid = synth.activations(seed, 1, D)
+    per = {}
+    for name, (window, rope) in {"window": (513, True), "full": (0, False)}.items():
+        t0, n = time.perf_counter(), 0
+        while time.perf_counter() - t0 < seconds * 0.3 or n == 0:
+            A.prenorm_step(resid[0], ctx - 1, t, kc, vc, window=window, use_rope=rope)
+            n += 1
+        per[name] = (time.perf_counter() - t0) / n
+    t0, n = time.perf_counter(), 0
+    while time.perf_counter() - t0 < seconds * 0.3 or n == 0:
+        xh = oracle.f64_to_bf16(oracle.rmsnorm(resid))
+        oracle.moe_forward(xh, tensors, K_TOP, resid=resid)
+        n += 1
+    t_moe = (time.perf_counter() - t0) / n
+    rows = 8192
+    q, sc = synth.lm_head(seed, rows, D)
+    t1 = time.perf_counter()
+    oracle.lmhead(oracle.f64_to_bf16(oracle.rmsnorm(resid)), q, sc, want_logits=False)
+    t_lm = (time.perf_counter() - t1) * (V / rows)
+    t_step = (N_LAYERS - n_full) * per["window"] + n_full * per["full"] + N_LAYERS * t_moe + t_lm
+    return {"value": 1.0 / t_step, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"attention blocks at position {ctx - 1} ({per['window'] * 1e3:.0f} ms window, "
+                      f"{per['full'] * 1e3:.0f} ms whole context), MoE block {t_moe * 1e3:.0f} ms, each on one layer, "
+                      f"x {N_LAYERS - n_full} / {n_full} / {N_LAYERS} layers + LM head on {rows} of {V} rows scaled "
+                      f"({t_lm * 1e3:.0f} ms); fp64"}
+
+
 # ---------------------------------------------------------------- main
 
 
@@ -1040,6 +1213,9 @@ def reference_arm(args):
     elif wl == "attn":
         T = 1
         name, metric = attn_name(args.ctx, args.window), ATTN_METRIC
+    elif wl == "decoder":
+        T = 1
+        name, metric = f"decoder49_lmhead_ctx{args.ctx}", DECODER_METRIC
     else:
         T = args.T or 1
         name, metric = f"moe_stack49_lmhead_T{T}", STACK_METRIC
@@ -1052,6 +1228,8 @@ def reference_arm(args):
         cb = cpu_lmhead_sample(T, budget)
     elif wl == "attn":
         cb = cpu_attn_sample(args.ctx, args.window, budget)
+    elif wl == "decoder":
+        cb = cpu_decoder_sample(args.ctx, budget)
     else:
         cb = cpu_oracle_sample(wl, T, budget)
     el = time.perf_counter() - t0
@@ -1061,6 +1239,9 @@ def reference_arm(args):
     elif wl == "attn":
         cfg.update({"n_q_heads": NQ, "n_kv_heads": NKV, "head_dim": HD, "ctx": args.ctx, "window": args.window,
                     "rope": args.window > 0, "sinks": True})
+    elif wl == "decoder":
+        cfg.update({"layers": N_LAYERS, "E": E, "top_k": K_TOP, "I": I_FF, "V": V, "n_q_heads": NQ,
+                    "n_kv_heads": NKV, "head_dim": HD, "ctx": args.ctx})
     else:
         cfg.update({"E": E, "top_k": K_SHARED if wl == "shared" else K_TOP, "n_shared": int(wl == "shared"),
                     "I": I_FF})
@@ -1089,6 +1270,8 @@ def main():
         res = bench_lmhead(args, world, rank)
     elif args.workload == "attn":
         res = bench_attn(args, world, rank)
+    elif args.workload == "decoder":
+        res = bench_decoder(args, world, rank)
     else:
         res = bench_stack(args, world, rank)
     if rank == 0:
@@ -1100,6 +1283,8 @@ def main():
                 res["cpu_baseline"] = cpu_lmhead_sample(T, args.cpu_seconds, fmt=args.format)
             elif args.workload == "attn":
                 res["cpu_baseline"] = cpu_attn_sample(args.ctx, args.window, args.cpu_seconds)
+            elif args.workload == "decoder":
+                res["cpu_baseline"] = cpu_decoder_sample(args.ctx, args.cpu_seconds)
             else:
                 res["cpu_baseline"] = cpu_oracle_sample(args.workload, T, args.cpu_seconds, fmt=args.format)
         print(json.dumps(res))

@@ -112,6 +112,8 @@ _SIGS = {
     "attn_workspace_size": (_SZ, [ctypes.POINTER(AttnShape)]),
     "attn_decode_step": (ctypes.c_int, [_P, _P, _I64, ctypes.POINTER(AttnShape), ctypes.POINTER(AttnWeights), _P,
                                         _P, _P, _P, _P, _SZ, _P]),
+    "attn_decode_step_prenorm": (ctypes.c_int, [_P, _I64, ctypes.POINTER(AttnShape), ctypes.POINTER(AttnWeights),
+                                                _P, _P, _P, _P, _P, _SZ, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -575,6 +577,31 @@ def attn_workspace(layer: AttnLayer, max_len: int) -> torch.Tensor:
     return torch.zeros(n, dtype=torch.uint8, device="cuda")
 
 
+def _attn_caches(layer: AttnLayer, k_cache, v_cache):
+    _need(k_cache, torch.bfloat16, None, "k_cache")
+    _need(v_cache, torch.bfloat16, tuple(k_cache.shape), "v_cache")
+    if k_cache.dim() != 3 or k_cache.shape[0] != layer.n_kv or k_cache.shape[2] != 128:
+        raise ValueError("caches must be [n_kv, max_len, 128] (head-major)")
+
+
+def attn_decode_step_prenorm(residual, pos: int, layer: AttnLayer, k_cache, v_cache, workspace, out=None,
+                             out_f32=None):
+    """The pre-norm attention block: out = residual + Attn(bf16(RMSNorm(residual))) (eps =
+    layer.eps).  out may be residual itself.  Returns out [d] bf16."""
+    d = layer.d
+    _need(residual, torch.bfloat16, (d,), "residual")
+    _attn_caches(layer, k_cache, v_cache)
+    if out is None:
+        out = torch.empty(d, dtype=torch.bfloat16, device="cuda")
+    sh = layer.shape(k_cache.shape[1])
+    wts = layer.weights
+    _check("attn_decode_step_prenorm",
+           _lib.attn_decode_step_prenorm(_ptr(residual), int(pos), ctypes.byref(sh), ctypes.byref(wts),
+                                         _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(out_f32), _ptr(workspace),
+                                         workspace.numel(), _stream()))
+    return out
+
+
 def attn_decode_step(x, residual, pos: int, layer: AttnLayer, k_cache, v_cache, workspace, out=None, out_f32=None):
     """One token: x, residual [d] bf16; caches [n_kv, max_len, 128] bf16, head-major (row pos
     of every head is written).
@@ -582,10 +609,7 @@ def attn_decode_step(x, residual, pos: int, layer: AttnLayer, k_cache, v_cache, 
     d = layer.d
     _need(x, torch.bfloat16, (d,), "x")
     _need(residual, torch.bfloat16, (d,), "residual")
-    _need(k_cache, torch.bfloat16, None, "k_cache")
-    _need(v_cache, torch.bfloat16, tuple(k_cache.shape), "v_cache")
-    if k_cache.dim() != 3 or k_cache.shape[0] != layer.n_kv or k_cache.shape[2] != 128:
-        raise ValueError("caches must be [n_kv, max_len, 128] (head-major)")
+    _attn_caches(layer, k_cache, v_cache)
     if out is None:
         out = torch.empty(d, dtype=torch.bfloat16, device="cuda")
     sh = layer.shape(k_cache.shape[1])

@@ -339,6 +339,49 @@ AttnWs attn_layout(const bitmoe_attn_shape_t* sh, void* base) {
   return w;
 }
 
+// One attention decode step: x the block input (with prenorm, x = residual and the
+// projection normalises it).
+bitmoe_status_t attn_step(const uint16_t* x, const uint16_t* residual, int prenorm, int64_t pos,
+                          const bitmoe_attn_shape_t* shape, const bitmoe_attn_weights_t* weights,
+                          uint16_t* k_cache, uint16_t* v_cache, uint16_t* out, float* out_f32, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  bitmoe_status_t st = check_attn_shape(shape);
+  if (st != BITMOE_OK) return st;
+  if (pos < 0 || pos >= shape->max_len || !weights) return BITMOE_ERR_INVALID_ARG;
+  if (!x || !residual || !out || !k_cache || !v_cache || !weights->wqkv || !weights->wo)
+    return BITMOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(residual) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(weights->wqkv) || !aligned16(weights->wo) || (out_f32 && !aligned16(out_f32)))
+    return BITMOE_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < attn_layout(shape, nullptr).total)
+    return BITMOE_ERR_WORKSPACE;
+  const AttnWs w = attn_layout(shape, workspace);
+  AttnLaunch L;
+  L.x = x;
+  L.resid = residual;
+  L.prenorm = prenorm;
+  L.pos = pos;
+  L.d = (int)shape->d;
+  L.nq = (int)shape->n_q_heads;
+  L.nkv = (int)shape->n_kv_heads;
+  L.window = shape->window;
+  L.rope = shape->rope ? 1 : 0;
+  L.theta = shape->rope_theta;
+  L.eps = shape->eps;
+  L.wqkv = weights->wqkv;
+  L.wo = weights->wo;
+  L.sinks = weights->sinks;
+  L.k_cache = k_cache;
+  L.v_cache = v_cache;
+  L.max_len = shape->max_len;
+  L.out = out;
+  L.out_f32 = out_f32;
+  L.qkv = w.qkv;
+  L.part = w.part;
+  L.attn = w.attn;
+  return cuda_status(launch_attn_decode(L, (cudaStream_t)stream));
+}
+
 }  // namespace
 
 extern "C" {
@@ -578,40 +621,17 @@ bitmoe_status_t attn_decode_step(const uint16_t* x, const uint16_t* residual, in
                                  const bitmoe_attn_shape_t* shape, const bitmoe_attn_weights_t* weights,
                                  uint16_t* k_cache, uint16_t* v_cache, uint16_t* out, float* out_f32,
                                  void* workspace, size_t workspace_bytes, void* stream) {
-  bitmoe_status_t st = check_attn_shape(shape);
-  if (st != BITMOE_OK) return st;
-  if (pos < 0 || pos >= shape->max_len || !weights) return BITMOE_ERR_INVALID_ARG;
-  if (!x || !residual || !out || !k_cache || !v_cache || !weights->wqkv || !weights->wo)
-    return BITMOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(residual) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache) ||
-      !aligned16(weights->wqkv) || !aligned16(weights->wo) || (out_f32 && !aligned16(out_f32)))
-    return BITMOE_ERR_INVALID_ARG;
-  if (!workspace || !aligned16(workspace) || workspace_bytes < attn_layout(shape, nullptr).total)
-    return BITMOE_ERR_WORKSPACE;
-  const AttnWs w = attn_layout(shape, workspace);
-  AttnLaunch L;
-  L.x = x;
-  L.resid = residual;
-  L.pos = pos;
-  L.d = (int)shape->d;
-  L.nq = (int)shape->n_q_heads;
-  L.nkv = (int)shape->n_kv_heads;
-  L.window = shape->window;
-  L.rope = shape->rope ? 1 : 0;
-  L.theta = shape->rope_theta;
-  L.eps = shape->eps;
-  L.wqkv = weights->wqkv;
-  L.wo = weights->wo;
-  L.sinks = weights->sinks;
-  L.k_cache = k_cache;
-  L.v_cache = v_cache;
-  L.max_len = shape->max_len;
-  L.out = out;
-  L.out_f32 = out_f32;
-  L.qkv = w.qkv;
-  L.part = w.part;
-  L.attn = w.attn;
-  return cuda_status(launch_attn_decode(L, (cudaStream_t)stream));
+  if (!x) return BITMOE_ERR_INVALID_ARG;
+  return attn_step(x, residual, 0, pos, shape, weights, k_cache, v_cache, out, out_f32, workspace, workspace_bytes,
+                   stream);
+}
+
+bitmoe_status_t attn_decode_step_prenorm(const uint16_t* residual, int64_t pos, const bitmoe_attn_shape_t* shape,
+                                         const bitmoe_attn_weights_t* weights, uint16_t* k_cache,
+                                         uint16_t* v_cache, uint16_t* out, float* out_f32, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+  return attn_step(residual, residual, 1, pos, shape, weights, k_cache, v_cache, out, out_f32, workspace,
+                   workspace_bytes, stream);
 }
 
 size_t lmhead_workspace_size(int64_t T, int64_t d, int64_t V) {

@@ -8,7 +8,8 @@
 // queries and keys, learned attention sinks); 06:11 (dedicated attention kernels).
 //
 // For one token the step is four launches, chained with programmatic dependent launch:
-//   1. proj     q|k|v = Wqkv x: the int4 rows stacked; a CTA per 16-row tile, its eight
+//   1. proj     q|k|v = Wqkv x (x the RMS-normalised residual in the pre-norm form, the
+//               norm taken in the same launch): the int4 rows stacked; a CTA per 16-row tile, its eight
 //               warps splitting the tile's 128-column chunks (so a short matrix still
 //               spreads over every SM) and adding their sums in shared memory
 //   2. split    a CTA per (key/value head, span of the window): RMS norm and rotation
@@ -122,9 +123,11 @@ __device__ __forceinline__ uint32_t word_at(const uint4& q, int gg) {
 // ---------------------------------------------------------------- projections
 
 struct ProjArgs {
-  const uint16_t* x;      // [K] bf16
+  const uint16_t* x;      // [K] bf16 (with prenorm: the residual, normalised here)
   const uint8_t* w;       // packed int4 [rows, K]
   int K, rows;
+  int prenorm;            // x <- bf16(x / sqrt(mean(x^2) + eps)) before the product
+  float eps;
   float* y;               // [rows] W x (fp32), or with resid the unrounded sum (nullable)
   const uint16_t* resid;  // [rows] bf16 or null: out = resid + W x
   uint16_t* out;          // [rows] bf16 (with resid)
@@ -136,11 +139,14 @@ struct ProjArgs {
 // fp16 steps of the dequantised nibbles against x (every n column holds the token, so
 // any lane's first column is the row sum), scaled by the group's fp16 scale in fp32.
 // x is staged as fp16 times 2^s (largest magnitude in [2^14, 2^15): exact for bf16 input).
+// With prenorm the residual is first RMS-normalised in fp32 and rounded to bf16, as a
+// pre-norm layer feeds its block.
 __global__ void __launch_bounds__(kProjWarps * 32) attn_proj_kernel(const __grid_constant__ ProjArgs a) {
   extern __shared__ __align__(16) unsigned char psm[];
   uint16_t* xs = reinterpret_cast<uint16_t*>(psm);
   __shared__ float red[kProjWarps][kTileRows];
   __shared__ uint32_t wmax[kProjWarps];
+  __shared__ float wss[kProjWarps];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c = lane & 3;
   const int nch = a.K / kChunkK;
@@ -160,25 +166,50 @@ __global__ void __launch_bounds__(kProjWarps * 32) attn_proj_kernel(const __grid
       }
     }
   };
-  if (a.early) load(warp);
+  if (a.early) {
+    load(warp);
+  } else if (tid == 0) {
+    // the tile into L2 while the kernel before finishes: L2 is where every write lands,
+    // so the loads after the wait see the current weights whatever that kernel wrote
+    bulk_prefetch_l2(tile, (uint32_t)tile_bytes(a.K));
+  }
   pdl_enter();
   if (!a.early) load(warp);
 
-  // stage x: the largest magnitude, then x 2^s as fp16
+  // stage x: the largest magnitude (and with prenorm the sum of squares), then x 2^s as fp16
   uint32_t m = 0;
+  float ss = 0.f;
   for (int i = tid * 8; i < a.K; i += kProjWarps * 32 * 8) {
     const uint4 v = *reinterpret_cast<const uint4*>(a.x + i);
     const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) m = max(m, max(w4[j] & 0x7fffu, (w4[j] >> 16) & 0x7fffu));
+    for (int j = 0; j < 4; ++j) {
+      m = max(m, max(w4[j] & 0x7fffu, (w4[j] >> 16) & 0x7fffu));
+      const float lo = __uint_as_float(w4[j] << 16), hi = __uint_as_float(w4[j] & 0xffff0000u);
+      ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+    }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if (lane == 0) wmax[warp] = m;
+  for (int o = 16; o > 0; o >>= 1) {
+    m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  }
+  if (lane == 0) {
+    wmax[warp] = m;
+    wss[warp] = ss;
+  }
   __syncthreads();
   m = 0;
+  ss = 0.f;
 #pragma unroll
-  for (int w = 0; w < kProjWarps; ++w) m = max(m, wmax[w]);
+  for (int w = 0; w < kProjWarps; ++w) {
+    m = max(m, wmax[w]);
+    ss += wss[w];
+  }
+  // with prenorm every element becomes bf16(x / rms): rounding keeps order, so the largest
+  // magnitude is bf16(max |x| / rms)
+  const float inv = a.prenorm ? 1.0f / sqrtf(ss / (float)a.K + a.eps) : 1.0f;
+  if (a.prenorm) m = (uint32_t)f2bf(bf16f((uint16_t)m) * inv) & 0x7fffu;
   const int se = f16_row_exponent(m);
   const float f = pow2i(se);
   for (int i = tid * 8; i < a.K; i += kProjWarps * 32 * 8) {
@@ -187,8 +218,12 @@ __global__ void __launch_bounds__(kProjWarps * 32) attn_proj_kernel(const __grid
     uint32_t o[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const __half2 h2 =
-          __floats2half2_rn(__uint_as_float(w4[j] << 16) * f, __uint_as_float(w4[j] & 0xffff0000u) * f);
+      float lo = __uint_as_float(w4[j] << 16), hi = __uint_as_float(w4[j] & 0xffff0000u);
+      if (a.prenorm) {
+        lo = bf16f(f2bf(lo * inv));
+        hi = bf16f(f2bf(hi * inv));
+      }
+      const __half2 h2 = __floats2half2_rn(lo * f, hi * f);
       o[j] = *reinterpret_cast<const uint32_t*>(&h2);
     }
     *reinterpret_cast<uint4*>(xs + i) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -600,7 +635,7 @@ AttnPlan attn_plan(int64_t span, int nkv) {
 cudaError_t launch_attn_decode(const AttnLaunch& L, cudaStream_t s) {
   const int nq = L.nq, nkv = L.nkv, rows = (nq + 2 * nkv) * kHd;
   // 1. q | k | v
-  const ProjArgs p1 = {L.x, L.wqkv, L.d, rows, L.qkv, nullptr, nullptr, 0};
+  const ProjArgs p1 = {L.prenorm ? L.resid : L.x, L.wqkv, L.d, rows, L.prenorm, L.eps, L.qkv, nullptr, nullptr, 0};
   cudaError_t e =
       launch_pdl(attn_proj_kernel, dim3(rows / kTileRows), dim3(kProjWarps * 32), (size_t)L.d * 2, s, p1);
   if (e != cudaSuccess) return e;
@@ -640,7 +675,7 @@ cudaError_t launch_attn_decode(const AttnLaunch& L, cudaStream_t s) {
                       L.sinks, L.attn)) != cudaSuccess)
     return e;
   // 4. output projection plus the residual
-  const ProjArgs p2 = {L.attn, L.wo, nq * kHd, L.d, L.out_f32, L.resid, L.out, 1};
+  const ProjArgs p2 = {L.attn, L.wo, nq * kHd, L.d, 0, 0.f, L.out_f32, L.resid, L.out, 1};
   if ((e = launch_pdl(attn_proj_kernel, dim3(L.d / kTileRows), dim3(kProjWarps * 32), (size_t)nq * kHd * 2, s,
                       p2)) != cudaSuccess)
     return e;

@@ -154,8 +154,9 @@ struct AttnPlan {
 };
 AttnPlan attn_plan(int64_t span, int nkv);
 struct AttnLaunch {
-  const uint16_t* x;      // [d] bf16 (the normalised residual)
+  const uint16_t* x;      // [d] bf16 (the normalised residual; unused with prenorm)
   const uint16_t* resid;  // [d] bf16
+  int prenorm;            // 1: x = bf16(RMSNorm(resid)) with eps, formed in the projection
   int64_t pos;            // the token's position (its cache row)
   int d, nq, nkv;
   int64_t window;         // 0: the whole context

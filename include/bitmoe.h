@@ -193,10 +193,23 @@ typedef struct bitmoe_attn_weights {
 } bitmoe_attn_weights_t;
 
 size_t attn_workspace_size(const bitmoe_attn_shape_t* shape);
+/* x the block's input (the normalised residual); out may alias residual, not x. */
 bitmoe_status_t attn_decode_step(const uint16_t* x, const uint16_t* residual, int64_t pos,
                                  const bitmoe_attn_shape_t* shape, const bitmoe_attn_weights_t* weights,
                                  uint16_t* k_cache, uint16_t* v_cache, uint16_t* out, float* out_f32,
                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* The pre-norm attention block of a decoder layer, as the stack's MoE block
+ * (moe_forward_prenorm): x = bf16(residual / sqrt(mean(residual^2) + eps)) with the shape's
+ * eps (unit gain; the norm is formed inside the q|k|v projection launch), then
+ * out = residual + Attn(x) as attn_decode_step.  out may alias residual (in-place update
+ * of the residual stream).  A decoder layer is this call followed by moe_forward_prenorm.
+ * Source: "Flint 40B : Best Mid Sized LLM", transcript 03:05 (every mixture layer has an
+ * attention block before its experts); the pre-norm placement and unit gain are readings. */
+bitmoe_status_t attn_decode_step_prenorm(const uint16_t* residual, int64_t pos, const bitmoe_attn_shape_t* shape,
+                                         const bitmoe_attn_weights_t* weights, uint16_t* k_cache,
+                                         uint16_t* v_cache, uint16_t* out, float* out_f32, void* workspace,
+                                         size_t workspace_bytes, void* stream);
 
 /* Read (and clear, when clear != 0) the device status word of a workspace.
  * Synchronises `stream`.  *status_out receives BITMOE_OK, BITMOE_ERR_TIMEOUT

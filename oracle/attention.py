@@ -114,3 +114,17 @@ def decode_step(x_bits, resid_bits, pos, layer, k_cache_bits, v_cache_bits, wind
     out = oracle.bf16_to_f64(np.asarray(resid_bits, np.uint16)) + y
     return {"out": out, "out_bits": oracle.f64_to_bf16(out), "k_bits": k_bits, "v_bits": v_bits,
             "attn_bits": attn_bits, "o": o, "q": q, "k_cache_bits": kc, "v_cache_bits": vc}
+
+
+def prenorm_step(resid_bits, pos, layer, k_cache_bits, v_cache_bits, window=513, use_rope=True, n_q=32, n_kv=4,
+                 eps=oracle.RMS_EPS, theta=ROPE_THETA):
+    """The pre-norm attention block of a decoder layer: x = bf16(RMSNorm(residual)) (unit
+    gain), then decode_step(x, residual, ...), whose out is residual + Wo attn.  The same
+    norm the oracle's stack puts before each MoE block.  Returns decode_step's dict plus
+    x_bits."""
+    r = np.asarray(resid_bits, np.uint16)
+    x = oracle.f64_to_bf16(oracle.rmsnorm(r[None, :], eps))[0]
+    res = decode_step(x, r, pos, layer, k_cache_bits, v_cache_bits, window=window, use_rope=use_rope, n_q=n_q,
+                      n_kv=n_kv, eps=eps, theta=theta)
+    res["x_bits"] = x
+    return res

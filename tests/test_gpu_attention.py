@@ -86,6 +86,44 @@ def test_attention_at_long_context(window, rope):
     check_step(40000, window, rope, True, L=40960)
 
 
+def head_major(bits):
+    return torch_bf16_from_bits(np.ascontiguousarray(bits.transpose(1, 0, 2))).contiguous()
+
+
+def test_consecutive_steps_cross_the_window_edge():
+    """Positions 510 .. 514 in a row with a 513-token window: each step attends over the rows
+    the GPU wrote in the steps before it (the oracle chains its own cache), and the window's
+    first row moves from 0 to 2.  The last step, captured in a CUDA graph and replayed,
+    gives the eager result bit for bit."""
+    L2 = 1024
+    t = synth.attn_layer(5, D, NQ, NKV)
+    kref, vref = synth.kv_cache(6, L2, NKV)
+    lay = bm.AttnLayer.from_canonical(t, D, NQ, NKV, window=513, rope=True)
+    kd, vd = head_major(kref), head_major(vref)
+    ws = bm.attn_workspace(lay, L2)
+    for pos in range(510, 515):
+        x = synth.activations(7, 1, D, step=pos)[0]
+        res = synth.activations(8, 1, D, step=pos)[0]
+        ref = A.decode_step(x, res, pos, t, kref, vref, window=513, use_rope=True)
+        kref, vref = ref["k_cache_bits"], ref["v_cache_bits"]
+        xg, rg = torch_bf16_from_bits(x), torch_bf16_from_bits(res)
+        out_f32 = torch.empty(D, dtype=torch.float32, device="cuda")
+        out = bm.attn_decode_step(xg, rg, pos, lay, kd, vd, ws, out_f32=out_f32)
+        torch.cuda.synchronize()
+        o32 = out_f32.cpu().numpy().astype(np.float64)
+        ma, rl = max_abs(o32, ref["out"]), rel_l2(o32, ref["out"])
+        assert ma <= MAX_ABS and rl <= REL_L2, f"pos {pos}: max-abs {ma:.3g} rel-L2 {rl:.3g}"
+    assert bm.bitmoe_get_device_status(ws) == 0
+    eager = bits_from_torch_bf16(out)
+    g = torch.cuda.CUDAGraph()
+    out2 = torch.empty_like(out)
+    with torch.cuda.graph(g):
+        bm.attn_decode_step(xg, rg, 514, lay, kd, vd, ws, out=out2)
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(bits_from_torch_bf16(out2), eager)
+
+
 def test_attention_step_rejects_positions_outside_the_cache():
     t = synth.attn_layer(3, D, NQ, NKV)
     lay = bm.AttnLayer.from_canonical(t, D, NQ, NKV)

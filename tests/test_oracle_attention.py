@@ -173,3 +173,25 @@ def test_rotation_applies_to_queries_and_new_keys_only_on_rope_layers(pos):
     assert np.array_equal(plain["k_bits"], oracle.f64_to_bf16(kn.reshape(-1)).reshape(2, HD))
     assert np.allclose(rot["q"], A.rope(qn, pos), rtol=0, atol=0)
     assert np.array_equal(rot["q"], qn) == (pos == 0)
+
+
+def test_prenorm_block_normalises_the_residual_and_adds_to_it():
+    """Scaling the residual by 2 (exact in bf16) leaves the normalised input bit for bit (eps
+    0: every step of the norm scales exactly), so out moves by exactly the residual; a
+    constant residual normalises to ones; a zero output projection returns the residual."""
+    layer = small_layer()
+    kc, vc = caches(64, 2, 23)
+    kw = dict(n_q=4, n_kv=2, window=0, use_rope=False)
+    r = synth.f64_to_bf16_bits(np.random.default_rng(24).normal(0, 1, 256))
+    r2 = synth.f64_to_bf16_bits(2.0 * A.bf16_bits_to_f64(r))
+    a = A.prenorm_step(r, 20, layer, kc, vc, eps=0.0, **kw)
+    b = A.prenorm_step(r2, 20, layer, kc, vc, eps=0.0, **kw)
+    assert np.array_equal(a["x_bits"], b["x_bits"])
+    rv, r2v = A.bf16_bits_to_f64(r), A.bf16_bits_to_f64(r2)
+    assert np.array_equal(b["out"] - r2v, a["out"] - rv)
+    c = A.prenorm_step(np.full(256, 0x4040, np.uint16), 20, layer, kc, vc, eps=0.0, **kw)  # 3.0
+    assert np.all(c["x_bits"] == 0x3F80)  # 1.0
+    z = dict(layer, wo_q=np.zeros_like(layer["wo_q"]))
+    assert np.array_equal(A.prenorm_step(r, 20, z, kc, vc, **kw)["out"], rv)
+    # without the norm the block would see r itself: the normalised input differs from it
+    assert not np.array_equal(a["x_bits"], r)
