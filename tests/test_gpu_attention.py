@@ -25,18 +25,19 @@ import bit_expert_ffn_warp_b300 as bm  # noqa: E402
 D, NQ, NKV, L = 2048, 32, 4, 4608
 
 
-def run_step(pos, window, rope, sinks, seed=3, L=L):
-    t = synth.attn_layer(seed, D, NQ, NKV, sinks=sinks)
-    kc, vc = synth.kv_cache(seed + 1, L, NKV)
-    x = synth.activations(seed + 2, 1, D, step=pos)[0]
-    res = synth.activations(seed + 3, 1, D, step=pos)[0]
-    ref = A.decode_step(x, res, pos, t, kc, vc, window=window, use_rope=rope)
-    lay = bm.AttnLayer.from_canonical(t, D, NQ, NKV, window=window, rope=rope)
+def run_step(pos, window, rope, sinks, seed=3, L=L, dims=(D, NQ, NKV)):
+    d, nq, nkv = dims
+    t = synth.attn_layer(seed, d, nq, nkv, sinks=sinks)
+    kc, vc = synth.kv_cache(seed + 1, L, nkv)
+    x = synth.activations(seed + 2, 1, d, step=pos)[0]
+    res = synth.activations(seed + 3, 1, d, step=pos)[0]
+    ref = A.decode_step(x, res, pos, t, kc, vc, window=window, use_rope=rope, n_q=nq, n_kv=nkv)
+    lay = bm.AttnLayer.from_canonical(t, d, nq, nkv, window=window, rope=rope)
     # the oracle keeps [position, head, 128]; the library's cache is head-major
     kd = torch_bf16_from_bits(np.ascontiguousarray(kc.transpose(1, 0, 2))).contiguous()
     vd = torch_bf16_from_bits(np.ascontiguousarray(vc.transpose(1, 0, 2))).contiguous()
     ws = bm.attn_workspace(lay, L)
-    out_f32 = torch.empty(D, dtype=torch.float32, device="cuda")
+    out_f32 = torch.empty(d, dtype=torch.float32, device="cuda")
     out = bm.attn_decode_step(torch_bf16_from_bits(x), torch_bf16_from_bits(res), pos, lay, kd, vd, ws,
                               out_f32=out_f32)
     torch.cuda.synchronize()
@@ -52,8 +53,8 @@ def close_bf16_rows(got, want):
     assert np.mean(got != want) <= 0.01
 
 
-def check_step(pos, window, rope, sinks, L=L):
-    ref, kc, vc, out, out_f32, kd, vd = run_step(pos, window, rope, sinks, L=L)
+def check_step(pos, window, rope, sinks, L=L, dims=(D, NQ, NKV)):
+    ref, kc, vc, out, out_f32, kd, vd = run_step(pos, window, rope, sinks, L=L, dims=dims)
     o32 = out_f32.cpu().numpy().astype(np.float64)
     ma, rl = max_abs(o32, ref["out"]), rel_l2(o32, ref["out"])
     assert ma <= MAX_ABS and rl <= REL_L2, f"max-abs {ma:.3g} rel-L2 {rl:.3g}"
@@ -84,6 +85,14 @@ def test_attention_at_long_context(window, rope):
     """40001 positions: each warp of the split kernel runs nine 16-position tiles through
     its three-stage ring (the wrap-around), and the rotation angle reaches 4e4 radians."""
     check_step(40000, window, rope, True, L=40960)
+
+
+@pytest.mark.parametrize("dims,pos,window,rope", [
+    ((2048, 64, 8), 3000, 0, False),  # Wo has K = 8192: each projection warp takes two batches of chunks
+    ((1024, 16, 2), 2500, 513, True),  # two key/value heads: a finer split plan
+])
+def test_attention_other_head_counts(dims, pos, window, rope):
+    check_step(pos, window, rope, True, L=3072, dims=dims)
 
 
 def head_major(bits):
