@@ -147,3 +147,39 @@ def test_stack_call_rejects_on_the_host_without_gpu(built):
     bad = (bm.MoeWeights * 2)(w, bm.MoeWeights(1 << 20, None, 1 << 20, 1 << 20, None))
     assert lib.moe_stack_decode(fake, 1, ctypes.byref(sh), bad, 2, 1e-6, None, 0, None, None, None, fake,
                                 ws_bytes, None) == 1
+
+
+def test_attention_calls_reject_on_the_host_without_gpu(built):
+    """attn_workspace_size / attn_decode_step / attn_decode_step_prenorm: shapes the kernels
+    are not built for size no workspace, and every call below fails a check that returns
+    before any launch."""
+    import bit_expert_ffn_warp_b300 as bm
+    lib = bm._lib
+    S = lambda d=2048, nq=32, nkv=4, hd=128, L=4096, w=513, rope=1, eps=1e-6, th=1e6: bm.AttnShape(  # noqa: E731
+        d, nq, nkv, hd, L, w, rope, eps, th)
+    n = lib.attn_workspace_size(ctypes.byref(S()))
+    assert n >= 32 * 128 * 132 * 4  # the split records of every query head
+    assert lib.attn_workspace_size(ctypes.byref(S(L=131072))) == n  # independent of the cache length
+    for bad in (S(hd=64), S(nq=16), S(d=2000), S(d=32768), S(w=-1), S(L=0), S(eps=-1.0), S(th=0.0),
+                S(L=(1 << 31) + 1)):
+        assert lib.attn_workspace_size(ctypes.byref(bad)) == 0
+    assert lib.attn_workspace_size(ctypes.byref(S(rope=0, th=0.0))) == n  # no rotary: theta unused
+    fake = ctypes.c_void_p(1 << 20)  # 16-byte aligned stand-in, never dereferenced on these paths
+    odd = ctypes.c_void_p((1 << 20) + 2)
+    w = bm.AttnWeights(1 << 20, 1 << 20, None)
+    sh = S()
+
+    def step(x=fake, r=fake, pos=10, k=fake, v=fake, out=fake, ws=fake, nb=n, shape=sh, wts=w):
+        return lib.attn_decode_step(x, r, pos, ctypes.byref(shape), ctypes.byref(wts), k, v, out, None, ws, nb,
+                                    None)
+
+    def pre(r=fake, pos=10, nb=n):
+        return lib.attn_decode_step_prenorm(r, pos, ctypes.byref(sh), ctypes.byref(w), fake, fake, fake, None, fake,
+                                            nb, None)
+    assert step(pos=4096) == 1 and step(pos=-1) == 1        # outside the cache
+    assert step(x=None) == 1 and step(k=None) == 1 and step(out=None) == 1
+    assert step(x=odd) == 1 and step(v=odd) == 1            # not 16-byte aligned
+    assert step(nb=n - 1) == 3 and step(ws=None) == 3       # workspace too small or absent
+    assert step(shape=S(hd=64)) == 2                        # a shape the kernels are not built for
+    assert step(wts=bm.AttnWeights(1 << 20, None, None)) == 1
+    assert pre(pos=4096) == 1 and pre(r=None) == 1 and pre(nb=n - 1) == 3
